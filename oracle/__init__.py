@@ -1,0 +1,159 @@
+"""Float64 CPU oracle for the minGRU scan family.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+product path (the CUDA library and its Python binding) never imports it and
+shares no code with it.
+
+Each function is the plain sequential definition of one op of the
+``mingru.triton_scans`` API reference page (page "minGRU - Triton kernels"),
+evaluated in double precision by ``mg_oracle.c``:
+
+* ``linear_scan_fwd``   -- linear_scan_fwd: running product A, h_0 = 0 solution Bc
+* ``linear_scan_bwd``   -- linear_scan_bwd: da, db from a, A, Bc, gA, gBc
+* ``log_scan_fwd``      -- parallel_scan_log_fwd: h_1..h_T from log_coeffs, log_values
+* ``affine_scan_fwd``   -- affine_scan_fwd: Abar (running matrix product), Bbar
+* ``affine_scan_bwd``   -- affine_scan_bwd: dA, dB
+
+Inputs are converted to contiguous float64 numpy arrays (a float32 or bf16
+value widens exactly).  Outputs are float64 numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mg_oracle.c")
+_LIB = os.path.join(_HERE, "libmgoracle.so")
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
+    """Compile ``src`` (default ``mg_oracle.c``) into the shared library ``out``
+    (gcc, -O2, no fast-math, no FMA contraction).  Returns the library path."""
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11",
+           "-shared", "-fPIC", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _f64(x) -> np.ndarray:
+    """Contiguous float64 copy of a numpy array or a torch tensor (bf16 widens exactly)."""
+    if hasattr(x, "detach"):
+        import torch
+        x = x.detach().to("cpu", torch.float64).contiguous().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(x: np.ndarray):
+    return x.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+class Oracle:
+    """The five oracle functions bound to one build of the C source."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        P = ctypes.POINTER(ctypes.c_double)
+        I64 = ctypes.c_int64
+        I = ctypes.c_int
+        lib.orc_linear_scan_fwd.argtypes = [P, P, P, P, I64, I64, I64]
+        lib.orc_linear_scan_bwd.argtypes = [P, P, P, P, P, P, P, I64, I64, I64]
+        lib.orc_log_scan_fwd.argtypes = [P, P, P, I64, I64, I64]
+        lib.orc_affine_scan_fwd.argtypes = [P, P, P, P, I64, I64, I64, I, I]
+        lib.orc_affine_scan_bwd.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I, I]
+        for f in (lib.orc_linear_scan_fwd, lib.orc_linear_scan_bwd, lib.orc_log_scan_fwd,
+                  lib.orc_affine_scan_fwd, lib.orc_affine_scan_bwd):
+            f.restype = None
+        self._lib = lib
+
+    def linear_scan_fwd(self, a, b):
+        """(A, Bc) for a, b (B,T,D): A_t = a_t A_{t-1}, Bc_t = a_t Bc_{t-1} + b_t."""
+        a, b = _f64(a), _f64(b)
+        assert a.ndim == 3 and a.shape == b.shape
+        A = np.empty_like(a)
+        Bc = np.empty_like(a)
+        self._lib.orc_linear_scan_fwd(_ptr(a), _ptr(b), _ptr(A), _ptr(Bc), *a.shape)
+        return A, Bc
+
+    def linear_scan_bwd(self, a, A, Bc, gA, gBc):
+        """(da, db) for L = sum(gA*A) + sum(gBc*Bc), with A, Bc taken as given."""
+        a, A, Bc, gA, gBc = (_f64(x) for x in (a, A, Bc, gA, gBc))
+        assert a.ndim == 3 and all(x.shape == a.shape for x in (A, Bc, gA, gBc))
+        da = np.empty_like(a)
+        db = np.empty_like(a)
+        self._lib.orc_linear_scan_bwd(_ptr(a), _ptr(A), _ptr(Bc), _ptr(gA), _ptr(gBc),
+                                      _ptr(da), _ptr(db), *a.shape)
+        return da, db
+
+    def log_scan_fwd(self, log_coeffs, log_values):
+        """h_1..h_T (B,T,D) for log_coeffs (B,T,D), log_values (B,T+1,D)."""
+        lc, lv = _f64(log_coeffs), _f64(log_values)
+        B, T, D = lc.shape
+        assert lv.shape == (B, T + 1, D)
+        h = np.empty_like(lc)
+        self._lib.orc_log_scan_fwd(_ptr(lc), _ptr(lv), _ptr(h), B, T, D)
+        return h
+
+    def affine_scan_fwd(self, A, Bm):
+        """(Abar, Bbar) for A (B,T,n,k,k), Bm (B,T,n,k,v)."""
+        A, Bm = _f64(A), _f64(Bm)
+        B, T, n, k, k2 = A.shape
+        assert k == k2 and Bm.shape[:4] == (B, T, n, k)
+        v = Bm.shape[4]
+        Abar = np.empty_like(A)
+        Bbar = np.empty_like(Bm)
+        self._lib.orc_affine_scan_fwd(_ptr(A), _ptr(Bm), _ptr(Abar), _ptr(Bbar),
+                                      B, T, n, k, v)
+        return Abar, Bbar
+
+    def affine_scan_bwd(self, A, Abar, Bbar, gAbar, gBbar):
+        """(dA, dB) for L = <gAbar, Abar> + <gBbar, Bbar>, with Abar, Bbar taken as given."""
+        A, Abar, Bbar, gAbar, gBbar = (_f64(x) for x in (A, Abar, Bbar, gAbar, gBbar))
+        B, T, n, k, _ = A.shape
+        v = Bbar.shape[4]
+        assert Abar.shape == A.shape and gAbar.shape == A.shape
+        assert Bbar.shape == (B, T, n, k, v) and gBbar.shape == Bbar.shape
+        dA = np.empty_like(A)
+        dB = np.empty_like(Bbar)
+        self._lib.orc_affine_scan_bwd(_ptr(A), _ptr(Abar), _ptr(Bbar), _ptr(gAbar),
+                                      _ptr(gBbar), _ptr(dA), _ptr(dB), B, T, n, k, v)
+        return dA, dB
+
+
+_default = None
+
+
+def _oracle() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle(build())
+    return _default
+
+
+def linear_scan_fwd(a, b):
+    return _oracle().linear_scan_fwd(a, b)
+
+
+def linear_scan_bwd(a, A, Bc, gA, gBc):
+    return _oracle().linear_scan_bwd(a, A, Bc, gA, gBc)
+
+
+def log_scan_fwd(log_coeffs, log_values):
+    return _oracle().log_scan_fwd(log_coeffs, log_values)
+
+
+def affine_scan_fwd(A, Bm):
+    return _oracle().affine_scan_fwd(A, Bm)
+
+
+def affine_scan_bwd(A, Abar, Bbar, gAbar, gBbar):
+    return _oracle().affine_scan_bwd(A, Abar, Bbar, gAbar, gBbar)

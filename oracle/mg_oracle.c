@@ -1,0 +1,261 @@
+/*
+ * Float64 CPU oracle for the minGRU scan family.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file; only the test suite, the smoke check and the bench's CPU
+ * baseline leg do.  It shares no code, header or constant with the CUDA
+ * library: it is the plain sequential definition of each operation, written
+ * out in double precision so that a reader can check it against the source
+ * page ("minGRU - Triton kernels" API reference, mingru.triton_scans) by eye.
+ *
+ * Layout (the plain reading of the shapes on that page): row-major C order,
+ * last dimension fastest.
+ *   (B,T,D)      element (b,t,d)        at (b*T + t)*D + d
+ *   (B,T,n,k,k)  element (b,t,n,i,j)    at (((b*T + t)*n + n_)*k + i)*k + j
+ *   (B,T,n,k,v)  element (b,t,n,i,j)    at (((b*T + t)*n + n_)*k + i)*v + j
+ * Time index t runs 1..T in the formulas and is stored at 0..T-1.
+ *
+ * Build: gcc -O2 -ffp-contract=off -shared -fPIC (no fast-math, no FMA
+ * contraction), so both x86-64 and aarch64 evaluate the same IEEE sequence.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/*
+ * linear_scan_fwd -- "Channel-tiled k=1 affine prefix scan (Kernel 1)".
+ * Page: mingru.triton_scans.linear_scan_fwd.
+ *   A_t  = a_t * A_{t-1},           A_0 = 1   (running product, inclusive)
+ *   Bc_t = a_t * Bc_{t-1} + b_t,    Bc_0 = 0  (the h_0 = 0 solution)
+ */
+void orc_linear_scan_fwd(const double *a, const double *b, double *A, double *Bc,
+                         int64_t B, int64_t T, int64_t D)
+{
+    double *Ap = (double *)malloc((size_t)(D > 0 ? D : 1) * sizeof(double));
+    double *h = (double *)malloc((size_t)(D > 0 ? D : 1) * sizeof(double));
+    for (int64_t bi = 0; bi < B; ++bi) {
+        for (int64_t d = 0; d < D; ++d) {
+            Ap[d] = 1.0;
+            h[d] = 0.0;
+        }
+        for (int64_t t = 0; t < T; ++t) {
+            const int64_t row = (bi * T + t) * D;
+            for (int64_t d = 0; d < D; ++d) {
+                const double at = a[row + d];
+                Ap[d] = at * Ap[d];
+                h[d] = at * h[d] + b[row + d];
+                A[row + d] = Ap[d];
+                Bc[row + d] = h[d];
+            }
+        }
+    }
+    free(Ap);
+    free(h);
+}
+
+/*
+ * linear_scan_bwd -- "Channel-tiled k=1 affine-scan adjoint".
+ * Page: mingru.triton_scans.linear_scan_bwd.  Inputs are the forward input a,
+ * the forward outputs A and Bc (taken as given) and the upstream gradients
+ * gA, gBc of a loss L = sum(gA*A) + sum(gBc*Bc).  Outputs da = dL/da, db = dL/db.
+ *
+ * Reverse-mode adjoint of the forward recurrences:
+ *   mu_t  = gA_t  + a_{t+1} * mu_{t+1}     (mu_T  = gA_T)
+ *   lam_t = gBc_t + a_{t+1} * lam_{t+1}    (lam_T = gBc_T)
+ *   db_t  = lam_t
+ *   da_t  = mu_t * A_{t-1} + lam_t * Bc_{t-1},   A_0 = 1, Bc_0 = 0
+ */
+void orc_linear_scan_bwd(const double *a, const double *A, const double *Bc,
+                         const double *gA, const double *gBc, double *da, double *db,
+                         int64_t B, int64_t T, int64_t D)
+{
+    double *mu = (double *)malloc((size_t)(D > 0 ? D : 1) * sizeof(double));
+    double *lam = (double *)malloc((size_t)(D > 0 ? D : 1) * sizeof(double));
+    for (int64_t bi = 0; bi < B; ++bi) {
+        for (int64_t d = 0; d < D; ++d) {
+            mu[d] = 0.0;
+            lam[d] = 0.0;
+        }
+        for (int64_t t = T - 1; t >= 0; --t) {
+            const int64_t row = (bi * T + t) * D;
+            for (int64_t d = 0; d < D; ++d) {
+                const double a_next = (t + 1 < T) ? a[row + D + d] : 0.0;
+                mu[d] = gA[row + d] + a_next * mu[d];
+                lam[d] = gBc[row + d] + a_next * lam[d];
+                const double A_prev = (t > 0) ? A[row - D + d] : 1.0;
+                const double Bc_prev = (t > 0) ? Bc[row - D + d] : 0.0;
+                da[row + d] = mu[d] * A_prev + lam[d] * Bc_prev;
+                db[row + d] = lam[d];
+            }
+        }
+    }
+    free(mu);
+    free(lam);
+}
+
+/*
+ * parallel_scan_log_fwd -- "Fused log-space forward scan (Kernel 2)".
+ * Page: mingru.triton_scans.parallel_scan_log_fwd.  log_coeffs is (B,T,D),
+ * log_values is (B,T+1,D) with slot 0 = log h_0 and slots 1..T = log b_t.
+ * Returns h_1..h_T as (B,T,D), in linear space.
+ *
+ * The log-space scan reaches exactly the linear recurrence it encodes:
+ *   h_0 = exp(log_values[0])
+ *   h_t = exp(log_coeffs[t]) * h_{t-1} + exp(log_values[t]),   t = 1..T
+ * with log_coeffs[t] the t-th (1-based) step, i.e. storage index t-1.  Every
+ * term is non-negative, so the double-precision linear form has no
+ * cancellation; -inf inputs give exp(-inf) = 0 exactly.  Its range limit:
+ * inputs above about 709 overflow double.
+ */
+void orc_log_scan_fwd(const double *log_coeffs, const double *log_values, double *h_out,
+                      int64_t B, int64_t T, int64_t D)
+{
+    double *h = (double *)malloc((size_t)(D > 0 ? D : 1) * sizeof(double));
+    for (int64_t bi = 0; bi < B; ++bi) {
+        const int64_t v0 = (bi * (T + 1)) * D;
+        for (int64_t d = 0; d < D; ++d)
+            h[d] = exp(log_values[v0 + d]);
+        for (int64_t t = 1; t <= T; ++t) {
+            const int64_t crow = (bi * T + (t - 1)) * D;   /* log_coeffs / output row */
+            const int64_t vrow = (bi * (T + 1) + t) * D;   /* log_values row */
+            for (int64_t d = 0; d < D; ++d) {
+                h[d] = exp(log_coeffs[crow + d]) * h[d] + exp(log_values[vrow + d]);
+                h_out[crow + d] = h[d];
+            }
+        }
+    }
+    free(h);
+}
+
+/* C = X @ Y for row-major X (r x m), Y (m x c). */
+static void mat_mul(const double *X, const double *Y, double *C, int r, int m, int c)
+{
+    for (int i = 0; i < r; ++i)
+        for (int j = 0; j < c; ++j) {
+            double s = 0.0;
+            for (int l = 0; l < m; ++l)
+                s += X[i * m + l] * Y[l * c + j];
+            C[i * c + j] = s;
+        }
+}
+
+/* C = X^T @ Y for row-major X (m x r), Y (m x c). */
+static void mat_tmul(const double *X, const double *Y, double *C, int r, int m, int c)
+{
+    for (int i = 0; i < r; ++i)
+        for (int j = 0; j < c; ++j) {
+            double s = 0.0;
+            for (int l = 0; l < m; ++l)
+                s += X[l * r + i] * Y[l * c + j];
+            C[i * c + j] = s;
+        }
+}
+
+/* C += X @ Y^T for row-major X (r x m), Y (c x m). */
+static void mat_mul_tadd(const double *X, const double *Y, double *C, int r, int m, int c)
+{
+    for (int i = 0; i < r; ++i)
+        for (int j = 0; j < c; ++j) {
+            double s = 0.0;
+            for (int l = 0; l < m; ++l)
+                s += X[i * m + l] * Y[j * m + l];
+            C[i * c + j] += s;
+        }
+}
+
+/*
+ * affine_scan_fwd -- "Generic k x k affine prefix scan (Kernel 1)".
+ * Page: mingru.triton_scans.affine_scan_fwd.  A is (B,T,n,k,k), Bm is
+ * (B,T,n,k,v).  For each (b, n_) independently:
+ *   Abar_t = A_t @ Abar_{t-1},          Abar_0 = I   (composition A_current @ A_earlier)
+ *   Bbar_t = A_t @ Bbar_{t-1} + B_t,    Bbar_0 = 0   (the H_0 = 0 solution)
+ */
+void orc_affine_scan_fwd(const double *A, const double *Bm, double *Abar, double *Bbar,
+                         int64_t B, int64_t T, int64_t n, int k, int v)
+{
+    const int64_t kk = (int64_t)k * k, kv = (int64_t)k * v;
+    double *P = (double *)malloc((size_t)kk * sizeof(double));
+    double *H = (double *)malloc((size_t)kv * sizeof(double));
+    double *tmp = (double *)malloc((size_t)(kk > kv ? kk : kv) * sizeof(double));
+    for (int64_t bi = 0; bi < B; ++bi)
+        for (int64_t ni = 0; ni < n; ++ni) {
+            for (int i = 0; i < k; ++i)
+                for (int j = 0; j < k; ++j)
+                    P[i * k + j] = (i == j) ? 1.0 : 0.0;
+            memset(H, 0, (size_t)kv * sizeof(double));
+            for (int64_t t = 0; t < T; ++t) {
+                const int64_t s = (bi * T + t) * n + ni;
+                const double *At = A + s * kk;
+                mat_mul(At, P, tmp, k, k, k);
+                memcpy(P, tmp, (size_t)kk * sizeof(double));
+                mat_mul(At, H, tmp, k, k, v);
+                for (int64_t e = 0; e < kv; ++e)
+                    H[e] = tmp[e] + Bm[s * kv + e];
+                memcpy(Abar + s * kk, P, (size_t)kk * sizeof(double));
+                memcpy(Bbar + s * kv, H, (size_t)kv * sizeof(double));
+            }
+        }
+    free(P);
+    free(H);
+    free(tmp);
+}
+
+/*
+ * affine_scan_bwd -- "Generic k x k affine-scan adjoint (Kernel 3)".
+ * Page: mingru.triton_scans.affine_scan_bwd.  Inputs: forward input A, forward
+ * outputs Abar, Bbar (taken as given), upstream gradients gAbar, gBbar of
+ * L = <gAbar, Abar> + <gBbar, Bbar>.  Outputs dA (shape of A), dB (shape of Bbar).
+ *
+ * Reverse-mode adjoint of the forward recurrences:
+ *   M_t   = gAbar_t + A_{t+1}^T @ M_{t+1}     (k x k, M_T = gAbar_T)
+ *   Lam_t = gBbar_t + A_{t+1}^T @ Lam_{t+1}   (k x v, Lam_T = gBbar_T)
+ *   dB_t  = Lam_t
+ *   dA_t  = M_t @ Abar_{t-1}^T + Lam_t @ Bbar_{t-1}^T,   Abar_0 = I, Bbar_0 = 0
+ */
+void orc_affine_scan_bwd(const double *A, const double *Abar, const double *Bbar,
+                         const double *gAbar, const double *gBbar, double *dA, double *dB,
+                         int64_t B, int64_t T, int64_t n, int k, int v)
+{
+    const int64_t kk = (int64_t)k * k, kv = (int64_t)k * v;
+    double *M = (double *)malloc((size_t)kk * sizeof(double));
+    double *L = (double *)malloc((size_t)kv * sizeof(double));
+    double *tmp = (double *)malloc((size_t)(kk > kv ? kk : kv) * sizeof(double));
+    double *eye = (double *)malloc((size_t)kk * sizeof(double));
+    double *zero = (double *)calloc((size_t)kv, sizeof(double));
+    for (int i = 0; i < k; ++i)
+        for (int j = 0; j < k; ++j)
+            eye[i * k + j] = (i == j) ? 1.0 : 0.0;
+    for (int64_t bi = 0; bi < B; ++bi)
+        for (int64_t ni = 0; ni < n; ++ni) {
+            memset(M, 0, (size_t)kk * sizeof(double));
+            memset(L, 0, (size_t)kv * sizeof(double));
+            for (int64_t t = T - 1; t >= 0; --t) {
+                const int64_t s = (bi * T + t) * n + ni;
+                if (t + 1 < T) {
+                    const double *Anext = A + (s + n) * kk;
+                    mat_tmul(Anext, M, tmp, k, k, k);
+                    for (int64_t e = 0; e < kk; ++e)
+                        M[e] = tmp[e] + gAbar[s * kk + e];
+                    mat_tmul(Anext, L, tmp, k, k, v);
+                    for (int64_t e = 0; e < kv; ++e)
+                        L[e] = tmp[e] + gBbar[s * kv + e];
+                } else {
+                    memcpy(M, gAbar + s * kk, (size_t)kk * sizeof(double));
+                    memcpy(L, gBbar + s * kv, (size_t)kv * sizeof(double));
+                }
+                const double *Aprev = (t > 0) ? Abar + (s - n) * kk : eye;
+                const double *Bprev = (t > 0) ? Bbar + (s - n) * kv : zero;
+                double *dAt = dA + s * kk;
+                memset(dAt, 0, (size_t)kk * sizeof(double));
+                mat_mul_tadd(M, Aprev, dAt, k, k, k);
+                mat_mul_tadd(L, Bprev, dAt, k, v, k);
+                memcpy(dB + s * kv, L, (size_t)kv * sizeof(double));
+            }
+        }
+    free(M);
+    free(L);
+    free(tmp);
+    free(eye);
+    free(zero);
+}

@@ -1,0 +1,59 @@
+"""The parity metric shared by the GPU-vs-oracle tests.
+
+The stated bar is a maximum relative error of 1e-4 for float32 inputs and
+2e-2 for bf16 inputs (fp32 accumulation).  A plain elementwise |g - r| / |r|
+is undefined where r passes through zero (sums of signed terms) and
+meaningless where float32 underflows while float64 does not (long running
+products).  So every element is measured against its own scale:
+
+    err_i = |g_i - r_i| / (|r_i| + rho * S_i + tau),   rho = 1, tau = 1e-30
+
+with S_i the scale that rounding error is proportional to:
+
+* running products of positive factors (A of the linear scan, h of the log
+  scan): S = 0, i.e. pure relative error, floored at tau for underflow;
+* sums of signed terms in the channel-wise linear family (Bc, da, db): S is
+  the same quantity evaluated by the oracle on |inputs| -- the componentwise
+  condition scale sum |terms| of a sum of products;
+* matrix-valued affine outputs (Abar, Bbar, dA, dB): S is the RMS of the
+  k x k or k x v block at the same (b, t, n) -- products of matrices are
+  stable normwise, not entrywise.
+
+A NaN or inf where the reference is finite counts as an infinite error.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+RHO = 1.0
+TAU = 1e-30
+TOL_F32 = 1e-4
+TOL_BF16 = 2e-2
+
+
+def scaled_error(g, r, S=0.0, rho: float = RHO, tau: float = TAU) -> float:
+    g = np.asarray(g, dtype=np.float64)
+    r = np.asarray(r, dtype=np.float64)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    if r.size == 0:
+        return 0.0
+    bad = ~np.isfinite(g) & np.isfinite(r)
+    if bad.any():
+        return float("inf")
+    den = np.abs(r) + rho * np.asarray(S, dtype=np.float64) + tau
+    return float(np.max(np.abs(g - r) / den))
+
+
+def block_rms(x: np.ndarray) -> np.ndarray:
+    """RMS over the last two (matrix) axes, broadcast back to x's shape."""
+    x = np.asarray(x, dtype=np.float64)
+    rms = np.sqrt(np.mean(x * x, axis=(-2, -1), keepdims=True))
+    return np.broadcast_to(rms, x.shape)
+
+
+def normwise(g, r) -> float:
+    """||g - r||_2 / ||r||_2, reported alongside, never gating."""
+    g = np.asarray(g, dtype=np.float64)
+    r = np.asarray(r, dtype=np.float64)
+    n = np.linalg.norm(r)
+    return float(np.linalg.norm(g - r) / n) if n > 0 else float(np.linalg.norm(g))

@@ -1,0 +1,398 @@
+"""Pins of the float64 oracle to things other than itself.
+
+The pages print no worked example for any scan, so the oracle is pinned to:
+hand-derived golden cases (tests/golden), the O(T^2) closed forms written as
+brute-force Python loops, numpy/scipy routines in the special cases where the
+op reduces to one (cumsum, cumprod, logsumexp), agreement between the log-space
+and linear ops, between the affine op at k = v = 1 or diagonal A and the
+linear op, the explicit left-multiplied running product, the orthogonal-
+product invariant, central finite differences and torch.autograd for the
+adjoints.
+
+Each pin is a function of an oracle object so that ``test_planted_mistakes``
+can run the whole set against deliberately broken builds of the oracle's C
+source and check that every planted mistake is caught by at least one pin.
+"""
+from __future__ import annotations
+
+import functools
+import json
+import math
+import os
+import shutil
+import tempfile
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- pins ------
+
+def pin_golden_linear(orc):
+    g = _golden("linear_scan_T4.json")
+    a, b = np.array(g["a"]), np.array(g["b"])
+    A, Bc = orc.linear_scan_fwd(a, b)
+    np.testing.assert_array_equal(A, np.array(g["A"]))
+    np.testing.assert_array_equal(Bc, np.array(g["Bc"]))
+    da, db = orc.linear_scan_bwd(a, np.array(g["A"]), np.array(g["Bc"]),
+                                 np.array(g["gA"]), np.array(g["gBc"]))
+    np.testing.assert_array_equal(da, np.array(g["da"]))
+    np.testing.assert_array_equal(db, np.array(g["db"]))
+
+
+def pin_golden_log(orc):
+    g = _golden("log_scan_T3.json")
+    with np.errstate(divide="ignore"):
+        for case in g["cases"]:
+            lc = np.log(np.array(case["log_coeffs_exp"], dtype=np.float64))
+            lv = np.log(np.array(case["log_values_exp"], dtype=np.float64))
+            h = orc.log_scan_fwd(lc, lv)
+            np.testing.assert_allclose(h, np.array(case["h"]), rtol=1e-14, atol=0,
+                                       err_msg=case["name"])
+            assert np.all(np.isfinite(h))
+
+
+def pin_golden_affine(orc):
+    g = _golden("affine_scan_k2.json")
+    A, Bm = np.array(g["A"]), np.array(g["Bm"])
+    Abar, Bbar = orc.affine_scan_fwd(A, Bm)
+    np.testing.assert_array_equal(Abar, np.array(g["Abar"]))
+    np.testing.assert_array_equal(Bbar, np.array(g["Bbar"]))
+    dA, dB = orc.affine_scan_bwd(A, np.array(g["Abar"]), np.array(g["Bbar"]),
+                                 np.array(g["gAbar"]), np.array(g["gBbar"]))
+    np.testing.assert_array_equal(dA, np.array(g["dA"]))
+    np.testing.assert_array_equal(dB, np.array(g["dB"]))
+
+
+def _tiny_linear(seed, B=2, T=13, D=3, positive=False):
+    rng = np.random.default_rng(seed)
+    a = rng.uniform(0.2, 1.3, (B, T, D)) * (1 if positive else rng.choice([-1, 1], (B, T, D)))
+    b = rng.normal(size=(B, T, D))
+    if positive:
+        b = np.abs(b) + 0.1
+    return a, b
+
+
+def pin_linear_closed_form(orc):
+    """A_t = prod_{r<=t} a_r and h_t = sum_{s<=t} (prod_{s<r<=t} a_r) b_s, by brute force."""
+    for seed in range(3):
+        a, b = _tiny_linear(seed)
+        B, T, D = a.shape
+        A, Bc = orc.linear_scan_fwd(a, b)
+        for bi in range(B):
+            for d in range(D):
+                for t in range(T):
+                    prod = 1.0
+                    for r in range(t + 1):
+                        prod *= a[bi, r, d]
+                    tot = 0.0
+                    for s in range(t + 1):
+                        p = 1.0
+                        for r in range(s + 1, t + 1):
+                            p *= a[bi, r, d]
+                        tot += p * b[bi, s, d]
+                    assert math.isclose(A[bi, t, d], prod, rel_tol=1e-13, abs_tol=0)
+                    assert math.isclose(Bc[bi, t, d], tot, rel_tol=1e-12, abs_tol=1e-13)
+
+
+def pin_linear_special_cases(orc):
+    rng = np.random.default_rng(7)
+    b = rng.normal(size=(2, 20, 4))
+    A, Bc = orc.linear_scan_fwd(np.ones_like(b), b)
+    np.testing.assert_array_equal(A, np.ones_like(b))
+    np.testing.assert_allclose(Bc, np.cumsum(b, axis=1), rtol=1e-13, atol=1e-13)
+    a = rng.uniform(0.1, 1.5, size=(2, 20, 4))
+    A, Bc = orc.linear_scan_fwd(a, np.zeros_like(a))
+    np.testing.assert_allclose(A, np.cumprod(a, axis=1), rtol=1e-14, atol=0)
+    np.testing.assert_array_equal(Bc, np.zeros_like(a))
+    # h_0 folded in: with b_1 = h_0 * a_1 + b_1', h = Bc' + A * h_0
+    a, b = _tiny_linear(3)
+    h0 = rng.normal(size=(a.shape[0], 1, a.shape[2]))
+    A, Bc = orc.linear_scan_fwd(a, b)
+    b2 = b.copy()
+    b2[:, :1] += a[:, :1] * h0
+    _, Bc2 = orc.linear_scan_fwd(a, b2)
+    np.testing.assert_allclose(Bc2, Bc + A * h0, rtol=1e-12, atol=1e-12)
+
+
+def _loss_linear(orc, a, b, gA, gBc):
+    A, Bc = orc.linear_scan_fwd(a, b)
+    return float(np.sum(gA * A) + np.sum(gBc * Bc))
+
+
+def pin_linear_adjoint_fd(orc):
+    """Central finite differences of L = <gA, A> + <gBc, Bc>, step 1e-6."""
+    rng = np.random.default_rng(11)
+    a, b = _tiny_linear(5, B=1, T=8, D=2)
+    gA, gBc = rng.normal(size=a.shape), rng.normal(size=a.shape)
+    A, Bc = orc.linear_scan_fwd(a, b)
+    da, db = orc.linear_scan_bwd(a, A, Bc, gA, gBc)
+    eps = 1e-6
+    for idx in np.ndindex(a.shape):
+        for arr, grad in ((a, da), (b, db)):
+            old = arr[idx]
+            arr[idx] = old + eps
+            lp = _loss_linear(orc, a, b, gA, gBc)
+            arr[idx] = old - eps
+            lm = _loss_linear(orc, a, b, gA, gBc)
+            arr[idx] = old
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(fd)), (idx, fd, grad[idx])
+
+
+def pin_linear_adjoint_autograd(orc):
+    """torch.autograd through the forward recurrence written as a float64 loop."""
+    rng = np.random.default_rng(12)
+    a, b = _tiny_linear(6, B=2, T=9, D=3)
+    gA, gBc = rng.normal(size=a.shape), rng.normal(size=a.shape)
+    ta = torch.tensor(a, requires_grad=True)
+    tb = torch.tensor(b, requires_grad=True)
+    Ap = torch.ones(a.shape[0], a.shape[2], dtype=torch.float64)
+    h = torch.zeros_like(Ap)
+    As, hs = [], []
+    for t in range(a.shape[1]):
+        Ap = ta[:, t] * Ap
+        h = ta[:, t] * h + tb[:, t]
+        As.append(Ap)
+        hs.append(h)
+    L = (torch.stack(As, 1) * torch.tensor(gA)).sum() + (torch.stack(hs, 1) * torch.tensor(gBc)).sum()
+    ga, gb = torch.autograd.grad(L, (ta, tb))
+    A, Bc = orc.linear_scan_fwd(a, b)
+    da, db = orc.linear_scan_bwd(a, A, Bc, gA, gBc)
+    np.testing.assert_allclose(da, ga.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(db, gb.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def _tiny_log(seed, B=2, T=12, D=3):
+    rng = np.random.default_rng(seed)
+    lc = -np.log1p(np.exp(rng.normal(size=(B, T, D))))
+    lv = rng.normal(size=(B, T + 1, D))
+    return lc, lv
+
+
+def pin_log_vs_linear(orc):
+    """log_scan(log a, [log h0, log b]) = Bc + A * h0 of the linear op on a, b."""
+    lc, lv = _tiny_log(21)
+    h = orc.log_scan_fwd(lc, lv)
+    A, Bc = orc.linear_scan_fwd(np.exp(lc), np.exp(lv[:, 1:]))
+    h0 = np.exp(lv[:, :1])
+    np.testing.assert_allclose(h, Bc + A * h0, rtol=1e-13, atol=0)
+
+
+def pin_log_closed_form(orc):
+    """log h_t = logsumexp_{s=0..t} (lv_s + sum_{r=s+1..t} lc_r), scipy's logsumexp."""
+    lc, lv = _tiny_log(22, B=2, T=40, D=2)
+    h = orc.log_scan_fwd(lc, lv)
+    B, T, D = lc.shape
+    for bi in range(B):
+        for d in range(D):
+            for t in range(1, T + 1):
+                terms = [lv[bi, s, d] + sum(lc[bi, r - 1, d] for r in range(s + 1, t + 1))
+                         for s in range(t + 1)]
+                ref = scipy.special.logsumexp(terms)
+                assert math.isclose(math.log(h[bi, t - 1, d]), ref, rel_tol=1e-12, abs_tol=1e-12)
+
+
+def _rand_mats(rng, shape, k, v):
+    A = rng.normal(size=shape + (k, k)) * 0.7
+    Bm = rng.normal(size=shape + (k, v))
+    return A, Bm
+
+
+def pin_affine_k1_is_linear(orc):
+    a, b = _tiny_linear(31, B=2, T=11, D=3)
+    A5 = a[..., None, None]
+    B5 = b[..., None, None]
+    Abar, Bbar = orc.affine_scan_fwd(A5, B5)
+    A, Bc = orc.linear_scan_fwd(a, b)
+    np.testing.assert_allclose(Abar[..., 0, 0], A, rtol=1e-14, atol=0)
+    np.testing.assert_allclose(Bbar[..., 0, 0], Bc, rtol=1e-13, atol=1e-14)
+    rng = np.random.default_rng(32)
+    gA, gB = rng.normal(size=a.shape), rng.normal(size=a.shape)
+    dA, dB = orc.affine_scan_bwd(A5, Abar, Bbar, gA[..., None, None], gB[..., None, None])
+    da, db = orc.linear_scan_bwd(a, A, Bc, gA, gB)
+    np.testing.assert_allclose(dA[..., 0, 0], da, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dB[..., 0, 0], db, rtol=1e-12, atol=1e-12)
+
+
+def pin_affine_diagonal_is_linear(orc):
+    """Diagonal A: row i of Bbar is a linear scan with coefficient A[i,i]."""
+    rng = np.random.default_rng(33)
+    B, T, n, k, v = 1, 10, 2, 3, 2
+    diag = rng.uniform(0.3, 1.2, size=(B, T, n, k))
+    A = np.zeros((B, T, n, k, k))
+    for i in range(k):
+        A[..., i, i] = diag[..., i]
+    Bm = rng.normal(size=(B, T, n, k, v))
+    Abar, Bbar = orc.affine_scan_fwd(A, Bm)
+    for ni in range(n):
+        for i in range(k):
+            a = np.repeat(diag[:, :, ni, i][..., None], v, axis=-1)
+            Al, Bl = orc.linear_scan_fwd(a, Bm[:, :, ni, i, :])
+            np.testing.assert_allclose(Bbar[:, :, ni, i, :], Bl, rtol=1e-13, atol=1e-14)
+            np.testing.assert_allclose(Abar[:, :, ni, i, i], Al[..., 0], rtol=1e-14, atol=0)
+
+
+def pin_affine_running_product(orc):
+    """Abar_t = A_t @ ... @ A_1 and Bbar_t = sum_s (A_t ... A_{s+1}) B_s, explicitly."""
+    rng = np.random.default_rng(34)
+    for (k, v) in ((2, 3), (3, 1), (4, 4)):
+        A, Bm = _rand_mats(rng, (2, 7, 2), k, v)
+        Abar, Bbar = orc.affine_scan_fwd(A, Bm)
+        for bi in range(2):
+            for ni in range(2):
+                for t in range(7):
+                    mats = [A[bi, r, ni] for r in range(t, -1, -1)]  # A_t, ..., A_1
+                    P = functools.reduce(np.matmul, mats)
+                    np.testing.assert_allclose(Abar[bi, t, ni], P, rtol=1e-12, atol=1e-12)
+                    H = np.zeros((k, v))
+                    for s in range(t + 1):
+                        left = [A[bi, r, ni] for r in range(t, s, -1)]
+                        Ls = functools.reduce(np.matmul, left) if left else np.eye(k)
+                        H = H + Ls @ Bm[bi, s, ni]
+                    np.testing.assert_allclose(Bbar[bi, t, ni], H, rtol=1e-12, atol=1e-12)
+
+
+def pin_affine_orthogonal_invariant(orc):
+    """For A_t = 0.95 Q_t with Q_t orthogonal: Abar_t^T Abar_t = 0.95^(2t) I."""
+    from linear_recurrence_scans_gb300.workloads import haar_orthogonal
+    for k in (4, 16):
+        T = 40
+        Q = haar_orthogonal(T * 3, k, seed=5).numpy().reshape(1, T, 3, k, k)
+        A = 0.95 * Q
+        Abar, _ = orc.affine_scan_fwd(A, np.zeros((1, T, 3, k, 1)))
+        for t in range(T):
+            G = np.einsum("nij,nil->njl", Abar[0, t], Abar[0, t])
+            np.testing.assert_allclose(G, np.broadcast_to(0.95 ** (2 * (t + 1)) * np.eye(k), G.shape),
+                                       rtol=0, atol=1e-12)
+
+
+def _loss_affine(orc, A, Bm, gA, gB):
+    Abar, Bbar = orc.affine_scan_fwd(A, Bm)
+    return float(np.sum(gA * Abar) + np.sum(gB * Bbar))
+
+
+def pin_affine_adjoint_fd(orc):
+    rng = np.random.default_rng(35)
+    for (k, v) in ((2, 3), (3, 2)):
+        A, Bm = _rand_mats(rng, (1, 6, 2), k, v)
+        gA, gB = rng.normal(size=A.shape), rng.normal(size=Bm.shape)
+        Abar, Bbar = orc.affine_scan_fwd(A, Bm)
+        dA, dB = orc.affine_scan_bwd(A, Abar, Bbar, gA, gB)
+        eps = 1e-6
+        for arr, grad in ((A, dA), (Bm, dB)):
+            for idx in np.ndindex(arr.shape):
+                old = arr[idx]
+                arr[idx] = old + eps
+                lp = _loss_affine(orc, A, Bm, gA, gB)
+                arr[idx] = old - eps
+                lm = _loss_affine(orc, A, Bm, gA, gB)
+                arr[idx] = old
+                fd = (lp - lm) / (2 * eps)
+                assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(fd)), (k, v, idx, fd, grad[idx])
+
+
+def pin_affine_adjoint_autograd(orc):
+    rng = np.random.default_rng(36)
+    k, v = 3, 2
+    A, Bm = _rand_mats(rng, (2, 8, 2), k, v)
+    gA, gB = rng.normal(size=A.shape), rng.normal(size=Bm.shape)
+    tA = torch.tensor(A, requires_grad=True)
+    tB = torch.tensor(Bm, requires_grad=True)
+    P = torch.eye(k, dtype=torch.float64).expand(2, 2, k, k)
+    H = torch.zeros(2, 2, k, v, dtype=torch.float64)
+    Ps, Hs = [], []
+    for t in range(A.shape[1]):
+        P = tA[:, t] @ P
+        H = tA[:, t] @ H + tB[:, t]
+        Ps.append(P)
+        Hs.append(H)
+    L = (torch.stack(Ps, 1) * torch.tensor(gA)).sum() + (torch.stack(Hs, 1) * torch.tensor(gB)).sum()
+    gA_t, gB_t = torch.autograd.grad(L, (tA, tB))
+    Abar, Bbar = orc.affine_scan_fwd(A, Bm)
+    dA, dB = orc.affine_scan_bwd(A, Abar, Bbar, gA, gB)
+    np.testing.assert_allclose(dA, gA_t.numpy(), rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(dB, gB_t.numpy(), rtol=1e-11, atol=1e-11)
+
+
+def pin_degenerate_shapes(orc):
+    """T = 0 (and empty batch) give empty outputs; T = 1 is a single step."""
+    e = np.zeros((2, 0, 3))
+    A, Bc = orc.linear_scan_fwd(e, e)
+    assert A.shape == (2, 0, 3) and Bc.shape == (2, 0, 3)
+    h = orc.log_scan_fwd(e, np.zeros((2, 1, 3)))
+    assert h.shape == (2, 0, 3)
+    a, b = np.full((1, 1, 2), 0.5), np.array([[[1.0, -2.0]]])
+    A, Bc = orc.linear_scan_fwd(a, b)
+    np.testing.assert_array_equal(A, a)
+    np.testing.assert_array_equal(Bc, b)
+
+
+PINS = [
+    pin_golden_linear, pin_golden_log, pin_golden_affine,
+    pin_linear_closed_form, pin_linear_special_cases,
+    pin_linear_adjoint_fd, pin_linear_adjoint_autograd,
+    pin_log_vs_linear, pin_log_closed_form,
+    pin_affine_k1_is_linear, pin_affine_diagonal_is_linear,
+    pin_affine_running_product, pin_affine_orthogonal_invariant,
+    pin_affine_adjoint_fd, pin_affine_adjoint_autograd,
+    pin_degenerate_shapes,
+]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+def test_oracle_pin(pin):
+    pin(oracle._oracle())
+
+
+# Plausible mistakes, planted in copies of the oracle's C source.  Each must
+# make at least one pin fail.
+MUTANTS = {
+    "linear_fwd_dropped_coefficient": ("h[d] = at * h[d] + b[row + d];", "h[d] = h[d] + b[row + d];"),
+    "linear_fwd_exclusive_product": ("A[row + d] = Ap[d];", "A[row + d] = Ap[d] / at;"),
+    "linear_bwd_coefficient_index": ("a[row + D + d] : 0.0", "a[row + d] : 0.0"),
+    "linear_bwd_dropped_term": ("da[row + d] = mu[d] * A_prev + lam[d] * Bc_prev;",
+                                "da[row + d] = mu[d] * A_prev;"),
+    "linear_bwd_sign": ("mu[d] = gA[row + d] + a_next * mu[d];", "mu[d] = gA[row + d] - a_next * mu[d];"),
+    "linear_bwd_halo_index": ("const double A_prev = (t > 0) ? A[row - D + d] : 1.0;",
+                              "const double A_prev = (t > 0) ? A[row + d] : 1.0;"),
+    "log_value_slot": ("exp(log_values[vrow + d])", "exp(log_values[vrow - D + d])"),
+    "log_dropped_h0": ("h[d] = exp(log_values[v0 + d]);", "h[d] = 0.0;"),
+    "affine_fwd_order": ("mat_mul(At, P, tmp, k, k, k);", "mat_mul(P, At, tmp, k, k, k);"),
+    "affine_fwd_dropped_B": ("H[e] = tmp[e] + Bm[s * kv + e];", "H[e] = tmp[e];"),
+    "affine_bwd_untransposed": ("mat_tmul(Anext, M, tmp, k, k, k);", "mat_mul(Anext, M, tmp, k, k, k);"),
+    "affine_bwd_dropped_term": ("mat_mul_tadd(L, Bprev, dAt, k, v, k);", ""),
+    "matmul_transposed_operand": ("s += X[i * m + l] * Y[l * c + j];", "s += X[l * m + i] * Y[l * c + j];"),
+}
+
+
+def test_planted_mistakes_are_caught():
+    src = open(oracle._SRC).read()
+    tmp = tempfile.mkdtemp(prefix="orc_mut_")
+    try:
+        for name, (old, new) in MUTANTS.items():
+            assert src.count(old) == 1, name
+            path = os.path.join(tmp, f"{name}.c")
+            with open(path, "w") as f:
+                f.write(src.replace(old, new))
+            orc = oracle.Oracle(oracle.build(force=True, src=path, out=path[:-2] + ".so"))
+            caught = []
+            for pin in PINS:
+                try:
+                    pin(orc)
+                except AssertionError:
+                    caught.append(pin.__name__)
+            assert caught, f"planted mistake {name} passed every pin"
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
