@@ -1,0 +1,177 @@
+/*
+ * mg_scan.h -- C ABI of the GB300 (sm_103a) minGRU scan library.
+ *
+ * The operations are those of the page "minGRU - Triton kernels"
+ * (mingru.triton_scans API reference, section "Kernel entry points"):
+ *
+ *   mg_linear_scan_fwd   <- linear_scan_fwd        ("Channel-tiled k=1 affine prefix scan")
+ *   mg_linear_scan_bwd   <- linear_scan_bwd        ("Channel-tiled k=1 affine-scan adjoint")
+ *   mg_log_scan_fwd      <- parallel_scan_log_fwd  ("Fused log-space forward scan")
+ *   mg_affine_scan_fwd   <- affine_scan_fwd        ("Generic k x k affine prefix scan")
+ *   mg_affine_scan_bwd   <- affine_scan_bwd        ("Generic k x k affine-scan adjoint")
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout.  Every tensor is dense, row-major (C order), last dimension
+ *   fastest: (B,T,D) element (b,t,d) sits at (b*T + t)*D + d; (B,T,n,k,k)
+ *   element (b,t,n,i,j) is row i, column j of the step-t matrix.  Time index
+ *   t = 1..T in the formulas is stored at 0..T-1.
+ * Pointers.  All tensor pointers are DEVICE pointers of the current device,
+ *   16-byte aligned.  Inputs are read-only; outputs are written in full and
+ *   must not overlap any input or each other.
+ * Ownership.  The caller allocates every input, output and workspace buffer.
+ *   The library allocates nothing, frees nothing and keeps no state between
+ *   calls apart from what it leaves in the caller's workspace.
+ * Workspace.  Each call needs a device workspace of at least the size the
+ *   matching *_workspace_size function returns, 256-byte aligned, zero-filled
+ *   before its FIRST use (mg_workspace_init does that, or any memset to 0).
+ *   After that a workspace may be reused by any later call of any op and any
+ *   size up to the one it was sized for, without clearing: each launch resets
+ *   its own control words.  One workspace serves one call at a time: calls
+ *   that overlap on the GPU (two streams, or two threads) must use separate
+ *   workspaces or they race.
+ * Streams.  Calls are asynchronous on `stream` (0 = the legacy default
+ *   stream).  Argument errors are reported synchronously, before any launch,
+ *   by the return value.  The device-side chunk look-back waits are bounded;
+ *   if one gives up (a predecessor chunk never published), the kernel still
+ *   finishes, the outputs are unspecified, and the next mg_workspace_status
+ *   on that workspace returns MG_ERR_TIMEOUT.
+ * Errors.  Every entry point returns an mg_status.  On failure
+ *   mg_last_error_detail() gives a human-readable reason (thread-local, valid
+ *   until the next call on the same thread).  An out-of-envelope request
+ *   (unsupported dtype, k or v) returns MG_ERR_UNSUPPORTED: there is never a
+ *   silent downgrade to another implementation.
+ * Degenerate sizes.  B, T, D, n equal to 0 return MG_OK without a launch
+ *   (for mg_log_scan_fwd, T = 0 still needs log_values of shape (B,1,D), which
+ *   is not read).  Negative sizes return MG_ERR_INVALID_ARG.
+ * Precision.  Arithmetic and outputs are float32.  bf16 inputs (MG_BF16)
+ *   are widened to float32 on load.
+ */
+#ifndef MG_SCAN_H
+#define MG_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MG_SCAN_ABI_VERSION 1
+
+typedef enum mg_status {
+    MG_OK = 0,
+    MG_ERR_INVALID_ARG = 1,  /* bad pointer, alignment, size, overlap or workspace */
+    MG_ERR_UNSUPPORTED = 2,  /* outside the kernels' envelope (dtype, k, v)        */
+    MG_ERR_LAUNCH = 3,       /* the CUDA runtime refused the launch                */
+    MG_ERR_TIMEOUT = 4       /* a bounded device-side look-back wait gave up       */
+} mg_status;
+
+typedef enum mg_dtype {
+    MG_F32 = 0,
+    MG_BF16 = 1
+} mg_dtype;
+
+/* ABI version of the loaded library (MG_SCAN_ABI_VERSION at build time). */
+int mg_abi_version(void);
+
+/* Short fixed text for a status code. */
+const char *mg_strerror(mg_status status);
+
+/* Detail of the last failure on this thread ("" if none). */
+const char *mg_last_error_detail(void);
+
+/* Workspace bytes for mg_linear_scan_fwd and mg_linear_scan_bwd on (B,T,D),
+ * for either input dtype.  Returns 0 for invalid (negative) sizes. */
+size_t mg_linear_scan_workspace_size(int64_t B, int64_t T, int64_t D);
+
+/* Workspace bytes for mg_log_scan_fwd on log_coeffs of shape (B,T,D). */
+size_t mg_log_scan_workspace_size(int64_t B, int64_t T, int64_t D);
+
+/* Workspace bytes for mg_affine_scan_fwd and mg_affine_scan_bwd on
+ * A (B,T,n,k,k), Bm (B,T,n,k,v).  Returns 0 for an unsupported k or v. */
+size_t mg_affine_scan_workspace_size(int64_t B, int64_t T, int64_t n, int k, int v);
+
+/* Zero-fill a workspace before its first use (cudaMemsetAsync on `stream`). */
+mg_status mg_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Synchronise `stream`, then report whether any launch since the last check
+ * on this workspace gave up a look-back wait (MG_ERR_TIMEOUT), and clear the
+ * record.  MG_OK otherwise. */
+mg_status mg_workspace_status(void *ws, cudaStream_t stream);
+
+/*
+ * linear_scan_fwd (page section "linear_scan_fwd"): a, b of shape (B,T,D)
+ * with dtype in_dt (MG_F32 or MG_BF16, the same for both).  Writes float32
+ *   A[b,t,d]  = a_t * A_{t-1},          A_0 = 1  (running product, inclusive)
+ *   Bc[b,t,d] = a_t * Bc_{t-1} + b_t,   Bc_0 = 0 (the h_0 = 0 solution)
+ * for every channel (b,d) independently.  A and Bc are (B,T,D) float32.
+ */
+mg_status mg_linear_scan_fwd(const void *a, const void *b, mg_dtype in_dt,
+                             float *A, float *Bc,
+                             int64_t B, int64_t T, int64_t D,
+                             void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * linear_scan_bwd (page section "linear_scan_bwd"): reads the forward input
+ * a (dtype a_dt), the forward outputs A, Bc and the upstream gradients gA,
+ * gBc (all (B,T,D), float32 except a), and writes da = dL/da, db = dL/db of
+ * L = sum(gA*A) + sum(gBc*Bc) (float32, (B,T,D)):
+ *   mu_t  = gA_t  + a_{t+1} mu_{t+1},   lam_t = gBc_t + a_{t+1} lam_{t+1}  (zero past T)
+ *   db_t  = lam_t,   da_t = mu_t A_{t-1} + lam_t Bc_{t-1}   (A_0 = 1, Bc_0 = 0)
+ * The operator b is not needed.  A and Bc are used as given.
+ */
+mg_status mg_linear_scan_bwd(const void *a, mg_dtype a_dt,
+                             const float *A, const float *Bc,
+                             const float *gA, const float *gBc,
+                             float *da, float *db,
+                             int64_t B, int64_t T, int64_t D,
+                             void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * parallel_scan_log_fwd (page section "parallel_scan_log_fwd"):
+ * log_coeffs (B,T,D) and log_values (B,T+1,D) float32, slot 0 of log_values
+ * = log h_0 and slots 1..T = log b_t.  Writes the linear-space states
+ *   h[b,t-1,d] = h_t = exp(log_coeffs[b,t-1,d]) h_{t-1} + exp(log_values[b,t,d])
+ * for t = 1..T, computed as a log-space scan (log-sum-exp combine), so the
+ * running products may leave float32 range without loss.  -inf inputs mean
+ * zero coefficients or values and give h = 0 where every term is zero, never
+ * NaN.  h is (B,T,D) float32.
+ */
+mg_status mg_log_scan_fwd(const float *log_coeffs, const float *log_values, float *h,
+                          int64_t B, int64_t T, int64_t D,
+                          void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * affine_scan_fwd (page section "affine_scan_fwd"): A (B,T,n,k,k) and
+ * Bm (B,T,n,k,v) float32.  For every (b,n) independently writes
+ *   Abar_t = A_t @ Abar_{t-1},          Abar_0 = I   (composition A_current @ A_earlier)
+ *   Bbar_t = A_t @ Bbar_{t-1} + B_t,    Bbar_0 = 0
+ * Abar has the shape of A, Bbar that of Bm.  k, v in {1, 2, 4, 8, 16}.
+ */
+mg_status mg_affine_scan_fwd(const float *A, const float *Bm, float *Abar, float *Bbar,
+                             int64_t B, int64_t T, int64_t n, int k, int v,
+                             void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * affine_scan_bwd (page section "affine_scan_bwd"): reads the forward input
+ * A, the forward outputs Abar, Bbar and the upstream gradients gAbar, gBbar
+ * (shapes of Abar, Bbar) and writes dA (shape of A) and dB (shape of Bbar),
+ * the gradients of L = <gAbar, Abar> + <gBbar, Bbar>:
+ *   M_t = gAbar_t + A_{t+1}^T M_{t+1},   Lam_t = gBbar_t + A_{t+1}^T Lam_{t+1}  (zero past T)
+ *   dB_t = Lam_t,   dA_t = M_t Abar_{t-1}^T + Lam_t Bbar_{t-1}^T   (Abar_0 = I, Bbar_0 = 0)
+ * k, v in {1, 2, 4, 8, 16}.
+ */
+mg_status mg_affine_scan_bwd(const float *A, const float *Abar, const float *Bbar,
+                             const float *gAbar, const float *gBbar,
+                             float *dA, float *dB,
+                             int64_t B, int64_t T, int64_t n, int k, int v,
+                             void *ws, size_t ws_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MG_SCAN_H */

@@ -1,1 +1,295 @@
-"""GB300-native minGRU scan library (placeholder; the binding follows)."""
+"""GB300-native (sm_103a) minGRU scan family: Python binding of ``libmgscan.so``.
+
+The functions below marshal torch CUDA tensors into the C ABI declared in
+``include/mg_scan.h`` and nothing more: every step of every op runs in the
+library's CUDA kernels.  torch is used only for device memory and the current
+stream.  There is no fallback: if the library is missing or a call fails, an
+exception is raised.
+
+Ops (names of the C entry points; aliases with the names of the page
+"minGRU - Triton kernels" follow them):
+
+* ``mg_linear_scan_fwd(a, b)              -> (A, Bc)``       alias ``linear_scan_fwd``
+* ``mg_linear_scan_bwd(a, A, Bc, gA, gBc) -> (da, db)``      alias ``linear_scan_bwd``
+* ``mg_log_scan_fwd(log_coeffs, log_values) -> h``           alias ``parallel_scan_log_fwd``
+* ``mg_affine_scan_fwd(A, Bm)             -> (Abar, Bbar)``  alias ``affine_scan_fwd``
+* ``mg_affine_scan_bwd(A, Abar, Bbar, gAbar, gBbar) -> (dA, dB)``  alias ``affine_scan_bwd``
+
+Every op accepts optional preallocated outputs (``out=(...)``), a workspace
+tensor (``ws=``, uint8, zero-filled before first use) and a stream
+(``stream=``, a ``torch.cuda.Stream``); by default outputs are allocated with
+``torch.empty``, a cached per-(device, stream) workspace is used and the call
+is issued on the current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "MgScanError", "load", "library_path",
+    "mg_linear_scan_fwd", "mg_linear_scan_bwd", "mg_log_scan_fwd",
+    "mg_affine_scan_fwd", "mg_affine_scan_bwd",
+    "linear_scan_fwd", "linear_scan_bwd", "parallel_scan_log_fwd",
+    "affine_scan_fwd", "affine_scan_bwd",
+    "linear_workspace_size", "log_workspace_size", "affine_workspace_size",
+    "workspace_status", "new_workspace",
+]
+
+MG_OK, MG_ERR_INVALID_ARG, MG_ERR_UNSUPPORTED, MG_ERR_LAUNCH, MG_ERR_TIMEOUT = range(5)
+MG_F32, MG_BF16 = 0, 1
+
+SYMBOLS = (
+    "mg_abi_version", "mg_strerror", "mg_last_error_detail",
+    "mg_linear_scan_workspace_size", "mg_log_scan_workspace_size",
+    "mg_affine_scan_workspace_size", "mg_workspace_init", "mg_workspace_status",
+    "mg_linear_scan_fwd", "mg_linear_scan_bwd", "mg_log_scan_fwd",
+    "mg_affine_scan_fwd", "mg_affine_scan_bwd",
+)
+
+
+class MgScanError(RuntimeError):
+    """A failed call into libmgscan; ``status`` is the mg_status code."""
+
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load():
+    """Load ``libmgscan.so`` (built by ``__graft_entry__.build()`` or
+    ``python -m linear_recurrence_scans_gb300._build``).  Raises if missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build the CUDA library first "
+                               "(python -m linear_recurrence_scans_gb300._build)")
+        lib = ctypes.CDLL(path)
+        vp, i64, sz, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
+        st = ctypes.c_int
+        lib.mg_abi_version.argtypes, lib.mg_abi_version.restype = [], i32
+        lib.mg_strerror.argtypes, lib.mg_strerror.restype = [st], ctypes.c_char_p
+        lib.mg_last_error_detail.argtypes, lib.mg_last_error_detail.restype = [], ctypes.c_char_p
+        lib.mg_linear_scan_workspace_size.argtypes = [i64, i64, i64]
+        lib.mg_log_scan_workspace_size.argtypes = [i64, i64, i64]
+        lib.mg_affine_scan_workspace_size.argtypes = [i64, i64, i64, i32, i32]
+        for f in (lib.mg_linear_scan_workspace_size, lib.mg_log_scan_workspace_size,
+                  lib.mg_affine_scan_workspace_size):
+            f.restype = sz
+        lib.mg_workspace_init.argtypes = [vp, sz, vp]
+        lib.mg_workspace_status.argtypes = [vp, vp]
+        lib.mg_linear_scan_fwd.argtypes = [vp, vp, i32, vp, vp, i64, i64, i64, vp, sz, vp]
+        lib.mg_linear_scan_bwd.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, sz, vp]
+        lib.mg_log_scan_fwd.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
+        lib.mg_affine_scan_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, vp, sz, vp]
+        lib.mg_affine_scan_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, i32,
+                                           vp, sz, vp]
+        for name in ("mg_workspace_init", "mg_workspace_status", "mg_linear_scan_fwd",
+                     "mg_linear_scan_bwd", "mg_log_scan_fwd", "mg_affine_scan_fwd",
+                     "mg_affine_scan_bwd"):
+            getattr(lib, name).restype = st
+        _lib = lib
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != MG_OK:
+        lib = load()
+        msg = lib.mg_strerror(status).decode()
+        detail = lib.mg_last_error_detail().decode()
+        raise MgScanError(status, f"{what}: {msg}" + (f" ({detail})" if detail else ""))
+
+
+# ---------------------------------------------------------------- workspace
+
+def linear_workspace_size(B: int, T: int, D: int) -> int:
+    return int(load().mg_linear_scan_workspace_size(B, T, D))
+
+
+def log_workspace_size(B: int, T: int, D: int) -> int:
+    return int(load().mg_log_scan_workspace_size(B, T, D))
+
+
+def affine_workspace_size(B: int, T: int, n: int, k: int, v: int) -> int:
+    return int(load().mg_affine_scan_workspace_size(B, T, n, k, v))
+
+
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    """A zero-filled uint8 device buffer usable as a workspace."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+_ws_cache: dict = {}
+
+
+def _stream_handle(stream, device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return int(s.cuda_stream)
+
+
+def _workspace(nbytes: int, device, stream_handle: int, ws):
+    if ws is not None:
+        if ws.device != device or ws.dtype != torch.uint8 or not ws.is_contiguous():
+            raise ValueError("ws must be a contiguous uint8 tensor on the op's device")
+        return ws
+    key = (device.index, stream_handle)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        # Zero-filled on the current stream; wait for it so that the op's
+        # stream (possibly another one) sees a cleared workspace.
+        buf = new_workspace(int(nbytes * 1.25) + 4096, device)
+        torch.cuda.current_stream(device).synchronize()
+        _ws_cache[key] = buf
+    return buf
+
+
+def workspace_status(ws: torch.Tensor | None = None, stream=None) -> None:
+    """Raise MgScanError(MG_ERR_TIMEOUT) if a look-back wait gave up on ``ws``
+    (default: every cached workspace) since the last check."""
+    bufs = [ws] if ws is not None else list(_ws_cache.values())
+    for b in bufs:
+        _check(load().mg_workspace_status(b.data_ptr(), _stream_handle(stream, b.device)),
+               "mg_workspace_status")
+
+
+# ---------------------------------------------------------------- helpers
+
+def _prep(x: torch.Tensor, name: str, dtypes=(torch.float32,)) -> torch.Tensor:
+    if not isinstance(x, torch.Tensor) or not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if x.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {x.dtype} not in {dtypes}")
+    x = x.contiguous()
+    if x.data_ptr() % 16:
+        x = x.clone()
+    return x
+
+
+def _out(out, i, shape, like):
+    if out is not None and out[i] is not None:
+        o = out[i]
+        if tuple(o.shape) != tuple(shape) or o.dtype != torch.float32 or not o.is_contiguous() \
+                or o.device != like.device:
+            raise ValueError(f"out[{i}] must be a contiguous float32 tensor of shape {tuple(shape)}")
+        return o
+    return torch.empty(shape, dtype=torch.float32, device=like.device)
+
+
+_DT = {torch.float32: MG_F32, torch.bfloat16: MG_BF16}
+
+
+# ---------------------------------------------------------------- ops
+
+def mg_linear_scan_fwd(a, b, *, out=None, ws=None, stream=None):
+    """(A, Bc), float32 (B,T,D): A_t = a_t A_{t-1}, Bc_t = a_t Bc_{t-1} + b_t.
+    a, b: (B,T,D), both float32 or both bf16."""
+    a = _prep(a, "a", (torch.float32, torch.bfloat16))
+    b = _prep(b, "b", (a.dtype,))
+    if a.dim() != 3 or b.shape != a.shape:
+        raise ValueError("a and b must both be (B, T, D)")
+    B, T, D = a.shape
+    A, Bc = _out(out, 0, a.shape, a), _out(out, 1, a.shape, a)
+    sh = _stream_handle(stream, a.device)
+    w = _workspace(linear_workspace_size(B, T, D), a.device, sh, ws)
+    _check(load().mg_linear_scan_fwd(a.data_ptr(), b.data_ptr(), _DT[a.dtype], A.data_ptr(),
+                                     Bc.data_ptr(), B, T, D, w.data_ptr(), w.numel(), sh),
+           "mg_linear_scan_fwd")
+    return A, Bc
+
+
+def mg_linear_scan_bwd(a, A, Bc, gA, gBc, *, out=None, ws=None, stream=None):
+    """(da, db), float32 (B,T,D): grads of sum(gA*A) + sum(gBc*Bc) w.r.t. a, b.
+    a: float32 or bf16; A, Bc, gA, gBc: float32, all (B,T,D)."""
+    a = _prep(a, "a", (torch.float32, torch.bfloat16))
+    A, Bc, gA, gBc = (_prep(x, n) for x, n in ((A, "A"), (Bc, "Bc"), (gA, "gA"), (gBc, "gBc")))
+    if a.dim() != 3 or any(x.shape != a.shape for x in (A, Bc, gA, gBc)):
+        raise ValueError("a, A, Bc, gA, gBc must all be (B, T, D)")
+    B, T, D = a.shape
+    da, db = _out(out, 0, a.shape, a), _out(out, 1, a.shape, a)
+    sh = _stream_handle(stream, a.device)
+    w = _workspace(linear_workspace_size(B, T, D), a.device, sh, ws)
+    _check(load().mg_linear_scan_bwd(a.data_ptr(), _DT[a.dtype], A.data_ptr(), Bc.data_ptr(),
+                                     gA.data_ptr(), gBc.data_ptr(), da.data_ptr(), db.data_ptr(),
+                                     B, T, D, w.data_ptr(), w.numel(), sh),
+           "mg_linear_scan_bwd")
+    return da, db
+
+
+def mg_log_scan_fwd(log_coeffs, log_values, *, out=None, ws=None, stream=None):
+    """h (B,T,D) float32 from log_coeffs (B,T,D) and log_values (B,T+1,D)."""
+    lc = _prep(log_coeffs, "log_coeffs")
+    lv = _prep(log_values, "log_values")
+    if lc.dim() != 3:
+        raise ValueError("log_coeffs must be (B, T, D)")
+    B, T, D = lc.shape
+    if tuple(lv.shape) != (B, T + 1, D):
+        raise ValueError("log_values must be (B, T+1, D)")
+    h = _out(None if out is None else (out,), 0, lc.shape, lc)
+    sh = _stream_handle(stream, lc.device)
+    w = _workspace(log_workspace_size(B, T, D), lc.device, sh, ws)
+    _check(load().mg_log_scan_fwd(lc.data_ptr(), lv.data_ptr(), h.data_ptr(), B, T, D,
+                                  w.data_ptr(), w.numel(), sh),
+           "mg_log_scan_fwd")
+    return h
+
+
+def mg_affine_scan_fwd(A, Bm, *, out=None, ws=None, stream=None):
+    """(Abar, Bbar) for A (B,T,n,k,k), Bm (B,T,n,k,v), float32."""
+    A = _prep(A, "A")
+    Bm = _prep(Bm, "Bm")
+    if A.dim() != 5 or A.shape[3] != A.shape[4] or Bm.dim() != 5 or Bm.shape[:4] != A.shape[:4]:
+        raise ValueError("A must be (B,T,n,k,k) and Bm (B,T,n,k,v)")
+    B, T, n, k, _ = A.shape
+    v = Bm.shape[4]
+    Abar, Bbar = _out(out, 0, A.shape, A), _out(out, 1, Bm.shape, A)
+    sh = _stream_handle(stream, A.device)
+    w = _workspace(affine_workspace_size(B, T, n, k, v), A.device, sh, ws)
+    _check(load().mg_affine_scan_fwd(A.data_ptr(), Bm.data_ptr(), Abar.data_ptr(), Bbar.data_ptr(),
+                                     B, T, n, k, v, w.data_ptr(), w.numel(), sh),
+           "mg_affine_scan_fwd")
+    return Abar, Bbar
+
+
+def mg_affine_scan_bwd(A, Abar, Bbar, gAbar, gBbar, *, out=None, ws=None, stream=None):
+    """(dA, dB): grads of <gAbar, Abar> + <gBbar, Bbar> w.r.t. A and Bm, float32."""
+    A, Abar, Bbar, gAbar, gBbar = (_prep(x, nm) for x, nm in (
+        (A, "A"), (Abar, "Abar"), (Bbar, "Bbar"), (gAbar, "gAbar"), (gBbar, "gBbar")))
+    if A.dim() != 5 or Abar.shape != A.shape or gAbar.shape != A.shape \
+            or Bbar.dim() != 5 or gBbar.shape != Bbar.shape or Bbar.shape[:4] != A.shape[:4]:
+        raise ValueError("A, Abar, gAbar must be (B,T,n,k,k) and Bbar, gBbar (B,T,n,k,v)")
+    B, T, n, k, _ = A.shape
+    v = Bbar.shape[4]
+    dA, dB = _out(out, 0, A.shape, A), _out(out, 1, Bbar.shape, A)
+    sh = _stream_handle(stream, A.device)
+    w = _workspace(affine_workspace_size(B, T, n, k, v), A.device, sh, ws)
+    _check(load().mg_affine_scan_bwd(A.data_ptr(), Abar.data_ptr(), Bbar.data_ptr(),
+                                     gAbar.data_ptr(), gBbar.data_ptr(), dA.data_ptr(),
+                                     dB.data_ptr(), B, T, n, k, v, w.data_ptr(), w.numel(), sh),
+           "mg_affine_scan_bwd")
+    return dA, dB
+
+
+# Names of the page "minGRU - Triton kernels".
+linear_scan_fwd = mg_linear_scan_fwd
+linear_scan_bwd = mg_linear_scan_bwd
+parallel_scan_log_fwd = mg_log_scan_fwd
+affine_scan_fwd = mg_affine_scan_fwd
+affine_scan_bwd = mg_affine_scan_bwd

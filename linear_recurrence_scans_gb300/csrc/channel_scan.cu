@@ -1,0 +1,688 @@
+// Channel-wise chunked scans on (B,T,D): linear_scan_fwd, linear_scan_bwd and
+// parallel_scan_log_fwd of the page "minGRU - Triton kernels".
+//
+// All three evaluate the same associative pair operator
+//     (a1, b1) o (a2, b2) = (a2 a1, a2 b1 + b2)        (element 1 earlier)
+// over time, independently for every channel (b, d), in one kernel shape:
+//
+//   * a CTA owns a tile of DC = TX*VEC channels by TY*L time steps, taken by
+//     ticket (chunk-major, so predecessors have always started);
+//   * each thread loads VEC channels (one 16-byte vector) for L consecutive
+//     steps straight into registers -- a warp row reads 32 x 16 contiguous
+//     bytes, fully coalesced -- and folds them into its aggregate;
+//   * the TY thread aggregates of a channel are combined through shared memory;
+//   * warp 0 finds the chunk's carry-in by decoupled look-back over the
+//     previous chunks of the same channel tile (lookback.cuh);
+//   * every thread composes carry o (aggregates of the earlier threads of its
+//     chunk) and re-runs its L steps sequentially from that state, writing the
+//     outputs.  The re-run keeps the inputs in registers, so each input is read
+//     from HBM once and each output written once.
+//
+// The backward op is the same engine run in reverse time on the adjoint
+// recurrence; the log op carries log-space values as (m, s) with
+// value = s * 2^m so that one exp2 per combine suffices.
+#include <cmath>
+
+#include "common.cuh"
+
+namespace mg {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct ChanGeom {
+    int64_t B, T, D;
+    int nJb;  // channel tiles per batch row
+    int nJ;   // channel tiles in total (B * nJb)
+    int nC;   // chunks along time
+    unsigned n_tiles;  // nJ * nC
+};
+
+template <int NS, int VEC>
+struct St {
+    float v[NS][VEC];
+};
+
+// ----------------------------------------------------------- linear forward
+// Element of step t: (a_t, b_t).  State: (running product, h).
+template <typename Tin, int VEC_, int L_>
+struct LinFwd {
+    static constexpr int NS = 2, VEC = VEC_, L = L_;
+    static constexpr bool kReverse = false;
+    using S = St<NS, VEC>;
+    struct Args {
+        const Tin *a;
+        const Tin *b;
+        float *A;
+        float *Bc;
+    };
+    struct Regs {
+        float a[L][VEC];
+        float b[L][VEC];
+    };
+
+    __device__ static void load(const Args &p, const ChanGeom &g, int64_t bb, int64_t t0, int d,
+                                bool act, Regs &r)
+    {
+#pragma unroll
+        for (int i = 0; i < L; ++i) {
+            const int64_t t = t0 + i;
+            if (act && t < g.T) {
+                const int64_t off = (bb * g.T + t) * g.D + d;
+                load_vec<VEC>(p.a + off, r.a[i]);
+                load_vec<VEC>(p.b + off, r.b[i]);
+            } else {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    r.a[i][v] = 1.f;
+                    r.b[i][v] = 0.f;
+                }
+            }
+        }
+    }
+    __device__ static S element(const Regs &r, int i)
+    {
+        S e;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            e.v[0][v] = r.a[i][v];
+            e.v[1][v] = r.b[i][v];
+        }
+        return e;
+    }
+    __device__ static S identity()
+    {
+        S e;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            e.v[0][v] = 1.f;
+            e.v[1][v] = 0.f;
+        }
+        return e;
+    }
+    __device__ static S initial(const Args &, const ChanGeom &, int64_t, int, bool)
+    {
+        return identity();
+    }
+    __device__ static S combine(const S &x, const S &y)
+    {
+        S o;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            o.v[0][v] = y.v[0][v] * x.v[0][v];
+            o.v[1][v] = fmaf(y.v[0][v], x.v[1][v], y.v[1][v]);
+        }
+        return o;
+    }
+    __device__ static void epilogue(const Args &p, const ChanGeom &g, int64_t bb, int64_t t0,
+                                    int d, bool act, const Regs &r, const S &st)
+    {
+        float P[VEC], H[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            P[v] = st.v[0][v];
+            H[v] = st.v[1][v];
+        }
+#pragma unroll
+        for (int i = 0; i < L; ++i) {
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                P[v] = r.a[i][v] * P[v];
+                H[v] = fmaf(r.a[i][v], H[v], r.b[i][v]);
+            }
+            const int64_t t = t0 + i;
+            if (act && t < g.T) {
+                const int64_t off = (bb * g.T + t) * g.D + d;
+                store_vec<VEC>(p.A + off, P);
+                store_vec<VEC>(p.Bc + off, H);
+            }
+        }
+    }
+};
+
+// ---------------------------------------------------------- linear backward
+// Reverse time.  Element of step t: (c_t = a_{t+1}, gA_t, gBc_t) with
+// c_{T} = 0; state (C, mu, lam): mu_t = gA_t + c_t mu_{t+1}, same for lam.
+template <typename Tin, int VEC_, int L_>
+struct LinBwd {
+    static constexpr int NS = 3, VEC = VEC_, L = L_;
+    static constexpr bool kReverse = true;
+    using S = St<NS, VEC>;
+    struct Args {
+        const Tin *a;
+        const float *A;
+        const float *Bc;
+        const float *gA;
+        const float *gBc;
+        float *da;
+        float *db;
+    };
+    struct Regs {
+        float c[L][VEC];
+        float gA[L][VEC];
+        float gB[L][VEC];
+    };
+
+    __device__ static void load(const Args &p, const ChanGeom &g, int64_t bb, int64_t t0, int d,
+                                bool act, Regs &r)
+    {
+#pragma unroll
+        for (int i = 0; i < L; ++i) {
+            const int64_t t = t0 + i;
+            if (act && t < g.T) {
+                const int64_t off = (bb * g.T + t) * g.D + d;
+                load_vec<VEC>(p.gA + off, r.gA[i]);
+                load_vec<VEC>(p.gBc + off, r.gB[i]);
+                if (t + 1 < g.T) {
+                    load_vec<VEC>(p.a + off + g.D, r.c[i]);
+                } else {
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) r.c[i][v] = 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    r.c[i][v] = 1.f;
+                    r.gA[i][v] = 0.f;
+                    r.gB[i][v] = 0.f;
+                }
+            }
+        }
+    }
+    __device__ static S element(const Regs &r, int i)
+    {
+        S e;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            e.v[0][v] = r.c[i][v];
+            e.v[1][v] = r.gA[i][v];
+            e.v[2][v] = r.gB[i][v];
+        }
+        return e;
+    }
+    __device__ static S identity()
+    {
+        S e;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            e.v[0][v] = 1.f;
+            e.v[1][v] = 0.f;
+            e.v[2][v] = 0.f;
+        }
+        return e;
+    }
+    __device__ static S initial(const Args &, const ChanGeom &, int64_t, int, bool)
+    {
+        return identity();
+    }
+    __device__ static S combine(const S &x, const S &y)
+    {
+        S o;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            o.v[0][v] = y.v[0][v] * x.v[0][v];
+            o.v[1][v] = fmaf(y.v[0][v], x.v[1][v], y.v[1][v]);
+            o.v[2][v] = fmaf(y.v[0][v], x.v[2][v], y.v[2][v]);
+        }
+        return o;
+    }
+    __device__ static void epilogue(const Args &p, const ChanGeom &g, int64_t bb, int64_t t0,
+                                    int d, bool act, const Regs &r, const S &st)
+    {
+        // A_{t-1}, Bc_{t-1} for the L steps (A_0 = 1, Bc_0 = 0 before the first step).
+        float Ap[L][VEC], Bp[L][VEC];
+#pragma unroll
+        for (int i = 0; i < L; ++i) {
+            const int64_t t = t0 + i;
+            if (act && t < g.T && t > 0) {
+                const int64_t off = (bb * g.T + t - 1) * g.D + d;
+                load_vec<VEC>(p.A + off, Ap[i]);
+                load_vec<VEC>(p.Bc + off, Bp[i]);
+            } else {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    Ap[i][v] = 1.f;
+                    Bp[i][v] = 0.f;
+                }
+            }
+        }
+        float mu[VEC], lam[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            mu[v] = st.v[1][v];
+            lam[v] = st.v[2][v];
+        }
+#pragma unroll
+        for (int i = L - 1; i >= 0; --i) {
+            float da[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                mu[v] = fmaf(r.c[i][v], mu[v], r.gA[i][v]);
+                lam[v] = fmaf(r.c[i][v], lam[v], r.gB[i][v]);
+                da[v] = fmaf(mu[v], Ap[i][v], lam[v] * Bp[i][v]);
+            }
+            const int64_t t = t0 + i;
+            if (act && t < g.T) {
+                const int64_t off = (bb * g.T + t) * g.D + d;
+                store_vec<VEC>(p.da + off, da);
+                store_vec<VEC>(p.db + off, lam);
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------- log-space forward
+// Element of step t: (lc_t, LB = lv_t) in base-2 logs.  State (la, m, s):
+// la = sum of log-coefficients, LB = m + log2(s).  Combine (x earlier):
+//   la = x.la + y.la,  LB = log2(2^(y.la + LB_x) + 2^(LB_y))
+// evaluated with one exp2 of minus the gap between the two exponents.
+template <int VEC_, int L_>
+struct LogFwd {
+    static constexpr int NS = 3, VEC = VEC_, L = L_;
+    static constexpr bool kReverse = false;
+    using S = St<NS, VEC>;
+    struct Args {
+        const float *lc;
+        const float *lv;
+        float *h;
+    };
+    struct Regs {
+        float lc[L][VEC];
+        float lv[L][VEC];
+    };
+
+    __device__ static void load(const Args &p, const ChanGeom &g, int64_t bb, int64_t t0, int d,
+                                bool act, Regs &r)
+    {
+#pragma unroll
+        for (int i = 0; i < L; ++i) {
+            const int64_t t = t0 + i;
+            if (act && t < g.T) {
+                load_vec<VEC>(p.lc + (bb * g.T + t) * g.D + d, r.lc[i]);
+                load_vec<VEC>(p.lv + (bb * (g.T + 1) + t + 1) * g.D + d, r.lv[i]);
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    r.lc[i][v] *= kLog2e;
+                    r.lv[i][v] *= kLog2e;
+                }
+            } else {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    r.lc[i][v] = 0.f;
+                    r.lv[i][v] = -INFINITY;
+                }
+            }
+        }
+    }
+    __device__ static S element(const Regs &r, int i)
+    {
+        S e;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            e.v[0][v] = r.lc[i][v];
+            e.v[1][v] = r.lv[i][v];
+            e.v[2][v] = 1.f;
+        }
+        return e;
+    }
+    __device__ static S identity()
+    {
+        S e;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            e.v[0][v] = 0.f;
+            e.v[1][v] = -INFINITY;
+            e.v[2][v] = 0.f;
+        }
+        return e;
+    }
+    // State before step 1: LB_0 = log h_0 = log_values[b, 0, d].
+    __device__ static S initial(const Args &p, const ChanGeom &g, int64_t bb, int d, bool act)
+    {
+        S e = identity();
+        if (act) {
+            float l0[VEC];
+            load_vec<VEC>(p.lv + (bb * (g.T + 1)) * g.D + d, l0);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                e.v[1][v] = l0[v] * kLog2e;
+                e.v[2][v] = 1.f;
+            }
+        }
+        return e;
+    }
+    // log2(xs 2^u + ys 2^ym) as (m, s); both exponents -inf gives (-inf, 0).
+    __device__ static void lse2(float u, float xs, float ym, float ys, float &m, float &s)
+    {
+        const float gap = u - ym;
+        const float e = exp2f(-fabsf(gap));
+        const bool ge = gap >= 0.f;
+        m = ge ? u : ym;
+        s = ge ? fmaf(ys, e, xs) : fmaf(xs, e, ys);
+        if (gap != gap) {  // -inf - -inf
+            m = -INFINITY;
+            s = 0.f;
+        }
+    }
+    __device__ static S combine(const S &x, const S &y)
+    {
+        S o;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            o.v[0][v] = x.v[0][v] + y.v[0][v];
+            lse2(y.v[0][v] + x.v[1][v], x.v[2][v], y.v[1][v], y.v[2][v], o.v[1][v], o.v[2][v]);
+        }
+        return o;
+    }
+    __device__ static void epilogue(const Args &p, const ChanGeom &g, int64_t bb, int64_t t0,
+                                    int d, bool act, const Regs &r, const S &st)
+    {
+        float m[VEC], s[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            m[v] = st.v[1][v];
+            s[v] = st.v[2][v];
+        }
+#pragma unroll
+        for (int i = 0; i < L; ++i) {
+            float h[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                lse2(r.lc[i][v] + m[v], s[v], r.lv[i][v], 1.f, m[v], s[v]);
+                h[v] = s[v] * exp2f(m[v]);
+            }
+            const int64_t t = t0 + i;
+            if (act && t < g.T) store_vec<VEC>(p.h + (bb * g.T + t) * g.D + d, h);
+        }
+    }
+};
+
+// ------------------------------------------------------------ the engine
+
+template <class Op, int TX>
+__device__ __forceinline__ float *chan_record(const Lookback &lb, size_t slot, int kind, int s,
+                                              int lane)
+{
+    constexpr int DC = TX * Op::VEC;
+    return lb.data + ((slot * 2 + kind) * Op::NS + s) * DC + lane * Op::VEC;
+}
+
+template <class Op, int TX>
+__device__ __forceinline__ void put_record(const Lookback &lb, size_t slot, int kind, int lane,
+                                           const typename Op::S &x)
+{
+#pragma unroll
+    for (int s = 0; s < Op::NS; ++s) store_vec_cg<Op::VEC>(chan_record<Op, TX>(lb, slot, kind, s, lane), x.v[s]);
+}
+
+template <class Op, int TX>
+__device__ __forceinline__ typename Op::S get_record(const Lookback &lb, size_t slot, int kind,
+                                                     int lane)
+{
+    typename Op::S x;
+#pragma unroll
+    for (int s = 0; s < Op::NS; ++s) load_vec_cg<Op::VEC>(chan_record<Op, TX>(lb, slot, kind, s, lane), x.v[s]);
+    return x;
+}
+
+// Warp 0: exclusive carry-in of chunk c for channel tile j, given the chunk
+// aggregate `cta` of this lane's channels; publishes the chunk's records.
+template <class Op, int TX>
+__device__ typename Op::S lookback_chan(const typename Op::Args &args, const ChanGeom &g,
+                                        const Lookback &lb, int c, int j, int64_t bb, int ld,
+                                        bool lact, bool lchan, unsigned tile,
+                                        unsigned long long epoch, const typename Op::S &cta)
+{
+    using S = typename Op::S;
+    const int lane = threadIdx.x & 31;
+    const size_t slot = size_t(c) * g.nJ + j;
+    S excl = Op::identity();
+    if (c == 0) {
+        excl = Op::initial(args, g, bb, ld, lchan);
+        if (lact) put_record<Op, TX>(lb, slot, 1, lane, Op::combine(excl, cta));
+        publish(lb, slot, kStatusPrefix, epoch, tile);
+        return excl;
+    }
+    if (peek_status(lb, slot - g.nJ, epoch) != kStatusPrefix) {
+        if (lact) put_record<Op, TX>(lb, slot, 0, lane, cta);
+        publish(lb, slot, kStatusAggregate, epoch, tile);
+    }
+    int p = c - 1;
+    bool ok = true;
+    for (;;) {
+        const unsigned st = wait_status(lb, size_t(p) * g.nJ + j, epoch, tile);
+        if (st == kStatusPrefix) break;
+        if (st == kStatusNone || p == 0) {  // gave up (chunk 0 never holds an aggregate only)
+            ok = false;
+            break;
+        }
+        --p;
+    }
+    if (ok && lact) {
+        excl = get_record<Op, TX>(lb, size_t(p) * g.nJ + j, 1, lane);
+        for (int q = p + 1; q < c; ++q)
+            excl = Op::combine(excl, get_record<Op, TX>(lb, size_t(q) * g.nJ + j, 0, lane));
+    }
+    if (lact) put_record<Op, TX>(lb, slot, 1, lane, Op::combine(excl, cta));
+    publish(lb, slot, kStatusPrefix, epoch, tile);
+    return excl;
+}
+
+template <class Op, int TX, int TY>
+__global__ void __launch_bounds__(TX *TY)
+    channel_scan_kernel(const typename Op::Args args, const ChanGeom g, const Lookback lb)
+{
+    using S = typename Op::S;
+    constexpr int NS = Op::NS, VEC = Op::VEC, L = Op::L;
+    constexpr int DC = TX * VEC;
+    __shared__ __align__(16) float s_agg[TY][NS][DC];
+    __shared__ __align__(16) float s_carry[NS][DC];
+
+    unsigned tile;
+    unsigned long long epoch;
+    take_ticket(lb, tile, epoch);
+    if (tile >= g.n_tiles) {  // a workspace that was not zero-filled before first use
+        if (threadIdx.x == 0) atomicOr(&lb.ctl->error, kErrBadTicket);
+        finish_cta(lb, epoch);
+        return;
+    }
+    const int c = int(tile / unsigned(g.nJ));
+    const int j = int(tile % unsigned(g.nJ));
+    const int64_t bb = j / g.nJb;
+    const int dbase = (j % g.nJb) * DC;
+    const int tx = threadIdx.x % TX, ty = threadIdx.x / TX;
+    const int d = dbase + tx * VEC;
+    const bool act = d < g.D;
+    const int ct = Op::kReverse ? (g.nC - 1 - c) : c;
+    const int64_t t0 = int64_t(ct) * (TY * L) + ty * L;
+
+    typename Op::Regs r;
+    Op::load(args, g, bb, t0, d, act, r);
+
+    S agg = Op::element(r, Op::kReverse ? L - 1 : 0);
+#pragma unroll
+    for (int k = 1; k < L; ++k) agg = Op::combine(agg, Op::element(r, Op::kReverse ? L - 1 - k : k));
+#pragma unroll
+    for (int s = 0; s < NS; ++s) store_vec<VEC>(&s_agg[ty][s][tx * VEC], agg.v[s]);
+    __syncthreads();
+
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const bool lact = lane < TX;
+        const int ld = dbase + lane * VEC;
+        const bool lchan = lact && ld < g.D;
+        S cta = Op::identity();
+        if (lact) {
+#pragma unroll
+            for (int k = 0; k < TY; ++k) {
+                const int y = Op::kReverse ? TY - 1 - k : k;
+                S x;
+#pragma unroll
+                for (int s = 0; s < NS; ++s) load_vec<VEC>(&s_agg[y][s][lane * VEC], x.v[s]);
+                cta = (k == 0) ? x : Op::combine(cta, x);
+            }
+        }
+        const S excl = lookback_chan<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch, cta);
+        if (lact) {
+#pragma unroll
+            for (int s = 0; s < NS; ++s) store_vec<VEC>(&s_carry[s][lane * VEC], excl.v[s]);
+        }
+    }
+    __syncthreads();
+
+    S st;
+#pragma unroll
+    for (int s = 0; s < NS; ++s) load_vec<VEC>(&s_carry[s][tx * VEC], st.v[s]);
+    if (!Op::kReverse) {
+        for (int y = 0; y < ty; ++y) {
+            S x;
+#pragma unroll
+            for (int s = 0; s < NS; ++s) load_vec<VEC>(&s_agg[y][s][tx * VEC], x.v[s]);
+            st = Op::combine(st, x);
+        }
+    } else {
+        for (int y = TY - 1; y > ty; --y) {
+            S x;
+#pragma unroll
+            for (int s = 0; s < NS; ++s) load_vec<VEC>(&s_agg[y][s][tx * VEC], x.v[s]);
+            st = Op::combine(st, x);
+        }
+    }
+    Op::epilogue(args, g, bb, t0, d, act, r, st);
+    finish_cta(lb, epoch);
+}
+
+// ------------------------------------------------------------ launchers
+
+template <class Op, int TX, int TY>
+struct ChanPlan {
+    static constexpr int DC = TX * Op::VEC;
+    static constexpr int TC = TY * Op::L;
+    static ChanGeom geom(int64_t B, int64_t T, int64_t D)
+    {
+        ChanGeom g;
+        g.B = B;
+        g.T = T;
+        g.D = D;
+        g.nJb = int((D + DC - 1) / DC);
+        g.nJ = int(B * g.nJb);
+        g.nC = int((T + TC - 1) / TC);
+        g.n_tiles = unsigned(g.nJ) * unsigned(g.nC);
+        return g;
+    }
+    static size_t n_tiles(int64_t B, int64_t T, int64_t D)
+    {
+        const int64_t nJ = B * ((D + DC - 1) / DC);
+        const int64_t nC = (T + TC - 1) / TC;
+        return size_t(nJ) * size_t(nC);
+    }
+    static size_t ws_bytes(int64_t B, int64_t T, int64_t D)
+    {
+        return tiled_ws_bytes(n_tiles(B, T, D), size_t(2) * Op::NS * DC * sizeof(float));
+    }
+    static mg_status launch(const typename Op::Args &args, int64_t B, int64_t T, int64_t D,
+                            void *ws, size_t ws_bytes_given, cudaStream_t s, const LaunchOpts &o,
+                            const char *name)
+    {
+        const size_t nt = n_tiles(B, T, D);
+        if (nt >= (size_t(1) << 31) || B * ((D + DC - 1) / DC) >= (int64_t(1) << 31))
+            return fail(MG_ERR_UNSUPPORTED, "%s: %zu tiles exceed the 2^31 ticket range", name, nt);
+        const size_t need = ws_bytes(B, T, D);
+        if (ws_bytes_given < need)
+            return fail(MG_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", name,
+                        ws_bytes_given, need);
+        const ChanGeom g = geom(B, T, D);
+        const Lookback lb = make_lookback(ws, nt, o);
+        channel_scan_kernel<Op, TX, TY><<<unsigned(nt), TX * TY, 0, s>>>(args, g, lb);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return fail(MG_ERR_LAUNCH, "%s: launch failed: %s", name, cudaGetErrorString(e));
+        return MG_OK;
+    }
+};
+
+// Tile choices.  fp32: 4 channels (16 B) per thread; bf16: 8 channels (16 B).
+// A D that is not a multiple of the vector width takes the 1-channel variant.
+constexpr int kTX = 32, kTY = 8;
+using LinFwdF32 = ChanPlan<LinFwd<float, 4, 8>, kTX, kTY>;
+using LinFwdF32s = ChanPlan<LinFwd<float, 1, 8>, kTX, kTY>;
+using LinFwdB16 = ChanPlan<LinFwd<bf16_t, 8, 4>, kTX, kTY>;
+using LinFwdB16s = ChanPlan<LinFwd<bf16_t, 1, 8>, kTX, kTY>;
+using LinBwdF32 = ChanPlan<LinBwd<float, 4, 4>, kTX, kTY>;
+using LinBwdF32s = ChanPlan<LinBwd<float, 1, 4>, kTX, kTY>;
+using LinBwdB16 = ChanPlan<LinBwd<bf16_t, 4, 4>, kTX, kTY>;
+using LinBwdB16s = ChanPlan<LinBwd<bf16_t, 1, 4>, kTX, kTY>;
+using LogF32 = ChanPlan<LogFwd<4, 8>, kTX, kTY>;
+using LogF32s = ChanPlan<LogFwd<1, 8>, kTX, kTY>;
+
+template <class P>
+size_t mx(size_t a, int64_t B, int64_t T, int64_t D)
+{
+    const size_t b = P::ws_bytes(B, T, D);
+    return a > b ? a : b;
+}
+
+}  // namespace
+
+size_t linear_ws_bytes(int64_t B, int64_t T, int64_t D)
+{
+    size_t m = 0;
+    m = mx<LinFwdF32>(m, B, T, D);
+    m = mx<LinFwdF32s>(m, B, T, D);
+    m = mx<LinFwdB16>(m, B, T, D);
+    m = mx<LinFwdB16s>(m, B, T, D);
+    m = mx<LinBwdF32>(m, B, T, D);
+    m = mx<LinBwdF32s>(m, B, T, D);
+    m = mx<LinBwdB16>(m, B, T, D);
+    m = mx<LinBwdB16s>(m, B, T, D);
+    return m;
+}
+
+size_t log_ws_bytes(int64_t B, int64_t T, int64_t D)
+{
+    return mx<LogF32s>(mx<LogF32>(0, B, T, D), B, T, D);
+}
+
+mg_status launch_linear_fwd(const void *a, const void *b, mg_dtype dt, float *A, float *Bc,
+                            int64_t B, int64_t T, int64_t D, void *ws, size_t wsb, cudaStream_t s,
+                            const LaunchOpts &o)
+{
+    const char *nm = "mg_linear_scan_fwd";
+    if (dt == MG_F32) {
+        using F = const float *;
+        if (D % 4 == 0)
+            return LinFwdF32::launch({F(a), F(b), A, Bc}, B, T, D, ws, wsb, s, o, nm);
+        return LinFwdF32s::launch({F(a), F(b), A, Bc}, B, T, D, ws, wsb, s, o, nm);
+    }
+    using H = const bf16_t *;
+    if (D % 8 == 0) return LinFwdB16::launch({H(a), H(b), A, Bc}, B, T, D, ws, wsb, s, o, nm);
+    return LinFwdB16s::launch({H(a), H(b), A, Bc}, B, T, D, ws, wsb, s, o, nm);
+}
+
+mg_status launch_linear_bwd(const void *a, mg_dtype dt, const float *A, const float *Bc,
+                            const float *gA, const float *gBc, float *da, float *db, int64_t B,
+                            int64_t T, int64_t D, void *ws, size_t wsb, cudaStream_t s,
+                            const LaunchOpts &o)
+{
+    const char *nm = "mg_linear_scan_bwd";
+    if (dt == MG_F32) {
+        using F = const float *;
+        if (D % 4 == 0)
+            return LinBwdF32::launch({F(a), A, Bc, gA, gBc, da, db}, B, T, D, ws, wsb, s, o, nm);
+        return LinBwdF32s::launch({F(a), A, Bc, gA, gBc, da, db}, B, T, D, ws, wsb, s, o, nm);
+    }
+    using H = const bf16_t *;
+    if (D % 4 == 0)
+        return LinBwdB16::launch({H(a), A, Bc, gA, gBc, da, db}, B, T, D, ws, wsb, s, o, nm);
+    return LinBwdB16s::launch({H(a), A, Bc, gA, gBc, da, db}, B, T, D, ws, wsb, s, o, nm);
+}
+
+mg_status launch_log_fwd(const float *lc, const float *lv, float *h, int64_t B, int64_t T,
+                         int64_t D, void *ws, size_t wsb, cudaStream_t s, const LaunchOpts &o)
+{
+    const char *nm = "mg_log_scan_fwd";
+    if (D % 4 == 0) return LogF32::launch({lc, lv, h}, B, T, D, ws, wsb, s, o, nm);
+    return LogF32s::launch({lc, lv, h}, B, T, D, ws, wsb, s, o, nm);
+}
+
+}  // namespace mg

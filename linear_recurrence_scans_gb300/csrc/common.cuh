@@ -1,0 +1,185 @@
+// Internal declarations shared by the translation units of the library.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "lookback.cuh"
+#include "mg_scan.h"
+
+namespace mg {
+
+// ---------------------------------------------------------------- host side
+
+// Record a failure detail for mg_last_error_detail() and return `st`.
+mg_status fail(mg_status st, const char *fmt, ...);
+
+// Options a launcher takes beyond the op's own arguments.
+struct LaunchOpts {
+    unsigned long long wait_limit_ns = 2000000000ull;  // 2 s of %globaltimer
+    unsigned int max_polls = 1u << 24;
+    long long stall_tile = -1;                         // testing only
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace bytes for a tiled scan with `n_tiles` records of `record_bytes`.
+inline size_t tiled_ws_bytes(size_t n_tiles, size_t record_bytes)
+{
+    return kControlBytes + align_up(n_tiles * sizeof(unsigned long long), 256) +
+           n_tiles * record_bytes;
+}
+
+// Build the device-side look-back view of a workspace for `n_tiles` records.
+inline Lookback make_lookback(void *ws, size_t n_tiles, const LaunchOpts &o)
+{
+    Lookback lb;
+    char *base = static_cast<char *>(ws);
+    lb.ctl = reinterpret_cast<Control *>(base);
+    lb.flags = reinterpret_cast<unsigned long long *>(base + kControlBytes);
+    lb.data = reinterpret_cast<float *>(
+        base + kControlBytes + align_up(n_tiles * sizeof(unsigned long long), 256));
+    lb.wait_limit_ns = o.wait_limit_ns;
+    lb.max_polls = o.max_polls;
+    lb.stall_tile = o.stall_tile;
+    return lb;
+}
+
+// Launchers (defined in channel_scan.cu / affine_scan.cu).  They assume the
+// arguments were validated by the C entry points and B, T, D > 0.
+size_t linear_ws_bytes(int64_t B, int64_t T, int64_t D);
+size_t log_ws_bytes(int64_t B, int64_t T, int64_t D);
+size_t affine_ws_bytes(int64_t B, int64_t T, int64_t n, int k, int v);
+
+mg_status launch_linear_fwd(const void *a, const void *b, mg_dtype dt, float *A, float *Bc,
+                            int64_t B, int64_t T, int64_t D, void *ws, size_t ws_bytes,
+                            cudaStream_t s, const LaunchOpts &o);
+mg_status launch_linear_bwd(const void *a, mg_dtype dt, const float *A, const float *Bc,
+                            const float *gA, const float *gBc, float *da, float *db,
+                            int64_t B, int64_t T, int64_t D, void *ws, size_t ws_bytes,
+                            cudaStream_t s, const LaunchOpts &o);
+mg_status launch_log_fwd(const float *lc, const float *lv, float *h, int64_t B, int64_t T,
+                         int64_t D, void *ws, size_t ws_bytes, cudaStream_t s,
+                         const LaunchOpts &o);
+mg_status launch_affine_fwd(const float *A, const float *Bm, float *Abar, float *Bbar,
+                            int64_t B, int64_t T, int64_t n, int k, int v, void *ws,
+                            size_t ws_bytes, cudaStream_t s, const LaunchOpts &o);
+mg_status launch_affine_bwd(const float *A, const float *Abar, const float *Bbar,
+                            const float *gAbar, const float *gBbar, float *dA, float *dB,
+                            int64_t B, int64_t T, int64_t n, int k, int v, void *ws,
+                            size_t ws_bytes, cudaStream_t s, const LaunchOpts &o);
+
+// ------------------------------------------------------------- device side
+
+// bf16 storage type (raw bits); widening to float32 is exact.
+struct bf16_t {
+    unsigned short bits;
+};
+
+__device__ __forceinline__ float bf16_bits_to_float(unsigned int bits16)
+{
+    return __uint_as_float(bits16 << 16);
+}
+
+// Load VEC consecutive elements starting at p (aligned to VEC elements) and
+// widen them to float32.
+template <int VEC>
+__device__ __forceinline__ void load_vec(const float *p, float (&o)[VEC])
+{
+    if constexpr (VEC % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+            const float4 x = *reinterpret_cast<const float4 *>(p + 4 * q);
+            o[4 * q + 0] = x.x;
+            o[4 * q + 1] = x.y;
+            o[4 * q + 2] = x.z;
+            o[4 * q + 3] = x.w;
+        }
+    } else if constexpr (VEC == 2) {
+        const float2 x = *reinterpret_cast<const float2 *>(p);
+        o[0] = x.x;
+        o[1] = x.y;
+    } else {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) o[v] = p[v];
+    }
+}
+
+template <int VEC>
+__device__ __forceinline__ void load_vec(const bf16_t *p, float (&o)[VEC])
+{
+    if constexpr (VEC % 8 == 0) {
+#pragma unroll
+        for (int q = 0; q < VEC / 8; ++q) {
+            const uint4 x = *reinterpret_cast<const uint4 *>(p + 8 * q);
+            const unsigned w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                o[8 * q + 2 * e + 0] = __uint_as_float(w[e] << 16);
+                o[8 * q + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+            }
+        }
+    } else if constexpr (VEC == 4) {
+        const uint2 x = *reinterpret_cast<const uint2 *>(p);
+        o[0] = __uint_as_float(x.x << 16);
+        o[1] = __uint_as_float(x.x & 0xffff0000u);
+        o[2] = __uint_as_float(x.y << 16);
+        o[3] = __uint_as_float(x.y & 0xffff0000u);
+    } else {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) o[v] = bf16_bits_to_float(p[v].bits);
+    }
+}
+
+// Store VEC consecutive float32 values at p (aligned to VEC elements).
+template <int VEC>
+__device__ __forceinline__ void store_vec(float *p, const float (&x)[VEC])
+{
+    if constexpr (VEC % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q)
+            *reinterpret_cast<float4 *>(p + 4 * q) =
+                make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    } else {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) p[v] = x[v];
+    }
+}
+
+// L2-only (.cg) variants for look-back records written by one CTA and read
+// by another.
+template <int VEC>
+__device__ __forceinline__ void store_vec_cg(float *p, const float (&x)[VEC])
+{
+    if constexpr (VEC % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q)
+            __stcg(reinterpret_cast<float4 *>(p + 4 * q),
+                   make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
+    } else {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) __stcg(p + v, x[v]);
+    }
+}
+
+template <int VEC>
+__device__ __forceinline__ void load_vec_cg(const float *p, float (&o)[VEC])
+{
+    if constexpr (VEC % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(p + 4 * q));
+            o[4 * q + 0] = x.x;
+            o[4 * q + 1] = x.y;
+            o[4 * q + 2] = x.z;
+            o[4 * q + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) o[v] = __ldcg(p + v);
+    }
+}
+
+}  // namespace mg

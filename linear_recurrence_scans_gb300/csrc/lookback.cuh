@@ -1,0 +1,189 @@
+// Chunk look-back machinery shared by every scan kernel of the library.
+//
+// A scan along time is cut into chunks.  Each CTA takes one (channel tile,
+// chunk) pair by ticket, reduces its chunk to an aggregate, and needs the
+// composition of every earlier chunk of the same channel tile (its exclusive
+// prefix).  It finds that prefix with a decoupled look-back: it publishes its
+// aggregate, walks back over its predecessors' published records until it
+// meets one that holds an inclusive prefix, and publishes its own inclusive
+// prefix.  Tickets are handed out in launch order, chunk-major, so every
+// predecessor a CTA waits on has already started: the waits always end.
+//
+// Determinism.  After the walk back finds an inclusive prefix at chunk p, the
+// waiting CTA folds the aggregates p+1 .. c-1 FORWARD onto it.  Every prefix
+// is therefore the left fold agg(0) o agg(1) o ... o agg(c) in the same
+// order whatever the walk met, so results are bitwise reproducible run to run.
+//
+// Workspace layout (caller-owned, zero-filled once before first use):
+//   [0, 256)            Control
+//   [256, 256 + 8*N)    one 64-bit record flag per tile:  epoch << 2 | status
+//   then                per-tile data, op-specific (aggregate and prefix)
+// A flag counts only if its epoch equals the launch's epoch, so stale flags
+// of earlier launches need no clearing.  The last CTA of every launch resets
+// the ticket and done counters and advances the epoch.
+//
+// Bounded waits.  A wait gives up after `max_polls` polls or `wait_limit_ns`
+// nanoseconds of %globaltimer, or as soon as any CTA of the launch has given
+// up.  Giving up sets the sticky Control::error word (read by
+// mg_workspace_status) and the CTA carries on with an identity carry, so the
+// launch always finishes and the GPU stays usable.
+#pragma once
+
+#include <cstdint>
+
+namespace mg {
+
+enum : unsigned { kStatusNone = 0, kStatusAggregate = 1, kStatusPrefix = 2 };
+enum : unsigned { kErrLookbackTimeout = 1u, kErrBadTicket = 2u };
+
+struct Control {
+    unsigned int ticket;       // next tile ticket of the running launch
+    unsigned int done;         // CTAs of the running launch that have finished
+    unsigned long long epoch;  // launch counter; tags the record flags
+    unsigned int error;        // sticky error bits (kErr*)
+    unsigned int error_tile;   // 1 + a tile that gave up a wait (0 = none)
+    unsigned int pad[58];
+};
+static_assert(sizeof(Control) == 256, "control block is 256 bytes");
+
+constexpr size_t kControlBytes = 256;
+
+struct Lookback {
+    Control *ctl;
+    unsigned long long *flags;   // [n_tiles]
+    float *data;                 // op-specific per-tile records
+    unsigned long long wait_limit_ns;
+    unsigned int max_polls;
+    long long stall_tile;        // testing only: this tile never publishes (-1: none)
+};
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned int ld_relaxed_u32(const unsigned int *p)
+{
+    unsigned int v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" : : "l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Status of a flag word for this launch (kStatusNone if stale or unset).
+__device__ __forceinline__ unsigned flag_status(unsigned long long v, unsigned long long epoch)
+{
+    return ((v >> 2) == epoch) ? unsigned(v & 3ull) : kStatusNone;
+}
+
+// Take a ticket and read the launch epoch (thread 0 of the CTA); all threads
+// get both through shared memory.
+__device__ __forceinline__ void take_ticket(const Lookback &lb, unsigned &tile,
+                                            unsigned long long &epoch)
+{
+    __shared__ unsigned s_tile;
+    __shared__ unsigned long long s_epoch;
+    if (threadIdx.x == 0) {
+        s_tile = atomicAdd(&lb.ctl->ticket, 1u);
+        s_epoch = ld_relaxed_u64(&lb.ctl->epoch);
+    }
+    __syncthreads();
+    tile = s_tile;
+    epoch = s_epoch;
+}
+
+// Look at a record flag without waiting (warp-collective; lane 0 reads).
+__device__ __forceinline__ unsigned peek_status(const Lookback &lb, size_t slot,
+                                                unsigned long long epoch)
+{
+    unsigned st = 0;
+    if ((threadIdx.x & 31) == 0)
+        st = flag_status(ld_relaxed_u64(lb.flags + slot), epoch);
+    return __shfl_sync(0xffffffffu, st, 0);
+}
+
+// Wait until record `slot` holds an aggregate or a prefix of this launch.
+// Warp-collective.  Returns its status, or kStatusNone if the wait gave up.
+// Lane 0 polls; after it sees the record every lane acquires the flag itself,
+// so each lane's later loads of the record's data are ordered after the
+// publisher's release.
+static __device__ __noinline__ unsigned wait_status(const Lookback &lb, size_t slot,
+                                             unsigned long long epoch, unsigned my_tile)
+{
+    const unsigned lane = threadIdx.x & 31;
+    unsigned st = kStatusNone;
+    if (lane == 0) {
+        st = flag_status(ld_acquire_u64(lb.flags + slot), epoch);
+        if (st == kStatusNone) {
+            const unsigned long long t0 = global_timer_ns();
+            unsigned sleep_ns = 20;
+            for (unsigned it = 0;; ++it) {
+                __nanosleep(sleep_ns);
+                if (sleep_ns < 500) sleep_ns += sleep_ns;
+                st = flag_status(ld_acquire_u64(lb.flags + slot), epoch);
+                if (st != kStatusNone) break;
+                if (it >= lb.max_polls || global_timer_ns() - t0 > lb.wait_limit_ns ||
+                    ld_relaxed_u32(&lb.ctl->error) != 0) {
+                    atomicOr(&lb.ctl->error, kErrLookbackTimeout);
+                    atomicCAS(&lb.ctl->error_tile, 0u, my_tile + 1u);
+                    break;
+                }
+            }
+        }
+    }
+    st = __shfl_sync(0xffffffffu, st, 0);
+    __syncwarp();
+    if (st != kStatusNone)
+        (void)ld_acquire_u64(lb.flags + slot);
+    return st;
+}
+
+// Publish record `slot` with `status` (warp-collective).  Every lane must have
+// written its part of the record with plain or .cg stores before calling.
+__device__ __forceinline__ void publish(const Lookback &lb, size_t slot, unsigned status,
+                                        unsigned long long epoch, unsigned my_tile)
+{
+    __threadfence();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0 && (long long)my_tile != lb.stall_tile)
+        st_release_u64(lb.flags + slot, (epoch << 2) | status);
+}
+
+// End of a CTA: count it; the launch's last CTA resets the ticket and done
+// counters and advances the epoch for the next launch on this workspace.
+__device__ __forceinline__ void finish_cta(const Lookback &lb, unsigned long long epoch)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(&lb.ctl->done, 1u);
+        if (prev == gridDim.x - 1) {
+            lb.ctl->ticket = 0;
+            lb.ctl->done = 0;
+            lb.ctl->epoch = epoch + 1;
+            __threadfence();
+        }
+    }
+}
+
+}  // namespace mg

@@ -1,0 +1,270 @@
+// The C entry points of mg_scan.h: argument validation (all of it before any
+// launch), workspace bookkeeping and dispatch to the launchers.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <initializer_list>
+
+#include "common.cuh"
+
+namespace mg {
+
+static thread_local char g_detail[512];
+
+mg_status fail(mg_status st, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_detail, sizeof(g_detail), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+namespace {
+
+constexpr int64_t kMaxDim = int64_t(1) << 40;
+
+struct Buf {
+    const void *p;
+    size_t bytes;
+    const char *name;
+    bool output;
+};
+
+// NULL, alignment and overlap checks.  Outputs may overlap nothing.
+mg_status check_bufs(const char *fn, std::initializer_list<Buf> bufs)
+{
+    for (const Buf &b : bufs) {
+        if (b.p == nullptr) return fail(MG_ERR_INVALID_ARG, "%s: %s is NULL", fn, b.name);
+        if (reinterpret_cast<uintptr_t>(b.p) % 16 != 0)
+            return fail(MG_ERR_INVALID_ARG, "%s: %s is not 16-byte aligned", fn, b.name);
+    }
+    for (const Buf &o : bufs) {
+        if (!o.output) continue;
+        const uintptr_t o0 = reinterpret_cast<uintptr_t>(o.p), o1 = o0 + o.bytes;
+        for (const Buf &x : bufs) {
+            if (&x == &o) continue;
+            const uintptr_t x0 = reinterpret_cast<uintptr_t>(x.p), x1 = x0 + x.bytes;
+            if (o0 < x1 && x0 < o1)
+                return fail(MG_ERR_INVALID_ARG, "%s: output %s overlaps %s", fn, o.name, x.name);
+        }
+    }
+    return MG_OK;
+}
+
+mg_status check_dims(const char *fn, std::initializer_list<int64_t> dims)
+{
+    int64_t prod = 1;
+    for (int64_t d : dims) {
+        if (d < 0) return fail(MG_ERR_INVALID_ARG, "%s: negative size %lld", fn, (long long)d);
+        if (d > kMaxDim) return fail(MG_ERR_UNSUPPORTED, "%s: size %lld too large", fn, (long long)d);
+        if (d > 0 && prod > (int64_t(1) << 58) / d)
+            return fail(MG_ERR_UNSUPPORTED, "%s: tensor too large", fn);
+        prod *= (d > 0 ? d : 1);
+    }
+    return MG_OK;
+}
+
+mg_status check_ws(const char *fn, const void *ws, size_t ws_bytes, size_t need)
+{
+    if (ws == nullptr) return fail(MG_ERR_INVALID_ARG, "%s: workspace is NULL", fn);
+    if (reinterpret_cast<uintptr_t>(ws) % 256 != 0)
+        return fail(MG_ERR_INVALID_ARG, "%s: workspace is not 256-byte aligned", fn);
+    if (ws_bytes < need)
+        return fail(MG_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", fn, ws_bytes, need);
+    return MG_OK;
+}
+
+bool valid_kv(int x) { return x == 1 || x == 2 || x == 4 || x == 8 || x == 16; }
+
+#define MG_TRY(expr)                      \
+    do {                                  \
+        const mg_status st__ = (expr);    \
+        if (st__ != MG_OK) return st__;   \
+    } while (0)
+
+}  // namespace
+}  // namespace mg
+
+using namespace mg;
+
+extern "C" {
+
+int mg_abi_version(void) { return MG_SCAN_ABI_VERSION; }
+
+const char *mg_strerror(mg_status status)
+{
+    switch (status) {
+    case MG_OK: return "ok";
+    case MG_ERR_INVALID_ARG: return "invalid argument";
+    case MG_ERR_UNSUPPORTED: return "unsupported by the kernels";
+    case MG_ERR_LAUNCH: return "kernel launch failed";
+    case MG_ERR_TIMEOUT: return "a look-back wait timed out on the device";
+    }
+    return "unknown status";
+}
+
+const char *mg_last_error_detail(void) { return g_detail; }
+
+size_t mg_linear_scan_workspace_size(int64_t B, int64_t T, int64_t D)
+{
+    if (B < 0 || T < 0 || D < 0) return 0;
+    if (B == 0 || T == 0 || D == 0) return kControlBytes;
+    return linear_ws_bytes(B, T, D);
+}
+
+size_t mg_log_scan_workspace_size(int64_t B, int64_t T, int64_t D)
+{
+    if (B < 0 || T < 0 || D < 0) return 0;
+    if (B == 0 || T == 0 || D == 0) return kControlBytes;
+    return log_ws_bytes(B, T, D);
+}
+
+size_t mg_affine_scan_workspace_size(int64_t B, int64_t T, int64_t n, int k, int v)
+{
+    if (B < 0 || T < 0 || n < 0 || !valid_kv(k) || !valid_kv(v)) return 0;
+    if (B == 0 || T == 0 || n == 0) return kControlBytes;
+    return affine_ws_bytes(B, T, n, k, v);
+}
+
+mg_status mg_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    g_detail[0] = 0;
+    if (ws == nullptr) return fail(MG_ERR_INVALID_ARG, "mg_workspace_init: workspace is NULL");
+    const cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, stream);
+    if (e != cudaSuccess)
+        return fail(MG_ERR_LAUNCH, "mg_workspace_init: %s", cudaGetErrorString(e));
+    return MG_OK;
+}
+
+mg_status mg_workspace_status(void *ws, cudaStream_t stream)
+{
+    g_detail[0] = 0;
+    if (ws == nullptr) return fail(MG_ERR_INVALID_ARG, "mg_workspace_status: workspace is NULL");
+    unsigned int words[2] = {0, 0};  // Control::error, Control::error_tile
+    Control *ctl = static_cast<Control *>(ws);
+    cudaError_t e = cudaMemcpyAsync(words, &ctl->error, sizeof(words), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess)
+        return fail(MG_ERR_LAUNCH, "mg_workspace_status: %s", cudaGetErrorString(e));
+    if (words[0] == 0) return MG_OK;
+    e = cudaMemsetAsync(&ctl->error, 0, sizeof(words), stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess)
+        return fail(MG_ERR_LAUNCH, "mg_workspace_status: %s", cudaGetErrorString(e));
+    if (words[0] & kErrBadTicket)
+        return fail(MG_ERR_INVALID_ARG,
+                    "the workspace was not zero-filled before its first use (or is shared by "
+                    "overlapping calls); the outputs of that launch are unspecified");
+    return fail(MG_ERR_TIMEOUT,
+                "a chunk look-back wait gave up (first tile %u); the outputs of that launch are "
+                "unspecified", words[1] ? words[1] - 1 : 0u);
+}
+
+mg_status mg_linear_scan_fwd(const void *a, const void *b, mg_dtype in_dt, float *A, float *Bc,
+                             int64_t B, int64_t T, int64_t D, void *ws, size_t ws_bytes,
+                             cudaStream_t stream)
+{
+    const char *fn = "mg_linear_scan_fwd";
+    g_detail[0] = 0;
+    if (in_dt != MG_F32 && in_dt != MG_BF16)
+        return fail(MG_ERR_UNSUPPORTED, "%s: input dtype %d not supported", fn, int(in_dt));
+    MG_TRY(check_dims(fn, {B, T, D}));
+    if (B == 0 || T == 0 || D == 0) return MG_OK;
+    const size_t n = size_t(B) * T * D, isz = in_dt == MG_F32 ? 4 : 2;
+    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D)));
+    MG_TRY(check_bufs(fn, {{a, n * isz, "a", false},
+                           {b, n * isz, "b", false},
+                           {A, n * 4, "A", true},
+                           {Bc, n * 4, "Bc", true},
+                           {ws, ws_bytes, "workspace", true}}));
+    return launch_linear_fwd(a, b, in_dt, A, Bc, B, T, D, ws, ws_bytes, stream, LaunchOpts{});
+}
+
+mg_status mg_linear_scan_bwd(const void *a, mg_dtype a_dt, const float *A, const float *Bc,
+                             const float *gA, const float *gBc, float *da, float *db, int64_t B,
+                             int64_t T, int64_t D, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    const char *fn = "mg_linear_scan_bwd";
+    g_detail[0] = 0;
+    if (a_dt != MG_F32 && a_dt != MG_BF16)
+        return fail(MG_ERR_UNSUPPORTED, "%s: input dtype %d not supported", fn, int(a_dt));
+    MG_TRY(check_dims(fn, {B, T, D}));
+    if (B == 0 || T == 0 || D == 0) return MG_OK;
+    const size_t n = size_t(B) * T * D, isz = a_dt == MG_F32 ? 4 : 2;
+    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D)));
+    MG_TRY(check_bufs(fn, {{a, n * isz, "a", false},
+                           {A, n * 4, "A", false},
+                           {Bc, n * 4, "Bc", false},
+                           {gA, n * 4, "gA", false},
+                           {gBc, n * 4, "gBc", false},
+                           {da, n * 4, "da", true},
+                           {db, n * 4, "db", true},
+                           {ws, ws_bytes, "workspace", true}}));
+    return launch_linear_bwd(a, a_dt, A, Bc, gA, gBc, da, db, B, T, D, ws, ws_bytes, stream,
+                             LaunchOpts{});
+}
+
+mg_status mg_log_scan_fwd(const float *log_coeffs, const float *log_values, float *h, int64_t B,
+                          int64_t T, int64_t D, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    const char *fn = "mg_log_scan_fwd";
+    g_detail[0] = 0;
+    MG_TRY(check_dims(fn, {B, T + 1, D}));
+    if (T < 0) return fail(MG_ERR_INVALID_ARG, "%s: negative size", fn);
+    if (B == 0 || T == 0 || D == 0) return MG_OK;
+    const size_t n = size_t(B) * T * D, nv = size_t(B) * (T + 1) * D;
+    MG_TRY(check_ws(fn, ws, ws_bytes, log_ws_bytes(B, T, D)));
+    MG_TRY(check_bufs(fn, {{log_coeffs, n * 4, "log_coeffs", false},
+                           {log_values, nv * 4, "log_values", false},
+                           {h, n * 4, "h", true},
+                           {ws, ws_bytes, "workspace", true}}));
+    return launch_log_fwd(log_coeffs, log_values, h, B, T, D, ws, ws_bytes, stream, LaunchOpts{});
+}
+
+mg_status mg_affine_scan_fwd(const float *A, const float *Bm, float *Abar, float *Bbar, int64_t B,
+                             int64_t T, int64_t n, int k, int v, void *ws, size_t ws_bytes,
+                             cudaStream_t stream)
+{
+    const char *fn = "mg_affine_scan_fwd";
+    g_detail[0] = 0;
+    if (!valid_kv(k) || !valid_kv(v))
+        return fail(MG_ERR_UNSUPPORTED, "%s: k=%d v=%d outside {1,2,4,8,16}", fn, k, v);
+    MG_TRY(check_dims(fn, {B, T, n, k, k > v ? k : v}));
+    if (B == 0 || T == 0 || n == 0) return MG_OK;
+    const size_t s = size_t(B) * T * n;
+    MG_TRY(check_ws(fn, ws, ws_bytes, affine_ws_bytes(B, T, n, k, v)));
+    MG_TRY(check_bufs(fn, {{A, s * k * k * 4, "A", false},
+                           {Bm, s * k * v * 4, "Bm", false},
+                           {Abar, s * k * k * 4, "Abar", true},
+                           {Bbar, s * k * v * 4, "Bbar", true},
+                           {ws, ws_bytes, "workspace", true}}));
+    return launch_affine_fwd(A, Bm, Abar, Bbar, B, T, n, k, v, ws, ws_bytes, stream, LaunchOpts{});
+}
+
+mg_status mg_affine_scan_bwd(const float *A, const float *Abar, const float *Bbar,
+                             const float *gAbar, const float *gBbar, float *dA, float *dB,
+                             int64_t B, int64_t T, int64_t n, int k, int v, void *ws,
+                             size_t ws_bytes, cudaStream_t stream)
+{
+    const char *fn = "mg_affine_scan_bwd";
+    g_detail[0] = 0;
+    if (!valid_kv(k) || !valid_kv(v))
+        return fail(MG_ERR_UNSUPPORTED, "%s: k=%d v=%d outside {1,2,4,8,16}", fn, k, v);
+    MG_TRY(check_dims(fn, {B, T, n, k, k > v ? k : v}));
+    if (B == 0 || T == 0 || n == 0) return MG_OK;
+    const size_t s = size_t(B) * T * n;
+    MG_TRY(check_ws(fn, ws, ws_bytes, affine_ws_bytes(B, T, n, k, v)));
+    MG_TRY(check_bufs(fn, {{A, s * k * k * 4, "A", false},
+                           {Abar, s * k * k * 4, "Abar", false},
+                           {Bbar, s * k * v * 4, "Bbar", false},
+                           {gAbar, s * k * k * 4, "gAbar", false},
+                           {gBbar, s * k * v * 4, "gBbar", false},
+                           {dA, s * k * k * 4, "dA", true},
+                           {dB, s * k * v * 4, "dB", true},
+                           {ws, ws_bytes, "workspace", true}}));
+    return launch_affine_bwd(A, Abar, Bbar, gAbar, gBbar, dA, dB, B, T, n, k, v, ws, ws_bytes,
+                             stream, LaunchOpts{});
+}
+
+}  // extern "C"

@@ -57,3 +57,45 @@ def normwise(g, r) -> float:
     r = np.asarray(r, dtype=np.float64)
     n = np.linalg.norm(r)
     return float(np.linalg.norm(g - r) / n) if n > 0 else float(np.linalg.norm(g))
+
+
+# ------------------------------------------------------- op-level checkers
+# Each compares GPU outputs (torch tensors) with the oracle run on the same
+# inputs and returns {name: scaled error}.  Inputs may live on the GPU; they
+# are copied to the host for the oracle.
+
+def _np(x) -> np.ndarray:
+    return x.detach().to("cpu", dtype=__import__("torch").float64).numpy()
+
+
+def linear_fwd_errors(a, b, A, Bc) -> dict:
+    import oracle
+    rA, rBc = oracle.linear_scan_fwd(a, b)
+    SBc = oracle.linear_scan_fwd(np.abs(_np(a)), np.abs(_np(b)))[1]
+    return {"A": scaled_error(_np(A), rA), "Bc": scaled_error(_np(Bc), rBc, SBc)}
+
+
+def linear_bwd_errors(a, A, Bc, gA, gBc, da, db) -> dict:
+    import oracle
+    rda, rdb = oracle.linear_scan_bwd(a, A, Bc, gA, gBc)
+    Sda, Sdb = oracle.linear_scan_bwd(*(np.abs(_np(x)) for x in (a, A, Bc, gA, gBc)))
+    return {"da": scaled_error(_np(da), rda, Sda), "db": scaled_error(_np(db), rdb, Sdb)}
+
+
+def log_fwd_errors(lc, lv, h) -> dict:
+    import oracle
+    return {"h": scaled_error(_np(h), oracle.log_scan_fwd(lc, lv))}
+
+
+def affine_fwd_errors(A, Bm, Abar, Bbar) -> dict:
+    import oracle
+    rAbar, rBbar = oracle.affine_scan_fwd(A, Bm)
+    return {"Abar": scaled_error(_np(Abar), rAbar, block_rms(rAbar)),
+            "Bbar": scaled_error(_np(Bbar), rBbar, block_rms(rBbar))}
+
+
+def affine_bwd_errors(A, Abar, Bbar, gAbar, gBbar, dA, dB) -> dict:
+    import oracle
+    rdA, rdB = oracle.affine_scan_bwd(A, Abar, Bbar, gAbar, gBbar)
+    return {"dA": scaled_error(_np(dA), rdA, block_rms(rdA)),
+            "dB": scaled_error(_np(dB), rdB, block_rms(rdB))}
