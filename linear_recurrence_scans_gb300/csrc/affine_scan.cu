@@ -1,21 +1,863 @@
-// k x k affine scans (placeholder until the kernels land).
-#include "common.cuh"
+// k x k affine scans: affine_scan_fwd and affine_scan_bwd of the page
+// "minGRU - Triton kernels".
+//
+// Both are scans of the pair operator on (C, V) with C a k x k coefficient
+// and V a k x w value, element 1 earlier:
+//     (C1, V1) o (C2, V2) = (C2 C1, C2 V1 + V2)
+// forward:  element (A_t, B_t), w = v, outputs Abar_t = C, Bbar_t = V;
+// backward: reverse time, element (A_{t+1}^T, [gAbar_t | gBbar_t]), w = k + v,
+//           V = [M_t | Lam_t]; outputs dB_t = Lam_t and
+//           dA_t = M_t Abar_{t-1}^T + Lam_t Bbar_{t-1}^T.
+//
+// Two kernel shapes:
+//   * k <= 4: one thread owns one sequence's whole state (k x (k + w) floats
+//     in registers) for L steps; 32 sequences x TY sub-chunks per CTA on the
+//     generic chunk engine (scan_engine.cuh).
+//   * k in {8, 16}: one warp owns one sequence's sub-chunk of L steps; the
+//     state X = [C | V] (k x (k + w), padded to a multiple of 8 columns) is
+//     split into 4 row blocks x 8 column blocks, one per lane.  Each step
+//     X <- E_C X + [0 | E_V] reads the column strip of X that the lane needs
+//     from a double-buffered shared copy (one __syncwarp per step) and the
+//     lane's rows of E_C straight from global memory.  A CTA of NW warps
+//     covers NW*L consecutive steps of one sequence and takes part in the
+//     same decoupled look-back as every other scan (lookback.cuh).
+#include "scan_engine.cuh"
 
 namespace mg {
+namespace {
 
-size_t affine_ws_bytes(int64_t, int64_t, int64_t, int, int) { return kControlBytes; }
+// -------------------------------------------------------------- helpers
 
-mg_status launch_affine_fwd(const float *, const float *, float *, float *, int64_t, int64_t,
-                            int64_t, int, int, void *, size_t, cudaStream_t, const LaunchOpts &)
+template <int N>
+__device__ __forceinline__ void ld_floats(const float *p, float *o)
 {
-    return fail(MG_ERR_UNSUPPORTED, "mg_affine_scan_fwd: not built yet");
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < N / 4; ++q) {
+            const float4 x = *reinterpret_cast<const float4 *>(p + 4 * q);
+            o[4 * q] = x.x;
+            o[4 * q + 1] = x.y;
+            o[4 * q + 2] = x.z;
+            o[4 * q + 3] = x.w;
+        }
+    } else if constexpr (N % 2 == 0) {
+#pragma unroll
+        for (int q = 0; q < N / 2; ++q) {
+            const float2 x = *reinterpret_cast<const float2 *>(p + 2 * q);
+            o[2 * q] = x.x;
+            o[2 * q + 1] = x.y;
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < N; ++q) o[q] = p[q];
+    }
 }
 
-mg_status launch_affine_bwd(const float *, const float *, const float *, const float *,
-                            const float *, float *, float *, int64_t, int64_t, int64_t, int, int,
-                            void *, size_t, cudaStream_t, const LaunchOpts &)
+template <int N>
+__device__ __forceinline__ void st_floats(float *p, const float *x)
 {
-    return fail(MG_ERR_UNSUPPORTED, "mg_affine_scan_bwd: not built yet");
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < N / 4; ++q)
+            *reinterpret_cast<float4 *>(p + 4 * q) =
+                make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    } else if constexpr (N % 2 == 0) {
+#pragma unroll
+        for (int q = 0; q < N / 2; ++q)
+            *reinterpret_cast<float2 *>(p + 2 * q) = make_float2(x[2 * q], x[2 * q + 1]);
+    } else {
+#pragma unroll
+        for (int q = 0; q < N; ++q) p[q] = x[q];
+    }
+}
+
+// o (R x N) = X (R x M) @ Y (M x N) [+ Z], row-major register arrays.
+template <int R, int M, int N>
+__device__ __forceinline__ void mm(const float *X, const float *Y, float *o)
+{
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            float s = X[i * M] * Y[j];
+#pragma unroll
+            for (int l = 1; l < M; ++l) s = fmaf(X[i * M + l], Y[l * N + j], s);
+            o[i * N + j] = s;
+        }
+}
+
+template <int R, int M, int N>
+__device__ __forceinline__ void mm_add(const float *X, const float *Y, const float *Z, float *o)
+{
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            float s = Z[i * N + j];
+#pragma unroll
+            for (int l = 0; l < M; ++l) s = fmaf(X[i * M + l], Y[l * N + j], s);
+            o[i * N + j] = s;
+        }
+}
+
+// ============================================================ k <= 4
+// Thread-owned state on the generic engine (VEC = 1: one sequence per lane).
+// State layout: C (K*K, row-major) then V (K*W, row-major).
+
+template <int K, int V_, int L_>
+struct AffFwdSmall {
+    static constexpr int W = V_, KK = K * K, KW = K * W;
+    static constexpr int NS = KK + KW, VEC = 1, L = L_;
+    static constexpr bool kReverse = false;
+    using S = St<NS, 1>;
+    struct Args {
+        const float *A;
+        const float *Bm;
+        float *Abar;
+        float *Bbar;
+    };
+    struct Regs {
+        const float *A;
+        const float *Bm;
+        int64_t s0;      // step index (b, t0, n) = (b*T + t0)*n + n_
+        int64_t stride;  // steps between consecutive t: n
+        int nvalid;      // steps t0 .. t0+nvalid-1 are < T
+    };
+    __device__ static float *f(S &x) { return &x.v[0][0]; }
+    __device__ static const float *f(const S &x) { return &x.v[0][0]; }
+
+    __device__ static void load(const Args &p, const ChanGeom &g, int64_t bb, int64_t t0, int d,
+                                bool act, Regs &r)
+    {
+        r.A = p.A;
+        r.Bm = p.Bm;
+        r.s0 = (bb * g.T + t0) * g.D + d;
+        r.stride = g.D;
+        const int64_t rem = g.T - t0;
+        r.nvalid = act ? int(rem < 0 ? 0 : (rem > L ? L : rem)) : 0;
+    }
+    __device__ static S identity()
+    {
+        S e;
+#pragma unroll
+        for (int i = 0; i < NS; ++i) e.v[i][0] = 0.f;
+#pragma unroll
+        for (int i = 0; i < K; ++i) e.v[i * K + i][0] = 1.f;
+        return e;
+    }
+    __device__ static S element(const Regs &r, int i)
+    {
+        if (i >= r.nvalid) return identity();
+        S e;
+        const int64_t s = r.s0 + i * r.stride;
+        ld_floats<KK>(r.A + s * KK, f(e));
+        ld_floats<KW>(r.Bm + s * KW, f(e) + KK);
+        return e;
+    }
+    __device__ static S initial(const Args &, const ChanGeom &, int64_t, int, bool)
+    {
+        return identity();
+    }
+    __device__ static S combine(const S &x, const S &y)
+    {
+        S o;
+        mm<K, K, K>(f(y), f(x), f(o));
+        mm_add<K, K, W>(f(y), f(x) + KK, f(y) + KK, f(o) + KK);
+        return o;
+    }
+    __device__ static void epilogue(const Args &p, const ChanGeom &, int64_t, int64_t, int, bool,
+                                    const Regs &r, const S &st)
+    {
+        float C[KK], Vv[KW];
+#pragma unroll
+        for (int i = 0; i < KK; ++i) C[i] = st.v[i][0];
+#pragma unroll
+        for (int i = 0; i < KW; ++i) Vv[i] = st.v[KK + i][0];
+#pragma unroll
+        for (int i = 0; i < L; ++i) {
+            if (i < r.nvalid) {
+                const int64_t s = r.s0 + i * r.stride;
+                float At[KK], Bt[KW], nC[KK], nV[KW];
+                ld_floats<KK>(r.A + s * KK, At);
+                ld_floats<KW>(r.Bm + s * KW, Bt);
+                mm<K, K, K>(At, C, nC);
+                mm_add<K, K, W>(At, Vv, Bt, nV);
+#pragma unroll
+                for (int q = 0; q < KK; ++q) C[q] = nC[q];
+#pragma unroll
+                for (int q = 0; q < KW; ++q) Vv[q] = nV[q];
+                st_floats<KK>(p.Abar + s * KK, C);
+                st_floats<KW>(p.Bbar + s * KW, Vv);
+            }
+        }
+    }
+};
+
+template <int K, int V_, int L_>
+struct AffBwdSmall {
+    static constexpr int VV = V_, W = K + V_, KK = K * K, KW = K * W, KV = K * V_;
+    static constexpr int NS = KK + KW, VEC = 1, L = L_;
+    static constexpr bool kReverse = true;
+    using S = St<NS, 1>;
+    struct Args {
+        const float *A;
+        const float *Abar;
+        const float *Bbar;
+        const float *gAbar;
+        const float *gBbar;
+        float *dA;
+        float *dB;
+    };
+    struct Regs {
+        Args p;
+        int64_t s0, stride, t0, T;
+        bool act;
+    };
+    __device__ static float *f(S &x) { return &x.v[0][0]; }
+    __device__ static const float *f(const S &x) { return &x.v[0][0]; }
+
+    __device__ static void load(const Args &p, const ChanGeom &g, int64_t bb, int64_t t0, int d,
+                                bool act, Regs &r)
+    {
+        r.p = p;
+        r.s0 = (bb * g.T + t0) * g.D + d;
+        r.stride = g.D;
+        r.t0 = t0;
+        r.T = g.T;
+        r.act = act;
+    }
+    __device__ static S identity()
+    {
+        S e;
+#pragma unroll
+        for (int i = 0; i < NS; ++i) e.v[i][0] = 0.f;
+#pragma unroll
+        for (int i = 0; i < K; ++i) e.v[i * K + i][0] = 1.f;
+        return e;
+    }
+    // G = [gAbar_t | gBbar_t] (K x W) of step s.
+    __device__ static void load_g(const Regs &r, int64_t s, float *G)
+    {
+        float ga[KK], gb[KV];
+        ld_floats<KK>(r.p.gAbar + s * KK, ga);
+        ld_floats<KV>(r.p.gBbar + s * KV, gb);
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+#pragma unroll
+            for (int j = 0; j < K; ++j) G[i * W + j] = ga[i * K + j];
+#pragma unroll
+            for (int j = 0; j < VV; ++j) G[i * W + K + j] = gb[i * VV + j];
+        }
+    }
+    // E_C = A_{t+1}^T, or 0 at t = T-1.
+    __device__ static void load_ct(const Regs &r, int64_t t, int64_t s, float *Ct)
+    {
+        if (t + 1 < r.T) {
+            float a[KK];
+            ld_floats<KK>(r.p.A + (s + r.stride) * KK, a);
+#pragma unroll
+            for (int i = 0; i < K; ++i)
+#pragma unroll
+                for (int j = 0; j < K; ++j) Ct[i * K + j] = a[j * K + i];
+        } else {
+#pragma unroll
+            for (int q = 0; q < KK; ++q) Ct[q] = 0.f;
+        }
+    }
+    __device__ static S element(const Regs &r, int i)
+    {
+        const int64_t t = r.t0 + i;
+        if (!r.act || t >= r.T) return identity();
+        S e;
+        const int64_t s = r.s0 + i * r.stride;
+        load_ct(r, t, s, f(e));
+        load_g(r, s, f(e) + KK);
+        return e;
+    }
+    __device__ static S initial(const Args &, const ChanGeom &, int64_t, int, bool)
+    {
+        return identity();
+    }
+    __device__ static S combine(const S &x, const S &y)
+    {
+        S o;
+        mm<K, K, K>(f(y), f(x), f(o));
+        mm_add<K, K, W>(f(y), f(x) + KK, f(y) + KK, f(o) + KK);
+        return o;
+    }
+    __device__ static void epilogue(const Args &p, const ChanGeom &, int64_t, int64_t, int, bool,
+                                    const Regs &r, const S &st)
+    {
+        float Vv[KW];
+#pragma unroll
+        for (int i = 0; i < KW; ++i) Vv[i] = st.v[KK + i][0];
+#pragma unroll
+        for (int i = L - 1; i >= 0; --i) {
+            const int64_t t = r.t0 + i;
+            if (r.act && t < r.T) {
+                const int64_t s = r.s0 + i * r.stride;
+                float Ct[KK], G[KW], nV[KW];
+                load_ct(r, t, s, Ct);
+                load_g(r, s, G);
+                mm_add<K, K, W>(Ct, Vv, G, nV);
+#pragma unroll
+                for (int q = 0; q < KW; ++q) Vv[q] = nV[q];
+                // dB_t = Lam_t;  dA_t = M_t Abar_{t-1}^T + Lam_t Bbar_{t-1}^T
+                float dB[KV], dA[KK];
+#pragma unroll
+                for (int a = 0; a < K; ++a)
+#pragma unroll
+                    for (int c = 0; c < VV; ++c) dB[a * VV + c] = Vv[a * W + K + c];
+                if (t > 0) {
+                    float Ap[KK], Bp[KV];
+                    ld_floats<KK>(p.Abar + (s - r.stride) * KK, Ap);
+                    ld_floats<KV>(p.Bbar + (s - r.stride) * KV, Bp);
+#pragma unroll
+                    for (int a = 0; a < K; ++a)
+#pragma unroll
+                        for (int b = 0; b < K; ++b) {
+                            float acc = Vv[a * W] * Ap[b * K];
+#pragma unroll
+                            for (int l = 1; l < K; ++l) acc = fmaf(Vv[a * W + l], Ap[b * K + l], acc);
+#pragma unroll
+                            for (int l = 0; l < VV; ++l)
+                                acc = fmaf(Vv[a * W + K + l], Bp[b * VV + l], acc);
+                            dA[a * K + b] = acc;
+                        }
+                } else {
+#pragma unroll
+                    for (int a = 0; a < K; ++a)
+#pragma unroll
+                        for (int b = 0; b < K; ++b) dA[a * K + b] = Vv[a * W + b];
+                }
+                st_floats<KK>(p.dA + s * KK, dA);
+                st_floats<KV>(p.dB + s * KV, dB);
+            }
+        }
+    }
+};
+
+// ============================================================ k in {8, 16}
+
+template <int K_, int W_, bool BWD_, int NW_, int L_>
+struct WCfg {
+    static constexpr int K = K_, W = W_, NW = NW_, L = L_;
+    static constexpr bool BWD = BWD_;
+    static constexpr int VV = BWD ? W - K : W;  // v
+    static constexpr int NC = K + W;            // columns of X = [C | V]
+    static constexpr int NCP = (NC + 7) / 8 * 8;
+    static constexpr int R = K / 4;             // rows per lane (4 row blocks)
+    static constexpr int CC = NCP / 8;          // columns per lane (8 column blocks)
+    static constexpr int XS = NCP;              // shared row stride (floats)
+    static constexpr int MAT = K * XS;          // floats per shared matrix
+    static constexpr int REC = K * NC;          // floats per global record
+    static constexpr int TC = NW * L;           // steps per tile
+    static constexpr int JD = K / 8;            // dA columns per lane
+    // shared: xb[NW][2][MAT], G[NW][MAT], carry[MAT]
+    static constexpr size_t SMEM = size_t(3 * NW + 1) * MAT * sizeof(float);
+};
+
+struct AffGeom {
+    int64_t B, T, n;
+    int nJ;   // sequences B*n
+    int nC;   // chunks along time
+    unsigned n_tiles;
+};
+
+struct AffPtrs {
+    const float *A, *Bm;                            // forward inputs
+    float *Abar_out, *Bbar_out;                     // forward outputs
+    const float *Abar, *Bbar, *gAbar, *gBbar;       // backward inputs (A shared)
+    float *dA, *dB;                                 // backward outputs
+};
+
+// Lane block of the combine (x earlier, full matrix in shared memory) o
+// (y later, rows `yc` = y.C[rows][0..K) and `yv` = y.V on the lane's columns).
+template <class Cf>
+__device__ __forceinline__ void block_gemm(const float *xs, const float (&yc)[Cf::R][Cf::K],
+                                           const float (&yv)[Cf::R][Cf::CC], int cb,
+                                           float (&o)[Cf::R][Cf::CC])
+{
+#pragma unroll
+    for (int r = 0; r < Cf::R; ++r)
+#pragma unroll
+        for (int c = 0; c < Cf::CC; ++c) o[r][c] = yv[r][c];
+#pragma unroll
+    for (int l = 0; l < Cf::K; ++l) {
+        float xv[Cf::CC];
+        ld_floats<Cf::CC>(xs + l * Cf::XS + cb * Cf::CC, xv);
+#pragma unroll
+        for (int r = 0; r < Cf::R; ++r)
+#pragma unroll
+            for (int c = 0; c < Cf::CC; ++c) o[r][c] = fmaf(yc[r][l], xv[c], o[r][c]);
+    }
+}
+
+// y operand from a matrix stored with row stride `ld` (shared or global):
+// C part = columns 0..K-1, V part on the lane's columns (zero outside [K, NC)).
+template <class Cf, bool GLOBAL>
+__device__ __forceinline__ void load_y(const float *m, int ld, int rb, int cb,
+                                       float (&yc)[Cf::R][Cf::K], float (&yv)[Cf::R][Cf::CC])
+{
+#pragma unroll
+    for (int r = 0; r < Cf::R; ++r) {
+        const float *row = m + (rb * Cf::R + r) * ld;
+#pragma unroll
+        for (int l = 0; l < Cf::K; ++l) yc[r][l] = GLOBAL ? __ldcg(row + l) : row[l];
+#pragma unroll
+        for (int c = 0; c < Cf::CC; ++c) {
+            const int col = cb * Cf::CC + c;
+            yv[r][c] = (col >= Cf::K && col < Cf::NC) ? (GLOBAL ? __ldcg(row + col) : row[col]) : 0.f;
+        }
+    }
+}
+
+// The element of step t as a y operand.
+template <class Cf>
+__device__ __forceinline__ void load_elem(const AffPtrs &p, const AffGeom &g, int64_t bb,
+                                          int64_t nn, int64_t t, int rb, int cb,
+                                          float (&yc)[Cf::R][Cf::K], float (&yv)[Cf::R][Cf::CC])
+{
+    constexpr int K = Cf::K, KK = K * K, VV = Cf::VV, R = Cf::R;
+    const int64_t s = (bb * g.T + t) * g.n + nn;
+    if constexpr (!Cf::BWD) {
+        const float *At = p.A + s * KK;
+#pragma unroll
+        for (int r = 0; r < R; ++r) ld_floats<K>(At + (rb * R + r) * K, yc[r]);
+        const float *Bt = p.Bm + s * (K * VV);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int c = 0; c < Cf::CC; ++c) {
+                const int col = cb * Cf::CC + c;
+                yv[r][c] = (col >= K && col < Cf::NC) ? Bt[(rb * R + r) * VV + col - K] : 0.f;
+            }
+    } else {
+        if (t + 1 < g.T) {  // E_C[row][l] = A_{t+1}[l][row]
+            const float *An = p.A + (s + g.n) * KK;
+#pragma unroll
+            for (int l = 0; l < K; ++l) {
+                float a[R];
+                ld_floats<R>(An + l * K + rb * R, a);
+#pragma unroll
+                for (int r = 0; r < R; ++r) yc[r][l] = a[r];
+            }
+        } else {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int l = 0; l < K; ++l) yc[r][l] = 0.f;
+        }
+        const float *ga = p.gAbar + s * KK;
+        const float *gb = p.gBbar + s * (K * VV);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int c = 0; c < Cf::CC; ++c) {
+                const int col = cb * Cf::CC + c, row = rb * R + r;
+                float x = 0.f;
+                if (col >= K && col < 2 * K) x = ga[row * K + col - K];
+                else if (col >= 2 * K && col < Cf::NC) x = gb[row * VV + col - 2 * K];
+                yv[r][c] = x;
+            }
+    }
+}
+
+template <class Cf>
+__device__ __forceinline__ void identity_block(int rb, int cb, float (&o)[Cf::R][Cf::CC])
+{
+#pragma unroll
+    for (int r = 0; r < Cf::R; ++r)
+#pragma unroll
+        for (int c = 0; c < Cf::CC; ++c) o[r][c] = (rb * Cf::R + r == cb * Cf::CC + c) ? 1.f : 0.f;
+}
+
+template <class Cf>
+__device__ __forceinline__ void put_block_smem(float *xs, int rb, int cb,
+                                               const float (&o)[Cf::R][Cf::CC])
+{
+#pragma unroll
+    for (int r = 0; r < Cf::R; ++r) st_floats<Cf::CC>(xs + (rb * Cf::R + r) * Cf::XS + cb * Cf::CC, o[r]);
+}
+
+template <class Cf>
+__device__ __forceinline__ void put_block_record(float *rec, int rb, int cb,
+                                                 const float (&o)[Cf::R][Cf::CC])
+{
+#pragma unroll
+    for (int r = 0; r < Cf::R; ++r)
+#pragma unroll
+        for (int c = 0; c < Cf::CC; ++c) {
+            const int col = cb * Cf::CC + c;
+            if (col < Cf::NC) __stcg(rec + (rb * Cf::R + r) * Cf::NC + col, o[r][c]);
+        }
+}
+
+template <class Cf>
+__device__ __forceinline__ void get_block_record(const float *rec, int rb, int cb,
+                                                 float (&o)[Cf::R][Cf::CC])
+{
+#pragma unroll
+    for (int r = 0; r < Cf::R; ++r)
+#pragma unroll
+        for (int c = 0; c < Cf::CC; ++c) {
+            const int col = cb * Cf::CC + c;
+            o[r][c] = col < Cf::NC ? __ldcg(rec + (rb * Cf::R + r) * Cf::NC + col) : 0.f;
+        }
+}
+
+template <class Cf>
+__global__ void __launch_bounds__(Cf::NW * 32)
+    affine_warp_kernel(const AffPtrs p, const AffGeom g, const Lookback lb)
+{
+    constexpr int K = Cf::K, R = Cf::R, CC = Cf::CC, NW = Cf::NW, L = Cf::L, MAT = Cf::MAT;
+    constexpr int XS = Cf::XS, NC = Cf::NC, VV = Cf::VV;
+    extern __shared__ float4 aff_smem[];
+    float *const xb = reinterpret_cast<float *>(aff_smem);  // [NW][2][MAT]
+    float *const G = xb + NW * 2 * MAT;                     // [NW][MAT]
+    float *const carry = G + NW * MAT;                      // [MAT]
+
+    unsigned tile;
+    unsigned long long epoch;
+    take_ticket(lb, tile, epoch);
+    if (tile >= g.n_tiles) {
+        if (threadIdx.x == 0) atomicOr(&lb.ctl->error, kErrBadTicket);
+        finish_cta(lb, epoch);
+        return;
+    }
+    const int c = int(tile / unsigned(g.nJ));
+    const int j = int(tile % unsigned(g.nJ));
+    const int64_t bb = j / g.n, nn = j % g.n;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rb = lane >> 3, cb = lane & 7;
+    const int ct = Cf::BWD ? (g.nC - 1 - c) : c;
+    const int64_t tw = int64_t(ct) * Cf::TC + warp * L;  // first step of this warp
+    float *const xw = xb + warp * 2 * MAT;
+
+    float yc[R][K], yv[R][CC], o[R][CC];
+
+    // ---- aggregate of this warp's L steps, in processing order
+    // (pw = the warp's position in processing order: reversed for the adjoint)
+    const int pw = Cf::BWD ? NW - 1 - warp : warp;
+    int cur = 0;
+    identity_block<Cf>(rb, cb, o);
+    put_block_smem<Cf>(xw, rb, cb, o);
+    __syncwarp();
+#pragma unroll 1
+    for (int k = 0; k < L; ++k) {
+        const int i = Cf::BWD ? L - 1 - k : k;
+        const int64_t t = tw + i;
+        if (t >= g.T) continue;  // padding steps are the identity
+        load_elem<Cf>(p, g, bb, nn, t, rb, cb, yc, yv);
+        block_gemm<Cf>(xw + cur * MAT, yc, yv, cb, o);
+        cur ^= 1;
+        put_block_smem<Cf>(xw + cur * MAT, rb, cb, o);
+        __syncwarp();
+    }
+    put_block_smem<Cf>(G + pw * MAT, rb, cb, o);
+    __syncthreads();
+
+    // ---- warp 0: inclusive prefixes over the warps (processing order), then
+    //      the look-back
+    if (warp == 0) {
+        for (int w = 1; w < NW; ++w) {  // G[w] <- G[w-1] o G[w]
+            load_y<Cf, false>(G + w * MAT, XS, rb, cb, yc, yv);
+            block_gemm<Cf>(G + (w - 1) * MAT, yc, yv, cb, o);
+            __syncwarp();
+            put_block_smem<Cf>(G + w * MAT, rb, cb, o);
+            __syncwarp();
+        }
+        const float *cta = G + (NW - 1) * MAT;
+        const size_t slot = size_t(c) * g.nJ + j;
+        float *rec_agg = lb.data + slot * 2 * Cf::REC;
+        float *rec_pre = rec_agg + Cf::REC;
+        float cblk[R][CC];
+#pragma unroll
+        for (int r = 0; r < R; ++r) ld_floats<CC>(cta + (rb * R + r) * XS + cb * CC, cblk[r]);
+        if (c == 0) {
+            put_block_record<Cf>(rec_pre, rb, cb, cblk);
+            publish(lb, slot, kStatusPrefix, epoch, tile);
+            identity_block<Cf>(rb, cb, o);
+            put_block_smem<Cf>(carry, rb, cb, o);
+        } else {
+            if (peek_status(lb, slot - g.nJ, epoch) != kStatusPrefix) {
+                put_block_record<Cf>(rec_agg, rb, cb, cblk);
+                publish(lb, slot, kStatusAggregate, epoch, tile);
+            }
+            int pp = c - 1;
+            bool ok = true;
+            for (;;) {
+                const unsigned st = wait_status(lb, size_t(pp) * g.nJ + j, epoch, tile);
+                if (st == kStatusPrefix) break;
+                if (st == kStatusNone || pp == 0) {
+                    ok = false;
+                    break;
+                }
+                --pp;
+            }
+            if (ok) {
+                get_block_record<Cf>(lb.data + (size_t(pp) * g.nJ + j) * 2 * Cf::REC + Cf::REC, rb,
+                                     cb, o);
+            } else {
+                identity_block<Cf>(rb, cb, o);
+            }
+            put_block_smem<Cf>(carry, rb, cb, o);
+            __syncwarp();
+            if (ok) {
+                for (int q = pp + 1; q < c; ++q) {  // carry <- carry o agg(q)
+                    load_y<Cf, true>(lb.data + (size_t(q) * g.nJ + j) * 2 * Cf::REC, NC, rb, cb,
+                                     yc, yv);
+                    block_gemm<Cf>(carry, yc, yv, cb, o);
+                    __syncwarp();
+                    put_block_smem<Cf>(carry, rb, cb, o);
+                    __syncwarp();
+                }
+            }
+            // prefix of this chunk = carry o cta
+            load_y<Cf, false>(cta, XS, rb, cb, yc, yv);
+            block_gemm<Cf>(carry, yc, yv, cb, o);
+            put_block_record<Cf>(rec_pre, rb, cb, o);
+            publish(lb, slot, kStatusPrefix, epoch, tile);
+        }
+    }
+    __syncthreads();
+
+    // ---- start state of this warp: carry o G[pw-1]
+    if (pw == 0) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) ld_floats<CC>(carry + (rb * R + r) * XS + cb * CC, o[r]);
+    } else {
+        load_y<Cf, false>(G + (pw - 1) * MAT, XS, rb, cb, yc, yv);
+        block_gemm<Cf>(carry, yc, yv, cb, o);
+    }
+    cur = 0;
+    put_block_smem<Cf>(xw, rb, cb, o);
+    __syncwarp();
+
+    // ---- re-run the warp's steps from its start state and write outputs
+#pragma unroll 1
+    for (int k = 0; k < L; ++k) {
+        const int i = Cf::BWD ? L - 1 - k : k;
+        const int64_t t = tw + i;
+        if (t >= g.T) continue;
+        load_elem<Cf>(p, g, bb, nn, t, rb, cb, yc, yv);
+        block_gemm<Cf>(xw + cur * MAT, yc, yv, cb, o);
+        cur ^= 1;
+        put_block_smem<Cf>(xw + cur * MAT, rb, cb, o);
+        __syncwarp();
+        const int64_t s = (bb * g.T + t) * g.n + nn;
+        if constexpr (!Cf::BWD) {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int cc = 0; cc < CC; ++cc) {
+                    const int col = cb * CC + cc, row = rb * R + r;
+                    if (col < K) p.Abar_out[s * (K * K) + row * K + col] = o[r][cc];
+                    else if (col < NC) p.Bbar_out[s * (K * VV) + row * VV + col - K] = o[r][cc];
+                }
+        } else {
+            // dB_t = Lam_t (columns 2K .. NC of X)
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int cc = 0; cc < CC; ++cc) {
+                    const int col = cb * CC + cc, row = rb * R + r;
+                    if (col >= 2 * K && col < NC) p.dB[s * (K * VV) + row * VV + col - 2 * K] = o[r][cc];
+                }
+            // dA_t[row][jc] = sum_c X[row][K + c] * Y[jc][c],  Y = [Abar_{t-1} | Bbar_{t-1}]
+            const float *xs = xw + cur * MAT;
+            constexpr int JD = Cf::JD, WW = Cf::W;
+            float da[R][JD];
+            if (t > 0) {
+                const int64_t sp = s - g.n;
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int jj = 0; jj < JD; ++jj) da[r][jj] = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < JD; ++jj) {
+                    const int jc = cb * JD + jj;
+                    float y[WW];
+                    ld_floats<K>(p.Abar + sp * (K * K) + jc * K, y);
+                    ld_floats<VV>(p.Bbar + sp * (K * VV) + jc * VV, y + K);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const float *xr = xs + (rb * R + r) * XS + K;
+                        float acc = 0.f;
+#pragma unroll
+                        for (int q = 0; q < WW; ++q) acc = fmaf(xr[q], y[q], acc);
+                        da[r][jj] = acc;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int jj = 0; jj < JD; ++jj)
+                        da[r][jj] = xs[(rb * R + r) * XS + K + cb * JD + jj];
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+                st_floats<JD>(p.dA + s * (K * K) + (rb * R + r) * K + cb * JD, da[r]);
+        }
+    }
+    finish_cta(lb, epoch);
+}
+
+template <class Cf>
+struct WarpPlan {
+    static size_t n_tiles(int64_t B, int64_t T, int64_t n)
+    {
+        return size_t(B * n) * size_t((T + Cf::TC - 1) / Cf::TC);
+    }
+    static size_t ws_bytes(int64_t B, int64_t T, int64_t n)
+    {
+        return tiled_ws_bytes(n_tiles(B, T, n), size_t(2) * Cf::REC * sizeof(float));
+    }
+    static mg_status launch(const AffPtrs &p, int64_t B, int64_t T, int64_t n, void *ws,
+                            size_t wsb, cudaStream_t s, const LaunchOpts &o, const char *name)
+    {
+        const size_t nt = n_tiles(B, T, n);
+        if (nt >= (size_t(1) << 31) || B * n >= (int64_t(1) << 31))
+            return fail(MG_ERR_UNSUPPORTED, "%s: %zu tiles exceed the 2^31 ticket range", name, nt);
+        const size_t need = ws_bytes(B, T, n);
+        if (wsb < need)
+            return fail(MG_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", name, wsb, need);
+        AffGeom g;
+        g.B = B;
+        g.T = T;
+        g.n = n;
+        g.nJ = int(B * n);
+        g.nC = int((T + Cf::TC - 1) / Cf::TC);
+        g.n_tiles = unsigned(nt);
+        const Lookback lb = make_lookback(ws, nt, o);
+        if (Cf::SMEM > 48 * 1024) {
+            static const cudaError_t attr = cudaFuncSetAttribute(
+                affine_warp_kernel<Cf>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cf::SMEM));
+            if (attr != cudaSuccess)
+                return fail(MG_ERR_LAUNCH, "%s: %s", name, cudaGetErrorString(attr));
+        }
+        affine_warp_kernel<Cf><<<unsigned(nt), Cf::NW * 32, Cf::SMEM, s>>>(p, g, lb);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return fail(MG_ERR_LAUNCH, "%s: launch failed: %s", name, cudaGetErrorString(e));
+        return MG_OK;
+    }
+};
+
+// ------------------------------------------------------------ dispatch
+
+constexpr int kSmallTY = 8, kSmallL = 4, kWarpNW = 4, kWarpL = 8;
+
+template <int K, int V>
+using SmallFwd = ChanPlan<AffFwdSmall<K, V, kSmallL>, 32, kSmallTY>;
+template <int K, int V>
+using SmallBwd = ChanPlan<AffBwdSmall<K, V, (K * (2 * K + V) > 48 ? 2 : kSmallL)>, 32,
+                          (K * (2 * K + V) > 48 ? 4 : kSmallTY)>;
+template <int K, int V>
+using BigFwd = WarpPlan<WCfg<K, V, false, kWarpNW, kWarpL>>;
+template <int K, int V>
+using BigBwd = WarpPlan<WCfg<K, K + V, true, kWarpNW, kWarpL>>;
+
+template <int K, int V>
+size_t ws_kv(int64_t B, int64_t T, int64_t n)
+{
+    size_t a, b;
+    if constexpr (K <= 4) {
+        a = SmallFwd<K, V>::ws_bytes(B, T, n);
+        b = SmallBwd<K, V>::ws_bytes(B, T, n);
+    } else {
+        a = BigFwd<K, V>::ws_bytes(B, T, n);
+        b = BigBwd<K, V>::ws_bytes(B, T, n);
+    }
+    return a > b ? a : b;
+}
+
+template <int K, int V>
+mg_status fwd_kv(const float *A, const float *Bm, float *Abar, float *Bbar, int64_t B, int64_t T,
+                 int64_t n, void *ws, size_t wsb, cudaStream_t s, const LaunchOpts &o)
+{
+    const char *nm = "mg_affine_scan_fwd";
+    if constexpr (K <= 4) {
+        return SmallFwd<K, V>::launch({A, Bm, Abar, Bbar}, B, T, n, ws, wsb, s, o, nm);
+    } else {
+        AffPtrs p{};
+        p.A = A;
+        p.Bm = Bm;
+        p.Abar_out = Abar;
+        p.Bbar_out = Bbar;
+        return BigFwd<K, V>::launch(p, B, T, n, ws, wsb, s, o, nm);
+    }
+}
+
+template <int K, int V>
+mg_status bwd_kv(const float *A, const float *Abar, const float *Bbar, const float *gAbar,
+                 const float *gBbar, float *dA, float *dB, int64_t B, int64_t T, int64_t n,
+                 void *ws, size_t wsb, cudaStream_t s, const LaunchOpts &o)
+{
+    const char *nm = "mg_affine_scan_bwd";
+    if constexpr (K <= 4) {
+        return SmallBwd<K, V>::launch({A, Abar, Bbar, gAbar, gBbar, dA, dB}, B, T, n, ws, wsb, s,
+                                      o, nm);
+    } else {
+        AffPtrs p{};
+        p.A = A;
+        p.Abar = Abar;
+        p.Bbar = Bbar;
+        p.gAbar = gAbar;
+        p.gBbar = gBbar;
+        p.dA = dA;
+        p.dB = dB;
+        return BigBwd<K, V>::launch(p, B, T, n, ws, wsb, s, o, nm);
+    }
+}
+
+// Expand CALL(K, V) for the runtime (k, v) in {1,2,4,8,16}^2.
+#define MG_KV_DISPATCH(k, v, CALL)                                                        \
+    switch ((k) * 32 + (v)) {                                                             \
+    case 1 * 32 + 1: CALL(1, 1); case 1 * 32 + 2: CALL(1, 2); case 1 * 32 + 4: CALL(1, 4);    \
+    case 1 * 32 + 8: CALL(1, 8); case 1 * 32 + 16: CALL(1, 16);                             \
+    case 2 * 32 + 1: CALL(2, 1); case 2 * 32 + 2: CALL(2, 2); case 2 * 32 + 4: CALL(2, 4);    \
+    case 2 * 32 + 8: CALL(2, 8); case 2 * 32 + 16: CALL(2, 16);                             \
+    case 4 * 32 + 1: CALL(4, 1); case 4 * 32 + 2: CALL(4, 2); case 4 * 32 + 4: CALL(4, 4);    \
+    case 4 * 32 + 8: CALL(4, 8); case 4 * 32 + 16: CALL(4, 16);                             \
+    case 8 * 32 + 1: CALL(8, 1); case 8 * 32 + 2: CALL(8, 2); case 8 * 32 + 4: CALL(8, 4);    \
+    case 8 * 32 + 8: CALL(8, 8); case 8 * 32 + 16: CALL(8, 16);                             \
+    case 16 * 32 + 1: CALL(16, 1); case 16 * 32 + 2: CALL(16, 2);                          \
+    case 16 * 32 + 4: CALL(16, 4); case 16 * 32 + 8: CALL(16, 8);                          \
+    case 16 * 32 + 16: CALL(16, 16);                                                      \
+    default: break;                                                                       \
+    }
+
+}  // namespace
+
+size_t affine_ws_bytes(int64_t B, int64_t T, int64_t n, int k, int v)
+{
+#define MG_CALL(K, V) return ws_kv<K, V>(B, T, n)
+    MG_KV_DISPATCH(k, v, MG_CALL)
+#undef MG_CALL
+    return 0;
+}
+
+mg_status launch_affine_fwd(const float *A, const float *Bm, float *Abar, float *Bbar, int64_t B,
+                            int64_t T, int64_t n, int k, int v, void *ws, size_t wsb,
+                            cudaStream_t s, const LaunchOpts &o)
+{
+#define MG_CALL(K, V) return fwd_kv<K, V>(A, Bm, Abar, Bbar, B, T, n, ws, wsb, s, o)
+    MG_KV_DISPATCH(k, v, MG_CALL)
+#undef MG_CALL
+    return fail(MG_ERR_UNSUPPORTED, "mg_affine_scan_fwd: k=%d v=%d outside {1,2,4,8,16}", k, v);
+}
+
+mg_status launch_affine_bwd(const float *A, const float *Abar, const float *Bbar,
+                            const float *gAbar, const float *gBbar, float *dA, float *dB,
+                            int64_t B, int64_t T, int64_t n, int k, int v, void *ws, size_t wsb,
+                            cudaStream_t s, const LaunchOpts &o)
+{
+#define MG_CALL(K, V) return bwd_kv<K, V>(A, Abar, Bbar, gAbar, gBbar, dA, dB, B, T, n, ws, wsb, s, o)
+    MG_KV_DISPATCH(k, v, MG_CALL)
+#undef MG_CALL
+    return fail(MG_ERR_UNSUPPORTED, "mg_affine_scan_bwd: k=%d v=%d outside {1,2,4,8,16}", k, v);
 }
 
 }  // namespace mg

@@ -23,25 +23,12 @@
 // value = s * 2^m so that one exp2 per combine suffices.
 #include <cmath>
 
-#include "common.cuh"
+#include "scan_engine.cuh"
 
 namespace mg {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-
-struct ChanGeom {
-    int64_t B, T, D;
-    int nJb;  // channel tiles per batch row
-    int nJ;   // channel tiles in total (B * nJb)
-    int nC;   // chunks along time
-    unsigned n_tiles;  // nJ * nC
-};
-
-template <int NS, int VEC>
-struct St {
-    float v[NS][VEC];
-};
 
 // ----------------------------------------------------------- linear forward
 // Element of step t: (a_t, b_t).  State: (running product, h).
@@ -394,210 +381,6 @@ struct LogFwd {
             const int64_t t = t0 + i;
             if (act && t < g.T) store_vec<VEC>(p.h + (bb * g.T + t) * g.D + d, h);
         }
-    }
-};
-
-// ------------------------------------------------------------ the engine
-
-template <class Op, int TX>
-__device__ __forceinline__ float *chan_record(const Lookback &lb, size_t slot, int kind, int s,
-                                              int lane)
-{
-    constexpr int DC = TX * Op::VEC;
-    return lb.data + ((slot * 2 + kind) * Op::NS + s) * DC + lane * Op::VEC;
-}
-
-template <class Op, int TX>
-__device__ __forceinline__ void put_record(const Lookback &lb, size_t slot, int kind, int lane,
-                                           const typename Op::S &x)
-{
-#pragma unroll
-    for (int s = 0; s < Op::NS; ++s) store_vec_cg<Op::VEC>(chan_record<Op, TX>(lb, slot, kind, s, lane), x.v[s]);
-}
-
-template <class Op, int TX>
-__device__ __forceinline__ typename Op::S get_record(const Lookback &lb, size_t slot, int kind,
-                                                     int lane)
-{
-    typename Op::S x;
-#pragma unroll
-    for (int s = 0; s < Op::NS; ++s) load_vec_cg<Op::VEC>(chan_record<Op, TX>(lb, slot, kind, s, lane), x.v[s]);
-    return x;
-}
-
-// Warp 0: exclusive carry-in of chunk c for channel tile j, given the chunk
-// aggregate `cta` of this lane's channels; publishes the chunk's records.
-template <class Op, int TX>
-__device__ typename Op::S lookback_chan(const typename Op::Args &args, const ChanGeom &g,
-                                        const Lookback &lb, int c, int j, int64_t bb, int ld,
-                                        bool lact, bool lchan, unsigned tile,
-                                        unsigned long long epoch, const typename Op::S &cta)
-{
-    using S = typename Op::S;
-    const int lane = threadIdx.x & 31;
-    const size_t slot = size_t(c) * g.nJ + j;
-    S excl = Op::identity();
-    if (c == 0) {
-        excl = Op::initial(args, g, bb, ld, lchan);
-        if (lact) put_record<Op, TX>(lb, slot, 1, lane, Op::combine(excl, cta));
-        publish(lb, slot, kStatusPrefix, epoch, tile);
-        return excl;
-    }
-    if (peek_status(lb, slot - g.nJ, epoch) != kStatusPrefix) {
-        if (lact) put_record<Op, TX>(lb, slot, 0, lane, cta);
-        publish(lb, slot, kStatusAggregate, epoch, tile);
-    }
-    int p = c - 1;
-    bool ok = true;
-    for (;;) {
-        const unsigned st = wait_status(lb, size_t(p) * g.nJ + j, epoch, tile);
-        if (st == kStatusPrefix) break;
-        if (st == kStatusNone || p == 0) {  // gave up (chunk 0 never holds an aggregate only)
-            ok = false;
-            break;
-        }
-        --p;
-    }
-    if (ok && lact) {
-        excl = get_record<Op, TX>(lb, size_t(p) * g.nJ + j, 1, lane);
-        for (int q = p + 1; q < c; ++q)
-            excl = Op::combine(excl, get_record<Op, TX>(lb, size_t(q) * g.nJ + j, 0, lane));
-    }
-    if (lact) put_record<Op, TX>(lb, slot, 1, lane, Op::combine(excl, cta));
-    publish(lb, slot, kStatusPrefix, epoch, tile);
-    return excl;
-}
-
-template <class Op, int TX, int TY>
-__global__ void __launch_bounds__(TX *TY)
-    channel_scan_kernel(const typename Op::Args args, const ChanGeom g, const Lookback lb)
-{
-    using S = typename Op::S;
-    constexpr int NS = Op::NS, VEC = Op::VEC, L = Op::L;
-    constexpr int DC = TX * VEC;
-    __shared__ __align__(16) float s_agg[TY][NS][DC];
-    __shared__ __align__(16) float s_carry[NS][DC];
-
-    unsigned tile;
-    unsigned long long epoch;
-    take_ticket(lb, tile, epoch);
-    if (tile >= g.n_tiles) {  // a workspace that was not zero-filled before first use
-        if (threadIdx.x == 0) atomicOr(&lb.ctl->error, kErrBadTicket);
-        finish_cta(lb, epoch);
-        return;
-    }
-    const int c = int(tile / unsigned(g.nJ));
-    const int j = int(tile % unsigned(g.nJ));
-    const int64_t bb = j / g.nJb;
-    const int dbase = (j % g.nJb) * DC;
-    const int tx = threadIdx.x % TX, ty = threadIdx.x / TX;
-    const int d = dbase + tx * VEC;
-    const bool act = d < g.D;
-    const int ct = Op::kReverse ? (g.nC - 1 - c) : c;
-    const int64_t t0 = int64_t(ct) * (TY * L) + ty * L;
-
-    typename Op::Regs r;
-    Op::load(args, g, bb, t0, d, act, r);
-
-    S agg = Op::element(r, Op::kReverse ? L - 1 : 0);
-#pragma unroll
-    for (int k = 1; k < L; ++k) agg = Op::combine(agg, Op::element(r, Op::kReverse ? L - 1 - k : k));
-#pragma unroll
-    for (int s = 0; s < NS; ++s) store_vec<VEC>(&s_agg[ty][s][tx * VEC], agg.v[s]);
-    __syncthreads();
-
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        const bool lact = lane < TX;
-        const int ld = dbase + lane * VEC;
-        const bool lchan = lact && ld < g.D;
-        S cta = Op::identity();
-        if (lact) {
-#pragma unroll
-            for (int k = 0; k < TY; ++k) {
-                const int y = Op::kReverse ? TY - 1 - k : k;
-                S x;
-#pragma unroll
-                for (int s = 0; s < NS; ++s) load_vec<VEC>(&s_agg[y][s][lane * VEC], x.v[s]);
-                cta = (k == 0) ? x : Op::combine(cta, x);
-            }
-        }
-        const S excl = lookback_chan<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch, cta);
-        if (lact) {
-#pragma unroll
-            for (int s = 0; s < NS; ++s) store_vec<VEC>(&s_carry[s][lane * VEC], excl.v[s]);
-        }
-    }
-    __syncthreads();
-
-    S st;
-#pragma unroll
-    for (int s = 0; s < NS; ++s) load_vec<VEC>(&s_carry[s][tx * VEC], st.v[s]);
-    if (!Op::kReverse) {
-        for (int y = 0; y < ty; ++y) {
-            S x;
-#pragma unroll
-            for (int s = 0; s < NS; ++s) load_vec<VEC>(&s_agg[y][s][tx * VEC], x.v[s]);
-            st = Op::combine(st, x);
-        }
-    } else {
-        for (int y = TY - 1; y > ty; --y) {
-            S x;
-#pragma unroll
-            for (int s = 0; s < NS; ++s) load_vec<VEC>(&s_agg[y][s][tx * VEC], x.v[s]);
-            st = Op::combine(st, x);
-        }
-    }
-    Op::epilogue(args, g, bb, t0, d, act, r, st);
-    finish_cta(lb, epoch);
-}
-
-// ------------------------------------------------------------ launchers
-
-template <class Op, int TX, int TY>
-struct ChanPlan {
-    static constexpr int DC = TX * Op::VEC;
-    static constexpr int TC = TY * Op::L;
-    static ChanGeom geom(int64_t B, int64_t T, int64_t D)
-    {
-        ChanGeom g;
-        g.B = B;
-        g.T = T;
-        g.D = D;
-        g.nJb = int((D + DC - 1) / DC);
-        g.nJ = int(B * g.nJb);
-        g.nC = int((T + TC - 1) / TC);
-        g.n_tiles = unsigned(g.nJ) * unsigned(g.nC);
-        return g;
-    }
-    static size_t n_tiles(int64_t B, int64_t T, int64_t D)
-    {
-        const int64_t nJ = B * ((D + DC - 1) / DC);
-        const int64_t nC = (T + TC - 1) / TC;
-        return size_t(nJ) * size_t(nC);
-    }
-    static size_t ws_bytes(int64_t B, int64_t T, int64_t D)
-    {
-        return tiled_ws_bytes(n_tiles(B, T, D), size_t(2) * Op::NS * DC * sizeof(float));
-    }
-    static mg_status launch(const typename Op::Args &args, int64_t B, int64_t T, int64_t D,
-                            void *ws, size_t ws_bytes_given, cudaStream_t s, const LaunchOpts &o,
-                            const char *name)
-    {
-        const size_t nt = n_tiles(B, T, D);
-        if (nt >= (size_t(1) << 31) || B * ((D + DC - 1) / DC) >= (int64_t(1) << 31))
-            return fail(MG_ERR_UNSUPPORTED, "%s: %zu tiles exceed the 2^31 ticket range", name, nt);
-        const size_t need = ws_bytes(B, T, D);
-        if (ws_bytes_given < need)
-            return fail(MG_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", name,
-                        ws_bytes_given, need);
-        const ChanGeom g = geom(B, T, D);
-        const Lookback lb = make_lookback(ws, nt, o);
-        channel_scan_kernel<Op, TX, TY><<<unsigned(nt), TX * TY, 0, s>>>(args, g, lb);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess)
-            return fail(MG_ERR_LAUNCH, "%s: launch failed: %s", name, cudaGetErrorString(e));
-        return MG_OK;
     }
 };
 

@@ -124,11 +124,10 @@ __device__ __forceinline__ unsigned peek_status(const Lookback &lb, size_t slot,
 
 // Wait until record `slot` holds an aggregate or a prefix of this launch.
 // Warp-collective.  Returns its status, or kStatusNone if the wait gave up.
-// Lane 0 polls; after it sees the record every lane acquires the flag itself,
-// so each lane's later loads of the record's data are ordered after the
-// publisher's release.
+// Lane 0 polls with acquire loads; the __syncwarp that follows orders every
+// lane's later (L2) loads of the record's data after that acquire.
 static __device__ __noinline__ unsigned wait_status(const Lookback &lb, size_t slot,
-                                             unsigned long long epoch, unsigned my_tile)
+                                                    unsigned long long epoch, unsigned my_tile)
 {
     const unsigned lane = threadIdx.x & 31;
     unsigned st = kStatusNone;
@@ -153,17 +152,15 @@ static __device__ __noinline__ unsigned wait_status(const Lookback &lb, size_t s
     }
     st = __shfl_sync(0xffffffffu, st, 0);
     __syncwarp();
-    if (st != kStatusNone)
-        (void)ld_acquire_u64(lb.flags + slot);
     return st;
 }
 
 // Publish record `slot` with `status` (warp-collective).  Every lane must have
-// written its part of the record with plain or .cg stores before calling.
+// written its part of the record (.cg stores) before calling; the __syncwarp
+// orders those writes before lane 0's release store, which is cumulative.
 __device__ __forceinline__ void publish(const Lookback &lb, size_t slot, unsigned status,
                                         unsigned long long epoch, unsigned my_tile)
 {
-    __threadfence();
     __syncwarp();
     if ((threadIdx.x & 31) == 0 && (long long)my_tile != lb.stall_tile)
         st_release_u64(lb.flags + slot, (epoch << 2) | status);

@@ -65,6 +65,8 @@ def normwise(g, r) -> float:
 # are copied to the host for the oracle.
 
 def _np(x) -> np.ndarray:
+    if isinstance(x, np.ndarray):
+        return x.astype(np.float64, copy=False)
     return x.detach().to("cpu", dtype=__import__("torch").float64).numpy()
 
 
