@@ -66,7 +66,9 @@ _lock = threading.Lock()
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    """The in-tree build, or the library named by MGSCAN_LIBRARY (another
+    build of the same sources, e.g. with different tile sizes)."""
+    return os.environ.get("MGSCAN_LIBRARY") or _build.LIB_PATH
 
 
 def load():
@@ -78,7 +80,7 @@ def load():
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.LIB_PATH
+        path = library_path()
         if not os.path.exists(path):
             raise RuntimeError(f"{path} is missing: build the CUDA library first "
                                "(python -m linear_recurrence_scans_gb300._build)")

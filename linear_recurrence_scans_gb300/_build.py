@@ -54,18 +54,21 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in sources() + _headers() + [__file__])
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link ``_lib/libmgscan.so``; returns its path."""
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, defines=(), out_dir: str = OUT_DIR) -> str:
+    """Compile and link ``libmgscan.so`` into ``out_dir`` (default ``_lib/``);
+    returns its path.  ``defines`` are extra ``-D`` flags (tile overrides)."""
+    lib_path = os.path.join(out_dir, LIB_NAME)
+    if not force and not defines and out_dir == OUT_DIR and up_to_date():
         return LIB_PATH
     cuda = _cuda_home()
     nvcc = os.path.join(cuda, "bin", "nvcc")
-    os.makedirs(OUT_DIR, exist_ok=True)
+    os.makedirs(out_dir, exist_ok=True)
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *[f"-D{d}" for d in defines], "-I", INCLUDE, "-I", CSRC,
+               "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -76,14 +79,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
             objs.append(obj)
             if verbose:
                 sys.stderr.write(log)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", f"-rpath,{os.path.join(cuda, 'lib64')}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -584,17 +584,8 @@ __global__ void __launch_bounds__(Cf::NW * 32)
                 put_block_record<Cf>(rec_agg, rb, cb, cblk);
                 publish(lb, slot, kStatusAggregate, epoch, tile);
             }
-            int pp = c - 1;
-            bool ok = true;
-            for (;;) {
-                const unsigned st = wait_status(lb, size_t(pp) * g.nJ + j, epoch, tile);
-                if (st == kStatusPrefix) break;
-                if (st == kStatusNone || pp == 0) {
-                    ok = false;
-                    break;
-                }
-                --pp;
-            }
+            const int pp = wait_window(lb, size_t(j), size_t(g.nJ), c, epoch, tile);
+            const bool ok = pp >= 0;
             if (ok) {
                 get_block_record<Cf>(lb.data + (size_t(pp) * g.nJ + j) * 2 * Cf::REC + Cf::REC, rb,
                                      cb, o);

@@ -384,18 +384,68 @@ struct LogFwd {
     }
 };
 
-// Tile choices.  fp32: 4 channels (16 B) per thread; bf16: 8 channels (16 B).
-// A D that is not a multiple of the vector width takes the 1-channel variant.
+// Tile choices (threads along channels TX, thread rows TY, steps per thread
+// L, minimum resident CTAs per SM).  fp32: 4 channels (16 B) per thread;
+// bf16: 8 channels (16 B).  A D that is not a multiple of the vector width
+// takes the 1-channel variant.  Each can be overridden at build time.
+#ifndef MG_LINF_TX
+#define MG_LINF_TX 32
+#endif
+#ifndef MG_LINF_TY
+#define MG_LINF_TY 8
+#endif
+#ifndef MG_LINF_L
+#define MG_LINF_L 8
+#endif
+#ifndef MG_LINF_MB
+#define MG_LINF_MB 1
+#endif
+#ifndef MG_LINF16_TX
+#define MG_LINF16_TX 32
+#endif
+#ifndef MG_LINF16_TY
+#define MG_LINF16_TY 8
+#endif
+#ifndef MG_LINF16_L
+#define MG_LINF16_L 8
+#endif
+#ifndef MG_LINF16_MB
+#define MG_LINF16_MB 1
+#endif
+#ifndef MG_LINB_TX
+#define MG_LINB_TX 32
+#endif
+#ifndef MG_LINB_TY
+#define MG_LINB_TY 8
+#endif
+#ifndef MG_LINB_L
+#define MG_LINB_L 4
+#endif
+#ifndef MG_LINB_MB
+#define MG_LINB_MB 1
+#endif
+#ifndef MG_LOG_TX
+#define MG_LOG_TX 32
+#endif
+#ifndef MG_LOG_TY
+#define MG_LOG_TY 8
+#endif
+#ifndef MG_LOG_L
+#define MG_LOG_L 8
+#endif
+#ifndef MG_LOG_MB
+#define MG_LOG_MB 1
+#endif
 constexpr int kTX = 32, kTY = 8;
-using LinFwdF32 = ChanPlan<LinFwd<float, 4, 8>, kTX, kTY>;
+using LinFwdF32 = ChanPlan<LinFwd<float, 4, MG_LINF_L>, MG_LINF_TX, MG_LINF_TY, MG_LINF_MB>;
 using LinFwdF32s = ChanPlan<LinFwd<float, 1, 8>, kTX, kTY>;
-using LinFwdB16 = ChanPlan<LinFwd<bf16_t, 8, 4>, kTX, kTY>;
+using LinFwdB16 = ChanPlan<LinFwd<bf16_t, 8, MG_LINF16_L>, MG_LINF16_TX, MG_LINF16_TY, MG_LINF16_MB>;
 using LinFwdB16s = ChanPlan<LinFwd<bf16_t, 1, 8>, kTX, kTY>;
-using LinBwdF32 = ChanPlan<LinBwd<float, 4, 4>, kTX, kTY>;
+using LinBwdF32 = ChanPlan<LinBwd<float, 4, MG_LINB_L>, MG_LINB_TX, MG_LINB_TY, MG_LINB_MB>;
 using LinBwdF32s = ChanPlan<LinBwd<float, 1, 4>, kTX, kTY>;
-using LinBwdB16 = ChanPlan<LinBwd<bf16_t, 4, 4>, kTX, kTY>;
+using LinBwdB16 = ChanPlan<LinBwd<bf16_t, 4, MG_LINB_L>, MG_LINB_TX, MG_LINB_TY, MG_LINB_MB>;
 using LinBwdB16s = ChanPlan<LinBwd<bf16_t, 1, 4>, kTX, kTY>;
-using LogF32 = ChanPlan<LogFwd<4, 8>, kTX, kTY>;
+using LogF32 = ChanPlan<LogFwd<4, MG_LOG_L>, MG_LOG_TX, MG_LOG_TY, MG_LOG_MB>;
 using LogF32s = ChanPlan<LogFwd<1, 8>, kTX, kTY>;
 
 template <class P>

@@ -155,6 +155,48 @@ static __device__ __noinline__ unsigned wait_status(const Lookback &lb, size_t s
     return st;
 }
 
+// Parallel look-back window (warp-collective).  Chunk c of a chain whose
+// records sit at slots q*stride + j looks at its 32 nearest predecessors at
+// once: lane l polls chunk c-1-l.  The wait ends when the nearest predecessor
+// holding an inclusive prefix is inside the window and every chunk between it
+// and c holds at least an aggregate.  Returns that chunk p, or -1 if the wait
+// gave up.  Lanes past chunk 0 read as "prefix" (a sentinel that can never
+// be chosen: chunk 0 only ever publishes a prefix, so while it is unpublished
+// an unset flag precedes the sentinel).  The __syncwarp before returning
+// orders every lane's later record loads after the acquires.
+static __device__ __noinline__ int wait_window(const Lookback &lb, size_t j, size_t stride, int c,
+                                               unsigned long long epoch, unsigned my_tile)
+{
+    const int lane = threadIdx.x & 31;
+    const int q = c - 1 - lane;
+    const unsigned long long t0 = global_timer_ns();
+    unsigned sleep_ns = 20;
+    for (unsigned it = 0;; ++it) {
+        unsigned st = kStatusPrefix;
+        if (q >= 0) st = flag_status(ld_acquire_u64(lb.flags + size_t(q) * stride + j), epoch);
+        const unsigned pmask = __ballot_sync(0xffffffffu, st == kStatusPrefix);
+        const unsigned xmask = __ballot_sync(0xffffffffu, st == kStatusNone);
+        if (pmask != 0u) {
+            const int first = __ffs(pmask) - 1;
+            const unsigned before = first == 0 ? 0u : (0xffffffffu >> (32 - first));
+            if ((xmask & before) == 0u) {
+                __syncwarp();
+                return first <= c - 1 ? c - 1 - first : -1;
+            }
+        }
+        int stop = 0;
+        if (lane == 0 && (it >= lb.max_polls || global_timer_ns() - t0 > lb.wait_limit_ns ||
+                          ld_relaxed_u32(&lb.ctl->error) != 0)) {
+            atomicOr(&lb.ctl->error, kErrLookbackTimeout);
+            atomicCAS(&lb.ctl->error_tile, 0u, my_tile + 1u);
+            stop = 1;
+        }
+        if (__shfl_sync(0xffffffffu, stop, 0)) return -1;
+        __nanosleep(sleep_ns);
+        if (sleep_ns < 400) sleep_ns += sleep_ns;
+    }
+}
+
 // Publish record `slot` with `status` (warp-collective).  Every lane must have
 // written its part of the record (.cg stores) before calling; the __syncwarp
 // orders those writes before lane 0's release store, which is cumulative.

@@ -79,29 +79,28 @@ __device__ typename Op::S lookback_chan(const typename Op::Args &args, const Cha
         if (lact) put_record<Op, TX>(lb, slot, 0, lane, cta);
         publish(lb, slot, kStatusAggregate, epoch, tile);
     }
-    int p = c - 1;
-    bool ok = true;
-    for (;;) {
-        const unsigned st = wait_status(lb, size_t(p) * g.nJ + j, epoch, tile);
-        if (st == kStatusPrefix) break;
-        if (st == kStatusNone || p == 0) {  // gave up (chunk 0 never holds an aggregate only)
-            ok = false;
-            break;
-        }
-        --p;
-    }
-    if (ok && lact) {
+    const int p = wait_window(lb, size_t(j), size_t(g.nJ), c, epoch, tile);
+    if (p >= 0 && lact) {
+        // excl = pref(p) o agg(p+1) o ... o agg(c-1), folded left to right;
+        // the record loads of a batch are independent and issued together.
         excl = get_record<Op, TX>(lb, size_t(p) * g.nJ + j, 1, lane);
-        for (int q = p + 1; q < c; ++q)
-            excl = Op::combine(excl, get_record<Op, TX>(lb, size_t(q) * g.nJ + j, 0, lane));
+        int q = p + 1;
+        for (; q + 4 <= c; q += 4) {
+            const S r0 = get_record<Op, TX>(lb, size_t(q) * g.nJ + j, 0, lane);
+            const S r1 = get_record<Op, TX>(lb, size_t(q + 1) * g.nJ + j, 0, lane);
+            const S r2 = get_record<Op, TX>(lb, size_t(q + 2) * g.nJ + j, 0, lane);
+            const S r3 = get_record<Op, TX>(lb, size_t(q + 3) * g.nJ + j, 0, lane);
+            excl = Op::combine(Op::combine(Op::combine(Op::combine(excl, r0), r1), r2), r3);
+        }
+        for (; q < c; ++q) excl = Op::combine(excl, get_record<Op, TX>(lb, size_t(q) * g.nJ + j, 0, lane));
     }
     if (lact) put_record<Op, TX>(lb, slot, 1, lane, Op::combine(excl, cta));
     publish(lb, slot, kStatusPrefix, epoch, tile);
     return excl;
 }
 
-template <class Op, int TX, int TY>
-__global__ void __launch_bounds__(TX *TY)
+template <class Op, int TX, int TY, int MINB>
+__global__ void __launch_bounds__(TX *TY, MINB)
     channel_scan_kernel(const typename Op::Args args, const ChanGeom g, const Lookback lb)
 {
     using S = typename Op::S;
@@ -197,7 +196,7 @@ __global__ void __launch_bounds__(TX *TY)
 
 // ------------------------------------------------------------ launchers
 
-template <class Op, int TX, int TY>
+template <class Op, int TX, int TY, int MINB = 1>
 struct ChanPlan {
     static constexpr int DC = TX * Op::VEC;
     static constexpr int TC = TY * Op::L;
@@ -239,12 +238,12 @@ struct ChanPlan {
         constexpr size_t smem = size_t(TY + 1) * Op::NS * DC * sizeof(float);
         if (smem > 48 * 1024) {
             static const cudaError_t attr = cudaFuncSetAttribute(
-                channel_scan_kernel<Op, TX, TY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                channel_scan_kernel<Op, TX, TY, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                 int(smem));
             if (attr != cudaSuccess)
                 return fail(MG_ERR_LAUNCH, "%s: %s", name, cudaGetErrorString(attr));
         }
-        channel_scan_kernel<Op, TX, TY><<<unsigned(nt), TX * TY, smem, s>>>(args, g, lb);
+        channel_scan_kernel<Op, TX, TY, MINB><<<unsigned(nt), TX * TY, smem, s>>>(args, g, lb);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return fail(MG_ERR_LAUNCH, "%s: launch failed: %s", name, cudaGetErrorString(e));

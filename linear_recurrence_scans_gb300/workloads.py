@@ -103,7 +103,7 @@ def haar_affine(B: int, T: int, n: int, k: int, v: int, seed: int = 0, device="c
     draw is made on the CPU in float64 and rounded to float32 after scaling.
     """
     q = haar_orthogonal(B * T * n, k, seed)
-    A = (decay * q).to(torch.float32).reshape(B, T, n, k, k).to(device)
+    A = (decay * q).to(torch.float32).reshape(B, T, n, k, k).contiguous().to(device)
     Bm = torch.randn((B, T, n, k, v), generator=_gen(seed + 1), dtype=torch.float32).to(device)
     if not grads:
         return A, Bm, None, None

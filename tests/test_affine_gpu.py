@@ -14,7 +14,7 @@ DEV = "cuda"
 
 
 def _nan(x):
-    return torch.full_like(x, float("nan"))
+    return torch.full(x.shape, float("nan"), device=x.device)
 
 
 def _run(mg, A, Bm, gAbar, gBbar, tol=TOL_F32):
