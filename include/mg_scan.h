@@ -170,6 +170,21 @@ mg_status mg_affine_scan_bwd(const float *A, const float *Abar, const float *Bba
                              int64_t B, int64_t T, int64_t n, int k, int v,
                              void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * Testing hook for the look-back's failure path (no counterpart on the page).
+ * Runs mg_linear_scan_fwd (float32 inputs) with the look-back record of tile
+ * `stall_tile` never published and every look-back wait bounded by
+ * `wait_limit_ns` nanoseconds.  A successor of that tile must give up its
+ * wait; the launch still completes, its outputs are unspecified, and the next
+ * mg_workspace_status on `ws` returns MG_ERR_TIMEOUT.  The workspace and the
+ * CUDA context stay usable.  stall_tile < 0 stalls nothing.
+ */
+mg_status mg_testing_linear_scan_fwd_stall(const float *a, const float *b, float *A, float *Bc,
+                                           int64_t B, int64_t T, int64_t D,
+                                           void *ws, size_t ws_bytes,
+                                           int64_t stall_tile, uint64_t wait_limit_ns,
+                                           cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -104,6 +104,9 @@ def load():
         lib.mg_affine_scan_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, vp, sz, vp]
         lib.mg_affine_scan_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, i32,
                                            vp, sz, vp]
+        lib.mg_testing_linear_scan_fwd_stall.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, sz,
+                                                         i64, ctypes.c_uint64, vp]
+        lib.mg_testing_linear_scan_fwd_stall.restype = st
         for name in ("mg_workspace_init", "mg_workspace_status", "mg_linear_scan_fwd",
                      "mg_linear_scan_bwd", "mg_log_scan_fwd", "mg_affine_scan_fwd",
                      "mg_affine_scan_bwd"):

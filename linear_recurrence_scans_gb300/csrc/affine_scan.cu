@@ -339,22 +339,31 @@ struct AffBwdSmall {
 
 // ============================================================ k in {8, 16}
 
-template <int K_, int W_, bool BWD_, int NW_, int L_>
+template <int K_, int W_, bool BWD_, int NW_, int L_, bool DB_>
 struct WCfg {
     static constexpr int K = K_, W = W_, NW = NW_, L = L_;
-    static constexpr bool BWD = BWD_;
+    static constexpr bool BWD = BWD_, DB = DB_;  // DB: double-buffered state exchange
     static constexpr int VV = BWD ? W - K : W;  // v
+    static constexpr int KK = K * K, KV = K * VV;
     static constexpr int NC = K + W;            // columns of X = [C | V]
     static constexpr int NCP = (NC + 7) / 8 * 8;
     static constexpr int R = K / 4;             // rows per lane (4 row blocks)
     static constexpr int CC = NCP / 8;          // columns per lane (8 column blocks)
     static constexpr int XS = NCP;              // shared row stride (floats)
-    static constexpr int MAT = K * XS;          // floats per shared matrix
+    static constexpr int MAT = K * XS;          // floats per shared state matrix
     static constexpr int REC = K * NC;          // floats per global record
     static constexpr int TC = NW * L;           // steps per tile
-    static constexpr int JD = K / 8;            // dA columns per lane
-    // shared: xb[NW][2][MAT], G[NW][MAT], carry[MAT]
-    static constexpr size_t SMEM = size_t(3 * NW + 1) * MAT * sizeof(float);
+    static constexpr int JD = K >= 8 ? K / 8 : 1;  // dA columns per lane (lanes cb*JD < K)
+    // Staged inputs of the tile's TC steps, region-major, each step block a
+    // multiple of 16 bytes.  Forward: A_t, B_t.  Backward: A_{t+1}, gAbar_t,
+    // gBbar_t, Abar_{t-1}, Bbar_{t-1}.
+    static constexpr int STEP = BWD ? 3 * KK + 2 * KV : KK + KV;
+    static constexpr int STAGE = TC * STEP;
+    static constexpr int NXB = DB ? 2 : 1;
+    static constexpr size_t SMEM =
+        16 + size_t(STAGE) * sizeof(float) + size_t((NXB + 1) * NW + 1) * MAT * sizeof(float);
+    static_assert(K >= 4 && K % 4 == 0, "warp kernel needs k in {4, 8, 16}");
+    static_assert((KV * 4) % 16 == 0 && (KK * 4) % 16 == 0, "bulk copies need 16-byte blocks");
 };
 
 struct AffGeom {
@@ -412,19 +421,18 @@ __device__ __forceinline__ void load_y(const float *m, int ld, int rb, int cb,
     }
 }
 
-// The element of step t as a y operand.
+// The staged element of tile step i as a y operand.  `has_next`: step t+1
+// exists (the adjoint's coefficient A_{t+1}^T is zero at t = T-1).
 template <class Cf>
-__device__ __forceinline__ void load_elem(const AffPtrs &p, const AffGeom &g, int64_t bb,
-                                          int64_t nn, int64_t t, int rb, int cb,
+__device__ __forceinline__ void load_elem(const float *stage, int i, bool has_next, int rb, int cb,
                                           float (&yc)[Cf::R][Cf::K], float (&yv)[Cf::R][Cf::CC])
 {
-    constexpr int K = Cf::K, KK = K * K, VV = Cf::VV, R = Cf::R;
-    const int64_t s = (bb * g.T + t) * g.n + nn;
+    constexpr int K = Cf::K, KK = Cf::KK, KV = Cf::KV, VV = Cf::VV, R = Cf::R, TC = Cf::TC;
     if constexpr (!Cf::BWD) {
-        const float *At = p.A + s * KK;
+        const float *At = stage + i * KK;
+        const float *Bt = stage + TC * KK + i * KV;
 #pragma unroll
         for (int r = 0; r < R; ++r) ld_floats<K>(At + (rb * R + r) * K, yc[r]);
-        const float *Bt = p.Bm + s * (K * VV);
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -433,8 +441,10 @@ __device__ __forceinline__ void load_elem(const AffPtrs &p, const AffGeom &g, in
                 yv[r][c] = (col >= K && col < Cf::NC) ? Bt[(rb * R + r) * VV + col - K] : 0.f;
             }
     } else {
-        if (t + 1 < g.T) {  // E_C[row][l] = A_{t+1}[l][row]
-            const float *An = p.A + (s + g.n) * KK;
+        const float *An = stage + i * KK;
+        const float *ga = stage + TC * KK + i * KK;
+        const float *gb = stage + 2 * TC * KK + i * KV;
+        if (has_next) {  // E_C[row][l] = A_{t+1}[l][row]
 #pragma unroll
             for (int l = 0; l < K; ++l) {
                 float a[R];
@@ -448,8 +458,6 @@ __device__ __forceinline__ void load_elem(const AffPtrs &p, const AffGeom &g, in
 #pragma unroll
                 for (int l = 0; l < K; ++l) yc[r][l] = 0.f;
         }
-        const float *ga = p.gAbar + s * KK;
-        const float *gb = p.gBbar + s * (K * VV);
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -506,16 +514,39 @@ __device__ __forceinline__ void get_block_record(const float *rec, int rb, int c
         }
 }
 
+// One step of a warp's scan: o <- E o X + [0 | E_V] with X read from the warp's
+// shared state buffer(s), then the new X written back.  `cur` selects the
+// buffer holding X (double-buffered) and is advanced.
+template <class Cf>
+__device__ __forceinline__ void warp_step(float *xw, int &cur, const float (&yc)[Cf::R][Cf::K],
+                                          const float (&yv)[Cf::R][Cf::CC], int rb, int cb,
+                                          float (&o)[Cf::R][Cf::CC])
+{
+    if constexpr (Cf::DB) {
+        block_gemm<Cf>(xw + cur * Cf::MAT, yc, yv, cb, o);
+        cur ^= 1;
+        put_block_smem<Cf>(xw + cur * Cf::MAT, rb, cb, o);
+        __syncwarp();
+    } else {
+        block_gemm<Cf>(xw, yc, yv, cb, o);
+        __syncwarp();
+        put_block_smem<Cf>(xw, rb, cb, o);
+        __syncwarp();
+    }
+}
+
 template <class Cf>
 __global__ void __launch_bounds__(Cf::NW * 32)
     affine_warp_kernel(const AffPtrs p, const AffGeom g, const Lookback lb)
 {
     constexpr int K = Cf::K, R = Cf::R, CC = Cf::CC, NW = Cf::NW, L = Cf::L, MAT = Cf::MAT;
-    constexpr int XS = Cf::XS, NC = Cf::NC, VV = Cf::VV;
+    constexpr int XS = Cf::XS, NC = Cf::NC, VV = Cf::VV, KK = Cf::KK, KV = Cf::KV, TC = Cf::TC;
     extern __shared__ float4 aff_smem[];
-    float *const xb = reinterpret_cast<float *>(aff_smem);  // [NW][2][MAT]
-    float *const G = xb + NW * 2 * MAT;                     // [NW][MAT]
-    float *const carry = G + NW * MAT;                      // [MAT]
+    unsigned long long *const bar = reinterpret_cast<unsigned long long *>(aff_smem);
+    float *const stage = reinterpret_cast<float *>(aff_smem) + 4;       // [STAGE]
+    float *const xb = stage + Cf::STAGE;                                // [NW][NXB][MAT]
+    float *const G = xb + NW * Cf::NXB * MAT;                           // [NW][MAT]
+    float *const carry = G + NW * MAT;                                  // [MAT]
 
     unsigned tile;
     unsigned long long epoch;
@@ -531,34 +562,74 @@ __global__ void __launch_bounds__(Cf::NW * 32)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rb = lane >> 3, cb = lane & 7;
     const int ct = Cf::BWD ? (g.nC - 1 - c) : c;
-    const int64_t tw = int64_t(ct) * Cf::TC + warp * L;  // first step of this warp
-    float *const xw = xb + warp * 2 * MAT;
+    const int64_t t0 = int64_t(ct) * TC;           // first step of the tile
+    const int nv = int(g.T - t0 < TC ? g.T - t0 : TC);  // valid steps in the tile
+    float *const xw = xb + warp * Cf::NXB * MAT;
+    auto step_index = [&](int64_t t) { return (bb * g.T + t) * g.n + nn; };
+
+    // ---- stage the tile's inputs with 1D bulk copies (warp 0), one mbarrier
+    if (threadIdx.x == 0) mbar_init(bar, 1);
+    __syncthreads();
+    if (warp == 0) {
+        unsigned bytes = 0;
+        for (int i = lane; i < nv; i += 32) {
+            const int64_t t = t0 + i;
+            if constexpr (!Cf::BWD) {
+                bytes += (KK + KV) * 4;
+            } else {
+                bytes += (KK + KV) * 4;                    // gAbar_t, gBbar_t
+                if (t + 1 < g.T) bytes += KK * 4;          // A_{t+1}
+                if (t >= 1) bytes += (KK + KV) * 4;        // Abar_{t-1}, Bbar_{t-1}
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, off);
+        if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
+        __syncwarp();
+        for (int i = lane; i < nv; i += 32) {
+            const int64_t t = t0 + i, s = step_index(t);
+            if constexpr (!Cf::BWD) {
+                tma_load_1d(stage + i * KK, p.A + s * KK, KK * 4, bar);
+                tma_load_1d(stage + TC * KK + i * KV, p.Bm + s * KV, KV * 4, bar);
+            } else {
+                tma_load_1d(stage + TC * KK + i * KK, p.gAbar + s * KK, KK * 4, bar);
+                tma_load_1d(stage + 2 * TC * KK + i * KV, p.gBbar + s * KV, KV * 4, bar);
+                if (t + 1 < g.T) tma_load_1d(stage + i * KK, p.A + (s + g.n) * KK, KK * 4, bar);
+                if (t >= 1) {
+                    tma_load_1d(stage + 2 * TC * KK + TC * KV + i * KK, p.Abar + (s - g.n) * KK,
+                                KK * 4, bar);
+                    tma_load_1d(stage + 3 * TC * KK + TC * KV + i * KV, p.Bbar + (s - g.n) * KV,
+                                KV * 4, bar);
+                }
+            }
+        }
+    }
+    if (!mbar_wait_bounded(bar, 0, lb.wait_limit_ns)) {
+        atomicOr(&lb.ctl->error, kErrLookbackTimeout);
+        mbar_wait_bounded(bar, 0, lb.wait_limit_ns);  // let copies in flight land
+    }
 
     float yc[R][K], yv[R][CC], o[R][CC];
+    const int pw = Cf::BWD ? NW - 1 - warp : warp;  // position in processing order
+    const int wbase = warp * L;                     // first tile step of this warp
 
-    // ---- aggregate of this warp's L steps, in processing order
-    // (pw = the warp's position in processing order: reversed for the adjoint)
-    const int pw = Cf::BWD ? NW - 1 - warp : warp;
+    // ---- pass 1: aggregate of the warp's L steps, in processing order
     int cur = 0;
     identity_block<Cf>(rb, cb, o);
     put_block_smem<Cf>(xw, rb, cb, o);
     __syncwarp();
 #pragma unroll 1
     for (int k = 0; k < L; ++k) {
-        const int i = Cf::BWD ? L - 1 - k : k;
-        const int64_t t = tw + i;
-        if (t >= g.T) continue;  // padding steps are the identity
-        load_elem<Cf>(p, g, bb, nn, t, rb, cb, yc, yv);
-        block_gemm<Cf>(xw + cur * MAT, yc, yv, cb, o);
-        cur ^= 1;
-        put_block_smem<Cf>(xw + cur * MAT, rb, cb, o);
-        __syncwarp();
+        const int i = wbase + (Cf::BWD ? L - 1 - k : k);
+        if (i >= nv) continue;  // padding steps are the identity
+        load_elem<Cf>(stage, i, t0 + i + 1 < g.T, rb, cb, yc, yv);
+        warp_step<Cf>(xw, cur, yc, yv, rb, cb, o);
     }
     put_block_smem<Cf>(G + pw * MAT, rb, cb, o);
     __syncthreads();
 
     // ---- warp 0: inclusive prefixes over the warps (processing order), then
-    //      the look-back
+    //      the look-back for the tile's carry-in
     if (warp == 0) {
         for (int w = 1; w < NW; ++w) {  // G[w] <- G[w-1] o G[w]
             load_y<Cf, false>(G + w * MAT, XS, rb, cb, yc, yv);
@@ -585,8 +656,7 @@ __global__ void __launch_bounds__(Cf::NW * 32)
                 publish(lb, slot, kStatusAggregate, epoch, tile);
             }
             const int pp = wait_window(lb, size_t(j), size_t(g.nJ), c, epoch, tile);
-            const bool ok = pp >= 0;
-            if (ok) {
+            if (pp >= 0) {
                 get_block_record<Cf>(lb.data + (size_t(pp) * g.nJ + j) * 2 * Cf::REC + Cf::REC, rb,
                                      cb, o);
             } else {
@@ -594,7 +664,7 @@ __global__ void __launch_bounds__(Cf::NW * 32)
             }
             put_block_smem<Cf>(carry, rb, cb, o);
             __syncwarp();
-            if (ok) {
+            if (pp >= 0) {
                 for (int q = pp + 1; q < c; ++q) {  // carry <- carry o agg(q)
                     load_y<Cf, true>(lb.data + (size_t(q) * g.nJ + j) * 2 * Cf::REC, NC, rb, cb,
                                      yc, yv);
@@ -604,7 +674,7 @@ __global__ void __launch_bounds__(Cf::NW * 32)
                     __syncwarp();
                 }
             }
-            // prefix of this chunk = carry o cta
+            // prefix of this tile = carry o cta
             load_y<Cf, false>(cta, XS, rb, cb, yc, yv);
             block_gemm<Cf>(carry, yc, yv, cb, o);
             put_block_record<Cf>(rec_pre, rb, cb, o);
@@ -625,27 +695,35 @@ __global__ void __launch_bounds__(Cf::NW * 32)
     put_block_smem<Cf>(xw, rb, cb, o);
     __syncwarp();
 
-    // ---- re-run the warp's steps from its start state and write outputs
+    // ---- pass 2: re-run the warp's steps from its start state, write outputs
 #pragma unroll 1
     for (int k = 0; k < L; ++k) {
-        const int i = Cf::BWD ? L - 1 - k : k;
-        const int64_t t = tw + i;
-        if (t >= g.T) continue;
-        load_elem<Cf>(p, g, bb, nn, t, rb, cb, yc, yv);
-        block_gemm<Cf>(xw + cur * MAT, yc, yv, cb, o);
-        cur ^= 1;
-        put_block_smem<Cf>(xw + cur * MAT, rb, cb, o);
-        __syncwarp();
-        const int64_t s = (bb * g.T + t) * g.n + nn;
+        const int i = wbase + (Cf::BWD ? L - 1 - k : k);
+        if (i >= nv) continue;
+        const int64_t t = t0 + i, s = step_index(t);
+        load_elem<Cf>(stage, i, t + 1 < g.T, rb, cb, yc, yv);
+        warp_step<Cf>(xw, cur, yc, yv, rb, cb, o);
         if constexpr (!Cf::BWD) {
 #pragma unroll
-            for (int r = 0; r < R; ++r)
+            for (int r = 0; r < R; ++r) {
+                const int row = rb * R + r;
+                if constexpr (CC % 4 == 0 && K % 4 == 0 && VV % 4 == 0) {
 #pragma unroll
-                for (int cc = 0; cc < CC; ++cc) {
-                    const int col = cb * CC + cc, row = rb * R + r;
-                    if (col < K) p.Abar_out[s * (K * K) + row * K + col] = o[r][cc];
-                    else if (col < NC) p.Bbar_out[s * (K * VV) + row * VV + col - K] = o[r][cc];
+                    for (int q = 0; q < CC; q += 4) {
+                        const int col = cb * CC + q;
+                        float v4[4] = {o[r][q], o[r][q + 1], o[r][q + 2], o[r][q + 3]};
+                        if (col < K) st_floats<4>(p.Abar_out + s * KK + row * K + col, v4);
+                        else if (col < NC) st_floats<4>(p.Bbar_out + s * KV + row * VV + col - K, v4);
+                    }
+                } else {
+#pragma unroll
+                    for (int cc = 0; cc < CC; ++cc) {
+                        const int col = cb * CC + cc;
+                        if (col < K) p.Abar_out[s * KK + row * K + col] = o[r][cc];
+                        else if (col < NC) p.Bbar_out[s * KV + row * VV + col - K] = o[r][cc];
+                    }
                 }
+            }
         } else {
             // dB_t = Lam_t (columns 2K .. NC of X)
 #pragma unroll
@@ -653,24 +731,26 @@ __global__ void __launch_bounds__(Cf::NW * 32)
 #pragma unroll
                 for (int cc = 0; cc < CC; ++cc) {
                     const int col = cb * CC + cc, row = rb * R + r;
-                    if (col >= 2 * K && col < NC) p.dB[s * (K * VV) + row * VV + col - 2 * K] = o[r][cc];
+                    if (col >= 2 * K && col < NC) p.dB[s * KV + row * VV + col - 2 * K] = o[r][cc];
                 }
-            // dA_t[row][jc] = sum_c X[row][K + c] * Y[jc][c],  Y = [Abar_{t-1} | Bbar_{t-1}]
-            const float *xs = xw + cur * MAT;
+            // dA_t[row][jc] = sum_q X[row][K + q] * Y[jc][q],  Y = [Abar_{t-1} | Bbar_{t-1}]
             constexpr int JD = Cf::JD, WW = Cf::W;
-            float da[R][JD];
-            if (t > 0) {
-                const int64_t sp = s - g.n;
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-#pragma unroll
-                    for (int jj = 0; jj < JD; ++jj) da[r][jj] = 0.f;
+            if (cb * JD < K) {
+                const float *xs = xw + (Cf::DB ? cur * MAT : 0);
+                const float *Ap = stage + 2 * TC * KK + TC * KV + i * KK;
+                const float *Bp = stage + 3 * TC * KK + TC * KV + i * KV;
+                float da[R][JD];
 #pragma unroll
                 for (int jj = 0; jj < JD; ++jj) {
                     const int jc = cb * JD + jj;
                     float y[WW];
-                    ld_floats<K>(p.Abar + sp * (K * K) + jc * K, y);
-                    ld_floats<VV>(p.Bbar + sp * (K * VV) + jc * VV, y + K);
+                    if (t > 0) {
+                        ld_floats<K>(Ap + jc * K, y);
+                        ld_floats<VV>(Bp + jc * VV, y + K);
+                    } else {  // Abar_0 = I, Bbar_0 = 0
+#pragma unroll
+                        for (int q = 0; q < WW; ++q) y[q] = (q == jc) ? 1.f : 0.f;
+                    }
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         const float *xr = xs + (rb * R + r) * XS + K;
@@ -680,16 +760,11 @@ __global__ void __launch_bounds__(Cf::NW * 32)
                         da[r][jj] = acc;
                     }
                 }
-            } else {
 #pragma unroll
                 for (int r = 0; r < R; ++r)
-#pragma unroll
-                    for (int jj = 0; jj < JD; ++jj)
-                        da[r][jj] = xs[(rb * R + r) * XS + K + cb * JD + jj];
+                    st_floats<JD>(p.dA + s * KK + (rb * R + r) * K + cb * JD, da[r]);
             }
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-                st_floats<JD>(p.dA + s * (K * K) + (rb * R + r) * K + cb * JD, da[r]);
+            if constexpr (!Cf::DB) __syncwarp();  // the next step overwrites xw
         }
     }
     finish_cta(lb, epoch);
@@ -738,23 +813,25 @@ struct WarpPlan {
 
 // ------------------------------------------------------------ dispatch
 
-constexpr int kSmallTY = 8, kSmallL = 4, kWarpNW = 4, kWarpL = 8;
+constexpr int kSmallTY = 8, kSmallL = 4;
 
 template <int K, int V>
 using SmallFwd = ChanPlan<AffFwdSmall<K, V, kSmallL>, 32, kSmallTY>;
 template <int K, int V>
-using SmallBwd = ChanPlan<AffBwdSmall<K, V, (K * (2 * K + V) > 48 ? 2 : kSmallL)>, 32,
-                          (K * (2 * K + V) > 48 ? 4 : kSmallTY)>;
+using SmallBwd = ChanPlan<AffBwdSmall<K, V, kSmallL>, 32, kSmallTY>;
+// Warp kernel tiles: k = 4 carries little data per step, so a tile covers
+// 4 x 16 steps; k = 8, 16 cover 4 x 8 (forward) and 4 x 4 (backward, five
+// staged inputs per step) with a single-buffered exchange to fit two CTAs/SM.
 template <int K, int V>
-using BigFwd = WarpPlan<WCfg<K, V, false, kWarpNW, kWarpL>>;
+using BigFwd = WarpPlan<WCfg<K, V, false, 4, (K == 4 ? 16 : 8), true>>;
 template <int K, int V>
-using BigBwd = WarpPlan<WCfg<K, K + V, true, kWarpNW, kWarpL>>;
+using BigBwd = WarpPlan<WCfg<K, K + V, true, 4, (K == 4 ? 16 : 4), (K < 16)>>;
 
 template <int K, int V>
 size_t ws_kv(int64_t B, int64_t T, int64_t n)
 {
     size_t a, b;
-    if constexpr (K <= 4) {
+    if constexpr (K <= 2) {
         a = SmallFwd<K, V>::ws_bytes(B, T, n);
         b = SmallBwd<K, V>::ws_bytes(B, T, n);
     } else {
@@ -769,7 +846,7 @@ mg_status fwd_kv(const float *A, const float *Bm, float *Abar, float *Bbar, int6
                  int64_t n, void *ws, size_t wsb, cudaStream_t s, const LaunchOpts &o)
 {
     const char *nm = "mg_affine_scan_fwd";
-    if constexpr (K <= 4) {
+    if constexpr (K <= 2) {
         return SmallFwd<K, V>::launch({A, Bm, Abar, Bbar}, B, T, n, ws, wsb, s, o, nm);
     } else {
         AffPtrs p{};
@@ -787,7 +864,7 @@ mg_status bwd_kv(const float *A, const float *Abar, const float *Bbar, const flo
                  void *ws, size_t wsb, cudaStream_t s, const LaunchOpts &o)
 {
     const char *nm = "mg_affine_scan_bwd";
-    if constexpr (K <= 4) {
+    if constexpr (K <= 2) {
         return SmallBwd<K, V>::launch({A, Abar, Bbar, gAbar, gBbar, dA, dB}, B, T, n, ws, wsb, s,
                                       o, nm);
     } else {

@@ -267,4 +267,28 @@ mg_status mg_affine_scan_bwd(const float *A, const float *Abar, const float *Bba
                              stream, LaunchOpts{});
 }
 
+mg_status mg_testing_linear_scan_fwd_stall(const float *a, const float *b, float *A, float *Bc,
+                                           int64_t B, int64_t T, int64_t D, void *ws,
+                                           size_t ws_bytes, int64_t stall_tile,
+                                           uint64_t wait_limit_ns, cudaStream_t stream)
+{
+    const char *fn = "mg_testing_linear_scan_fwd_stall";
+    g_detail[0] = 0;
+    MG_TRY(check_dims(fn, {B, T, D}));
+    if (B == 0 || T == 0 || D == 0) return MG_OK;
+    const size_t n = size_t(B) * T * D;
+    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D)));
+    MG_TRY(check_bufs(fn, {{a, n * 4, "a", false},
+                           {b, n * 4, "b", false},
+                           {A, n * 4, "A", true},
+                           {Bc, n * 4, "Bc", true},
+                           {ws, ws_bytes, "workspace", true}}));
+    if (wait_limit_ns == 0 || wait_limit_ns > 10000000000ull)
+        return fail(MG_ERR_INVALID_ARG, "%s: wait_limit_ns must be in (0, 1e10]", fn);
+    LaunchOpts o;
+    o.wait_limit_ns = wait_limit_ns;
+    o.stall_tile = stall_tile;
+    return launch_linear_fwd(a, b, MG_F32, A, Bc, B, T, D, ws, ws_bytes, stream, o);
+}
+
 }  // extern "C"

@@ -1,0 +1,57 @@
+"""Failure detection on the GPU without a GPU fault: a look-back wait that
+runs out (its predecessor never publishes) gives up within its bound, the
+launch completes, the host reads MG_ERR_TIMEOUT, and the context and the
+workspace stay usable.  A workspace that was not zero-filled is reported,
+not faulted on."""
+from __future__ import annotations
+
+import pytest
+import torch
+
+from linear_recurrence_scans_gb300 import workloads as wl
+from parity import TOL_F32, linear_fwd_errors
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def test_stalled_predecessor_times_out_and_recovers(cuda_lib):
+    mg = cuda_lib
+    lib = mg.load()
+    B, T, D = 1, 4096, 128   # one channel tile, many time chunks
+    a, b, _, _ = wl.mingru_linear(B, T, D, seed=21, grads=False)
+    ad, bd = a.to(DEV), b.to(DEV)
+    A, Bc = torch.empty_like(ad), torch.empty_like(ad)
+    ws = mg.new_workspace(mg.linear_workspace_size(B, T, D), DEV)
+    s = torch.cuda.current_stream().cuda_stream
+    st = lib.mg_testing_linear_scan_fwd_stall(ad.data_ptr(), bd.data_ptr(), A.data_ptr(),
+                                              Bc.data_ptr(), B, T, D, ws.data_ptr(), ws.numel(),
+                                              5, 20_000_000, s)   # tile 5 stalls; 20 ms waits
+    assert st == mg.MG_OK
+    with pytest.raises(mg.MgScanError) as ei:
+        mg.workspace_status(ws)
+    assert ei.value.status == mg.MG_ERR_TIMEOUT
+    mg.workspace_status(ws)          # the record was cleared
+    # the same workspace and context still give correct results
+    A2, Bc2 = mg.linear_scan_fwd(ad, bd, ws=ws)
+    errs = linear_fwd_errors(a, b, A2, Bc2)
+    assert max(errs.values()) <= TOL_F32, errs
+    mg.workspace_status(ws)
+
+
+def test_non_zeroed_workspace_is_reported(cuda_lib):
+    mg = cuda_lib
+    B, T, D = 2, 700, 64
+    a, b, _, _ = wl.mingru_linear(B, T, D, seed=22, grads=False, device=DEV)
+    ws = mg.new_workspace(mg.linear_workspace_size(B, T, D), DEV)
+    ws.fill_(255)
+    mg.linear_scan_fwd(a, b, ws=ws)
+    with pytest.raises(mg.MgScanError) as ei:
+        mg.workspace_status(ws)
+    assert ei.value.status == mg.MG_ERR_INVALID_ARG
+    lib = mg.load()
+    assert lib.mg_workspace_init(ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream) == 0
+    A, Bc = mg.linear_scan_fwd(a, b, ws=ws)
+    mg.workspace_status(ws)
+    errs = linear_fwd_errors(a.cpu(), b.cpu(), A, Bc)
+    assert max(errs.values()) <= TOL_F32, errs
