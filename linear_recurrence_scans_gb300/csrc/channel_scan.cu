@@ -468,12 +468,15 @@ size_t linear_ws_bytes(int64_t B, int64_t T, int64_t D)
     m = mx<LinBwdF32s>(m, B, T, D);
     m = mx<LinBwdB16>(m, B, T, D);
     m = mx<LinBwdB16s>(m, B, T, D);
-    return m;
+    const size_t st = stream_linear_ws_bytes(B, T, D);
+    return m > st ? m : st;
 }
 
 size_t log_ws_bytes(int64_t B, int64_t T, int64_t D)
 {
-    return mx<LogF32s>(mx<LogF32>(0, B, T, D), B, T, D);
+    const size_t m = mx<LogF32s>(mx<LogF32>(0, B, T, D), B, T, D);
+    const size_t st = stream_log_ws_bytes(B, T, D);
+    return m > st ? m : st;
 }
 
 mg_status launch_linear_fwd(const void *a, const void *b, mg_dtype dt, float *A, float *Bc,
@@ -481,6 +484,8 @@ mg_status launch_linear_fwd(const void *a, const void *b, mg_dtype dt, float *A,
                             const LaunchOpts &o)
 {
     const char *nm = "mg_linear_scan_fwd";
+    if (o.engine != LaunchOpts::kChunked && stream_linear_ok(dt, D))
+        return stream_linear_fwd(a, b, dt, A, Bc, B, T, D, ws, wsb, s, o);
     if (dt == MG_F32) {
         using F = const float *;
         if (D % 4 == 0)
@@ -498,6 +503,8 @@ mg_status launch_linear_bwd(const void *a, mg_dtype dt, const float *A, const fl
                             const LaunchOpts &o)
 {
     const char *nm = "mg_linear_scan_bwd";
+    if (o.engine != LaunchOpts::kChunked && stream_linear_ok(dt, D))
+        return stream_linear_bwd(a, dt, A, Bc, gA, gBc, da, db, B, T, D, ws, wsb, s, o);
     if (dt == MG_F32) {
         using F = const float *;
         if (D % 4 == 0)
@@ -514,6 +521,8 @@ mg_status launch_log_fwd(const float *lc, const float *lv, float *h, int64_t B, 
                          int64_t D, void *ws, size_t wsb, cudaStream_t s, const LaunchOpts &o)
 {
     const char *nm = "mg_log_scan_fwd";
+    if (o.engine != LaunchOpts::kChunked && stream_log_ok(D))
+        return stream_log_fwd(lc, lv, h, B, T, D, ws, wsb, s, o);
     if (D % 4 == 0) return LogF32::launch({lc, lv, h}, B, T, D, ws, wsb, s, o, nm);
     return LogF32s::launch({lc, lv, h}, B, T, D, ws, wsb, s, o, nm);
 }

@@ -21,6 +21,10 @@ struct LaunchOpts {
     unsigned long long wait_limit_ns = 2000000000ull;  // 2 s of %globaltimer
     unsigned int max_polls = 1u << 24;
     long long stall_tile = -1;                         // testing only
+    // Which kernel shape serves the channel-wise ops: the persistent
+    // warp-specialised one where D allows it (default), or the one-tile-per-CTA
+    // chunk engine.
+    enum Engine { kAuto = 0, kChunked = 1 } engine = kAuto;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -70,6 +74,23 @@ mg_status launch_affine_bwd(const float *A, const float *Abar, const float *Bbar
                             const float *gAbar, const float *gBbar, float *dA, float *dB,
                             int64_t B, int64_t T, int64_t n, int k, int v, void *ws,
                             size_t ws_bytes, cudaStream_t s, const LaunchOpts &o);
+
+// Persistent warp-specialised variants (stream_scan.cu), used when D is a
+// multiple of the 16-byte vector width.
+bool stream_linear_ok(mg_dtype dt, int64_t D);
+bool stream_log_ok(int64_t D);
+size_t stream_linear_ws_bytes(int64_t B, int64_t T, int64_t D);
+size_t stream_log_ws_bytes(int64_t B, int64_t T, int64_t D);
+mg_status stream_linear_fwd(const void *a, const void *b, mg_dtype dt, float *A, float *Bc,
+                            int64_t B, int64_t T, int64_t D, void *ws, size_t ws_bytes,
+                            cudaStream_t s, const LaunchOpts &o);
+mg_status stream_linear_bwd(const void *a, mg_dtype dt, const float *A, const float *Bc,
+                            const float *gA, const float *gBc, float *da, float *db, int64_t B,
+                            int64_t T, int64_t D, void *ws, size_t ws_bytes, cudaStream_t s,
+                            const LaunchOpts &o);
+mg_status stream_log_fwd(const float *lc, const float *lv, float *h, int64_t B, int64_t T,
+                         int64_t D, void *ws, size_t ws_bytes, cudaStream_t s,
+                         const LaunchOpts &o);
 
 // ------------------------------------------------------------- device side
 

@@ -1,0 +1,74 @@
+"""Run one op of the library on one named workload a few times (for profilers).
+
+    python -m linear_recurrence_scans_gb300.run_case <case> [repeats]
+
+Cases (inputs seeded, resident on cuda:0 before the first launch):
+
+  linear_fwd / linear_bwd        minGRU linear scan, B=8 T=4096 D=1024, fp32
+  linear_bf16_fwd / _bwd         minGRU linear scan, B=4 T=8192 D=4096, bf16 a, b
+                                 (a quarter of the 2^31-element workload, same tiles)
+  log_fwd                        minGRU log-space scan, B=8 T=2048 D=2048
+  affine4_fwd / affine4_bwd      Haar affine scan, B=4 T=2048 n=64 k=v=4
+  affine16_fwd / affine16_bwd    Haar affine scan, B=2 T=1024 n=32 k=v=16
+
+Every case runs its op `repeats` times (default 3) after one set-up call of
+the forward op where the backward needs the forward's outputs.  Each input is
+larger than L2 except for the affine cases (134 MB and 268 MB in total).
+"""
+from __future__ import annotations
+
+import sys
+
+import torch
+
+import linear_recurrence_scans_gb300 as mg
+from linear_recurrence_scans_gb300 import workloads as wl
+
+CASES = ("linear_fwd", "linear_bwd", "linear_bf16_fwd", "linear_bf16_bwd", "log_fwd",
+         "affine4_fwd", "affine4_bwd", "affine16_fwd", "affine16_bwd")
+
+
+def main(argv):
+    if not argv or argv[0] not in CASES:
+        print(__doc__)
+        return 2
+    case = argv[0]
+    reps = int(argv[1]) if len(argv) > 1 else 3
+    dev = torch.device("cuda", 0)
+    mg.load()
+    if case.startswith("linear"):
+        bf16 = "bf16" in case
+        shape = (4, 8192, 4096) if bf16 else (8, 4096, 1024)
+        a, b, gA, gBc = wl.mingru_linear(*shape, seed=0, device=dev,
+                                         in_dtype=torch.bfloat16 if bf16 else torch.float32)
+        A, Bc = mg.linear_scan_fwd(a, b)
+        da, db = torch.empty_like(A), torch.empty_like(A)
+        for _ in range(reps):
+            if case.endswith("fwd"):
+                mg.linear_scan_fwd(a, b, out=(A, Bc))
+            else:
+                mg.linear_scan_bwd(a, A, Bc, gA, gBc, out=(da, db))
+    elif case == "log_fwd":
+        lc, lv = wl.mingru_log(8, 2048, 2048, seed=0, device=dev)
+        h = torch.empty_like(lc)
+        for _ in range(reps):
+            mg.parallel_scan_log_fwd(lc, lv, out=h)
+    else:
+        k = 4 if case.startswith("affine4") else 16
+        shape = (4, 2048, 64) if k == 4 else (2, 1024, 32)
+        A, Bm, gA, gB = wl.haar_affine(*shape, k, k, seed=0, device=dev)
+        Abar, Bbar = mg.affine_scan_fwd(A, Bm)
+        dA, dB = torch.empty_like(A), torch.empty_like(Bm)
+        for _ in range(reps):
+            if case.endswith("fwd"):
+                mg.affine_scan_fwd(A, Bm, out=(Abar, Bbar))
+            else:
+                mg.affine_scan_bwd(A, Abar, Bbar, gA, gB, out=(dA, dB))
+    torch.cuda.synchronize(dev)
+    mg.workspace_status()
+    print(f"ok {case} x{reps}")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main(sys.argv[1:]))
