@@ -233,7 +233,7 @@ def run_ours(args, ws_size, rank, local):
                         "GB_s": round(BWD_BYTES_PER_ELT * n / bwd_avg / 1e9, 1),
                         "frac": round(BWD_BYTES_PER_ELT * n / bwd_avg / 1e9 / peak, 4)}}
 
-    e2e = run_e2e(mg, sets[0], dev, stream, args, ws)
+    e2e = run_e2e(mg, sets[0], dev, stream, args, ws, ws_size)
     extra = run_extra(mg, dev, peak) if (rank == 0 and not args.no_extra) else None
     cpu = cpu_baseline() if (rank == 0 and ws_size == 1 and not args.no_cpu) else None
 
@@ -257,7 +257,7 @@ def run_ours(args, ws_size, rank, local):
     return line
 
 
-def run_e2e(mg, inputs, dev, stream, args, ws):
+def run_e2e(mg, inputs, dev, stream, args, ws, ws_size):
     """Same metric through the public API with host buffers: each step copies
     a, b, gA, gBc from pinned host memory, runs fwd + bwd and copies A, Bc,
     da, db back to pinned host memory."""
@@ -277,6 +277,7 @@ def run_e2e(mg, inputs, dev, stream, args, ws):
     for _ in range(3):
         step()
     torch.cuda.synchronize(dev)
+    barrier(ws_size)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     w0 = time.perf_counter()
@@ -286,8 +287,8 @@ def run_e2e(mg, inputs, dev, stream, args, ws):
     t1.record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - w0
-    el = max(t0.elapsed_time(t1) * 1e-3, wall)
-    return {"value": B * T * D * k / el, "unit": UNIT, "steps": k,
+    el, units = aggregate(max(t0.elapsed_time(t1) * 1e-3, wall), float(B * T * D * k), ws_size)
+    return {"value": units / el, "unit": UNIT, "steps": k,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "ms_per_step": el / k * 1e3}
 

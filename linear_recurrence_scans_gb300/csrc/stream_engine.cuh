@@ -7,18 +7,19 @@
 //   warp 0        producer: takes tickets and streams each tile's input rows
 //                 into a ring of STAGES shared-memory buffers with 1D TMA bulk
 //                 copies (one mbarrier per stage counts the bytes);
-//   warp 1        look-back: folds the compute warps' row aggregates into the
-//                 tile aggregate, runs the decoupled look-back (lookback.cuh)
-//                 and hands the tile's carry-in back through shared memory;
-//   warps 2..     compute: each owns L consecutive steps of a tile for 32*VEC
+//   warps 1..NLB  look-back: warp w takes the CTA's tiles i = w-1 (mod NLB);
+//                 it folds the compute warps' row aggregates into the tile
+//                 aggregate, runs the decoupled look-back (lookback.cuh) and
+//                 hands the tile's carry-in back through shared memory;
+//   the rest      compute: each owns L consecutive steps of a tile for 32*VEC
 //                 channels (one 16-byte vector per lane per row).  Pass 1 folds
 //                 the steps into a row aggregate; pass 2 re-runs them from the
 //                 row's start state (carry o earlier rows) and writes outputs.
 //
-// The compute warps run pass 1 of tile i+1 before pass 2 of tile i, so the
-// look-back of tile i overlaps useful work, and the producer keeps the next
-// tiles' loads in flight meanwhile.  Inputs are read from HBM once (staged),
-// outputs written once (vector stores from registers).
+// The compute warps run pass 2 of tile i only after pass 1 of tile i+NLB, so
+// NLB look-backs (each a few L2 round trips) are in flight per SM at once,
+// overlapped with the compute warps' work and the producer's loads.  Inputs
+// are read from HBM once (staged), outputs written once (vector stores).
 //
 // Synchronisation per stage s (phase parity = use count & 1):
 //   full[s]   producer -> compute, look-back    (tx bytes of the copies)
@@ -82,6 +83,7 @@ struct StreamLayout {
     static constexpr size_t AGG = size_t(NCW) * NS * DC;  // floats per stage
     static constexpr size_t SMEM = HDR + size_t(SG) * STAGE + size_t(SG) * (AGG + NS * DC) * 4;
     static_assert(STAGE % 16 == 0, "stage buffers must stay 16-byte aligned");
+    static_assert(SMEM + 64 <= 232448, "more shared memory than one SM offers");
 };
 
 // Row i of staged array a, at this lane's channel group.
@@ -93,14 +95,38 @@ __device__ __forceinline__ const E *srow(const char *st, int a, int i, int lane)
            lane * Op::VEC;
 }
 
+// Wait for phase `parity` of `bar`, or until iteration `it` is past the end
+// of the CTA's work (`*end` set by the producer).  1 = phase done, 0 = past
+// the end, -1 = gave up (error recorded).
+__device__ __forceinline__ int mbar_wait_or_end(unsigned long long *bar, unsigned parity,
+                                                const Lookback &lb, const volatile int *end,
+                                                int it)
+{
+    if (mbar_try_wait(bar, parity)) return 1;
+    const unsigned long long t0 = global_timer_ns();
+    for (unsigned k = 1;; ++k) {
+        if (mbar_try_wait(bar, parity)) return 1;
+        if (it >= *end) return 0;
+        if ((k & 31u) == 0u) {
+            if (ld_relaxed_u32(&lb.ctl->error) != 0) return -1;
+            if (global_timer_ns() - t0 > lb.wait_limit_ns || k >= lb.max_polls) {
+                atomicOr(&lb.ctl->error, kErrLookbackTimeout);
+                return -1;
+            }
+        }
+    }
+}
+
 template <class Op>
-__global__ void __launch_bounds__((Op::NCW + 2) * 32, 1)
+__global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
     stream_scan_kernel(const typename Op::Args args, const ChanGeom g, const Lookback lb)
 {
     using S = typename Op::S;
     using Ly = StreamLayout<Op>;
     constexpr int NS = Op::NS, VEC = Op::VEC, L = Op::L, NCW = Op::NCW, SG = Ly::SG;
+    constexpr int NLB = Op::NLB, LAG = NLB;
     constexpr int DC = Ly::DC, TC = Ly::TC;
+    static_assert(SG >= LAG + 2, "the ring needs the lagged tiles plus one in flight");
     extern __shared__ float4 stream_smem[];
     char *const smem = reinterpret_cast<char *>(stream_smem);
     unsigned long long *const full = reinterpret_cast<unsigned long long *>(smem);
@@ -112,6 +138,7 @@ __global__ void __launch_bounds__((Op::NCW + 2) * 32, 1)
     float *const s_agg = reinterpret_cast<float *>(stages + size_t(SG) * Ly::STAGE);
     float *const s_carry = s_agg + SG * Ly::AGG;
     __shared__ unsigned long long s_epoch;
+    __shared__ int s_end;  // first iteration index without a tile
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SG; ++s) {
@@ -121,10 +148,12 @@ __global__ void __launch_bounds__((Op::NCW + 2) * 32, 1)
             mbar_init(carry + s, 1);
         }
         s_epoch = ld_relaxed_u64(&lb.ctl->epoch);
+        s_end = 0x7fffffff;
     }
     __syncthreads();
     const unsigned long long epoch = s_epoch;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int *const end = &s_end;
 
     auto geom_of = [&](unsigned tile, int &c, int &j, int64_t &bb, int &d0, int64_t &t0) {
         c = int(tile / unsigned(g.nJ));
@@ -147,8 +176,9 @@ __global__ void __launch_bounds__((Op::NCW + 2) * 32, 1)
             tile = __shfl_sync(0xffffffffu, tile, 0);
             if (tile >= g.n_tiles) {
                 if (lane == 0) {
-                    s_tile[s] = kSentinelTile;
                     if (tile >= g.n_tiles + gridDim.x) atomicOr(&lb.ctl->error, kErrBadTicket);
+                    s_tile[s] = kSentinelTile;
+                    *end = it;
                     mbar_arrive(full + s);
                 }
                 ++it;
@@ -189,17 +219,18 @@ __global__ void __launch_bounds__((Op::NCW + 2) * 32, 1)
                 }
             }
         }
+        if (lane == 0 && *end > it) *end = it;  // stopped early on an error
         // Drain: the copies of the last uses of every stage must land before
         // the CTA's shared memory is released (normally already done).
         for (int k = (it > SG ? it - SG : 0); k < it; ++k)
             mbar_wait_bounded(full + (k % SG), unsigned(k / SG) & 1u, lb.wait_limit_ns);
-    } else if (warp == 1) {
+    } else if (warp <= NLB) {
         // ----------------------------------------------------------- look-back
-        for (int it = 0;; ++it) {
+        for (int it = warp - 1;; it += NLB) {
             const int s = it % SG;
-            if (!mbar_wait_or_error(aggr + s, unsigned(it / SG) & 1u, lb)) break;
+            if (mbar_wait_or_end(aggr + s, unsigned(it / SG) & 1u, lb, end, it) != 1) break;
             const unsigned tile = s_tile[s];
-            if (tile == kSentinelTile || tile >= g.n_tiles) break;
+            if (tile >= g.n_tiles) break;
             int c, j, d0;
             int64_t bb, t0;
             geom_of(tile, c, j, bb, d0, t0);
@@ -225,7 +256,7 @@ __global__ void __launch_bounds__((Op::NCW + 2) * 32, 1)
         }
     } else {
         // ------------------------------------------------------------- compute
-        const int ty = warp - 2;
+        const int ty = warp - 1 - NLB;
         auto pass1 = [&](int s, unsigned tile) {
             int c, j, d0;
             int64_t bb, t0;
@@ -268,33 +299,36 @@ __global__ void __launch_bounds__((Op::NCW + 2) * 32, 1)
                 Op::step2(args, st, i, lane, t0 + i, g, bb, d, act, state);
             }
         };
-
-        int it = 0;
-        if (!mbar_wait_or_error(full, 0, lb)) {
-            if (lane == 0) mbar_arrive(aggr);
-        } else {
-            unsigned tile = s_tile[0];
-            bool have = tile < g.n_tiles;
-            if (have) pass1(0, tile);
+        // pass 2 of iteration k: wait for its carry, re-run, free the stage
+        auto finish = [&](int k) -> bool {
+            const int s = k % SG;
+            if (!mbar_wait_or_error(carry + s, unsigned(k / SG) & 1u, lb)) return false;
+            pass2(s, s_tile[s]);
             __syncwarp();
-            if (lane == 0) mbar_arrive(aggr);
-            while (have) {
-                const int s = it % SG, s1 = (it + 1) % SG;
-                if (!mbar_wait_or_error(full + s1, unsigned((it + 1) / SG) & 1u, lb)) break;
-                const unsigned tile1 = s_tile[s1];
-                const bool have1 = tile1 < g.n_tiles;
-                if (have1) pass1(s1, tile1);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(aggr + s1);
-                if (!mbar_wait_or_error(carry + s, unsigned(it / SG) & 1u, lb)) break;
-                pass2(s, tile);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty + s);
-                ++it;
-                tile = tile1;
-                have = have1;
+            if (lane == 0) mbar_arrive(empty + s);
+            return true;
+        };
+        int it = 0;
+        bool ok = true;
+        for (;; ++it) {
+            const int s = it % SG;
+            if (!mbar_wait_or_error(full + s, unsigned(it / SG) & 1u, lb)) {
+                ok = false;
+                break;
+            }
+            const unsigned tile = s_tile[s];
+            if (tile >= g.n_tiles) break;
+            pass1(s, tile);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(aggr + s);
+            if (it >= LAG && !finish(it - LAG)) {
+                ok = false;
+                break;
             }
         }
+        if (ok)
+            for (int k = (it > LAG ? it - LAG : 0); k < it; ++k)
+                if (!finish(k)) break;
     }
     finish_cta(lb, epoch);
 }
@@ -352,7 +386,7 @@ struct StreamPlan {
         const ChanGeom g = geom(B, T, D);
         const Lookback lb = make_lookback(ws, nt, o);
         const unsigned grid = unsigned(nt < size_t(n_sm) ? nt : size_t(n_sm));
-        stream_scan_kernel<Op><<<grid, (Op::NCW + 2) * 32, Ly::SMEM, s>>>(args, g, lb);
+        stream_scan_kernel<Op><<<grid, (Op::NCW + Op::NLB + 1) * 32, Ly::SMEM, s>>>(args, g, lb);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return fail(MG_ERR_LAUNCH, "%s: launch failed: %s", name, cudaGetErrorString(e));
