@@ -78,10 +78,11 @@ struct StreamLayout {
     static constexpr int arr_bytes(int a) { return TC * DC * Op::elt(a); }
     static constexpr int arr_off(int a) { return a == 0 ? 0 : arr_off(a - 1) + arr_bytes(a - 1); }
     static constexpr int STAGE = arr_off(NARR);
+    static constexpr int NAG = Op::NLB + 1;  // tiles between pass 1 and pass 2
     static constexpr int BAR_BYTES = 4 * SG * 8;
     static constexpr int HDR = (BAR_BYTES + SG * 4 + 127) / 128 * 128;
-    static constexpr size_t AGG = size_t(NCW) * NS * DC;  // floats per stage
-    static constexpr size_t SMEM = HDR + size_t(SG) * STAGE + size_t(SG) * (AGG + NS * DC) * 4;
+    static constexpr size_t AGG = size_t(NCW) * NS * DC;  // floats per aggregate slot
+    static constexpr size_t SMEM = HDR + size_t(SG) * STAGE + size_t(NAG) * (AGG + NS * DC) * 4;
     static_assert(STAGE % 16 == 0, "stage buffers must stay 16-byte aligned");
     static_assert(SMEM + 64 <= 232448, "more shared memory than one SM offers");
 };
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
     unsigned *const s_tile = reinterpret_cast<unsigned *>(smem + Ly::BAR_BYTES);
     char *const stages = smem + Ly::HDR;
     float *const s_agg = reinterpret_cast<float *>(stages + size_t(SG) * Ly::STAGE);
-    float *const s_carry = s_agg + SG * Ly::AGG;
+    float *const s_carry = s_agg + Ly::NAG * Ly::AGG;
     __shared__ unsigned long long s_epoch;
     __shared__ int s_end;  // first iteration index without a tile
 
@@ -236,7 +237,8 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
             geom_of(tile, c, j, bb, d0, t0);
             const int ld = d0 + lane * VEC;
             const bool lchan = ld < g.D;
-            const float *agg = s_agg + s * Ly::AGG;
+            const int a_slot = it % Ly::NAG;
+            const float *agg = s_agg + a_slot * Ly::AGG;
             S cta;
 #pragma unroll
             for (int k = 0; k < NCW; ++k) {
@@ -248,7 +250,7 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
             }
             const S excl = lookback_chan<Op, 32>(args, g, lb, c, j, bb, ld, true, lchan, tile,
                                                  epoch, cta);
-            float *cr = s_carry + s * NS * DC;
+            float *cr = s_carry + a_slot * NS * DC;
 #pragma unroll
             for (int q = 0; q < NS; ++q) store_vec<VEC>(&cr[q * DC + lane * VEC], excl.v[q]);
             __syncwarp();
@@ -257,7 +259,7 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
     } else {
         // ------------------------------------------------------------- compute
         const int ty = warp - 1 - NLB;
-        auto pass1 = [&](int s, unsigned tile) {
+        auto pass1 = [&](int s, int a_slot, unsigned tile) {
             int c, j, d0;
             int64_t bb, t0;
             geom_of(tile, c, j, bb, d0, t0);
@@ -269,17 +271,17 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
                 const S e = Op::elem(st, i, lane, t0 + i, g);
                 agg = (k == 0) ? e : Op::combine(agg, e);
             }
-            float *dst = s_agg + s * Ly::AGG;
+            float *dst = s_agg + a_slot * Ly::AGG;
 #pragma unroll
             for (int q = 0; q < NS; ++q) store_vec<VEC>(&dst[(ty * NS + q) * DC + lane * VEC], agg.v[q]);
         };
-        auto pass2 = [&](int s, unsigned tile) {
+        auto pass2 = [&](int s, int a_slot, unsigned tile) {
             int c, j, d0;
             int64_t bb, t0;
             geom_of(tile, c, j, bb, d0, t0);
             const char *st = stages + size_t(s) * Ly::STAGE;
-            const float *agg = s_agg + s * Ly::AGG;
-            const float *cr = s_carry + s * NS * DC;
+            const float *agg = s_agg + a_slot * Ly::AGG;
+            const float *cr = s_carry + a_slot * NS * DC;
             S state;
 #pragma unroll
             for (int q = 0; q < NS; ++q) load_vec<VEC>(&cr[q * DC + lane * VEC], state.v[q]);
@@ -303,7 +305,7 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
         auto finish = [&](int k) -> bool {
             const int s = k % SG;
             if (!mbar_wait_or_error(carry + s, unsigned(k / SG) & 1u, lb)) return false;
-            pass2(s, s_tile[s]);
+            pass2(s, k % Ly::NAG, s_tile[s]);
             __syncwarp();
             if (lane == 0) mbar_arrive(empty + s);
             return true;
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
             }
             const unsigned tile = s_tile[s];
             if (tile >= g.n_tiles) break;
-            pass1(s, tile);
+            pass1(s, it % Ly::NAG, tile);
             __syncwarp();
             if (lane == 0) mbar_arrive(aggr + s);
             if (it >= LAG && !finish(it - LAG)) {

@@ -14,10 +14,10 @@ constexpr float kLog2eS = 1.4426950408889634f;
 
 // ----------------------------------------------------------- linear forward
 // Staged: 0 = a (row t), 1 = b (row t).  State (running product, h).
-template <typename Tin, int VEC_, int NCW_, int L_, int NLB_>
+template <typename Tin, int VEC_, int NCW_, int L_, int NLB_, int SG_>
 struct LinFwdT {
     static constexpr int NS = 2, VEC = VEC_, NCW = NCW_, L = L_, NARR = 2;
-    static constexpr int NLB = NLB_, STAGES = NLB_ + 2;
+    static constexpr int NLB = NLB_, STAGES = SG_;
     static constexpr bool kReverse = false;
     using S = St<NS, VEC>;
     static constexpr int elt(int) { return int(sizeof(Tin)); }
@@ -79,10 +79,10 @@ struct LinFwdT {
 // ---------------------------------------------------------- linear backward
 // Reverse time.  Staged: 0 = a (row t+1), 1 = gA (t), 2 = gBc (t),
 // 3 = A (t-1), 4 = Bc (t-1).  State (C, mu, lam).
-template <typename Tin, int NCW_, int L_, int NLB_>
+template <typename Tin, int NCW_, int L_, int NLB_, int SG_>
 struct LinBwdT {
     static constexpr int NS = 3, VEC = 4, NCW = NCW_, L = L_, NARR = 5;
-    static constexpr int NLB = NLB_, STAGES = NLB_ + 2;
+    static constexpr int NLB = NLB_, STAGES = SG_;
     static constexpr bool kReverse = true;
     using S = St<NS, VEC>;
     static constexpr int elt(int a) { return a == 0 ? int(sizeof(Tin)) : 4; }
@@ -169,10 +169,10 @@ struct LinBwdT {
 // ------------------------------------------------------- log-space forward
 // Staged: 0 = log_coeffs (row t), 1 = log_values (row t+1 of T+1).  State
 // (la, m, s) in base-2 logs, value = s * 2^m.
-template <int NCW_, int L_, int NLB_>
+template <int NCW_, int L_, int NLB_, int SG_>
 struct LogFwdT {
     static constexpr int NS = 3, VEC = 4, NCW = NCW_, L = L_, NARR = 2;
-    static constexpr int NLB = NLB_, STAGES = NLB_ + 2;
+    static constexpr int NLB = NLB_, STAGES = SG_;
     static constexpr bool kReverse = false;
     using S = St<NS, VEC>;
     static constexpr int elt(int) { return 4; }
@@ -268,8 +268,8 @@ struct LogFwdT {
     }
 };
 
-// Tiles: compute warps NCW x steps per warp L, NLB concurrent look-backs per
-// SM (ring of NLB + 2 stages).  fp32 forward stage = 2 x 16 x 128 x 4 B = 16 KB.
+// Tiles: NCW compute warps x L steps per warp, NLB concurrent look-backs per
+// SM, a ring of SG staged tiles (SG - NLB - 1 of them loading ahead).
 #ifndef MG_SF_NCW
 #define MG_SF_NCW 4
 #endif
@@ -277,7 +277,10 @@ struct LogFwdT {
 #define MG_SF_L 4
 #endif
 #ifndef MG_SF_NLB
-#define MG_SF_NLB 4
+#define MG_SF_NLB 3
+#endif
+#ifndef MG_SF_SG
+#define MG_SF_SG 10
 #endif
 #ifndef MG_SB_NCW
 #define MG_SB_NCW 4
@@ -286,7 +289,10 @@ struct LogFwdT {
 #define MG_SB_L 2
 #endif
 #ifndef MG_SB_NLB
-#define MG_SB_NLB 4
+#define MG_SB_NLB 3
+#endif
+#ifndef MG_SB_SG
+#define MG_SB_SG 8
 #endif
 #ifndef MG_SL_NCW
 #define MG_SL_NCW 4
@@ -295,13 +301,16 @@ struct LogFwdT {
 #define MG_SL_L 4
 #endif
 #ifndef MG_SL_NLB
-#define MG_SL_NLB 4
+#define MG_SL_NLB 3
 #endif
-using SFwdF32 = StreamPlan<LinFwdT<float, 4, MG_SF_NCW, MG_SF_L, MG_SF_NLB>>;
-using SFwdB16 = StreamPlan<LinFwdT<bf16_t, 8, MG_SF_NCW, MG_SF_L, MG_SF_NLB>>;
-using SBwdF32 = StreamPlan<LinBwdT<float, MG_SB_NCW, MG_SB_L, MG_SB_NLB>>;
-using SBwdB16 = StreamPlan<LinBwdT<bf16_t, MG_SB_NCW, MG_SB_L, MG_SB_NLB>>;
-using SLog = StreamPlan<LogFwdT<MG_SL_NCW, MG_SL_L, MG_SL_NLB>>;
+#ifndef MG_SL_SG
+#define MG_SL_SG 10
+#endif
+using SFwdF32 = StreamPlan<LinFwdT<float, 4, MG_SF_NCW, MG_SF_L, MG_SF_NLB, MG_SF_SG>>;
+using SFwdB16 = StreamPlan<LinFwdT<bf16_t, 8, MG_SF_NCW, MG_SF_L, MG_SF_NLB, MG_SF_SG>>;
+using SBwdF32 = StreamPlan<LinBwdT<float, MG_SB_NCW, MG_SB_L, MG_SB_NLB, MG_SB_SG>>;
+using SBwdB16 = StreamPlan<LinBwdT<bf16_t, MG_SB_NCW, MG_SB_L, MG_SB_NLB, MG_SB_SG>>;
+using SLog = StreamPlan<LogFwdT<MG_SL_NCW, MG_SL_L, MG_SL_NLB, MG_SL_SG>>;
 
 Staged staged(const void *p, int64_t rows) { return Staged{static_cast<const char *>(p), rows}; }
 
