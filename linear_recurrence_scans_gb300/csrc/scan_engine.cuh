@@ -57,28 +57,42 @@ __device__ __forceinline__ typename Op::S get_record(const Lookback &lb, size_t 
     return x;
 }
 
-// Warp 0: exclusive carry-in of chunk c for channel tile j, given the chunk
-// aggregate `cta` of this lane's channels; publishes the chunk's records.
+// First half of the look-back (one warp): publish this chunk's record as
+// early as possible.  Chunk 0 publishes its inclusive prefix (initial o cta)
+// at once; any other chunk publishes its aggregate, unless its predecessor
+// already holds a prefix (then the prefix follows shortly anyway).
 template <class Op, int TX>
-__device__ typename Op::S lookback_chan(const typename Op::Args &args, const ChanGeom &g,
+__device__ void publish_first(const typename Op::Args &args, const ChanGeom &g,
+                              const Lookback &lb, int c, int j, int64_t bb, int ld, bool lact,
+                              bool lchan, unsigned tile, unsigned long long epoch,
+                              const typename Op::S &cta)
+{
+    const int lane = threadIdx.x & 31;
+    const size_t slot = size_t(c) * g.nJ + j;
+    if (c == 0) {
+        if (lact) put_record<Op, TX>(lb, slot, 1, lane, Op::combine(Op::initial(args, g, bb, ld, lchan), cta));
+        publish(lb, slot, kStatusPrefix, epoch, tile);
+        return;
+    }
+    if (peek_status(lb, slot - g.nJ, epoch) != kStatusPrefix) {
+        if (lact) put_record<Op, TX>(lb, slot, 0, lane, cta);
+        publish(lb, slot, kStatusAggregate, epoch, tile);
+    }
+}
+
+// Second half (one warp): the exclusive carry-in of chunk c of channel tile j,
+// after publish_first; publishes the chunk's inclusive prefix (c > 0).
+template <class Op, int TX>
+__device__ typename Op::S resolve_carry(const typename Op::Args &args, const ChanGeom &g,
                                         const Lookback &lb, int c, int j, int64_t bb, int ld,
                                         bool lact, bool lchan, unsigned tile,
                                         unsigned long long epoch, const typename Op::S &cta)
 {
     using S = typename Op::S;
     const int lane = threadIdx.x & 31;
+    if (c == 0) return Op::initial(args, g, bb, ld, lchan);
     const size_t slot = size_t(c) * g.nJ + j;
     S excl = Op::identity();
-    if (c == 0) {
-        excl = Op::initial(args, g, bb, ld, lchan);
-        if (lact) put_record<Op, TX>(lb, slot, 1, lane, Op::combine(excl, cta));
-        publish(lb, slot, kStatusPrefix, epoch, tile);
-        return excl;
-    }
-    if (peek_status(lb, slot - g.nJ, epoch) != kStatusPrefix) {
-        if (lact) put_record<Op, TX>(lb, slot, 0, lane, cta);
-        publish(lb, slot, kStatusAggregate, epoch, tile);
-    }
     const int p = wait_window(lb, size_t(j), size_t(g.nJ), c, epoch, tile);
     if (p >= 0 && lact) {
         // excl = pref(p) o agg(p+1) o ... o agg(c-1), folded left to right;
@@ -97,6 +111,17 @@ __device__ typename Op::S lookback_chan(const typename Op::Args &args, const Cha
     if (lact) put_record<Op, TX>(lb, slot, 1, lane, Op::combine(excl, cta));
     publish(lb, slot, kStatusPrefix, epoch, tile);
     return excl;
+}
+
+// Both halves back to back (the one-tile-per-CTA engine).
+template <class Op, int TX>
+__device__ typename Op::S lookback_chan(const typename Op::Args &args, const ChanGeom &g,
+                                        const Lookback &lb, int c, int j, int64_t bb, int ld,
+                                        bool lact, bool lchan, unsigned tile,
+                                        unsigned long long epoch, const typename Op::S &cta)
+{
+    publish_first<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch, cta);
+    return resolve_carry<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch, cta);
 }
 
 template <class Op, int TX, int TY, int MINB>

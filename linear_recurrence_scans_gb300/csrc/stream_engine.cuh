@@ -82,18 +82,20 @@ struct StreamLayout {
     static constexpr int BAR_BYTES = 4 * SG * 8;
     static constexpr int HDR = (BAR_BYTES + SG * 4 + 127) / 128 * 128;
     static constexpr size_t AGG = size_t(NCW) * NS * DC;  // floats per aggregate slot
-    static constexpr size_t SMEM = HDR + size_t(SG) * STAGE + size_t(NAG) * (AGG + NS * DC) * 4;
+    // per aggregate slot: row aggregates, the tile aggregate, the carry-in
+    static constexpr size_t SMEM = HDR + size_t(SG) * STAGE + size_t(NAG) * (AGG + 2 * NS * DC) * 4;
     static_assert(STAGE % 16 == 0, "stage buffers must stay 16-byte aligned");
     static_assert(SMEM + 64 <= 232448, "more shared memory than one SM offers");
 };
 
-// Row i of staged array a, at this lane's channel group.
+// Row i of staged array a, at this lane's channel group (VEC channels of
+// elt(a) bytes each; a "channel" may be a whole matrix).
 template <class Op, typename E>
 __device__ __forceinline__ const E *srow(const char *st, int a, int i, int lane)
 {
     using Ly = StreamLayout<Op>;
-    return reinterpret_cast<const E *>(st + Ly::arr_off(a) + size_t(i) * Ly::DC * Op::elt(a)) +
-           lane * Op::VEC;
+    return reinterpret_cast<const E *>(
+        st + Ly::arr_off(a) + (size_t(i) * Ly::DC + size_t(lane) * Op::VEC) * Op::elt(a));
 }
 
 // Wait for phase `parity` of `bar`, or until iteration `it` is past the end
@@ -137,7 +139,8 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
     unsigned *const s_tile = reinterpret_cast<unsigned *>(smem + Ly::BAR_BYTES);
     char *const stages = smem + Ly::HDR;
     float *const s_agg = reinterpret_cast<float *>(stages + size_t(SG) * Ly::STAGE);
-    float *const s_carry = s_agg + Ly::NAG * Ly::AGG;
+    float *const s_carry = s_agg + Ly::NAG * Ly::AGG;   // [NAG][NS][DC]
+    float *const s_cta = s_carry + Ly::NAG * NS * DC;    // [NAG][NS][DC]
     __shared__ unsigned long long s_epoch;
     __shared__ int s_end;  // first iteration index without a tile
 
@@ -145,7 +148,7 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
         for (int s = 0; s < SG; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, NCW);
-            mbar_init(aggr + s, NCW);
+            mbar_init(aggr + s, 1);
             mbar_init(carry + s, 1);
         }
         s_epoch = ld_relaxed_u64(&lb.ctl->epoch);
@@ -238,17 +241,11 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
             const int ld = d0 + lane * VEC;
             const bool lchan = ld < g.D;
             const int a_slot = it % Ly::NAG;
-            const float *agg = s_agg + a_slot * Ly::AGG;
             S cta;
 #pragma unroll
-            for (int k = 0; k < NCW; ++k) {
-                const int y = Op::kReverse ? NCW - 1 - k : k;
-                S x;
-#pragma unroll
-                for (int q = 0; q < NS; ++q) load_vec<VEC>(&agg[(y * NS + q) * DC + lane * VEC], x.v[q]);
-                cta = (k == 0) ? x : Op::combine(cta, x);
-            }
-            const S excl = lookback_chan<Op, 32>(args, g, lb, c, j, bb, ld, true, lchan, tile,
+            for (int q = 0; q < NS; ++q)
+                load_vec<VEC>(&s_cta[(a_slot * NS + q) * DC + lane * VEC], cta.v[q]);
+            const S excl = resolve_carry<Op, 32>(args, g, lb, c, j, bb, ld, true, lchan, tile,
                                                  epoch, cta);
             float *cr = s_carry + a_slot * NS * DC;
 #pragma unroll
@@ -320,9 +317,34 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
             }
             const unsigned tile = s_tile[s];
             if (tile >= g.n_tiles) break;
-            pass1(s, it % Ly::NAG, tile);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(aggr + s);
+            const int a_slot = it % Ly::NAG;
+            pass1(s, a_slot, tile);
+            // all row aggregates written -> compute warp 0 folds them into the
+            // tile aggregate and publishes it at once (the look-back warps only
+            // resolve carries)
+            asm volatile("bar.sync 1, %0;" : : "r"(NCW * 32) : "memory");
+            if (ty == 0) {
+                int c, j, d0;
+                int64_t bb, t0;
+                geom_of(tile, c, j, bb, d0, t0);
+                const int ld = d0 + lane * VEC;
+                const float *agg = s_agg + a_slot * Ly::AGG;
+                S cta;
+#pragma unroll
+                for (int k = 0; k < NCW; ++k) {
+                    const int y = Op::kReverse ? NCW - 1 - k : k;
+                    S x;
+#pragma unroll
+                    for (int q = 0; q < NS; ++q) load_vec<VEC>(&agg[(y * NS + q) * DC + lane * VEC], x.v[q]);
+                    cta = (k == 0) ? x : Op::combine(cta, x);
+                }
+#pragma unroll
+                for (int q = 0; q < NS; ++q)
+                    store_vec<VEC>(&s_cta[(a_slot * NS + q) * DC + lane * VEC], cta.v[q]);
+                publish_first<Op, 32>(args, g, lb, c, j, bb, ld, true, ld < g.D, tile, epoch, cta);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(aggr + s);
+            }
             if (it >= LAG && !finish(it - LAG)) {
                 ok = false;
                 break;
