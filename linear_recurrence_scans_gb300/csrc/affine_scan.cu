@@ -349,7 +349,7 @@ struct AffPick {
     static constexpr int ROW = 32 * 4 * (BWD ? 3 * K * K + 2 * K * V : K * K + K * V);
     static constexpr size_t smem(int ncw, int l, int nlb, int sg)
     {
-        return 256 + size_t(sg) * ncw * l * ROW + size_t(nlb + 1) * size_t(ncw + 2) * NS * 32 * 4;
+        return 256 + size_t(sg) * (size_t(ncw) * l * ROW + size_t(ncw + 2) * NS * 32 * 4);
     }
     static constexpr int C[8][4] = {{4, 2, 3, 6}, {4, 2, 2, 5}, {4, 1, 2, 5}, {2, 2, 2, 5},
                                     {2, 2, 1, 4}, {2, 1, 1, 4}, {1, 2, 1, 3}, {1, 1, 1, 3}};

@@ -2,6 +2,7 @@
 // launch), workspace bookkeeping and dispatch to the launchers.
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <initializer_list>
 
@@ -76,6 +77,21 @@ mg_status check_ws(const char *fn, const void *ws, size_t ws_bytes, size_t need)
 }
 
 bool valid_kv(int x) { return x == 1 || x == 2 || x == 4 || x == 8 || x == 16; }
+
+// Default launch options.  MGSCAN_ENGINE=chunked selects the one-tile-per-CTA
+// engine for every op that has both shapes (for comparisons and tuning);
+// unset or any other value selects the persistent streaming engine where the
+// sizes allow it.
+LaunchOpts default_opts()
+{
+    static const LaunchOpts o = [] {
+        LaunchOpts x;
+        const char *e = getenv("MGSCAN_ENGINE");
+        if (e != nullptr && strcmp(e, "chunked") == 0) x.engine = LaunchOpts::kChunked;
+        return x;
+    }();
+    return o;
+}
 
 #define MG_TRY(expr)                      \
     do {                                  \
@@ -178,7 +194,7 @@ mg_status mg_linear_scan_fwd(const void *a, const void *b, mg_dtype in_dt, float
                            {A, n * 4, "A", true},
                            {Bc, n * 4, "Bc", true},
                            {ws, ws_bytes, "workspace", true}}));
-    return launch_linear_fwd(a, b, in_dt, A, Bc, B, T, D, ws, ws_bytes, stream, LaunchOpts{});
+    return launch_linear_fwd(a, b, in_dt, A, Bc, B, T, D, ws, ws_bytes, stream, default_opts());
 }
 
 mg_status mg_linear_scan_bwd(const void *a, mg_dtype a_dt, const float *A, const float *Bc,
@@ -202,7 +218,7 @@ mg_status mg_linear_scan_bwd(const void *a, mg_dtype a_dt, const float *A, const
                            {db, n * 4, "db", true},
                            {ws, ws_bytes, "workspace", true}}));
     return launch_linear_bwd(a, a_dt, A, Bc, gA, gBc, da, db, B, T, D, ws, ws_bytes, stream,
-                             LaunchOpts{});
+                             default_opts());
 }
 
 mg_status mg_log_scan_fwd(const float *log_coeffs, const float *log_values, float *h, int64_t B,
@@ -219,7 +235,7 @@ mg_status mg_log_scan_fwd(const float *log_coeffs, const float *log_values, floa
                            {log_values, nv * 4, "log_values", false},
                            {h, n * 4, "h", true},
                            {ws, ws_bytes, "workspace", true}}));
-    return launch_log_fwd(log_coeffs, log_values, h, B, T, D, ws, ws_bytes, stream, LaunchOpts{});
+    return launch_log_fwd(log_coeffs, log_values, h, B, T, D, ws, ws_bytes, stream, default_opts());
 }
 
 mg_status mg_affine_scan_fwd(const float *A, const float *Bm, float *Abar, float *Bbar, int64_t B,
@@ -239,7 +255,7 @@ mg_status mg_affine_scan_fwd(const float *A, const float *Bm, float *Abar, float
                            {Abar, s * k * k * 4, "Abar", true},
                            {Bbar, s * k * v * 4, "Bbar", true},
                            {ws, ws_bytes, "workspace", true}}));
-    return launch_affine_fwd(A, Bm, Abar, Bbar, B, T, n, k, v, ws, ws_bytes, stream, LaunchOpts{});
+    return launch_affine_fwd(A, Bm, Abar, Bbar, B, T, n, k, v, ws, ws_bytes, stream, default_opts());
 }
 
 mg_status mg_affine_scan_bwd(const float *A, const float *Abar, const float *Bbar,
@@ -264,7 +280,7 @@ mg_status mg_affine_scan_bwd(const float *A, const float *Abar, const float *Bba
                            {dB, s * k * v * 4, "dB", true},
                            {ws, ws_bytes, "workspace", true}}));
     return launch_affine_bwd(A, Abar, Bbar, gAbar, gBbar, dA, dB, B, T, n, k, v, ws, ws_bytes,
-                             stream, LaunchOpts{});
+                             stream, default_opts());
 }
 
 mg_status mg_testing_linear_scan_fwd_stall(const float *a, const float *b, float *A, float *Bc,
@@ -285,7 +301,7 @@ mg_status mg_testing_linear_scan_fwd_stall(const float *a, const float *b, float
                            {ws, ws_bytes, "workspace", true}}));
     if (wait_limit_ns == 0 || wait_limit_ns > 10000000000ull)
         return fail(MG_ERR_INVALID_ARG, "%s: wait_limit_ns must be in (0, 1e10]", fn);
-    LaunchOpts o;
+    LaunchOpts o = default_opts();
     o.wait_limit_ns = wait_limit_ns;
     o.stall_tile = stall_tile;
     return launch_linear_fwd(a, b, MG_F32, A, Bc, B, T, D, ws, ws_bytes, stream, o);

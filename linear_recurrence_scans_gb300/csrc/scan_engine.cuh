@@ -59,9 +59,9 @@ __device__ __forceinline__ typename Op::S get_record(const Lookback &lb, size_t 
 
 // First half of the look-back (one warp): publish this chunk's record as
 // early as possible.  Chunk 0 publishes its inclusive prefix (initial o cta)
-// at once; any other chunk publishes its aggregate, unless its predecessor
-// already holds a prefix (then the prefix follows shortly anyway).
-template <class Op, int TX>
+// at once; any other chunk publishes its aggregate, unless `peek` is set and
+// its predecessor already holds a prefix (then the prefix follows shortly).
+template <class Op, int TX, bool PEEK = true>
 __device__ void publish_first(const typename Op::Args &args, const ChanGeom &g,
                               const Lookback &lb, int c, int j, int64_t bb, int ld, bool lact,
                               bool lchan, unsigned tile, unsigned long long epoch,
@@ -74,7 +74,7 @@ __device__ void publish_first(const typename Op::Args &args, const ChanGeom &g,
         publish(lb, slot, kStatusPrefix, epoch, tile);
         return;
     }
-    if (peek_status(lb, slot - g.nJ, epoch) != kStatusPrefix) {
+    if (!PEEK || peek_status(lb, slot - g.nJ, epoch) != kStatusPrefix) {
         if (lact) put_record<Op, TX>(lb, slot, 0, lane, cta);
         publish(lb, slot, kStatusAggregate, epoch, tile);
     }

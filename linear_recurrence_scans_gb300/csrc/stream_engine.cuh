@@ -7,10 +7,14 @@
 //   warp 0        producer: takes tickets and streams each tile's input rows
 //                 into a ring of STAGES shared-memory buffers with 1D TMA bulk
 //                 copies (one mbarrier per stage counts the bytes);
-//   warps 1..NLB  look-back: warp w takes the CTA's tiles i = w-1 (mod NLB);
-//                 it folds the compute warps' row aggregates into the tile
-//                 aggregate, runs the decoupled look-back (lookback.cuh) and
-//                 hands the tile's carry-in back through shared memory;
+//   publishers    (NPUB warps, tiles round-robin) fold the compute warps' row
+//                 aggregates into the tile aggregate and publish it at once
+//                 (the first half of the decoupled look-back, lookback.cuh),
+//                 so successors in other CTAs never wait on this CTA's
+//                 look-back warps;
+//   look-back     (NLB warps, tiles round-robin) resolve each tile's carry-in
+//                 from its predecessors' records and hand it back through
+//                 shared memory;
 //   the rest      compute: each owns L consecutive steps of a tile for 32*VEC
 //                 channels (one 16-byte vector per lane per row).  Pass 1 folds
 //                 the steps into a row aggregate; pass 2 re-runs them from the
@@ -22,10 +26,11 @@
 // are read from HBM once (staged), outputs written once (vector stores).
 //
 // Synchronisation per stage s (phase parity = use count & 1):
-//   full[s]   producer -> compute, look-back    (tx bytes of the copies)
-//   aggr[s]   compute  -> look-back             (row aggregates written)
-//   carry[s]  look-back -> compute              (carry-in written)
-//   empty[s]  compute  -> producer              (stage free again)
+//   full[s]   producer  -> compute             (tx bytes of the copies)
+//   aggr[s]   compute   -> publisher           (row aggregates written)
+//   pub[s]    publisher -> look-back           (tile aggregate published)
+//   carry[s]  look-back -> compute             (carry-in written)
+//   empty[s]  compute   -> producer            (stage free again)
 // Every wait is bounded (time and the launch's error word); a role that gives
 // up leaves its loop, the producer drains its copies, and the launch ends
 // with the error recorded for mg_workspace_status.
@@ -78,8 +83,10 @@ struct StreamLayout {
     static constexpr int arr_bytes(int a) { return TC * DC * Op::elt(a); }
     static constexpr int arr_off(int a) { return a == 0 ? 0 : arr_off(a - 1) + arr_bytes(a - 1); }
     static constexpr int STAGE = arr_off(NARR);
-    static constexpr int NAG = Op::NLB + 1;  // tiles between pass 1 and pass 2
-    static constexpr int BAR_BYTES = 4 * SG * 8;
+    // Aggregate buffers live per stage: a stage is refilled (and its
+    // aggregates rewritten) only after every compute warp released it.
+    static constexpr int NAG = SG;
+    static constexpr int BAR_BYTES = 5 * SG * 8;
     static constexpr int HDR = (BAR_BYTES + SG * 4 + 127) / 128 * 128;
     static constexpr size_t AGG = size_t(NCW) * NS * DC;  // floats per aggregate slot
     // per aggregate slot: row aggregates, the tile aggregate, the carry-in
@@ -120,8 +127,10 @@ __device__ __forceinline__ int mbar_wait_or_end(unsigned long long *bar, unsigne
     }
 }
 
+constexpr int kNPub = 2;  // publisher warps per CTA
+
 template <class Op>
-__global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
+__global__ void __launch_bounds__((Op::NCW + Op::NLB + 1 + kNPub) * 32, 1)
     stream_scan_kernel(const typename Op::Args args, const ChanGeom g, const Lookback lb)
 {
     using S = typename Op::S;
@@ -136,9 +145,10 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
     unsigned long long *const empty = full + SG;
     unsigned long long *const aggr = empty + SG;
     unsigned long long *const carry = aggr + SG;
+    unsigned long long *const pub = carry + SG;
     unsigned *const s_tile = reinterpret_cast<unsigned *>(smem + Ly::BAR_BYTES);
     char *const stages = smem + Ly::HDR;
-    float *const s_agg = reinterpret_cast<float *>(stages + size_t(SG) * Ly::STAGE);
+    float *const s_agg = reinterpret_cast<float *>(stages + size_t(SG) * Ly::STAGE);  // [SG][NCW][NS][DC]
     float *const s_carry = s_agg + Ly::NAG * Ly::AGG;   // [NAG][NS][DC]
     float *const s_cta = s_carry + Ly::NAG * NS * DC;    // [NAG][NS][DC]
     __shared__ unsigned long long s_epoch;
@@ -148,8 +158,9 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
         for (int s = 0; s < SG; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, NCW);
-            mbar_init(aggr + s, 1);
+            mbar_init(aggr + s, NCW);
             mbar_init(carry + s, 1);
+            mbar_init(pub + s, 1);
         }
         s_epoch = ld_relaxed_u64(&lb.ctl->epoch);
         s_end = 0x7fffffff;
@@ -228,9 +239,9 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
         // the CTA's shared memory is released (normally already done).
         for (int k = (it > SG ? it - SG : 0); k < it; ++k)
             mbar_wait_bounded(full + (k % SG), unsigned(k / SG) & 1u, lb.wait_limit_ns);
-    } else if (warp <= NLB) {
-        // ----------------------------------------------------------- look-back
-        for (int it = warp - 1;; it += NLB) {
+    } else if (warp <= kNPub) {
+        // ----------------------------------------------------------- publisher
+        for (int it = warp - 1;; it += kNPub) {
             const int s = it % SG;
             if (mbar_wait_or_end(aggr + s, unsigned(it / SG) & 1u, lb, end, it) != 1) break;
             const unsigned tile = s_tile[s];
@@ -239,8 +250,37 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
             int64_t bb, t0;
             geom_of(tile, c, j, bb, d0, t0);
             const int ld = d0 + lane * VEC;
+            const int a_slot = s;
+            const float *agg = s_agg + a_slot * Ly::AGG;
+            S cta;
+#pragma unroll
+            for (int k = 0; k < NCW; ++k) {
+                const int y = Op::kReverse ? NCW - 1 - k : k;
+                S x;
+#pragma unroll
+                for (int q = 0; q < NS; ++q) load_vec<VEC>(&agg[(y * NS + q) * DC + lane * VEC], x.v[q]);
+                cta = (k == 0) ? x : Op::combine(cta, x);
+            }
+#pragma unroll
+            for (int q = 0; q < NS; ++q)
+                store_vec<VEC>(&s_cta[(a_slot * NS + q) * DC + lane * VEC], cta.v[q]);
+            publish_first<Op, 32, false>(args, g, lb, c, j, bb, ld, true, ld < g.D, tile, epoch, cta);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pub + s);
+        }
+    } else if (warp <= kNPub + NLB) {
+        // ----------------------------------------------------------- look-back
+        for (int it = warp - 1 - kNPub;; it += NLB) {
+            const int s = it % SG;
+            if (mbar_wait_or_end(pub + s, unsigned(it / SG) & 1u, lb, end, it) != 1) break;
+            const unsigned tile = s_tile[s];
+            if (tile >= g.n_tiles) break;
+            int c, j, d0;
+            int64_t bb, t0;
+            geom_of(tile, c, j, bb, d0, t0);
+            const int ld = d0 + lane * VEC;
             const bool lchan = ld < g.D;
-            const int a_slot = it % Ly::NAG;
+            const int a_slot = s;
             S cta;
 #pragma unroll
             for (int q = 0; q < NS; ++q)
@@ -255,7 +295,7 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
         }
     } else {
         // ------------------------------------------------------------- compute
-        const int ty = warp - 1 - NLB;
+        const int ty = warp - 1 - kNPub - NLB;
         auto pass1 = [&](int s, int a_slot, unsigned tile) {
             int c, j, d0;
             int64_t bb, t0;
@@ -302,7 +342,7 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
         auto finish = [&](int k) -> bool {
             const int s = k % SG;
             if (!mbar_wait_or_error(carry + s, unsigned(k / SG) & 1u, lb)) return false;
-            pass2(s, k % Ly::NAG, s_tile[s]);
+            pass2(s, s, s_tile[s]);
             __syncwarp();
             if (lane == 0) mbar_arrive(empty + s);
             return true;
@@ -317,34 +357,9 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1) * 32, 1)
             }
             const unsigned tile = s_tile[s];
             if (tile >= g.n_tiles) break;
-            const int a_slot = it % Ly::NAG;
-            pass1(s, a_slot, tile);
-            // all row aggregates written -> compute warp 0 folds them into the
-            // tile aggregate and publishes it at once (the look-back warps only
-            // resolve carries)
-            asm volatile("bar.sync 1, %0;" : : "r"(NCW * 32) : "memory");
-            if (ty == 0) {
-                int c, j, d0;
-                int64_t bb, t0;
-                geom_of(tile, c, j, bb, d0, t0);
-                const int ld = d0 + lane * VEC;
-                const float *agg = s_agg + a_slot * Ly::AGG;
-                S cta;
-#pragma unroll
-                for (int k = 0; k < NCW; ++k) {
-                    const int y = Op::kReverse ? NCW - 1 - k : k;
-                    S x;
-#pragma unroll
-                    for (int q = 0; q < NS; ++q) load_vec<VEC>(&agg[(y * NS + q) * DC + lane * VEC], x.v[q]);
-                    cta = (k == 0) ? x : Op::combine(cta, x);
-                }
-#pragma unroll
-                for (int q = 0; q < NS; ++q)
-                    store_vec<VEC>(&s_cta[(a_slot * NS + q) * DC + lane * VEC], cta.v[q]);
-                publish_first<Op, 32>(args, g, lb, c, j, bb, ld, true, ld < g.D, tile, epoch, cta);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(aggr + s);
-            }
+            pass1(s, s, tile);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(aggr + s);
             if (it >= LAG && !finish(it - LAG)) {
                 ok = false;
                 break;
@@ -410,7 +425,7 @@ struct StreamPlan {
         const ChanGeom g = geom(B, T, D);
         const Lookback lb = make_lookback(ws, nt, o);
         const unsigned grid = unsigned(nt < size_t(n_sm) ? nt : size_t(n_sm));
-        stream_scan_kernel<Op><<<grid, (Op::NCW + Op::NLB + 1) * 32, Ly::SMEM, s>>>(args, g, lb);
+        stream_scan_kernel<Op><<<grid, (Op::NCW + Op::NLB + 1 + kNPub) * 32, Ly::SMEM, s>>>(args, g, lb);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return fail(MG_ERR_LAUNCH, "%s: launch failed: %s", name, cudaGetErrorString(e));

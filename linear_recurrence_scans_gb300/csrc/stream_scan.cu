@@ -269,7 +269,8 @@ struct LogFwdT {
 };
 
 // Tiles: NCW compute warps x L steps per warp, NLB concurrent look-backs per
-// SM, a ring of SG staged tiles (SG - NLB - 1 of them loading ahead).
+// SM, a ring of SG staged tiles (SG - NLB - 1 of them loading ahead), sized
+// to fit one SM's shared memory.
 #ifndef MG_SF_NCW
 #define MG_SF_NCW 4
 #endif
@@ -280,7 +281,10 @@ struct LogFwdT {
 #define MG_SF_NLB 3
 #endif
 #ifndef MG_SF_SG
-#define MG_SF_SG 10
+#define MG_SF_SG 9
+#endif
+#ifndef MG_SF16_SG
+#define MG_SF16_SG 7
 #endif
 #ifndef MG_SB_NCW
 #define MG_SB_NCW 4
@@ -292,7 +296,7 @@ struct LogFwdT {
 #define MG_SB_NLB 3
 #endif
 #ifndef MG_SB_SG
-#define MG_SB_SG 8
+#define MG_SB_SG 7
 #endif
 #ifndef MG_SL_NCW
 #define MG_SL_NCW 4
@@ -304,10 +308,10 @@ struct LogFwdT {
 #define MG_SL_NLB 3
 #endif
 #ifndef MG_SL_SG
-#define MG_SL_SG 10
+#define MG_SL_SG 8
 #endif
 using SFwdF32 = StreamPlan<LinFwdT<float, 4, MG_SF_NCW, MG_SF_L, MG_SF_NLB, MG_SF_SG>>;
-using SFwdB16 = StreamPlan<LinFwdT<bf16_t, 8, MG_SF_NCW, MG_SF_L, MG_SF_NLB, MG_SF_SG>>;
+using SFwdB16 = StreamPlan<LinFwdT<bf16_t, 8, MG_SF_NCW, MG_SF_L, MG_SF_NLB, MG_SF16_SG>>;
 using SBwdF32 = StreamPlan<LinBwdT<float, MG_SB_NCW, MG_SB_L, MG_SB_NLB, MG_SB_SG>>;
 using SBwdB16 = StreamPlan<LinBwdT<bf16_t, MG_SB_NCW, MG_SB_L, MG_SB_NLB, MG_SB_SG>>;
 using SLog = StreamPlan<LogFwdT<MG_SL_NCW, MG_SL_L, MG_SL_NLB, MG_SL_SG>>;
