@@ -389,10 +389,10 @@ struct LogFwd {
 // bf16: 8 channels (16 B).  A D that is not a multiple of the vector width
 // takes the 1-channel variant.  Each can be overridden at build time.
 #ifndef MG_LINF_TX
-#define MG_LINF_TX 32
+#define MG_LINF_TX 16
 #endif
 #ifndef MG_LINF_TY
-#define MG_LINF_TY 8
+#define MG_LINF_TY 16
 #endif
 #ifndef MG_LINF_L
 #define MG_LINF_L 8
@@ -413,13 +413,13 @@ struct LogFwd {
 #define MG_LINF16_MB 1
 #endif
 #ifndef MG_LINB_TX
-#define MG_LINB_TX 32
+#define MG_LINB_TX 8
 #endif
 #ifndef MG_LINB_TY
-#define MG_LINB_TY 8
+#define MG_LINB_TY 16
 #endif
 #ifndef MG_LINB_L
-#define MG_LINB_L 4
+#define MG_LINB_L 8
 #endif
 #ifndef MG_LINB_MB
 #define MG_LINB_MB 1
@@ -431,7 +431,7 @@ struct LogFwd {
 #define MG_LOG_TY 8
 #endif
 #ifndef MG_LOG_L
-#define MG_LOG_L 8
+#define MG_LOG_L 4
 #endif
 #ifndef MG_LOG_MB
 #define MG_LOG_MB 1

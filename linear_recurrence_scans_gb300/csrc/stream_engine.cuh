@@ -42,6 +42,7 @@ namespace mg {
 namespace {
 
 constexpr unsigned kSentinelTile = 0xffffffffu;
+constexpr int kTicketBatch = 4;  // tiles per ticket grab
 
 // A staged input: rows of `elt`-byte elements; tile row i of a tile starting
 // at step t0 copies source row t0 + i + shift of a tensor with `rows` rows per
@@ -181,18 +182,31 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1 + kNPub) * 32, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // Tickets come in batches of kTicketBatch consecutive tiles; the next
+        // batch's atomic is issued as soon as a batch starts, so its latency
+        // stays off the load path.  Consecutive tickets are different channel
+        // tiles of one chunk (or later chunks), so a CTA never waits on its
+        // own later tiles.
         int it = 0;
+        unsigned next_batch = 0, batch = 0;
+        int left = 0;
+        if (lane == 0) next_batch = atomicAdd(&lb.ctl->ticket, unsigned(kTicketBatch));
         for (;; ++it) {
             const int s = it % SG;
             const unsigned u = unsigned(it / SG);
             if (u > 0 && !mbar_wait_or_error(empty + s, (u - 1) & 1u, lb)) break;
-            unsigned tile = 0;
-            if (lane == 0) tile = atomicAdd(&lb.ctl->ticket, 1u);
-            tile = __shfl_sync(0xffffffffu, tile, 0);
+            if (left == 0) {
+                batch = __shfl_sync(0xffffffffu, next_batch, 0);
+                left = kTicketBatch;
+                if (lane == 0 && batch < g.n_tiles)
+                    next_batch = atomicAdd(&lb.ctl->ticket, unsigned(kTicketBatch));
+            }
+            const unsigned tile = batch + unsigned(kTicketBatch - left);
+            --left;
             if (tile >= g.n_tiles) {
                 if (lane == 0) {
-                    if (tile >= g.n_tiles + gridDim.x) atomicOr(&lb.ctl->error, kErrBadTicket);
-                    s_tile[s] = kSentinelTile;
+                    if (batch >= g.n_tiles + 2u * kTicketBatch * gridDim.x)
+                        atomicOr(&lb.ctl->error, kErrBadTicket);                    s_tile[s] = kSentinelTile;
                     *end = it;
                     mbar_arrive(full + s);
                 }
@@ -401,7 +415,7 @@ struct StreamPlan {
                             const char *name)
     {
         const size_t nt = n_tiles(B, T, D);
-        if (nt >= (size_t(1) << 31) - 4096 || B * ((D + DC - 1) / DC) >= (int64_t(1) << 31))
+        if (nt >= (size_t(1) << 30) || B * ((D + DC - 1) / DC) >= (int64_t(1) << 31))
             return fail(MG_ERR_UNSUPPORTED, "%s: %zu tiles exceed the 2^31 ticket range", name, nt);
         const size_t need = ws_bytes(B, T, D);
         if (wsb < need)
