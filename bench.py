@@ -389,14 +389,15 @@ def _oracle_step_on_sample(ncols: int, seed: int = 0):
     return a.size, time.perf_counter() - t0
 
 
-def cpu_baseline(target_s: float = 12.0):
+def cpu_baseline(target_s: float = 10.0):
     """The oracle as it stands (single-threaded C, float64) on a bounded
-    sample: whole batch rows of the workload (all T, all D of one b) repeated
-    until about `target_s` seconds of CPU work."""
+    sample: whole batch rows of the workload (all T, all D of one b), one
+    after another (different seeds), until about `target_s` seconds of CPU
+    work."""
     import oracle
     oracle.build()
     els, secs, reps = 0, 0.0, 0
-    while secs < target_s and reps < 8:
+    while secs < target_s and reps < 400:
         e, s = _oracle_step_on_sample(D, seed=reps)
         els += e
         secs += s

@@ -1055,7 +1055,7 @@ mg_status fwd_kv(const float *A, const float *Bm, float *Abar, float *Bbar, int6
 {
     const char *nm = "mg_affine_scan_fwd";
     if constexpr (K <= 4) {
-        if (o.engine != LaunchOpts::kChunked && aff_stream_ok<K, V>(n))
+        if (o.engine == LaunchOpts::kStream && aff_stream_ok<K, V>(n))
             return StreamPlan<AffFwdT<K, V>>::launch(
                 {{Staged{reinterpret_cast<const char *>(A), T}, Staged{reinterpret_cast<const char *>(Bm), T}},
                  Abar, Bbar},
@@ -1079,7 +1079,7 @@ mg_status bwd_kv(const float *A, const float *Abar, const float *Bbar, const flo
     const char *nm = "mg_affine_scan_bwd";
     if constexpr (K <= 4) {
         auto stg = [&](const float *x) { return Staged{reinterpret_cast<const char *>(x), T}; };
-        if (o.engine != LaunchOpts::kChunked && aff_stream_ok<K, V>(n))
+        if (o.engine == LaunchOpts::kStream && aff_stream_ok<K, V>(n))
             return StreamPlan<AffBwdT<K, V>>::launch(
                 {{stg(A), stg(gAbar), stg(gBbar), stg(Abar), stg(Bbar)}, dA, dB}, B, T, n, ws, wsb,
                 s, o, nm);

@@ -484,7 +484,9 @@ mg_status launch_linear_fwd(const void *a, const void *b, mg_dtype dt, float *A,
                             const LaunchOpts &o)
 {
     const char *nm = "mg_linear_scan_fwd";
-    if (o.engine != LaunchOpts::kChunked && stream_linear_ok(dt, D))
+    const bool stream_fwd = o.engine == LaunchOpts::kStream ||
+                            (o.engine == LaunchOpts::kAuto && dt == MG_BF16);
+    if (stream_fwd && stream_linear_ok(dt, D))
         return stream_linear_fwd(a, b, dt, A, Bc, B, T, D, ws, wsb, s, o);
     if (dt == MG_F32) {
         using F = const float *;
@@ -503,7 +505,7 @@ mg_status launch_linear_bwd(const void *a, mg_dtype dt, const float *A, const fl
                             const LaunchOpts &o)
 {
     const char *nm = "mg_linear_scan_bwd";
-    if (o.engine != LaunchOpts::kChunked && stream_linear_ok(dt, D))
+    if (o.engine == LaunchOpts::kStream && stream_linear_ok(dt, D))
         return stream_linear_bwd(a, dt, A, Bc, gA, gBc, da, db, B, T, D, ws, wsb, s, o);
     if (dt == MG_F32) {
         using F = const float *;
@@ -521,7 +523,7 @@ mg_status launch_log_fwd(const float *lc, const float *lv, float *h, int64_t B, 
                          int64_t D, void *ws, size_t wsb, cudaStream_t s, const LaunchOpts &o)
 {
     const char *nm = "mg_log_scan_fwd";
-    if (o.engine != LaunchOpts::kChunked && stream_log_ok(D))
+    if (o.engine == LaunchOpts::kStream && stream_log_ok(D))
         return stream_log_fwd(lc, lv, h, B, T, D, ws, wsb, s, o);
     if (D % 4 == 0) return LogF32::launch({lc, lv, h}, B, T, D, ws, wsb, s, o, nm);
     return LogF32s::launch({lc, lv, h}, B, T, D, ws, wsb, s, o, nm);

@@ -21,10 +21,11 @@ struct LaunchOpts {
     unsigned long long wait_limit_ns = 2000000000ull;  // 2 s of %globaltimer
     unsigned int max_polls = 1u << 24;
     long long stall_tile = -1;                         // testing only
-    // Which kernel shape serves the channel-wise ops: the persistent
-    // warp-specialised one where D allows it (default), or the one-tile-per-CTA
-    // chunk engine.
-    enum Engine { kAuto = 0, kChunked = 1 } engine = kAuto;
+    // Which kernel shape serves an op that has two: kAuto picks the one
+    // measured faster for it (the persistent streaming engine for the bf16
+    // linear forward, the one-tile-per-CTA chunk engine otherwise); kChunked
+    // and kStream force one (the streaming engine only where D allows it).
+    enum Engine { kAuto = 0, kChunked = 1, kStream = 2 } engine = kAuto;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -78,16 +78,16 @@ mg_status check_ws(const char *fn, const void *ws, size_t ws_bytes, size_t need)
 
 bool valid_kv(int x) { return x == 1 || x == 2 || x == 4 || x == 8 || x == 16; }
 
-// Default launch options.  MGSCAN_ENGINE=chunked selects the one-tile-per-CTA
-// engine for every op that has both shapes (for comparisons and tuning);
-// unset or any other value selects the persistent streaming engine where the
-// sizes allow it.
+// Default launch options.  MGSCAN_ENGINE=chunked or =stream forces one
+// kernel shape for every op that has both (for comparisons and tuning);
+// otherwise each op takes the shape measured faster for it.
 LaunchOpts default_opts()
 {
     static const LaunchOpts o = [] {
         LaunchOpts x;
         const char *e = getenv("MGSCAN_ENGINE");
         if (e != nullptr && strcmp(e, "chunked") == 0) x.engine = LaunchOpts::kChunked;
+        if (e != nullptr && strcmp(e, "stream") == 0) x.engine = LaunchOpts::kStream;
         return x;
     }();
     return o;

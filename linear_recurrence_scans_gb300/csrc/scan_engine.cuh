@@ -80,18 +80,17 @@ __device__ void publish_first(const typename Op::Args &args, const ChanGeom &g,
     }
 }
 
-// Second half (one warp): the exclusive carry-in of chunk c of channel tile j,
-// after publish_first; publishes the chunk's inclusive prefix (c > 0).
+// Second half (one warp): the exclusive carry-in of chunk c of channel tile j
+// from its predecessors' records (after publish_first).
 template <class Op, int TX>
-__device__ typename Op::S resolve_carry(const typename Op::Args &args, const ChanGeom &g,
-                                        const Lookback &lb, int c, int j, int64_t bb, int ld,
-                                        bool lact, bool lchan, unsigned tile,
-                                        unsigned long long epoch, const typename Op::S &cta)
+__device__ typename Op::S find_carry(const typename Op::Args &args, const ChanGeom &g,
+                                     const Lookback &lb, int c, int j, int64_t bb, int ld,
+                                     bool lact, bool lchan, unsigned tile,
+                                     unsigned long long epoch)
 {
     using S = typename Op::S;
     const int lane = threadIdx.x & 31;
     if (c == 0) return Op::initial(args, g, bb, ld, lchan);
-    const size_t slot = size_t(c) * g.nJ + j;
     S excl = Op::identity();
     const int p = wait_window(lb, size_t(j), size_t(g.nJ), c, epoch, tile);
     if (p >= 0 && lact) {
@@ -108,20 +107,21 @@ __device__ typename Op::S resolve_carry(const typename Op::Args &args, const Cha
         }
         for (; q < c; ++q) excl = Op::combine(excl, get_record<Op, TX>(lb, size_t(q) * g.nJ + j, 0, lane));
     }
-    if (lact) put_record<Op, TX>(lb, slot, 1, lane, Op::combine(excl, cta));
-    publish(lb, slot, kStatusPrefix, epoch, tile);
     return excl;
 }
 
-// Both halves back to back (the one-tile-per-CTA engine).
+// Publish chunk c's inclusive prefix excl o cta (chunk 0 did at once).  Kept
+// apart from find_carry so that the carry can be handed to the consumers
+// before this release store's fence.
 template <class Op, int TX>
-__device__ typename Op::S lookback_chan(const typename Op::Args &args, const ChanGeom &g,
-                                        const Lookback &lb, int c, int j, int64_t bb, int ld,
-                                        bool lact, bool lchan, unsigned tile,
-                                        unsigned long long epoch, const typename Op::S &cta)
+__device__ void publish_prefix(const ChanGeom &g, const Lookback &lb, int c, int j, bool lact,
+                               unsigned tile, unsigned long long epoch,
+                               const typename Op::S &excl, const typename Op::S &cta)
 {
-    publish_first<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch, cta);
-    return resolve_carry<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch, cta);
+    if (c == 0) return;
+    const size_t slot = size_t(c) * g.nJ + j;
+    if (lact) put_record<Op, TX>(lb, slot, 1, threadIdx.x & 31, Op::combine(excl, cta));
+    publish(lb, slot, kStatusPrefix, epoch, tile);
 }
 
 template <class Op, int TX, int TY, int MINB>
@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(TX *TY, MINB)
     for (int s = 0; s < NS; ++s) store_vec<VEC>(&s_agg[((ty) * NS + s) * DC + tx * VEC], agg.v[s]);
     __syncthreads();
 
+    S excl = Op::identity(), cta_keep = Op::identity();
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
         const bool lact = lane < TX;
@@ -186,13 +187,18 @@ __global__ void __launch_bounds__(TX *TY, MINB)
                 cta = (k == 0) ? x : Op::combine(cta, x);
             }
         }
-        const S excl = lookback_chan<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch, cta);
+        publish_first<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch, cta);
+        excl = find_carry<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch);
         if (lact) {
 #pragma unroll
             for (int s = 0; s < NS; ++s) store_vec<VEC>(&s_carry[s * DC + lane * VEC], excl.v[s]);
         }
+        cta_keep = cta;
     }
     __syncthreads();
+    // warp 0 publishes the chunk's prefix while the others start pass 2
+    if (threadIdx.x < 32)
+        publish_prefix<Op, TX>(g, lb, c, j, (threadIdx.x & 31) < TX, tile, epoch, excl, cta_keep);
 
     S st;
 #pragma unroll

@@ -299,13 +299,13 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1 + kNPub) * 32, 1)
 #pragma unroll
             for (int q = 0; q < NS; ++q)
                 load_vec<VEC>(&s_cta[(a_slot * NS + q) * DC + lane * VEC], cta.v[q]);
-            const S excl = resolve_carry<Op, 32>(args, g, lb, c, j, bb, ld, true, lchan, tile,
-                                                 epoch, cta);
+            const S excl = find_carry<Op, 32>(args, g, lb, c, j, bb, ld, true, lchan, tile, epoch);
             float *cr = s_carry + a_slot * NS * DC;
 #pragma unroll
             for (int q = 0; q < NS; ++q) store_vec<VEC>(&cr[q * DC + lane * VEC], excl.v[q]);
             __syncwarp();
             if (lane == 0) mbar_arrive(carry + s);
+            publish_prefix<Op, 32>(g, lb, c, j, true, tile, epoch, excl, cta);
         }
     } else {
         // ------------------------------------------------------------- compute
