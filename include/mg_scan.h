@@ -171,6 +171,35 @@ mg_status mg_affine_scan_bwd(const float *A, const float *Abar, const float *Bba
                              void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * mg_linear_scan_fwd without a workspace argument (the page has no
+ * counterpart: this entry point exists for callers, not for the method).
+ * Some callers cannot allocate device memory when they call the scan: a
+ * plugin that its host framework gives no allocator, or code that must not
+ * allocate once it has started (real-time loops, fixed memory budgets).  This
+ * variant allocates nothing and frees nothing: its look-back workspace is a
+ * static device array of mg_linear_scan_fwd_noalloc_max_scratch() bytes
+ * (32 MiB) inside the library, which every GPU that loads the library holds
+ * until the process exits.  The caller still passes inputs and outputs,
+ * exactly as for mg_linear_scan_fwd.
+ *
+ * The first call on a device looks up that device's address of the array
+ * (with the device current); make that first call before any stream capture.
+ * Each call clears the part of the array it uses (an asynchronous memset on
+ * `stream`) and then launches the same kernel as mg_linear_scan_fwd.  All
+ * calls share the one array: calls whose work overlaps on the GPU (other
+ * streams, other host threads) race and must be serialised by the caller.
+ * Sizes whose workspace would exceed the array return MG_ERR_INVALID_ARG
+ * before any launch (with float32 inputs the limit is reached near 2^28
+ * elements); use mg_linear_scan_fwd with a caller workspace there.
+ */
+mg_status mg_linear_scan_fwd_noalloc(const void *a, const void *b, mg_dtype in_dt,
+                                     float *A, float *Bc,
+                                     int64_t B, int64_t T, int64_t D, cudaStream_t stream);
+
+/* Bytes of the static scratch behind mg_linear_scan_fwd_noalloc. */
+size_t mg_linear_scan_fwd_noalloc_max_scratch(void);
+
+/*
  * Testing hook for the look-back's failure path (no counterpart on the page).
  * Runs mg_linear_scan_fwd (float32 inputs) with the look-back record of tile
  * `stall_tile` never published and every look-back wait bounded by

@@ -107,6 +107,10 @@ def load():
         lib.mg_testing_linear_scan_fwd_stall.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, sz,
                                                          i64, ctypes.c_uint64, vp]
         lib.mg_testing_linear_scan_fwd_stall.restype = st
+        lib.mg_linear_scan_fwd_noalloc.argtypes = [vp, vp, i32, vp, vp, i64, i64, i64, vp]
+        lib.mg_linear_scan_fwd_noalloc.restype = st
+        lib.mg_linear_scan_fwd_noalloc_max_scratch.argtypes = []
+        lib.mg_linear_scan_fwd_noalloc_max_scratch.restype = sz
         for name in ("mg_workspace_init", "mg_workspace_status", "mg_linear_scan_fwd",
                      "mg_linear_scan_bwd", "mg_log_scan_fwd", "mg_affine_scan_fwd",
                      "mg_affine_scan_bwd"):
@@ -290,6 +294,24 @@ def mg_affine_scan_bwd(A, Abar, Bbar, gAbar, gBbar, *, out=None, ws=None, stream
                                      dB.data_ptr(), B, T, n, k, v, w.data_ptr(), w.numel(), sh),
            "mg_affine_scan_bwd")
     return dA, dB
+
+
+def mg_linear_scan_fwd_noalloc(a, b, *, out=None, stream=None):
+    """mg_linear_scan_fwd with the library's static scratch instead of a
+    workspace: the C entry point allocates nothing (for callers that cannot
+    allocate device memory at call time).  Outputs are allocated here unless
+    given; calls that overlap on the GPU must be serialised by the caller."""
+    a = _prep(a, "a", (torch.float32, torch.bfloat16))
+    b = _prep(b, "b", (a.dtype,))
+    if a.dim() != 3 or b.shape != a.shape:
+        raise ValueError("a and b must both be (B, T, D)")
+    B, T, D = a.shape
+    A, Bc = _out(out, 0, a.shape, a), _out(out, 1, a.shape, a)
+    sh = _stream_handle(stream, a.device)
+    _check(load().mg_linear_scan_fwd_noalloc(a.data_ptr(), b.data_ptr(), _DT[a.dtype],
+                                             A.data_ptr(), Bc.data_ptr(), B, T, D, sh),
+           "mg_linear_scan_fwd_noalloc")
+    return A, Bc
 
 
 # Names of the page "minGRU - Triton kernels".

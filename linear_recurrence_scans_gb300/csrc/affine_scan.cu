@@ -1032,16 +1032,17 @@ template <int K, int V>
 using BigBwd = WarpPlan<WCfg<K, K + V, true, 4, (K == 4 ? 16 : 4), (K < 16)>>;
 
 template <int K, int V>
-size_t ws_kv(int64_t B, int64_t T, int64_t n)
+size_t ws_kv(int64_t B, int64_t T, int64_t n, const LaunchOpts &o)
 {
     size_t a, b;
     if constexpr (K <= 4) {
-        a = SmallFwd<K, V>::ws_bytes(B, T, n);
-        b = SmallBwd<K, V>::ws_bytes(B, T, n);
-        const size_t c = StreamPlan<AffFwdT<K, V>>::ws_bytes(B, T, n);
-        const size_t d = StreamPlan<AffBwdT<K, V>>::ws_bytes(B, T, n);
-        a = a > c ? a : c;
-        b = b > d ? b : d;
+        if (o.engine == LaunchOpts::kStream && aff_stream_ok<K, V>(n)) {
+            a = StreamPlan<AffFwdT<K, V>>::ws_bytes(B, T, n);
+            b = StreamPlan<AffBwdT<K, V>>::ws_bytes(B, T, n);
+        } else {
+            a = SmallFwd<K, V>::ws_bytes(B, T, n);
+            b = SmallBwd<K, V>::ws_bytes(B, T, n);
+        }
     } else {
         a = BigFwd<K, V>::ws_bytes(B, T, n);
         b = BigBwd<K, V>::ws_bytes(B, T, n);
@@ -1117,9 +1118,9 @@ mg_status bwd_kv(const float *A, const float *Abar, const float *Bbar, const flo
 
 }  // namespace
 
-size_t affine_ws_bytes(int64_t B, int64_t T, int64_t n, int k, int v)
+size_t affine_ws_bytes(int64_t B, int64_t T, int64_t n, int k, int v, const LaunchOpts &o)
 {
-#define MG_CALL(K, V) return ws_kv<K, V>(B, T, n)
+#define MG_CALL(K, V) return ws_kv<K, V>(B, T, n, o)
     MG_KV_DISPATCH(k, v, MG_CALL)
 #undef MG_CALL
     return 0;

@@ -448,35 +448,49 @@ using LinBwdB16s = ChanPlan<LinBwd<bf16_t, 1, 4>, kTX, kTY>;
 using LogF32 = ChanPlan<LogFwd<4, MG_LOG_L>, MG_LOG_TX, MG_LOG_TY, MG_LOG_MB>;
 using LogF32s = ChanPlan<LogFwd<1, 8>, kTX, kTY>;
 
-template <class P>
-size_t mx(size_t a, int64_t B, int64_t T, int64_t D)
-{
-    const size_t b = P::ws_bytes(B, T, D);
-    return a > b ? a : b;
-}
-
 }  // namespace
 
-size_t linear_ws_bytes(int64_t B, int64_t T, int64_t D)
+namespace {
+bool use_stream_fwd(mg_dtype dt, int64_t D, const LaunchOpts &o)
 {
-    size_t m = 0;
-    m = mx<LinFwdF32>(m, B, T, D);
-    m = mx<LinFwdF32s>(m, B, T, D);
-    m = mx<LinFwdB16>(m, B, T, D);
-    m = mx<LinFwdB16s>(m, B, T, D);
-    m = mx<LinBwdF32>(m, B, T, D);
-    m = mx<LinBwdF32s>(m, B, T, D);
-    m = mx<LinBwdB16>(m, B, T, D);
-    m = mx<LinBwdB16s>(m, B, T, D);
-    const size_t st = stream_linear_ws_bytes(B, T, D);
-    return m > st ? m : st;
+    const bool want = o.engine == LaunchOpts::kStream || (o.engine == LaunchOpts::kAuto && dt == MG_BF16);
+    return want && stream_linear_ok(dt, D);
+}
+bool use_stream_bwd(mg_dtype dt, int64_t D, const LaunchOpts &o)
+{
+    return o.engine == LaunchOpts::kStream && stream_linear_ok(dt, D);
+}
+}  // namespace
+
+size_t linear_fwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D, const LaunchOpts &o)
+{
+    if (use_stream_fwd(dt, D, o)) return stream_linear_fwd_ws_bytes(dt, B, T, D);
+    if (dt == MG_F32) return D % 4 == 0 ? LinFwdF32::ws_bytes(B, T, D) : LinFwdF32s::ws_bytes(B, T, D);
+    return D % 8 == 0 ? LinFwdB16::ws_bytes(B, T, D) : LinFwdB16s::ws_bytes(B, T, D);
 }
 
-size_t log_ws_bytes(int64_t B, int64_t T, int64_t D)
+size_t linear_bwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D, const LaunchOpts &o)
 {
-    const size_t m = mx<LogF32s>(mx<LogF32>(0, B, T, D), B, T, D);
-    const size_t st = stream_log_ws_bytes(B, T, D);
-    return m > st ? m : st;
+    if (use_stream_bwd(dt, D, o)) return stream_linear_bwd_ws_bytes(dt, B, T, D);
+    if (dt == MG_F32) return D % 4 == 0 ? LinBwdF32::ws_bytes(B, T, D) : LinBwdF32s::ws_bytes(B, T, D);
+    return D % 4 == 0 ? LinBwdB16::ws_bytes(B, T, D) : LinBwdB16s::ws_bytes(B, T, D);
+}
+
+size_t linear_ws_bytes(int64_t B, int64_t T, int64_t D, const LaunchOpts &o)
+{
+    size_t m = 0;
+    for (mg_dtype dt : {MG_F32, MG_BF16}) {
+        const size_t f = linear_fwd_ws_bytes(dt, B, T, D, o), b = linear_bwd_ws_bytes(dt, B, T, D, o);
+        m = f > m ? f : m;
+        m = b > m ? b : m;
+    }
+    return m;
+}
+
+size_t log_ws_bytes(int64_t B, int64_t T, int64_t D, const LaunchOpts &o)
+{
+    if (o.engine == LaunchOpts::kStream && stream_log_ok(D)) return stream_log_ws_bytes(B, T, D);
+    return D % 4 == 0 ? LogF32::ws_bytes(B, T, D) : LogF32s::ws_bytes(B, T, D);
 }
 
 mg_status launch_linear_fwd(const void *a, const void *b, mg_dtype dt, float *A, float *Bc,
@@ -484,10 +498,7 @@ mg_status launch_linear_fwd(const void *a, const void *b, mg_dtype dt, float *A,
                             const LaunchOpts &o)
 {
     const char *nm = "mg_linear_scan_fwd";
-    const bool stream_fwd = o.engine == LaunchOpts::kStream ||
-                            (o.engine == LaunchOpts::kAuto && dt == MG_BF16);
-    if (stream_fwd && stream_linear_ok(dt, D))
-        return stream_linear_fwd(a, b, dt, A, Bc, B, T, D, ws, wsb, s, o);
+    if (use_stream_fwd(dt, D, o)) return stream_linear_fwd(a, b, dt, A, Bc, B, T, D, ws, wsb, s, o);
     if (dt == MG_F32) {
         using F = const float *;
         if (D % 4 == 0)
@@ -505,7 +516,7 @@ mg_status launch_linear_bwd(const void *a, mg_dtype dt, const float *A, const fl
                             const LaunchOpts &o)
 {
     const char *nm = "mg_linear_scan_bwd";
-    if (o.engine == LaunchOpts::kStream && stream_linear_ok(dt, D))
+    if (use_stream_bwd(dt, D, o))
         return stream_linear_bwd(a, dt, A, Bc, gA, gBc, da, db, B, T, D, ws, wsb, s, o);
     if (dt == MG_F32) {
         using F = const float *;

@@ -54,9 +54,13 @@ inline Lookback make_lookback(void *ws, size_t n_tiles, const LaunchOpts &o)
 
 // Launchers (defined in channel_scan.cu / affine_scan.cu).  They assume the
 // arguments were validated by the C entry points and B, T, D > 0.
-size_t linear_ws_bytes(int64_t B, int64_t T, int64_t D);
-size_t log_ws_bytes(int64_t B, int64_t T, int64_t D);
-size_t affine_ws_bytes(int64_t B, int64_t T, int64_t n, int k, int v);
+// Workspace bytes a launch with options `o` needs (each mirrors its
+// launcher's choice of kernel shape).
+size_t linear_fwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D, const LaunchOpts &o);
+size_t linear_bwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D, const LaunchOpts &o);
+size_t linear_ws_bytes(int64_t B, int64_t T, int64_t D, const LaunchOpts &o);  // both, both dtypes
+size_t log_ws_bytes(int64_t B, int64_t T, int64_t D, const LaunchOpts &o);
+size_t affine_ws_bytes(int64_t B, int64_t T, int64_t n, int k, int v, const LaunchOpts &o);
 
 mg_status launch_linear_fwd(const void *a, const void *b, mg_dtype dt, float *A, float *Bc,
                             int64_t B, int64_t T, int64_t D, void *ws, size_t ws_bytes,
@@ -80,7 +84,8 @@ mg_status launch_affine_bwd(const float *A, const float *Abar, const float *Bbar
 // multiple of the 16-byte vector width.
 bool stream_linear_ok(mg_dtype dt, int64_t D);
 bool stream_log_ok(int64_t D);
-size_t stream_linear_ws_bytes(int64_t B, int64_t T, int64_t D);
+size_t stream_linear_fwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D);
+size_t stream_linear_bwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D);
 size_t stream_log_ws_bytes(int64_t B, int64_t T, int64_t D);
 mg_status stream_linear_fwd(const void *a, const void *b, mg_dtype dt, float *A, float *Bc,
                             int64_t B, int64_t T, int64_t D, void *ws, size_t ws_bytes,

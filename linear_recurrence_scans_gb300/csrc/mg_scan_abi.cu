@@ -5,6 +5,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <initializer_list>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -93,6 +94,41 @@ LaunchOpts default_opts()
     return o;
 }
 
+// ------------------------------------------------ static scratch (no-alloc)
+// mg_linear_scan_fwd_noalloc keeps its look-back workspace in this array
+// instead of a caller buffer.  Every device that loads the library holds it
+// (kNoAllocScratchBytes) until the process exits.  Host code must not use the
+// symbol as an address: the device address is obtained once per device with
+// cudaGetSymbolAddress and cached below.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the static scratch on the current device (set-up on the
+// first call per device, with that device current).
+mg_status noalloc_scratch(const char *fn, void **out)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(MG_ERR_LAUNCH, "%s: cudaGetDevice: %s", fn, cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(MG_ERR_UNSUPPORTED, "%s: device ordinal %d beyond %d", fn, dev, kMaxDevices);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return fail(MG_ERR_LAUNCH, "%s: cudaGetSymbolAddress of the static scratch: %s", fn,
+                        cudaGetErrorString(e));
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return MG_OK;
+}
+
 #define MG_TRY(expr)                      \
     do {                                  \
         const mg_status st__ = (expr);    \
@@ -126,21 +162,21 @@ size_t mg_linear_scan_workspace_size(int64_t B, int64_t T, int64_t D)
 {
     if (B < 0 || T < 0 || D < 0) return 0;
     if (B == 0 || T == 0 || D == 0) return kControlBytes;
-    return linear_ws_bytes(B, T, D);
+    return linear_ws_bytes(B, T, D, default_opts());
 }
 
 size_t mg_log_scan_workspace_size(int64_t B, int64_t T, int64_t D)
 {
     if (B < 0 || T < 0 || D < 0) return 0;
     if (B == 0 || T == 0 || D == 0) return kControlBytes;
-    return log_ws_bytes(B, T, D);
+    return log_ws_bytes(B, T, D, default_opts());
 }
 
 size_t mg_affine_scan_workspace_size(int64_t B, int64_t T, int64_t n, int k, int v)
 {
     if (B < 0 || T < 0 || n < 0 || !valid_kv(k) || !valid_kv(v)) return 0;
     if (B == 0 || T == 0 || n == 0) return kControlBytes;
-    return affine_ws_bytes(B, T, n, k, v);
+    return affine_ws_bytes(B, T, n, k, v, default_opts());
 }
 
 mg_status mg_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream)
@@ -188,7 +224,7 @@ mg_status mg_linear_scan_fwd(const void *a, const void *b, mg_dtype in_dt, float
     MG_TRY(check_dims(fn, {B, T, D}));
     if (B == 0 || T == 0 || D == 0) return MG_OK;
     const size_t n = size_t(B) * T * D, isz = in_dt == MG_F32 ? 4 : 2;
-    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D)));
+    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D, default_opts())));
     MG_TRY(check_bufs(fn, {{a, n * isz, "a", false},
                            {b, n * isz, "b", false},
                            {A, n * 4, "A", true},
@@ -208,7 +244,7 @@ mg_status mg_linear_scan_bwd(const void *a, mg_dtype a_dt, const float *A, const
     MG_TRY(check_dims(fn, {B, T, D}));
     if (B == 0 || T == 0 || D == 0) return MG_OK;
     const size_t n = size_t(B) * T * D, isz = a_dt == MG_F32 ? 4 : 2;
-    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D)));
+    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D, default_opts())));
     MG_TRY(check_bufs(fn, {{a, n * isz, "a", false},
                            {A, n * 4, "A", false},
                            {Bc, n * 4, "Bc", false},
@@ -230,7 +266,7 @@ mg_status mg_log_scan_fwd(const float *log_coeffs, const float *log_values, floa
     if (T < 0) return fail(MG_ERR_INVALID_ARG, "%s: negative size", fn);
     if (B == 0 || T == 0 || D == 0) return MG_OK;
     const size_t n = size_t(B) * T * D, nv = size_t(B) * (T + 1) * D;
-    MG_TRY(check_ws(fn, ws, ws_bytes, log_ws_bytes(B, T, D)));
+    MG_TRY(check_ws(fn, ws, ws_bytes, log_ws_bytes(B, T, D, default_opts())));
     MG_TRY(check_bufs(fn, {{log_coeffs, n * 4, "log_coeffs", false},
                            {log_values, nv * 4, "log_values", false},
                            {h, n * 4, "h", true},
@@ -249,7 +285,7 @@ mg_status mg_affine_scan_fwd(const float *A, const float *Bm, float *Abar, float
     MG_TRY(check_dims(fn, {B, T, n, k, k > v ? k : v}));
     if (B == 0 || T == 0 || n == 0) return MG_OK;
     const size_t s = size_t(B) * T * n;
-    MG_TRY(check_ws(fn, ws, ws_bytes, affine_ws_bytes(B, T, n, k, v)));
+    MG_TRY(check_ws(fn, ws, ws_bytes, affine_ws_bytes(B, T, n, k, v, default_opts())));
     MG_TRY(check_bufs(fn, {{A, s * k * k * 4, "A", false},
                            {Bm, s * k * v * 4, "Bm", false},
                            {Abar, s * k * k * 4, "Abar", true},
@@ -270,7 +306,7 @@ mg_status mg_affine_scan_bwd(const float *A, const float *Abar, const float *Bba
     MG_TRY(check_dims(fn, {B, T, n, k, k > v ? k : v}));
     if (B == 0 || T == 0 || n == 0) return MG_OK;
     const size_t s = size_t(B) * T * n;
-    MG_TRY(check_ws(fn, ws, ws_bytes, affine_ws_bytes(B, T, n, k, v)));
+    MG_TRY(check_ws(fn, ws, ws_bytes, affine_ws_bytes(B, T, n, k, v, default_opts())));
     MG_TRY(check_bufs(fn, {{A, s * k * k * 4, "A", false},
                            {Abar, s * k * k * 4, "Abar", false},
                            {Bbar, s * k * v * 4, "Bbar", false},
@@ -293,7 +329,7 @@ mg_status mg_testing_linear_scan_fwd_stall(const float *a, const float *b, float
     MG_TRY(check_dims(fn, {B, T, D}));
     if (B == 0 || T == 0 || D == 0) return MG_OK;
     const size_t n = size_t(B) * T * D;
-    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D)));
+    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D, default_opts())));
     MG_TRY(check_bufs(fn, {{a, n * 4, "a", false},
                            {b, n * 4, "b", false},
                            {A, n * 4, "A", true},
@@ -305,6 +341,40 @@ mg_status mg_testing_linear_scan_fwd_stall(const float *a, const float *b, float
     o.wait_limit_ns = wait_limit_ns;
     o.stall_tile = stall_tile;
     return launch_linear_fwd(a, b, MG_F32, A, Bc, B, T, D, ws, ws_bytes, stream, o);
+}
+
+size_t mg_linear_scan_fwd_noalloc_max_scratch(void) { return kNoAllocScratchBytes; }
+
+mg_status mg_linear_scan_fwd_noalloc(const void *a, const void *b, mg_dtype in_dt, float *A,
+                                     float *Bc, int64_t B, int64_t T, int64_t D,
+                                     cudaStream_t stream)
+{
+    const char *fn = "mg_linear_scan_fwd_noalloc";
+    g_detail[0] = 0;
+    if (in_dt != MG_F32 && in_dt != MG_BF16)
+        return fail(MG_ERR_UNSUPPORTED, "%s: input dtype %d not supported", fn, int(in_dt));
+    MG_TRY(check_dims(fn, {B, T, D}));
+    if (B == 0 || T == 0 || D == 0) return MG_OK;
+    const LaunchOpts o = default_opts();
+    const size_t need = linear_fwd_ws_bytes(in_dt, B, T, D, o);
+    if (need > kNoAllocScratchBytes)
+        return fail(MG_ERR_INVALID_ARG,
+                    "%s: (B,T,D) = (%lld,%lld,%lld) needs %zu bytes of scratch; the static scratch "
+                    "holds %zu (use mg_linear_scan_fwd with a caller workspace)",
+                    fn, (long long)B, (long long)T, (long long)D, need, kNoAllocScratchBytes);
+    void *scratch = nullptr;
+    MG_TRY(noalloc_scratch(fn, &scratch));
+    const size_t n = size_t(B) * T * D, isz = in_dt == MG_F32 ? 4 : 2;
+    MG_TRY(check_bufs(fn, {{a, n * isz, "a", false},
+                           {b, n * isz, "b", false},
+                           {A, n * 4, "A", true},
+                           {Bc, n * 4, "Bc", true}}));
+    // The array keeps the previous call's control words and records: clear
+    // the part this call uses so it starts from a zero-filled workspace.
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, need, stream);
+    if (e != cudaSuccess)
+        return fail(MG_ERR_LAUNCH, "%s: clearing the scratch: %s", fn, cudaGetErrorString(e));
+    return launch_linear_fwd(a, b, in_dt, A, Bc, B, T, D, scratch, kNoAllocScratchBytes, stream, o);
 }
 
 }  // extern "C"

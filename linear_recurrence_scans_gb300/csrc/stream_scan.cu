@@ -323,13 +323,14 @@ Staged staged(const void *p, int64_t rows) { return Staged{static_cast<const cha
 bool stream_linear_ok(mg_dtype dt, int64_t D) { return dt == MG_F32 ? D % 4 == 0 : D % 8 == 0; }
 bool stream_log_ok(int64_t D) { return D % 4 == 0; }
 
-size_t stream_linear_ws_bytes(int64_t B, int64_t T, int64_t D)
+size_t stream_linear_fwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D)
 {
-    size_t m = SFwdF32::ws_bytes(B, T, D);
-    const size_t cand[] = {SFwdB16::ws_bytes(B, T, D), SBwdF32::ws_bytes(B, T, D),
-                           SBwdB16::ws_bytes(B, T, D)};
-    for (size_t c : cand) m = c > m ? c : m;
-    return m;
+    return dt == MG_F32 ? SFwdF32::ws_bytes(B, T, D) : SFwdB16::ws_bytes(B, T, D);
+}
+
+size_t stream_linear_bwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D)
+{
+    return dt == MG_F32 ? SBwdF32::ws_bytes(B, T, D) : SBwdB16::ws_bytes(B, T, D);
 }
 
 size_t stream_log_ws_bytes(int64_t B, int64_t T, int64_t D) { return SLog::ws_bytes(B, T, D); }
