@@ -413,16 +413,16 @@ struct LogFwd {
 #define MG_LINF16_MB 1
 #endif
 #ifndef MG_LINB_TX
-#define MG_LINB_TX 8
+#define MG_LINB_TX 16
 #endif
 #ifndef MG_LINB_TY
-#define MG_LINB_TY 16
+#define MG_LINB_TY 8
 #endif
 #ifndef MG_LINB_L
 #define MG_LINB_L 8
 #endif
 #ifndef MG_LINB_MB
-#define MG_LINB_MB 1
+#define MG_LINB_MB 2
 #endif
 #ifndef MG_LOG_TX
 #define MG_LOG_TX 32
@@ -434,7 +434,7 @@ struct LogFwd {
 #define MG_LOG_L 4
 #endif
 #ifndef MG_LOG_MB
-#define MG_LOG_MB 1
+#define MG_LOG_MB 4
 #endif
 constexpr int kTX = 32, kTY = 8;
 using LinFwdF32 = ChanPlan<LinFwd<float, 4, MG_LINF_L>, MG_LINF_TX, MG_LINF_TY, MG_LINF_MB>;
