@@ -1017,19 +1017,55 @@ struct WarpPlan {
 
 // ------------------------------------------------------------ dispatch
 
-constexpr int kSmallTY = 8, kSmallL = 4;
+// Tiles, each overridable at build time.  k <= 4 (thread-owned state on the
+// chunk engine): TY thread rows x L steps of 32 sequences, MB minimum CTAs per
+// SM.  k = 8, 16 (warp kernel): NW warps x L steps of one sequence, DB =
+// double-buffered state exchange.
+#ifndef MG_AFS_TY
+#define MG_AFS_TY 8
+#endif
+#ifndef MG_AFS_L
+#define MG_AFS_L 4
+#endif
+#ifndef MG_AFS_MB
+#define MG_AFS_MB 1
+#endif
+#ifndef MG_AFSB_TY
+#define MG_AFSB_TY 8
+#endif
+#ifndef MG_AFSB_L
+#define MG_AFSB_L 4
+#endif
+#ifndef MG_AFSB_MB
+#define MG_AFSB_MB 1
+#endif
+#ifndef MG_AFW_NW
+#define MG_AFW_NW 4
+#endif
+#ifndef MG_AFW_L
+#define MG_AFW_L 8
+#endif
+#ifndef MG_AFW_DB
+#define MG_AFW_DB 1
+#endif
+#ifndef MG_AFWB_NW
+#define MG_AFWB_NW 4
+#endif
+#ifndef MG_AFWB_L
+#define MG_AFWB_L 4
+#endif
+#ifndef MG_AFWB_DB
+#define MG_AFWB_DB 0
+#endif
 
 template <int K, int V>
-using SmallFwd = ChanPlan<AffFwdSmall<K, V, kSmallL>, 32, kSmallTY>;
+using SmallFwd = ChanPlan<AffFwdSmall<K, V, MG_AFS_L>, 32, MG_AFS_TY, MG_AFS_MB>;
 template <int K, int V>
-using SmallBwd = ChanPlan<AffBwdSmall<K, V, kSmallL>, 32, kSmallTY>;
-// Warp kernel tiles (k = 8, 16): 4 warps x 8 steps (forward) and 4 x 4
-// (backward, five staged inputs per step) with a single-buffered exchange to
-// fit two CTAs per SM.
+using SmallBwd = ChanPlan<AffBwdSmall<K, V, MG_AFSB_L>, 32, MG_AFSB_TY, MG_AFSB_MB>;
 template <int K, int V>
-using BigFwd = WarpPlan<WCfg<K, V, false, 4, (K == 4 ? 16 : 8), true>>;
+using BigFwd = WarpPlan<WCfg<K, V, false, MG_AFW_NW, MG_AFW_L, bool(MG_AFW_DB)>>;
 template <int K, int V>
-using BigBwd = WarpPlan<WCfg<K, K + V, true, 4, (K == 4 ? 16 : 4), (K < 16)>>;
+using BigBwd = WarpPlan<WCfg<K, K + V, true, MG_AFWB_NW, MG_AFWB_L, bool(MG_AFWB_DB)>>;
 
 template <int K, int V>
 size_t ws_kv(int64_t B, int64_t T, int64_t n, const LaunchOpts &o)
