@@ -424,6 +424,18 @@ struct LogFwd {
 #ifndef MG_LINB_MB
 #define MG_LINB_MB 2
 #endif
+#ifndef MG_LINB16_TX
+#define MG_LINB16_TX 32
+#endif
+#ifndef MG_LINB16_TY
+#define MG_LINB16_TY 8
+#endif
+#ifndef MG_LINB16_L
+#define MG_LINB16_L 4
+#endif
+#ifndef MG_LINB16_MB
+#define MG_LINB16_MB 1
+#endif
 #ifndef MG_LOG_TX
 #define MG_LOG_TX 32
 #endif
@@ -443,7 +455,7 @@ using LinFwdB16 = ChanPlan<LinFwd<bf16_t, 8, MG_LINF16_L>, MG_LINF16_TX, MG_LINF
 using LinFwdB16s = ChanPlan<LinFwd<bf16_t, 1, 8>, kTX, kTY>;
 using LinBwdF32 = ChanPlan<LinBwd<float, 4, MG_LINB_L>, MG_LINB_TX, MG_LINB_TY, MG_LINB_MB>;
 using LinBwdF32s = ChanPlan<LinBwd<float, 1, 4>, kTX, kTY>;
-using LinBwdB16 = ChanPlan<LinBwd<bf16_t, 4, MG_LINB_L>, MG_LINB_TX, MG_LINB_TY, MG_LINB_MB>;
+using LinBwdB16 = ChanPlan<LinBwd<bf16_t, 4, MG_LINB16_L>, MG_LINB16_TX, MG_LINB16_TY, MG_LINB16_MB>;
 using LinBwdB16s = ChanPlan<LinBwd<bf16_t, 1, 4>, kTX, kTY>;
 using LogF32 = ChanPlan<LogFwd<4, MG_LOG_L>, MG_LOG_TX, MG_LOG_TY, MG_LOG_MB>;
 using LogF32s = ChanPlan<LogFwd<1, 8>, kTX, kTY>;

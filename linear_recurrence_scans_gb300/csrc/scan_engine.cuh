@@ -16,6 +16,11 @@
 namespace mg {
 namespace {
 
+#ifndef MG_CHUNK_PREFETCH
+#define MG_CHUNK_PREFETCH 0
+#endif
+constexpr bool kChunkPrefetch = MG_CHUNK_PREFETCH != 0;
+
 struct ChanGeom {
     int64_t B, T, D;
     int nJb;  // channel tiles per batch row
@@ -168,6 +173,10 @@ __global__ void __launch_bounds__(TX *TY, MINB)
     }
 #pragma unroll
     for (int s = 0; s < NS; ++s) store_vec<VEC>(&s_agg[((ty) * NS + s) * DC + tx * VEC], agg.v[s]);
+    // With MG_CHUNK_PREFETCH, pass 2's loads are issued here, before the
+    // barrier that waits for the look-back, so their latency overlaps it.
+    typename Op::Regs r2;
+    if constexpr (kChunkPrefetch) Op::load(args, g, bb, t0, d, act, r2);
     __syncthreads();
 
     S excl = Op::identity(), cta_keep = Op::identity();
@@ -219,9 +228,8 @@ __global__ void __launch_bounds__(TX *TY, MINB)
         }
     }
     // Pass 2: re-read the steps and re-run them from the start state.
-    typename Op::Regs r;
-    Op::load(args, g, bb, t0, d, act, r);
-    Op::epilogue(args, g, bb, t0, d, act, r, st);
+    if constexpr (!kChunkPrefetch) Op::load(args, g, bb, t0, d, act, r2);
+    Op::epilogue(args, g, bb, t0, d, act, r2, st);
     finish_cta(lb, epoch);
 }
 
