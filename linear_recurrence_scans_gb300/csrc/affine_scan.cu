@@ -166,7 +166,7 @@ struct AffFwdSmall {
         return o;
     }
     __device__ static void epilogue(const Args &p, const ChanGeom &, int64_t, int64_t, int, bool,
-                                    const Regs &r, const S &st)
+                                    const Regs &r, S &st)
     {
         float C[KK], Vv[KW];
 #pragma unroll
@@ -190,6 +190,10 @@ struct AffFwdSmall {
                 st_floats<KW>(p.Bbar + s * KW, Vv);
             }
         }
+#pragma unroll
+        for (int i = 0; i < KK; ++i) st.v[i][0] = C[i];
+#pragma unroll
+        for (int i = 0; i < KW; ++i) st.v[KK + i][0] = Vv[i];
     }
 };
 
@@ -286,7 +290,7 @@ struct AffBwdSmall {
         return o;
     }
     __device__ static void epilogue(const Args &p, const ChanGeom &, int64_t, int64_t, int, bool,
-                                    const Regs &r, const S &st)
+                                    const Regs &r, S &st)
     {
         float Vv[KW];
 #pragma unroll
@@ -334,6 +338,9 @@ struct AffBwdSmall {
                 st_floats<KV>(p.dB + s * KV, dB);
             }
         }
+        // (the running transition product is not needed past the outputs)
+#pragma unroll
+        for (int i = 0; i < KW; ++i) st.v[KK + i][0] = Vv[i];
     }
 };
 

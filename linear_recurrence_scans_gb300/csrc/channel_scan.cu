@@ -102,7 +102,7 @@ struct LinFwd {
         return o;
     }
     __device__ static void epilogue(const Args &p, const ChanGeom &g, int64_t bb, int64_t t0,
-                                    int d, bool act, const Regs &r, const S &st)
+                                    int d, bool act, const Regs &r, S &st)
     {
         float P[VEC], H[VEC];
 #pragma unroll
@@ -123,6 +123,11 @@ struct LinFwd {
                 store_vec<VEC>(p.A + off, P);
                 store_vec<VEC>(p.Bc + off, H);
             }
+        }
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            st.v[0][v] = P[v];
+            st.v[1][v] = H[v];
         }
     }
 };
@@ -214,7 +219,7 @@ struct LinBwd {
         return o;
     }
     __device__ static void epilogue(const Args &p, const ChanGeom &g, int64_t bb, int64_t t0,
-                                    int d, bool act, const Regs &r, const S &st)
+                                    int d, bool act, const Regs &r, S &st)
     {
         // A_{t-1}, Bc_{t-1} for the L steps (A_0 = 1, Bc_0 = 0 before the first step).
         float Ap[L][VEC], Bp[L][VEC];
@@ -254,6 +259,12 @@ struct LinBwd {
                 store_vec<VEC>(p.da + off, da);
                 store_vec<VEC>(p.db + off, lam);
             }
+        }
+        // (the running coefficient product is not needed past the outputs)
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            st.v[1][v] = mu[v];
+            st.v[2][v] = lam[v];
         }
     }
 };
@@ -362,7 +373,7 @@ struct LogFwd {
         return o;
     }
     __device__ static void epilogue(const Args &p, const ChanGeom &g, int64_t bb, int64_t t0,
-                                    int d, bool act, const Regs &r, const S &st)
+                                    int d, bool act, const Regs &r, S &st)
     {
         float m[VEC], s[VEC];
 #pragma unroll
@@ -381,11 +392,17 @@ struct LogFwd {
             const int64_t t = t0 + i;
             if (act && t < g.T) store_vec<VEC>(p.h + (bb * g.T + t) * g.D + d, h);
         }
+        // (the summed log-coefficient is not needed past the outputs)
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            st.v[1][v] = m[v];
+            st.v[2][v] = s[v];
+        }
     }
 };
 
 // Tile choices (threads along channels TX, thread rows TY, steps per thread
-// L, minimum resident CTAs per SM).  fp32: 4 channels (16 B) per thread;
+// and round L, minimum resident CTAs per SM, rounds per thread R).  fp32: 4 channels (16 B) per thread;
 // bf16: 8 channels (16 B).  A D that is not a multiple of the vector width
 // takes the 1-channel variant.  Each can be overridden at build time.
 #ifndef MG_LINF_TX
@@ -448,16 +465,31 @@ struct LogFwd {
 #ifndef MG_LOG_MB
 #define MG_LOG_MB 4
 #endif
+#ifndef MG_LINF_R
+#define MG_LINF_R 2
+#endif
+#ifndef MG_LINF16_R
+#define MG_LINF16_R 2
+#endif
+#ifndef MG_LINB_R
+#define MG_LINB_R 2
+#endif
+#ifndef MG_LINB16_R
+#define MG_LINB16_R 2
+#endif
+#ifndef MG_LOG_R
+#define MG_LOG_R 1
+#endif
 constexpr int kTX = 32, kTY = 8;
-using LinFwdF32 = ChanPlan<LinFwd<float, 4, MG_LINF_L>, MG_LINF_TX, MG_LINF_TY, MG_LINF_MB>;
+using LinFwdF32 = ChanPlan<LinFwd<float, 4, MG_LINF_L>, MG_LINF_TX, MG_LINF_TY, MG_LINF_MB, MG_LINF_R>;
 using LinFwdF32s = ChanPlan<LinFwd<float, 1, 8>, kTX, kTY>;
-using LinFwdB16 = ChanPlan<LinFwd<bf16_t, 8, MG_LINF16_L>, MG_LINF16_TX, MG_LINF16_TY, MG_LINF16_MB>;
+using LinFwdB16 = ChanPlan<LinFwd<bf16_t, 8, MG_LINF16_L>, MG_LINF16_TX, MG_LINF16_TY, MG_LINF16_MB, MG_LINF16_R>;
 using LinFwdB16s = ChanPlan<LinFwd<bf16_t, 1, 8>, kTX, kTY>;
-using LinBwdF32 = ChanPlan<LinBwd<float, 4, MG_LINB_L>, MG_LINB_TX, MG_LINB_TY, MG_LINB_MB>;
+using LinBwdF32 = ChanPlan<LinBwd<float, 4, MG_LINB_L>, MG_LINB_TX, MG_LINB_TY, MG_LINB_MB, MG_LINB_R>;
 using LinBwdF32s = ChanPlan<LinBwd<float, 1, 4>, kTX, kTY>;
-using LinBwdB16 = ChanPlan<LinBwd<bf16_t, 4, MG_LINB16_L>, MG_LINB16_TX, MG_LINB16_TY, MG_LINB16_MB>;
+using LinBwdB16 = ChanPlan<LinBwd<bf16_t, 4, MG_LINB16_L>, MG_LINB16_TX, MG_LINB16_TY, MG_LINB16_MB, MG_LINB16_R>;
 using LinBwdB16s = ChanPlan<LinBwd<bf16_t, 1, 4>, kTX, kTY>;
-using LogF32 = ChanPlan<LogFwd<4, MG_LOG_L>, MG_LOG_TX, MG_LOG_TY, MG_LOG_MB>;
+using LogF32 = ChanPlan<LogFwd<4, MG_LOG_L>, MG_LOG_TX, MG_LOG_TY, MG_LOG_MB, MG_LOG_R>;
 using LogF32s = ChanPlan<LogFwd<1, 8>, kTX, kTY>;
 
 }  // namespace

@@ -3,12 +3,12 @@
 //
 // An op supplies: NS floats of state per channel group of VEC channels, the
 // identity, the combine (x earlier, y later), the initial state of chunk 0,
-// how a thread loads its L steps and forms their elements, and the epilogue
-// that re-runs the thread's steps from its start state and writes outputs.
-// The engine does the rest: ticketed tiles of DC = TX*VEC channels by
-// TC = TY*L steps, a shared-memory combine of the TY thread aggregates, the
-// decoupled look-back of warp 0, and the hand-off of each thread's start
-// state.  kReverse ops walk time backwards (adjoint scans).
+// how a thread loads L steps and forms their elements, and the epilogue
+// that re-runs those steps from a start state, writes the outputs and leaves
+// the state after the last step.  The engine does the rest: ticketed tiles of
+// DC = TX*VEC channels by TC = TY*L*R steps (R rounds of L steps per thread),
+// a shared-memory combine of the TY thread aggregates, the decoupled
+// look-back of warp 0, and the hand-off of each thread's start state.  kReverse ops walk time backwards (adjoint scans).
 #pragma once
 
 #include "common.cuh"
@@ -129,7 +129,7 @@ __device__ void publish_prefix(const ChanGeom &g, const Lookback &lb, int c, int
     publish(lb, slot, kStatusPrefix, epoch, tile);
 }
 
-template <class Op, int TX, int TY, int MINB>
+template <class Op, int TX, int TY, int MINB, int R>
 __global__ void __launch_bounds__(TX *TY, MINB)
     channel_scan_kernel(const typename Op::Args args, const ChanGeom g, const Lookback lb)
 {
@@ -157,26 +157,33 @@ __global__ void __launch_bounds__(TX *TY, MINB)
     const int d = dbase + tx * VEC;
     const bool act = d < g.D;
     const int ct = Op::kReverse ? (g.nC - 1 - c) : c;
-    const int64_t t0 = int64_t(ct) * (TY * L) + ty * L;
+    // The thread owns R*L consecutive steps, handled as R rounds of L steps
+    // (the register footprint of one round); rounds run in processing order.
+    const int64_t tspan = int64_t(ct) * (TY * L * R) + int64_t(ty) * (L * R);
+    auto round_t0 = [&](int k) { return tspan + int64_t(Op::kReverse ? R - 1 - k : k) * L; };
 
-    // Pass 1: read the thread's L steps and fold them into its aggregate.  The
+    // Pass 1: read the thread's steps and fold them into its aggregate.  The
     // inputs are not kept across the look-back: pass 2 reads them again (the
     // tile is still in L1/L2), so registers stay free for occupancy.
     S agg;
-    {
+#pragma unroll 1
+    for (int k = 0; k < R; ++k) {
         typename Op::Regs r;
-        Op::load(args, g, bb, t0, d, act, r);
-        agg = Op::element(r, Op::kReverse ? L - 1 : 0);
+        Op::load(args, g, bb, round_t0(k), d, act, r);
+        S ragg = Op::element(r, Op::kReverse ? L - 1 : 0);
 #pragma unroll
-        for (int k = 1; k < L; ++k)
-            agg = Op::combine(agg, Op::element(r, Op::kReverse ? L - 1 - k : k));
+        for (int i = 1; i < L; ++i)
+            ragg = Op::combine(ragg, Op::element(r, Op::kReverse ? L - 1 - i : i));
+        agg = (k == 0) ? ragg : Op::combine(agg, ragg);
     }
 #pragma unroll
     for (int s = 0; s < NS; ++s) store_vec<VEC>(&s_agg[((ty) * NS + s) * DC + tx * VEC], agg.v[s]);
-    // With MG_CHUNK_PREFETCH, pass 2's loads are issued here, before the
-    // barrier that waits for the look-back, so their latency overlaps it.
+    // With MG_CHUNK_PREFETCH (one round only), pass 2's loads are issued
+    // here, before the barrier that waits for the look-back, so their latency
+    // overlaps it.
+    constexpr bool kPrefetch = kChunkPrefetch && R == 1;
     typename Op::Regs r2;
-    if constexpr (kChunkPrefetch) Op::load(args, g, bb, t0, d, act, r2);
+    if constexpr (kPrefetch) Op::load(args, g, bb, round_t0(0), d, act, r2);
     __syncthreads();
 
     S excl = Op::identity(), cta_keep = Op::identity();
@@ -227,18 +234,26 @@ __global__ void __launch_bounds__(TX *TY, MINB)
             st = Op::combine(st, x);
         }
     }
-    // Pass 2: re-read the steps and re-run them from the start state.
-    if constexpr (!kChunkPrefetch) Op::load(args, g, bb, t0, d, act, r2);
-    Op::epilogue(args, g, bb, t0, d, act, r2, st);
+    // Pass 2: re-read the steps and re-run them from the start state; the
+    // epilogue leaves in `st` the state after its round.
+    if constexpr (kPrefetch) {
+        Op::epilogue(args, g, bb, round_t0(0), d, act, r2, st);
+    } else {
+#pragma unroll 1
+        for (int k = 0; k < R; ++k) {
+            Op::load(args, g, bb, round_t0(k), d, act, r2);
+            Op::epilogue(args, g, bb, round_t0(k), d, act, r2, st);
+        }
+    }
     finish_cta(lb, epoch);
 }
 
 // ------------------------------------------------------------ launchers
 
-template <class Op, int TX, int TY, int MINB = 1>
+template <class Op, int TX, int TY, int MINB = 1, int R = 1>
 struct ChanPlan {
     static constexpr int DC = TX * Op::VEC;
-    static constexpr int TC = TY * Op::L;
+    static constexpr int TC = TY * Op::L * R;
     static ChanGeom geom(int64_t B, int64_t T, int64_t D)
     {
         ChanGeom g;
@@ -277,12 +292,12 @@ struct ChanPlan {
         constexpr size_t smem = size_t(TY + 1) * Op::NS * DC * sizeof(float);
         if (smem > 48 * 1024) {
             static const cudaError_t attr = cudaFuncSetAttribute(
-                channel_scan_kernel<Op, TX, TY, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                channel_scan_kernel<Op, TX, TY, MINB, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                 int(smem));
             if (attr != cudaSuccess)
                 return fail(MG_ERR_LAUNCH, "%s: %s", name, cudaGetErrorString(attr));
         }
-        channel_scan_kernel<Op, TX, TY, MINB><<<unsigned(nt), TX * TY, smem, s>>>(args, g, lb);
+        channel_scan_kernel<Op, TX, TY, MINB, R><<<unsigned(nt), TX * TY, smem, s>>>(args, g, lb);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return fail(MG_ERR_LAUNCH, "%s: launch failed: %s", name, cudaGetErrorString(e));
