@@ -20,15 +20,13 @@
 //
 // The backward op is the same engine run in reverse time on the adjoint
 // recurrence; the log op carries log-space values as (m, s) with
-// value = s * 2^m so that one exp2 per combine suffices.
+// value = s * e^m so that one exp2 per combine suffices.
 #include <cmath>
 
 #include "scan_engine.cuh"
 
 namespace mg {
 namespace {
-
-constexpr float kLog2e = 1.4426950408889634f;
 
 // ----------------------------------------------------------- linear forward
 // Element of step t: (a_t, b_t).  State: (running product, h).
@@ -270,10 +268,10 @@ struct LinBwd {
 };
 
 // ------------------------------------------------------- log-space forward
-// Element of step t: (lc_t, LB = lv_t) in base-2 logs.  State (la, m, s):
-// la = sum of log-coefficients, LB = m + log2(s).  Combine (x earlier):
-//   la = x.la + y.la,  LB = log2(2^(y.la + LB_x) + 2^(LB_y))
-// evaluated with one exp2 of minus the gap between the two exponents.
+// Element of step t: (lc_t, lv_t) in natural logs.  State (la, m, s): la =
+// sum of log-coefficients, the log value being m + log(s).  Combine (x
+// earlier): la = x.la + y.la and the value log(e^(y.la + LB_x) + e^(LB_y)),
+// one log_add (one exp2) per combine.
 template <int VEC_, int L_>
 struct LogFwd {
     static constexpr int NS = 3, VEC = VEC_, L = L_;
@@ -298,11 +296,6 @@ struct LogFwd {
             if (act && t < g.T) {
                 load_vec<VEC>(p.lc + (bb * g.T + t) * g.D + d, r.lc[i]);
                 load_vec<VEC>(p.lv + (bb * (g.T + 1) + t + 1) * g.D + d, r.lv[i]);
-#pragma unroll
-                for (int v = 0; v < VEC; ++v) {
-                    r.lc[i][v] *= kLog2e;
-                    r.lv[i][v] *= kLog2e;
-                }
             } else {
 #pragma unroll
                 for (int v = 0; v < VEC; ++v) {
@@ -334,7 +327,7 @@ struct LogFwd {
         }
         return e;
     }
-    // State before step 1: LB_0 = log h_0 = log_values[b, 0, d].
+    // State before step 1: log h_0 = log_values[b, 0, d].
     __device__ static S initial(const Args &p, const ChanGeom &g, int64_t bb, int d, bool act)
     {
         S e = identity();
@@ -343,24 +336,11 @@ struct LogFwd {
             load_vec<VEC>(p.lv + (bb * (g.T + 1)) * g.D + d, l0);
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
-                e.v[1][v] = l0[v] * kLog2e;
+                e.v[1][v] = l0[v];
                 e.v[2][v] = 1.f;
             }
         }
         return e;
-    }
-    // log2(xs 2^u + ys 2^ym) as (m, s); both exponents -inf gives (-inf, 0).
-    __device__ static void lse2(float u, float xs, float ym, float ys, float &m, float &s)
-    {
-        const float gap = u - ym;
-        const float e = exp2f(-fabsf(gap));
-        const bool ge = gap >= 0.f;
-        m = ge ? u : ym;
-        s = ge ? fmaf(ys, e, xs) : fmaf(xs, e, ys);
-        if (gap != gap) {  // -inf - -inf
-            m = -INFINITY;
-            s = 0.f;
-        }
     }
     __device__ static S combine(const S &x, const S &y)
     {
@@ -368,7 +348,7 @@ struct LogFwd {
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
             o.v[0][v] = x.v[0][v] + y.v[0][v];
-            lse2(y.v[0][v] + x.v[1][v], x.v[2][v], y.v[1][v], y.v[2][v], o.v[1][v], o.v[2][v]);
+            log_add(y.v[0][v] + x.v[1][v], x.v[2][v], y.v[1][v], y.v[2][v], o.v[1][v], o.v[2][v]);
         }
         return o;
     }
@@ -386,8 +366,8 @@ struct LogFwd {
             float h[VEC];
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
-                lse2(r.lc[i][v] + m[v], s[v], r.lv[i][v], 1.f, m[v], s[v]);
-                h[v] = s[v] * exp2f(m[v]);
+                log_add(r.lc[i][v] + m[v], s[v], r.lv[i][v], 1.f, m[v], s[v]);
+                h[v] = s[v] * ex2_sub(m[v] * kLog2eF);
             }
             const int64_t t = t0 + i;
             if (act && t < g.T) store_vec<VEC>(p.h + (bb * g.T + t) * g.D + d, h);
@@ -478,7 +458,7 @@ struct LogFwd {
 #define MG_LINB16_R 2
 #endif
 #ifndef MG_LOG_R
-#define MG_LOG_R 1
+#define MG_LOG_R 2
 #endif
 constexpr int kTX = 32, kTY = 8;
 using LinFwdF32 = ChanPlan<LinFwd<float, 4, MG_LINF_L>, MG_LINF_TX, MG_LINF_TY, MG_LINF_MB, MG_LINF_R>;

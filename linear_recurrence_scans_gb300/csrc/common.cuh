@@ -209,6 +209,37 @@ __device__ __forceinline__ void load_vec_cg(const float *p, float (&o)[VEC])
     }
 }
 
+// ------------------------------------------------------ log-space helpers
+// 2^x by the PTX instruction ex2.approx (relative error near 2^-22).  The ftz
+// form flushes subnormal results to zero (used for weights in [0, 1] whose
+// tiny values cannot matter); the plain form keeps subnormal results.
+__device__ __forceinline__ float ex2_ftz(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float ex2_sub(float x)
+{
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kLog2eF = 1.4426950408889634f;
+
+// log(xs e^u + ys e^ym) returned as (m, s), the value being s e^m (natural
+// logs; xs, ys >= 0 and finite).  m is the larger exponent, so one weight is
+// 1 and the other e^-|u - ym|.  Both exponents -inf (both terms zero) make the
+// gap NaN: the weight is then taken as 1 and m stays -inf, still the value 0.
+__device__ __forceinline__ void log_add(float u, float xs, float ym, float ys, float &m, float &s)
+{
+    const float gap = u - ym;
+    const float w = ex2_ftz(fminf(-fabsf(gap) * kLog2eF, 0.f));
+    const bool ge = gap >= 0.f;
+    m = ge ? u : ym;
+    s = ge ? fmaf(ys, w, xs) : fmaf(xs, w, ys);
+}
+
 // ------------------------------------------------- TMA bulk copies (1D)
 // One-dimensional bulk copies global -> shared completed on an mbarrier (the
 // Hopper/Blackwell async copy engine; no tensor map needed).  Addresses and

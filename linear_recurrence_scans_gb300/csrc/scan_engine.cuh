@@ -7,8 +7,9 @@
 // that re-runs those steps from a start state, writes the outputs and leaves
 // the state after the last step.  The engine does the rest: ticketed tiles of
 // DC = TX*VEC channels by TC = TY*L*R steps (R rounds of L steps per thread),
-// a shared-memory combine of the TY thread aggregates, the decoupled
-// look-back of warp 0, and the hand-off of each thread's start state.  kReverse ops walk time backwards (adjoint scans).
+// a shared-memory fold of the TY thread aggregates (which also leaves each
+// row its exclusive prefix within the tile), the decoupled look-back of warp
+// 0, and the hand-off of each thread's start state.  kReverse ops walk time backwards (adjoint scans).
 #pragma once
 
 #include "common.cuh"
@@ -194,12 +195,20 @@ __global__ void __launch_bounds__(TX *TY, MINB)
         const bool lchan = lact && ld < g.D;
         S cta = Op::identity();
         if (lact) {
+            // Fold the rows in processing order; each row but the first gets
+            // back the fold of the rows before it (its exclusive prefix
+            // within the tile), so every thread needs one combine below.
 #pragma unroll
             for (int k = 0; k < TY; ++k) {
                 const int y = Op::kReverse ? TY - 1 - k : k;
+                float *const row = &s_agg[(y * NS) * DC + lane * VEC];
                 S x;
 #pragma unroll
-                for (int s = 0; s < NS; ++s) load_vec<VEC>(&s_agg[((y) * NS + s) * DC + lane * VEC], x.v[s]);
+                for (int s = 0; s < NS; ++s) load_vec<VEC>(row + s * DC, x.v[s]);
+                if (k > 0) {
+#pragma unroll
+                    for (int s = 0; s < NS; ++s) store_vec<VEC>(row + s * DC, cta.v[s]);
+                }
                 cta = (k == 0) ? x : Op::combine(cta, x);
             }
         }
@@ -216,23 +225,15 @@ __global__ void __launch_bounds__(TX *TY, MINB)
     if (threadIdx.x < 32)
         publish_prefix<Op, TX>(g, lb, c, j, (threadIdx.x & 31) < TX, tile, epoch, excl, cta_keep);
 
+    // start state: carry o (rows before this one within the tile)
     S st;
 #pragma unroll
     for (int s = 0; s < NS; ++s) load_vec<VEC>(&s_carry[s * DC + tx * VEC], st.v[s]);
-    if (!Op::kReverse) {
-        for (int y = 0; y < ty; ++y) {
-            S x;
+    if (ty != (Op::kReverse ? TY - 1 : 0)) {
+        S x;
 #pragma unroll
-            for (int s = 0; s < NS; ++s) load_vec<VEC>(&s_agg[((y) * NS + s) * DC + tx * VEC], x.v[s]);
-            st = Op::combine(st, x);
-        }
-    } else {
-        for (int y = TY - 1; y > ty; --y) {
-            S x;
-#pragma unroll
-            for (int s = 0; s < NS; ++s) load_vec<VEC>(&s_agg[((y) * NS + s) * DC + tx * VEC], x.v[s]);
-            st = Op::combine(st, x);
-        }
+        for (int s = 0; s < NS; ++s) load_vec<VEC>(&s_agg[(ty * NS + s) * DC + tx * VEC], x.v[s]);
+        st = Op::combine(st, x);
     }
     // Pass 2: re-read the steps and re-run them from the start state; the
     // epilogue leaves in `st` the state after its round.

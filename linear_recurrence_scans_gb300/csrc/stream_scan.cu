@@ -10,7 +10,6 @@
 namespace mg {
 namespace {
 
-constexpr float kLog2eS = 1.4426950408889634f;
 
 // ----------------------------------------------------------- linear forward
 // Staged: 0 = a (row t), 1 = b (row t).  State (running product, h).
@@ -168,7 +167,7 @@ struct LinBwdT {
 
 // ------------------------------------------------------- log-space forward
 // Staged: 0 = log_coeffs (row t), 1 = log_values (row t+1 of T+1).  State
-// (la, m, s) in base-2 logs, value = s * 2^m.
+// (la, m, s) in natural logs, value = s * e^m.
 template <int NCW_, int L_, int NLB_, int SG_>
 struct LogFwdT {
     static constexpr int NS = 3, VEC = 4, NCW = NCW_, L = L_, NARR = 2;
@@ -200,23 +199,11 @@ struct LogFwdT {
             load_vec<VEC>(reinterpret_cast<const float *>(p.src[1].base) + (bb * (g.T + 1)) * g.D + d, l0);
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
-                e.v[1][v] = l0[v] * kLog2eS;
+                e.v[1][v] = l0[v];
                 e.v[2][v] = 1.f;
             }
         }
         return e;
-    }
-    __device__ static void lse2(float u, float xs, float ym, float ys, float &m, float &s)
-    {
-        const float gap = u - ym;
-        const float e = exp2f(-fabsf(gap));
-        const bool ge = gap >= 0.f;
-        m = ge ? u : ym;
-        s = ge ? fmaf(ys, e, xs) : fmaf(xs, e, ys);
-        if (gap != gap) {
-            m = -INFINITY;
-            s = 0.f;
-        }
     }
     __device__ static S combine(const S &x, const S &y)
     {
@@ -224,7 +211,7 @@ struct LogFwdT {
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
             o.v[0][v] = x.v[0][v] + y.v[0][v];
-            lse2(y.v[0][v] + x.v[1][v], x.v[2][v], y.v[1][v], y.v[2][v], o.v[1][v], o.v[2][v]);
+            log_add(y.v[0][v] + x.v[1][v], x.v[2][v], y.v[1][v], y.v[2][v], o.v[1][v], o.v[2][v]);
         }
         return o;
     }
@@ -244,11 +231,7 @@ struct LogFwdT {
         load_vec<VEC>(srow<LogFwdT, float>(st, 0, i, lane), e.v[0]);
         load_vec<VEC>(srow<LogFwdT, float>(st, 1, i, lane), e.v[1]);
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            e.v[0][v] *= kLog2eS;
-            e.v[1][v] *= kLog2eS;
-            e.v[2][v] = 1.f;
-        }
+        for (int v = 0; v < VEC; ++v) e.v[2][v] = 1.f;
         return e;
     }
     __device__ static void step2(const Args &p, const char *st, int i, int lane, int64_t t,
@@ -260,9 +243,8 @@ struct LogFwdT {
         load_vec<VEC>(srow<LogFwdT, float>(st, 1, i, lane), lv);
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
-            lse2(fmaf(lc[v], kLog2eS, state.v[1][v]), state.v[2][v], lv[v] * kLog2eS, 1.f,
-                 state.v[1][v], state.v[2][v]);
-            h[v] = state.v[2][v] * exp2f(state.v[1][v]);
+            log_add(lc[v] + state.v[1][v], state.v[2][v], lv[v], 1.f, state.v[1][v], state.v[2][v]);
+            h[v] = state.v[2][v] * ex2_sub(state.v[1][v] * kLog2eF);
         }
         if (act) store_vec<VEC>(p.h + (bb * g.T + t) * g.D + d, h);
     }

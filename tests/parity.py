@@ -15,9 +15,15 @@ with S_i the scale that rounding error is proportional to:
 * sums of signed terms in the channel-wise linear family (Bc, da, db): S is
   the same quantity evaluated by the oracle on |inputs| -- the componentwise
   condition scale sum |terms| of a sum of products;
-* matrix-valued affine outputs (Abar, Bbar, dA, dB): S is the RMS of the
-  k x k or k x v block at the same (b, t, n) -- products of matrices are
-  stable normwise, not entrywise.
+* matrix-valued affine outputs (Abar, Bbar, dA, dB) for k >= 2: S is the
+  RMS of the k x k or k x v block at the same (b, t, n) -- products of
+  matrices are stable normwise, not entrywise (the same chain with |A| in
+  place of A grows without bound for orthogonal A, so the componentwise scale
+  says nothing there);
+* affine outputs for k = 1: the scan is then the scalar linear recurrence
+  (one independent recurrence per column of B), and the 1 x 1 or 1 x v
+  "block" degenerates to |r| itself; S is the componentwise scale as for the
+  linear family, the oracle run on |inputs|.
 
 A NaN or inf where the reference is finite counts as an infinite error.
 """
@@ -92,12 +98,20 @@ def log_fwd_errors(lc, lv, h) -> dict:
 def affine_fwd_errors(A, Bm, Abar, Bbar) -> dict:
     import oracle
     rAbar, rBbar = oracle.affine_scan_fwd(A, Bm)
-    return {"Abar": scaled_error(_np(Abar), rAbar, block_rms(rAbar)),
-            "Bbar": scaled_error(_np(Bbar), rBbar, block_rms(rBbar))}
+    if _np(A).shape[-1] == 1:
+        SA, SB = oracle.affine_scan_fwd(np.abs(_np(A)), np.abs(_np(Bm)))
+    else:
+        SA, SB = block_rms(rAbar), block_rms(rBbar)
+    return {"Abar": scaled_error(_np(Abar), rAbar, SA),
+            "Bbar": scaled_error(_np(Bbar), rBbar, SB)}
 
 
 def affine_bwd_errors(A, Abar, Bbar, gAbar, gBbar, dA, dB) -> dict:
     import oracle
     rdA, rdB = oracle.affine_scan_bwd(A, Abar, Bbar, gAbar, gBbar)
-    return {"dA": scaled_error(_np(dA), rdA, block_rms(rdA)),
-            "dB": scaled_error(_np(dB), rdB, block_rms(rdB))}
+    if _np(A).shape[-1] == 1:
+        SA, SB = oracle.affine_scan_bwd(*(np.abs(_np(x)) for x in (A, Abar, Bbar, gAbar, gBbar)))
+    else:
+        SA, SB = block_rms(rdA), block_rms(rdB)
+    return {"dA": scaled_error(_np(dA), rdA, SA),
+            "dB": scaled_error(_np(dB), rdB, SB)}
