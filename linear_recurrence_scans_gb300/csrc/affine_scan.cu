@@ -21,6 +21,11 @@
 //     lane's rows of E_C straight from global memory.  A CTA of NW warps
 //     covers NW*L consecutive steps of one sequence and takes part in the
 //     same decoupled look-back as every other scan (lookback.cuh).
+#include <type_traits>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "stream_engine.cuh"
 
 namespace mg {
@@ -344,6 +349,418 @@ struct AffBwdSmall {
     }
 };
 
+// ============================= k <= 4: one sequence per lane, TMA-fed tiles
+// A tile is 32 consecutive sequences of one batch row x TC = NW*L steps; warp
+// w owns steps [w*L, (w+1)*L) of the tile, lane l sequence n0 + l, and keeps
+// that sequence's state in registers.  At one step the block's 32 matrices
+// are consecutive rows of a (rows = b*T*n + t*n + n_, S bytes) view of each
+// array, so every array of a step arrives with one 2D tensor copy (box = 32
+// rows) into a slot of the warp's ring (NSL slots, one mbarrier each).  The
+// copy swizzles 16-byte chunks within the S-byte rows (S = 32, 64 or 128),
+// so the 32 lanes reading one chunk of their own rows hit distinct banks.
+// Pass 1 folds the warp's steps into its aggregate; the warps' aggregates are
+// folded in shared memory (leaving each warp its exclusive prefix); warp 0
+// finds the tile's carry-in by decoupled look-back; pass 2 streams the same
+// steps again (now from L2) from each warp's start state and writes the
+// outputs.  Needs every per-sequence block to be 16..128 bytes: k = 4 with
+// v <= 8, or k = 2 with 2 <= v.
+
+// Swizzle of a tensor copy whose rows are `bytes` long (16: none).
+constexpr CUtensorMapSwizzle row_swizzle(int bytes)
+{
+    return bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+         : bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+         : bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+}
+
+// The E floats of lane `lane`'s row in a swizzled 32-row box (base aligned
+// to 1024 bytes): 16-byte chunk q of row r sits at chunk q ^ ((r*S >> 7) &
+// (S/16 - 1)) of that row, the pattern of the tensor-copy swizzle modes.
+template <int E>
+__device__ __forceinline__ void lane_row(const float *box, int lane, float *o)
+{
+    constexpr int S = E * 4, NQ = S / 16;
+    static_assert(S % 16 == 0 && S <= 128, "rows of 16..128 bytes");
+    const char *row = reinterpret_cast<const char *>(box) + lane * S;
+    const int sw = ((lane * S) >> 7) & (NQ - 1);
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        const float4 x = *reinterpret_cast<const float4 *>(row + 16 * (q ^ sw));
+        o[4 * q] = x.x;
+        o[4 * q + 1] = x.y;
+        o[4 * q + 2] = x.z;
+        o[4 * q + 3] = x.w;
+    }
+}
+
+__device__ __forceinline__ void tma_load_rows(void *dst, const CUtensorMap *map, int row,
+                                              unsigned long long *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        : : "r"(smem_addr(dst)), "l"(map), "r"(0), "r"(row), "r"(smem_addr(bar)) : "memory");
+}
+
+// Tensor maps of the staged arrays, in slot order.
+struct LaneMaps {
+    CUtensorMap m[5];
+};
+
+template <int K_, int V_, bool BWD_, int NW_, int L_, int NSL_>
+struct LCfg {
+    static constexpr int K = K_, VV = V_, L = L_, NSL = NSL_;
+    static constexpr bool BWD = BWD_;
+    static constexpr int KK = K * K, KV = K * VV;
+    using Op = typename std::conditional<BWD, AffBwdSmall<K, VV, 1>, AffFwdSmall<K, VV, 1>>::type;
+    static constexpr int NS = Op::NS, W = Op::W;
+    // Slot arrays (32 rows each, every region 1024-byte aligned).  Forward:
+    // A_t, B_t.  Backward: A_{t+1}, gAbar_t, gBbar_t, Abar_{t-1}, Bbar_{t-1}.
+    static constexpr int NARR = BWD ? 5 : 2;
+    static constexpr int elems(int a) { return BWD ? ((a == 2 || a == 4) ? KV : KK) : (a == 1 ? KV : KK); }
+    static constexpr int region(int a) { return (32 * elems(a) + 255) / 256 * 256; }  // floats
+    static constexpr int offset(int a) { return a == 0 ? 0 : offset(a - 1) + region(a - 1); }
+    static constexpr int STEP = offset(NARR);  // floats per slot
+    static constexpr size_t smem_for(int nw)
+    {
+        return 1024 + size_t(nw * NSL * STEP) * sizeof(float) +
+               size_t((nw + 1) * NS * 32) * sizeof(float) + size_t(nw * NSL) * 8;
+    }
+    // warps per CTA: NW_, halved while the CTA would not fit in shared memory
+    static constexpr size_t kMax = 225 * 1024;
+    static constexpr int NW = smem_for(NW_) <= kMax ? NW_
+                              : smem_for(NW_ / 2) <= kMax ? NW_ / 2
+                              : smem_for(NW_ / 4) <= kMax ? NW_ / 4 : 1;
+    static constexpr int TC = NW * L;
+    static constexpr size_t SMEM = smem_for(NW);
+    static_assert(SMEM <= kMax, "tile does not fit in shared memory");
+};
+
+template <int K, int V>
+constexpr bool lane_kernel_ok()
+{
+    return K <= 4 && (K * K * 4) % 16 == 0 && (K * V * 4) % 16 == 0 && K * K * 4 <= 128 &&
+           K * V * 4 <= 128;
+}
+
+template <class Cf>
+__global__ void __launch_bounds__(Cf::NW * 32)
+    affine_lane_kernel(const typename Cf::Op::Args args, const __grid_constant__ LaneMaps maps,
+                       const ChanGeom g, const Lookback lb)
+{
+    using Op = typename Cf::Op;
+    using S = typename Op::S;
+    constexpr int K = Cf::K, KK = Cf::KK, KV = Cf::KV, VV = Cf::VV, NS = Cf::NS, W = Cf::W;
+    constexpr int NW = Cf::NW, L = Cf::L, NSL = Cf::NSL, STEP = Cf::STEP, NARR = Cf::NARR;
+    extern __shared__ float4 lane_smem[];
+    // ring first, 1024-byte aligned for the swizzle, then the rest
+    float *const ring = reinterpret_cast<float *>(
+        (reinterpret_cast<uintptr_t>(lane_smem) + 1023) & ~uintptr_t(1023));  // [NW][NSL][STEP]
+    float *const s_agg = ring + NW * NSL * STEP;                                // [NW][NS][32]
+    float *const s_carry = s_agg + NW * NS * 32;                                // [NS][32]
+    unsigned long long *const bars =
+        reinterpret_cast<unsigned long long *>(s_carry + NS * 32);             // [NW][NSL]
+
+    unsigned tile;
+    unsigned long long epoch;
+    take_ticket(lb, tile, epoch);
+    if (tile >= g.n_tiles) {
+        if (threadIdx.x == 0) atomicOr(&lb.ctl->error, kErrBadTicket);
+        finish_cta(lb, epoch);
+        return;
+    }
+    const int c = int(tile / unsigned(g.nJ));
+    const int j = int(tile % unsigned(g.nJ));
+    const int64_t bb = j / g.nJb;
+    const int n0 = (j % g.nJb) * 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int d = n0 + lane;                         // this lane's sequence in the row
+    const bool act = d < g.D;
+    const int ct = Cf::BWD ? (g.nC - 1 - c) : c;
+    const int64_t t0 = int64_t(ct) * Cf::TC;
+    const int nv = int(g.T - t0 < Cf::TC ? g.T - t0 : Cf::TC);
+    const int wbase = warp * L;
+    const int nvw = nv - wbase < 0 ? 0 : (nv - wbase < L ? nv - wbase : L);
+    const int pw = Cf::BWD ? NW - 1 - warp : warp;  // position in processing order
+    unsigned long long *const wbar = bars + warp * NSL;
+    float *const wring = ring + warp * NSL * STEP;
+    auto row = [&](int64_t t) { return (bb * g.T + t) * g.D + n0; };  // row of lane 0
+    auto tile_step = [&](int q) {
+        const int k = q < nvw ? q : q - nvw;
+        return Cf::BWD ? wbase + nvw - 1 - k : wbase + k;
+    };
+    const int nq = 2 * nvw;
+
+    auto issue = [&](int q) {  // lane 0
+        if (q >= nq) return;
+        unsigned long long *bar = wbar + q % NSL;
+        float *buf = wring + (q % NSL) * STEP;
+        const int64_t t = t0 + tile_step(q);
+        const int r = int(row(t));
+        if constexpr (!Cf::BWD) {
+            mbar_arrive_expect_tx(bar, 32 * (KK + KV) * 4);
+            tma_load_rows(buf + Cf::offset(0), &maps.m[0], r, bar);
+            tma_load_rows(buf + Cf::offset(1), &maps.m[1], r, bar);
+        } else {
+            const bool next = t + 1 < g.T, prev = q >= nvw && t >= 1;
+            mbar_arrive_expect_tx(bar, 32 * 4 * ((KK + KV) + (next ? KK : 0) + (prev ? KK + KV : 0)));
+            tma_load_rows(buf + Cf::offset(1), &maps.m[1], r, bar);
+            tma_load_rows(buf + Cf::offset(2), &maps.m[2], r, bar);
+            if (next) tma_load_rows(buf + Cf::offset(0), &maps.m[0], r + int(g.D), bar);
+            if (prev) {
+                tma_load_rows(buf + Cf::offset(3), &maps.m[3], r - int(g.D), bar);
+                tma_load_rows(buf + Cf::offset(4), &maps.m[4], r - int(g.D), bar);
+            }
+        }
+    };
+    auto wait_slot = [&](int q) -> const float * {
+        unsigned long long *bar = wbar + q % NSL;
+        const unsigned parity = unsigned(q / NSL) & 1u;
+        if (!mbar_wait_bounded(bar, parity, lb.wait_limit_ns)) {
+            if (lane == 0) atomicOr(&lb.ctl->error, kErrLookbackTimeout);
+            mbar_wait_bounded(bar, parity, lb.wait_limit_ns);
+        }
+        return wring + (q % NSL) * STEP;
+    };
+    // the lane's element of a step: coefficient E (k x k) and value (k x W)
+    auto element = [&](const float *slot, int64_t t, S &e) {
+        float *f = &e.v[0][0];
+        if constexpr (!Cf::BWD) {
+            lane_row<KK>(slot + Cf::offset(0), lane, f);
+            lane_row<KV>(slot + Cf::offset(1), lane, f + KK);
+        } else {
+            if (t + 1 < g.T) {  // E = A_{t+1}^T
+                float a[KK];
+                lane_row<KK>(slot + Cf::offset(0), lane, a);
+#pragma unroll
+                for (int r = 0; r < K; ++r)
+#pragma unroll
+                    for (int q = 0; q < K; ++q) f[r * K + q] = a[q * K + r];
+            } else {
+#pragma unroll
+                for (int q = 0; q < KK; ++q) f[q] = 0.f;
+            }
+            float ga[KK], gb[KV];
+            lane_row<KK>(slot + Cf::offset(1), lane, ga);
+            lane_row<KV>(slot + Cf::offset(2), lane, gb);
+#pragma unroll
+            for (int r = 0; r < K; ++r) {
+#pragma unroll
+                for (int q = 0; q < K; ++q) f[KK + r * W + q] = ga[r * K + q];
+#pragma unroll
+                for (int q = 0; q < VV; ++q) f[KK + r * W + K + q] = gb[r * VV + q];
+            }
+        }
+    };
+
+    if (lane == 0) {
+        for (int q = 0; q < NSL; ++q) mbar_init(wbar + q, 1);
+        for (int q = 0; q < NSL; ++q) issue(q);
+    }
+    __syncwarp();
+
+    // ---- pass 1: the warp's aggregate, in processing order
+    S agg = Op::identity();
+#pragma unroll 1
+    for (int q = 0; q < nvw; ++q) {
+        const int64_t t = t0 + tile_step(q);
+        const float *slot = wait_slot(q);
+        S e;
+        if (act) element(slot, t, e);
+        __syncwarp();
+        if (lane == 0) issue(q + NSL);
+        if (act) agg = Op::combine(agg, e);
+    }
+#pragma unroll
+    for (int s = 0; s < NS; ++s) s_agg[(pw * NS + s) * 32 + lane] = agg.v[s][0];
+    __syncthreads();
+
+    // ---- warp 0: fold the warps' aggregates (each row gets its exclusive
+    //      prefix back), then the look-back for the tile's carry-in
+    S excl = Op::identity(), cta = Op::identity();
+    if (warp == 0) {
+#pragma unroll 1
+        for (int w = 0; w < NW; ++w) {
+            S x;
+#pragma unroll
+            for (int s = 0; s < NS; ++s) x.v[s][0] = s_agg[(w * NS + s) * 32 + lane];
+            if (w > 0) {
+#pragma unroll
+                for (int s = 0; s < NS; ++s) s_agg[(w * NS + s) * 32 + lane] = cta.v[s][0];
+            }
+            cta = (w == 0) ? x : Op::combine(cta, x);
+        }
+        publish_first<Op, 32>(args, g, lb, c, j, bb, d, true, act, tile, epoch, cta);
+        excl = find_carry<Op, 32>(args, g, lb, c, j, bb, d, true, act, tile, epoch);
+#pragma unroll
+        for (int s = 0; s < NS; ++s) s_carry[s * 32 + lane] = excl.v[s][0];
+    }
+    __syncthreads();
+    if (warp == 0) publish_prefix<Op, 32>(g, lb, c, j, true, tile, epoch, excl, cta);
+
+    // ---- start state of this warp: carry o (warps before it)
+    S st;
+#pragma unroll
+    for (int s = 0; s < NS; ++s) st.v[s][0] = s_carry[s * 32 + lane];
+    if (pw > 0) {
+        S x;
+#pragma unroll
+        for (int s = 0; s < NS; ++s) x.v[s][0] = s_agg[(pw * NS + s) * 32 + lane];
+        st = Op::combine(st, x);
+    }
+
+    // ---- pass 2: re-run the steps from the start state, write the outputs
+#pragma unroll 1
+    for (int q = nvw; q < nq; ++q) {
+        const int64_t t = t0 + tile_step(q), sidx = row(t) + lane;
+        const float *slot = wait_slot(q);
+        if constexpr (!Cf::BWD) {
+            S e;
+            if (act) element(slot, t, e);
+            __syncwarp();
+            if (lane == 0) issue(q + NSL);
+            if (act) {
+                st = Op::combine(st, e);
+                st_floats<KK>(args.Abar + sidx * KK, &st.v[0][0]);
+                st_floats<KV>(args.Bbar + sidx * KV, &st.v[KK][0]);
+            }
+        } else {
+            if (act) {
+                S e;
+                element(slot, t, e);
+                float *V = &st.v[KK][0];
+                float nV[K * W];
+                mm_add<K, K, W>(&e.v[0][0], V, &e.v[KK][0], nV);
+#pragma unroll
+                for (int q2 = 0; q2 < K * W; ++q2) V[q2] = nV[q2];
+                // dB_t = Lam_t;  dA_t = M_t Abar_{t-1}^T + Lam_t Bbar_{t-1}^T
+                float dB[KV], dA[KK];
+#pragma unroll
+                for (int a = 0; a < K; ++a)
+#pragma unroll
+                    for (int b2 = 0; b2 < VV; ++b2) dB[a * VV + b2] = V[a * W + K + b2];
+                if (t > 0) {
+                    float Ap[KK], Bp[KV];
+                    lane_row<KK>(slot + Cf::offset(3), lane, Ap);
+                    lane_row<KV>(slot + Cf::offset(4), lane, Bp);
+#pragma unroll
+                    for (int a = 0; a < K; ++a)
+#pragma unroll
+                        for (int b2 = 0; b2 < K; ++b2) {
+                            float acc = V[a * W] * Ap[b2 * K];
+#pragma unroll
+                            for (int l = 1; l < K; ++l) acc = fmaf(V[a * W + l], Ap[b2 * K + l], acc);
+#pragma unroll
+                            for (int l = 0; l < VV; ++l) acc = fmaf(V[a * W + K + l], Bp[b2 * VV + l], acc);
+                            dA[a * K + b2] = acc;
+                        }
+                } else {
+#pragma unroll
+                    for (int a = 0; a < K; ++a)
+#pragma unroll
+                        for (int b2 = 0; b2 < K; ++b2) dA[a * K + b2] = V[a * W + b2];
+                }
+                st_floats<KK>(args.dA + sidx * KK, dA);
+                st_floats<KV>(args.dB + sidx * KV, dB);
+            }
+            __syncwarp();  // every lane has read the slot
+            if (lane == 0) issue(q + NSL);
+        }
+    }
+    finish_cta(lb, epoch);
+}
+
+// cuTensorMapEncodeTiled from the driver, found once through the runtime.
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// A (rows x E floats) view of `base` copied 32 rows at a time, swizzled.
+inline bool encode_rows_map(CUtensorMap *m, const float *base, int E, int64_t rows)
+{
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(E), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(E) * 4};
+    const cuuint32_t box[2] = {cuuint32_t(E), 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, row_swizzle(E * 4),
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <class Cf>
+struct LanePlan {
+    static ChanGeom geom(int64_t B, int64_t T, int64_t n)
+    {
+        ChanGeom g;
+        g.B = B;
+        g.T = T;
+        g.D = n;
+        g.nJb = int((n + 31) / 32);
+        g.nJ = int(B * g.nJb);
+        g.nC = int((T + Cf::TC - 1) / Cf::TC);
+        g.n_tiles = unsigned(g.nJ) * unsigned(g.nC);
+        return g;
+    }
+    static size_t n_tiles(int64_t B, int64_t T, int64_t n)
+    {
+        return size_t(B * ((n + 31) / 32)) * size_t((T + Cf::TC - 1) / Cf::TC);
+    }
+    static size_t ws_bytes(int64_t B, int64_t T, int64_t n)
+    {
+        return tiled_ws_bytes(n_tiles(B, T, n), size_t(2) * Cf::NS * 32 * sizeof(float));
+    }
+    // rows of the tensor views must be addressable with 32-bit coordinates
+    static bool fits(int64_t B, int64_t T, int64_t n) { return B * T * n < (int64_t(1) << 31) - 64; }
+    static mg_status launch(const typename Cf::Op::Args &args, int64_t B, int64_t T, int64_t n,
+                            void *ws, size_t wsb, cudaStream_t s, const LaunchOpts &o,
+                            const char *name)
+    {
+        const size_t nt = n_tiles(B, T, n);
+        if (nt >= (size_t(1) << 31) || B * ((n + 31) / 32) >= (int64_t(1) << 31))
+            return fail(MG_ERR_UNSUPPORTED, "%s: %zu tiles exceed the 2^31 ticket range", name, nt);
+        const size_t need = ws_bytes(B, T, n);
+        if (wsb < need)
+            return fail(MG_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", name, wsb, need);
+        LaneMaps maps;
+        const int64_t rows = B * T * n;
+        bool ok;
+        if constexpr (!Cf::BWD) {
+            ok = encode_rows_map(&maps.m[0], args.A, Cf::KK, rows) &&
+                 encode_rows_map(&maps.m[1], args.Bm, Cf::KV, rows);
+        } else {
+            ok = encode_rows_map(&maps.m[0], args.A, Cf::KK, rows) &&
+                 encode_rows_map(&maps.m[1], args.gAbar, Cf::KK, rows) &&
+                 encode_rows_map(&maps.m[2], args.gBbar, Cf::KV, rows) &&
+                 encode_rows_map(&maps.m[3], args.Abar, Cf::KK, rows) &&
+                 encode_rows_map(&maps.m[4], args.Bbar, Cf::KV, rows);
+        }
+        if (!ok) return fail(MG_ERR_LAUNCH, "%s: could not encode the tensor maps", name);
+        const ChanGeom g = geom(B, T, n);
+        const Lookback lb = make_lookback(ws, nt, o);
+        static const cudaError_t attr = cudaFuncSetAttribute(
+            affine_lane_kernel<Cf>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cf::SMEM));
+        if (attr != cudaSuccess) return fail(MG_ERR_LAUNCH, "%s: %s", name, cudaGetErrorString(attr));
+        affine_lane_kernel<Cf><<<unsigned(nt), Cf::NW * 32, Cf::SMEM, s>>>(args, maps, g, lb);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return fail(MG_ERR_LAUNCH, "%s: launch failed: %s", name, cudaGetErrorString(e));
+        return MG_OK;
+    }
+};
+
 // ============================================ k <= 4 on the streaming engine
 // One sequence per lane: a tile is 32 consecutive sequences x TC steps, and at
 // one step those sequences' matrices are contiguous, so each staged row is one
@@ -550,9 +967,9 @@ bool aff_stream_ok(int64_t n)
 
 // ============================================================ k in {8, 16}
 
-template <int K_, int W_, bool BWD_, int NW_, int L_, bool DB_>
+template <int K_, int W_, bool BWD_, int NW_, int L_, bool DB_, int NSL_>
 struct WCfg {
-    static constexpr int K = K_, W = W_, NW = NW_, L = L_;
+    static constexpr int K = K_, W = W_, NW = NW_, L = L_, NSL = NSL_;
     static constexpr bool BWD = BWD_, DB = DB_;  // DB: double-buffered state exchange
     static constexpr int VV = BWD ? W - K : W;  // v
     static constexpr int KK = K * K, KV = K * VV;
@@ -563,17 +980,19 @@ struct WCfg {
     static constexpr int XS = NCP;              // shared row stride (floats)
     static constexpr int MAT = K * XS;          // floats per shared state matrix
     static constexpr int REC = K * NC;          // floats per global record
-    static constexpr int TC = NW * L;           // steps per tile
-    static constexpr int JD = K >= 8 ? K / 8 : 1;  // dA columns per lane (lanes cb*JD < K)
-    // Staged inputs of the tile's TC steps, region-major, each step block a
-    // multiple of 16 bytes.  Forward: A_t, B_t.  Backward: A_{t+1}, gAbar_t,
-    // gBbar_t, Abar_{t-1}, Bbar_{t-1}.
+    static constexpr int TC = NW * L;           // steps per tile (L per warp)
+    static constexpr int JD = K / 8;            // dA columns per lane (8 column blocks)
+    // One ring slot holds the inputs of one step.  Forward: A_t, B_t.
+    // Backward: A_{t+1}, gAbar_t, gBbar_t, Abar_{t-1}, Bbar_{t-1}.  Each block
+    // is a multiple of 16 bytes.
     static constexpr int STEP = BWD ? 3 * KK + 2 * KV : KK + KV;
-    static constexpr int STAGE = TC * STEP;
+    static constexpr int OFF_G = KK, OFF_GB = 2 * KK, OFF_AP = 2 * KK + KV, OFF_BP = 3 * KK + KV;
     static constexpr int NXB = DB ? 2 : 1;
-    static constexpr size_t SMEM =
-        16 + size_t(STAGE) * sizeof(float) + size_t((NXB + 1) * NW + 1) * MAT * sizeof(float);
-    static_assert(K >= 4 && K % 4 == 0, "warp kernel needs k in {4, 8, 16}");
+    static constexpr int BAR_FLOATS = (NW * NSL * 2 + 3) / 4 * 4;  // mbarriers, 16-byte padded
+    static constexpr size_t SMEM = size_t(BAR_FLOATS + NW * NSL * STEP) * sizeof(float) +
+                                   size_t((NXB + 1) * NW + 1) * MAT * sizeof(float);
+    static_assert(K == 8 || K == 16, "warp kernel is for k in {8, 16}");
+    static_assert(NSL >= 2, "the ring needs two slots at least");
     static_assert((KV * 4) % 16 == 0 && (KK * 4) % 16 == 0, "bulk copies need 16-byte blocks");
 };
 
@@ -593,6 +1012,9 @@ struct AffPtrs {
 
 // Lane block of the combine (x earlier, full matrix in shared memory) o
 // (y later, rows `yc` = y.C[rows][0..K) and `yv` = y.V on the lane's columns).
+#ifndef MG_AFW_HOIST
+#define MG_AFW_HOIST 0
+#endif
 template <class Cf>
 __device__ __forceinline__ void block_gemm(const float *xs, const float (&yc)[Cf::R][Cf::K],
                                            const float (&yv)[Cf::R][Cf::CC], int cb,
@@ -602,14 +1024,27 @@ __device__ __forceinline__ void block_gemm(const float *xs, const float (&yc)[Cf
     for (int r = 0; r < Cf::R; ++r)
 #pragma unroll
         for (int c = 0; c < Cf::CC; ++c) o[r][c] = yv[r][c];
+    if constexpr (MG_AFW_HOIST != 0) {
+        // every row of X first, then the FMAs with no load in between
+        float xv[Cf::K][Cf::CC];
 #pragma unroll
-    for (int l = 0; l < Cf::K; ++l) {
-        float xv[Cf::CC];
-        ld_floats<Cf::CC>(xs + l * Cf::XS + cb * Cf::CC, xv);
+        for (int l = 0; l < Cf::K; ++l) ld_floats<Cf::CC>(xs + l * Cf::XS + cb * Cf::CC, xv[l]);
 #pragma unroll
-        for (int r = 0; r < Cf::R; ++r)
+        for (int l = 0; l < Cf::K; ++l)
 #pragma unroll
-            for (int c = 0; c < Cf::CC; ++c) o[r][c] = fmaf(yc[r][l], xv[c], o[r][c]);
+            for (int r = 0; r < Cf::R; ++r)
+#pragma unroll
+                for (int c = 0; c < Cf::CC; ++c) o[r][c] = fmaf(yc[r][l], xv[l][c], o[r][c]);
+    } else {
+#pragma unroll
+        for (int l = 0; l < Cf::K; ++l) {
+            float xv[Cf::CC];
+            ld_floats<Cf::CC>(xs + l * Cf::XS + cb * Cf::CC, xv);
+#pragma unroll
+            for (int r = 0; r < Cf::R; ++r)
+#pragma unroll
+                for (int c = 0; c < Cf::CC; ++c) o[r][c] = fmaf(yc[r][l], xv[c], o[r][c]);
+        }
     }
 }
 
@@ -632,29 +1067,43 @@ __device__ __forceinline__ void load_y(const float *m, int ld, int rb, int cb,
     }
 }
 
-// The staged element of tile step i as a y operand.  `has_next`: step t+1
+// The element held in a ring slot as a y operand.  `has_next`: step t+1
 // exists (the adjoint's coefficient A_{t+1}^T is zero at t = T-1).
 template <class Cf>
-__device__ __forceinline__ void load_elem(const float *stage, int i, bool has_next, int rb, int cb,
+__device__ __forceinline__ void load_elem(const float *slot, bool has_next, int rb, int cb,
                                           float (&yc)[Cf::R][Cf::K], float (&yv)[Cf::R][Cf::CC])
 {
-    constexpr int K = Cf::K, KK = Cf::KK, KV = Cf::KV, VV = Cf::VV, R = Cf::R, TC = Cf::TC;
+    constexpr int K = Cf::K, KK = Cf::KK, VV = Cf::VV, R = Cf::R;
     if constexpr (!Cf::BWD) {
-        const float *At = stage + i * KK;
-        const float *Bt = stage + TC * KK + i * KV;
+        const float *At = slot;
+        const float *Bt = slot + KK;
 #pragma unroll
         for (int r = 0; r < R; ++r) ld_floats<K>(At + (rb * R + r) * K, yc[r]);
+        if constexpr (K % Cf::CC == 0 && VV % Cf::CC == 0) {
+            // a lane's columns lie wholly in the C part (zero) or in B_t
+            const int col = cb * Cf::CC;
 #pragma unroll
-        for (int r = 0; r < R; ++r)
+            for (int r = 0; r < R; ++r) {
+                if (col >= K) {
+                    ld_floats<Cf::CC>(Bt + (rb * R + r) * VV + col - K, yv[r]);
+                } else {
 #pragma unroll
-            for (int c = 0; c < Cf::CC; ++c) {
-                const int col = cb * Cf::CC + c;
-                yv[r][c] = (col >= K && col < Cf::NC) ? Bt[(rb * R + r) * VV + col - K] : 0.f;
+                    for (int c = 0; c < Cf::CC; ++c) yv[r][c] = 0.f;
+                }
             }
+        } else {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int c = 0; c < Cf::CC; ++c) {
+                    const int col = cb * Cf::CC + c;
+                    yv[r][c] = (col >= K && col < Cf::NC) ? Bt[(rb * R + r) * VV + col - K] : 0.f;
+                }
+        }
     } else {
-        const float *An = stage + i * KK;
-        const float *ga = stage + TC * KK + i * KK;
-        const float *gb = stage + 2 * TC * KK + i * KV;
+        const float *An = slot;
+        const float *ga = slot + Cf::OFF_G;
+        const float *gb = slot + Cf::OFF_GB;
         if (has_next) {  // E_C[row][l] = A_{t+1}[l][row]
 #pragma unroll
             for (int l = 0; l < K; ++l) {
@@ -746,18 +1195,25 @@ __device__ __forceinline__ void warp_step(float *xw, int &cur, const float (&yc)
     }
 }
 
+// One tile = one sequence x TC steps, warp w owning L consecutive steps.
+// Each warp streams its steps through its own ring of NSL slots (1D bulk
+// copies completing on one mbarrier per slot): pass 1 folds them into the
+// warp's aggregate, pass 2 streams them again (now from L2) and writes the
+// outputs.  Both passes form one issue sequence, so the first loads of pass 2
+// are in flight while warp 0 does the look-back.
 template <class Cf>
 __global__ void __launch_bounds__(Cf::NW * 32)
     affine_warp_kernel(const AffPtrs p, const AffGeom g, const Lookback lb)
 {
     constexpr int K = Cf::K, R = Cf::R, CC = Cf::CC, NW = Cf::NW, L = Cf::L, MAT = Cf::MAT;
-    constexpr int XS = Cf::XS, NC = Cf::NC, VV = Cf::VV, KK = Cf::KK, KV = Cf::KV, TC = Cf::TC;
+    constexpr int XS = Cf::XS, NC = Cf::NC, VV = Cf::VV, KK = Cf::KK, KV = Cf::KV;
+    constexpr int NSL = Cf::NSL, STEP = Cf::STEP;
     extern __shared__ float4 aff_smem[];
-    unsigned long long *const bar = reinterpret_cast<unsigned long long *>(aff_smem);
-    float *const stage = reinterpret_cast<float *>(aff_smem) + 4;       // [STAGE]
-    float *const xb = stage + Cf::STAGE;                                // [NW][NXB][MAT]
-    float *const G = xb + NW * Cf::NXB * MAT;                           // [NW][MAT]
-    float *const carry = G + NW * MAT;                                  // [MAT]
+    unsigned long long *const bars = reinterpret_cast<unsigned long long *>(aff_smem);  // [NW][NSL]
+    float *const ring = reinterpret_cast<float *>(aff_smem) + Cf::BAR_FLOATS;          // [NW][NSL][STEP]
+    float *const xb = ring + NW * NSL * STEP;                                          // [NW][NXB][MAT]
+    float *const G = xb + NW * Cf::NXB * MAT;                                          // [NW][MAT]
+    float *const carry = G + NW * MAT;                                                 // [MAT]
 
     unsigned tile;
     unsigned long long epoch;
@@ -773,67 +1229,77 @@ __global__ void __launch_bounds__(Cf::NW * 32)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rb = lane >> 3, cb = lane & 7;
     const int ct = Cf::BWD ? (g.nC - 1 - c) : c;
-    const int64_t t0 = int64_t(ct) * TC;           // first step of the tile
-    const int nv = int(g.T - t0 < TC ? g.T - t0 : TC);  // valid steps in the tile
+    const int64_t t0 = int64_t(ct) * Cf::TC;        // first step of the tile
+    const int nv = int(g.T - t0 < Cf::TC ? g.T - t0 : Cf::TC);  // valid steps in the tile
+    const int wbase = warp * L;                     // first tile step of this warp
+    const int nvw = nv - wbase < 0 ? 0 : (nv - wbase < L ? nv - wbase : L);  // its valid steps
+    const int pw = Cf::BWD ? NW - 1 - warp : warp;  // position in processing order
     float *const xw = xb + warp * Cf::NXB * MAT;
+    unsigned long long *const wbar = bars + warp * NSL;
+    float *const wring = ring + warp * NSL * STEP;
     auto step_index = [&](int64_t t) { return (bb * g.T + t) * g.n + nn; };
+    // issue-sequence entry q: pass 1 for q < nvw, pass 2 after; the tile step
+    // in processing order (reverse time for the adjoint)
+    auto tile_step = [&](int q) {
+        const int k = q < nvw ? q : q - nvw;
+        return Cf::BWD ? wbase + nvw - 1 - k : wbase + k;
+    };
+    const int nq = 2 * nvw;
 
-    // ---- stage the tile's inputs with 1D bulk copies (warp 0), one mbarrier
-    if (threadIdx.x == 0) mbar_init(bar, 1);
-    __syncthreads();
-    if (warp == 0) {
-        unsigned bytes = 0;
-        for (int i = lane; i < nv; i += 32) {
-            const int64_t t = t0 + i;
-            if constexpr (!Cf::BWD) {
-                bytes += (KK + KV) * 4;
-            } else {
-                bytes += (KK + KV) * 4;                    // gAbar_t, gBbar_t
-                if (t + 1 < g.T) bytes += KK * 4;          // A_{t+1}
-                if (t >= 1) bytes += (KK + KV) * 4;        // Abar_{t-1}, Bbar_{t-1}
+    // lane 0 of each warp: arm slot q % NSL and start its copies
+    auto issue = [&](int q) {
+        if (q >= nq) return;
+        unsigned long long *bar = wbar + q % NSL;
+        float *buf = wring + (q % NSL) * STEP;
+        const int64_t t = t0 + tile_step(q), s = step_index(t);
+        if constexpr (!Cf::BWD) {
+            mbar_arrive_expect_tx(bar, (KK + KV) * 4);
+            tma_load_1d(buf, p.A + s * KK, KK * 4, bar);
+            tma_load_1d(buf + KK, p.Bm + s * KV, KV * 4, bar);
+        } else {
+            const bool next = t + 1 < g.T, prev = q >= nvw && t >= 1;
+            mbar_arrive_expect_tx(bar, (KK + KV + (next ? KK : 0) + (prev ? KK + KV : 0)) * 4);
+            tma_load_1d(buf + Cf::OFF_G, p.gAbar + s * KK, KK * 4, bar);
+            tma_load_1d(buf + Cf::OFF_GB, p.gBbar + s * KV, KV * 4, bar);
+            if (next) tma_load_1d(buf, p.A + (s + g.n) * KK, KK * 4, bar);
+            if (prev) {
+                tma_load_1d(buf + Cf::OFF_AP, p.Abar + (s - g.n) * KK, KK * 4, bar);
+                tma_load_1d(buf + Cf::OFF_BP, p.Bbar + (s - g.n) * KV, KV * 4, bar);
             }
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, off);
-        if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
-        __syncwarp();
-        for (int i = lane; i < nv; i += 32) {
-            const int64_t t = t0 + i, s = step_index(t);
-            if constexpr (!Cf::BWD) {
-                tma_load_1d(stage + i * KK, p.A + s * KK, KK * 4, bar);
-                tma_load_1d(stage + TC * KK + i * KV, p.Bm + s * KV, KV * 4, bar);
-            } else {
-                tma_load_1d(stage + TC * KK + i * KK, p.gAbar + s * KK, KK * 4, bar);
-                tma_load_1d(stage + 2 * TC * KK + i * KV, p.gBbar + s * KV, KV * 4, bar);
-                if (t + 1 < g.T) tma_load_1d(stage + i * KK, p.A + (s + g.n) * KK, KK * 4, bar);
-                if (t >= 1) {
-                    tma_load_1d(stage + 2 * TC * KK + TC * KV + i * KK, p.Abar + (s - g.n) * KK,
-                                KK * 4, bar);
-                    tma_load_1d(stage + 3 * TC * KK + TC * KV + i * KV, p.Bbar + (s - g.n) * KV,
-                                KV * 4, bar);
-                }
-            }
+    };
+    // every lane: wait for entry q (bounded; a second bounded wait after a
+    // timeout lets the copies land before the slot is reused or the CTA ends)
+    auto wait_slot = [&](int q) -> const float * {
+        unsigned long long *bar = wbar + q % NSL;
+        const unsigned parity = unsigned(q / NSL) & 1u;
+        if (!mbar_wait_bounded(bar, parity, lb.wait_limit_ns)) {
+            if (lane == 0) atomicOr(&lb.ctl->error, kErrLookbackTimeout);
+            mbar_wait_bounded(bar, parity, lb.wait_limit_ns);
         }
+        return wring + (q % NSL) * STEP;
+    };
+
+    if (lane == 0) {
+        for (int q = 0; q < NSL; ++q) mbar_init(wbar + q, 1);
+        for (int q = 0; q < NSL; ++q) issue(q);
     }
-    if (!mbar_wait_bounded(bar, 0, lb.wait_limit_ns)) {
-        atomicOr(&lb.ctl->error, kErrLookbackTimeout);
-        mbar_wait_bounded(bar, 0, lb.wait_limit_ns);  // let copies in flight land
-    }
+    __syncwarp();
 
     float yc[R][K], yv[R][CC], o[R][CC];
-    const int pw = Cf::BWD ? NW - 1 - warp : warp;  // position in processing order
-    const int wbase = warp * L;                     // first tile step of this warp
 
-    // ---- pass 1: aggregate of the warp's L steps, in processing order
+    // ---- pass 1: aggregate of the warp's steps, in processing order
     int cur = 0;
     identity_block<Cf>(rb, cb, o);
     put_block_smem<Cf>(xw, rb, cb, o);
     __syncwarp();
 #pragma unroll 1
-    for (int k = 0; k < L; ++k) {
-        const int i = wbase + (Cf::BWD ? L - 1 - k : k);
-        if (i >= nv) continue;  // padding steps are the identity
-        load_elem<Cf>(stage, i, t0 + i + 1 < g.T, rb, cb, yc, yv);
+    for (int q = 0; q < nvw; ++q) {
+        const int64_t t = t0 + tile_step(q);
+        const float *slot = wait_slot(q);
+        load_elem<Cf>(slot, t + 1 < g.T, rb, cb, yc, yv);
+        __syncwarp();  // every lane has read the slot
+        if (lane == 0) issue(q + NSL);
         warp_step<Cf>(xw, cur, yc, yv, rb, cb, o);
     }
     put_block_smem<Cf>(G + pw * MAT, rb, cb, o);
@@ -908,11 +1374,14 @@ __global__ void __launch_bounds__(Cf::NW * 32)
 
     // ---- pass 2: re-run the warp's steps from its start state, write outputs
 #pragma unroll 1
-    for (int k = 0; k < L; ++k) {
-        const int i = wbase + (Cf::BWD ? L - 1 - k : k);
-        if (i >= nv) continue;
-        const int64_t t = t0 + i, s = step_index(t);
-        load_elem<Cf>(stage, i, t + 1 < g.T, rb, cb, yc, yv);
+    for (int q = nvw; q < nq; ++q) {
+        const int64_t t = t0 + tile_step(q), s = step_index(t);
+        const float *slot = wait_slot(q);
+        load_elem<Cf>(slot, t + 1 < g.T, rb, cb, yc, yv);
+        if constexpr (!Cf::BWD) {
+            __syncwarp();  // every lane has read the slot
+            if (lane == 0) issue(q + NSL);
+        }
         warp_step<Cf>(xw, cur, yc, yv, rb, cb, o);
         if constexpr (!Cf::BWD) {
 #pragma unroll
@@ -920,9 +1389,9 @@ __global__ void __launch_bounds__(Cf::NW * 32)
                 const int row = rb * R + r;
                 if constexpr (CC % 4 == 0 && K % 4 == 0 && VV % 4 == 0) {
 #pragma unroll
-                    for (int q = 0; q < CC; q += 4) {
-                        const int col = cb * CC + q;
-                        float v4[4] = {o[r][q], o[r][q + 1], o[r][q + 2], o[r][q + 3]};
+                    for (int qq = 0; qq < CC; qq += 4) {
+                        const int col = cb * CC + qq;
+                        float v4[4] = {o[r][qq], o[r][qq + 1], o[r][qq + 2], o[r][qq + 3]};
                         if (col < K) st_floats<4>(p.Abar_out + s * KK + row * K + col, v4);
                         else if (col < NC) st_floats<4>(p.Bbar_out + s * KV + row * VV + col - K, v4);
                     }
@@ -946,36 +1415,40 @@ __global__ void __launch_bounds__(Cf::NW * 32)
                 }
             // dA_t[row][jc] = sum_q X[row][K + q] * Y[jc][q],  Y = [Abar_{t-1} | Bbar_{t-1}]
             constexpr int JD = Cf::JD, WW = Cf::W;
-            if (cb * JD < K) {
-                const float *xs = xw + (Cf::DB ? cur * MAT : 0);
-                const float *Ap = stage + 2 * TC * KK + TC * KV + i * KK;
-                const float *Bp = stage + 3 * TC * KK + TC * KV + i * KV;
-                float da[R][JD];
+            const float *xs = xw + (Cf::DB ? cur * MAT : 0);
+            const float *Ap = slot + Cf::OFF_AP;
+            const float *Bp = slot + Cf::OFF_BP;
+            // the JD rows of Y first, then each row of X once
+            float y[JD][WW];
+#pragma unroll
+            for (int jj = 0; jj < JD; ++jj) {
+                const int jc = cb * JD + jj;
+                if (t > 0) {
+                    ld_floats<K>(Ap + jc * K, y[jj]);
+                    ld_floats<VV>(Bp + jc * VV, y[jj] + K);
+                } else {  // Abar_0 = I, Bbar_0 = 0
+#pragma unroll
+                    for (int qq = 0; qq < WW; ++qq) y[jj][qq] = (qq == jc) ? 1.f : 0.f;
+                }
+            }
+            float da[R][JD];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float xr[WW];
+                ld_floats<WW>(xs + (rb * R + r) * XS + K, xr);
 #pragma unroll
                 for (int jj = 0; jj < JD; ++jj) {
-                    const int jc = cb * JD + jj;
-                    float y[WW];
-                    if (t > 0) {
-                        ld_floats<K>(Ap + jc * K, y);
-                        ld_floats<VV>(Bp + jc * VV, y + K);
-                    } else {  // Abar_0 = I, Bbar_0 = 0
+                    float acc = 0.f;
 #pragma unroll
-                        for (int q = 0; q < WW; ++q) y[q] = (q == jc) ? 1.f : 0.f;
-                    }
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const float *xr = xs + (rb * R + r) * XS + K;
-                        float acc = 0.f;
-#pragma unroll
-                        for (int q = 0; q < WW; ++q) acc = fmaf(xr[q], y[q], acc);
-                        da[r][jj] = acc;
-                    }
+                    for (int qq = 0; qq < WW; ++qq) acc = fmaf(xr[qq], y[jj][qq], acc);
+                    da[r][jj] = acc;
                 }
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-                    st_floats<JD>(p.dA + s * KK + (rb * R + r) * K + cb * JD, da[r]);
             }
-            if constexpr (!Cf::DB) __syncwarp();  // the next step overwrites xw
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+                st_floats<JD>(p.dA + s * KK + (rb * R + r) * K + cb * JD, da[r]);
+            __syncwarp();  // the slot and xw are read by every lane before reuse
+            if (lane == 0) issue(q + NSL);
         }
     }
     finish_cta(lb, epoch);
@@ -1027,7 +1500,7 @@ struct WarpPlan {
 // Tiles, each overridable at build time.  k <= 4 (thread-owned state on the
 // chunk engine): TY thread rows x L steps of 32 sequences, MB minimum CTAs per
 // SM.  k = 8, 16 (warp kernel): NW warps x L steps of one sequence, DB =
-// double-buffered state exchange.
+// double-buffered state exchange, NSL ring slots per warp.
 #ifndef MG_AFS_TY
 #define MG_AFS_TY 8
 #endif
@@ -1046,33 +1519,72 @@ struct WarpPlan {
 #ifndef MG_AFSB_MB
 #define MG_AFSB_MB 1
 #endif
+#ifndef MG_AFL_NW
+#define MG_AFL_NW 4
+#endif
+#ifndef MG_AFL_L
+#define MG_AFL_L 32
+#endif
+#ifndef MG_AFL_NSL
+#define MG_AFL_NSL 6
+#endif
+#ifndef MG_AFLB_NW
+#define MG_AFLB_NW 4
+#endif
+#ifndef MG_AFLB_L
+#define MG_AFLB_L 32
+#endif
+#ifndef MG_AFLB_NSL
+#define MG_AFLB_NSL 4
+#endif
 #ifndef MG_AFW_NW
 #define MG_AFW_NW 4
 #endif
 #ifndef MG_AFW_L
-#define MG_AFW_L 8
+#define MG_AFW_L 16
 #endif
 #ifndef MG_AFW_DB
 #define MG_AFW_DB 1
+#endif
+#ifndef MG_AFW_NSL
+#define MG_AFW_NSL 5
 #endif
 #ifndef MG_AFWB_NW
 #define MG_AFWB_NW 4
 #endif
 #ifndef MG_AFWB_L
-#define MG_AFWB_L 4
+#define MG_AFWB_L 16
 #endif
 #ifndef MG_AFWB_DB
 #define MG_AFWB_DB 0
 #endif
+#ifndef MG_AFWB_NSL
+#define MG_AFWB_NSL 2
+#endif
 
+template <int K, int V>
+using LaneFwd = LanePlan<LCfg<K, V, false, MG_AFL_NW, MG_AFL_L, MG_AFL_NSL>>;
+template <int K, int V>
+using LaneBwd = LanePlan<LCfg<K, V, true, MG_AFLB_NW, MG_AFLB_L, MG_AFLB_NSL>>;
 template <int K, int V>
 using SmallFwd = ChanPlan<AffFwdSmall<K, V, MG_AFS_L>, 32, MG_AFS_TY, MG_AFS_MB>;
 template <int K, int V>
 using SmallBwd = ChanPlan<AffBwdSmall<K, V, MG_AFSB_L>, 32, MG_AFSB_TY, MG_AFSB_MB>;
 template <int K, int V>
-using BigFwd = WarpPlan<WCfg<K, V, false, MG_AFW_NW, MG_AFW_L, bool(MG_AFW_DB)>>;
+using BigFwd = WarpPlan<WCfg<K, V, false, MG_AFW_NW, MG_AFW_L, bool(MG_AFW_DB), MG_AFW_NSL>>;
 template <int K, int V>
-using BigBwd = WarpPlan<WCfg<K, K + V, true, MG_AFWB_NW, MG_AFWB_L, bool(MG_AFWB_DB)>>;
+using BigBwd = WarpPlan<WCfg<K, K + V, true, MG_AFWB_NW, MG_AFWB_L, bool(MG_AFWB_DB), MG_AFWB_NSL>>;
+
+// k <= 4: the lane kernel by default, the chunk engine with MGSCAN_ENGINE=chunked
+// (or where the blocks are not 16-byte multiples), the streaming engine with
+// MGSCAN_ENGINE=stream.
+template <int K, int V>
+bool use_lane(const LaunchOpts &o, int64_t B, int64_t T, int64_t n)
+{
+    if constexpr (lane_kernel_ok<K, V>())
+        return o.engine == LaunchOpts::kAuto && LanePlan<LCfg<K, V, false, 1, 1, 2>>::fits(B, T, n);
+    return false;
+}
 
 template <int K, int V>
 size_t ws_kv(int64_t B, int64_t T, int64_t n, const LaunchOpts &o)
@@ -1082,6 +1594,11 @@ size_t ws_kv(int64_t B, int64_t T, int64_t n, const LaunchOpts &o)
         if (o.engine == LaunchOpts::kStream && aff_stream_ok<K, V>(n)) {
             a = StreamPlan<AffFwdT<K, V>>::ws_bytes(B, T, n);
             b = StreamPlan<AffBwdT<K, V>>::ws_bytes(B, T, n);
+        } else if (use_lane<K, V>(o, B, T, n)) {
+            if constexpr (lane_kernel_ok<K, V>()) {
+                a = LaneFwd<K, V>::ws_bytes(B, T, n);
+                b = LaneBwd<K, V>::ws_bytes(B, T, n);
+            }
         } else {
             a = SmallFwd<K, V>::ws_bytes(B, T, n);
             b = SmallBwd<K, V>::ws_bytes(B, T, n);
@@ -1104,6 +1621,10 @@ mg_status fwd_kv(const float *A, const float *Bm, float *Abar, float *Bbar, int6
                 {{Staged{reinterpret_cast<const char *>(A), T}, Staged{reinterpret_cast<const char *>(Bm), T}},
                  Abar, Bbar},
                 B, T, n, ws, wsb, s, o, nm);
+        if constexpr (lane_kernel_ok<K, V>()) {
+            if (use_lane<K, V>(o, B, T, n))
+                return LaneFwd<K, V>::launch({A, Bm, Abar, Bbar}, B, T, n, ws, wsb, s, o, nm);
+        }
         return SmallFwd<K, V>::launch({A, Bm, Abar, Bbar}, B, T, n, ws, wsb, s, o, nm);
     } else {
         AffPtrs p{};
@@ -1127,6 +1648,11 @@ mg_status bwd_kv(const float *A, const float *Abar, const float *Bbar, const flo
             return StreamPlan<AffBwdT<K, V>>::launch(
                 {{stg(A), stg(gAbar), stg(gBbar), stg(Abar), stg(Bbar)}, dA, dB}, B, T, n, ws, wsb,
                 s, o, nm);
+        if constexpr (lane_kernel_ok<K, V>()) {
+            if (use_lane<K, V>(o, B, T, n))
+                return LaneBwd<K, V>::launch({A, Abar, Bbar, gAbar, gBbar, dA, dB}, B, T, n, ws,
+                                             wsb, s, o, nm);
+        }
         return SmallBwd<K, V>::launch({A, Abar, Bbar, gAbar, gBbar, dA, dB}, B, T, n, ws, wsb, s,
                                       o, nm);
     } else {

@@ -46,7 +46,7 @@ def test_every_k_v(cuda_lib, k, v):
 
 
 @pytest.mark.parametrize("shape", [(1, 1, 1), (1, 3, 2), (2, 333, 5), (1, 700, 1)])
-@pytest.mark.parametrize("k", [4, 16])
+@pytest.mark.parametrize("k", [4, 8, 16])
 def test_shapes(cuda_lib, shape, k):
     A, Bm, gA, gB = wl.haar_affine(*shape, k, k, seed=7)
     _run(cuda_lib, A, Bm, gA, gB)
