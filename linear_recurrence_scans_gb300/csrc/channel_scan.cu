@@ -397,6 +397,9 @@ struct LogFwd {
 #ifndef MG_LINF_MB
 #define MG_LINF_MB 1
 #endif
+#ifndef MG_LINF16_VEC
+#define MG_LINF16_VEC 8
+#endif
 #ifndef MG_LINF16_TX
 #define MG_LINF16_TX 32
 #endif
@@ -463,7 +466,7 @@ struct LogFwd {
 constexpr int kTX = 32, kTY = 8;
 using LinFwdF32 = ChanPlan<LinFwd<float, 4, MG_LINF_L>, MG_LINF_TX, MG_LINF_TY, MG_LINF_MB, MG_LINF_R>;
 using LinFwdF32s = ChanPlan<LinFwd<float, 1, 8>, kTX, kTY>;
-using LinFwdB16 = ChanPlan<LinFwd<bf16_t, 8, MG_LINF16_L>, MG_LINF16_TX, MG_LINF16_TY, MG_LINF16_MB, MG_LINF16_R>;
+using LinFwdB16 = ChanPlan<LinFwd<bf16_t, MG_LINF16_VEC, MG_LINF16_L>, MG_LINF16_TX, MG_LINF16_TY, MG_LINF16_MB, MG_LINF16_R>;
 using LinFwdB16s = ChanPlan<LinFwd<bf16_t, 1, 8>, kTX, kTY>;
 using LinBwdF32 = ChanPlan<LinBwd<float, 4, MG_LINB_L>, MG_LINB_TX, MG_LINB_TY, MG_LINB_MB, MG_LINB_R>;
 using LinBwdF32s = ChanPlan<LinBwd<float, 1, 4>, kTX, kTY>;
@@ -490,7 +493,7 @@ size_t linear_fwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D, const L
 {
     if (use_stream_fwd(dt, D, o)) return stream_linear_fwd_ws_bytes(dt, B, T, D);
     if (dt == MG_F32) return D % 4 == 0 ? LinFwdF32::ws_bytes(B, T, D) : LinFwdF32s::ws_bytes(B, T, D);
-    return D % 8 == 0 ? LinFwdB16::ws_bytes(B, T, D) : LinFwdB16s::ws_bytes(B, T, D);
+    return D % MG_LINF16_VEC == 0 ? LinFwdB16::ws_bytes(B, T, D) : LinFwdB16s::ws_bytes(B, T, D);
 }
 
 size_t linear_bwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D, const LaunchOpts &o)
@@ -530,7 +533,7 @@ mg_status launch_linear_fwd(const void *a, const void *b, mg_dtype dt, float *A,
         return LinFwdF32s::launch({F(a), F(b), A, Bc}, B, T, D, ws, wsb, s, o, nm);
     }
     using H = const bf16_t *;
-    if (D % 8 == 0) return LinFwdB16::launch({H(a), H(b), A, Bc}, B, T, D, ws, wsb, s, o, nm);
+    if (D % MG_LINF16_VEC == 0) return LinFwdB16::launch({H(a), H(b), A, Bc}, B, T, D, ws, wsb, s, o, nm);
     return LinFwdB16s::launch({H(a), H(b), A, Bc}, B, T, D, ws, wsb, s, o, nm);
 }
 
