@@ -23,9 +23,6 @@
 //     same decoupled look-back as every other scan (lookback.cuh).
 #include <type_traits>
 
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "stream_engine.cuh"
 
 namespace mg {
@@ -349,15 +346,15 @@ struct AffBwdSmall {
     }
 };
 
-// ============================= k <= 4: one sequence per lane, TMA-fed tiles
+// ===================== k <= 4: one sequence per lane, asynchronously fed
 // A tile is 32 consecutive sequences of one batch row x TC = NW*L steps; warp
 // w owns steps [w*L, (w+1)*L) of the tile, lane l sequence n0 + l, and keeps
 // that sequence's state in registers.  At one step the block's 32 matrices
-// are consecutive rows of a (rows = b*T*n + t*n + n_, S bytes) view of each
-// array, so every array of a step arrives with one 2D tensor copy (box = 32
-// rows) into a slot of the warp's ring (NSL slots, one mbarrier each).  The
-// copy swizzles 16-byte chunks within the S-byte rows (S = 32, 64 or 128),
-// so the 32 lanes reading one chunk of their own rows hit distinct banks.
+// are 32 consecutive rows (S bytes each) of each array; the warp copies them
+// with coalesced 16-byte asynchronous copies (cp.async, one commit group per
+// step) into a slot of its ring (NSL slots), placing 16-byte chunk c of row r
+// at chunk c ^ ((r*S >> 7) & (S/16 - 1)) of that row, so the 32 lanes then
+// reading one chunk of their own rows hit distinct banks.
 // Pass 1 folds the warp's steps into its aggregate; the warps' aggregates are
 // folded in shared memory (leaving each warp its exclusive prefix); warp 0
 // finds the tile's carry-in by decoupled look-back; pass 2 streams the same
@@ -365,17 +362,9 @@ struct AffBwdSmall {
 // outputs.  Needs every per-sequence block to be 16..128 bytes: k = 4 with
 // v <= 8, or k = 2 with 2 <= v.
 
-// Swizzle of a tensor copy whose rows are `bytes` long (16: none).
-constexpr CUtensorMapSwizzle row_swizzle(int bytes)
-{
-    return bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
-         : bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
-         : bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
-}
-
-// The E floats of lane `lane`'s row in a swizzled 32-row box (base aligned
+// The E floats of lane `lane`'s row in a swizzled 32-row block (base aligned
 // to 1024 bytes): 16-byte chunk q of row r sits at chunk q ^ ((r*S >> 7) &
-// (S/16 - 1)) of that row, the pattern of the tensor-copy swizzle modes.
+// (S/16 - 1)) of that row.
 template <int E>
 __device__ __forceinline__ void lane_row(const float *box, int lane, float *o)
 {
@@ -392,20 +381,6 @@ __device__ __forceinline__ void lane_row(const float *box, int lane, float *o)
         o[4 * q + 3] = x.w;
     }
 }
-
-__device__ __forceinline__ void tma_load_rows(void *dst, const CUtensorMap *map, int row,
-                                              unsigned long long *bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];"
-        : : "r"(smem_addr(dst)), "l"(map), "r"(0), "r"(row), "r"(smem_addr(bar)) : "memory");
-}
-
-// Tensor maps of the staged arrays, in slot order.
-struct LaneMaps {
-    CUtensorMap m[5];
-};
 
 template <int K_, int V_, bool BWD_, int NW_, int L_, int NSL_>
 struct LCfg {
@@ -424,7 +399,7 @@ struct LCfg {
     static constexpr size_t smem_for(int nw)
     {
         return 1024 + size_t(nw * NSL * STEP) * sizeof(float) +
-               size_t((nw + 1) * NS * 32) * sizeof(float) + size_t(nw * NSL) * 8;
+               size_t((nw + 1) * NS * 32) * sizeof(float);
     }
     // warps per CTA: NW_, halved while the CTA would not fit in shared memory
     static constexpr size_t kMax = 225 * 1024;
@@ -445,21 +420,18 @@ constexpr bool lane_kernel_ok()
 
 template <class Cf>
 __global__ void __launch_bounds__(Cf::NW * 32)
-    affine_lane_kernel(const typename Cf::Op::Args args, const __grid_constant__ LaneMaps maps,
-                       const ChanGeom g, const Lookback lb)
+    affine_lane_kernel(const typename Cf::Op::Args args, const ChanGeom g, const Lookback lb)
 {
     using Op = typename Cf::Op;
     using S = typename Op::S;
     constexpr int K = Cf::K, KK = Cf::KK, KV = Cf::KV, VV = Cf::VV, NS = Cf::NS, W = Cf::W;
-    constexpr int NW = Cf::NW, L = Cf::L, NSL = Cf::NSL, STEP = Cf::STEP, NARR = Cf::NARR;
+    constexpr int NW = Cf::NW, L = Cf::L, NSL = Cf::NSL, STEP = Cf::STEP;
     extern __shared__ float4 lane_smem[];
     // ring first, 1024-byte aligned for the swizzle, then the rest
     float *const ring = reinterpret_cast<float *>(
         (reinterpret_cast<uintptr_t>(lane_smem) + 1023) & ~uintptr_t(1023));  // [NW][NSL][STEP]
     float *const s_agg = ring + NW * NSL * STEP;                                // [NW][NS][32]
     float *const s_carry = s_agg + NW * NS * 32;                                // [NS][32]
-    unsigned long long *const bars =
-        reinterpret_cast<unsigned long long *>(s_carry + NS * 32);             // [NW][NSL]
 
     unsigned tile;
     unsigned long long epoch;
@@ -476,13 +448,13 @@ __global__ void __launch_bounds__(Cf::NW * 32)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int d = n0 + lane;                         // this lane's sequence in the row
     const bool act = d < g.D;
+    const int nseq = int(g.D - n0 < 32 ? g.D - n0 : 32);  // sequences in the block
     const int ct = Cf::BWD ? (g.nC - 1 - c) : c;
     const int64_t t0 = int64_t(ct) * Cf::TC;
     const int nv = int(g.T - t0 < Cf::TC ? g.T - t0 : Cf::TC);
     const int wbase = warp * L;
     const int nvw = nv - wbase < 0 ? 0 : (nv - wbase < L ? nv - wbase : L);
     const int pw = Cf::BWD ? NW - 1 - warp : warp;  // position in processing order
-    unsigned long long *const wbar = bars + warp * NSL;
     float *const wring = ring + warp * NSL * STEP;
     auto row = [&](int64_t t) { return (bb * g.T + t) * g.D + n0; };  // row of lane 0
     auto tile_step = [&](int q) {
@@ -491,35 +463,41 @@ __global__ void __launch_bounds__(Cf::NW * 32)
     };
     const int nq = 2 * nvw;
 
-    auto issue = [&](int q) {  // lane 0
-        if (q >= nq) return;
-        unsigned long long *bar = wbar + q % NSL;
-        float *buf = wring + (q % NSL) * STEP;
-        const int64_t t = t0 + tile_step(q);
-        const int r = int(row(t));
-        if constexpr (!Cf::BWD) {
-            mbar_arrive_expect_tx(bar, 32 * (KK + KV) * 4);
-            tma_load_rows(buf + Cf::offset(0), &maps.m[0], r, bar);
-            tma_load_rows(buf + Cf::offset(1), &maps.m[1], r, bar);
-        } else {
-            const bool next = t + 1 < g.T, prev = q >= nvw && t >= 1;
-            mbar_arrive_expect_tx(bar, 32 * 4 * ((KK + KV) + (next ? KK : 0) + (prev ? KK + KV : 0)));
-            tma_load_rows(buf + Cf::offset(1), &maps.m[1], r, bar);
-            tma_load_rows(buf + Cf::offset(2), &maps.m[2], r, bar);
-            if (next) tma_load_rows(buf + Cf::offset(0), &maps.m[0], r + int(g.D), bar);
-            if (prev) {
-                tma_load_rows(buf + Cf::offset(3), &maps.m[3], r - int(g.D), bar);
-                tma_load_rows(buf + Cf::offset(4), &maps.m[4], r - int(g.D), bar);
+    // every lane copies 16-byte pieces of the step's rows (coalesced) into
+    // their swizzled positions; every call closes one group, empty or not
+    auto issue = [&](int q) {
+        if (q < nq) {
+            float *buf = wring + (q % NSL) * STEP;
+            const int64_t t = t0 + tile_step(q), r = row(t);
+            auto rows = [&](float *dst, const float *src, int E) {  // nseq rows of E floats
+                const int S = E * 4, per = S / 16, n = nseq * per;
+                for (int i = lane; i < n; i += 32) {
+                    const int rr = i / per, c = i % per;
+                    const int sw = ((rr * S) >> 7) & (per - 1);
+                    cp_async16(reinterpret_cast<char *>(dst) + rr * S + 16 * (c ^ sw),
+                               src + int64_t(i) * 4);
+                }
+            };
+            if constexpr (!Cf::BWD) {
+                rows(buf + Cf::offset(0), args.A + r * KK, KK);
+                rows(buf + Cf::offset(1), args.Bm + r * KV, KV);
+            } else {
+                rows(buf + Cf::offset(1), args.gAbar + r * KK, KK);
+                rows(buf + Cf::offset(2), args.gBbar + r * KV, KV);
+                if (t + 1 < g.T) rows(buf + Cf::offset(0), args.A + (r + g.D) * KK, KK);
+                if (q >= nvw && t >= 1) {
+                    rows(buf + Cf::offset(3), args.Abar + (r - g.D) * KK, KK);
+                    rows(buf + Cf::offset(4), args.Bbar + (r - g.D) * KV, KV);
+                }
             }
         }
+        cp_async_commit();
     };
+    // entry q has landed for every lane (this lane's group q, then a warp
+    // barrier for the others' copies)
     auto wait_slot = [&](int q) -> const float * {
-        unsigned long long *bar = wbar + q % NSL;
-        const unsigned parity = unsigned(q / NSL) & 1u;
-        if (!mbar_wait_bounded(bar, parity, lb.wait_limit_ns)) {
-            if (lane == 0) atomicOr(&lb.ctl->error, kErrLookbackTimeout);
-            mbar_wait_bounded(bar, parity, lb.wait_limit_ns);
-        }
+        cp_async_wait<NSL - 1>();
+        __syncwarp();
         return wring + (q % NSL) * STEP;
     };
     // the lane's element of a step: coefficient E (k x k) and value (k x W)
@@ -553,11 +531,8 @@ __global__ void __launch_bounds__(Cf::NW * 32)
         }
     };
 
-    if (lane == 0) {
-        for (int q = 0; q < NSL; ++q) mbar_init(wbar + q, 1);
-        for (int q = 0; q < NSL; ++q) issue(q);
-    }
-    __syncwarp();
+    for (int q = 0; q < NSL; ++q) issue(q);
+    auto refill = [&](int q) { issue(q); };  // after every lane has read entry q - NSL
 
     // ---- pass 1: the warp's aggregate, in processing order
     S agg = Op::identity();
@@ -568,7 +543,7 @@ __global__ void __launch_bounds__(Cf::NW * 32)
         S e;
         if (act) element(slot, t, e);
         __syncwarp();
-        if (lane == 0) issue(q + NSL);
+        refill(q + NSL);
         if (act) agg = Op::combine(agg, e);
     }
 #pragma unroll
@@ -618,7 +593,7 @@ __global__ void __launch_bounds__(Cf::NW * 32)
             S e;
             if (act) element(slot, t, e);
             __syncwarp();
-            if (lane == 0) issue(q + NSL);
+            refill(q + NSL);
             if (act) {
                 st = Op::combine(st, e);
                 st_floats<KK>(args.Abar + sidx * KK, &st.v[0][0]);
@@ -664,40 +639,10 @@ __global__ void __launch_bounds__(Cf::NW * 32)
                 st_floats<KV>(args.dB + sidx * KV, dB);
             }
             __syncwarp();  // every lane has read the slot
-            if (lane == 0) issue(q + NSL);
+            refill(q + NSL);
         }
     }
     finish_cta(lb, epoch);
-}
-
-// cuTensorMapEncodeTiled from the driver, found once through the runtime.
-inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
-{
-    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }();
-    return fn;
-}
-
-// A (rows x E floats) view of `base` copied 32 rows at a time, swizzled.
-inline bool encode_rows_map(CUtensorMap *m, const float *base, int E, int64_t rows)
-{
-    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (enc == nullptr) return false;
-    const cuuint64_t dims[2] = {cuuint64_t(E), cuuint64_t(rows)};
-    const cuuint64_t strides[1] = {cuuint64_t(E) * 4};
-    const cuuint32_t box[2] = {cuuint32_t(E), 32};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, row_swizzle(E * 4),
-               CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <class Cf>
@@ -722,8 +667,6 @@ struct LanePlan {
     {
         return tiled_ws_bytes(n_tiles(B, T, n), size_t(2) * Cf::NS * 32 * sizeof(float));
     }
-    // rows of the tensor views must be addressable with 32-bit coordinates
-    static bool fits(int64_t B, int64_t T, int64_t n) { return B * T * n < (int64_t(1) << 31) - 64; }
     static mg_status launch(const typename Cf::Op::Args &args, int64_t B, int64_t T, int64_t n,
                             void *ws, size_t wsb, cudaStream_t s, const LaunchOpts &o,
                             const char *name)
@@ -734,26 +677,12 @@ struct LanePlan {
         const size_t need = ws_bytes(B, T, n);
         if (wsb < need)
             return fail(MG_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", name, wsb, need);
-        LaneMaps maps;
-        const int64_t rows = B * T * n;
-        bool ok;
-        if constexpr (!Cf::BWD) {
-            ok = encode_rows_map(&maps.m[0], args.A, Cf::KK, rows) &&
-                 encode_rows_map(&maps.m[1], args.Bm, Cf::KV, rows);
-        } else {
-            ok = encode_rows_map(&maps.m[0], args.A, Cf::KK, rows) &&
-                 encode_rows_map(&maps.m[1], args.gAbar, Cf::KK, rows) &&
-                 encode_rows_map(&maps.m[2], args.gBbar, Cf::KV, rows) &&
-                 encode_rows_map(&maps.m[3], args.Abar, Cf::KK, rows) &&
-                 encode_rows_map(&maps.m[4], args.Bbar, Cf::KV, rows);
-        }
-        if (!ok) return fail(MG_ERR_LAUNCH, "%s: could not encode the tensor maps", name);
         const ChanGeom g = geom(B, T, n);
         const Lookback lb = make_lookback(ws, nt, o);
         static const cudaError_t attr = cudaFuncSetAttribute(
             affine_lane_kernel<Cf>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cf::SMEM));
         if (attr != cudaSuccess) return fail(MG_ERR_LAUNCH, "%s: %s", name, cudaGetErrorString(attr));
-        affine_lane_kernel<Cf><<<unsigned(nt), Cf::NW * 32, Cf::SMEM, s>>>(args, maps, g, lb);
+        affine_lane_kernel<Cf><<<unsigned(nt), Cf::NW * 32, Cf::SMEM, s>>>(args, g, lb);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return fail(MG_ERR_LAUNCH, "%s: launch failed: %s", name, cudaGetErrorString(e));
@@ -1285,24 +1214,29 @@ __global__ void __launch_bounds__(Cf::NW * 32)
         for (int q = 0; q < NSL; ++q) issue(q);
     }
     __syncwarp();
+    auto refill = [&](int q) {  // after every lane has read entry q - NSL
+        if (lane == 0) issue(q);
+    };
 
     float yc[R][K], yv[R][CC], o[R][CC];
 
     // ---- pass 1: aggregate of the warp's steps, in processing order
     int cur = 0;
-    identity_block<Cf>(rb, cb, o);
-    put_block_smem<Cf>(xw, rb, cb, o);
-    __syncwarp();
+    {
+        identity_block<Cf>(rb, cb, o);
+        put_block_smem<Cf>(xw, rb, cb, o);
+        __syncwarp();
 #pragma unroll 1
-    for (int q = 0; q < nvw; ++q) {
-        const int64_t t = t0 + tile_step(q);
-        const float *slot = wait_slot(q);
-        load_elem<Cf>(slot, t + 1 < g.T, rb, cb, yc, yv);
-        __syncwarp();  // every lane has read the slot
-        if (lane == 0) issue(q + NSL);
-        warp_step<Cf>(xw, cur, yc, yv, rb, cb, o);
+        for (int q = 0; q < nvw; ++q) {
+            const int64_t t = t0 + tile_step(q);
+            const float *slot = wait_slot(q);
+            load_elem<Cf>(slot, t + 1 < g.T, rb, cb, yc, yv);
+            __syncwarp();  // every lane has read the slot
+            refill(q + NSL);
+            warp_step<Cf>(xw, cur, yc, yv, rb, cb, o);
+        }
+        put_block_smem<Cf>(G + pw * MAT, rb, cb, o);
     }
-    put_block_smem<Cf>(G + pw * MAT, rb, cb, o);
     __syncthreads();
 
     // ---- warp 0: inclusive prefixes over the warps (processing order), then
@@ -1380,7 +1314,7 @@ __global__ void __launch_bounds__(Cf::NW * 32)
         load_elem<Cf>(slot, t + 1 < g.T, rb, cb, yc, yv);
         if constexpr (!Cf::BWD) {
             __syncwarp();  // every lane has read the slot
-            if (lane == 0) issue(q + NSL);
+            refill(q + NSL);
         }
         warp_step<Cf>(xw, cur, yc, yv, rb, cb, o);
         if constexpr (!Cf::BWD) {
@@ -1448,7 +1382,7 @@ __global__ void __launch_bounds__(Cf::NW * 32)
             for (int r = 0; r < R; ++r)
                 st_floats<JD>(p.dA + s * KK + (rb * R + r) * K + cb * JD, da[r]);
             __syncwarp();  // the slot and xw are read by every lane before reuse
-            if (lane == 0) issue(q + NSL);
+            refill(q + NSL);
         }
     }
     finish_cta(lb, epoch);
@@ -1579,10 +1513,9 @@ using BigBwd = WarpPlan<WCfg<K, K + V, true, MG_AFWB_NW, MG_AFWB_L, bool(MG_AFWB
 // (or where the blocks are not 16-byte multiples), the streaming engine with
 // MGSCAN_ENGINE=stream.
 template <int K, int V>
-bool use_lane(const LaunchOpts &o, int64_t B, int64_t T, int64_t n)
+bool use_lane(const LaunchOpts &o)
 {
-    if constexpr (lane_kernel_ok<K, V>())
-        return o.engine == LaunchOpts::kAuto && LanePlan<LCfg<K, V, false, 1, 1, 2>>::fits(B, T, n);
+    if constexpr (lane_kernel_ok<K, V>()) return o.engine == LaunchOpts::kAuto;
     return false;
 }
 
@@ -1594,7 +1527,7 @@ size_t ws_kv(int64_t B, int64_t T, int64_t n, const LaunchOpts &o)
         if (o.engine == LaunchOpts::kStream && aff_stream_ok<K, V>(n)) {
             a = StreamPlan<AffFwdT<K, V>>::ws_bytes(B, T, n);
             b = StreamPlan<AffBwdT<K, V>>::ws_bytes(B, T, n);
-        } else if (use_lane<K, V>(o, B, T, n)) {
+        } else if (use_lane<K, V>(o)) {
             if constexpr (lane_kernel_ok<K, V>()) {
                 a = LaneFwd<K, V>::ws_bytes(B, T, n);
                 b = LaneBwd<K, V>::ws_bytes(B, T, n);
@@ -1622,7 +1555,7 @@ mg_status fwd_kv(const float *A, const float *Bm, float *Abar, float *Bbar, int6
                  Abar, Bbar},
                 B, T, n, ws, wsb, s, o, nm);
         if constexpr (lane_kernel_ok<K, V>()) {
-            if (use_lane<K, V>(o, B, T, n))
+            if (use_lane<K, V>(o))
                 return LaneFwd<K, V>::launch({A, Bm, Abar, Bbar}, B, T, n, ws, wsb, s, o, nm);
         }
         return SmallFwd<K, V>::launch({A, Bm, Abar, Bbar}, B, T, n, ws, wsb, s, o, nm);
@@ -1649,7 +1582,7 @@ mg_status bwd_kv(const float *A, const float *Abar, const float *Bbar, const flo
                 {{stg(A), stg(gAbar), stg(gBbar), stg(Abar), stg(Bbar)}, dA, dB}, B, T, n, ws, wsb,
                 s, o, nm);
         if constexpr (lane_kernel_ok<K, V>()) {
-            if (use_lane<K, V>(o, B, T, n))
+            if (use_lane<K, V>(o))
                 return LaneBwd<K, V>::launch({A, Abar, Bbar, gAbar, gBbar, dA, dB}, B, T, n, ws,
                                              wsb, s, o, nm);
         }

@@ -284,6 +284,21 @@ __device__ __forceinline__ void tma_load_1d(void *dst, const void *src, unsigned
         : : "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
 }
 
+// Per-thread asynchronous 16-byte copies global -> shared (LDGSTS), grouped
+// per thread: commit closes a group, wait<N> returns once at most N of this
+// thread's groups are still in flight.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" : : "r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" : : : "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" : : "n"(N) : "memory");
+}
+
 // Bounded wait for phase `parity` of `bar`; false if it gave up (the caller
 // records the error; the copies themselves always complete).
 __device__ __forceinline__ bool mbar_wait_bounded(unsigned long long *bar, unsigned parity,
