@@ -52,6 +52,21 @@ def test_shapes(cuda_lib, shape, k):
     _run(cuda_lib, A, Bm, gA, gB)
 
 
+@pytest.mark.parametrize("k,v,shape", [
+    (2, 2, (2, 600, 37)),   # lane kernel, 5 chunks, a full and a 5-sequence block
+    (2, 16, (1, 300, 33)),
+    (4, 1, (2, 400, 40)),
+    (4, 8, (1, 300, 64)),
+    (4, 16, (1, 200, 35)),  # k=4, v=16 stays on the chunk engine
+    (1, 4, (2, 300, 45)),
+])
+def test_multichunk_ragged_blocks(cuda_lib, k, v, shape):
+    """Several chunks in time and a ragged last block of sequences for the
+    k <= 4 kernels (the look-back and the partial-block copies)."""
+    A, Bm, gA, gB = wl.haar_affine(*shape, k, v, seed=k * 10 + v)
+    _run(cuda_lib, A, Bm, gA, gB)
+
+
 def test_general_matrices(cuda_lib):
     """Non-orthogonal transitions with entries of both signs."""
     g = torch.Generator().manual_seed(8)
