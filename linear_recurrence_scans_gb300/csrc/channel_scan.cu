@@ -458,10 +458,10 @@ struct LogFwd {
 #define MG_LINB_R 2
 #endif
 #ifndef MG_LINB16_R
-#define MG_LINB16_R 3
+#define MG_LINB16_R 2
 #endif
 #ifndef MG_LOG_R
-#define MG_LOG_R 3
+#define MG_LOG_R 2
 #endif
 constexpr int kTX = 32, kTY = 8;
 using LinFwdF32 = ChanPlan<LinFwd<float, 4, MG_LINF_L>, MG_LINF_TX, MG_LINF_TY, MG_LINF_MB, MG_LINF_R>;
