@@ -1124,6 +1124,74 @@ __device__ __forceinline__ void warp_step(float *xw, int &cur, const float (&yc)
     }
 }
 
+// ------------------------------------------------ dA_t on the tensor cores
+// dA_t = Xv Y^T with Xv = [M_t | Lam_t] (16 x W) and Y = [Abar_{t-1} |
+// Bbar_{t-1}] (16 x W), W = 16 + v: an independent product per step (no
+// recurrence runs through it), done as mma.sync.m16n8k8 tf32 tiles (M = 16,
+// N = 16, K = W).  Each fp32 operand is split into a tf32 high part and a
+// tf32 remainder and the products hi*hi, hi*lo, lo*hi are accumulated in
+// fp32: the dropped lo*lo term is below 2^-22 of each product.
+
+#ifndef MG_AFW_MMA_DA
+#define MG_AFW_MMA_DA 1
+#endif
+
+__device__ __forceinline__ void split_tf32(float x, unsigned &hi, unsigned &lo)
+{
+    unsigned h, l;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(h) : "f"(x));
+    const float rem = x - __uint_as_float(h);
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(l) : "f"(rem));
+    hi = h;
+    lo = l;
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const unsigned (&a)[4], unsigned b0,
+                                         unsigned b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// xs: X rows with stride XS (Xv = columns 16 .. 16+W-1); ap, bp: Abar_{t-1}
+// (16 x 16) and Bbar_{t-1} (16 x V) row-major; writes dA (16 x 16) at `out`.
+template <int XS, int V>
+__device__ __forceinline__ void mma_dA16(const float *xs, const float *ap, const float *bp,
+                                         int lane, float *out)
+{
+    constexpr int W = 16 + V, NKT = W / 8;
+    const int g = lane >> 2, q = lane & 3;
+    float d[2][4] = {};
+#pragma unroll
+    for (int kt = 0; kt < NKT; ++kt) {
+        unsigned ah[4], al[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            split_tf32(xs[(g + 8 * (e & 1)) * XS + 16 + 8 * kt + q + 4 * (e >> 1)], ah[e], al[e]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            unsigned bh[2], bl[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {  // B[k][n] = Y[n][k]
+                const int n = 8 * nt + g, k = 8 * kt + q + 4 * e;
+                split_tf32(k < 16 ? ap[n * 16 + k] : bp[n * V + k - 16], bh[e], bl[e]);
+            }
+            mma_tf32(d[nt], al, bh[0], bh[1]);
+            mma_tf32(d[nt], ah, bl[0], bl[1]);
+            mma_tf32(d[nt], ah, bh[0], bh[1]);
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            *reinterpret_cast<float2 *>(out + (g + 8 * h) * 16 + 8 * nt + 2 * q) =
+                make_float2(d[nt][2 * h], d[nt][2 * h + 1]);
+}
+
 // One tile = one sequence x TC steps, warp w owning L consecutive steps.
 // Each warp streams its steps through its own ring of NSL slots (1D bulk
 // copies completing on one mbarrier per slot): pass 1 folds them into the
@@ -1306,6 +1374,95 @@ __global__ void __launch_bounds__(Cf::NW * 32)
     put_block_smem<Cf>(xw, rb, cb, o);
     __syncwarp();
 
+    // ---- pass 2 of the k = 16 adjoint on [M | Lam] only: the running
+    //      product C (the first 16 columns of X) feeds the aggregates of pass
+    //      1 and no output, so pass 2 updates the W = 16 + v columns after it
+    //      with C2 = W / 8 columns per lane.
+    if constexpr (Cf::BWD && K == 16 && (K + VV) % 8 == 0 && MG_AFW_MMA_DA != 0) {
+        constexpr int C2 = (K + VV) / 8, WV = K + VV;
+#pragma unroll 1
+        for (int q = nvw; q < nq; ++q) {
+            const int64_t t = t0 + tile_step(q), s = step_index(t);
+            const float *slot = wait_slot(q);
+            // E rows (A_{t+1}^T) as in the full step; values [gA | gB] on the lane's columns
+            if (t + 1 < g.T) {
+#pragma unroll
+                for (int l = 0; l < K; ++l) {
+                    float a[R];
+                    ld_floats<R>(slot + l * K + rb * R, a);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) yc[r][l] = a[r];
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int l = 0; l < K; ++l) yc[r][l] = 0.f;
+            }
+            float y2[R][C2], o2[R][C2];
+            const int col0 = cb * C2;  // in [M | Lam]
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int row = rb * R + r;
+                if constexpr (C2 == 4) {
+                    if (col0 < K) ld_floats<4>(slot + Cf::OFF_G + row * K + col0, y2[r]);
+                    else ld_floats<4>(slot + Cf::OFF_GB + row * VV + col0 - K, y2[r]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < C2; ++c) {
+                        const int j = col0 + c;
+                        y2[r][c] = j < K ? slot[Cf::OFF_G + row * K + j] : slot[Cf::OFF_GB + row * VV + j - K];
+                    }
+                }
+            }
+            // o2 = E [M | Lam] + [gA | gB] on the lane's block
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int c = 0; c < C2; ++c) o2[r][c] = y2[r][c];
+#pragma unroll
+            for (int l = 0; l < K; ++l) {
+                float xv[C2];
+                ld_floats<C2>(xw + l * XS + K + col0, xv);
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int c = 0; c < C2; ++c) o2[r][c] = fmaf(yc[r][l], xv[c], o2[r][c]);
+            }
+            __syncwarp();  // every lane has read X
+#pragma unroll
+            for (int r = 0; r < R; ++r) st_floats<C2>(xw + (rb * R + r) * XS + K + col0, o2[r]);
+            __syncwarp();
+            // dB_t = Lam_t
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int row = rb * R + r;
+                if constexpr (C2 == 4) {
+                    if (col0 >= K) st_floats<4>(p.dB + s * KV + row * VV + col0 - K, o2[r]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < C2; ++c)
+                        if (col0 + c >= K) p.dB[s * KV + row * VV + col0 + c - K] = o2[r][c];
+                }
+            }
+            // dA_t = M_t Abar_{t-1}^T + Lam_t Bbar_{t-1}^T  (Abar_0 = I, Bbar_0 = 0)
+            if (t > 0) {
+                mma_dA16<XS, VV>(xw, slot + Cf::OFF_AP, slot + Cf::OFF_BP, lane, p.dA + s * KK);
+            } else {
+#pragma unroll
+                for (int e = 0; e < KK / 32; ++e) {
+                    const int idx = lane + 32 * e, a = idx / K, b2 = idx % K;
+                    p.dA[s * KK + idx] = xw[a * XS + K + b2];
+                }
+            }
+            (void)WV;
+            __syncwarp();  // the slot and xw are read by every lane before reuse
+            refill(q + NSL);
+        }
+        finish_cta(lb, epoch);
+        return;
+    }
+
     // ---- pass 2: re-run the warp's steps from its start state, write outputs
 #pragma unroll 1
     for (int q = nvw; q < nq; ++q) {
@@ -1352,6 +1509,14 @@ __global__ void __launch_bounds__(Cf::NW * 32)
             const float *xs = xw + (Cf::DB ? cur * MAT : 0);
             const float *Ap = slot + Cf::OFF_AP;
             const float *Bp = slot + Cf::OFF_BP;
+            if constexpr (MG_AFW_MMA_DA != 0 && K == 16 && VV % 8 == 0) {
+                if (t > 0) {
+                    mma_dA16<XS, VV>(xs, Ap, Bp, lane, p.dA + s * KK);
+                    __syncwarp();  // the slot and xw are read by every lane before reuse
+                    refill(q + NSL);
+                    continue;
+                }
+            }
             // the JD rows of Y first, then each row of X once
             float y[JD][WW];
 #pragma unroll
