@@ -58,7 +58,7 @@ def _ptr(x: np.ndarray):
 
 
 class Oracle:
-    """The five oracle functions bound to one build of the C source."""
+    """The oracle functions bound to one build of the C source."""
 
     def __init__(self, lib_path: str):
         lib = ctypes.CDLL(lib_path)
@@ -68,10 +68,11 @@ class Oracle:
         lib.orc_linear_scan_fwd.argtypes = [P, P, P, P, I64, I64, I64]
         lib.orc_linear_scan_bwd.argtypes = [P, P, P, P, P, P, P, I64, I64, I64]
         lib.orc_log_scan_fwd.argtypes = [P, P, P, I64, I64, I64]
+        lib.orc_log_scan_bwd.argtypes = [P, P, P, P, P, I64, I64, I64]
         lib.orc_affine_scan_fwd.argtypes = [P, P, P, P, I64, I64, I64, I, I]
         lib.orc_affine_scan_bwd.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I, I]
         for f in (lib.orc_linear_scan_fwd, lib.orc_linear_scan_bwd, lib.orc_log_scan_fwd,
-                  lib.orc_affine_scan_fwd, lib.orc_affine_scan_bwd):
+                  lib.orc_log_scan_bwd, lib.orc_affine_scan_fwd, lib.orc_affine_scan_bwd):
             f.restype = None
         self._lib = lib
 
@@ -102,6 +103,16 @@ class Oracle:
         h = np.empty_like(lc)
         self._lib.orc_log_scan_fwd(_ptr(lc), _ptr(lv), _ptr(h), B, T, D)
         return h
+
+    def log_scan_bwd(self, log_coeffs, log_values, gh):
+        """(dlog_coeffs (B,T,D), dlog_values (B,T+1,D)) for L = sum(gh * h)."""
+        lc, lv, g = _f64(log_coeffs), _f64(log_values), _f64(gh)
+        B, T, D = lc.shape
+        assert lv.shape == (B, T + 1, D) and g.shape == lc.shape
+        dlc = np.empty_like(lc)
+        dlv = np.empty_like(lv)
+        self._lib.orc_log_scan_bwd(_ptr(lc), _ptr(lv), _ptr(g), _ptr(dlc), _ptr(dlv), B, T, D)
+        return dlc, dlv
 
     def affine_scan_fwd(self, A, Bm):
         """(Abar, Bbar) for A (B,T,n,k,k), Bm (B,T,n,k,v)."""
@@ -149,6 +160,10 @@ def linear_scan_bwd(a, A, Bc, gA, gBc):
 
 def log_scan_fwd(log_coeffs, log_values):
     return _oracle().log_scan_fwd(log_coeffs, log_values)
+
+
+def log_scan_bwd(log_coeffs, log_values, gh):
+    return _oracle().log_scan_bwd(log_coeffs, log_values, gh)
 
 
 def affine_scan_fwd(A, Bm):

@@ -128,6 +128,45 @@ void orc_log_scan_fwd(const double *log_coeffs, const double *log_values, double
     free(h);
 }
 
+/*
+ * Log-space scan adjoint (the backward of parallel_scan_log_fwd, for
+ * training; the page lists only the forward op, the gradient is derived).
+ * For a loss L = sum_t gh_t * h_t with h_t = a_t h_{t-1} + b_t,
+ * a_t = exp(log_coeffs_t), b_t = exp(log_values_t), h_0 = exp(log_values_0):
+ *   mu_t        = gh_t + a_{t+1} * mu_{t+1}          (mu_T = gh_T)
+ *   dlog_coeffs_t = mu_t * a_t * h_{t-1}             t = 1..T
+ *   dlog_values_t = mu_t * b_t                        t = 1..T
+ *   dlog_values_0 = a_1 * mu_1 * h_0                  (dL/dh_0 times h_0)
+ * h is recomputed here in double from the inputs.  dlog_values has the shape
+ * of log_values, (B,T+1,D).
+ */
+void orc_log_scan_bwd(const double *log_coeffs, const double *log_values, const double *gh,
+                      double *dlog_coeffs, double *dlog_values, int64_t B, int64_t T, int64_t D)
+{
+    double *h = (double *)malloc((size_t)(T + 1) * sizeof(double));
+    for (int64_t bi = 0; bi < B; ++bi) {
+        for (int64_t d = 0; d < D; ++d) {
+            h[0] = exp(log_values[(bi * (T + 1)) * D + d]);
+            for (int64_t t = 1; t <= T; ++t)
+                h[t] = exp(log_coeffs[(bi * T + (t - 1)) * D + d]) * h[t - 1] +
+                       exp(log_values[(bi * (T + 1) + t) * D + d]);
+            double mu = 0.0;
+            for (int64_t t = T; t >= 1; --t) {
+                const int64_t crow = (bi * T + (t - 1)) * D + d;
+                const int64_t vrow = (bi * (T + 1) + t) * D + d;
+                const double a_next = t < T ? exp(log_coeffs[crow + D]) : 0.0;
+                mu = gh[crow] + a_next * mu;
+                dlog_coeffs[crow] = mu * exp(log_coeffs[crow]) * h[t - 1];
+                dlog_values[vrow] = mu * exp(log_values[vrow]);
+            }
+            /* after the loop mu = mu_1 */
+            const int64_t v0 = (bi * (T + 1)) * D + d;
+            dlog_values[v0] = T >= 1 ? exp(log_coeffs[(bi * T) * D + d]) * mu * h[0] : 0.0;
+        }
+    }
+    free(h);
+}
+
 /* C = X @ Y for row-major X (r x m), Y (m x c). */
 static void mat_mul(const double *X, const double *Y, double *C, int r, int m, int c)
 {

@@ -326,6 +326,76 @@ def pin_affine_adjoint_autograd(orc):
     np.testing.assert_allclose(dB, gB_t.numpy(), rtol=1e-11, atol=1e-11)
 
 
+def pin_golden_log_bwd(orc):
+    g = _golden("log_scan_bwd_T2.json")
+    lc = np.log(np.array(g["inputs"]["log_coeffs_exp"], dtype=np.float64))
+    lv = np.log(np.array(g["inputs"]["log_values_exp"], dtype=np.float64))
+    gh = np.array(g["inputs"]["gh"], dtype=np.float64)
+    dlc, dlv = orc.log_scan_bwd(lc, lv, gh)
+    np.testing.assert_allclose(dlc, np.array(g["expected"]["dlog_coeffs"]), rtol=1e-14)
+    np.testing.assert_allclose(dlv, np.array(g["expected"]["dlog_values"]), rtol=1e-14)
+
+
+def _loss_log(orc, lc, lv, gh):
+    return float(np.sum(gh * orc.log_scan_fwd(lc, lv)))
+
+
+def pin_log_adjoint_fd(orc):
+    """Central differences of L = sum(gh * h) in every log input."""
+    rng = np.random.default_rng(41)
+    lc = -rng.uniform(0.05, 1.5, size=(1, 6, 2))
+    lv = rng.normal(scale=0.7, size=(1, 7, 2))
+    gh = rng.normal(size=lc.shape)
+    dlc, dlv = orc.log_scan_bwd(lc, lv, gh)
+    eps = 1e-6
+    for arr, grad in ((lc, dlc), (lv, dlv)):
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + eps
+            lp = _loss_log(orc, lc, lv, gh)
+            arr[idx] = old - eps
+            lm = _loss_log(orc, lc, lv, gh)
+            arr[idx] = old
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(fd)), (idx, fd, grad[idx])
+
+
+def pin_log_adjoint_autograd(orc):
+    rng = np.random.default_rng(42)
+    lc = -rng.uniform(0.05, 2.0, size=(2, 9, 3))
+    lv = rng.normal(scale=0.8, size=(2, 10, 3))
+    gh = rng.normal(size=lc.shape)
+    tlc = torch.tensor(lc, requires_grad=True)
+    tlv = torch.tensor(lv, requires_grad=True)
+    h = torch.exp(tlv[:, 0])
+    hs = []
+    for t in range(lc.shape[1]):
+        h = torch.exp(tlc[:, t]) * h + torch.exp(tlv[:, t + 1])
+        hs.append(h)
+    L = (torch.stack(hs, 1) * torch.tensor(gh)).sum()
+    g_lc, g_lv = torch.autograd.grad(L, (tlc, tlv))
+    dlc, dlv = orc.log_scan_bwd(lc, lv, gh)
+    np.testing.assert_allclose(dlc, g_lc.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dlv, g_lv.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def pin_log_adjoint_vs_linear(orc):
+    """The chain rule through the linear op: h = A h0 + Bc with a = exp(lc),
+    b = exp(lv[1:]), so dL/dlc = da * a and dL/dlv[1:] = db * b for the
+    linear adjoint at gA = gh * h0, gBc = gh, and dL/dlv[0] = h0 sum_t gh_t A_t."""
+    rng = np.random.default_rng(43)
+    lc = -rng.uniform(0.01, 1.0, size=(2, 30, 4))
+    lv = rng.normal(scale=0.5, size=(2, 31, 4))
+    gh = rng.normal(size=lc.shape)
+    a, b, h0 = np.exp(lc), np.exp(lv[:, 1:]), np.exp(lv[:, :1])
+    A, Bc = orc.linear_scan_fwd(a, b)
+    da, db = orc.linear_scan_bwd(a, A, Bc, gh * h0, gh)
+    dlc, dlv = orc.log_scan_bwd(lc, lv, gh)
+    np.testing.assert_allclose(dlc, da * a, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dlv[:, 1:], db * b, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dlv[:, 0], h0[:, 0] * np.sum(gh * A, axis=1), rtol=1e-12, atol=1e-13)
+
+
 def pin_degenerate_shapes(orc):
     """T = 0 (and empty batch) give empty outputs; T = 1 is a single step."""
     e = np.zeros((2, 0, 3))
@@ -344,6 +414,7 @@ PINS = [
     pin_linear_closed_form, pin_linear_special_cases,
     pin_linear_adjoint_fd, pin_linear_adjoint_autograd,
     pin_log_vs_linear, pin_log_closed_form,
+    pin_golden_log_bwd, pin_log_adjoint_fd, pin_log_adjoint_autograd, pin_log_adjoint_vs_linear,
     pin_affine_k1_is_linear, pin_affine_diagonal_is_linear,
     pin_affine_running_product, pin_affine_orthogonal_invariant,
     pin_affine_adjoint_fd, pin_affine_adjoint_autograd,
@@ -369,6 +440,12 @@ MUTANTS = {
                               "const double A_prev = (t > 0) ? A[row + d] : 1.0;"),
     "log_value_slot": ("exp(log_values[vrow + d])", "exp(log_values[vrow - D + d])"),
     "log_dropped_h0": ("h[d] = exp(log_values[v0 + d]);", "h[d] = 0.0;"),
+    "log_bwd_coefficient_index": ("const double a_next = t < T ? exp(log_coeffs[crow + D]) : 0.0;",
+                                  "const double a_next = t < T ? exp(log_coeffs[crow]) : 0.0;"),
+    "log_bwd_halo_index": ("dlog_coeffs[crow] = mu * exp(log_coeffs[crow]) * h[t - 1];",
+                           "dlog_coeffs[crow] = mu * exp(log_coeffs[crow]) * h[t];"),
+    "log_bwd_dropped_slot0": ("dlog_values[v0] = T >= 1 ? exp(log_coeffs[(bi * T) * D + d]) * mu * h[0] : 0.0;",
+                              "dlog_values[v0] = 0.0;"),
     "affine_fwd_order": ("mat_mul(At, P, tmp, k, k, k);", "mat_mul(P, At, tmp, k, k, k);"),
     "affine_fwd_dropped_B": ("H[e] = tmp[e] + Bm[s * kv + e];", "H[e] = tmp[e];"),
     "affine_bwd_untransposed": ("mat_tmul(Anext, M, tmp, k, k, k);", "mat_mul(Anext, M, tmp, k, k, k);"),
