@@ -358,7 +358,15 @@ def run_extra(mg, dev, peak):
     out["mingru_log_16x2048x2048"] = {"op": "mg_log_scan_fwd", "ms": t * 1e3,
                                       "elements_per_s": n / t, "GB_s": byt / t / 1e9,
                                       "frac": byt / t / 1e9 / peak, "algorithmic_bytes": byt}
-    del lc, lv, h
+    # its adjoint: reads log_coeffs, log_values, h, gh; writes dlog_coeffs, dlog_values
+    gh = torch.randn(lc.shape, device=dev, generator=torch.Generator(dev).manual_seed(1))
+    dlc, dlv = torch.empty_like(lc), torch.empty_like(lv)
+    t = _time_op(lambda: mg.mg_log_scan_bwd(lc, lv, h, gh, out=(dlc, dlv)), 10, dev, flush)
+    byt = 24 * n + 8 * 16 * 2048
+    out["mingru_log_bwd_16x2048x2048"] = {"op": "mg_log_scan_bwd", "ms": t * 1e3,
+                                          "elements_per_s": n / t, "GB_s": byt / t / 1e9,
+                                          "frac": byt / t / 1e9 / peak, "algorithmic_bytes": byt}
+    del lc, lv, h, gh, dlc, dlv
     # affine scans
     fp32_peak_tflops = 152 * 128 * 2 * 2.07e9 / 1e12  # FFMA lanes x 2 flop x max SM clock
     for name, (Bq, Tq, nq, k, v) in (("haar_affine_4x2048x64_k4v4", (4, 2048, 64, 4, 4)),

@@ -7,6 +7,7 @@
  *   mg_linear_scan_fwd   <- linear_scan_fwd        ("Channel-tiled k=1 affine prefix scan")
  *   mg_linear_scan_bwd   <- linear_scan_bwd        ("Channel-tiled k=1 affine-scan adjoint")
  *   mg_log_scan_fwd      <- parallel_scan_log_fwd  ("Fused log-space forward scan")
+ *   mg_log_scan_bwd      <- its adjoint (derived; the page lists the forward only)
  *   mg_affine_scan_fwd   <- affine_scan_fwd        ("Generic k x k affine prefix scan")
  *   mg_affine_scan_bwd   <- affine_scan_bwd        ("Generic k x k affine-scan adjoint")
  *
@@ -87,7 +88,8 @@ const char *mg_last_error_detail(void);
  * for either input dtype.  Returns 0 for invalid (negative) sizes. */
 size_t mg_linear_scan_workspace_size(int64_t B, int64_t T, int64_t D);
 
-/* Workspace bytes for mg_log_scan_fwd on log_coeffs of shape (B,T,D). */
+/* Workspace bytes for mg_log_scan_fwd and mg_log_scan_bwd on log_coeffs of
+ * shape (B,T,D). */
 size_t mg_log_scan_workspace_size(int64_t B, int64_t T, int64_t D);
 
 /* Workspace bytes for mg_affine_scan_fwd and mg_affine_scan_bwd on
@@ -141,6 +143,26 @@ mg_status mg_linear_scan_bwd(const void *a, mg_dtype a_dt,
  * NaN.  h is (B,T,D) float32.
  */
 mg_status mg_log_scan_fwd(const float *log_coeffs, const float *log_values, float *h,
+                          int64_t B, int64_t T, int64_t D,
+                          void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Log-space scan adjoint (the backward of mg_log_scan_fwd for training; the
+ * page lists only the forward op, section "parallel_scan_log_fwd", and this
+ * is the gradient of its recurrence).  Inputs: log_coeffs (B,T,D),
+ * log_values (B,T+1,D), the forward output h (B,T,D) and the upstream
+ * gradient gh (B,T,D), all float32.  For L = sum_t gh_t h_t with
+ * a_t = exp(log_coeffs_t), b_t = exp(log_values_t), h_0 = exp(log_values_0):
+ *   mu_t = gh_t + a_{t+1} mu_{t+1}                    (mu_T = gh_T)
+ *   dlog_coeffs_t = mu_t a_t h_{t-1}                    t = 1..T
+ *   dlog_values_t = mu_t b_t (t = 1..T),   dlog_values_0 = a_1 mu_1 h_0
+ * dlog_coeffs is (B,T,D), dlog_values (B,T+1,D), both written in full (for
+ * T = 0, dlog_values is zero-filled).  The mu recurrence runs in linear
+ * space: coefficients a_t <= 1 (log_coeffs <= 0, as in minGRU) keep it in
+ * range.  Workspace: mg_log_scan_workspace_size covers this call too.
+ */
+mg_status mg_log_scan_bwd(const float *log_coeffs, const float *log_values, const float *h,
+                          const float *gh, float *dlog_coeffs, float *dlog_values,
                           int64_t B, int64_t T, int64_t D,
                           void *ws, size_t ws_bytes, cudaStream_t stream);
 

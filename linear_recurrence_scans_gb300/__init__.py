@@ -12,6 +12,8 @@ Ops (names of the C entry points; aliases with the names of the page
 * ``mg_linear_scan_fwd(a, b)              -> (A, Bc)``       alias ``linear_scan_fwd``
 * ``mg_linear_scan_bwd(a, A, Bc, gA, gBc) -> (da, db)``      alias ``linear_scan_bwd``
 * ``mg_log_scan_fwd(log_coeffs, log_values) -> h``           alias ``parallel_scan_log_fwd``
+* ``mg_log_scan_bwd(log_coeffs, log_values, h, gh) -> (dlog_coeffs, dlog_values)``
+  alias ``parallel_scan_log_bwd`` (the adjoint of the log-space scan)
 * ``mg_affine_scan_fwd(A, Bm)             -> (Abar, Bbar)``  alias ``affine_scan_fwd``
 * ``mg_affine_scan_bwd(A, Abar, Bbar, gAbar, gBbar) -> (dA, dB)``  alias ``affine_scan_bwd``
 
@@ -33,9 +35,9 @@ from . import _build
 
 __all__ = [
     "MgScanError", "load", "library_path",
-    "mg_linear_scan_fwd", "mg_linear_scan_bwd", "mg_log_scan_fwd",
+    "mg_linear_scan_fwd", "mg_linear_scan_bwd", "mg_log_scan_fwd", "mg_log_scan_bwd",
     "mg_affine_scan_fwd", "mg_affine_scan_bwd",
-    "linear_scan_fwd", "linear_scan_bwd", "parallel_scan_log_fwd",
+    "linear_scan_fwd", "linear_scan_bwd", "parallel_scan_log_fwd", "parallel_scan_log_bwd",
     "affine_scan_fwd", "affine_scan_bwd",
     "linear_workspace_size", "log_workspace_size", "affine_workspace_size",
     "workspace_status", "new_workspace",
@@ -48,7 +50,7 @@ SYMBOLS = (
     "mg_abi_version", "mg_strerror", "mg_last_error_detail",
     "mg_linear_scan_workspace_size", "mg_log_scan_workspace_size",
     "mg_affine_scan_workspace_size", "mg_workspace_init", "mg_workspace_status",
-    "mg_linear_scan_fwd", "mg_linear_scan_bwd", "mg_log_scan_fwd",
+    "mg_linear_scan_fwd", "mg_linear_scan_bwd", "mg_log_scan_fwd", "mg_log_scan_bwd",
     "mg_affine_scan_fwd", "mg_affine_scan_bwd",
 )
 
@@ -101,6 +103,7 @@ def load():
         lib.mg_linear_scan_fwd.argtypes = [vp, vp, i32, vp, vp, i64, i64, i64, vp, sz, vp]
         lib.mg_linear_scan_bwd.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, sz, vp]
         lib.mg_log_scan_fwd.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
+        lib.mg_log_scan_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, sz, vp]
         lib.mg_affine_scan_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, vp, sz, vp]
         lib.mg_affine_scan_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, i32,
                                            vp, sz, vp]
@@ -112,8 +115,8 @@ def load():
         lib.mg_linear_scan_fwd_noalloc_max_scratch.argtypes = []
         lib.mg_linear_scan_fwd_noalloc_max_scratch.restype = sz
         for name in ("mg_workspace_init", "mg_workspace_status", "mg_linear_scan_fwd",
-                     "mg_linear_scan_bwd", "mg_log_scan_fwd", "mg_affine_scan_fwd",
-                     "mg_affine_scan_bwd"):
+                     "mg_linear_scan_bwd", "mg_log_scan_fwd", "mg_log_scan_bwd",
+                     "mg_affine_scan_fwd", "mg_affine_scan_bwd"):
             getattr(lib, name).restype = st
         _lib = lib
     return _lib
@@ -260,6 +263,29 @@ def mg_log_scan_fwd(log_coeffs, log_values, *, out=None, ws=None, stream=None):
     return h
 
 
+def mg_log_scan_bwd(log_coeffs, log_values, h, gh, *, out=None, ws=None, stream=None):
+    """(dlog_coeffs (B,T,D), dlog_values (B,T+1,D)) float32: gradients of
+    sum(gh * h) for h = mg_log_scan_fwd(log_coeffs, log_values)."""
+    lc = _prep(log_coeffs, "log_coeffs")
+    lv = _prep(log_values, "log_values")
+    h = _prep(h, "h")
+    gh = _prep(gh, "gh")
+    if lc.dim() != 3:
+        raise ValueError("log_coeffs must be (B, T, D)")
+    B, T, D = lc.shape
+    if tuple(lv.shape) != (B, T + 1, D) or h.shape != lc.shape or gh.shape != lc.shape:
+        raise ValueError("log_values must be (B, T+1, D); h and gh (B, T, D)")
+    dlc = _out(out, 0, lc.shape, lc)
+    dlv = _out(out, 1, lv.shape, lc)
+    sh = _stream_handle(stream, lc.device)
+    w = _workspace(log_workspace_size(B, T, D), lc.device, sh, ws)
+    _check(load().mg_log_scan_bwd(lc.data_ptr(), lv.data_ptr(), h.data_ptr(), gh.data_ptr(),
+                                  dlc.data_ptr(), dlv.data_ptr(), B, T, D, w.data_ptr(),
+                                  w.numel(), sh),
+           "mg_log_scan_bwd")
+    return dlc, dlv
+
+
 def mg_affine_scan_fwd(A, Bm, *, out=None, ws=None, stream=None):
     """(Abar, Bbar) for A (B,T,n,k,k), Bm (B,T,n,k,v), float32."""
     A = _prep(A, "A")
@@ -318,5 +344,6 @@ def mg_linear_scan_fwd_noalloc(a, b, *, out=None, stream=None):
 linear_scan_fwd = mg_linear_scan_fwd
 linear_scan_bwd = mg_linear_scan_bwd
 parallel_scan_log_fwd = mg_log_scan_fwd
+parallel_scan_log_bwd = mg_log_scan_bwd
 affine_scan_fwd = mg_affine_scan_fwd
 affine_scan_bwd = mg_affine_scan_bwd

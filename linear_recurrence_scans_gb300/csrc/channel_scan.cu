@@ -1,5 +1,6 @@
 // Channel-wise chunked scans on (B,T,D): linear_scan_fwd, linear_scan_bwd and
-// parallel_scan_log_fwd of the page "minGRU - Triton kernels".
+// parallel_scan_log_fwd of the page "minGRU - Triton kernels", and the
+// adjoint of the log-space scan.
 //
 // All three evaluate the same associative pair operator
 //     (a1, b1) o (a2, b2) = (a2 a1, a2 b1 + b2)        (element 1 earlier)
@@ -381,6 +382,127 @@ struct LogFwd {
     }
 };
 
+// ------------------------------------------------------ log-space adjoint
+// Gradient of the log-space scan for L = sum_t gh_t h_t (the forward's
+// recurrence h_t = a_t h_{t-1} + b_t, a_t = exp(lc_t), b_t = exp(lv_t)).
+// Reverse time, element of step t: (c_t = a_{t+1}, gh_t) with c_T = 0; state
+// (C, mu): mu_t = gh_t + a_{t+1} mu_{t+1}.  Epilogue: dlc_t = mu_t a_t h_{t-1}
+// (h_0 = exp(lv_0)), dlv_t = mu_t b_t, and dlv_0 = a_1 mu_1 h_0 = dlc_1.
+// A round loads L + 1 rows of lc, so a_t and a_{t+1} share the exponentials.
+template <int VEC_, int L_>
+struct LogBwd {
+    static constexpr int NS = 2, VEC = VEC_, L = L_;
+    static constexpr bool kReverse = true;
+    using S = St<NS, VEC>;
+    struct Args {
+        const float *lc;
+        const float *lv;
+        const float *h;
+        const float *gh;
+        float *dlc;
+        float *dlv;
+    };
+    struct Regs {
+        float ea[L + 1][VEC];  // exp(lc) of steps t0 .. t0+L (0 past T)
+        float g[L][VEC];
+        int nval;              // steps of the round that are < T
+    };
+
+    __device__ static void load(const Args &p, const ChanGeom &g, int64_t bb, int64_t t0, int d,
+                                bool act, Regs &r)
+    {
+        const int64_t rem = g.T - t0;
+        r.nval = act ? int(rem < 0 ? 0 : (rem > L ? L : rem)) : 0;
+#pragma unroll
+        for (int i = 0; i <= L; ++i) {
+            const int64_t t = t0 + i;
+            if (act && t < g.T) {
+                load_vec<VEC>(p.lc + (bb * g.T + t) * g.D + d, r.ea[i]);
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) r.ea[i][v] = ex2_sub(r.ea[i][v] * kLog2eF);
+            } else {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) r.ea[i][v] = 0.f;
+            }
+            if (i < L) {
+                if (act && t < g.T) {
+                    load_vec<VEC>(p.gh + (bb * g.T + t) * g.D + d, r.g[i]);
+                } else {
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) r.g[i][v] = 0.f;
+                }
+            }
+        }
+    }
+    __device__ static S element(const Regs &r, int i)
+    {
+        S e;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            e.v[0][v] = i < r.nval ? r.ea[i + 1][v] : 1.f;  // past T: the identity
+            e.v[1][v] = r.g[i][v];
+        }
+        return e;
+    }
+    __device__ static S identity()
+    {
+        S e;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            e.v[0][v] = 1.f;
+            e.v[1][v] = 0.f;
+        }
+        return e;
+    }
+    __device__ static S initial(const Args &, const ChanGeom &, int64_t, int, bool)
+    {
+        return identity();
+    }
+    __device__ static S combine(const S &x, const S &y)
+    {
+        S o;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            o.v[0][v] = y.v[0][v] * x.v[0][v];
+            o.v[1][v] = fmaf(y.v[0][v], x.v[1][v], y.v[1][v]);
+        }
+        return o;
+    }
+    __device__ static void epilogue(const Args &p, const ChanGeom &g, int64_t bb, int64_t t0,
+                                    int d, bool act, const Regs &r, S &st)
+    {
+        float mu[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) mu[v] = st.v[1][v];
+#pragma unroll
+        for (int i = L - 1; i >= 0; --i) {
+            if (i < r.nval) {
+                const int64_t t = t0 + i;
+                float hp[VEC], lvv[VEC], dlc[VEC], dlv[VEC];
+                if (t > 0) {
+                    load_vec<VEC>(p.h + (bb * g.T + t - 1) * g.D + d, hp);
+                } else {
+                    load_vec<VEC>(p.lv + (bb * (g.T + 1)) * g.D + d, hp);
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) hp[v] = ex2_sub(hp[v] * kLog2eF);
+                }
+                load_vec<VEC>(p.lv + (bb * (g.T + 1) + t + 1) * g.D + d, lvv);
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    mu[v] = fmaf(r.ea[i + 1][v], mu[v], r.g[i][v]);
+                    dlc[v] = mu[v] * r.ea[i][v] * hp[v];
+                    dlv[v] = mu[v] * ex2_sub(lvv[v] * kLog2eF);
+                }
+                store_vec<VEC>(p.dlc + (bb * g.T + t) * g.D + d, dlc);
+                store_vec<VEC>(p.dlv + (bb * (g.T + 1) + t + 1) * g.D + d, dlv);
+                if (t == 0) store_vec<VEC>(p.dlv + (bb * (g.T + 1)) * g.D + d, dlc);
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) st.v[1][v] = mu[v];
+    }
+};
+
 // Tile choices (threads along channels TX, thread rows TY, steps per thread
 // and round L, minimum resident CTAs per SM, rounds per thread R).  fp32: 4 channels (16 B) per thread;
 // bf16: 8 channels (16 B).  A D that is not a multiple of the vector width
@@ -463,6 +585,21 @@ struct LogFwd {
 #ifndef MG_LOG_R
 #define MG_LOG_R 2
 #endif
+#ifndef MG_LOGB_TX
+#define MG_LOGB_TX 32
+#endif
+#ifndef MG_LOGB_TY
+#define MG_LOGB_TY 8
+#endif
+#ifndef MG_LOGB_L
+#define MG_LOGB_L 2
+#endif
+#ifndef MG_LOGB_MB
+#define MG_LOGB_MB 4
+#endif
+#ifndef MG_LOGB_R
+#define MG_LOGB_R 4
+#endif
 constexpr int kTX = 32, kTY = 8;
 using LinFwdF32 = ChanPlan<LinFwd<float, 4, MG_LINF_L>, MG_LINF_TX, MG_LINF_TY, MG_LINF_MB, MG_LINF_R>;
 using LinFwdF32s = ChanPlan<LinFwd<float, 1, 8>, kTX, kTY>;
@@ -473,6 +610,8 @@ using LinBwdF32s = ChanPlan<LinBwd<float, 1, 4>, kTX, kTY>;
 using LinBwdB16 = ChanPlan<LinBwd<bf16_t, 4, MG_LINB16_L>, MG_LINB16_TX, MG_LINB16_TY, MG_LINB16_MB, MG_LINB16_R>;
 using LinBwdB16s = ChanPlan<LinBwd<bf16_t, 1, 4>, kTX, kTY>;
 using LogF32 = ChanPlan<LogFwd<4, MG_LOG_L>, MG_LOG_TX, MG_LOG_TY, MG_LOG_MB, MG_LOG_R>;
+using LogBwdF32 = ChanPlan<LogBwd<4, MG_LOGB_L>, MG_LOGB_TX, MG_LOGB_TY, MG_LOGB_MB, MG_LOGB_R>;
+using LogBwdF32s = ChanPlan<LogBwd<1, 4>, kTX, kTY>;
 using LogF32s = ChanPlan<LogFwd<1, 8>, kTX, kTY>;
 
 }  // namespace
@@ -516,8 +655,11 @@ size_t linear_ws_bytes(int64_t B, int64_t T, int64_t D, const LaunchOpts &o)
 
 size_t log_ws_bytes(int64_t B, int64_t T, int64_t D, const LaunchOpts &o)
 {
-    if (o.engine == LaunchOpts::kStream && stream_log_ok(D)) return stream_log_ws_bytes(B, T, D);
-    return D % 4 == 0 ? LogF32::ws_bytes(B, T, D) : LogF32s::ws_bytes(B, T, D);
+    size_t f;
+    if (o.engine == LaunchOpts::kStream && stream_log_ok(D)) f = stream_log_ws_bytes(B, T, D);
+    else f = D % 4 == 0 ? LogF32::ws_bytes(B, T, D) : LogF32s::ws_bytes(B, T, D);
+    const size_t b = D % 4 == 0 ? LogBwdF32::ws_bytes(B, T, D) : LogBwdF32s::ws_bytes(B, T, D);
+    return f > b ? f : b;
 }
 
 mg_status launch_linear_fwd(const void *a, const void *b, mg_dtype dt, float *A, float *Bc,
@@ -555,6 +697,15 @@ mg_status launch_linear_bwd(const void *a, mg_dtype dt, const float *A, const fl
     if (D % 4 == 0)
         return LinBwdB16::launch({H(a), A, Bc, gA, gBc, da, db}, B, T, D, ws, wsb, s, o, nm);
     return LinBwdB16s::launch({H(a), A, Bc, gA, gBc, da, db}, B, T, D, ws, wsb, s, o, nm);
+}
+
+mg_status launch_log_bwd(const float *lc, const float *lv, const float *h, const float *gh,
+                         float *dlc, float *dlv, int64_t B, int64_t T, int64_t D, void *ws,
+                         size_t wsb, cudaStream_t s, const LaunchOpts &o)
+{
+    const char *nm = "mg_log_scan_bwd";
+    if (D % 4 == 0) return LogBwdF32::launch({lc, lv, h, gh, dlc, dlv}, B, T, D, ws, wsb, s, o, nm);
+    return LogBwdF32s::launch({lc, lv, h, gh, dlc, dlv}, B, T, D, ws, wsb, s, o, nm);
 }
 
 mg_status launch_log_fwd(const float *lc, const float *lv, float *h, int64_t B, int64_t T,

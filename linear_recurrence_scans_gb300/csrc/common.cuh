@@ -69,6 +69,9 @@ mg_status launch_linear_bwd(const void *a, mg_dtype dt, const float *A, const fl
                             const float *gA, const float *gBc, float *da, float *db,
                             int64_t B, int64_t T, int64_t D, void *ws, size_t ws_bytes,
                             cudaStream_t s, const LaunchOpts &o);
+mg_status launch_log_bwd(const float *lc, const float *lv, const float *h, const float *gh,
+                         float *dlc, float *dlv, int64_t B, int64_t T, int64_t D, void *ws,
+                         size_t wsb, cudaStream_t s, const LaunchOpts &o);
 mg_status launch_log_fwd(const float *lc, const float *lv, float *h, int64_t B, int64_t T,
                          int64_t D, void *ws, size_t ws_bytes, cudaStream_t s,
                          const LaunchOpts &o);

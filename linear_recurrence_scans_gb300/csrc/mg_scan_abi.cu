@@ -274,6 +274,33 @@ mg_status mg_log_scan_fwd(const float *log_coeffs, const float *log_values, floa
     return launch_log_fwd(log_coeffs, log_values, h, B, T, D, ws, ws_bytes, stream, default_opts());
 }
 
+mg_status mg_log_scan_bwd(const float *log_coeffs, const float *log_values, const float *h,
+                          const float *gh, float *dlog_coeffs, float *dlog_values, int64_t B,
+                          int64_t T, int64_t D, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    const char *fn = "mg_log_scan_bwd";
+    g_detail[0] = 0;
+    MG_TRY(check_dims(fn, {B, T + 1, D}));
+    if (T < 0) return fail(MG_ERR_INVALID_ARG, "%s: negative size", fn);
+    if (B == 0 || D == 0) return MG_OK;
+    const size_t n = size_t(B) * T * D, nv = size_t(B) * (T + 1) * D;
+    if (T == 0) {  // L does not depend on h_0: its gradient is zero
+        MG_TRY(check_bufs(fn, {{dlog_values, nv * 4, "dlog_values", true}}));
+        const cudaError_t e = cudaMemsetAsync(dlog_values, 0, nv * 4, stream);
+        return e == cudaSuccess ? MG_OK : fail(MG_ERR_LAUNCH, "%s: %s", fn, cudaGetErrorString(e));
+    }
+    MG_TRY(check_ws(fn, ws, ws_bytes, log_ws_bytes(B, T, D, default_opts())));
+    MG_TRY(check_bufs(fn, {{log_coeffs, n * 4, "log_coeffs", false},
+                           {log_values, nv * 4, "log_values", false},
+                           {h, n * 4, "h", false},
+                           {gh, n * 4, "gh", false},
+                           {dlog_coeffs, n * 4, "dlog_coeffs", true},
+                           {dlog_values, nv * 4, "dlog_values", true},
+                           {ws, ws_bytes, "workspace", true}}));
+    return launch_log_bwd(log_coeffs, log_values, h, gh, dlog_coeffs, dlog_values, B, T, D, ws,
+                          ws_bytes, stream, default_opts());
+}
+
 mg_status mg_affine_scan_fwd(const float *A, const float *Bm, float *Abar, float *Bbar, int64_t B,
                              int64_t T, int64_t n, int k, int v, void *ws, size_t ws_bytes,
                              cudaStream_t stream)

@@ -7,7 +7,7 @@ Cases (inputs seeded, resident on cuda:0 before the first launch):
   linear_fwd / linear_bwd        minGRU linear scan, B=8 T=4096 D=1024, fp32
   linear_bf16_fwd / _bwd         minGRU linear scan, B=4 T=8192 D=4096, bf16 a, b
                                  (a quarter of the 2^31-element workload, same tiles)
-  log_fwd                        minGRU log-space scan, B=8 T=2048 D=2048
+  log_fwd / log_bwd              minGRU log-space scan and its adjoint, B=8 T=2048 D=2048
   affine4_fwd / affine4_bwd      Haar affine scan, B=4 T=2048 n=64 k=v=4
   affine16_fwd / affine16_bwd    Haar affine scan, B=2 T=1024 n=32 k=v=16
 
@@ -24,7 +24,7 @@ import torch
 import linear_recurrence_scans_gb300 as mg
 from linear_recurrence_scans_gb300 import workloads as wl
 
-CASES = ("linear_fwd", "linear_bwd", "linear_bf16_fwd", "linear_bf16_bwd", "log_fwd",
+CASES = ("linear_fwd", "linear_bwd", "linear_bf16_fwd", "linear_bf16_bwd", "log_fwd", "log_bwd",
          "affine4_fwd", "affine4_bwd", "affine16_fwd", "affine16_bwd")
 
 
@@ -48,11 +48,16 @@ def main(argv):
                 mg.linear_scan_fwd(a, b, out=(A, Bc))
             else:
                 mg.linear_scan_bwd(a, A, Bc, gA, gBc, out=(da, db))
-    elif case == "log_fwd":
+    elif case.startswith("log"):
         lc, lv = wl.mingru_log(8, 2048, 2048, seed=0, device=dev)
-        h = torch.empty_like(lc)
+        h = mg.parallel_scan_log_fwd(lc, lv)
+        gh = torch.randn(lc.shape, device=dev, generator=torch.Generator(dev).manual_seed(1))
+        dlc, dlv = torch.empty_like(lc), torch.empty_like(lv)
         for _ in range(reps):
-            mg.parallel_scan_log_fwd(lc, lv, out=h)
+            if case == "log_fwd":
+                mg.parallel_scan_log_fwd(lc, lv, out=h)
+            else:
+                mg.parallel_scan_log_bwd(lc, lv, h, gh, out=(dlc, dlv))
     else:
         k = 4 if case.startswith("affine4") else 16
         shape = (4, 2048, 64) if k == 4 else (2, 1024, 32)

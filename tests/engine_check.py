@@ -23,7 +23,7 @@ import linear_recurrence_scans_gb300 as mg  # noqa: E402
 import oracle  # noqa: E402
 from linear_recurrence_scans_gb300 import workloads as wl  # noqa: E402
 from parity import (TOL_BF16, TOL_F32, affine_bwd_errors, affine_fwd_errors,  # noqa: E402
-                    linear_bwd_errors, linear_fwd_errors, log_fwd_errors)
+                    linear_bwd_errors, linear_fwd_errors, log_bwd_errors, log_fwd_errors)
 
 DEV = "cuda"
 
@@ -51,6 +51,10 @@ def main() -> int:
         lc, lv = wl.mingru_log(*shape, seed=22)
         h = mg.parallel_scan_log_fwd(lc.to(DEV), lv.to(DEV))
         report(f"log_fwd {shape}", log_fwd_errors(lc, lv, h), TOL_F32)
+        gh = torch.randn(lc.shape, generator=torch.Generator().manual_seed(26))
+        h32 = torch.from_numpy(oracle.log_scan_fwd(lc, lv)).float()
+        dlc, dlv = mg.parallel_scan_log_bwd(lc.to(DEV), lv.to(DEV), h32.to(DEV), gh.to(DEV))
+        report(f"log_bwd {shape}", log_bwd_errors(lc, lv, gh, dlc, dlv), TOL_F32)
 
     for (B, T, n), k, v in (((2, 333, 5), 2, 2), ((2, 333, 5), 4, 4), ((1, 700, 3), 4, 16),
                             ((2, 200, 3), 8, 8), ((2, 150, 3), 16, 16)):

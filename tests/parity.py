@@ -95,6 +95,16 @@ def log_fwd_errors(lc, lv, h) -> dict:
     return {"h": scaled_error(_np(h), oracle.log_scan_fwd(lc, lv))}
 
 
+def log_bwd_errors(lc, lv, gh, dlc, dlv) -> dict:
+    """The log-space adjoint's outputs are sums of signed terms (mu carries the
+    sign of gh): S is the oracle on |gh|, the componentwise condition scale."""
+    import oracle
+    rdlc, rdlv = oracle.log_scan_bwd(lc, lv, gh)
+    Sdlc, Sdlv = oracle.log_scan_bwd(lc, lv, np.abs(_np(gh)))
+    return {"dlog_coeffs": scaled_error(_np(dlc), rdlc, Sdlc),
+            "dlog_values": scaled_error(_np(dlv), rdlv, Sdlv)}
+
+
 def affine_fwd_errors(A, Bm, Abar, Bbar) -> dict:
     import oracle
     rAbar, rBbar = oracle.affine_scan_fwd(A, Bm)
