@@ -941,9 +941,6 @@ struct AffPtrs {
 
 // Lane block of the combine (x earlier, full matrix in shared memory) o
 // (y later, rows `yc` = y.C[rows][0..K) and `yv` = y.V on the lane's columns).
-#ifndef MG_AFW_HOIST
-#define MG_AFW_HOIST 0
-#endif
 template <class Cf>
 __device__ __forceinline__ void block_gemm(const float *xs, const float (&yc)[Cf::R][Cf::K],
                                            const float (&yv)[Cf::R][Cf::CC], int cb,
@@ -953,27 +950,14 @@ __device__ __forceinline__ void block_gemm(const float *xs, const float (&yc)[Cf
     for (int r = 0; r < Cf::R; ++r)
 #pragma unroll
         for (int c = 0; c < Cf::CC; ++c) o[r][c] = yv[r][c];
-    if constexpr (MG_AFW_HOIST != 0) {
-        // every row of X first, then the FMAs with no load in between
-        float xv[Cf::K][Cf::CC];
 #pragma unroll
-        for (int l = 0; l < Cf::K; ++l) ld_floats<Cf::CC>(xs + l * Cf::XS + cb * Cf::CC, xv[l]);
+    for (int l = 0; l < Cf::K; ++l) {
+        float xv[Cf::CC];
+        ld_floats<Cf::CC>(xs + l * Cf::XS + cb * Cf::CC, xv);
 #pragma unroll
-        for (int l = 0; l < Cf::K; ++l)
+        for (int r = 0; r < Cf::R; ++r)
 #pragma unroll
-            for (int r = 0; r < Cf::R; ++r)
-#pragma unroll
-                for (int c = 0; c < Cf::CC; ++c) o[r][c] = fmaf(yc[r][l], xv[l][c], o[r][c]);
-    } else {
-#pragma unroll
-        for (int l = 0; l < Cf::K; ++l) {
-            float xv[Cf::CC];
-            ld_floats<Cf::CC>(xs + l * Cf::XS + cb * Cf::CC, xv);
-#pragma unroll
-            for (int r = 0; r < Cf::R; ++r)
-#pragma unroll
-                for (int c = 0; c < Cf::CC; ++c) o[r][c] = fmaf(yc[r][l], xv[c], o[r][c]);
-        }
+            for (int c = 0; c < Cf::CC; ++c) o[r][c] = fmaf(yc[r][l], xv[c], o[r][c]);
     }
 }
 

@@ -17,11 +17,6 @@
 namespace mg {
 namespace {
 
-#ifndef MG_CHUNK_PREFETCH
-#define MG_CHUNK_PREFETCH 0
-#endif
-constexpr bool kChunkPrefetch = MG_CHUNK_PREFETCH != 0;
-
 struct ChanGeom {
     int64_t B, T, D;
     int nJb;  // channel tiles per batch row
@@ -179,12 +174,6 @@ __global__ void __launch_bounds__(TX *TY, MINB)
     }
 #pragma unroll
     for (int s = 0; s < NS; ++s) store_vec<VEC>(&s_agg[((ty) * NS + s) * DC + tx * VEC], agg.v[s]);
-    // With MG_CHUNK_PREFETCH (one round only), pass 2's loads are issued
-    // here, before the barrier that waits for the look-back, so their latency
-    // overlaps it.
-    constexpr bool kPrefetch = kChunkPrefetch && R == 1;
-    typename Op::Regs r2;
-    if constexpr (kPrefetch) Op::load(args, g, bb, round_t0(0), d, act, r2);
     __syncthreads();
 
     S excl = Op::identity(), cta_keep = Op::identity();
@@ -237,14 +226,11 @@ __global__ void __launch_bounds__(TX *TY, MINB)
     }
     // Pass 2: re-read the steps and re-run them from the start state; the
     // epilogue leaves in `st` the state after its round.
-    if constexpr (kPrefetch) {
-        Op::epilogue(args, g, bb, round_t0(0), d, act, r2, st);
-    } else {
 #pragma unroll 1
-        for (int k = 0; k < R; ++k) {
-            Op::load(args, g, bb, round_t0(k), d, act, r2);
-            Op::epilogue(args, g, bb, round_t0(k), d, act, r2, st);
-        }
+    for (int k = 0; k < R; ++k) {
+        typename Op::Regs r2;
+        Op::load(args, g, bb, round_t0(k), d, act, r2);
+        Op::epilogue(args, g, bb, round_t0(k), d, act, r2, st);
     }
     finish_cta(lb, epoch);
 }
