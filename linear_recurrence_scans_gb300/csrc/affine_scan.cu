@@ -9,18 +9,21 @@
 //           V = [M_t | Lam_t]; outputs dB_t = Lam_t and
 //           dA_t = M_t Abar_{t-1}^T + Lam_t Bbar_{t-1}^T.
 //
-// Two kernel shapes:
-//   * k <= 4: one thread owns one sequence's whole state (k x (k + w) floats
-//     in registers) for L steps; 32 sequences x TY sub-chunks per CTA on the
-//     generic chunk engine (scan_engine.cuh).
+// Kernel shapes:
+//   * k <= 4 (k = 4 with v <= 8, k = 2 with v >= 2): one lane owns one
+//     sequence's whole state (k x (k + w) floats in registers); each warp
+//     streams its steps through a ring of asynchronous copies
+//     (affine_lane_kernel below).  The other small shapes keep the state in
+//     one thread on the generic chunk engine (scan_engine.cuh).
 //   * k in {8, 16}: one warp owns one sequence's sub-chunk of L steps; the
 //     state X = [C | V] (k x (k + w), padded to a multiple of 8 columns) is
 //     split into 4 row blocks x 8 column blocks, one per lane.  Each step
 //     X <- E_C X + [0 | E_V] reads the column strip of X that the lane needs
-//     from a double-buffered shared copy (one __syncwarp per step) and the
-//     lane's rows of E_C straight from global memory.  A CTA of NW warps
-//     covers NW*L consecutive steps of one sequence and takes part in the
-//     same decoupled look-back as every other scan (lookback.cuh).
+//     from a shared copy and the lane's rows of E_C from the warp's ring of
+//     bulk copies (affine_warp_kernel below).  A CTA of NW warps covers NW*L
+//     consecutive steps of one sequence.
+// Every shape takes part in the same decoupled look-back as the other scans
+// (lookback.cuh).
 #include <type_traits>
 
 #include "stream_engine.cuh"

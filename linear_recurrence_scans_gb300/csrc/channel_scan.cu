@@ -2,25 +2,27 @@
 // parallel_scan_log_fwd of the page "minGRU - Triton kernels", and the
 // adjoint of the log-space scan.
 //
-// All three evaluate the same associative pair operator
+// All of them evaluate the same associative pair operator
 //     (a1, b1) o (a2, b2) = (a2 a1, a2 b1 + b2)        (element 1 earlier)
-// over time, independently for every channel (b, d), in one kernel shape:
+// over time, independently for every channel (b, d), in one kernel shape
+// (scan_engine.cuh):
 //
-//   * a CTA owns a tile of DC = TX*VEC channels by TY*L time steps, taken by
-//     ticket (chunk-major, so predecessors have always started);
+//   * a CTA owns a tile of DC = TX*VEC channels by TY*L*R time steps, taken
+//     by ticket (chunk-major, so predecessors have always started);
 //   * each thread loads VEC channels (one 16-byte vector) for L consecutive
-//     steps straight into registers -- a warp row reads 32 x 16 contiguous
-//     bytes, fully coalesced -- and folds them into its aggregate;
-//   * the TY thread aggregates of a channel are combined through shared memory;
+//     steps at a time straight into registers -- a warp row reads up to
+//     32 x 16 contiguous bytes, fully coalesced -- and folds its R rounds of
+//     L steps into its aggregate;
+//   * the TY thread aggregates of a channel are folded through shared memory,
+//     leaving each row its exclusive prefix within the tile;
 //   * warp 0 finds the chunk's carry-in by decoupled look-back over the
 //     previous chunks of the same channel tile (lookback.cuh);
-//   * every thread composes carry o (aggregates of the earlier threads of its
-//     chunk) and re-runs its L steps sequentially from that state, writing the
-//     outputs.  The re-run keeps the inputs in registers, so each input is read
-//     from HBM once and each output written once.
+//   * every thread composes carry o (its row's prefix) and re-runs its steps
+//     from that state, re-reading them (now from L2) and writing the outputs,
+//     so each input is read from HBM once and each output written once.
 //
-// The backward op is the same engine run in reverse time on the adjoint
-// recurrence; the log op carries log-space values as (m, s) with
+// The backward ops are the same engine run in reverse time on the adjoint
+// recurrences; the log op carries log-space values as (m, s) with
 // value = s * e^m so that one exp2 per combine suffices.
 #include <cmath>
 
