@@ -165,6 +165,11 @@ def _workspace(nbytes: int, device, stream_handle: int, ws):
     key = (device.index, stream_handle)
     buf = _ws_cache.get(key)
     if buf is None or buf.numel() < nbytes:
+        if buf is not None:
+            # Kernels on the op's stream (which torch's allocator does not
+            # track for this buffer) may still use the smaller workspace:
+            # let them finish before it can be freed and reused.
+            torch.cuda.synchronize(device)
         # Zero-filled on the current stream; wait for it so that the op's
         # stream (possibly another one) sees a cleared workspace.
         buf = new_workspace(int(nbytes * 1.25) + 4096, device)
