@@ -446,6 +446,13 @@ MUTANTS = {
                            "dlog_coeffs[crow] = mu * exp(log_coeffs[crow]) * h[t];"),
     "log_bwd_dropped_slot0": ("dlog_values[v0] = T >= 1 ? exp(log_coeffs[(bi * T) * D + d]) * mu * h[0] : 0.0;",
                               "dlog_values[v0] = 0.0;"),
+    "linear_fwd_product_from_zero": ("            Ap[d] = 1.0;\n", "            Ap[d] = 0.0;\n"),
+    "log_fwd_coefficient_sign": ("h[d] = exp(log_coeffs[crow + d]) * h[d] + exp(log_values[vrow + d]);",
+                                 "h[d] = exp(-log_coeffs[crow + d]) * h[d] + exp(log_values[vrow + d]);"),
+    "affine_bwd_coefficient_index": ("const double *Anext = A + (s + n) * kk;",
+                                     "const double *Anext = A + s * kk;"),
+    "affine_bwd_halo_index": ("const double *Aprev = (t > 0) ? Abar + (s - n) * kk : eye;",
+                              "const double *Aprev = (t > 0) ? Abar + s * kk : eye;"),
     "affine_fwd_order": ("mat_mul(At, P, tmp, k, k, k);", "mat_mul(P, At, tmp, k, k, k);"),
     "affine_fwd_dropped_B": ("H[e] = tmp[e] + Bm[s * kv + e];", "H[e] = tmp[e];"),
     "affine_bwd_untransposed": ("mat_tmul(Anext, M, tmp, k, k, k);", "mat_mul(Anext, M, tmp, k, k, k);"),
