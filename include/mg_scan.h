@@ -35,8 +35,11 @@
  *   stream).  Argument errors are reported synchronously, before any launch,
  *   by the return value.  The device-side chunk look-back waits are bounded;
  *   if one gives up (a predecessor chunk never published), the kernel still
- *   finishes, the outputs are unspecified, and the next mg_workspace_status
- *   on that workspace returns MG_ERR_TIMEOUT.
+ *   finishes, the outputs OF THAT LAUNCH are unspecified, and the next
+ *   mg_workspace_status on that workspace returns MG_ERR_TIMEOUT.  The error
+ *   record is tagged with the launch it belongs to: later launches on the
+ *   same workspace run normally (their waits do not give up early because of
+ *   it) whether or not the caller has read the record yet.
  * Errors.  Every entry point returns an mg_status.  On failure
  *   mg_last_error_detail() gives a human-readable reason (thread-local, valid
  *   until the next call on the same thread).  An out-of-envelope request
@@ -44,7 +47,9 @@
  *   silent downgrade to another implementation.
  * Degenerate sizes.  B, T, D, n equal to 0 return MG_OK without a launch
  *   (for mg_log_scan_fwd, T = 0 still needs log_values of shape (B,1,D), which
- *   is not read).  Negative sizes return MG_ERR_INVALID_ARG.
+ *   is not read).  Negative sizes return MG_ERR_INVALID_ARG.  The channel-wise
+ *   ops (linear, log) index channels with 32-bit integers: D above
+ *   2^31 - 2^16 returns MG_ERR_UNSUPPORTED.
  * Precision.  Arithmetic and outputs are float32.  bf16 inputs (MG_BF16)
  *   are widened to float32 on load.
  */
@@ -205,14 +210,24 @@ mg_status mg_affine_scan_bwd(const float *A, const float *Abar, const float *Bba
  * exactly as for mg_linear_scan_fwd.
  *
  * The first call on a device looks up that device's address of the array
- * (with the device current); make that first call before any stream capture.
- * Each call clears the part of the array it uses (an asynchronous memset on
- * `stream`) and then launches the same kernel as mg_linear_scan_fwd.  All
- * calls share the one array: calls whose work overlaps on the GPU (other
- * streams, other host threads) race and must be serialised by the caller.
- * Sizes whose workspace would exceed the array return MG_ERR_INVALID_ARG
- * before any launch (with float32 inputs the limit is reached near 2^28
- * elements); use mg_linear_scan_fwd with a caller workspace there.
+ * (with the device current) and keeps it for the life of the process; make
+ * that first call before any stream capture.  The address belongs to the
+ * device's primary context: after cudaDeviceReset, or from another context
+ * on the same device, the kept address is not valid and this entry point
+ * must not be used.
+ * Each call clears the array's two launch counters (an asynchronous memset
+ * of 8 bytes on `stream`; everything else the kernel needs is tagged with
+ * the launch, so the previous call's contents do no harm) and then launches
+ * the same kernel as mg_linear_scan_fwd, so both give bitwise the same
+ * outputs.  All calls share the one array: calls whose work overlaps on the
+ * GPU (other streams, other host threads) race and must be serialised by the
+ * caller.  Sizes whose forward workspace would exceed the array return
+ * MG_ERR_INVALID_ARG before any launch.  That workspace depends on the
+ * input dtype and on how B, T and D fall into tiles; every (B,T,D) with
+ * mg_linear_scan_workspace_size(B,T,D) <= mg_linear_scan_fwd_noalloc_max_scratch()
+ * is accepted.  Use mg_linear_scan_fwd with a caller workspace beyond it.  A
+ * device-side wait that gave up is reported by
+ * mg_linear_scan_fwd_noalloc_status.
  */
 mg_status mg_linear_scan_fwd_noalloc(const void *a, const void *b, mg_dtype in_dt,
                                      float *A, float *Bc,
@@ -220,6 +235,13 @@ mg_status mg_linear_scan_fwd_noalloc(const void *a, const void *b, mg_dtype in_d
 
 /* Bytes of the static scratch behind mg_linear_scan_fwd_noalloc. */
 size_t mg_linear_scan_fwd_noalloc_max_scratch(void);
+
+/* mg_workspace_status for the static scratch of mg_linear_scan_fwd_noalloc on
+ * the current device: synchronises `stream`, then returns MG_ERR_TIMEOUT if a
+ * look-back wait of any mg_linear_scan_fwd_noalloc call since the last query
+ * gave up (MG_ERR_INVALID_ARG if calls overlapped and took bad tickets), and
+ * clears the record; MG_OK otherwise.  Allocates nothing. */
+mg_status mg_linear_scan_fwd_noalloc_status(cudaStream_t stream);
 
 /*
  * Testing hook for the look-back's failure path (no counterpart on the page).

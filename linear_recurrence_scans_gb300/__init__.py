@@ -114,6 +114,8 @@ def load():
         lib.mg_linear_scan_fwd_noalloc.restype = st
         lib.mg_linear_scan_fwd_noalloc_max_scratch.argtypes = []
         lib.mg_linear_scan_fwd_noalloc_max_scratch.restype = sz
+        lib.mg_linear_scan_fwd_noalloc_status.argtypes = [vp]
+        lib.mg_linear_scan_fwd_noalloc_status.restype = st
         for name in ("mg_workspace_init", "mg_workspace_status", "mg_linear_scan_fwd",
                      "mg_linear_scan_bwd", "mg_log_scan_fwd", "mg_log_scan_bwd",
                      "mg_affine_scan_fwd", "mg_affine_scan_bwd"):
@@ -343,6 +345,15 @@ def mg_linear_scan_fwd_noalloc(a, b, *, out=None, stream=None):
                                              A.data_ptr(), Bc.data_ptr(), B, T, D, sh),
            "mg_linear_scan_fwd_noalloc")
     return A, Bc
+
+
+def noalloc_status(stream=None, device=None) -> None:
+    """Raise MgScanError if a device-side wait of a mg_linear_scan_fwd_noalloc
+    call on the current device gave up since the last check (synchronises
+    the stream)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    _check(load().mg_linear_scan_fwd_noalloc_status(_stream_handle(stream, dev)),
+           "mg_linear_scan_fwd_noalloc_status")
 
 
 # Names of the page "minGRU - Triton kernels".

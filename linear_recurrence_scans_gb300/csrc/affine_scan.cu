@@ -440,7 +440,7 @@ __global__ void __launch_bounds__(Cf::NW * 32)
     unsigned long long epoch;
     take_ticket(lb, tile, epoch);
     if (tile >= g.n_tiles) {
-        if (threadIdx.x == 0) atomicOr(&lb.ctl->error, kErrBadTicket);
+        if (threadIdx.x == 0) raise_error(lb, epoch, kErrBadTicket);
         finish_cta(lb, epoch);
         return;
     }
@@ -1203,7 +1203,7 @@ __global__ void __launch_bounds__(Cf::NW * 32)
     unsigned long long epoch;
     take_ticket(lb, tile, epoch);
     if (tile >= g.n_tiles) {
-        if (threadIdx.x == 0) atomicOr(&lb.ctl->error, kErrBadTicket);
+        if (threadIdx.x == 0) raise_error(lb, epoch, kErrBadTicket);
         finish_cta(lb, epoch);
         return;
     }
@@ -1258,7 +1258,7 @@ __global__ void __launch_bounds__(Cf::NW * 32)
         unsigned long long *bar = wbar + q % NSL;
         const unsigned parity = unsigned(q / NSL) & 1u;
         if (!mbar_wait_bounded(bar, parity, lb.wait_limit_ns)) {
-            if (lane == 0) atomicOr(&lb.ctl->error, kErrLookbackTimeout);
+            if (lane == 0) raise_error(lb, epoch, kErrLookbackTimeout);
             mbar_wait_bounded(bar, parity, lb.wait_limit_ns);
         }
         return wring + (q % NSL) * STEP;

@@ -16,17 +16,26 @@
 //
 // Workspace layout (caller-owned, zero-filled once before first use):
 //   [0, 256)            Control
-//   [256, 256 + 8*N)    one 64-bit record flag per tile:  epoch << 2 | status
+//   [256, 256 + 8*N)    one 64-bit record flag per tile:
+//                       kFlagTag | epoch << 2 | status
 //   then                per-tile data, op-specific (aggregate and prefix)
 // A flag counts only if its epoch equals the launch's epoch, so stale flags
 // of earlier launches need no clearing.  The last CTA of every launch resets
-// the ticket and done counters and advances the epoch.
+// the ticket and done counters and advances the epoch.  Where the flags of a
+// launch with more tiles overlay the data records of an earlier launch with
+// fewer, the old words are float pairs; the tag sets the top 13 bits, which
+// as the upper float of a pair is a negative quiet NaN with a non-zero
+// payload bit pattern that no arithmetic result has (the GPU's NaN is
+// 0x7fffffff), so no stale record reads as a flag of the running launch.
 //
 // Bounded waits.  A wait gives up after `max_polls` polls or `wait_limit_ns`
-// nanoseconds of %globaltimer, or as soon as any CTA of the launch has given
-// up.  Giving up sets the sticky Control::error word (read by
-// mg_workspace_status) and the CTA carries on with an identity carry, so the
-// launch always finishes and the GPU stays usable.
+// nanoseconds of %globaltimer, or as soon as another CTA of the SAME launch
+// has given up.  Giving up sets the sticky Control::error word (read and
+// cleared by mg_workspace_status), tags it with the launch's epoch
+// (Control::error_epoch), and the CTA carries on with an identity carry, so
+// the launch always finishes and the GPU stays usable.  A later launch on the
+// same workspace does not give up early because of an earlier launch's
+// error: it compares the tag with its own epoch.
 #pragma once
 
 #include <cstdint>
@@ -42,7 +51,8 @@ struct Control {
     unsigned long long epoch;  // launch counter; tags the record flags
     unsigned int error;        // sticky error bits (kErr*)
     unsigned int error_tile;   // 1 + a tile that gave up a wait (0 = none)
-    unsigned int pad[58];
+    unsigned long long error_epoch;  // 1 + epoch of the last launch that set an error
+    unsigned int pad[56];
 };
 static_assert(sizeof(Control) == 256, "control block is 256 bytes");
 
@@ -90,10 +100,35 @@ __device__ __forceinline__ unsigned long long global_timer_ns()
     return t;
 }
 
+constexpr unsigned long long kFlagTag = 0xfff8000000000000ull;
+constexpr unsigned long long kEpochMask = (1ull << 49) - 1;
+
+// The flag word of `status` in the launch of `epoch`.
+__device__ __forceinline__ unsigned long long flag_word(unsigned long long epoch, unsigned status)
+{
+    return kFlagTag | ((epoch & kEpochMask) << 2) | status;
+}
+
 // Status of a flag word for this launch (kStatusNone if stale or unset).
 __device__ __forceinline__ unsigned flag_status(unsigned long long v, unsigned long long epoch)
 {
-    return ((v >> 2) == epoch) ? unsigned(v & 3ull) : kStatusNone;
+    return ((v & ~3ull) == flag_word(epoch, 0)) ? unsigned(v & 3ull) : kStatusNone;
+}
+
+// Record an error of the launch of `epoch` (any thread): the sticky bits,
+// the first tile that gave up (if `tile` names one) and the launch tag.
+__device__ __forceinline__ void raise_error(const Lookback &lb, unsigned long long epoch,
+                                            unsigned bits, unsigned tile_plus1 = 0u)
+{
+    atomicOr(&lb.ctl->error, bits);
+    if (tile_plus1 != 0u) atomicCAS(&lb.ctl->error_tile, 0u, tile_plus1);
+    atomicMax(&lb.ctl->error_epoch, epoch + 1ull);
+}
+
+// Whether another CTA of the launch of `epoch` has already given up a wait.
+__device__ __forceinline__ bool launch_failed(const Lookback &lb, unsigned long long epoch)
+{
+    return ld_relaxed_u64(&lb.ctl->error_epoch) == epoch + 1ull;
 }
 
 // Take a ticket and read the launch epoch (thread 0 of the CTA); all threads
@@ -142,9 +177,8 @@ static __device__ __noinline__ unsigned wait_status(const Lookback &lb, size_t s
                 st = flag_status(ld_acquire_u64(lb.flags + slot), epoch);
                 if (st != kStatusNone) break;
                 if (it >= lb.max_polls || global_timer_ns() - t0 > lb.wait_limit_ns ||
-                    ld_relaxed_u32(&lb.ctl->error) != 0) {
-                    atomicOr(&lb.ctl->error, kErrLookbackTimeout);
-                    atomicCAS(&lb.ctl->error_tile, 0u, my_tile + 1u);
+                    launch_failed(lb, epoch)) {
+                    raise_error(lb, epoch, kErrLookbackTimeout, my_tile + 1u);
                     break;
                 }
             }
@@ -186,9 +220,8 @@ static __device__ __noinline__ int wait_window(const Lookback &lb, size_t j, siz
         }
         int stop = 0;
         if (lane == 0 && (it >= lb.max_polls || global_timer_ns() - t0 > lb.wait_limit_ns ||
-                          ld_relaxed_u32(&lb.ctl->error) != 0)) {
-            atomicOr(&lb.ctl->error, kErrLookbackTimeout);
-            atomicCAS(&lb.ctl->error_tile, 0u, my_tile + 1u);
+                          launch_failed(lb, epoch))) {
+            raise_error(lb, epoch, kErrLookbackTimeout, my_tile + 1u);
             stop = 1;
         }
         if (__shfl_sync(0xffffffffu, stop, 0)) return -1;
@@ -205,7 +238,7 @@ __device__ __forceinline__ void publish(const Lookback &lb, size_t slot, unsigne
 {
     __syncwarp();
     if ((threadIdx.x & 31) == 0 && (long long)my_tile != lb.stall_tile)
-        st_release_u64(lb.flags + slot, (epoch << 2) | status);
+        st_release_u64(lb.flags + slot, flag_word(epoch, status));
 }
 
 // End of a CTA: count it; the launch's last CTA resets the ticket and done

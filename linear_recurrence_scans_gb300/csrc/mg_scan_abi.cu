@@ -1,6 +1,7 @@
 // The C entry points of mg_scan.h: argument validation (all of it before any
 // launch), workspace bookkeeping and dispatch to the launchers.
 #include <cstdarg>
+#include <cstddef>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -67,6 +68,18 @@ mg_status check_dims(const char *fn, std::initializer_list<int64_t> dims)
     return MG_OK;
 }
 
+// The channel-wise kernels index channels with 32-bit integers (a tile's
+// first channel plus the lane's offset): D must stay clear of 2^31.
+constexpr int64_t kMaxChannels = (int64_t(1) << 31) - (int64_t(1) << 16);
+
+mg_status check_channels(const char *fn, int64_t D)
+{
+    if (D > kMaxChannels)
+        return fail(MG_ERR_UNSUPPORTED, "%s: D = %lld channels exceeds %lld", fn, (long long)D,
+                    (long long)kMaxChannels);
+    return MG_OK;
+}
+
 mg_status check_ws(const char *fn, const void *ws, size_t ws_bytes, size_t need)
 {
     if (ws == nullptr) return fail(MG_ERR_INVALID_ARG, "%s: workspace is NULL", fn);
@@ -127,6 +140,34 @@ mg_status noalloc_scratch(const char *fn, void **out)
     }
     *out = g_noalloc_ptr[dev];
     return MG_OK;
+}
+
+// Read and clear the error record of the workspace `ws` (synchronises
+// `stream`).  The record is Control::error, error_tile and error_epoch (16
+// contiguous bytes).
+mg_status read_status(const char *fn, void *ws, cudaStream_t stream)
+{
+    static_assert(offsetof(Control, error_tile) == offsetof(Control, error) + 4 &&
+                      offsetof(Control, error_epoch) == offsetof(Control, error) + 8,
+                  "the error record is contiguous");
+    unsigned int words[2] = {0, 0};  // Control::error, Control::error_tile
+    Control *ctl = static_cast<Control *>(ws);
+    cudaError_t e = cudaMemcpyAsync(words, &ctl->error, sizeof(words), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess)
+        return fail(MG_ERR_LAUNCH, "%s: %s", fn, cudaGetErrorString(e));
+    if (words[0] == 0) return MG_OK;
+    e = cudaMemsetAsync(&ctl->error, 0, 16, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess)
+        return fail(MG_ERR_LAUNCH, "%s: %s", fn, cudaGetErrorString(e));
+    if (words[0] & kErrBadTicket)
+        return fail(MG_ERR_INVALID_ARG,
+                    "the workspace was not zero-filled before its first use (or is shared by "
+                    "overlapping calls); the outputs of that launch are unspecified");
+    return fail(MG_ERR_TIMEOUT,
+                "a chunk look-back wait gave up (first tile %u); the outputs of that launch are "
+                "unspecified", words[1] ? words[1] - 1 : 0u);
 }
 
 #define MG_TRY(expr)                      \
@@ -193,25 +234,9 @@ mg_status mg_workspace_status(void *ws, cudaStream_t stream)
 {
     g_detail[0] = 0;
     if (ws == nullptr) return fail(MG_ERR_INVALID_ARG, "mg_workspace_status: workspace is NULL");
-    unsigned int words[2] = {0, 0};  // Control::error, Control::error_tile
-    Control *ctl = static_cast<Control *>(ws);
-    cudaError_t e = cudaMemcpyAsync(words, &ctl->error, sizeof(words), cudaMemcpyDeviceToHost, stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess)
-        return fail(MG_ERR_LAUNCH, "mg_workspace_status: %s", cudaGetErrorString(e));
-    if (words[0] == 0) return MG_OK;
-    e = cudaMemsetAsync(&ctl->error, 0, sizeof(words), stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess)
-        return fail(MG_ERR_LAUNCH, "mg_workspace_status: %s", cudaGetErrorString(e));
-    if (words[0] & kErrBadTicket)
-        return fail(MG_ERR_INVALID_ARG,
-                    "the workspace was not zero-filled before its first use (or is shared by "
-                    "overlapping calls); the outputs of that launch are unspecified");
-    return fail(MG_ERR_TIMEOUT,
-                "a chunk look-back wait gave up (first tile %u); the outputs of that launch are "
-                "unspecified", words[1] ? words[1] - 1 : 0u);
+    return read_status("mg_workspace_status", ws, stream);
 }
+
 
 mg_status mg_linear_scan_fwd(const void *a, const void *b, mg_dtype in_dt, float *A, float *Bc,
                              int64_t B, int64_t T, int64_t D, void *ws, size_t ws_bytes,
@@ -222,6 +247,7 @@ mg_status mg_linear_scan_fwd(const void *a, const void *b, mg_dtype in_dt, float
     if (in_dt != MG_F32 && in_dt != MG_BF16)
         return fail(MG_ERR_UNSUPPORTED, "%s: input dtype %d not supported", fn, int(in_dt));
     MG_TRY(check_dims(fn, {B, T, D}));
+    MG_TRY(check_channels(fn, D));
     if (B == 0 || T == 0 || D == 0) return MG_OK;
     const size_t n = size_t(B) * T * D, isz = in_dt == MG_F32 ? 4 : 2;
     MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D, default_opts())));
@@ -242,6 +268,7 @@ mg_status mg_linear_scan_bwd(const void *a, mg_dtype a_dt, const float *A, const
     if (a_dt != MG_F32 && a_dt != MG_BF16)
         return fail(MG_ERR_UNSUPPORTED, "%s: input dtype %d not supported", fn, int(a_dt));
     MG_TRY(check_dims(fn, {B, T, D}));
+    MG_TRY(check_channels(fn, D));
     if (B == 0 || T == 0 || D == 0) return MG_OK;
     const size_t n = size_t(B) * T * D, isz = a_dt == MG_F32 ? 4 : 2;
     MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D, default_opts())));
@@ -263,6 +290,7 @@ mg_status mg_log_scan_fwd(const float *log_coeffs, const float *log_values, floa
     const char *fn = "mg_log_scan_fwd";
     g_detail[0] = 0;
     MG_TRY(check_dims(fn, {B, T + 1, D}));
+    MG_TRY(check_channels(fn, D));
     if (T < 0) return fail(MG_ERR_INVALID_ARG, "%s: negative size", fn);
     if (B == 0 || T == 0 || D == 0) return MG_OK;
     const size_t n = size_t(B) * T * D, nv = size_t(B) * (T + 1) * D;
@@ -281,6 +309,7 @@ mg_status mg_log_scan_bwd(const float *log_coeffs, const float *log_values, cons
     const char *fn = "mg_log_scan_bwd";
     g_detail[0] = 0;
     MG_TRY(check_dims(fn, {B, T + 1, D}));
+    MG_TRY(check_channels(fn, D));
     if (T < 0) return fail(MG_ERR_INVALID_ARG, "%s: negative size", fn);
     if (B == 0 || D == 0) return MG_OK;
     const size_t n = size_t(B) * T * D, nv = size_t(B) * (T + 1) * D;
@@ -354,6 +383,7 @@ mg_status mg_testing_linear_scan_fwd_stall(const float *a, const float *b, float
     const char *fn = "mg_testing_linear_scan_fwd_stall";
     g_detail[0] = 0;
     MG_TRY(check_dims(fn, {B, T, D}));
+    MG_TRY(check_channels(fn, D));
     if (B == 0 || T == 0 || D == 0) return MG_OK;
     const size_t n = size_t(B) * T * D;
     MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D, default_opts())));
@@ -381,6 +411,7 @@ mg_status mg_linear_scan_fwd_noalloc(const void *a, const void *b, mg_dtype in_d
     if (in_dt != MG_F32 && in_dt != MG_BF16)
         return fail(MG_ERR_UNSUPPORTED, "%s: input dtype %d not supported", fn, int(in_dt));
     MG_TRY(check_dims(fn, {B, T, D}));
+    MG_TRY(check_channels(fn, D));
     if (B == 0 || T == 0 || D == 0) return MG_OK;
     const LaunchOpts o = default_opts();
     const size_t need = linear_fwd_ws_bytes(in_dt, B, T, D, o);
@@ -396,12 +427,28 @@ mg_status mg_linear_scan_fwd_noalloc(const void *a, const void *b, mg_dtype in_d
                            {b, n * isz, "b", false},
                            {A, n * 4, "A", true},
                            {Bc, n * 4, "Bc", true}}));
-    // The array keeps the previous call's control words and records: clear
-    // the part this call uses so it starts from a zero-filled workspace.
-    const cudaError_t e = cudaMemsetAsync(scratch, 0, need, stream);
+    // The array keeps the previous call's contents.  Only the ticket and done
+    // counters must start at zero (every completed launch leaves them so;
+    // clearing them here also covers a launch that never started).  The
+    // launch epoch is kept: it makes the previous calls' flags stale, and it
+    // keeps the error record of earlier calls (read by
+    // mg_linear_scan_fwd_noalloc_status) from being taken for this call's.
+    static_assert(offsetof(Control, ticket) == 0 && offsetof(Control, done) == 4,
+                  "the counters open the control block");
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, 2 * sizeof(unsigned int), stream);
     if (e != cudaSuccess)
-        return fail(MG_ERR_LAUNCH, "%s: clearing the scratch: %s", fn, cudaGetErrorString(e));
+        return fail(MG_ERR_LAUNCH, "%s: clearing the scratch counters: %s", fn,
+                    cudaGetErrorString(e));
     return launch_linear_fwd(a, b, in_dt, A, Bc, B, T, D, scratch, kNoAllocScratchBytes, stream, o);
+}
+
+mg_status mg_linear_scan_fwd_noalloc_status(cudaStream_t stream)
+{
+    const char *fn = "mg_linear_scan_fwd_noalloc_status";
+    g_detail[0] = 0;
+    void *scratch = nullptr;
+    MG_TRY(noalloc_scratch(fn, &scratch));
+    return read_status(fn, scratch, stream);
 }
 
 }  // extern "C"

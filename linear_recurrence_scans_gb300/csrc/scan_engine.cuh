@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(TX *TY, MINB)
     unsigned long long epoch;
     take_ticket(lb, tile, epoch);
     if (tile >= g.n_tiles) {  // a workspace that was not zero-filled before first use
-        if (threadIdx.x == 0) atomicOr(&lb.ctl->error, kErrBadTicket);
+        if (threadIdx.x == 0) raise_error(lb, epoch, kErrBadTicket);
         finish_cta(lb, epoch);
         return;
     }

@@ -60,16 +60,16 @@ __device__ __forceinline__ void mbar_arrive(unsigned long long *bar)
 
 // Bounded wait that also gives up as soon as the launch has an error.
 __device__ __forceinline__ bool mbar_wait_or_error(unsigned long long *bar, unsigned parity,
-                                                   const Lookback &lb)
+                                                   const Lookback &lb, unsigned long long epoch)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     for (unsigned it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 31u) == 0u) {
-            if (ld_relaxed_u32(&lb.ctl->error) != 0) return false;
+            if (launch_failed(lb, epoch)) return false;
             if (global_timer_ns() - t0 > lb.wait_limit_ns || it >= lb.max_polls) {
-                atomicOr(&lb.ctl->error, kErrLookbackTimeout);
+                raise_error(lb, epoch, kErrLookbackTimeout);
                 return false;
             }
         }
@@ -110,8 +110,8 @@ __device__ __forceinline__ const E *srow(const char *st, int a, int i, int lane)
 // of the CTA's work (`*end` set by the producer).  1 = phase done, 0 = past
 // the end, -1 = gave up (error recorded).
 __device__ __forceinline__ int mbar_wait_or_end(unsigned long long *bar, unsigned parity,
-                                                const Lookback &lb, const volatile int *end,
-                                                int it)
+                                                const Lookback &lb, unsigned long long epoch,
+                                                const volatile int *end, int it)
 {
     if (mbar_try_wait(bar, parity)) return 1;
     const unsigned long long t0 = global_timer_ns();
@@ -119,9 +119,9 @@ __device__ __forceinline__ int mbar_wait_or_end(unsigned long long *bar, unsigne
         if (mbar_try_wait(bar, parity)) return 1;
         if (it >= *end) return 0;
         if ((k & 31u) == 0u) {
-            if (ld_relaxed_u32(&lb.ctl->error) != 0) return -1;
+            if (launch_failed(lb, epoch)) return -1;
             if (global_timer_ns() - t0 > lb.wait_limit_ns || k >= lb.max_polls) {
-                atomicOr(&lb.ctl->error, kErrLookbackTimeout);
+                raise_error(lb, epoch, kErrLookbackTimeout);
                 return -1;
             }
         }
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1 + kNPub) * 32, 1)
         for (;; ++it) {
             const int s = it % SG;
             const unsigned u = unsigned(it / SG);
-            if (u > 0 && !mbar_wait_or_error(empty + s, (u - 1) & 1u, lb)) break;
+            if (u > 0 && !mbar_wait_or_error(empty + s, (u - 1) & 1u, lb, epoch)) break;
             if (left == 0) {
                 batch = __shfl_sync(0xffffffffu, next_batch, 0);
                 left = kTicketBatch;
@@ -206,7 +206,8 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1 + kNPub) * 32, 1)
             if (tile >= g.n_tiles) {
                 if (lane == 0) {
                     if (batch >= g.n_tiles + 2u * kTicketBatch * gridDim.x)
-                        atomicOr(&lb.ctl->error, kErrBadTicket);                    s_tile[s] = kSentinelTile;
+                        raise_error(lb, epoch, kErrBadTicket);
+                    s_tile[s] = kSentinelTile;
                     *end = it;
                     mbar_arrive(full + s);
                 }
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1 + kNPub) * 32, 1)
         // ----------------------------------------------------------- publisher
         for (int it = warp - 1;; it += kNPub) {
             const int s = it % SG;
-            if (mbar_wait_or_end(aggr + s, unsigned(it / SG) & 1u, lb, end, it) != 1) break;
+            if (mbar_wait_or_end(aggr + s, unsigned(it / SG) & 1u, lb, epoch, end, it) != 1) break;
             const unsigned tile = s_tile[s];
             if (tile >= g.n_tiles) break;
             int c, j, d0;
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1 + kNPub) * 32, 1)
         // ----------------------------------------------------------- look-back
         for (int it = warp - 1 - kNPub;; it += NLB) {
             const int s = it % SG;
-            if (mbar_wait_or_end(pub + s, unsigned(it / SG) & 1u, lb, end, it) != 1) break;
+            if (mbar_wait_or_end(pub + s, unsigned(it / SG) & 1u, lb, epoch, end, it) != 1) break;
             const unsigned tile = s_tile[s];
             if (tile >= g.n_tiles) break;
             int c, j, d0;
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1 + kNPub) * 32, 1)
         // pass 2 of iteration k: wait for its carry, re-run, free the stage
         auto finish = [&](int k) -> bool {
             const int s = k % SG;
-            if (!mbar_wait_or_error(carry + s, unsigned(k / SG) & 1u, lb)) return false;
+            if (!mbar_wait_or_error(carry + s, unsigned(k / SG) & 1u, lb, epoch)) return false;
             pass2(s, s, s_tile[s]);
             __syncwarp();
             if (lane == 0) mbar_arrive(empty + s);
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__((Op::NCW + Op::NLB + 1 + kNPub) * 32, 1)
         bool ok = true;
         for (;; ++it) {
             const int s = it % SG;
-            if (!mbar_wait_or_error(full + s, unsigned(it / SG) & 1u, lb)) {
+            if (!mbar_wait_or_error(full + s, unsigned(it / SG) & 1u, lb, epoch)) {
                 ok = false;
                 break;
             }

@@ -99,3 +99,38 @@ def test_binding_rejects_cpu_tensors():
     import torch
     with pytest.raises(ValueError):
         mg.linear_scan_fwd(torch.zeros(1, 2, 4), torch.zeros(1, 2, 4))
+
+
+def test_rejects_channel_counts_beyond_32_bit_indexing(lib):
+    """The channel-wise kernels index channels with 32-bit integers: a D at or
+    above 2^31 is refused before launch (it would wrap), a D just below the
+    limit is not refused for its size."""
+    D = 1 << 31
+    assert _fwd(lib, B=1, T=1, D=D) == mg.MG_ERR_UNSUPPORTED
+    assert b"channels" in lib.mg_last_error_detail()
+    assert lib.mg_linear_scan_bwd(None, 0, None, None, None, None, None, None, 1, 1, D,
+                                  None, 0, None) == mg.MG_ERR_UNSUPPORTED
+    assert lib.mg_log_scan_fwd(None, None, None, 1, 1, D, None, 0, None) == mg.MG_ERR_UNSUPPORTED
+    assert lib.mg_log_scan_bwd(None, None, None, None, None, None, 1, 1, D, None, 0,
+                               None) == mg.MG_ERR_UNSUPPORTED
+    # below the limit: the next check (the NULL workspace) is what fails
+    assert _fwd(lib, B=1, T=1, D=(1 << 31) - (1 << 16)) == mg.MG_ERR_INVALID_ARG
+
+
+def test_noalloc_size_limit_matches_the_workspace_size(lib):
+    """Every shape whose workspace fits the static scratch is accepted by the
+    size check of mg_linear_scan_fwd_noalloc (without a GPU the call then
+    stops at the device query, MG_ERR_LAUNCH, never at the size check), and
+    a shape far beyond it is refused for its size."""
+    cap = int(lib.mg_linear_scan_fwd_noalloc_max_scratch())
+    base = 1 << 40
+    for shape in ((1, 1 << 13, 1 << 16), (8, 4096, 1024), (2, 1 << 15, 4096), (3, 517, 300)):
+        need = mg.linear_workspace_size(*shape)
+        st = lib.mg_linear_scan_fwd_noalloc(base, base + (1 << 36), mg.MG_F32, base + (2 << 36),
+                                            base + (3 << 36), *shape, None)
+        if need <= cap:
+            assert b"static scratch" not in lib.mg_last_error_detail(), shape
+            assert st != mg.MG_ERR_INVALID_ARG or b"scratch" not in lib.mg_last_error_detail()
+    st = lib.mg_linear_scan_fwd_noalloc(base, base + (1 << 36), mg.MG_F32, base + (2 << 36),
+                                        base + (3 << 36), 64, 65536, 4096, None)
+    assert st == mg.MG_ERR_INVALID_ARG and b"static scratch" in lib.mg_last_error_detail()

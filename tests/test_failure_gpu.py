@@ -55,3 +55,51 @@ def test_non_zeroed_workspace_is_reported(cuda_lib):
     mg.workspace_status(ws)
     errs = linear_fwd_errors(a.cpu(), b.cpu(), A, Bc)
     assert max(errs.values()) <= TOL_F32, errs
+
+
+def test_timeout_does_not_poison_later_launches(cuda_lib):
+    """A launch that gave up a wait leaves its error record in the workspace.
+    Later launches on that workspace, run WITHOUT reading the record first,
+    must still wait normally and give correct results; the next status read
+    reports the one timeout, once."""
+    mg = cuda_lib
+    lib = mg.load()
+    B, T, D = 1, 4096, 128
+    a, b, _, _ = wl.mingru_linear(B, T, D, seed=23, grads=False)
+    ad, bd = a.to(DEV), b.to(DEV)
+    A, Bc = torch.empty_like(ad), torch.empty_like(ad)
+    ws = mg.new_workspace(mg.linear_workspace_size(B, T, D), DEV)
+    s = torch.cuda.current_stream().cuda_stream
+    st = lib.mg_testing_linear_scan_fwd_stall(ad.data_ptr(), bd.data_ptr(), A.data_ptr(),
+                                              Bc.data_ptr(), B, T, D, ws.data_ptr(), ws.numel(),
+                                              3, 20_000_000, s)   # tile 3 stalls; 20 ms waits
+    assert st == mg.MG_OK
+    for _ in range(2):   # no status read in between
+        A2, Bc2 = mg.linear_scan_fwd(ad, bd, ws=ws)
+        errs = linear_fwd_errors(a, b, A2, Bc2)
+        assert max(errs.values()) <= TOL_F32, errs
+    with pytest.raises(mg.MgScanError) as ei:
+        mg.workspace_status(ws)
+    assert ei.value.status == mg.MG_ERR_TIMEOUT
+    mg.workspace_status(ws)          # reported once, then cleared
+
+
+def test_small_then_large_tile_count_on_one_workspace(cuda_lib):
+    """The flags of a launch with many tiles lie where an earlier launch with
+    few tiles (or another op) kept its data records; the flag tag keeps those
+    stale records from reading as flags."""
+    from parity import affine_fwd_errors
+    mg = cuda_lib
+    big = (2, 4000, 512)
+    ws = mg.new_workspace(max(mg.linear_workspace_size(*big),
+                              mg.affine_workspace_size(2, 300, 4, 4, 4)), DEV)
+    Am, Bm, _, _ = wl.haar_affine(2, 300, 4, 4, 4, seed=24)
+    Abar, Bbar = mg.affine_scan_fwd(Am.to(DEV), Bm.to(DEV), ws=ws)
+    errs = affine_fwd_errors(Am, Bm, Abar, Bbar)
+    assert max(errs.values()) <= TOL_F32, errs
+    for shape in ((1, 64, 8), big):
+        a, b, _, _ = wl.mingru_linear(*shape, seed=25)
+        A, Bc = mg.linear_scan_fwd(a.to(DEV), b.to(DEV), ws=ws)
+        errs = linear_fwd_errors(a, b, A, Bc)
+        assert max(errs.values()) <= TOL_F32, (shape, errs)
+    mg.workspace_status(ws)
