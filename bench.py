@@ -1,10 +1,12 @@
 """Benchmark of the minGRU scan library on one or more GB300s.
 
-One step = one pass of the scan hot path over one synthetic minGRU batch
-(B=8, T=4096, D=1024, float32): mg_linear_scan_fwd then mg_linear_scan_bwd
-(the backward consumes the forward's outputs, as in training).  The metric is
-scan elements per second (B*T*D per step), whole job.  The other workloads
-(log-space scan, k x k affine scans, the large bf16 run) are measured once per
+One step = one pass of the scan hot path over one synthetic minGRU batch,
+the largest workload: B=16, T=32768, D=4096 (2^31 elements), a and b in
+bf16, float32 accumulation and float32 outputs: mg_linear_scan_fwd then
+mg_linear_scan_bwd (the backward consumes the forward's outputs, as in
+training).  The metric is scan elements per second (B*T*D per step), whole
+job.  The other workloads (the float32 minGRU batch 8x4096x1024, the
+log-space scan and its adjoint, the k x k affine scans) are measured once per
 run and reported under "per_workload".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -13,7 +15,7 @@ Under torchrun (N > 1) every rank runs the same step on its own GPU with its
 own batch (weak scaling, no data-path collective); the timed region is
 bracketed by a barrier and the max elapsed time over ranks is used.
 ``--impl reference`` times the float64 CPU oracle instead, on a bounded
-sample of the same workload, on the host cores.
+sample of the same workload (whole-T channel columns), on the host cores.
 """
 from __future__ import annotations
 
@@ -21,9 +23,11 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 import numpy as np
@@ -32,12 +36,12 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = "mingru_linear_8x4096x1024"
-B, T, D = 8, 4096, 1024
+WORKLOAD = "mingru_linear_bf16_16x32768x4096"
+B, T, D = 16, 32768, 4096
 METRIC = "scan elements/s (B*T*D per fwd+bwd step)"
 UNIT = "elements/s"
-FWD_BYTES_PER_ELT = 16   # read a, b; write A, Bc (fp32)
-BWD_BYTES_PER_ELT = 28   # read a, A, Bc, gA, gBc; write da, db (fp32)
+FWD_BYTES_PER_ELT = 12   # read a, b (bf16); write A, Bc (fp32)
+BWD_BYTES_PER_ELT = 26   # read a (bf16), A, Bc, gA, gBc; write da, db (fp32)
 
 
 # ------------------------------------------------------------- helpers
@@ -92,7 +96,9 @@ def source_hash() -> str:
 
 def profiled_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` on the bench workload from the
-    committed ncu summary, or None when the kernels changed since."""
+    committed ncu summary (scaled from the captured case to a full launch by
+    the elements processed, as the record states), or None when the kernels
+    changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -105,21 +111,24 @@ def profiled_traffic(kernel: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples during the timed region."""
+    """nvidia-smi clock/throttle samples every `period_ms` while active."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 20):
         self.gpu = gpu_index
+        self.period = period_ms
         self.proc = None
+        self.out = ""
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)   # let the first samples arrive before the timed work
         except (OSError, ValueError):
             self.proc = None
         return self
@@ -134,23 +143,50 @@ class ClockSampler:
                 self.proc.kill()
                 self.out, _ = self.proc.communicate()
 
-    def summary(self):
+    def summary(self, window: str):
         rows = []
         for line in (self.out or "").strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
             except ValueError:
                 continue
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows),
+        reasons = sorted({names[i] for *_, r in rows for i, v in enumerate(r) if v == "Active"})
+        # samples under load: the power draw separates them from the idle edges
+        pmax = max(r[2] for r in rows)
+        load = [r for r in rows if r[2] >= 0.5 * pmax] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in load),
                 "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
-                "samples": len(rows)}
+                "samples": len(rows), "samples_under_load": len(load),
+                "power_w_max": pmax, "period_ms": self.period, "window": window}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def events_ms(pairs):
+    return [s.elapsed_time(e) for s, e in pairs]
 
 
 # ------------------------------------------------------------- our arm
@@ -164,20 +200,15 @@ def run_ours(args, ws_size, rank, local):
     mg.load()
     stream = torch.cuda.current_stream(dev)
 
-    # Two resident input sets, used alternately, so no step reads what the
-    # previous one left in L2 (each input tensor alone is larger than L2).
-    sets = []
-    for s in range(2):
-        a, b, gA, gBc = wl.mingru_linear(B, T, D, seed=1000 * rank + 10 * s, device=dev)
-        sets.append((a, b, gA, gBc))
-    A = torch.empty_like(sets[0][0])
-    Bc = torch.empty_like(A)
-    da = torch.empty_like(A)
-    db = torch.empty_like(A)
+    # One resident batch: every input tensor (4.3 GB bf16, 8.6 GB fp32) is
+    # far larger than L2, so no step finds the previous one's data there.
+    a, b, gA, gBc = wl.mingru_linear(B, T, D, seed=1000 * rank, device=dev,
+                                     in_dtype=torch.bfloat16)
+    A = torch.empty(a.shape, dtype=torch.float32, device=dev)
+    Bc, da, db = torch.empty_like(A), torch.empty_like(A), torch.empty_like(A)
     ws = mg.new_workspace(mg.linear_workspace_size(B, T, D), dev)
 
-    def step(i, evs=None):
-        a, b, gA, gBc = sets[i & 1]
+    def step(evs=None):
         if evs is not None:
             evs[0].record(stream)
         mg.mg_linear_scan_fwd(a, b, out=(A, Bc), ws=ws)
@@ -187,8 +218,8 @@ def run_ours(args, ws_size, rank, local):
         if evs is not None:
             evs[2].record(stream)
 
-    for i in range(args.warmup):
-        step(i)
+    for _ in range(args.warmup):
+        step()
     torch.cuda.synchronize(dev)
     mg.workspace_status(ws)
 
@@ -200,14 +231,14 @@ def run_ours(args, ws_size, rank, local):
     with ClockSampler(local) as clk:
         t0.record(stream)
         for i in range(args.steps):
-            step(i, evs[i])
+            step(evs[i])
         t1.record(stream)
         torch.cuda.synchronize(dev)
     barrier(ws_size)
     elapsed = t0.elapsed_time(t1) * 1e-3
     mg.workspace_status(ws)
-    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    fwd_ms = events_ms((e[0], e[1]) for e in evs)
+    bwd_ms = events_ms((e[1], e[2]) for e in evs)
 
     n = B * T * D
     max_elapsed, total_units = aggregate(elapsed, float(n * args.steps), ws_size)
@@ -217,23 +248,34 @@ def run_ours(args, ws_size, rank, local):
     fwd_avg = statistics.mean(fwd_ms) * 1e-3
     bwd_avg = statistics.mean(bwd_ms) * 1e-3
     dom = "bwd" if bwd_avg >= fwd_avg else "fwd"
-    kname = "linear_scan_bwd" if dom == "bwd" else "linear_scan_fwd"
+    kname = "linear_scan_bwd_bf16" if dom == "bwd" else "linear_scan_fwd_bf16"
     algo = (BWD_BYTES_PER_ELT if dom == "bwd" else FWD_BYTES_PER_ELT) * n
     dur = bwd_avg if dom == "bwd" else fwd_avg
     achieved = algo / dur / 1e9
+
+    def leg(bpe, avg, ms):
+        return {"avg_ms": round(avg * 1e3, 4), "median_ms": round(statistics.median(ms), 4),
+                "GB_s": round(bpe * n / avg / 1e9, 1),
+                "frac": round(bpe * n / avg / 1e9 / peak, 4),
+                "algorithmic_bytes_per_launch": bpe * n,
+                "traffic": profiled_traffic("linear_scan_fwd_bf16" if bpe == FWD_BYTES_PER_ELT
+                                            else "linear_scan_bwd_bf16")}
+
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
+                "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json), burst copy",
                 "traffic": profiled_traffic(kname),
                 "algorithmic_bytes_per_launch": algo,
-                "fwd": {"avg_ms": round(fwd_avg * 1e3, 4),
-                        "GB_s": round(FWD_BYTES_PER_ELT * n / fwd_avg / 1e9, 1),
-                        "frac": round(FWD_BYTES_PER_ELT * n / fwd_avg / 1e9 / peak, 4)},
-                "bwd": {"avg_ms": round(bwd_avg * 1e3, 4),
-                        "GB_s": round(BWD_BYTES_PER_ELT * n / bwd_avg / 1e9, 1),
-                        "frac": round(BWD_BYTES_PER_ELT * n / bwd_avg / 1e9 / peak, 4)}}
+                "fwd": leg(FWD_BYTES_PER_ELT, fwd_avg, fwd_ms),
+                "bwd": leg(BWD_BYTES_PER_ELT, bwd_avg, bwd_ms)}
+    clocks = clk.summary(f"timed region: {args.steps} steps, {max_elapsed * 1e3:.1f} ms")
+    del A, Bc, da, db, ws
+    inputs = (a, b, gA, gBc)
+    del a, b, gA, gBc
 
-    e2e = run_e2e(mg, sets[0], dev, stream, args, ws, ws_size)
+    e2e = run_e2e(mg, inputs, dev, args, ws_size)
+    del inputs
+    torch.cuda.empty_cache()
     extra = run_extra(mg, dev, peak) if (rank == 0 and not args.no_extra) else None
     cpu = cpu_baseline() if (rank == 0 and ws_size == 1 and not args.no_cpu) else None
 
@@ -241,72 +283,118 @@ def run_ours(args, ws_size, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_size,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": max_elapsed / args.steps * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, f32 accumulation and out",
+        "data": "synthetic",
         "config": {"workload": WORKLOAD, "B": B, "T": T, "D": D,
                    "ops": ["mg_linear_scan_fwd", "mg_linear_scan_bwd"],
-                   "inputs": "minGRU gate: a = 1 - sigmoid(x1), b = sigmoid(x1) g(x2), "
-                             "gA, gBc ~ N(0,1); seeded",
-                   "l2": "inputs larger than L2 (each 134 MB tensor > 129 MB L2), two "
-                         "resident input sets alternated between steps; no flush",
+                   "inputs": "minGRU gate: a = 1 - sigmoid(x1), b = sigmoid(x1) g(x2) rounded "
+                             "to bf16; gA, gBc ~ N(0,1) float32; seeded, generated on the GPU",
+                   "l2": "inputs larger than L2 (4.3 GB bf16 and 8.6 GB fp32 tensors against "
+                         "a 129 MB L2); no flush",
                    "parallelism": f"replicas x{ws_size} (channels/batches independent)"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
+        "gpu_launches": 2 * args.steps, "clocks": clocks,
     }
     if extra is not None:
         line["per_workload"] = extra
     return line
 
 
-def run_e2e(mg, inputs, dev, stream, args, ws, ws_size):
-    """Same metric through the public API with host buffers: each step copies
-    a, b, gA, gBc from pinned host memory, runs fwd + bwd and copies A, Bc,
-    da, db back to pinned host memory.  Steps are pipelined the way a caller
-    streaming batches would: copies in, compute and copies out run on three
-    streams over two device buffer sets, ordered by events, so step i's
-    copy-out overlaps step i+1's copy-in and compute.  The timed region spans
-    every step's copies and kernels."""
-    host_in = [x.cpu().pin_memory() for x in inputs]
-    host_out = [[torch.empty(inputs[0].shape, dtype=torch.float32).pin_memory() for _ in range(4)]
+def link_rates(dev, nbytes=1 << 30):
+    """Raw pinned host <-> device copy rates (GB/s): each direction alone and
+    both at once on two streams; median of 5."""
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn):
+        ts = []
+        for _ in range(6):
+            torch.cuda.synchronize(dev)
+            w = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(dev)
+            ts.append(time.perf_counter() - w)
+        return statistics.median(ts[1:])
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            d_in.copy_(h_in, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_out, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    th, td, tb = timed(h2d), timed(d2h), timed(both)
+    return {"h2d_GB_s": round(nbytes / th / 1e9, 1), "d2h_GB_s": round(nbytes / td / 1e9, 1),
+            "bidirectional_GB_s_each": round(nbytes / tb / 1e9, 1),
+            "how": "1 GiB pinned copies, median of 5, wall clock around synchronize"}
+
+
+def run_e2e(mg, inputs, dev, args, ws_size):
+    """Same metric through the public API with host buffers.  A caller streams
+    the batch through the GPU one batch row (T x D = 2^27 elements) at a time:
+    per row, a and b (bf16) and gA, gBc (fp32) are copied from pinned host
+    memory, fwd + bwd run on the row, and A, Bc, da, db are copied back to
+    pinned host memory.  Rows are pipelined on three streams (copy in,
+    compute, copy out) over two device buffer sets and two pinned host buffer
+    sets (the host ring a data loader would use), so host memory stays at two
+    rows.  A step is all B rows; the timed region spans every row's copies
+    and kernels."""
+    a, b, gA, gBc = inputs
+    host_in = [[x[r].cpu().pin_memory() for x in (a, b, gA, gBc)] for r in range(2)]
+    row_shape = (1, T, D)
+    host_out = [[torch.empty(row_shape, dtype=torch.float32).pin_memory() for _ in range(4)]
                 for _ in range(2)]
-    bi = sum(x.numel() * x.element_size() for x in host_in)
-    bo = sum(x.numel() * x.element_size() for x in host_out[0])
-    dev_in = [[torch.empty_like(x, device=dev) for x in host_in] for _ in range(2)]
-    dev_out = [[torch.empty(inputs[0].shape, dtype=torch.float32, device=dev) for _ in range(4)]
+    bi_row = sum(x.numel() * x.element_size() for x in host_in[0])
+    bo_row = sum(x.numel() * x.element_size() for x in host_out[0])
+    dev_in = [[torch.empty(row_shape, dtype=x.dtype, device=dev) for x in host_in[0]]
+              for _ in range(2)]
+    dev_out = [[torch.empty(row_shape, dtype=torch.float32, device=dev) for _ in range(4)]
                for _ in range(2)]
+    ws = mg.new_workspace(mg.linear_workspace_size(1, T, D), dev)
     s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
     ev = lambda: torch.cuda.Event()  # noqa: E731
-    k = max(3, min(args.steps, 20))
+    k = 3
+    rate = link_rates(dev)
 
     def run(nsteps):
         done_cmp, done_out = [None, None], [None, None]
-        for i in range(nsteps):
+        for i in range(nsteps * B):
             j = i % 2
             with torch.cuda.stream(s_in):          # inputs of buffer j are free
                 if done_cmp[j] is not None:
                     s_in.wait_event(done_cmp[j])
-                for d, h in zip(dev_in[j], host_in):
-                    d.copy_(h, non_blocking=True)
+                for d_, h in zip(dev_in[j], host_in[j]):
+                    d_.copy_(h.view(row_shape), non_blocking=True)
                 e_in = ev()
                 e_in.record(s_in)
             with torch.cuda.stream(s_cmp):         # outputs of buffer j are free
                 s_cmp.wait_event(e_in)
                 if done_out[j] is not None:
                     s_cmp.wait_event(done_out[j])
-                a, b, gA, gBc = dev_in[j]
-                A, Bc, da, db = dev_out[j]
-                mg.mg_linear_scan_fwd(a, b, out=(A, Bc), ws=ws)
-                mg.mg_linear_scan_bwd(a, A, Bc, gA, gBc, out=(da, db), ws=ws)
+                ra, rb, rgA, rgB = dev_in[j]
+                rA, rBc, rda, rdb = dev_out[j]
+                mg.mg_linear_scan_fwd(ra, rb, out=(rA, rBc), ws=ws)
+                mg.mg_linear_scan_bwd(ra, rA, rBc, rgA, rgB, out=(rda, rdb), ws=ws)
                 done_cmp[j] = ev()
                 done_cmp[j].record(s_cmp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(done_cmp[j])
-                for h, d in zip(host_out[j], dev_out[j]):
-                    h.copy_(d, non_blocking=True)
+                for h, d_ in zip(host_out[j], dev_out[j]):
+                    h.copy_(d_, non_blocking=True)
                 done_out[j] = ev()
                 done_out[j].record(s_out)
 
-    run(3)
+    run(1)
     torch.cuda.synchronize(dev)
+    mg.workspace_status(ws)
     barrier(ws_size)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -318,11 +406,18 @@ def run_e2e(mg, inputs, dev, stream, args, ws, ws_size):
     t1.record(s_out)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - w0
+    mg.workspace_status(ws)
     el, units = aggregate(max(t0.elapsed_time(t1) * 1e-3, wall), float(B * T * D * k), ws_size)
+    bi, bo = bi_row * B, bo_row * B
+    ms = el / k * 1e3
     return {"value": units / el, "unit": UNIT, "steps": k,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-            "ms_per_step": el / k * 1e3,
-            "pipelining": "copy-in / compute / copy-out on three streams, two buffer sets"}
+            "ms_per_step": ms,
+            "copy_GB_s_each_way": {"h2d": round(bi / (ms * 1e-3) / 1e9, 1),
+                                   "d2h": round(bo / (ms * 1e-3) / 1e9, 1)},
+            "link": rate,
+            "pipelining": f"{B} batch rows per step; copy-in / compute / copy-out on three "
+                          "streams, two device and two pinned host row buffers"}
 
 
 def _time_op(fn, iters, dev, flush):
@@ -344,11 +439,27 @@ def _time_op(fn, iters, dev, flush):
 
 
 def run_extra(mg, dev, peak):
-    """Each other workload once: median of a few repetitions, L2 flushed
+    """Each other workload once: median of several repetitions, L2 flushed
     before each, CUDA events."""
     from linear_recurrence_scans_gb300 import workloads as wl
     out = {}
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    # the float32 minGRU batch
+    Bq, Tq, Dq = 8, 4096, 1024
+    a, b, gA, gBc = wl.mingru_linear(Bq, Tq, Dq, seed=0, device=dev)
+    A, Bc = mg.mg_linear_scan_fwd(a, b)
+    da, db = torch.empty_like(A), torch.empty_like(A)
+    n = a.numel()
+    tf = _time_op(lambda: mg.mg_linear_scan_fwd(a, b, out=(A, Bc)), 20, dev, flush)
+    tb = _time_op(lambda: mg.mg_linear_scan_bwd(a, A, Bc, gA, gBc, out=(da, db)), 20, dev, flush)
+    out["mingru_linear_8x4096x1024"] = {
+        "op": "mg_linear_scan_fwd + mg_linear_scan_bwd (fp32)", "elements": n,
+        "fwd": {"ms": tf * 1e3, "elements_per_s": n / tf, "GB_s": 16 * n / tf / 1e9,
+                "frac": 16 * n / tf / 1e9 / peak},
+        "bwd": {"ms": tb * 1e3, "elements_per_s": n / tb, "GB_s": 28 * n / tb / 1e9,
+                "frac": 28 * n / tb / 1e9 / peak},
+        "step_elements_per_s": n / (tf + tb)}
+    del a, b, gA, gBc, A, Bc, da, db
     # log-space scan
     lc, lv = wl.mingru_log(16, 2048, 2048, seed=0, device=dev)
     h = torch.empty_like(lc)
@@ -371,12 +482,12 @@ def run_extra(mg, dev, peak):
     fp32_peak_tflops = 152 * 128 * 2 * 2.07e9 / 1e12  # FFMA lanes x 2 flop x max SM clock
     for name, (Bq, Tq, nq, k, v) in (("haar_affine_4x2048x64_k4v4", (4, 2048, 64, 4, 4)),
                                      ("haar_affine_2x1024x32_k16v16", (2, 1024, 32, 16, 16))):
-        A, Bm, gA, gB = wl.haar_affine(Bq, Tq, nq, k, v, seed=0, device=dev)
-        Abar, Bbar = torch.empty_like(A), torch.empty_like(Bm)
-        dA, dB = torch.empty_like(A), torch.empty_like(Bm)
+        Am, Bm, gAm, gBm = wl.haar_affine(Bq, Tq, nq, k, v, seed=0, device=dev)
+        Abar, Bbar = torch.empty_like(Am), torch.empty_like(Bm)
+        dA, dB = torch.empty_like(Am), torch.empty_like(Bm)
         S = Bq * Tq * nq
-        tf = _time_op(lambda: mg.mg_affine_scan_fwd(A, Bm, out=(Abar, Bbar)), 10, dev, flush)
-        tb = _time_op(lambda: mg.mg_affine_scan_bwd(A, Abar, Bbar, gA, gB, out=(dA, dB)), 10,
+        tf = _time_op(lambda: mg.mg_affine_scan_fwd(Am, Bm, out=(Abar, Bbar)), 10, dev, flush)
+        tb = _time_op(lambda: mg.mg_affine_scan_bwd(Am, Abar, Bbar, gAm, gBm, out=(dA, dB)), 10,
                       dev, flush)
         fb, bb = S * 4 * 2 * (k * k + k * v), S * 4 * (4 * k * k + 3 * k * v)
         ff, bf = S * 2 * (k ** 3 + k * k * v), S * 4 * (k ** 3 + k * k * v)
@@ -392,23 +503,8 @@ def run_extra(mg, dev, peak):
                              "roofline_frac": rb / tb},
                      "roofline": "max(bytes / HBM peak, flops / FP32 FFMA peak "
                                  f"{fp32_peak_tflops:.1f} TFLOP/s at 2070 MHz)"}
-        del A, Bm, gA, gB, Abar, Bbar, dA, dB
-    # large bf16 linear scan (2^31 elements)
-    Bq, Tq, Dq = 16, 32768, 4096
-    a, b, gA, gBc = wl.mingru_linear(Bq, Tq, Dq, seed=0, device=dev, in_dtype=torch.bfloat16)
-    A, Bc = mg.mg_linear_scan_fwd(a, b)
-    da, db = torch.empty_like(A), torch.empty_like(A)
-    n = a.numel()
-    tf = _time_op(lambda: mg.mg_linear_scan_fwd(a, b, out=(A, Bc)), 5, dev, flush)
-    tb = _time_op(lambda: mg.mg_linear_scan_bwd(a, A, Bc, gA, gBc, out=(da, db)), 5, dev, flush)
-    out["mingru_linear_bf16_16x32768x4096"] = {
-        "op": "mg_linear_scan_fwd + mg_linear_scan_bwd (bf16 a, b)", "elements": n,
-        "fwd": {"ms": tf * 1e3, "elements_per_s": n / tf, "GB_s": 12 * n / tf / 1e9,
-                "frac": 12 * n / tf / 1e9 / peak},
-        "bwd": {"ms": tb * 1e3, "elements_per_s": n / tb, "GB_s": 26 * n / tb / 1e9,
-                "frac": 26 * n / tb / 1e9 / peak},
-        "step_elements_per_s": n / (tf + tb)}
-    del a, b, gA, gBc, A, Bc, da, db, flush
+        del Am, Bm, gAm, gBm, Abar, Bbar, dA, dB
+    del flush
     mg.workspace_status()
     torch.cuda.empty_cache()
     return out
@@ -416,52 +512,114 @@ def run_extra(mg, dev, peak):
 
 # ------------------------------------------------------------- CPU legs
 
-def _oracle_step_on_sample(ncols: int, seed: int = 0):
-    """Oracle fwd + bwd on `ncols` independent channels (all of T) of the
-    workload: exact for those channels.  Returns (elements, seconds)."""
-    import oracle
+SAMPLE_COLS = 128   # whole-T channel columns per oracle call
+
+
+def _sample(seed: int, ncols: int = SAMPLE_COLS):
+    """`ncols` independent whole-T channels of the workload (a, b rounded to
+    bf16 as on the GPU, widened exactly to float64)."""
     from linear_recurrence_scans_gb300 import workloads as wl
-    a, b, gA, gBc = wl.mingru_linear(1, T, ncols, seed=seed)
-    a, b, gA, gBc = (x.double().numpy() for x in (a, b, gA, gBc))
-    t0 = time.perf_counter()
+    a, b, gA, gBc = wl.mingru_linear(1, T, ncols, seed=seed, in_dtype=torch.bfloat16)
+    return tuple(np.ascontiguousarray(x.double().numpy()) for x in (a, b, gA, gBc))
+
+
+def _oracle_fwd_bwd(sample):
+    """The oracle's fwd + bwd on one sample; returns its elements."""
+    import oracle
+    a, b, gA, gBc = sample
     A, Bc = oracle.linear_scan_fwd(a, b)
     oracle.linear_scan_bwd(a, A, Bc, gA, gBc)
-    return a.size, time.perf_counter() - t0
+    return a.size
+
+
+def _oracle_run(samples, threads: int, target_s: float):
+    """Run the oracle over `samples` (cycled) on `threads` host threads until
+    about `target_s` seconds have passed.  ctypes releases the GIL for the
+    duration of each C call, so the threads run on separate cores.  Returns
+    (elements, seconds, calls)."""
+    stop = time.perf_counter() + target_s
+    counts = [0] * threads
+    calls = [0] * threads
+
+    def worker(w):
+        i = w
+        while time.perf_counter() < stop:
+            counts[w] += _oracle_fwd_bwd(samples[i % len(samples)])
+            calls[w] += 1
+            i += threads
+
+    t0 = time.perf_counter()
+    ths = [threading.Thread(target=worker, args=(w,)) for w in range(threads)]
+    for t in ths:
+        t.start()
+    for t in ths:
+        t.join()
+    return sum(counts), time.perf_counter() - t0, sum(calls)
 
 
 def cpu_baseline(target_s: float = 10.0):
-    """The oracle as it stands (single-threaded C, float64) on a bounded
-    sample: whole batch rows of the workload (all T, all D of one b), one
-    after another (different seeds), until about `target_s` seconds of CPU
-    work."""
+    """The oracle as it stands (sequential float64 C) on bounded samples of
+    the workload: seeded whole-T channel columns (exact for those channels,
+    which are independent).  One leg on one core, one leg on every host core
+    (one oracle call per thread, each on its own sample)."""
     import oracle
     oracle.build()
-    els, secs, reps = 0, 0.0, 0
-    while secs < target_s and reps < 400:
-        e, s = _oracle_step_on_sample(D, seed=reps)
-        els += e
-        secs += s
-        reps += 1
-    return {"value": els / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{reps} x one batch row (T={T}, D={D}) of {WORKLOAD}, fwd+bwd, "
-                      f"float64 C oracle, {secs:.1f} s"}
+    cores = os.cpu_count() or 1
+    samples = [_sample(seed) for seed in range(4)]
+    e1, s1, c1 = _oracle_run(samples, 1, target_s)
+    eN, sN, cN = _oracle_run(samples, cores, target_s)
+    return {"value": e1 / s1, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{c1} oracle fwd+bwd calls on {SAMPLE_COLS} whole-T (T={T}) channel "
+                      f"columns of {WORKLOAD} (4 seeded samples cycled), {s1:.1f} s on one core",
+            "cpu_model": cpu_model(),
+            "all_cores": {"value": eN / sN, "unit": UNIT, "cores": cores,
+                          "sample": f"{cN} calls on {cores} threads, {sN:.1f} s"}}
 
 
 def run_reference(args, ws_size, rank):
-    """--impl reference: the oracle on the host cores, each step a bounded
-    sample of the workload (whole-T channel columns)."""
+    """--impl reference: the oracle on every host core, each step a bounded
+    sample of the workload (whole-T channel columns, one oracle call per
+    core)."""
     import oracle
     oracle.build()
-    # calibrate: size the per-step sample so the whole run stays within ~90 s
-    e, s = _oracle_step_on_sample(64)
-    per_col = s / 64
-    budget = 90.0 / max(1, args.steps + args.warmup)
-    ncols = int(max(8, min(D, budget / per_col)))
-    for i in range(args.warmup):
-        _oracle_step_on_sample(ncols, seed=i)
+    cores = os.cpu_count() or 1
+    samples = [_sample(seed) for seed in range(4)]
+    t = time.perf_counter()
+    _oracle_fwd_bwd(samples[0])
+    per_call = time.perf_counter() - t
+    # each step: `reps` calls per core, about 2 s of work on every core
+    reps = int(min(200, max(1, 2.0 / max(per_call, 1e-3))))
+
+    def one_step():
+        stop_calls = reps * cores
+        done = [0]
+        lock = threading.Lock()
+        els = [0]
+
+        def worker(w):
+            while True:
+                with lock:
+                    if done[0] >= stop_calls:
+                        return
+                    i = done[0]
+                    done[0] += 1
+                e = _oracle_fwd_bwd(samples[i % len(samples)])
+                with lock:
+                    els[0] += e
+
+        t0 = time.perf_counter()
+        ths = [threading.Thread(target=worker, args=(w,)) for w in range(cores)]
+        for th in ths:
+            th.start()
+        for th in ths:
+            th.join()
+        return els[0], time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        one_step()
     els, secs = 0, 0.0
-    for i in range(args.steps):
-        e, s = _oracle_step_on_sample(ncols, seed=100 + i)
+    for _ in range(args.steps):
+        e, s = one_step()
         els += e
         secs += s
     value = els / secs
@@ -472,8 +630,10 @@ def run_reference(args, ws_size, rank):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "B": B, "T": T, "D": D,
                    "ops": ["oracle.linear_scan_fwd", "oracle.linear_scan_bwd"]},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{ncols} whole-T channels of {WORKLOAD} per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "cpu_model": cpu_model(),
+                         "sample": f"{reps * cores} oracle calls per step on {SAMPLE_COLS} "
+                                   f"whole-T channel columns of {WORKLOAD}, {cores} threads"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -482,8 +642,8 @@ def run_reference(args, ws_size, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")

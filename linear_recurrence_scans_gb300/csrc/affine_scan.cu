@@ -26,7 +26,7 @@
 // (lookback.cuh).
 #include <type_traits>
 
-#include "stream_engine.cuh"
+#include "scan_engine.cuh"
 
 namespace mg {
 namespace {
@@ -692,210 +692,6 @@ struct LanePlan {
         return MG_OK;
     }
 };
-
-// ============================================ k <= 4 on the streaming engine
-// One sequence per lane: a tile is 32 consecutive sequences x TC steps, and at
-// one step those sequences' matrices are contiguous, so each staged row is one
-// bulk copy of 32 * k*k (or k*v) floats.  State as in the thread-owned ops.
-
-template <int K, int V, bool BWD>
-struct AffPick {
-    static constexpr int W = BWD ? K + V : V;
-    static constexpr int NS = K * K + K * W;
-    static constexpr int ROW = 32 * 4 * (BWD ? 3 * K * K + 2 * K * V : K * K + K * V);
-    static constexpr size_t smem(int ncw, int l, int nlb, int sg)
-    {
-        return 256 + size_t(sg) * (size_t(ncw) * l * ROW + size_t(ncw + 2) * NS * 32 * 4);
-    }
-    static constexpr int C[8][4] = {{4, 2, 3, 6}, {4, 2, 2, 5}, {4, 1, 2, 5}, {2, 2, 2, 5},
-                                    {2, 2, 1, 4}, {2, 1, 1, 4}, {1, 2, 1, 3}, {1, 1, 1, 3}};
-    static constexpr int pick()
-    {
-        for (int q = 0; q < 8; ++q)
-            if (smem(C[q][0], C[q][1], C[q][2], C[q][3]) <= 220 * 1024) return q;
-        return 7;
-    }
-    static constexpr int Q = pick();
-    static constexpr int NCW = C[Q][0], L = C[Q][1], NLB = C[Q][2], SG = C[Q][3];
-};
-
-template <int K, int V_>
-struct AffFwdT {
-    using P = AffPick<K, V_, false>;
-    static constexpr int VV = V_, KK = K * K, KV = K * V_;
-    static constexpr int NS = KK + KV, VEC = 1, NARR = 2;
-    static constexpr int NCW = P::NCW, L = P::L, NLB = P::NLB, STAGES = P::SG;
-    static constexpr bool kReverse = false;
-    using S = St<NS, 1>;
-    static constexpr int elt(int a) { return a == 0 ? KK * 4 : KV * 4; }
-    static constexpr int shift(int) { return 0; }
-    struct Args {
-        Staged src[NARR];
-        float *Abar;
-        float *Bbar;
-    };
-    __device__ static float *f(S &x) { return &x.v[0][0]; }
-    __device__ static const float *f(const S &x) { return &x.v[0][0]; }
-    __device__ static S identity()
-    {
-        S e;
-#pragma unroll
-        for (int i = 0; i < NS; ++i) e.v[i][0] = 0.f;
-#pragma unroll
-        for (int i = 0; i < K; ++i) e.v[i * K + i][0] = 1.f;
-        return e;
-    }
-    __device__ static S initial(const Args &, const ChanGeom &, int64_t, int, bool) { return identity(); }
-    __device__ static S combine(const S &x, const S &y)
-    {
-        S o;
-        mm<K, K, K>(f(y), f(x), f(o));
-        mm_add<K, K, VV>(f(y), f(x) + KK, f(y) + KK, f(o) + KK);
-        return o;
-    }
-    __device__ static S elem(const char *st, int i, int lane, int64_t t, const ChanGeom &g)
-    {
-        if (t >= g.T) return identity();
-        S e;
-        ld_floats<KK>(srow<AffFwdT, float>(st, 0, i, lane), f(e));
-        ld_floats<KV>(srow<AffFwdT, float>(st, 1, i, lane), f(e) + KK);
-        return e;
-    }
-    __device__ static void step2(const Args &p, const char *st, int i, int lane, int64_t t,
-                                 const ChanGeom &g, int64_t bb, int d, bool act, S &state)
-    {
-        if (t >= g.T) return;
-        state = combine(state, elem(st, i, lane, t, g));
-        if (act) {
-            const int64_t s = (bb * g.T + t) * g.D + d;
-            st_floats<KK>(p.Abar + s * KK, f(state));
-            st_floats<KV>(p.Bbar + s * KV, f(state) + KK);
-        }
-    }
-};
-
-template <int K, int V_>
-struct AffBwdT {
-    using P = AffPick<K, V_, true>;
-    static constexpr int VV = V_, W = K + V_, KK = K * K, KV = K * V_, KW = K * W;
-    static constexpr int NS = KK + KW, VEC = 1, NARR = 5;
-    static constexpr int NCW = P::NCW, L = P::L, NLB = P::NLB, STAGES = P::SG;
-    static constexpr bool kReverse = true;
-    using S = St<NS, 1>;
-    // 0 = A (row t+1), 1 = gAbar (t), 2 = gBbar (t), 3 = Abar (t-1), 4 = Bbar (t-1)
-    static constexpr int elt(int a) { return (a == 2 || a == 4) ? KV * 4 : KK * 4; }
-    static constexpr int shift(int a) { return a == 0 ? 1 : (a >= 3 ? -1 : 0); }
-    struct Args {
-        Staged src[NARR];
-        float *dA;
-        float *dB;
-    };
-    __device__ static float *f(S &x) { return &x.v[0][0]; }
-    __device__ static const float *f(const S &x) { return &x.v[0][0]; }
-    __device__ static S identity()
-    {
-        S e;
-#pragma unroll
-        for (int i = 0; i < NS; ++i) e.v[i][0] = 0.f;
-#pragma unroll
-        for (int i = 0; i < K; ++i) e.v[i * K + i][0] = 1.f;
-        return e;
-    }
-    __device__ static S initial(const Args &, const ChanGeom &, int64_t, int, bool) { return identity(); }
-    __device__ static S combine(const S &x, const S &y)
-    {
-        S o;
-        mm<K, K, K>(f(y), f(x), f(o));
-        mm_add<K, K, W>(f(y), f(x) + KK, f(y) + KK, f(o) + KK);
-        return o;
-    }
-    // E_C = A_{t+1}^T (zero at t = T-1), E_V = [gAbar_t | gBbar_t]
-    __device__ static void coef(const char *st, int i, int lane, int64_t t, const ChanGeom &g,
-                                float *Ct)
-    {
-        if (t + 1 < g.T) {
-            float a[KK];
-            ld_floats<KK>(srow<AffBwdT, float>(st, 0, i, lane), a);
-#pragma unroll
-            for (int r = 0; r < K; ++r)
-#pragma unroll
-                for (int c = 0; c < K; ++c) Ct[r * K + c] = a[c * K + r];
-        } else {
-#pragma unroll
-            for (int q = 0; q < KK; ++q) Ct[q] = 0.f;
-        }
-    }
-    __device__ static void value(const char *st, int i, int lane, float *G)
-    {
-        float ga[KK], gb[KV];
-        ld_floats<KK>(srow<AffBwdT, float>(st, 1, i, lane), ga);
-        ld_floats<KV>(srow<AffBwdT, float>(st, 2, i, lane), gb);
-#pragma unroll
-        for (int r = 0; r < K; ++r) {
-#pragma unroll
-            for (int c = 0; c < K; ++c) G[r * W + c] = ga[r * K + c];
-#pragma unroll
-            for (int c = 0; c < VV; ++c) G[r * W + K + c] = gb[r * VV + c];
-        }
-    }
-    __device__ static S elem(const char *st, int i, int lane, int64_t t, const ChanGeom &g)
-    {
-        if (t >= g.T) return identity();
-        S e;
-        coef(st, i, lane, t, g, f(e));
-        value(st, i, lane, f(e) + KK);
-        return e;
-    }
-    __device__ static void step2(const Args &p, const char *st, int i, int lane, int64_t t,
-                                 const ChanGeom &g, int64_t bb, int d, bool act, S &state)
-    {
-        if (t >= g.T) return;
-        float Ct[KK], G[KW], nV[KW];
-        coef(st, i, lane, t, g, Ct);
-        value(st, i, lane, G);
-        mm_add<K, K, W>(Ct, f(state) + KK, G, nV);
-#pragma unroll
-        for (int q = 0; q < KW; ++q) state.v[KK + q][0] = nV[q];
-        if (!act) return;
-        float dA[KK], dB[KV];
-#pragma unroll
-        for (int r = 0; r < K; ++r)
-#pragma unroll
-            for (int c = 0; c < VV; ++c) dB[r * VV + c] = nV[r * W + K + c];
-        if (t > 0) {
-            float Ap[KK], Bp[KV];
-            ld_floats<KK>(srow<AffBwdT, float>(st, 3, i, lane), Ap);
-            ld_floats<KV>(srow<AffBwdT, float>(st, 4, i, lane), Bp);
-#pragma unroll
-            for (int r = 0; r < K; ++r)
-#pragma unroll
-                for (int c = 0; c < K; ++c) {
-                    float acc = nV[r * W] * Ap[c * K];
-#pragma unroll
-                    for (int l = 1; l < K; ++l) acc = fmaf(nV[r * W + l], Ap[c * K + l], acc);
-#pragma unroll
-                    for (int l = 0; l < VV; ++l) acc = fmaf(nV[r * W + K + l], Bp[c * VV + l], acc);
-                    dA[r * K + c] = acc;
-                }
-        } else {
-#pragma unroll
-            for (int r = 0; r < K; ++r)
-#pragma unroll
-                for (int c = 0; c < K; ++c) dA[r * K + c] = nV[r * W + c];
-        }
-        const int64_t s = (bb * g.T + t) * g.D + d;
-        st_floats<KK>(p.dA + s * KK, dA);
-        st_floats<KV>(p.dB + s * KV, dB);
-    }
-};
-
-// The streaming variant needs every staged row (n sequences x element bytes)
-// to be a multiple of 16 bytes.
-template <int K, int V>
-bool aff_stream_ok(int64_t n)
-{
-    return (n * K * K * 4) % 16 == 0 && (n * K * V * 4) % 16 == 0;
-}
 
 // ============================================================ k in {8, 16}
 
@@ -1661,29 +1457,16 @@ using BigFwd = WarpPlan<WCfg<K, V, false, MG_AFW_NW, MG_AFW_L, bool(MG_AFW_DB), 
 template <int K, int V>
 using BigBwd = WarpPlan<WCfg<K, K + V, true, MG_AFWB_NW, MG_AFWB_L, bool(MG_AFWB_DB), MG_AFWB_NSL>>;
 
-// k <= 4: the lane kernel by default, the chunk engine with MGSCAN_ENGINE=chunked
-// (or where the blocks are not 16-byte multiples), the streaming engine with
-// MGSCAN_ENGINE=stream.
+// k <= 4: the lane kernel where its blocks are 16 to 128 bytes, the chunk
+// engine otherwise; k in {8, 16}: the warp kernel.
 template <int K, int V>
-bool use_lane(const LaunchOpts &o)
-{
-    if constexpr (lane_kernel_ok<K, V>()) return o.engine == LaunchOpts::kAuto;
-    return false;
-}
-
-template <int K, int V>
-size_t ws_kv(int64_t B, int64_t T, int64_t n, const LaunchOpts &o)
+size_t ws_kv(int64_t B, int64_t T, int64_t n)
 {
     size_t a, b;
     if constexpr (K <= 4) {
-        if (o.engine == LaunchOpts::kStream && aff_stream_ok<K, V>(n)) {
-            a = StreamPlan<AffFwdT<K, V>>::ws_bytes(B, T, n);
-            b = StreamPlan<AffBwdT<K, V>>::ws_bytes(B, T, n);
-        } else if (use_lane<K, V>(o)) {
-            if constexpr (lane_kernel_ok<K, V>()) {
-                a = LaneFwd<K, V>::ws_bytes(B, T, n);
-                b = LaneBwd<K, V>::ws_bytes(B, T, n);
-            }
+        if constexpr (lane_kernel_ok<K, V>()) {
+            a = LaneFwd<K, V>::ws_bytes(B, T, n);
+            b = LaneBwd<K, V>::ws_bytes(B, T, n);
         } else {
             a = SmallFwd<K, V>::ws_bytes(B, T, n);
             b = SmallBwd<K, V>::ws_bytes(B, T, n);
@@ -1701,16 +1484,10 @@ mg_status fwd_kv(const float *A, const float *Bm, float *Abar, float *Bbar, int6
 {
     const char *nm = "mg_affine_scan_fwd";
     if constexpr (K <= 4) {
-        if (o.engine == LaunchOpts::kStream && aff_stream_ok<K, V>(n))
-            return StreamPlan<AffFwdT<K, V>>::launch(
-                {{Staged{reinterpret_cast<const char *>(A), T}, Staged{reinterpret_cast<const char *>(Bm), T}},
-                 Abar, Bbar},
-                B, T, n, ws, wsb, s, o, nm);
-        if constexpr (lane_kernel_ok<K, V>()) {
-            if (use_lane<K, V>(o))
-                return LaneFwd<K, V>::launch({A, Bm, Abar, Bbar}, B, T, n, ws, wsb, s, o, nm);
-        }
-        return SmallFwd<K, V>::launch({A, Bm, Abar, Bbar}, B, T, n, ws, wsb, s, o, nm);
+        if constexpr (lane_kernel_ok<K, V>())
+            return LaneFwd<K, V>::launch({A, Bm, Abar, Bbar}, B, T, n, ws, wsb, s, o, nm);
+        else
+            return SmallFwd<K, V>::launch({A, Bm, Abar, Bbar}, B, T, n, ws, wsb, s, o, nm);
     } else {
         AffPtrs p{};
         p.A = A;
@@ -1728,18 +1505,12 @@ mg_status bwd_kv(const float *A, const float *Abar, const float *Bbar, const flo
 {
     const char *nm = "mg_affine_scan_bwd";
     if constexpr (K <= 4) {
-        auto stg = [&](const float *x) { return Staged{reinterpret_cast<const char *>(x), T}; };
-        if (o.engine == LaunchOpts::kStream && aff_stream_ok<K, V>(n))
-            return StreamPlan<AffBwdT<K, V>>::launch(
-                {{stg(A), stg(gAbar), stg(gBbar), stg(Abar), stg(Bbar)}, dA, dB}, B, T, n, ws, wsb,
-                s, o, nm);
-        if constexpr (lane_kernel_ok<K, V>()) {
-            if (use_lane<K, V>(o))
-                return LaneBwd<K, V>::launch({A, Abar, Bbar, gAbar, gBbar, dA, dB}, B, T, n, ws,
-                                             wsb, s, o, nm);
-        }
-        return SmallBwd<K, V>::launch({A, Abar, Bbar, gAbar, gBbar, dA, dB}, B, T, n, ws, wsb, s,
-                                      o, nm);
+        if constexpr (lane_kernel_ok<K, V>())
+            return LaneBwd<K, V>::launch({A, Abar, Bbar, gAbar, gBbar, dA, dB}, B, T, n, ws, wsb,
+                                         s, o, nm);
+        else
+            return SmallBwd<K, V>::launch({A, Abar, Bbar, gAbar, gBbar, dA, dB}, B, T, n, ws, wsb,
+                                          s, o, nm);
     } else {
         AffPtrs p{};
         p.A = A;
@@ -1772,9 +1543,9 @@ mg_status bwd_kv(const float *A, const float *Abar, const float *Bbar, const flo
 
 }  // namespace
 
-size_t affine_ws_bytes(int64_t B, int64_t T, int64_t n, int k, int v, const LaunchOpts &o)
+size_t affine_ws_bytes(int64_t B, int64_t T, int64_t n, int k, int v)
 {
-#define MG_CALL(K, V) return ws_kv<K, V>(B, T, n, o)
+#define MG_CALL(K, V) return ws_kv<K, V>(B, T, n)
     MG_KV_DISPATCH(k, v, MG_CALL)
 #undef MG_CALL
     return 0;

@@ -45,8 +45,8 @@ struct LinFwd {
         float *Bc;
     };
     struct Regs {
-        float a[L][VEC];
-        float b[L][VEC];
+        Raw<Tin, VEC> a[L];
+        Raw<Tin, VEC> b[L];
     };
 
     __device__ static void load(const Args &p, const ChanGeom &g, int64_t bb, int64_t t0, int d,
@@ -57,14 +57,11 @@ struct LinFwd {
             const int64_t t = t0 + i;
             if (act && t < g.T) {
                 const int64_t off = (bb * g.T + t) * g.D + d;
-                load_vec<VEC>(p.a + off, r.a[i]);
-                load_vec<VEC>(p.b + off, r.b[i]);
+                r.a[i].load(p.a + off);
+                r.b[i].load(p.b + off);
             } else {
-#pragma unroll
-                for (int v = 0; v < VEC; ++v) {
-                    r.a[i][v] = 1.f;
-                    r.b[i][v] = 0.f;
-                }
+                r.a[i].fill(1.f);
+                r.b[i].fill(0.f);
             }
         }
     }
@@ -151,7 +148,7 @@ struct LinBwd {
         float *db;
     };
     struct Regs {
-        float c[L][VEC];
+        Raw<Tin, VEC> c[L];
         float gA[L][VEC];
         float gB[L][VEC];
     };
@@ -167,15 +164,14 @@ struct LinBwd {
                 load_vec<VEC>(p.gA + off, r.gA[i]);
                 load_vec<VEC>(p.gBc + off, r.gB[i]);
                 if (t + 1 < g.T) {
-                    load_vec<VEC>(p.a + off + g.D, r.c[i]);
+                    r.c[i].load(p.a + off + g.D);
                 } else {
-#pragma unroll
-                    for (int v = 0; v < VEC; ++v) r.c[i][v] = 0.f;
+                    r.c[i].fill(0.f);
                 }
             } else {
+                r.c[i].fill(1.f);
 #pragma unroll
                 for (int v = 0; v < VEC; ++v) {
-                    r.c[i][v] = 1.f;
                     r.gA[i][v] = 0.f;
                     r.gB[i][v] = 0.f;
                 }
@@ -415,16 +411,15 @@ struct LogBwd {
     {
         const int64_t rem = g.T - t0;
         r.nval = act ? int(rem < 0 ? 0 : (rem > L ? L : rem)) : 0;
+        // every load of the round is issued before the first exponential
 #pragma unroll
         for (int i = 0; i <= L; ++i) {
             const int64_t t = t0 + i;
             if (act && t < g.T) {
                 load_vec<VEC>(p.lc + (bb * g.T + t) * g.D + d, r.ea[i]);
-#pragma unroll
-                for (int v = 0; v < VEC; ++v) r.ea[i][v] = ex2_sub(r.ea[i][v] * kLog2eF);
             } else {
 #pragma unroll
-                for (int v = 0; v < VEC; ++v) r.ea[i][v] = 0.f;
+                for (int v = 0; v < VEC; ++v) r.ea[i][v] = -INFINITY;
             }
             if (i < L) {
                 if (act && t < g.T) {
@@ -435,6 +430,10 @@ struct LogBwd {
                 }
             }
         }
+#pragma unroll
+        for (int i = 0; i <= L; ++i)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) r.ea[i][v] = ex2_sub(r.ea[i][v] * kLog2eF);
     }
     __device__ static S element(const Regs &r, int i)
     {
@@ -522,19 +521,19 @@ struct LogBwd {
 #define MG_LINF_MB 1
 #endif
 #ifndef MG_LINF16_VEC
-#define MG_LINF16_VEC 8
+#define MG_LINF16_VEC 4
 #endif
 #ifndef MG_LINF16_TX
 #define MG_LINF16_TX 32
 #endif
 #ifndef MG_LINF16_TY
-#define MG_LINF16_TY 8
+#define MG_LINF16_TY 2
 #endif
 #ifndef MG_LINF16_L
 #define MG_LINF16_L 8
 #endif
 #ifndef MG_LINF16_MB
-#define MG_LINF16_MB 1
+#define MG_LINF16_MB 4
 #endif
 #ifndef MG_LINB_TX
 #define MG_LINB_TX 16
@@ -552,13 +551,13 @@ struct LogBwd {
 #define MG_LINB16_TX 32
 #endif
 #ifndef MG_LINB16_TY
-#define MG_LINB16_TY 8
+#define MG_LINB16_TY 4
 #endif
 #ifndef MG_LINB16_L
 #define MG_LINB16_L 4
 #endif
 #ifndef MG_LINB16_MB
-#define MG_LINB16_MB 1
+#define MG_LINB16_MB 3
 #endif
 #ifndef MG_LOG_TX
 #define MG_LOG_TX 32
@@ -618,48 +617,32 @@ using LogF32s = ChanPlan<LogFwd<1, 8>, kTX, kTY>;
 
 }  // namespace
 
-namespace {
-bool use_stream_fwd(mg_dtype dt, int64_t D, const LaunchOpts &o)
+size_t linear_fwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D)
 {
-    const bool want = o.engine == LaunchOpts::kStream || (o.engine == LaunchOpts::kAuto && dt == MG_BF16);
-    return want && stream_linear_ok(dt, D);
-}
-bool use_stream_bwd(mg_dtype dt, int64_t D, const LaunchOpts &o)
-{
-    return o.engine == LaunchOpts::kStream && stream_linear_ok(dt, D);
-}
-}  // namespace
-
-size_t linear_fwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D, const LaunchOpts &o)
-{
-    if (use_stream_fwd(dt, D, o)) return stream_linear_fwd_ws_bytes(dt, B, T, D);
     if (dt == MG_F32) return D % 4 == 0 ? LinFwdF32::ws_bytes(B, T, D) : LinFwdF32s::ws_bytes(B, T, D);
     return D % MG_LINF16_VEC == 0 ? LinFwdB16::ws_bytes(B, T, D) : LinFwdB16s::ws_bytes(B, T, D);
 }
 
-size_t linear_bwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D, const LaunchOpts &o)
+size_t linear_bwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D)
 {
-    if (use_stream_bwd(dt, D, o)) return stream_linear_bwd_ws_bytes(dt, B, T, D);
     if (dt == MG_F32) return D % 4 == 0 ? LinBwdF32::ws_bytes(B, T, D) : LinBwdF32s::ws_bytes(B, T, D);
     return D % 4 == 0 ? LinBwdB16::ws_bytes(B, T, D) : LinBwdB16s::ws_bytes(B, T, D);
 }
 
-size_t linear_ws_bytes(int64_t B, int64_t T, int64_t D, const LaunchOpts &o)
+size_t linear_ws_bytes(int64_t B, int64_t T, int64_t D)
 {
     size_t m = 0;
     for (mg_dtype dt : {MG_F32, MG_BF16}) {
-        const size_t f = linear_fwd_ws_bytes(dt, B, T, D, o), b = linear_bwd_ws_bytes(dt, B, T, D, o);
+        const size_t f = linear_fwd_ws_bytes(dt, B, T, D), b = linear_bwd_ws_bytes(dt, B, T, D);
         m = f > m ? f : m;
         m = b > m ? b : m;
     }
     return m;
 }
 
-size_t log_ws_bytes(int64_t B, int64_t T, int64_t D, const LaunchOpts &o)
+size_t log_ws_bytes(int64_t B, int64_t T, int64_t D)
 {
-    size_t f;
-    if (o.engine == LaunchOpts::kStream && stream_log_ok(D)) f = stream_log_ws_bytes(B, T, D);
-    else f = D % 4 == 0 ? LogF32::ws_bytes(B, T, D) : LogF32s::ws_bytes(B, T, D);
+    const size_t f = D % 4 == 0 ? LogF32::ws_bytes(B, T, D) : LogF32s::ws_bytes(B, T, D);
     const size_t b = D % 4 == 0 ? LogBwdF32::ws_bytes(B, T, D) : LogBwdF32s::ws_bytes(B, T, D);
     return f > b ? f : b;
 }
@@ -669,7 +652,6 @@ mg_status launch_linear_fwd(const void *a, const void *b, mg_dtype dt, float *A,
                             const LaunchOpts &o)
 {
     const char *nm = "mg_linear_scan_fwd";
-    if (use_stream_fwd(dt, D, o)) return stream_linear_fwd(a, b, dt, A, Bc, B, T, D, ws, wsb, s, o);
     if (dt == MG_F32) {
         using F = const float *;
         if (D % 4 == 0)
@@ -687,8 +669,6 @@ mg_status launch_linear_bwd(const void *a, mg_dtype dt, const float *A, const fl
                             const LaunchOpts &o)
 {
     const char *nm = "mg_linear_scan_bwd";
-    if (use_stream_bwd(dt, D, o))
-        return stream_linear_bwd(a, dt, A, Bc, gA, gBc, da, db, B, T, D, ws, wsb, s, o);
     if (dt == MG_F32) {
         using F = const float *;
         if (D % 4 == 0)
@@ -714,8 +694,6 @@ mg_status launch_log_fwd(const float *lc, const float *lv, float *h, int64_t B, 
                          int64_t D, void *ws, size_t wsb, cudaStream_t s, const LaunchOpts &o)
 {
     const char *nm = "mg_log_scan_fwd";
-    if (o.engine == LaunchOpts::kStream && stream_log_ok(D))
-        return stream_log_fwd(lc, lv, h, B, T, D, ws, wsb, s, o);
     if (D % 4 == 0) return LogF32::launch({lc, lv, h}, B, T, D, ws, wsb, s, o, nm);
     return LogF32s::launch({lc, lv, h}, B, T, D, ws, wsb, s, o, nm);
 }

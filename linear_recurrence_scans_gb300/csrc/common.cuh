@@ -21,11 +21,6 @@ struct LaunchOpts {
     unsigned long long wait_limit_ns = 2000000000ull;  // 2 s of %globaltimer
     unsigned int max_polls = 1u << 24;
     long long stall_tile = -1;                         // testing only
-    // Which kernel shape serves an op that has two: kAuto picks the one
-    // measured faster for it (the persistent streaming engine for the bf16
-    // linear forward, the one-tile-per-CTA chunk engine otherwise); kChunked
-    // and kStream force one (the streaming engine only where D allows it).
-    enum Engine { kAuto = 0, kChunked = 1, kStream = 2 } engine = kAuto;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -54,13 +49,13 @@ inline Lookback make_lookback(void *ws, size_t n_tiles, const LaunchOpts &o)
 
 // Launchers (defined in channel_scan.cu / affine_scan.cu).  They assume the
 // arguments were validated by the C entry points and B, T, D > 0.
-// Workspace bytes a launch with options `o` needs (each mirrors its
-// launcher's choice of kernel shape).
-size_t linear_fwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D, const LaunchOpts &o);
-size_t linear_bwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D, const LaunchOpts &o);
-size_t linear_ws_bytes(int64_t B, int64_t T, int64_t D, const LaunchOpts &o);  // both, both dtypes
-size_t log_ws_bytes(int64_t B, int64_t T, int64_t D, const LaunchOpts &o);
-size_t affine_ws_bytes(int64_t B, int64_t T, int64_t n, int k, int v, const LaunchOpts &o);
+// Workspace bytes each launch needs (each mirrors its launcher's choice of
+// kernel shape).
+size_t linear_fwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D);
+size_t linear_bwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D);
+size_t linear_ws_bytes(int64_t B, int64_t T, int64_t D);  // both, both dtypes
+size_t log_ws_bytes(int64_t B, int64_t T, int64_t D);
+size_t affine_ws_bytes(int64_t B, int64_t T, int64_t n, int k, int v);
 
 mg_status launch_linear_fwd(const void *a, const void *b, mg_dtype dt, float *A, float *Bc,
                             int64_t B, int64_t T, int64_t D, void *ws, size_t ws_bytes,
@@ -82,24 +77,6 @@ mg_status launch_affine_bwd(const float *A, const float *Abar, const float *Bbar
                             const float *gAbar, const float *gBbar, float *dA, float *dB,
                             int64_t B, int64_t T, int64_t n, int k, int v, void *ws,
                             size_t ws_bytes, cudaStream_t s, const LaunchOpts &o);
-
-// Persistent warp-specialised variants (stream_scan.cu), used when D is a
-// multiple of the 16-byte vector width.
-bool stream_linear_ok(mg_dtype dt, int64_t D);
-bool stream_log_ok(int64_t D);
-size_t stream_linear_fwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D);
-size_t stream_linear_bwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D);
-size_t stream_log_ws_bytes(int64_t B, int64_t T, int64_t D);
-mg_status stream_linear_fwd(const void *a, const void *b, mg_dtype dt, float *A, float *Bc,
-                            int64_t B, int64_t T, int64_t D, void *ws, size_t ws_bytes,
-                            cudaStream_t s, const LaunchOpts &o);
-mg_status stream_linear_bwd(const void *a, mg_dtype dt, const float *A, const float *Bc,
-                            const float *gA, const float *gBc, float *da, float *db, int64_t B,
-                            int64_t T, int64_t D, void *ws, size_t ws_bytes, cudaStream_t s,
-                            const LaunchOpts &o);
-mg_status stream_log_fwd(const float *lc, const float *lv, float *h, int64_t B, int64_t T,
-                         int64_t D, void *ws, size_t ws_bytes, cudaStream_t s,
-                         const LaunchOpts &o);
 
 // ------------------------------------------------------------- device side
 
@@ -162,6 +139,65 @@ __device__ __forceinline__ void load_vec(const bf16_t *p, float (&o)[VEC])
         for (int v = 0; v < VEC; ++v) o[v] = bf16_bits_to_float(p[v].bits);
     }
 }
+
+// VEC consecutive input elements of type T kept in registers as loaded:
+// bf16 stays packed (two per 32-bit word, one for VEC = 1) until each value
+// is used, so a load is never tied to the instructions that widen it and
+// the registers it needs are halved.  v-th value: x[v]; fill(c) sets every
+// value to c (c exactly representable in T).
+template <typename T, int VEC>
+struct Raw;
+
+template <int VEC>
+struct Raw<float, VEC> {
+    float w[VEC];
+    __device__ __forceinline__ void load(const float *p) { load_vec<VEC>(p, w); }
+    __device__ __forceinline__ float operator[](int v) const { return w[v]; }
+    __device__ __forceinline__ void fill(float c)
+    {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) w[v] = c;
+    }
+};
+
+template <int VEC>
+struct Raw<bf16_t, VEC> {
+    static constexpr int NW = VEC == 1 ? 1 : VEC / 2;
+    static_assert(VEC == 1 || VEC % 2 == 0, "packed bf16 pairs");
+    unsigned w[NW];
+    __device__ __forceinline__ void load(const bf16_t *p)
+    {
+        if constexpr (VEC % 8 == 0) {
+#pragma unroll
+            for (int q = 0; q < VEC / 8; ++q) {
+                const uint4 x = *reinterpret_cast<const uint4 *>(p + 8 * q);
+                w[4 * q + 0] = x.x;
+                w[4 * q + 1] = x.y;
+                w[4 * q + 2] = x.z;
+                w[4 * q + 3] = x.w;
+            }
+        } else if constexpr (VEC == 4) {
+            const uint2 x = *reinterpret_cast<const uint2 *>(p);
+            w[0] = x.x;
+            w[1] = x.y;
+        } else if constexpr (VEC == 2) {
+            w[0] = *reinterpret_cast<const unsigned *>(p);
+        } else {
+            w[0] = p[0].bits;
+        }
+    }
+    __device__ __forceinline__ float operator[](int v) const
+    {
+        if constexpr (VEC == 1) return __uint_as_float(w[0] << 16);
+        return (v & 1) ? __uint_as_float(w[v >> 1] & 0xffff0000u) : __uint_as_float(w[v >> 1] << 16);
+    }
+    __device__ __forceinline__ void fill(float c)
+    {
+        const unsigned h = __float_as_uint(c) >> 16;
+#pragma unroll
+        for (int q = 0; q < NW; ++q) w[q] = VEC == 1 ? h : (h | (h << 16));
+    }
+};
 
 // Store VEC consecutive float32 values at p (aligned to VEC elements).
 template <int VEC>

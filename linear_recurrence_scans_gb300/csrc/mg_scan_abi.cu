@@ -92,20 +92,8 @@ mg_status check_ws(const char *fn, const void *ws, size_t ws_bytes, size_t need)
 
 bool valid_kv(int x) { return x == 1 || x == 2 || x == 4 || x == 8 || x == 16; }
 
-// Default launch options.  MGSCAN_ENGINE=chunked or =stream forces one
-// kernel shape for every op that has both (for comparisons and tuning);
-// otherwise each op takes the shape measured faster for it.
-LaunchOpts default_opts()
-{
-    static const LaunchOpts o = [] {
-        LaunchOpts x;
-        const char *e = getenv("MGSCAN_ENGINE");
-        if (e != nullptr && strcmp(e, "chunked") == 0) x.engine = LaunchOpts::kChunked;
-        if (e != nullptr && strcmp(e, "stream") == 0) x.engine = LaunchOpts::kStream;
-        return x;
-    }();
-    return o;
-}
+// Default launch options (bounded waits of 2 s, no stalled tile).
+LaunchOpts default_opts() { return LaunchOpts{}; }
 
 // ------------------------------------------------ static scratch (no-alloc)
 // mg_linear_scan_fwd_noalloc keeps its look-back workspace in this array
@@ -203,21 +191,21 @@ size_t mg_linear_scan_workspace_size(int64_t B, int64_t T, int64_t D)
 {
     if (B < 0 || T < 0 || D < 0) return 0;
     if (B == 0 || T == 0 || D == 0) return kControlBytes;
-    return linear_ws_bytes(B, T, D, default_opts());
+    return linear_ws_bytes(B, T, D);
 }
 
 size_t mg_log_scan_workspace_size(int64_t B, int64_t T, int64_t D)
 {
     if (B < 0 || T < 0 || D < 0) return 0;
     if (B == 0 || T == 0 || D == 0) return kControlBytes;
-    return log_ws_bytes(B, T, D, default_opts());
+    return log_ws_bytes(B, T, D);
 }
 
 size_t mg_affine_scan_workspace_size(int64_t B, int64_t T, int64_t n, int k, int v)
 {
     if (B < 0 || T < 0 || n < 0 || !valid_kv(k) || !valid_kv(v)) return 0;
     if (B == 0 || T == 0 || n == 0) return kControlBytes;
-    return affine_ws_bytes(B, T, n, k, v, default_opts());
+    return affine_ws_bytes(B, T, n, k, v);
 }
 
 mg_status mg_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream)
@@ -250,7 +238,7 @@ mg_status mg_linear_scan_fwd(const void *a, const void *b, mg_dtype in_dt, float
     MG_TRY(check_channels(fn, D));
     if (B == 0 || T == 0 || D == 0) return MG_OK;
     const size_t n = size_t(B) * T * D, isz = in_dt == MG_F32 ? 4 : 2;
-    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D, default_opts())));
+    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D)));
     MG_TRY(check_bufs(fn, {{a, n * isz, "a", false},
                            {b, n * isz, "b", false},
                            {A, n * 4, "A", true},
@@ -271,7 +259,7 @@ mg_status mg_linear_scan_bwd(const void *a, mg_dtype a_dt, const float *A, const
     MG_TRY(check_channels(fn, D));
     if (B == 0 || T == 0 || D == 0) return MG_OK;
     const size_t n = size_t(B) * T * D, isz = a_dt == MG_F32 ? 4 : 2;
-    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D, default_opts())));
+    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D)));
     MG_TRY(check_bufs(fn, {{a, n * isz, "a", false},
                            {A, n * 4, "A", false},
                            {Bc, n * 4, "Bc", false},
@@ -294,7 +282,7 @@ mg_status mg_log_scan_fwd(const float *log_coeffs, const float *log_values, floa
     if (T < 0) return fail(MG_ERR_INVALID_ARG, "%s: negative size", fn);
     if (B == 0 || T == 0 || D == 0) return MG_OK;
     const size_t n = size_t(B) * T * D, nv = size_t(B) * (T + 1) * D;
-    MG_TRY(check_ws(fn, ws, ws_bytes, log_ws_bytes(B, T, D, default_opts())));
+    MG_TRY(check_ws(fn, ws, ws_bytes, log_ws_bytes(B, T, D)));
     MG_TRY(check_bufs(fn, {{log_coeffs, n * 4, "log_coeffs", false},
                            {log_values, nv * 4, "log_values", false},
                            {h, n * 4, "h", true},
@@ -318,7 +306,7 @@ mg_status mg_log_scan_bwd(const float *log_coeffs, const float *log_values, cons
         const cudaError_t e = cudaMemsetAsync(dlog_values, 0, nv * 4, stream);
         return e == cudaSuccess ? MG_OK : fail(MG_ERR_LAUNCH, "%s: %s", fn, cudaGetErrorString(e));
     }
-    MG_TRY(check_ws(fn, ws, ws_bytes, log_ws_bytes(B, T, D, default_opts())));
+    MG_TRY(check_ws(fn, ws, ws_bytes, log_ws_bytes(B, T, D)));
     MG_TRY(check_bufs(fn, {{log_coeffs, n * 4, "log_coeffs", false},
                            {log_values, nv * 4, "log_values", false},
                            {h, n * 4, "h", false},
@@ -341,7 +329,7 @@ mg_status mg_affine_scan_fwd(const float *A, const float *Bm, float *Abar, float
     MG_TRY(check_dims(fn, {B, T, n, k, k > v ? k : v}));
     if (B == 0 || T == 0 || n == 0) return MG_OK;
     const size_t s = size_t(B) * T * n;
-    MG_TRY(check_ws(fn, ws, ws_bytes, affine_ws_bytes(B, T, n, k, v, default_opts())));
+    MG_TRY(check_ws(fn, ws, ws_bytes, affine_ws_bytes(B, T, n, k, v)));
     MG_TRY(check_bufs(fn, {{A, s * k * k * 4, "A", false},
                            {Bm, s * k * v * 4, "Bm", false},
                            {Abar, s * k * k * 4, "Abar", true},
@@ -362,7 +350,7 @@ mg_status mg_affine_scan_bwd(const float *A, const float *Abar, const float *Bba
     MG_TRY(check_dims(fn, {B, T, n, k, k > v ? k : v}));
     if (B == 0 || T == 0 || n == 0) return MG_OK;
     const size_t s = size_t(B) * T * n;
-    MG_TRY(check_ws(fn, ws, ws_bytes, affine_ws_bytes(B, T, n, k, v, default_opts())));
+    MG_TRY(check_ws(fn, ws, ws_bytes, affine_ws_bytes(B, T, n, k, v)));
     MG_TRY(check_bufs(fn, {{A, s * k * k * 4, "A", false},
                            {Abar, s * k * k * 4, "Abar", false},
                            {Bbar, s * k * v * 4, "Bbar", false},
@@ -386,7 +374,7 @@ mg_status mg_testing_linear_scan_fwd_stall(const float *a, const float *b, float
     MG_TRY(check_channels(fn, D));
     if (B == 0 || T == 0 || D == 0) return MG_OK;
     const size_t n = size_t(B) * T * D;
-    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D, default_opts())));
+    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D)));
     MG_TRY(check_bufs(fn, {{a, n * 4, "a", false},
                            {b, n * 4, "b", false},
                            {A, n * 4, "A", true},
@@ -414,7 +402,7 @@ mg_status mg_linear_scan_fwd_noalloc(const void *a, const void *b, mg_dtype in_d
     MG_TRY(check_channels(fn, D));
     if (B == 0 || T == 0 || D == 0) return MG_OK;
     const LaunchOpts o = default_opts();
-    const size_t need = linear_fwd_ws_bytes(in_dt, B, T, D, o);
+    const size_t need = linear_fwd_ws_bytes(in_dt, B, T, D);
     if (need > kNoAllocScratchBytes)
         return fail(MG_ERR_INVALID_ARG,
                     "%s: (B,T,D) = (%lld,%lld,%lld) needs %zu bytes of scratch; the static scratch "
