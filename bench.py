@@ -337,27 +337,30 @@ def link_rates(dev, nbytes=1 << 30):
             "how": "1 GiB pinned copies, median of 5, wall clock around synchronize"}
 
 
+NBUF = 3   # row buffers in the end-to-end pipeline (device and pinned host each)
+
+
 def run_e2e(mg, inputs, dev, args, ws_size):
     """Same metric through the public API with host buffers.  A caller streams
     the batch through the GPU one batch row (T x D = 2^27 elements) at a time:
     per row, a and b (bf16) and gA, gBc (fp32) are copied from pinned host
     memory, fwd + bwd run on the row, and A, Bc, da, db are copied back to
     pinned host memory.  Rows are pipelined on three streams (copy in,
-    compute, copy out) over two device buffer sets and two pinned host buffer
-    sets (the host ring a data loader would use), so host memory stays at two
-    rows.  A step is all B rows; the timed region spans every row's copies
-    and kernels."""
+    compute, copy out) over NBUF device buffer sets and NBUF pinned host
+    buffer sets (the host ring a data loader would use), so host memory
+    stays at NBUF rows.  A step is all B rows; the timed region spans every
+    row's copies and kernels."""
     a, b, gA, gBc = inputs
-    host_in = [[x[r].cpu().pin_memory() for x in (a, b, gA, gBc)] for r in range(2)]
+    host_in = [[x[r].cpu().pin_memory() for x in (a, b, gA, gBc)] for r in range(NBUF)]
     row_shape = (1, T, D)
     host_out = [[torch.empty(row_shape, dtype=torch.float32).pin_memory() for _ in range(4)]
-                for _ in range(2)]
+                for _ in range(NBUF)]
     bi_row = sum(x.numel() * x.element_size() for x in host_in[0])
     bo_row = sum(x.numel() * x.element_size() for x in host_out[0])
     dev_in = [[torch.empty(row_shape, dtype=x.dtype, device=dev) for x in host_in[0]]
-              for _ in range(2)]
+              for _ in range(NBUF)]
     dev_out = [[torch.empty(row_shape, dtype=torch.float32, device=dev) for _ in range(4)]
-               for _ in range(2)]
+               for _ in range(NBUF)]
     ws = mg.new_workspace(mg.linear_workspace_size(1, T, D), dev)
     s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
     ev = lambda: torch.cuda.Event()  # noqa: E731
@@ -365,9 +368,9 @@ def run_e2e(mg, inputs, dev, args, ws_size):
     rate = link_rates(dev)
 
     def run(nsteps):
-        done_cmp, done_out = [None, None], [None, None]
+        done_cmp, done_out = [None] * NBUF, [None] * NBUF
         for i in range(nsteps * B):
-            j = i % 2
+            j = i % NBUF
             with torch.cuda.stream(s_in):          # inputs of buffer j are free
                 if done_cmp[j] is not None:
                     s_in.wait_event(done_cmp[j])
@@ -416,8 +419,10 @@ def run_e2e(mg, inputs, dev, args, ws_size):
             "copy_GB_s_each_way": {"h2d": round(bi / (ms * 1e-3) / 1e9, 1),
                                    "d2h": round(bo / (ms * 1e-3) / 1e9, 1)},
             "link": rate,
+            "link_bound_ms_per_step": round(max(bi, bo) / (rate["bidirectional_GB_s_each"] * 1e9)
+                                            * 1e3, 1),
             "pipelining": f"{B} batch rows per step; copy-in / compute / copy-out on three "
-                          "streams, two device and two pinned host row buffers"}
+                          f"streams, {NBUF} device and {NBUF} pinned host row buffers"}
 
 
 def _time_op(fn, iters, dev, flush):
