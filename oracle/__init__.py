@@ -14,6 +14,12 @@ evaluated in double precision by ``mg_oracle.c``:
 * ``log_scan_fwd``      -- parallel_scan_log_fwd: h_1..h_T from log_coeffs, log_values
 * ``affine_scan_fwd``   -- affine_scan_fwd: Abar (running matrix product), Bbar
 * ``affine_scan_bwd``   -- affine_scan_bwd: dA, dB
+* ``mingru_gate``, ``mingru_scan_fwd``, ``mingru_scan_bwd`` -- the minGRU gate
+  (a = 1 - sigmoid(x1), b = sigmoid(x1) g(x2)) fused with the linear scan, and
+  its gradients with respect to x1, x2
+* ``linear_scan_varlen_fwd/bwd``, ``linear_scan_h0_fwd/bwd`` -- the linear
+  scan from a start state h0, over (B,T,D) or a packed variable-length batch
+* ``affine_scan_h0_fwd/bwd`` -- the affine scan from a start state H0
 
 Inputs are converted to contiguous float64 numpy arrays (a float32 or bf16
 value widens exactly).  Outputs are float64 numpy arrays.
@@ -71,8 +77,19 @@ class Oracle:
         lib.orc_log_scan_bwd.argtypes = [P, P, P, P, P, I64, I64, I64]
         lib.orc_affine_scan_fwd.argtypes = [P, P, P, P, I64, I64, I64, I, I]
         lib.orc_affine_scan_bwd.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I, I]
+        PI = ctypes.POINTER(ctypes.c_int64)
+        lib.orc_mingru_gate.argtypes = [P, P, P, P, I64]
+        lib.orc_mingru_scan_fwd.argtypes = [P, P, P, P, I64, I64, I64]
+        lib.orc_mingru_scan_bwd.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64]
+        lib.orc_linear_scan_varlen_fwd.argtypes = [P, P, PI, I64, P, P, P, I64]
+        lib.orc_linear_scan_varlen_bwd.argtypes = [P, PI, I64, P, P, P, P, P, P, P, P, I64]
+        lib.orc_affine_scan_h0_fwd.argtypes = [P, P, P, P, P, I64, I64, I64, I, I]
+        lib.orc_affine_scan_h0_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I64, I64, I64, I, I]
         for f in (lib.orc_linear_scan_fwd, lib.orc_linear_scan_bwd, lib.orc_log_scan_fwd,
-                  lib.orc_log_scan_bwd, lib.orc_affine_scan_fwd, lib.orc_affine_scan_bwd):
+                  lib.orc_log_scan_bwd, lib.orc_affine_scan_fwd, lib.orc_affine_scan_bwd,
+                  lib.orc_mingru_gate, lib.orc_mingru_scan_fwd, lib.orc_mingru_scan_bwd,
+                  lib.orc_linear_scan_varlen_fwd, lib.orc_linear_scan_varlen_bwd,
+                  lib.orc_affine_scan_h0_fwd, lib.orc_affine_scan_h0_bwd):
             f.restype = None
         self._lib = lib
 
@@ -140,6 +157,111 @@ class Oracle:
         return dA, dB
 
 
+    # -------------------------------------------- fused minGRU gate + scan
+
+    def mingru_gate(self, x1, x2):
+        """(a, b) = (1 - sigmoid(x1), sigmoid(x1) g(x2)), elementwise."""
+        x1, x2 = _f64(x1), _f64(x2)
+        assert x1.shape == x2.shape
+        a, b = np.empty_like(x1), np.empty_like(x1)
+        self._lib.orc_mingru_gate(_ptr(x1), _ptr(x2), _ptr(a), _ptr(b), x1.size)
+        return a, b
+
+    def mingru_scan_fwd(self, x1, x2):
+        """(A, Bc) of the linear scan on the minGRU gate of x1, x2 (B,T,D)."""
+        x1, x2 = _f64(x1), _f64(x2)
+        assert x1.ndim == 3 and x1.shape == x2.shape
+        A, Bc = np.empty_like(x1), np.empty_like(x1)
+        self._lib.orc_mingru_scan_fwd(_ptr(x1), _ptr(x2), _ptr(A), _ptr(Bc), *x1.shape)
+        return A, Bc
+
+    def mingru_scan_bwd(self, x1, x2, A, Bc, gA, gBc):
+        """(dx1, dx2) for L = sum(gA*A) + sum(gBc*Bc), A and Bc taken as given."""
+        x1, x2, A, Bc, gA, gBc = (_f64(x) for x in (x1, x2, A, Bc, gA, gBc))
+        assert x1.ndim == 3 and all(x.shape == x1.shape for x in (x2, A, Bc, gA, gBc))
+        dx1, dx2 = np.empty_like(x1), np.empty_like(x1)
+        self._lib.orc_mingru_scan_bwd(_ptr(x1), _ptr(x2), _ptr(A), _ptr(Bc), _ptr(gA), _ptr(gBc),
+                                      _ptr(dx1), _ptr(dx2), *x1.shape)
+        return dx1, dx2
+
+    # ------------------------------------------ start states, varlen batches
+
+    @staticmethod
+    def _cu(cu, Ttot):
+        cu = np.ascontiguousarray(np.asarray(cu, dtype=np.int64))
+        assert cu.ndim == 1 and cu[0] == 0 and cu[-1] == Ttot and np.all(np.diff(cu) >= 0)
+        return cu
+
+    def linear_scan_varlen_fwd(self, a, b, cu_seqlens, h0=None):
+        """(A, H) over packed rows a, b (Ttot, D); sequence s is rows
+        cu[s]..cu[s+1]-1, started from h0[s] (nseq, D) or 0."""
+        a, b = _f64(a), _f64(b)
+        assert a.ndim == 2 and a.shape == b.shape
+        cu = self._cu(cu_seqlens, a.shape[0])
+        nseq = cu.size - 1
+        h = None if h0 is None else _f64(h0)
+        assert h is None or h.shape == (nseq, a.shape[1])
+        A, H = np.empty_like(a), np.empty_like(a)
+        self._lib.orc_linear_scan_varlen_fwd(_ptr(a), _ptr(b), cu.ctypes.data_as(
+            ctypes.POINTER(ctypes.c_int64)), nseq, None if h is None else _ptr(h), _ptr(A), _ptr(H),
+            a.shape[1])
+        return A, H
+
+    def linear_scan_varlen_bwd(self, a, cu_seqlens, A, H, gA, gH, h0=None):
+        """(da, db, dh0) for L = sum(gA*A) + sum(gH*H); dh0 is None without h0."""
+        a, A, H, gA, gH = (_f64(x) for x in (a, A, H, gA, gH))
+        assert a.ndim == 2 and all(x.shape == a.shape for x in (A, H, gA, gH))
+        cu = self._cu(cu_seqlens, a.shape[0])
+        nseq = cu.size - 1
+        h = None if h0 is None else _f64(h0)
+        da, db = np.empty_like(a), np.empty_like(a)
+        dh0 = None if h is None else np.empty_like(h)
+        self._lib.orc_linear_scan_varlen_bwd(
+            _ptr(a), cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), nseq,
+            None if h is None else _ptr(h), _ptr(A), _ptr(H), _ptr(gA), _ptr(gH), _ptr(da), _ptr(db),
+            None if dh0 is None else _ptr(dh0), a.shape[1])
+        return da, db, dh0
+
+    def linear_scan_h0_fwd(self, a, b, h0):
+        """(A, H) for a, b (B,T,D) with start states h0 (B,D): the varlen op on
+        B sequences of length T."""
+        a, b = _f64(a), _f64(b)
+        Bn, T, D = a.shape
+        A, H = self.linear_scan_varlen_fwd(a.reshape(Bn * T, D), b.reshape(Bn * T, D),
+                                           np.arange(Bn + 1) * T, h0)
+        return A.reshape(a.shape), H.reshape(a.shape)
+
+    def linear_scan_h0_bwd(self, a, h0, A, H, gA, gH):
+        """(da, db, dh0) for the (B,T,D) forward with start states h0 (B,D)."""
+        a = _f64(a)
+        Bn, T, D = a.shape
+        flat = lambda x: _f64(x).reshape(Bn * T, D)  # noqa: E731
+        da, db, dh0 = self.linear_scan_varlen_bwd(flat(a), np.arange(Bn + 1) * T, flat(A), flat(H),
+                                                  flat(gA), flat(gH), h0)
+        return da.reshape(a.shape), db.reshape(a.shape), dh0
+
+    def affine_scan_h0_fwd(self, A, Bm, H0):
+        """(Abar, Bbar) for A (B,T,n,k,k), Bm (B,T,n,k,v) started from H0 (B,n,k,v)."""
+        A, Bm, H0 = _f64(A), _f64(Bm), _f64(H0)
+        B, T, n, k, _ = A.shape
+        v = Bm.shape[4]
+        assert H0.shape == (B, n, k, v)
+        Abar, Bbar = np.empty_like(A), np.empty_like(Bm)
+        self._lib.orc_affine_scan_h0_fwd(_ptr(A), _ptr(Bm), _ptr(H0), _ptr(Abar), _ptr(Bbar),
+                                         B, T, n, k, v)
+        return Abar, Bbar
+
+    def affine_scan_h0_bwd(self, A, H0, Abar, Bbar, gAbar, gBbar):
+        """(dA, dB, dH0) for L = <gAbar, Abar> + <gBbar, Bbar> with start state H0."""
+        A, H0, Abar, Bbar, gAbar, gBbar = (_f64(x) for x in (A, H0, Abar, Bbar, gAbar, gBbar))
+        B, T, n, k, _ = A.shape
+        v = Bbar.shape[4]
+        dA, dB, dH0 = np.empty_like(A), np.empty_like(Bbar), np.empty_like(H0)
+        self._lib.orc_affine_scan_h0_bwd(_ptr(A), _ptr(H0), _ptr(Abar), _ptr(Bbar), _ptr(gAbar),
+                                         _ptr(gBbar), _ptr(dA), _ptr(dB), _ptr(dH0), B, T, n, k, v)
+        return dA, dB, dH0
+
+
 _default = None
 
 
@@ -172,3 +294,39 @@ def affine_scan_fwd(A, Bm):
 
 def affine_scan_bwd(A, Abar, Bbar, gAbar, gBbar):
     return _oracle().affine_scan_bwd(A, Abar, Bbar, gAbar, gBbar)
+
+
+def mingru_gate(x1, x2):
+    return _oracle().mingru_gate(x1, x2)
+
+
+def mingru_scan_fwd(x1, x2):
+    return _oracle().mingru_scan_fwd(x1, x2)
+
+
+def mingru_scan_bwd(x1, x2, A, Bc, gA, gBc):
+    return _oracle().mingru_scan_bwd(x1, x2, A, Bc, gA, gBc)
+
+
+def linear_scan_varlen_fwd(a, b, cu_seqlens, h0=None):
+    return _oracle().linear_scan_varlen_fwd(a, b, cu_seqlens, h0)
+
+
+def linear_scan_varlen_bwd(a, cu_seqlens, A, H, gA, gH, h0=None):
+    return _oracle().linear_scan_varlen_bwd(a, cu_seqlens, A, H, gA, gH, h0)
+
+
+def linear_scan_h0_fwd(a, b, h0):
+    return _oracle().linear_scan_h0_fwd(a, b, h0)
+
+
+def linear_scan_h0_bwd(a, h0, A, H, gA, gH):
+    return _oracle().linear_scan_h0_bwd(a, h0, A, H, gA, gH)
+
+
+def affine_scan_h0_fwd(A, Bm, H0):
+    return _oracle().affine_scan_h0_fwd(A, Bm, H0)
+
+
+def affine_scan_h0_bwd(A, H0, Abar, Bbar, gAbar, gBbar):
+    return _oracle().affine_scan_h0_bwd(A, H0, Abar, Bbar, gAbar, gBbar)

@@ -298,3 +298,231 @@ void orc_affine_scan_bwd(const double *A, const double *Abar, const double *Bbar
     free(eye);
     free(zero);
 }
+
+/*
+ * ---------------------------------------------------------------------------
+ * The minGRU gate fused with the linear scan.
+ *
+ * A minGRU layer (the module whose scans the page "minGRU - Triton kernels"
+ * serves; its dispatch section names linear_scan_fwd and
+ * parallel_scan_log_fwd as the ops it calls) computes from two projections
+ * x1, x2 of its input the gate z = sigmoid(x1), the coefficient a = 1 - z
+ * and the value b = z * g(x2), with g(x) = x + 0.5 for x >= 0 and sigmoid(x)
+ * otherwise, then scans h_t = a_t h_{t-1} + b_t.  The gate is written here as
+ * that definition; 1 - sigmoid(x) is evaluated as sigmoid(-x), the same
+ * number without the cancellation of 1 - z near z = 1.
+ */
+static double orc_sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+static double orc_g(double x) { return x >= 0.0 ? x + 0.5 : orc_sigmoid(x); }
+
+/* dg/dx; at x = 0 the derivative of the branch that defines g there (x + 0.5). */
+static double orc_g_grad(double x)
+{
+    if (x >= 0.0) return 1.0;
+    const double s = orc_sigmoid(x);
+    return s * (1.0 - s);
+}
+
+/* a = 1 - sigmoid(x1), b = sigmoid(x1) g(x2), elementwise over n values. */
+void orc_mingru_gate(const double *x1, const double *x2, double *a, double *b, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        a[i] = orc_sigmoid(-x1[i]);
+        b[i] = orc_sigmoid(x1[i]) * orc_g(x2[i]);
+    }
+}
+
+/* The gate, then linear_scan_fwd: A and Bc of the scan on (a, b). */
+void orc_mingru_scan_fwd(const double *x1, const double *x2, double *A, double *Bc,
+                         int64_t B, int64_t T, int64_t D)
+{
+    const int64_t n = B * T * D;
+    double *a = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+    double *b = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+    orc_mingru_gate(x1, x2, a, b, n);
+    orc_linear_scan_fwd(a, b, A, Bc, B, T, D);
+    free(a);
+    free(b);
+}
+
+/*
+ * Gradients dx1, dx2 of L = sum(gA*A) + sum(gBc*Bc) for the fused op, A and
+ * Bc taken as given: linear_scan_bwd on the gate's (a, b) gives da, db, and
+ * the chain rule through the gate gives, with z = sigmoid(x1),
+ *   da/dx1 = -z (1 - z),   db/dx1 = z (1 - z) g(x2),   db/dx2 = z g'(x2)
+ *   dx1 = (db g(x2) - da) z (1 - z),   dx2 = db z g'(x2).
+ */
+void orc_mingru_scan_bwd(const double *x1, const double *x2, const double *A, const double *Bc,
+                         const double *gA, const double *gBc, double *dx1, double *dx2,
+                         int64_t B, int64_t T, int64_t D)
+{
+    const int64_t n = B * T * D;
+    const size_t bytes = (size_t)(n > 0 ? n : 1) * sizeof(double);
+    double *a = (double *)malloc(bytes), *b = (double *)malloc(bytes);
+    double *da = (double *)malloc(bytes), *db = (double *)malloc(bytes);
+    orc_mingru_gate(x1, x2, a, b, n);
+    orc_linear_scan_bwd(a, A, Bc, gA, gBc, da, db, B, T, D);
+    for (int64_t i = 0; i < n; ++i) {
+        const double z = orc_sigmoid(x1[i]);
+        dx1[i] = (db[i] * orc_g(x2[i]) - da[i]) * z * (1.0 - z);
+        dx2[i] = db[i] * z * orc_g_grad(x2[i]);
+    }
+    free(a);
+    free(b);
+    free(da);
+    free(db);
+}
+
+/*
+ * ---------------------------------------------------------------------------
+ * Nonzero initial state and packed variable-length batches.
+ *
+ * The page's log-space op takes log h_0 in slot 0 of log_values; the linear
+ * and affine ops start from h_0 = 0.  These give the linear recurrence a
+ * caller-chosen start state and let one packed (Ttot, D) tensor hold several
+ * sequences of different lengths, sequence s occupying rows cu[s] ..
+ * cu[s+1]-1 (cu[0] = 0, cu[nseq] = Ttot, non-decreasing).  For each sequence
+ * and channel d, with h0 the sequence's start state (0 when h0 is NULL):
+ *   A_t = a_t A_{t-1},          A before the first row = 1
+ *   H_t = a_t H_{t-1} + b_t,    H before the first row = h0[s, d]
+ */
+void orc_linear_scan_varlen_fwd(const double *a, const double *b, const int64_t *cu, int64_t nseq,
+                                const double *h0, double *A, double *H, int64_t D)
+{
+    for (int64_t s = 0; s < nseq; ++s)
+        for (int64_t d = 0; d < D; ++d) {
+            double Ap = 1.0, h = h0 ? h0[s * D + d] : 0.0;
+            for (int64_t r = cu[s]; r < cu[s + 1]; ++r) {
+                const double at = a[r * D + d];
+                Ap = at * Ap;
+                h = at * h + b[r * D + d];
+                A[r * D + d] = Ap;
+                H[r * D + d] = h;
+            }
+        }
+}
+
+/*
+ * Gradients of L = sum(gA*A) + sum(gH*H) for the varlen forward, A and H
+ * taken as given.  Within each sequence (rows r0 .. r1-1):
+ *   mu_r  = gA_r + a_{r+1} mu_{r+1},   lam_r = gH_r + a_{r+1} lam_{r+1}   (zero past r1-1)
+ *   da_r  = mu_r A_{r-1} + lam_r H_{r-1},  db_r = lam_r
+ * with A_{r0-1} = 1 and H_{r0-1} = h0[s, d]; and dL/dh0[s, d] = a_{r0} lam_{r0}
+ * (0 for an empty sequence).  dh0 is written only when h0 is not NULL.
+ */
+void orc_linear_scan_varlen_bwd(const double *a, const int64_t *cu, int64_t nseq,
+                                const double *h0, const double *A, const double *H,
+                                const double *gA, const double *gH, double *da, double *db,
+                                double *dh0, int64_t D)
+{
+    for (int64_t s = 0; s < nseq; ++s)
+        for (int64_t d = 0; d < D; ++d) {
+            double mu = 0.0, lam = 0.0;
+            const int64_t r0 = cu[s], r1 = cu[s + 1];
+            for (int64_t r = r1 - 1; r >= r0; --r) {
+                const double a_next = (r + 1 < r1) ? a[(r + 1) * D + d] : 0.0;
+                mu = gA[r * D + d] + a_next * mu;
+                lam = gH[r * D + d] + a_next * lam;
+                const double A_prev = (r > r0) ? A[(r - 1) * D + d] : 1.0;
+                const double H_prev = (r > r0) ? H[(r - 1) * D + d] : (h0 ? h0[s * D + d] : 0.0);
+                da[r * D + d] = mu * A_prev + lam * H_prev;
+                db[r * D + d] = lam;
+            }
+            /* after the loop lam is lam_{r0} (or 0 for an empty sequence) */
+            if (h0 && dh0) dh0[s * D + d] = r1 > r0 ? a[r0 * D + d] * lam : 0.0;
+        }
+}
+
+/*
+ * affine_scan_fwd with a caller-chosen start state H0 (B,n,k,v):
+ *   Abar_t = A_t @ Abar_{t-1},  Abar_0 = I
+ *   Bbar_t = A_t @ Bbar_{t-1} + B_t,  Bbar_0 = H0[b, n]
+ */
+void orc_affine_scan_h0_fwd(const double *A, const double *Bm, const double *H0, double *Abar,
+                            double *Bbar, int64_t B, int64_t T, int64_t n, int k, int v)
+{
+    const int64_t kk = (int64_t)k * k, kv = (int64_t)k * v;
+    double *P = (double *)malloc((size_t)kk * sizeof(double));
+    double *Hs = (double *)malloc((size_t)kv * sizeof(double));
+    double *tmp = (double *)malloc((size_t)(kk > kv ? kk : kv) * sizeof(double));
+    for (int64_t bi = 0; bi < B; ++bi)
+        for (int64_t ni = 0; ni < n; ++ni) {
+            for (int i = 0; i < k; ++i)
+                for (int j = 0; j < k; ++j)
+                    P[i * k + j] = (i == j) ? 1.0 : 0.0;
+            memcpy(Hs, H0 + (bi * n + ni) * kv, (size_t)kv * sizeof(double));
+            for (int64_t t = 0; t < T; ++t) {
+                const int64_t s = (bi * T + t) * n + ni;
+                const double *At = A + s * kk;
+                mat_mul(At, P, tmp, k, k, k);
+                memcpy(P, tmp, (size_t)kk * sizeof(double));
+                mat_mul(At, Hs, tmp, k, k, v);
+                for (int64_t e = 0; e < kv; ++e)
+                    Hs[e] = tmp[e] + Bm[s * kv + e];
+                memcpy(Abar + s * kk, P, (size_t)kk * sizeof(double));
+                memcpy(Bbar + s * kv, Hs, (size_t)kv * sizeof(double));
+            }
+        }
+    free(P);
+    free(Hs);
+    free(tmp);
+}
+
+/*
+ * Gradients of L = <gAbar, Abar> + <gBbar, Bbar> for the forward with H0:
+ * the affine adjoint recurrences, with Bbar_0 = H0 in dA_1, and
+ *   dH0 = A_1^T @ Lam_1   (k x v; zero when T = 0).
+ */
+void orc_affine_scan_h0_bwd(const double *A, const double *H0, const double *Abar,
+                            const double *Bbar, const double *gAbar, const double *gBbar,
+                            double *dA, double *dB, double *dH0, int64_t B, int64_t T, int64_t n,
+                            int k, int v)
+{
+    const int64_t kk = (int64_t)k * k, kv = (int64_t)k * v;
+    double *M = (double *)malloc((size_t)kk * sizeof(double));
+    double *L = (double *)malloc((size_t)kv * sizeof(double));
+    double *tmp = (double *)malloc((size_t)(kk > kv ? kk : kv) * sizeof(double));
+    double *eye = (double *)malloc((size_t)kk * sizeof(double));
+    for (int i = 0; i < k; ++i)
+        for (int j = 0; j < k; ++j)
+            eye[i * k + j] = (i == j) ? 1.0 : 0.0;
+    for (int64_t bi = 0; bi < B; ++bi)
+        for (int64_t ni = 0; ni < n; ++ni) {
+            const double *h0 = H0 + (bi * n + ni) * kv;
+            memset(M, 0, (size_t)kk * sizeof(double));
+            memset(L, 0, (size_t)kv * sizeof(double));
+            for (int64_t t = T - 1; t >= 0; --t) {
+                const int64_t s = (bi * T + t) * n + ni;
+                if (t + 1 < T) {
+                    const double *Anext = A + (s + n) * kk;
+                    mat_tmul(Anext, M, tmp, k, k, k);
+                    for (int64_t e = 0; e < kk; ++e)
+                        M[e] = tmp[e] + gAbar[s * kk + e];
+                    mat_tmul(Anext, L, tmp, k, k, v);
+                    for (int64_t e = 0; e < kv; ++e)
+                        L[e] = tmp[e] + gBbar[s * kv + e];
+                } else {
+                    memcpy(M, gAbar + s * kk, (size_t)kk * sizeof(double));
+                    memcpy(L, gBbar + s * kv, (size_t)kv * sizeof(double));
+                }
+                const double *Aprev = (t > 0) ? Abar + (s - n) * kk : eye;
+                const double *Bprev = (t > 0) ? Bbar + (s - n) * kv : h0;
+                double *dAt = dA + s * kk;
+                memset(dAt, 0, (size_t)kk * sizeof(double));
+                mat_mul_tadd(M, Aprev, dAt, k, k, k);
+                mat_mul_tadd(L, Bprev, dAt, k, v, k);
+                memcpy(dB + s * kv, L, (size_t)kv * sizeof(double));
+            }
+            /* after the loop L = Lam_1 */
+            double *dh = dH0 + (bi * n + ni) * kv;
+            if (T > 0)
+                mat_tmul(A + ((bi * T) * n + ni) * kk, L, dh, k, k, v);
+            else
+                memset(dh, 0, (size_t)kv * sizeof(double));
+        }
+    free(M);
+    free(L);
+    free(tmp);
+    free(eye);
+}

@@ -409,6 +409,280 @@ def pin_degenerate_shapes(orc):
     np.testing.assert_array_equal(Bc, b)
 
 
+# ------------------------------------------- fused minGRU gate + linear scan
+
+def _torch_gate(x1, x2):
+    """The minGRU gate written with torch float64 ops (independent of the C)."""
+    t1, t2 = torch.as_tensor(x1, dtype=torch.float64), torch.as_tensor(x2, dtype=torch.float64)
+    z = torch.sigmoid(t1)
+    g = torch.where(t2 >= 0, t2 + 0.5, torch.sigmoid(t2))
+    return (1 - z), z * g
+
+
+def pin_golden_mingru(orc):
+    g = _golden("mingru_gate_scan_T2.json")
+    gA, gBc = np.array([[[1.0], [0.0]]]), np.array([[[0.0], [1.0]]])
+    for case in g["cases"]:
+        x1 = np.array(case["x1"]) if "x1" in case else np.log(np.array(case["x1_exp"]))
+        x2 = np.array(case["x2"])
+        a, b = orc.mingru_gate(x1, x2)
+        A, Bc = orc.mingru_scan_fwd(x1, x2)
+        dx1, dx2 = orc.mingru_scan_bwd(x1, x2, A, Bc, gA, gBc)
+        for name, got in (("a", a), ("b", b), ("A", A), ("Bc", Bc), ("dx1", dx1), ("dx2", dx2)):
+            want = np.array(case[name])
+            if case["exact"]:
+                np.testing.assert_array_equal(got, want, err_msg=f"{case['name']} {name}")
+            else:
+                np.testing.assert_allclose(got, want, rtol=1e-14, atol=0,
+                                           err_msg=f"{case['name']} {name}")
+
+
+def pin_mingru_gate_vs_torch(orc):
+    """The gate against torch's float64 sigmoid, across the range (|x| up to 40,
+    where 1 - sigmoid must keep its relative accuracy), and its fixed points."""
+    rng = np.random.default_rng(51)
+    x1 = np.concatenate([rng.normal(scale=3, size=400), np.linspace(-40, 40, 81)])
+    x2 = np.concatenate([rng.normal(scale=3, size=400), np.linspace(-40, 40, 81)])
+    a, b = orc.mingru_gate(x1, x2)
+    ta = torch.sigmoid(-torch.tensor(x1)).numpy()          # 1 - sigmoid(x1), relatively exact
+    _, tb = _torch_gate(x1, x2)
+    np.testing.assert_allclose(a, ta, rtol=1e-14, atol=0)
+    np.testing.assert_allclose(b, tb.numpy(), rtol=1e-14, atol=0)
+    a0, b0 = orc.mingru_gate(np.zeros(3), np.array([0.0, 2.0, -np.inf]))
+    np.testing.assert_array_equal(a0, [0.5, 0.5, 0.5])
+    np.testing.assert_array_equal(b0, [0.25, 1.25, 0.0])
+
+
+def pin_mingru_fwd_closed_form(orc):
+    """A and Bc of the fused op by brute-force products and sums of torch's gate."""
+    rng = np.random.default_rng(52)
+    x1, x2 = rng.normal(size=(2, 9, 3)), rng.normal(size=(2, 9, 3))
+    a, b = (t.numpy() for t in _torch_gate(x1, x2))
+    A, Bc = orc.mingru_scan_fwd(x1, x2)
+    Bn, T, D = x1.shape
+    for bi in range(Bn):
+        for d in range(D):
+            for t in range(T):
+                prod = float(np.prod(a[bi, :t + 1, d]))
+                tot = sum(float(np.prod(a[bi, s + 1:t + 1, d])) * b[bi, s, d] for s in range(t + 1))
+                assert math.isclose(A[bi, t, d], prod, rel_tol=1e-13, abs_tol=0)
+                assert math.isclose(Bc[bi, t, d], tot, rel_tol=1e-12, abs_tol=1e-14)
+
+
+def _loss_mingru(orc, x1, x2, gA, gBc):
+    A, Bc = orc.mingru_scan_fwd(x1, x2)
+    return float(np.sum(gA * A) + np.sum(gBc * Bc))
+
+
+def pin_mingru_adjoint_fd(orc):
+    """Central differences of L in every x1, x2 (x2 kept off g's branch point)."""
+    rng = np.random.default_rng(53)
+    x1 = rng.normal(size=(1, 7, 2))
+    x2 = rng.normal(size=(1, 7, 2))
+    x2 = np.where(np.abs(x2) < 0.05, 0.3, x2)
+    gA, gBc = rng.normal(size=x1.shape), rng.normal(size=x1.shape)
+    A, Bc = orc.mingru_scan_fwd(x1, x2)
+    dx1, dx2 = orc.mingru_scan_bwd(x1, x2, A, Bc, gA, gBc)
+    eps = 1e-6
+    for arr, grad in ((x1, dx1), (x2, dx2)):
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + eps
+            lp = _loss_mingru(orc, x1, x2, gA, gBc)
+            arr[idx] = old - eps
+            lm = _loss_mingru(orc, x1, x2, gA, gBc)
+            arr[idx] = old
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(fd)), (idx, fd, grad[idx])
+
+
+def pin_mingru_adjoint_autograd(orc):
+    """torch.autograd through the gate and a float64 recurrence loop."""
+    rng = np.random.default_rng(54)
+    x1, x2 = rng.normal(size=(2, 8, 3)), rng.normal(size=(2, 8, 3))
+    x2[0, 3, 1] = 0.0                 # g's branch point: its derivative is that of x + 0.5
+    gA, gBc = rng.normal(size=x1.shape), rng.normal(size=x1.shape)
+    t1 = torch.tensor(x1, requires_grad=True)
+    t2 = torch.tensor(x2, requires_grad=True)
+    a, b = _torch_gate(t1, t2)
+    Ap = torch.ones(2, 3, dtype=torch.float64)
+    h = torch.zeros_like(Ap)
+    As, hs = [], []
+    for t in range(8):
+        Ap = a[:, t] * Ap
+        h = a[:, t] * h + b[:, t]
+        As.append(Ap)
+        hs.append(h)
+    L = (torch.stack(As, 1) * torch.tensor(gA)).sum() + (torch.stack(hs, 1) * torch.tensor(gBc)).sum()
+    g1, g2 = torch.autograd.grad(L, (t1, t2))
+    A, Bc = orc.mingru_scan_fwd(x1, x2)
+    dx1, dx2 = orc.mingru_scan_bwd(x1, x2, A, Bc, gA, gBc)
+    np.testing.assert_allclose(dx1, g1.numpy(), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dx2, g2.numpy(), rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------ start states, varlen batches
+
+def pin_golden_varlen_h0(orc):
+    g = _golden("linear_scan_varlen_h0.json")
+    a, b, h0 = np.array(g["a"]), np.array(g["b"]), np.array(g["h0"])
+    A, H = orc.linear_scan_varlen_fwd(a, b, g["cu_seqlens"], h0)
+    np.testing.assert_array_equal(A, np.array(g["A"]))
+    np.testing.assert_array_equal(H, np.array(g["H"]))
+    da, db, dh0 = orc.linear_scan_varlen_bwd(a, g["cu_seqlens"], A, H, np.array(g["gA"]),
+                                             np.array(g["gH"]), h0)
+    np.testing.assert_array_equal(da, np.array(g["da"]))
+    np.testing.assert_array_equal(db, np.array(g["db"]))
+    np.testing.assert_array_equal(dh0, np.array(g["dh0"]))
+
+
+def _packed(rng, lens, D):
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    a = rng.uniform(0.2, 1.3, (cu[-1], D)) * rng.choice([-1, 1], (cu[-1], D))
+    b = rng.normal(size=(cu[-1], D))
+    return a, b, cu
+
+
+def pin_varlen_is_independent_scans(orc):
+    """Each packed sequence is the plain scan of its own rows: without h0 the
+    linear op's (A, Bc) and adjoint; with h0, H = Bc + A h0 (the start state
+    carried by the running product) and A unchanged."""
+    rng = np.random.default_rng(61)
+    lens = [5, 0, 1, 9, 3]
+    a, b, cu = _packed(rng, lens, 3)
+    h0 = rng.normal(size=(len(lens), 3))
+    gA, gH = rng.normal(size=a.shape), rng.normal(size=a.shape)
+    A0, H0 = orc.linear_scan_varlen_fwd(a, b, cu)
+    A1, H1 = orc.linear_scan_varlen_fwd(a, b, cu, h0)
+    da0, db0, dh = orc.linear_scan_varlen_bwd(a, cu, A0, H0, gA, gH)
+    assert dh is None
+    for s in range(len(lens)):
+        r0, r1 = cu[s], cu[s + 1]
+        if r1 == r0:
+            continue
+        A, Bc = orc.linear_scan_fwd(a[None, r0:r1], b[None, r0:r1])
+        np.testing.assert_array_equal(A0[r0:r1], A[0])
+        np.testing.assert_array_equal(H0[r0:r1], Bc[0])
+        np.testing.assert_array_equal(A1[r0:r1], A[0])
+        np.testing.assert_allclose(H1[r0:r1], Bc[0] + A[0] * h0[s], rtol=1e-12, atol=1e-12)
+        da, db = orc.linear_scan_bwd(a[None, r0:r1], A, Bc, gA[None, r0:r1], gH[None, r0:r1])
+        np.testing.assert_array_equal(da0[r0:r1], da[0])
+        np.testing.assert_array_equal(db0[r0:r1], db[0])
+
+
+def pin_h0_batch_is_varlen(orc):
+    """The (B,T,D) form with h0 (B,D) against the identity H = Bc + A h0 of the
+    plain op (a start state folded into the first value, b_1 + a_1 h0)."""
+    rng = np.random.default_rng(62)
+    a, b = _tiny_linear(63, B=3, T=7, D=2)
+    h0 = rng.normal(size=(3, 2))
+    A, H = orc.linear_scan_h0_fwd(a, b, h0)
+    b2 = b.copy()
+    b2[:, 0] += a[:, 0] * h0
+    A2, Bc2 = orc.linear_scan_fwd(a, b2)
+    np.testing.assert_array_equal(A, A2)
+    np.testing.assert_allclose(H, Bc2, rtol=1e-13, atol=1e-13)
+
+
+def _loss_varlen(orc, a, b, cu, h0, gA, gH):
+    A, H = orc.linear_scan_varlen_fwd(a, b, cu, h0)
+    return float(np.sum(gA * A) + np.sum(gH * H))
+
+
+def pin_varlen_adjoint_fd(orc):
+    rng = np.random.default_rng(64)
+    a, b, cu = _packed(rng, [4, 0, 3, 1], 2)
+    h0 = rng.normal(size=(4, 2))
+    gA, gH = rng.normal(size=a.shape), rng.normal(size=a.shape)
+    A, H = orc.linear_scan_varlen_fwd(a, b, cu, h0)
+    da, db, dh0 = orc.linear_scan_varlen_bwd(a, cu, A, H, gA, gH, h0)
+    eps = 1e-6
+    for arr, grad in ((a, da), (b, db), (h0, dh0)):
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + eps
+            lp = _loss_varlen(orc, a, b, cu, h0, gA, gH)
+            arr[idx] = old - eps
+            lm = _loss_varlen(orc, a, b, cu, h0, gA, gH)
+            arr[idx] = old
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(fd)), (idx, fd, grad[idx])
+
+
+def pin_golden_affine_h0(orc):
+    g = _golden("affine_scan_h0_k2.json")
+    A, Bm, H0 = np.array(g["A"]), np.array(g["Bm"]), np.array(g["H0"])
+    Abar, Bbar = orc.affine_scan_h0_fwd(A, Bm, H0)
+    np.testing.assert_array_equal(Abar, np.array(g["Abar"]))
+    np.testing.assert_array_equal(Bbar, np.array(g["Bbar"]))
+    dA, dB, dH0 = orc.affine_scan_h0_bwd(A, H0, Abar, Bbar, np.array(g["gAbar"]),
+                                         np.array(g["gBbar"]))
+    np.testing.assert_array_equal(dA, np.array(g["dA"]))
+    np.testing.assert_array_equal(dB, np.array(g["dB"]))
+    np.testing.assert_array_equal(dH0, np.array(g["dH0"]))
+
+
+def pin_affine_h0_identity(orc):
+    """Bbar(H0) = Bbar(0) + Abar H0 (numpy matmul); Abar does not depend on H0;
+    H0 = 0 gives the plain op and its adjoint."""
+    rng = np.random.default_rng(65)
+    for (k, v) in ((2, 3), (4, 1), (3, 3)):
+        A, Bm = _rand_mats(rng, (2, 6, 3), k, v)
+        H0 = rng.normal(size=(2, 3, k, v))
+        Abar, Bbar = orc.affine_scan_h0_fwd(A, Bm, H0)
+        Abar0, Bbar0 = orc.affine_scan_fwd(A, Bm)
+        np.testing.assert_array_equal(Abar, Abar0)
+        np.testing.assert_allclose(Bbar, Bbar0 + Abar @ H0[:, None], rtol=1e-12, atol=1e-12)
+        gA, gB = rng.normal(size=A.shape), rng.normal(size=Bm.shape)
+        Z = np.zeros_like(H0)
+        Ab, Bb = orc.affine_scan_h0_fwd(A, Bm, Z)
+        dA, dB, _ = orc.affine_scan_h0_bwd(A, Z, Ab, Bb, gA, gB)
+        dA0, dB0 = orc.affine_scan_bwd(A, Abar0, Bbar0, gA, gB)
+        np.testing.assert_array_equal(dA, dA0)
+        np.testing.assert_array_equal(dB, dB0)
+
+
+def _loss_affine_h0(orc, A, Bm, H0, gA, gB):
+    Abar, Bbar = orc.affine_scan_h0_fwd(A, Bm, H0)
+    return float(np.sum(gA * Abar) + np.sum(gB * Bbar))
+
+
+def pin_affine_h0_adjoint_fd(orc):
+    rng = np.random.default_rng(66)
+    k, v = 2, 3
+    A, Bm = _rand_mats(rng, (1, 5, 2), k, v)
+    H0 = rng.normal(size=(1, 2, k, v))
+    gA, gB = rng.normal(size=A.shape), rng.normal(size=Bm.shape)
+    Abar, Bbar = orc.affine_scan_h0_fwd(A, Bm, H0)
+    dA, dB, dH0 = orc.affine_scan_h0_bwd(A, H0, Abar, Bbar, gA, gB)
+    eps = 1e-6
+    for arr, grad in ((A, dA), (Bm, dB), (H0, dH0)):
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + eps
+            lp = _loss_affine_h0(orc, A, Bm, H0, gA, gB)
+            arr[idx] = old - eps
+            lm = _loss_affine_h0(orc, A, Bm, H0, gA, gB)
+            arr[idx] = old
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(fd)), (idx, fd, grad[idx])
+
+
+def pin_new_degenerate_shapes(orc):
+    """Empty sequences and empty batches; T = 0 with H0 gives dH0 = 0."""
+    e = np.zeros((0, 3))
+    A, H = orc.linear_scan_varlen_fwd(e, e, [0, 0, 0], np.ones((2, 3)))
+    assert A.shape == (0, 3)
+    _, _, dh0 = orc.linear_scan_varlen_bwd(e, [0, 0, 0], e, e, e, e, np.ones((2, 3)))
+    np.testing.assert_array_equal(dh0, np.zeros((2, 3)))
+    A5 = np.zeros((1, 0, 2, 3, 3))
+    B5 = np.zeros((1, 0, 2, 3, 1))
+    H0 = np.ones((1, 2, 3, 1))
+    Ab, Bb = orc.affine_scan_h0_fwd(A5, B5, H0)
+    _, _, dH0 = orc.affine_scan_h0_bwd(A5, H0, Ab, Bb, A5, B5)
+    np.testing.assert_array_equal(dH0, np.zeros_like(H0))
+
+
 PINS = [
     pin_golden_linear, pin_golden_log, pin_golden_affine,
     pin_linear_closed_form, pin_linear_special_cases,
@@ -419,6 +693,11 @@ PINS = [
     pin_affine_running_product, pin_affine_orthogonal_invariant,
     pin_affine_adjoint_fd, pin_affine_adjoint_autograd,
     pin_degenerate_shapes,
+    pin_golden_mingru, pin_mingru_gate_vs_torch, pin_mingru_fwd_closed_form,
+    pin_mingru_adjoint_fd, pin_mingru_adjoint_autograd,
+    pin_golden_varlen_h0, pin_varlen_is_independent_scans, pin_h0_batch_is_varlen,
+    pin_varlen_adjoint_fd, pin_golden_affine_h0, pin_affine_h0_identity,
+    pin_affine_h0_adjoint_fd, pin_new_degenerate_shapes,
 ]
 
 
@@ -427,8 +706,8 @@ def test_oracle_pin(pin):
     pin(oracle._oracle())
 
 
-# Plausible mistakes, planted in copies of the oracle's C source.  Each must
-# make at least one pin fail.
+# Plausible mistakes, planted in copies of the oracle's C source (in every
+# function where the line occurs).  Each must make at least one pin fail.
 MUTANTS = {
     "linear_fwd_dropped_coefficient": ("h[d] = at * h[d] + b[row + d];", "h[d] = h[d] + b[row + d];"),
     "linear_fwd_exclusive_product": ("A[row + d] = Ap[d];", "A[row + d] = Ap[d] / at;"),
@@ -458,6 +737,25 @@ MUTANTS = {
     "affine_bwd_untransposed": ("mat_tmul(Anext, M, tmp, k, k, k);", "mat_mul(Anext, M, tmp, k, k, k);"),
     "affine_bwd_dropped_term": ("mat_mul_tadd(L, Bprev, dAt, k, v, k);", ""),
     "matmul_transposed_operand": ("s += X[i * m + l] * Y[l * c + j];", "s += X[l * m + i] * Y[l * c + j];"),
+    "gate_coefficient_sign": ("a[i] = orc_sigmoid(-x1[i]);", "a[i] = orc_sigmoid(x1[i]);"),
+    "gate_g_branch": ("return x >= 0.0 ? x + 0.5 : orc_sigmoid(x);",
+                      "return x >= 0.0 ? x + 0.5 : orc_sigmoid(-x);"),
+    "gate_g_grad_at_positive": ("if (x >= 0.0) return 1.0;", "if (x >= 0.0) return 0.5;"),
+    "gate_bwd_dx1_sign": ("dx1[i] = (db[i] * orc_g(x2[i]) - da[i]) * z * (1.0 - z);",
+                          "dx1[i] = (db[i] * orc_g(x2[i]) + da[i]) * z * (1.0 - z);"),
+    "gate_bwd_dx2_dropped_z": ("dx2[i] = db[i] * z * orc_g_grad(x2[i]);",
+                               "dx2[i] = db[i] * orc_g_grad(x2[i]);"),
+    "varlen_dropped_h0": ("double Ap = 1.0, h = h0 ? h0[s * D + d] : 0.0;", "double Ap = 1.0, h = 0.0;"),
+    "varlen_bwd_start_state": ("(h0 ? h0[s * D + d] : 0.0)", "0.0"),
+    "varlen_bwd_crosses_sequences": ("const double A_prev = (r > r0) ? A[(r - 1) * D + d] : 1.0;",
+                                     "const double A_prev = (r > 0) ? A[(r - 1) * D + d] : 1.0;"),
+    "varlen_dh0_index": ("a[r0 * D + d] * lam", "a[(r1 - 1) * D + d] * lam"),
+    "affine_h0_dropped": ("memcpy(Hs, H0 + (bi * n + ni) * kv, (size_t)kv * sizeof(double));",
+                          "memset(Hs, 0, (size_t)kv * sizeof(double));"),
+    "affine_h0_bwd_start_state": ("const double *Bprev = (t > 0) ? Bbar + (s - n) * kv : h0;",
+                                  "const double *Bprev = (t > 0) ? Bbar + (s - n) * kv : Bbar + s * kv;"),
+    "affine_dh0_untransposed": ("mat_tmul(A + ((bi * T) * n + ni) * kk, L, dh, k, k, v);",
+                                "mat_mul(A + ((bi * T) * n + ni) * kk, L, dh, k, k, v);"),
 }
 
 
@@ -466,7 +764,7 @@ def test_planted_mistakes_are_caught():
     tmp = tempfile.mkdtemp(prefix="orc_mut_")
     try:
         for name, (old, new) in MUTANTS.items():
-            assert src.count(old) == 1, name
+            assert src.count(old) >= 1, name   # planted wherever the line occurs
             path = os.path.join(tmp, f"{name}.c")
             with open(path, "w") as f:
                 f.write(src.replace(old, new))
