@@ -10,6 +10,9 @@
  *   mg_log_scan_bwd      <- its adjoint (derived; the page lists the forward only)
  *   mg_affine_scan_fwd   <- affine_scan_fwd        ("Generic k x k affine prefix scan")
  *   mg_affine_scan_bwd   <- affine_scan_bwd        ("Generic k x k affine-scan adjoint")
+ *   mg_mingru_scan_fwd/bwd, mg_linear_scan_bwd_bf16_grads <- the minGRU layer's
+ *                           gate fused into linear_scan_fwd/bwd, and the
+ *                           backward with bf16 gradients
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -134,6 +137,57 @@ mg_status mg_linear_scan_bwd(const void *a, mg_dtype a_dt,
                              const float *A, const float *Bc,
                              const float *gA, const float *gBc,
                              float *da, float *db,
+                             int64_t B, int64_t T, int64_t D,
+                             void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * linear_scan_bwd with the gradients rounded to bf16 (round to nearest
+ * even) instead of float32: the same arguments as mg_linear_scan_bwd except
+ * that da and db are (B,T,D) bf16 buffers, as autograd returns gradients in
+ * the dtype of a bf16 input.  Arithmetic stays float32; only the stores
+ * round.  Workspace: mg_linear_scan_workspace_size.
+ */
+mg_status mg_linear_scan_bwd_bf16_grads(const void *a, mg_dtype a_dt,
+                                        const float *A, const float *Bc,
+                                        const float *gA, const float *gBc,
+                                        void *da, void *db,
+                                        int64_t B, int64_t T, int64_t D,
+                                        void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * The minGRU gate fused into linear_scan_fwd.  A minGRU layer feeds the
+ * scan (page section "linear_scan_fwd", the op the layer's scan dispatch
+ * min_gru._dispatch_scan calls) with, for two projections x1, x2 of its
+ * input,
+ *   z = sigmoid(x1),  a = 1 - z,  b = z g(x2),  g(x) = x + 0.5 (x >= 0), sigmoid(x) (x < 0)
+ * This op computes a and b in registers from x1, x2 ((B,T,D), dtype x_dt,
+ * MG_F32 or MG_BF16) and writes the scan of (a, b) exactly as
+ * mg_linear_scan_fwd would: A (running product; may be NULL, then it is not
+ * written) and Bc (the h_0 = 0 solution), float32 (B,T,D).  a and b never
+ * reach memory.  Workspace: mg_mingru_scan_workspace_size.
+ */
+size_t mg_mingru_scan_workspace_size(int64_t B, int64_t T, int64_t D);
+
+mg_status mg_mingru_scan_fwd(const void *x1, const void *x2, mg_dtype x_dt,
+                             float *A, float *Bc,
+                             int64_t B, int64_t T, int64_t D,
+                             void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Gradients of the fused op: for L = sum(gA*A) + sum(gBc*Bc), with A and Bc
+ * the forward outputs (used as given), writes
+ *   dx1 = (db g(x2) - da) z (1 - z),   dx2 = db z g'(x2)
+ * where da, db are the linear-scan adjoints (mg_linear_scan_bwd) at the
+ * gate's (a, b), and g'(0) = 1 (the branch x + 0.5 defines g at 0).  gA and
+ * A are optional together: NULL for both means gA = 0 (a minGRU layer's loss
+ * depends on Bc = h only), and then A is not read.  dx1, dx2 are (B,T,D) of
+ * dtype grad_dt (MG_F32, or MG_BF16 rounded to nearest even).  Workspace:
+ * mg_mingru_scan_workspace_size.
+ */
+mg_status mg_mingru_scan_bwd(const void *x1, const void *x2, mg_dtype x_dt,
+                             const float *A, const float *Bc,
+                             const float *gA, const float *gBc,
+                             void *dx1, void *dx2, mg_dtype grad_dt,
                              int64_t B, int64_t T, int64_t D,
                              void *ws, size_t ws_bytes, cudaStream_t stream);
 

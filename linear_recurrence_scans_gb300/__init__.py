@@ -16,6 +16,10 @@ Ops (names of the C entry points; aliases with the names of the page
   alias ``parallel_scan_log_bwd`` (the adjoint of the log-space scan)
 * ``mg_affine_scan_fwd(A, Bm)             -> (Abar, Bbar)``  alias ``affine_scan_fwd``
 * ``mg_affine_scan_bwd(A, Abar, Bbar, gAbar, gBbar) -> (dA, dB)``  alias ``affine_scan_bwd``
+* ``mg_linear_scan_bwd_bf16_grads(a, A, Bc, gA, gBc) -> (da, db)`` (bf16 gradients)
+* ``mg_mingru_scan_fwd(x1, x2) -> (A, Bc)`` and ``mg_mingru_scan_bwd(x1, x2, A, Bc, gA, gBc)
+  -> (dx1, dx2)``: the minGRU gate fused into the linear scan (aliases
+  ``mingru_scan_fwd``, ``mingru_scan_bwd``)
 
 Every op accepts optional preallocated outputs (``out=(...)``), a workspace
 tensor (``ws=``, uint8, zero-filled before first use) and a stream
@@ -41,6 +45,8 @@ __all__ = [
     "affine_scan_fwd", "affine_scan_bwd",
     "linear_workspace_size", "log_workspace_size", "affine_workspace_size",
     "workspace_status", "new_workspace",
+    "mg_linear_scan_bwd_bf16_grads", "mg_mingru_scan_fwd", "mg_mingru_scan_bwd",
+    "mingru_workspace_size", "mingru_scan_fwd", "mingru_scan_bwd",
 ]
 
 MG_OK, MG_ERR_INVALID_ARG, MG_ERR_UNSUPPORTED, MG_ERR_LAUNCH, MG_ERR_TIMEOUT = range(5)
@@ -52,6 +58,8 @@ SYMBOLS = (
     "mg_affine_scan_workspace_size", "mg_workspace_init", "mg_workspace_status",
     "mg_linear_scan_fwd", "mg_linear_scan_bwd", "mg_log_scan_fwd", "mg_log_scan_bwd",
     "mg_affine_scan_fwd", "mg_affine_scan_bwd",
+    "mg_linear_scan_bwd_bf16_grads", "mg_mingru_scan_workspace_size",
+    "mg_mingru_scan_fwd", "mg_mingru_scan_bwd",
 )
 
 
@@ -107,6 +115,13 @@ def load():
         lib.mg_affine_scan_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, vp, sz, vp]
         lib.mg_affine_scan_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, i32,
                                            vp, sz, vp]
+        lib.mg_linear_scan_bwd_bf16_grads.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, i64, i64,
+                                                      i64, vp, sz, vp]
+        lib.mg_mingru_scan_workspace_size.argtypes = [i64, i64, i64]
+        lib.mg_mingru_scan_workspace_size.restype = sz
+        lib.mg_mingru_scan_fwd.argtypes = [vp, vp, i32, vp, vp, i64, i64, i64, vp, sz, vp]
+        lib.mg_mingru_scan_bwd.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, i32, i64, i64, i64,
+                                           vp, sz, vp]
         lib.mg_testing_linear_scan_fwd_stall.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, sz,
                                                          i64, ctypes.c_uint64, vp]
         lib.mg_testing_linear_scan_fwd_stall.restype = st
@@ -118,7 +133,8 @@ def load():
         lib.mg_linear_scan_fwd_noalloc_status.restype = st
         for name in ("mg_workspace_init", "mg_workspace_status", "mg_linear_scan_fwd",
                      "mg_linear_scan_bwd", "mg_log_scan_fwd", "mg_log_scan_bwd",
-                     "mg_affine_scan_fwd", "mg_affine_scan_bwd"):
+                     "mg_affine_scan_fwd", "mg_affine_scan_bwd", "mg_linear_scan_bwd_bf16_grads",
+                     "mg_mingru_scan_fwd", "mg_mingru_scan_bwd"):
             getattr(lib, name).restype = st
         _lib = lib
     return _lib
@@ -144,6 +160,10 @@ def log_workspace_size(B: int, T: int, D: int) -> int:
 
 def affine_workspace_size(B: int, T: int, n: int, k: int, v: int) -> int:
     return int(load().mg_affine_scan_workspace_size(B, T, n, k, v))
+
+
+def mingru_workspace_size(B: int, T: int, D: int) -> int:
+    return int(load().mg_mingru_scan_workspace_size(B, T, D))
 
 
 def new_workspace(nbytes: int, device) -> torch.Tensor:
@@ -202,14 +222,14 @@ def _prep(x: torch.Tensor, name: str, dtypes=(torch.float32,)) -> torch.Tensor:
     return x
 
 
-def _out(out, i, shape, like):
+def _out(out, i, shape, like, dtype=torch.float32):
     if out is not None and out[i] is not None:
         o = out[i]
-        if tuple(o.shape) != tuple(shape) or o.dtype != torch.float32 or not o.is_contiguous() \
+        if tuple(o.shape) != tuple(shape) or o.dtype != dtype or not o.is_contiguous() \
                 or o.device != like.device:
-            raise ValueError(f"out[{i}] must be a contiguous float32 tensor of shape {tuple(shape)}")
+            raise ValueError(f"out[{i}] must be a contiguous {dtype} tensor of shape {tuple(shape)}")
         return o
-    return torch.empty(shape, dtype=torch.float32, device=like.device)
+    return torch.empty(shape, dtype=dtype, device=like.device)
 
 
 _DT = {torch.float32: MG_F32, torch.bfloat16: MG_BF16}
@@ -250,6 +270,77 @@ def mg_linear_scan_bwd(a, A, Bc, gA, gBc, *, out=None, ws=None, stream=None):
                                      B, T, D, w.data_ptr(), w.numel(), sh),
            "mg_linear_scan_bwd")
     return da, db
+
+
+def mg_linear_scan_bwd_bf16_grads(a, A, Bc, gA, gBc, *, out=None, ws=None, stream=None):
+    """(da, db), bf16 (B,T,D): mg_linear_scan_bwd with the gradients rounded
+    to bf16.  a: float32 or bf16; A, Bc, gA, gBc: float32."""
+    a = _prep(a, "a", (torch.float32, torch.bfloat16))
+    A, Bc, gA, gBc = (_prep(x, n) for x, n in ((A, "A"), (Bc, "Bc"), (gA, "gA"), (gBc, "gBc")))
+    if a.dim() != 3 or any(x.shape != a.shape for x in (A, Bc, gA, gBc)):
+        raise ValueError("a, A, Bc, gA, gBc must all be (B, T, D)")
+    B, T, D = a.shape
+    da = _out(out, 0, a.shape, a, torch.bfloat16)
+    db = _out(out, 1, a.shape, a, torch.bfloat16)
+    sh = _stream_handle(stream, a.device)
+    w = _workspace(linear_workspace_size(B, T, D), a.device, sh, ws)
+    _check(load().mg_linear_scan_bwd_bf16_grads(a.data_ptr(), _DT[a.dtype], A.data_ptr(),
+                                                Bc.data_ptr(), gA.data_ptr(), gBc.data_ptr(),
+                                                da.data_ptr(), db.data_ptr(), B, T, D,
+                                                w.data_ptr(), w.numel(), sh),
+           "mg_linear_scan_bwd_bf16_grads")
+    return da, db
+
+
+def mg_mingru_scan_fwd(x1, x2, *, want_A=True, out=None, ws=None, stream=None):
+    """(A, Bc) float32 (B,T,D) of the linear scan on the minGRU gate
+    a = 1 - sigmoid(x1), b = sigmoid(x1) g(x2), computed inside the scan.
+    x1, x2: (B,T,D), both float32 or both bf16.  With want_A=False, A is not
+    written and None is returned in its place."""
+    x1 = _prep(x1, "x1", (torch.float32, torch.bfloat16))
+    x2 = _prep(x2, "x2", (x1.dtype,))
+    if x1.dim() != 3 or x2.shape != x1.shape:
+        raise ValueError("x1 and x2 must both be (B, T, D)")
+    B, T, D = x1.shape
+    A = _out(out, 0, x1.shape, x1) if want_A else None
+    Bc = _out(out, 1, x1.shape, x1)
+    sh = _stream_handle(stream, x1.device)
+    w = _workspace(mingru_workspace_size(B, T, D), x1.device, sh, ws)
+    _check(load().mg_mingru_scan_fwd(x1.data_ptr(), x2.data_ptr(), _DT[x1.dtype],
+                                     None if A is None else A.data_ptr(), Bc.data_ptr(), B, T, D,
+                                     w.data_ptr(), w.numel(), sh),
+           "mg_mingru_scan_fwd")
+    return A, Bc
+
+
+def mg_mingru_scan_bwd(x1, x2, A, Bc, gA, gBc, *, grad_dtype=torch.float32, out=None, ws=None,
+                       stream=None):
+    """(dx1, dx2) (B,T,D) of dtype grad_dtype: gradients of
+    sum(gA*A) + sum(gBc*Bc) through the fused gate + scan.  A and gA may both
+    be None (gA = 0, A not read)."""
+    x1 = _prep(x1, "x1", (torch.float32, torch.bfloat16))
+    x2 = _prep(x2, "x2", (x1.dtype,))
+    if (A is None) != (gA is None):
+        raise ValueError("A and gA must be given together (or both None)")
+    Bc, gBc = _prep(Bc, "Bc"), _prep(gBc, "gBc")
+    if A is not None:
+        A, gA = _prep(A, "A"), _prep(gA, "gA")
+    if x1.dim() != 3 or any(x is not None and x.shape != x1.shape for x in (x2, A, Bc, gA, gBc)):
+        raise ValueError("x1, x2, A, Bc, gA, gBc must all be (B, T, D)")
+    if grad_dtype not in _DT:
+        raise ValueError("grad_dtype must be float32 or bfloat16")
+    B, T, D = x1.shape
+    dx1 = _out(out, 0, x1.shape, x1, grad_dtype)
+    dx2 = _out(out, 1, x1.shape, x1, grad_dtype)
+    sh = _stream_handle(stream, x1.device)
+    w = _workspace(mingru_workspace_size(B, T, D), x1.device, sh, ws)
+    ptr = lambda x: None if x is None else x.data_ptr()  # noqa: E731
+    _check(load().mg_mingru_scan_bwd(x1.data_ptr(), x2.data_ptr(), _DT[x1.dtype], ptr(A),
+                                     Bc.data_ptr(), ptr(gA), gBc.data_ptr(), dx1.data_ptr(),
+                                     dx2.data_ptr(), _DT[grad_dtype], B, T, D, w.data_ptr(),
+                                     w.numel(), sh),
+           "mg_mingru_scan_bwd")
+    return dx1, dx2
 
 
 def mg_log_scan_fwd(log_coeffs, log_values, *, out=None, ws=None, stream=None):
@@ -363,3 +454,5 @@ parallel_scan_log_fwd = mg_log_scan_fwd
 parallel_scan_log_bwd = mg_log_scan_bwd
 affine_scan_fwd = mg_affine_scan_fwd
 affine_scan_bwd = mg_affine_scan_bwd
+mingru_scan_fwd = mg_mingru_scan_fwd
+mingru_scan_bwd = mg_mingru_scan_bwd

@@ -133,7 +133,8 @@ struct LinFwd {
 // ---------------------------------------------------------- linear backward
 // Reverse time.  Element of step t: (c_t = a_{t+1}, gA_t, gBc_t) with
 // c_{T} = 0; state (C, mu, lam): mu_t = gA_t + c_t mu_{t+1}, same for lam.
-template <typename Tin, int VEC_, int L_>
+// The gradients are stored as Tout (float32, or bf16 rounded to nearest).
+template <typename Tin, int VEC_, int L_, typename Tout = float>
 struct LinBwd {
     static constexpr int NS = 3, VEC = VEC_, L = L_;
     static constexpr bool kReverse = true;
@@ -144,8 +145,8 @@ struct LinBwd {
         const float *Bc;
         const float *gA;
         const float *gBc;
-        float *da;
-        float *db;
+        Tout *da;
+        Tout *db;
     };
     struct Regs {
         Raw<Tin, VEC> c[L];
@@ -610,6 +611,10 @@ using LinBwdF32 = ChanPlan<LinBwd<float, 4, MG_LINB_L>, MG_LINB_TX, MG_LINB_TY, 
 using LinBwdF32s = ChanPlan<LinBwd<float, 1, 4>, kTX, kTY>;
 using LinBwdB16 = ChanPlan<LinBwd<bf16_t, 4, MG_LINB16_L>, MG_LINB16_TX, MG_LINB16_TY, MG_LINB16_MB, MG_LINB16_R>;
 using LinBwdB16s = ChanPlan<LinBwd<bf16_t, 1, 4>, kTX, kTY>;
+using LinBwdB16G = ChanPlan<LinBwd<bf16_t, 4, MG_LINB16_L, bf16_t>, MG_LINB16_TX, MG_LINB16_TY, MG_LINB16_MB, MG_LINB16_R>;
+using LinBwdB16Gs = ChanPlan<LinBwd<bf16_t, 1, 4, bf16_t>, kTX, kTY>;
+using LinBwdF32G = ChanPlan<LinBwd<float, 4, MG_LINB_L, bf16_t>, MG_LINB_TX, MG_LINB_TY, MG_LINB_MB, MG_LINB_R>;
+using LinBwdF32Gs = ChanPlan<LinBwd<float, 1, 4, bf16_t>, kTX, kTY>;
 using LogF32 = ChanPlan<LogFwd<4, MG_LOG_L>, MG_LOG_TX, MG_LOG_TY, MG_LOG_MB, MG_LOG_R>;
 using LogBwdF32 = ChanPlan<LogBwd<4, MG_LOGB_L>, MG_LOGB_TX, MG_LOGB_TY, MG_LOGB_MB, MG_LOGB_R>;
 using LogBwdF32s = ChanPlan<LogBwd<1, 4>, kTX, kTY>;
@@ -629,13 +634,21 @@ size_t linear_bwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D)
     return D % 4 == 0 ? LinBwdB16::ws_bytes(B, T, D) : LinBwdB16s::ws_bytes(B, T, D);
 }
 
+size_t linear_bwd16_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D)
+{
+    if (dt == MG_F32) return D % 4 == 0 ? LinBwdF32G::ws_bytes(B, T, D) : LinBwdF32Gs::ws_bytes(B, T, D);
+    return D % 4 == 0 ? LinBwdB16G::ws_bytes(B, T, D) : LinBwdB16Gs::ws_bytes(B, T, D);
+}
+
 size_t linear_ws_bytes(int64_t B, int64_t T, int64_t D)
 {
     size_t m = 0;
     for (mg_dtype dt : {MG_F32, MG_BF16}) {
         const size_t f = linear_fwd_ws_bytes(dt, B, T, D), b = linear_bwd_ws_bytes(dt, B, T, D);
+        const size_t b16 = linear_bwd16_ws_bytes(dt, B, T, D);
         m = f > m ? f : m;
         m = b > m ? b : m;
+        m = b16 > m ? b16 : m;
     }
     return m;
 }
@@ -679,6 +692,24 @@ mg_status launch_linear_bwd(const void *a, mg_dtype dt, const float *A, const fl
     if (D % 4 == 0)
         return LinBwdB16::launch({H(a), A, Bc, gA, gBc, da, db}, B, T, D, ws, wsb, s, o, nm);
     return LinBwdB16s::launch({H(a), A, Bc, gA, gBc, da, db}, B, T, D, ws, wsb, s, o, nm);
+}
+
+mg_status launch_linear_bwd_bf16_grads(const void *a, mg_dtype dt, const float *A, const float *Bc,
+                                       const float *gA, const float *gBc, bf16_t *da, bf16_t *db,
+                                       int64_t B, int64_t T, int64_t D, void *ws, size_t wsb,
+                                       cudaStream_t s, const LaunchOpts &o)
+{
+    const char *nm = "mg_linear_scan_bwd_bf16_grads";
+    if (dt == MG_F32) {
+        using F = const float *;
+        if (D % 4 == 0)
+            return LinBwdF32G::launch({F(a), A, Bc, gA, gBc, da, db}, B, T, D, ws, wsb, s, o, nm);
+        return LinBwdF32Gs::launch({F(a), A, Bc, gA, gBc, da, db}, B, T, D, ws, wsb, s, o, nm);
+    }
+    using H = const bf16_t *;
+    if (D % 4 == 0)
+        return LinBwdB16G::launch({H(a), A, Bc, gA, gBc, da, db}, B, T, D, ws, wsb, s, o, nm);
+    return LinBwdB16Gs::launch({H(a), A, Bc, gA, gBc, da, db}, B, T, D, ws, wsb, s, o, nm);
 }
 
 mg_status launch_log_bwd(const float *lc, const float *lv, const float *h, const float *gh,

@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "lookback.cuh"
@@ -47,6 +48,8 @@ inline Lookback make_lookback(void *ws, size_t n_tiles, const LaunchOpts &o)
     return lb;
 }
 
+struct bf16_t;  // bf16 storage type (raw bits), defined below
+
 // Launchers (defined in channel_scan.cu / affine_scan.cu).  They assume the
 // arguments were validated by the C entry points and B, T, D > 0.
 // Workspace bytes each launch needs (each mirrors its launcher's choice of
@@ -64,6 +67,20 @@ mg_status launch_linear_bwd(const void *a, mg_dtype dt, const float *A, const fl
                             const float *gA, const float *gBc, float *da, float *db,
                             int64_t B, int64_t T, int64_t D, void *ws, size_t ws_bytes,
                             cudaStream_t s, const LaunchOpts &o);
+size_t linear_bwd16_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D);
+mg_status launch_linear_bwd_bf16_grads(const void *a, mg_dtype dt, const float *A, const float *Bc,
+                                       const float *gA, const float *gBc, bf16_t *da,
+                                       bf16_t *db, int64_t B, int64_t T, int64_t D,
+                                       void *ws, size_t ws_bytes, cudaStream_t s,
+                                       const LaunchOpts &o);
+size_t mingru_ws_bytes(int64_t B, int64_t T, int64_t D);
+mg_status launch_mingru_fwd(const void *x1, const void *x2, mg_dtype dt, float *A, float *Bc,
+                            int64_t B, int64_t T, int64_t D, void *ws, size_t ws_bytes,
+                            cudaStream_t s, const LaunchOpts &o);
+mg_status launch_mingru_bwd(const void *x1, const void *x2, mg_dtype dt, const float *A,
+                            const float *Bc, const float *gA, const float *gBc, void *dx1,
+                            void *dx2, mg_dtype grad_dt, int64_t B, int64_t T, int64_t D,
+                            void *ws, size_t ws_bytes, cudaStream_t s, const LaunchOpts &o);
 mg_status launch_log_bwd(const float *lc, const float *lv, const float *h, const float *gh,
                          float *dlc, float *dlv, int64_t B, int64_t T, int64_t D, void *ws,
                          size_t wsb, cudaStream_t s, const LaunchOpts &o);
@@ -211,6 +228,33 @@ __device__ __forceinline__ void store_vec(float *p, const float (&x)[VEC])
     } else {
 #pragma unroll
         for (int v = 0; v < VEC; ++v) p[v] = x[v];
+    }
+}
+
+// Store VEC consecutive values at p rounded to bf16 (round to nearest even).
+__device__ __forceinline__ unsigned pack_bf16x2(float lo, float hi)
+{
+    const unsigned l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+    const unsigned h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+    return l | (h << 16);
+}
+
+template <int VEC>
+__device__ __forceinline__ void store_vec(bf16_t *p, const float (&x)[VEC])
+{
+    if constexpr (VEC % 8 == 0) {
+#pragma unroll
+        for (int q = 0; q < VEC / 8; ++q)
+            *reinterpret_cast<uint4 *>(p + 8 * q) =
+                make_uint4(pack_bf16x2(x[8 * q], x[8 * q + 1]), pack_bf16x2(x[8 * q + 2], x[8 * q + 3]),
+                           pack_bf16x2(x[8 * q + 4], x[8 * q + 5]), pack_bf16x2(x[8 * q + 6], x[8 * q + 7]));
+    } else if constexpr (VEC == 4) {
+        *reinterpret_cast<uint2 *>(p) = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+    } else if constexpr (VEC == 2) {
+        *reinterpret_cast<unsigned *>(p) = pack_bf16x2(x[0], x[1]);
+    } else {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) p[v].bits = __bfloat16_as_ushort(__float2bfloat16_rn(x[v]));
     }
 }
 

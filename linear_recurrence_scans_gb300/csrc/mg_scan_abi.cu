@@ -32,21 +32,23 @@ struct Buf {
     size_t bytes;
     const char *name;
     bool output;
+    bool optional = false;   // NULL allowed (the buffer is then not used)
 };
 
 // NULL, alignment and overlap checks.  Outputs may overlap nothing.
 mg_status check_bufs(const char *fn, std::initializer_list<Buf> bufs)
 {
     for (const Buf &b : bufs) {
+        if (b.p == nullptr && b.optional) continue;
         if (b.p == nullptr) return fail(MG_ERR_INVALID_ARG, "%s: %s is NULL", fn, b.name);
         if (reinterpret_cast<uintptr_t>(b.p) % 16 != 0)
             return fail(MG_ERR_INVALID_ARG, "%s: %s is not 16-byte aligned", fn, b.name);
     }
     for (const Buf &o : bufs) {
-        if (!o.output) continue;
+        if (!o.output || o.p == nullptr) continue;
         const uintptr_t o0 = reinterpret_cast<uintptr_t>(o.p), o1 = o0 + o.bytes;
         for (const Buf &x : bufs) {
-            if (&x == &o) continue;
+            if (&x == &o || x.p == nullptr) continue;
             const uintptr_t x0 = reinterpret_cast<uintptr_t>(x.p), x1 = x0 + x.bytes;
             if (o0 < x1 && x0 < o1)
                 return fail(MG_ERR_INVALID_ARG, "%s: output %s overlaps %s", fn, o.name, x.name);
@@ -270,6 +272,93 @@ mg_status mg_linear_scan_bwd(const void *a, mg_dtype a_dt, const float *A, const
                            {ws, ws_bytes, "workspace", true}}));
     return launch_linear_bwd(a, a_dt, A, Bc, gA, gBc, da, db, B, T, D, ws, ws_bytes, stream,
                              default_opts());
+}
+
+mg_status mg_linear_scan_bwd_bf16_grads(const void *a, mg_dtype a_dt, const float *A,
+                                        const float *Bc, const float *gA, const float *gBc,
+                                        void *da, void *db, int64_t B, int64_t T, int64_t D,
+                                        void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    const char *fn = "mg_linear_scan_bwd_bf16_grads";
+    g_detail[0] = 0;
+    if (a_dt != MG_F32 && a_dt != MG_BF16)
+        return fail(MG_ERR_UNSUPPORTED, "%s: input dtype %d not supported", fn, int(a_dt));
+    MG_TRY(check_dims(fn, {B, T, D}));
+    MG_TRY(check_channels(fn, D));
+    if (B == 0 || T == 0 || D == 0) return MG_OK;
+    const size_t n = size_t(B) * T * D, isz = a_dt == MG_F32 ? 4 : 2;
+    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D)));
+    MG_TRY(check_bufs(fn, {{a, n * isz, "a", false},
+                           {A, n * 4, "A", false},
+                           {Bc, n * 4, "Bc", false},
+                           {gA, n * 4, "gA", false},
+                           {gBc, n * 4, "gBc", false},
+                           {da, n * 2, "da", true},
+                           {db, n * 2, "db", true},
+                           {ws, ws_bytes, "workspace", true}}));
+    return launch_linear_bwd_bf16_grads(a, a_dt, A, Bc, gA, gBc, static_cast<bf16_t *>(da),
+                                        static_cast<bf16_t *>(db), B, T, D, ws, ws_bytes, stream,
+                                        default_opts());
+}
+
+size_t mg_mingru_scan_workspace_size(int64_t B, int64_t T, int64_t D)
+{
+    if (B < 0 || T < 0 || D < 0) return 0;
+    if (B == 0 || T == 0 || D == 0) return kControlBytes;
+    return mingru_ws_bytes(B, T, D);
+}
+
+mg_status mg_mingru_scan_fwd(const void *x1, const void *x2, mg_dtype x_dt, float *A, float *Bc,
+                             int64_t B, int64_t T, int64_t D, void *ws, size_t ws_bytes,
+                             cudaStream_t stream)
+{
+    const char *fn = "mg_mingru_scan_fwd";
+    g_detail[0] = 0;
+    if (x_dt != MG_F32 && x_dt != MG_BF16)
+        return fail(MG_ERR_UNSUPPORTED, "%s: input dtype %d not supported", fn, int(x_dt));
+    MG_TRY(check_dims(fn, {B, T, D}));
+    MG_TRY(check_channels(fn, D));
+    if (B == 0 || T == 0 || D == 0) return MG_OK;
+    const size_t n = size_t(B) * T * D, isz = x_dt == MG_F32 ? 4 : 2;
+    MG_TRY(check_ws(fn, ws, ws_bytes, mingru_ws_bytes(B, T, D)));
+    MG_TRY(check_bufs(fn, {{x1, n * isz, "x1", false},
+                           {x2, n * isz, "x2", false},
+                           {A, n * 4, "A", true, true},
+                           {Bc, n * 4, "Bc", true},
+                           {ws, ws_bytes, "workspace", true}}));
+    return launch_mingru_fwd(x1, x2, x_dt, A, Bc, B, T, D, ws, ws_bytes, stream, default_opts());
+}
+
+mg_status mg_mingru_scan_bwd(const void *x1, const void *x2, mg_dtype x_dt, const float *A,
+                             const float *Bc, const float *gA, const float *gBc, void *dx1,
+                             void *dx2, mg_dtype grad_dt, int64_t B, int64_t T, int64_t D,
+                             void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    const char *fn = "mg_mingru_scan_bwd";
+    g_detail[0] = 0;
+    if (x_dt != MG_F32 && x_dt != MG_BF16)
+        return fail(MG_ERR_UNSUPPORTED, "%s: input dtype %d not supported", fn, int(x_dt));
+    if (grad_dt != MG_F32 && grad_dt != MG_BF16)
+        return fail(MG_ERR_UNSUPPORTED, "%s: gradient dtype %d not supported", fn, int(grad_dt));
+    MG_TRY(check_dims(fn, {B, T, D}));
+    MG_TRY(check_channels(fn, D));
+    if (B == 0 || T == 0 || D == 0) return MG_OK;
+    if ((gA == nullptr) != (A == nullptr))
+        return fail(MG_ERR_INVALID_ARG, "%s: A and gA must be given together (or both NULL)", fn);
+    const size_t n = size_t(B) * T * D, isz = x_dt == MG_F32 ? 4 : 2;
+    const size_t gsz = grad_dt == MG_F32 ? 4 : 2;
+    MG_TRY(check_ws(fn, ws, ws_bytes, mingru_ws_bytes(B, T, D)));
+    MG_TRY(check_bufs(fn, {{x1, n * isz, "x1", false},
+                           {x2, n * isz, "x2", false},
+                           {A, n * 4, "A", false, true},
+                           {Bc, n * 4, "Bc", false},
+                           {gA, n * 4, "gA", false, true},
+                           {gBc, n * 4, "gBc", false},
+                           {dx1, n * gsz, "dx1", true},
+                           {dx2, n * gsz, "dx2", true},
+                           {ws, ws_bytes, "workspace", true}}));
+    return launch_mingru_bwd(x1, x2, x_dt, A, Bc, gA, gBc, dx1, dx2, grad_dt, B, T, D, ws,
+                             ws_bytes, stream, default_opts());
 }
 
 mg_status mg_log_scan_fwd(const float *log_coeffs, const float *log_values, float *h, int64_t B,

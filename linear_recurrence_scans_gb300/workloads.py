@@ -17,6 +17,8 @@ kernels"):
 * ``mingru_linear``    x1,x2 ~ N(0,1); z = sigmoid(x1); a = 1 - z;
                        b = z * g(x2), g(x) = x + 0.5 (x >= 0) else sigmoid(x);
                        gA, gBc ~ N(0,1)                              (B,T,D)
+* ``mingru_x``         x1, x2 ~ N(0,1) raw (the fused gate + scan's inputs);
+                       gA, gBc ~ N(0,1)
 * ``mingru_log``       k, x ~ N(0,1); log_coeffs = -softplus(k);
                        log_values[:, 0] = log 0.5,
                        log_values[:, t] = -softplus(-k_{t-1}) + log g(x_{t-1})
@@ -69,6 +71,23 @@ def mingru_linear(B: int, T: int, D: int, seed: int = 0, device="cpu",
     gA = torch.randn(shape, generator=_gen(seed + 2, device), device=device, dtype=torch.float32)
     gBc = torch.randn(shape, generator=_gen(seed + 3, device), device=device, dtype=torch.float32)
     return a, b, gA, gBc
+
+
+def mingru_x(B: int, T: int, D: int, seed: int = 0, device="cpu", in_dtype=torch.float32,
+             grads: bool = True):
+    """(x1, x2, gA, gBc): the two gate projections of a minGRU layer, drawn
+    as in ``mingru_linear`` (same streams and seeds, so the gate of these x1,
+    x2 is that workload's a, b) but returned raw, for the fused gate + scan.
+    x1, x2 are cast to ``in_dtype``; gA, gBc are float32."""
+    shape = (B, T, D)
+    x1 = torch.randn(shape, generator=_gen(seed, device), device=device, dtype=torch.float32)
+    x2 = torch.randn(shape, generator=_gen(seed + 1, device), device=device, dtype=torch.float32)
+    x1, x2 = x1.to(in_dtype), x2.to(in_dtype)
+    if not grads:
+        return x1, x2, None, None
+    gA = torch.randn(shape, generator=_gen(seed + 2, device), device=device, dtype=torch.float32)
+    gBc = torch.randn(shape, generator=_gen(seed + 3, device), device=device, dtype=torch.float32)
+    return x1, x2, gA, gBc
 
 
 def mingru_log(B: int, T: int, D: int, seed: int = 0, device="cpu"):

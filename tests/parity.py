@@ -125,3 +125,43 @@ def affine_bwd_errors(A, Abar, Bbar, gAbar, gBbar, dA, dB) -> dict:
         SA, SB = block_rms(rdA), block_rms(rdB)
     return {"dA": scaled_error(_np(dA), rdA, SA),
             "dB": scaled_error(_np(dB), rdB, SB)}
+
+
+# ----------------------------------------------------- fused minGRU gate
+
+def _gate_scales(x1, x2):
+    """z = sigmoid(x1), g(x2) and |g'(x2)| in float64 (tolerance scales only)."""
+    x1, x2 = _np(x1), _np(x2)
+    z = 1.0 / (1.0 + np.exp(-x1))
+    s2 = 1.0 / (1.0 + np.exp(-x2))
+    g = np.where(x2 >= 0, x2 + 0.5, s2)
+    gp = np.where(x2 >= 0, 1.0, s2 * (1 - s2))
+    return z, g, gp
+
+
+def mingru_fwd_errors(x1, x2, A, Bc) -> dict:
+    """A is a product of positive factors (S = 0); Bc a sum of positive terms
+    (S = the oracle's Bc, its own componentwise scale).  A may be None."""
+    import oracle
+    rA, rBc = oracle.mingru_scan_fwd(x1, x2)
+    out = {"Bc": scaled_error(_np(Bc), rBc, np.abs(rBc))}
+    if A is not None:
+        out["A"] = scaled_error(_np(A), rA)
+    return out
+
+
+def mingru_bwd_errors(x1, x2, A, Bc, gA, gBc, dx1, dx2) -> dict:
+    """dx1 = (db g - da) z (1 - z), dx2 = db z g': S is that expression with
+    the linear adjoint's componentwise scales (the oracle on |inputs|) and
+    the magnitudes of each factor.  gA, A may be None (gA = 0)."""
+    import oracle
+    x1n, Bcn, gBcn = _np(x1), _np(Bc), _np(gBc)
+    gAn = np.zeros_like(x1n) if gA is None else _np(gA)
+    An = np.ones_like(x1n) if A is None else _np(A)
+    r1, r2 = oracle.mingru_scan_bwd(x1n, _np(x2), An, Bcn, gAn, gBcn)
+    a, _ = oracle.mingru_gate(x1n, _np(x2))
+    Sda, Sdb = oracle.linear_scan_bwd(a, np.abs(An), np.abs(Bcn), np.abs(gAn), np.abs(gBcn))
+    z, g, gp = _gate_scales(x1, x2)
+    S1 = (Sdb * g + Sda) * z * (1 - z)
+    S2 = Sdb * z * gp
+    return {"dx1": scaled_error(_np(dx1), r1, S1), "dx2": scaled_error(_np(dx2), r2, S2)}
