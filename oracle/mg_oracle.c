@@ -351,7 +351,8 @@ void orc_mingru_scan_fwd(const double *x1, const double *x2, double *A, double *
  * Bc taken as given: linear_scan_bwd on the gate's (a, b) gives da, db, and
  * the chain rule through the gate gives, with z = sigmoid(x1),
  *   da/dx1 = -z (1 - z),   db/dx1 = z (1 - z) g(x2),   db/dx2 = z g'(x2)
- *   dx1 = (db g(x2) - da) z (1 - z),   dx2 = db z g'(x2).
+ *   dx1 = (db g(x2) - da) z (1 - z),   dx2 = db z g'(x2),
+ * with 1 - z taken as sigmoid(-x1) here too.
  */
 void orc_mingru_scan_bwd(const double *x1, const double *x2, const double *A, const double *Bc,
                          const double *gA, const double *gBc, double *dx1, double *dx2,
@@ -364,8 +365,11 @@ void orc_mingru_scan_bwd(const double *x1, const double *x2, const double *A, co
     orc_mingru_gate(x1, x2, a, b, n);
     orc_linear_scan_bwd(a, A, Bc, gA, gBc, da, db, B, T, D);
     for (int64_t i = 0; i < n; ++i) {
-        const double z = orc_sigmoid(x1[i]);
-        dx1[i] = (db[i] * orc_g(x2[i]) - da[i]) * z * (1.0 - z);
+        /* z (1 - z) as sigmoid(x1) sigmoid(-x1): the same number without the
+         * cancellation of 1 - z near z = 1 (for x1 above ~37, 1 - z is 0 in
+         * double while z (1 - z) is still representable) */
+        const double z = orc_sigmoid(x1[i]), zc = orc_sigmoid(-x1[i]);
+        dx1[i] = (db[i] * orc_g(x2[i]) - da[i]) * z * zc;
         dx2[i] = db[i] * z * orc_g_grad(x2[i]);
     }
     free(a);

@@ -130,13 +130,14 @@ def affine_bwd_errors(A, Abar, Bbar, gAbar, gBbar, dA, dB) -> dict:
 # ----------------------------------------------------- fused minGRU gate
 
 def _gate_scales(x1, x2):
-    """z = sigmoid(x1), g(x2) and |g'(x2)| in float64 (tolerance scales only)."""
+    """z = sigmoid(x1), 1 - z, g(x2) and |g'(x2)| in float64 (tolerance scales only)."""
     x1, x2 = _np(x1), _np(x2)
     z = 1.0 / (1.0 + np.exp(-x1))
+    zc = 1.0 / (1.0 + np.exp(x1))          # 1 - z without cancellation
     s2 = 1.0 / (1.0 + np.exp(-x2))
     g = np.where(x2 >= 0, x2 + 0.5, s2)
     gp = np.where(x2 >= 0, 1.0, s2 * (1 - s2))
-    return z, g, gp
+    return z, zc, g, gp
 
 
 def mingru_fwd_errors(x1, x2, A, Bc) -> dict:
@@ -161,7 +162,7 @@ def mingru_bwd_errors(x1, x2, A, Bc, gA, gBc, dx1, dx2) -> dict:
     r1, r2 = oracle.mingru_scan_bwd(x1n, _np(x2), An, Bcn, gAn, gBcn)
     a, _ = oracle.mingru_gate(x1n, _np(x2))
     Sda, Sdb = oracle.linear_scan_bwd(a, np.abs(An), np.abs(Bcn), np.abs(gAn), np.abs(gBcn))
-    z, g, gp = _gate_scales(x1, x2)
-    S1 = (Sdb * g + Sda) * z * (1 - z)
+    z, zc, g, gp = _gate_scales(x1, x2)
+    S1 = (Sdb * g + Sda) * z * zc
     S2 = Sdb * z * gp
     return {"dx1": scaled_error(_np(dx1), r1, S1), "dx2": scaled_error(_np(dx2), r2, S2)}

@@ -453,6 +453,18 @@ def pin_mingru_gate_vs_torch(orc):
     np.testing.assert_array_equal(b0, [0.25, 1.25, 0.0])
 
 
+def pin_mingru_saturated_gate_derivative(orc):
+    """For T = 1 with gA = 0, gBc = 1: L = b = z g(x2), so dL/dx1 = z(1-z) g(x2)
+    exactly; at |x1| up to 60 (1 - z below double's resolution near 1) the
+    oracle must keep its relative accuracy (z(1-z) = e^-|x1| / (1 + e^-|x1|)^2)."""
+    x1 = np.array([[[-60.0, -40.0, -5.0, 0.0, 5.0, 40.0, 60.0]]])
+    x2 = np.full_like(x1, 1.5)
+    A, Bc = orc.mingru_scan_fwd(x1, x2)
+    dx1, _ = orc.mingru_scan_bwd(x1, x2, A, Bc, np.zeros_like(x1), np.ones_like(x1))
+    e = np.exp(-np.abs(x1))
+    np.testing.assert_allclose(dx1, e / (1 + e) ** 2 * 2.0, rtol=1e-13, atol=0)
+
+
 def pin_mingru_fwd_closed_form(orc):
     """A and Bc of the fused op by brute-force products and sums of torch's gate."""
     rng = np.random.default_rng(52)
@@ -694,6 +706,7 @@ PINS = [
     pin_affine_adjoint_fd, pin_affine_adjoint_autograd,
     pin_degenerate_shapes,
     pin_golden_mingru, pin_mingru_gate_vs_torch, pin_mingru_fwd_closed_form,
+    pin_mingru_saturated_gate_derivative,
     pin_mingru_adjoint_fd, pin_mingru_adjoint_autograd,
     pin_golden_varlen_h0, pin_varlen_is_independent_scans, pin_h0_batch_is_varlen,
     pin_varlen_adjoint_fd, pin_golden_affine_h0, pin_affine_h0_identity,
@@ -741,8 +754,10 @@ MUTANTS = {
     "gate_g_branch": ("return x >= 0.0 ? x + 0.5 : orc_sigmoid(x);",
                       "return x >= 0.0 ? x + 0.5 : orc_sigmoid(-x);"),
     "gate_g_grad_at_positive": ("if (x >= 0.0) return 1.0;", "if (x >= 0.0) return 0.5;"),
-    "gate_bwd_dx1_sign": ("dx1[i] = (db[i] * orc_g(x2[i]) - da[i]) * z * (1.0 - z);",
-                          "dx1[i] = (db[i] * orc_g(x2[i]) + da[i]) * z * (1.0 - z);"),
+    "gate_bwd_dx1_sign": ("dx1[i] = (db[i] * orc_g(x2[i]) - da[i]) * z * zc;",
+                          "dx1[i] = (db[i] * orc_g(x2[i]) + da[i]) * z * zc;"),
+    "gate_bwd_dx1_dropped_zc": ("dx1[i] = (db[i] * orc_g(x2[i]) - da[i]) * z * zc;",
+                                "dx1[i] = (db[i] * orc_g(x2[i]) - da[i]) * z;"),
     "gate_bwd_dx2_dropped_z": ("dx2[i] = db[i] * z * orc_g_grad(x2[i]);",
                                "dx2[i] = db[i] * orc_g_grad(x2[i]);"),
     "varlen_dropped_h0": ("double Ap = 1.0, h = h0 ? h0[s * D + d] : 0.0;", "double Ap = 1.0, h = 0.0;"),
