@@ -465,6 +465,33 @@ def run_extra(mg, dev, peak):
                 "frac": 28 * n / tb / 1e9 / peak},
         "step_elements_per_s": n / (tf + tb)}
     del a, b, gA, gBc, A, Bc, da, db
+    # the fused minGRU gate + scan, as a minGRU layer trains: forward without
+    # A, backward without gA (the loss depends on h = Bc only)
+    for name, (Bq, Tq, Dq, xdt) in (("mingru_fused_8x4096x1024", (8, 4096, 1024, torch.float32)),
+                                    ("mingru_fused_bf16_16x32768x4096",
+                                     (16, 32768, 4096, torch.bfloat16))):
+        x1, x2, _, gBc = wl.mingru_x(Bq, Tq, Dq, seed=0, device=dev, in_dtype=xdt)
+        _, Bc = mg.mingru_scan_fwd(x1, x2, want_A=False)
+        dx1, dx2 = torch.empty_like(x1), torch.empty_like(x1)
+        n = x1.numel()
+        xs = x1.element_size()
+        reps = 20 if n < (1 << 28) else 5
+        tf = _time_op(lambda: mg.mingru_scan_fwd(x1, x2, want_A=False, out=(None, Bc)), reps,
+                      dev, flush)
+        tb = _time_op(lambda: mg.mingru_scan_bwd(x1, x2, None, Bc, None, gBc, grad_dtype=xdt,
+                                                 out=(dx1, dx2)), reps, dev, flush)
+        fb = (2 * xs + 4) * n          # read x1, x2; write Bc
+        bb = (2 * xs + 8 + 2 * xs) * n  # read x1, x2, Bc, gBc; write dx1, dx2
+        out[name] = {
+            "op": "mg_mingru_scan_fwd (no A) + mg_mingru_scan_bwd (no gA), gradients in the "
+                  "input dtype", "elements": n,
+            "fwd": {"ms": tf * 1e3, "elements_per_s": n / tf, "GB_s": fb / tf / 1e9,
+                    "frac": fb / tf / 1e9 / peak, "algorithmic_bytes": fb},
+            "bwd": {"ms": tb * 1e3, "elements_per_s": n / tb, "GB_s": bb / tb / 1e9,
+                    "frac": bb / tb / 1e9 / peak, "algorithmic_bytes": bb},
+            "step_elements_per_s": n / (tf + tb)}
+        del x1, x2, gBc, Bc, dx1, dx2
+        torch.cuda.empty_cache()
     # log-space scan
     lc, lv = wl.mingru_log(16, 2048, 2048, seed=0, device=dev)
     h = torch.empty_like(lc)

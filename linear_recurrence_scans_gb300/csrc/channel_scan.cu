@@ -531,7 +531,7 @@ struct LogBwd {
 #define MG_LINF16_TY 2
 #endif
 #ifndef MG_LINF16_L
-#define MG_LINF16_L 8
+#define MG_LINF16_L 12
 #endif
 #ifndef MG_LINF16_MB
 #define MG_LINF16_MB 4

@@ -11,9 +11,9 @@
 //
 // Both run on the chunk engine (scan_engine.cuh) exactly as the linear scan
 // and its adjoint do (channel_scan.cu); the ops below only form the elements
-// from the gate in registers.  Pass 1 and pass 2 each evaluate the gate from
-// the raw x1, x2 they load, so nothing beyond the inputs is kept across the
-// look-back.  Gradients:
+// from the gate in registers.  The forward keeps pass 1's elements in shared
+// memory for pass 2; the backward evaluates the coefficient in pass 1 and
+// the whole gate in pass 2.  Gradients:
 //   da, db from the linear adjoint (mu, lam recurrences, reverse time)
 //   dx1 = (db g(x2) - da) z (1 - z),   dx2 = db z g'(x2)
 // with g'(0) = 1 (the branch x + 0.5 defines g at 0).
@@ -26,44 +26,56 @@ namespace {
 
 // --------------------------------------------------------------- the gate
 // sigmoid(+-x) from one exponential of -|x| (never overflows): with
-// e = exp(-|x|) and r = 1 / (1 + e), sigmoid(|x|) = r and sigmoid(-|x|) = e r.
-// 1 - sigmoid(x1) is sigmoid(-x1): no cancellation as z approaches 1.
-struct GateVals {
-    float a;   // 1 - z
-    float z;   // sigmoid(x1)
+// e = exp(-|x|) and r = 1 / (1 + e), sigmoid(|x|) = r and sigmoid(-|x|) = e r,
+// so 1 - sigmoid(x1) is formed as sigmoid(-x1), without the cancellation of
+// 1 - z as z approaches 1.  The exponentials are the hardware 2^x (PTX
+// ex2.approx, relative error about 2^-22, subnormal results kept), and the
+// two reciprocals 1 / (1 + e1), 1 / (1 + e2) share one: with
+// R = 1 / ((1 + e1)(1 + e2)), 1 / (1 + e1) = R (1 + e2) and
+// 1 / (1 + e2) = R (1 + e1) (the product lies in (1, 4], no overflow).
+struct Gate {
+    float a;    // 1 - z
+    float z;    // sigmoid(x1)
+    float g;    // g(x2)
+    float gp;   // g'(x2)
 };
 
-__device__ __forceinline__ GateVals gate_z(float x1)
+__device__ __forceinline__ Gate gate(float x1, float x2)
 {
-    const float e = expf(-fabsf(x1));
-    const float r = __fdividef(1.f, 1.f + e);
-    const float er = e * r;
-    return x1 >= 0.f ? GateVals{er, r} : GateVals{r, er};
+    const float e1 = ex2_sub(-fabsf(x1) * kLog2eF);
+    const float e2 = ex2_sub(fminf(x2, 0.f) * kLog2eF);   // x2 < 0: sigmoid(x2) = e2 / (1 + e2)
+    const float p1 = 1.f + e1, p2 = 1.f + e2;
+    const float R = __fdividef(1.f, p1 * p2);
+    const float r1 = R * p2, r2 = R * p1;
+    const float er1 = e1 * r1, s2 = e2 * r2;
+    Gate q;
+    q.z = x1 >= 0.f ? r1 : er1;
+    q.a = x1 >= 0.f ? er1 : r1;
+    q.g = x2 >= 0.f ? x2 + 0.5f : s2;
+    q.gp = x2 >= 0.f ? 1.f : s2 * r2;
+    return q;
 }
 
-// g(x2) and, for the gradients, g'(x2) = 1 (x2 >= 0) or s (1 - s), s = sigmoid(x2).
-__device__ __forceinline__ float gate_g(float x2, float &gp)
+// 1 - sigmoid(x1) alone (the backward's coefficient a_{t+1}).
+__device__ __forceinline__ float gate_a(float x1)
 {
-    const float e = expf(fminf(x2, 0.f));     // x2 < 0: sigmoid(x2) = e / (1 + e)
-    const float r = __fdividef(1.f, 1.f + e);
-    const float s = e * r;
-    gp = x2 >= 0.f ? 1.f : s * r;
-    return x2 >= 0.f ? x2 + 0.5f : s;
-}
-
-__device__ __forceinline__ float gate_g(float x2)
-{
-    float gp;
-    return gate_g(x2, gp);
+    const float e1 = ex2_sub(-fabsf(x1) * kLog2eF);
+    const float r1 = __fdividef(1.f, 1.f + e1);
+    return x1 >= 0.f ? e1 * r1 : r1;
 }
 
 // ------------------------------------------------------------- forward
 // Element of step t: (a_t, b_t) from (x1_t, x2_t); state (A, h) as in the
-// linear forward.  WA: A is written (otherwise only Bc).
+// linear forward.  WA: A is written (otherwise only Bc).  Pass 1 keeps the
+// elements in shared memory (the engine's stash), so pass 2 neither reads
+// x1, x2 again nor evaluates the gate a second time.  Steps past T load
+// x1 = -inf, x2 = 0, whose gate is exactly the identity element (a = 1,
+// b = 0), so no step needs a bounds select.
 template <typename Tin, int VEC_, int L_, bool WA>
 struct MinFwd {
     static constexpr int NS = 2, VEC = VEC_, L = L_;
     static constexpr bool kReverse = false;
+    static constexpr bool kStash = true;
     using S = St<NS, VEC>;
     struct Args {
         const Tin *x1;
@@ -74,22 +86,25 @@ struct MinFwd {
     struct Regs {
         Raw<Tin, VEC> x1[L];
         Raw<Tin, VEC> x2[L];
-        int nv;   // steps of the round that are < T
     };
 
+    __device__ static int valid_steps(const ChanGeom &g, int64_t t0, bool act)
+    {
+        const int64_t rem = g.T - t0;
+        return act ? int(rem < 0 ? 0 : (rem > L ? L : rem)) : 0;
+    }
     __device__ static void load(const Args &p, const ChanGeom &g, int64_t bb, int64_t t0, int d,
                                 bool act, Regs &r)
     {
-        const int64_t rem = g.T - t0;
-        r.nv = act ? int(rem < 0 ? 0 : (rem > L ? L : rem)) : 0;
+        const int nv = valid_steps(g, t0, act);
 #pragma unroll
         for (int i = 0; i < L; ++i) {
-            if (i < r.nv) {
+            if (i < nv) {
                 const int64_t off = (bb * g.T + t0 + i) * g.D + d;
                 r.x1[i].load(p.x1 + off);
                 r.x2[i].load(p.x2 + off);
             } else {
-                r.x1[i].fill(0.f);
+                r.x1[i].fill(-INFINITY);
                 r.x2[i].fill(0.f);
             }
         }
@@ -99,10 +114,9 @@ struct MinFwd {
         S e;
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
-            const GateVals q = gate_z(r.x1[i][v]);
-            const bool ok = i < r.nv;
-            e.v[0][v] = ok ? q.a : 1.f;                       // past T: the identity
-            e.v[1][v] = ok ? q.z * gate_g(r.x2[i][v]) : 0.f;
+            const Gate q = gate(r.x1[i][v], r.x2[i][v]);
+            e.v[0][v] = q.a;
+            e.v[1][v] = q.z * q.g;
         }
         return e;
     }
@@ -130,33 +144,23 @@ struct MinFwd {
         }
         return o;
     }
-    __device__ static void epilogue(const Args &p, const ChanGeom &g, int64_t bb, int64_t t0,
-                                    int d, bool act, const Regs &r, S &st)
+    __device__ static void epilogue_stash(const Args &p, const ChanGeom &g, int64_t bb, int64_t t0,
+                                          int d, bool act, const StashView<MinFwd> &sv, S &st)
     {
-        float P[VEC], H[VEC];
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            P[v] = st.v[0][v];
-            H[v] = st.v[1][v];
-        }
+        const int nv = valid_steps(g, t0, act);
 #pragma unroll
         for (int i = 0; i < L; ++i) {
-            if (i < r.nv) {
+            if (i < nv) {
+                const S e = sv.get(i);
 #pragma unroll
                 for (int v = 0; v < VEC; ++v) {
-                    const GateVals q = gate_z(r.x1[i][v]);
-                    P[v] = q.a * P[v];
-                    H[v] = fmaf(q.a, H[v], q.z * gate_g(r.x2[i][v]));
+                    st.v[0][v] = e.v[0][v] * st.v[0][v];
+                    st.v[1][v] = fmaf(e.v[0][v], st.v[1][v], e.v[1][v]);
                 }
                 const int64_t off = (bb * g.T + t0 + i) * g.D + d;
-                if constexpr (WA) store_vec<VEC>(p.A + off, P);
-                store_vec<VEC>(p.Bc + off, H);
+                if constexpr (WA) store_vec<VEC>(p.A + off, st.v[0]);
+                store_vec<VEC>(p.Bc + off, st.v[1]);
             }
-        }
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            st.v[0][v] = P[v];
-            st.v[1][v] = H[v];
         }
     }
 };
@@ -200,7 +204,10 @@ struct MinBwd {
             if (i < r.nr) {
                 r.x1[i].load(p.x1 + off);
             } else {
-                r.x1[i].fill(0.f);
+                // row T (the step after the last): x1 = +inf, a = 0, which ends
+                // the adjoint recurrence; later rows: x1 = -inf, a = 1, whose
+                // steps (zero gradients) are the identity
+                r.x1[i].fill(act && t0 + i == g.T ? INFINITY : -INFINITY);
             }
             if (i < L) {
                 if (i < r.nr) {
@@ -216,12 +223,9 @@ struct MinBwd {
             }
         }
     }
-    // coefficient of step t0+i: a_{t+1}, 0 at t = T-1, 1 (identity) past T
-    __device__ static float coef(const Regs &r, int i, int v)
-    {
-        const float c = gate_z(r.x1[i + 1][v]).a;
-        return i + 1 < r.nr ? c : (i < r.nr ? 0.f : 1.f);
-    }
+    // coefficient of step t0+i: a_{t+1} (0 at t = T-1 and 1 past T, from the
+    // padding rows of load)
+    __device__ static float coef(const Regs &r, int i, int v) { return gate_a(r.x1[i + 1][v]); }
     __device__ static S element(const Regs &r, int i)
     {
         S e;
@@ -303,12 +307,10 @@ struct MinBwd {
                     lam[v] = fmaf(c, lam[v], r.gB[i][v]);
                     const float da = GA ? fmaf(mu[v], Ap[GA ? i : 0][v], lam[v] * Bp[i][v])
                                         : lam[v] * Bp[i][v];
-                    const GateVals q = gate_z(r.x1[i][v]);
-                    float gp;
-                    const float gx = gate_g(x2[i][v], gp);
+                    const Gate q = gate(r.x1[i][v], x2[i][v]);
                     const float zz = q.z * q.a;                  // z (1 - z)
-                    o1[v] = fmaf(lam[v], gx, -da) * zz;
-                    o2[v] = lam[v] * q.z * gp;
+                    o1[v] = fmaf(lam[v], q.g, -da) * zz;
+                    o2[v] = lam[v] * q.z * q.gp;
                 }
                 const int64_t off = (bb * g.T + t0 + i) * g.D + d;
                 store_vec<VEC>(p.dx1 + off, o1);
@@ -352,7 +354,7 @@ struct MinBwd {
 #define MG_MGB_MB 3
 #endif
 #ifndef MG_MGB_R
-#define MG_MGB_R 2
+#define MG_MGB_R 4
 #endif
 constexpr int kSTX = 32, kSTY = 8;
 

@@ -9,7 +9,8 @@
 // DC = TX*VEC channels by TC = TY*L*R steps (R rounds of L steps per thread),
 // a shared-memory fold of the TY thread aggregates (which also leaves each
 // row its exclusive prefix within the tile), the decoupled look-back of warp
-// 0, and the hand-off of each thread's start state.  kReverse ops walk time backwards (adjoint scans).
+// 0, and the hand-off of each thread's start state.  kReverse ops walk time
+// backwards (adjoint scans).
 #pragma once
 
 #include "common.cuh"
@@ -28,6 +29,44 @@ struct ChanGeom {
 template <int NS, int VEC>
 struct St {
     float v[NS][VEC];
+};
+
+// An op may ask the engine to keep the elements that pass 1 forms in shared
+// memory (static constexpr bool kStash = true): pass 2 then neither re-reads
+// the op's inputs nor forms the elements again (for ops whose elements cost
+// more to form than to keep).  Its pass 2 is epilogue_stash, which reads the
+// round's elements through a StashView.  Layout: [round][step][state][thread]
+// of VEC floats, so a warp's accesses to one (round, step, state) are one
+// contiguous run of 32 * VEC floats (no bank conflicts).
+template <class Op, class = void>
+struct op_stashes {
+    static constexpr bool value = false;
+};
+template <class Op>
+struct op_stashes<Op, decltype(void(Op::kStash))> {
+    static constexpr bool value = Op::kStash;
+};
+
+template <class Op>
+struct StashView {
+    float *base;   // this thread's slot of step 0, state 0 of the round
+    int nt;        // threads per CTA
+    __device__ __forceinline__ float *at(int i, int q) const
+    {
+        return base + size_t(i * Op::NS + q) * nt * Op::VEC;
+    }
+    __device__ __forceinline__ void put(int i, const typename Op::S &e) const
+    {
+#pragma unroll
+        for (int q = 0; q < Op::NS; ++q) store_vec<Op::VEC>(at(i, q), e.v[q]);
+    }
+    __device__ __forceinline__ typename Op::S get(int i) const
+    {
+        typename Op::S e;
+#pragma unroll
+        for (int q = 0; q < Op::NS; ++q) load_vec<Op::VEC>(at(i, q), e.v[q]);
+        return e;
+    }
 };
 
 // ------------------------------------------------------------ the engine
@@ -132,10 +171,16 @@ __global__ void __launch_bounds__(TX *TY, MINB)
     using S = typename Op::S;
     constexpr int NS = Op::NS, VEC = Op::VEC, L = Op::L;
     constexpr int DC = TX * VEC;
+    constexpr bool STASH = op_stashes<Op>::value;
     extern __shared__ float4 engine_smem[];
-    // s_agg[TY][NS][DC] then s_carry[NS][DC]
+    // s_agg[TY][NS][DC], s_carry[NS][DC], then (stashing ops) the elements
     float *const s_agg = reinterpret_cast<float *>(engine_smem);
     float *const s_carry = s_agg + TY * NS * DC;
+    float *const s_stash = s_carry + NS * DC;
+    auto stash = [&](int k) {
+        return StashView<Op>{s_stash + (size_t(k) * L * NS * (TX * TY) + threadIdx.x) * VEC,
+                             TX * TY};
+    };
 
     unsigned tile;
     unsigned long long epoch;
@@ -166,10 +211,16 @@ __global__ void __launch_bounds__(TX *TY, MINB)
     for (int k = 0; k < R; ++k) {
         typename Op::Regs r;
         Op::load(args, g, bb, round_t0(k), d, act, r);
-        S ragg = Op::element(r, Op::kReverse ? L - 1 : 0);
+        const int i0 = Op::kReverse ? L - 1 : 0;
+        S ragg = Op::element(r, i0);
+        if constexpr (STASH) stash(k).put(i0, ragg);
 #pragma unroll
-        for (int i = 1; i < L; ++i)
-            ragg = Op::combine(ragg, Op::element(r, Op::kReverse ? L - 1 - i : i));
+        for (int i = 1; i < L; ++i) {
+            const int ii = Op::kReverse ? L - 1 - i : i;
+            const S e = Op::element(r, ii);
+            if constexpr (STASH) stash(k).put(ii, e);
+            ragg = Op::combine(ragg, e);
+        }
         agg = (k == 0) ? ragg : Op::combine(agg, ragg);
     }
 #pragma unroll
@@ -228,9 +279,13 @@ __global__ void __launch_bounds__(TX *TY, MINB)
     // epilogue leaves in `st` the state after its round.
 #pragma unroll 1
     for (int k = 0; k < R; ++k) {
-        typename Op::Regs r2;
-        Op::load(args, g, bb, round_t0(k), d, act, r2);
-        Op::epilogue(args, g, bb, round_t0(k), d, act, r2, st);
+        if constexpr (STASH) {
+            Op::epilogue_stash(args, g, bb, round_t0(k), d, act, stash(k), st);
+        } else {
+            typename Op::Regs r2;
+            Op::load(args, g, bb, round_t0(k), d, act, r2);
+            Op::epilogue(args, g, bb, round_t0(k), d, act, r2, st);
+        }
     }
     finish_cta(lb, epoch);
 }
@@ -276,7 +331,11 @@ struct ChanPlan {
                         ws_bytes_given, need);
         const ChanGeom g = geom(B, T, D);
         const Lookback lb = make_lookback(ws, nt, o);
-        constexpr size_t smem = size_t(TY + 1) * Op::NS * DC * sizeof(float);
+        constexpr size_t smem =
+            (size_t(TY + 1) * Op::NS * DC +
+             (op_stashes<Op>::value ? size_t(R) * Op::L * Op::NS * TX * TY * Op::VEC : 0)) *
+            sizeof(float);
+        static_assert(smem <= 227 * 1024, "more shared memory than a CTA may have");
         if (smem > 48 * 1024) {
             static const cudaError_t attr = cudaFuncSetAttribute(
                 channel_scan_kernel<Op, TX, TY, MINB, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
