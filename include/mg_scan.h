@@ -13,6 +13,9 @@
  *   mg_mingru_scan_fwd/bwd, mg_linear_scan_bwd_bf16_grads <- the minGRU layer's
  *                           gate fused into linear_scan_fwd/bwd, and the
  *                           backward with bf16 gradients
+ *   mg_linear_scan_h0_fwd/bwd, mg_linear_scan_varlen_fwd/bwd <- linear_scan_fwd/bwd
+ *                           from start states, over (B,T,D) or packed
+ *                           variable-length sequences
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -153,6 +156,67 @@ mg_status mg_linear_scan_bwd_bf16_grads(const void *a, mg_dtype a_dt,
                                         void *da, void *db,
                                         int64_t B, int64_t T, int64_t D,
                                         void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * linear_scan_fwd from a start state.  The page's linear and affine ops start
+ * from h_0 = 0; its log-space op (section "parallel_scan_log_fwd") takes
+ * log h_0 in slot 0 of log_values.  These give the linear op the same start
+ * state: h0 is (B, D) float32 and, per channel,
+ *   A_t = a_t A_{t-1}  (A_0 = 1),   H_t = a_t H_{t-1} + b_t  (H_0 = h0[b, d])
+ * A and H are (B,T,D) float32 (H = Bc + A h0 of mg_linear_scan_fwd).
+ * Workspace: mg_linear_scan_workspace_size.
+ */
+mg_status mg_linear_scan_h0_fwd(const void *a, const void *b, mg_dtype in_dt, const float *h0,
+                                float *A, float *H,
+                                int64_t B, int64_t T, int64_t D,
+                                void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Gradients of L = sum(gA*A) + sum(gH*H) for mg_linear_scan_h0_fwd (A, H
+ * used as given): da, db as mg_linear_scan_bwd with H_0 = h0 in da_1, and
+ * dh0 = dL/dh0 = a_1 lam_1, (B, D) float32 (zero-filled for T = 0).
+ */
+mg_status mg_linear_scan_h0_bwd(const void *a, mg_dtype a_dt, const float *h0,
+                                const float *A, const float *H,
+                                const float *gA, const float *gH,
+                                float *da, float *db, float *dh0,
+                                int64_t B, int64_t T, int64_t D,
+                                void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * The linear scan over a packed batch of variable-length sequences (the
+ * ragged batch layout that the page on causal_conv1d lists among its
+ * unsupported features, applied to this op).  a, b are (Ttot, D) with
+ * sequence s in rows cu_seqlens[s] .. cu_seqlens[s+1]-1; cu_seqlens is a
+ * DEVICE array of nseq + 1 int64 offsets (8-byte aligned), non-decreasing
+ * from 0 to Ttot (empty sequences allowed).  Each sequence is an independent
+ * linear scan started from h0[s] ((nseq, D) float32; NULL means 0):
+ *   A_r = a_r A_{r-1},  H_r = a_r H_{r-1} + b_r,  (A, H) before the sequence = (1, h0[s])
+ * A, H are (Ttot, D) float32.  A cu_seqlens that breaks the rules above is
+ * detected on the device: the outputs are unspecified and the next
+ * mg_workspace_status returns MG_ERR_INVALID_ARG; no memory outside the
+ * buffers is touched.  Workspace: mg_linear_scan_varlen_workspace_size.
+ */
+size_t mg_linear_scan_varlen_workspace_size(int64_t Ttot, int64_t D);
+
+mg_status mg_linear_scan_varlen_fwd(const void *a, const void *b, mg_dtype in_dt,
+                                    const int64_t *cu_seqlens, int64_t nseq, const float *h0,
+                                    float *A, float *H, int64_t Ttot, int64_t D,
+                                    void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Gradients of L = sum(gA*A) + sum(gH*H) for mg_linear_scan_varlen_fwd (A, H
+ * used as given): per sequence, the adjoint of mg_linear_scan_bwd with
+ * (A, H) before the sequence = (1, h0[s]); dh0[s] = a_first lam_first, and 0
+ * for an empty sequence.  h0 and dh0 are given together or both NULL.
+ */
+mg_status mg_linear_scan_varlen_bwd(const void *a, mg_dtype a_dt,
+                                    const int64_t *cu_seqlens, int64_t nseq, const float *h0,
+                                    const float *A, const float *H,
+                                    const float *gA, const float *gH,
+                                    float *da, float *db, float *dh0,
+                                    int64_t Ttot, int64_t D,
+                                    void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * The minGRU gate fused into linear_scan_fwd.  A minGRU layer feeds the

@@ -20,6 +20,11 @@ Ops (names of the C entry points; aliases with the names of the page
 * ``mg_mingru_scan_fwd(x1, x2) -> (A, Bc)`` and ``mg_mingru_scan_bwd(x1, x2, A, Bc, gA, gBc)
   -> (dx1, dx2)``: the minGRU gate fused into the linear scan (aliases
   ``mingru_scan_fwd``, ``mingru_scan_bwd``)
+* ``mg_linear_scan_h0_fwd(a, b, h0) -> (A, H)``, ``mg_linear_scan_h0_bwd(a, h0, A, H, gA, gH)
+  -> (da, db, dh0)``: the linear scan from start states h0 (B, D)
+* ``mg_linear_scan_varlen_fwd(a, b, cu_seqlens, h0=None) -> (A, H)`` and
+  ``mg_linear_scan_varlen_bwd(a, cu_seqlens, A, H, gA, gH, h0=None) -> (da, db, dh0)``:
+  packed variable-length sequences (Ttot, D) with int64 offsets
 
 Every op accepts optional preallocated outputs (``out=(...)``), a workspace
 tensor (``ws=``, uint8, zero-filled before first use) and a stream
@@ -47,6 +52,8 @@ __all__ = [
     "workspace_status", "new_workspace",
     "mg_linear_scan_bwd_bf16_grads", "mg_mingru_scan_fwd", "mg_mingru_scan_bwd",
     "mingru_workspace_size", "mingru_scan_fwd", "mingru_scan_bwd",
+    "mg_linear_scan_h0_fwd", "mg_linear_scan_h0_bwd", "mg_linear_scan_varlen_fwd",
+    "mg_linear_scan_varlen_bwd", "varlen_workspace_size",
 ]
 
 MG_OK, MG_ERR_INVALID_ARG, MG_ERR_UNSUPPORTED, MG_ERR_LAUNCH, MG_ERR_TIMEOUT = range(5)
@@ -60,6 +67,8 @@ SYMBOLS = (
     "mg_affine_scan_fwd", "mg_affine_scan_bwd",
     "mg_linear_scan_bwd_bf16_grads", "mg_mingru_scan_workspace_size",
     "mg_mingru_scan_fwd", "mg_mingru_scan_bwd",
+    "mg_linear_scan_h0_fwd", "mg_linear_scan_h0_bwd", "mg_linear_scan_varlen_workspace_size",
+    "mg_linear_scan_varlen_fwd", "mg_linear_scan_varlen_bwd",
 )
 
 
@@ -122,6 +131,15 @@ def load():
         lib.mg_mingru_scan_fwd.argtypes = [vp, vp, i32, vp, vp, i64, i64, i64, vp, sz, vp]
         lib.mg_mingru_scan_bwd.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, i32, i64, i64, i64,
                                            vp, sz, vp]
+        lib.mg_linear_scan_h0_fwd.argtypes = [vp, vp, i32, vp, vp, vp, i64, i64, i64, vp, sz, vp]
+        lib.mg_linear_scan_h0_bwd.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64,
+                                              i64, vp, sz, vp]
+        lib.mg_linear_scan_varlen_workspace_size.argtypes = [i64, i64]
+        lib.mg_linear_scan_varlen_workspace_size.restype = sz
+        lib.mg_linear_scan_varlen_fwd.argtypes = [vp, vp, i32, vp, i64, vp, vp, vp, i64, i64, vp,
+                                                  sz, vp]
+        lib.mg_linear_scan_varlen_bwd.argtypes = [vp, i32, vp, i64, vp, vp, vp, vp, vp, vp, vp,
+                                                  vp, i64, i64, vp, sz, vp]
         lib.mg_testing_linear_scan_fwd_stall.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, sz,
                                                          i64, ctypes.c_uint64, vp]
         lib.mg_testing_linear_scan_fwd_stall.restype = st
@@ -134,7 +152,9 @@ def load():
         for name in ("mg_workspace_init", "mg_workspace_status", "mg_linear_scan_fwd",
                      "mg_linear_scan_bwd", "mg_log_scan_fwd", "mg_log_scan_bwd",
                      "mg_affine_scan_fwd", "mg_affine_scan_bwd", "mg_linear_scan_bwd_bf16_grads",
-                     "mg_mingru_scan_fwd", "mg_mingru_scan_bwd"):
+                     "mg_mingru_scan_fwd", "mg_mingru_scan_bwd", "mg_linear_scan_h0_fwd",
+                     "mg_linear_scan_h0_bwd", "mg_linear_scan_varlen_fwd",
+                     "mg_linear_scan_varlen_bwd"):
             getattr(lib, name).restype = st
         _lib = lib
     return _lib
@@ -164,6 +184,10 @@ def affine_workspace_size(B: int, T: int, n: int, k: int, v: int) -> int:
 
 def mingru_workspace_size(B: int, T: int, D: int) -> int:
     return int(load().mg_mingru_scan_workspace_size(B, T, D))
+
+
+def varlen_workspace_size(Ttot: int, D: int) -> int:
+    return int(load().mg_linear_scan_varlen_workspace_size(Ttot, D))
 
 
 def new_workspace(nbytes: int, device) -> torch.Tensor:
@@ -290,6 +314,108 @@ def mg_linear_scan_bwd_bf16_grads(a, A, Bc, gA, gBc, *, out=None, ws=None, strea
                                                 w.data_ptr(), w.numel(), sh),
            "mg_linear_scan_bwd_bf16_grads")
     return da, db
+
+
+def mg_linear_scan_h0_fwd(a, b, h0, *, out=None, ws=None, stream=None):
+    """(A, H) float32 (B,T,D): the linear scan of a, b (float32 or bf16) from
+    the start states h0 (B, D) float32: H_t = a_t H_{t-1} + b_t, H_0 = h0."""
+    a = _prep(a, "a", (torch.float32, torch.bfloat16))
+    b = _prep(b, "b", (a.dtype,))
+    h0 = _prep(h0, "h0")
+    if a.dim() != 3 or b.shape != a.shape or tuple(h0.shape) != (a.shape[0], a.shape[2]):
+        raise ValueError("a, b must be (B, T, D) and h0 (B, D)")
+    B, T, D = a.shape
+    A, H = _out(out, 0, a.shape, a), _out(out, 1, a.shape, a)
+    sh = _stream_handle(stream, a.device)
+    w = _workspace(linear_workspace_size(B, T, D), a.device, sh, ws)
+    _check(load().mg_linear_scan_h0_fwd(a.data_ptr(), b.data_ptr(), _DT[a.dtype], h0.data_ptr(),
+                                        A.data_ptr(), H.data_ptr(), B, T, D, w.data_ptr(),
+                                        w.numel(), sh),
+           "mg_linear_scan_h0_fwd")
+    return A, H
+
+
+def mg_linear_scan_h0_bwd(a, h0, A, H, gA, gH, *, out=None, ws=None, stream=None):
+    """(da, db, dh0): gradients of sum(gA*A) + sum(gH*H) for mg_linear_scan_h0_fwd."""
+    a = _prep(a, "a", (torch.float32, torch.bfloat16))
+    h0, A, H, gA, gH = (_prep(x, n) for x, n in ((h0, "h0"), (A, "A"), (H, "H"), (gA, "gA"),
+                                                  (gH, "gH")))
+    if a.dim() != 3 or any(x.shape != a.shape for x in (A, H, gA, gH)) \
+            or tuple(h0.shape) != (a.shape[0], a.shape[2]):
+        raise ValueError("a, A, H, gA, gH must be (B, T, D) and h0 (B, D)")
+    B, T, D = a.shape
+    da, db = _out(out, 0, a.shape, a), _out(out, 1, a.shape, a)
+    dh0 = _out(out, 2, h0.shape, a)
+    sh = _stream_handle(stream, a.device)
+    w = _workspace(linear_workspace_size(B, T, D), a.device, sh, ws)
+    _check(load().mg_linear_scan_h0_bwd(a.data_ptr(), _DT[a.dtype], h0.data_ptr(), A.data_ptr(),
+                                        H.data_ptr(), gA.data_ptr(), gH.data_ptr(), da.data_ptr(),
+                                        db.data_ptr(), dh0.data_ptr(), B, T, D, w.data_ptr(),
+                                        w.numel(), sh),
+           "mg_linear_scan_h0_bwd")
+    return da, db, dh0
+
+
+def _cu(cu_seqlens, like):
+    if not isinstance(cu_seqlens, torch.Tensor):
+        cu_seqlens = torch.as_tensor(cu_seqlens, dtype=torch.int64)
+    if cu_seqlens.dtype != torch.int64 or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+        raise ValueError("cu_seqlens must be a 1-D int64 tensor of nseq + 1 offsets")
+    return cu_seqlens.to(like.device).contiguous()
+
+
+def mg_linear_scan_varlen_fwd(a, b, cu_seqlens, h0=None, *, out=None, ws=None, stream=None):
+    """(A, H) float32 (Ttot, D) for packed sequences a, b (Ttot, D) with
+    offsets cu_seqlens (nseq + 1, int64), each started from h0[s] ((nseq, D)
+    float32) or 0."""
+    a = _prep(a, "a", (torch.float32, torch.bfloat16))
+    b = _prep(b, "b", (a.dtype,))
+    cu = _cu(cu_seqlens, a)
+    nseq = cu.numel() - 1
+    if a.dim() != 2 or b.shape != a.shape:
+        raise ValueError("a and b must both be (Ttot, D)")
+    if h0 is not None:
+        h0 = _prep(h0, "h0")
+        if tuple(h0.shape) != (nseq, a.shape[1]):
+            raise ValueError("h0 must be (nseq, D)")
+    Ttot, D = a.shape
+    A, H = _out(out, 0, a.shape, a), _out(out, 1, a.shape, a)
+    sh = _stream_handle(stream, a.device)
+    w = _workspace(varlen_workspace_size(Ttot, D), a.device, sh, ws)
+    _check(load().mg_linear_scan_varlen_fwd(a.data_ptr(), b.data_ptr(), _DT[a.dtype],
+                                            cu.data_ptr(), nseq,
+                                            None if h0 is None else h0.data_ptr(), A.data_ptr(),
+                                            H.data_ptr(), Ttot, D, w.data_ptr(), w.numel(), sh),
+           "mg_linear_scan_varlen_fwd")
+    return A, H
+
+
+def mg_linear_scan_varlen_bwd(a, cu_seqlens, A, H, gA, gH, h0=None, *, out=None, ws=None,
+                              stream=None):
+    """(da, db, dh0) for mg_linear_scan_varlen_fwd; dh0 is None without h0."""
+    a = _prep(a, "a", (torch.float32, torch.bfloat16))
+    A, H, gA, gH = (_prep(x, n) for x, n in ((A, "A"), (H, "H"), (gA, "gA"), (gH, "gH")))
+    cu = _cu(cu_seqlens, a)
+    nseq = cu.numel() - 1
+    if a.dim() != 2 or any(x.shape != a.shape for x in (A, H, gA, gH)):
+        raise ValueError("a, A, H, gA, gH must all be (Ttot, D)")
+    Ttot, D = a.shape
+    dh0 = None
+    if h0 is not None:
+        h0 = _prep(h0, "h0")
+        if tuple(h0.shape) != (nseq, D):
+            raise ValueError("h0 must be (nseq, D)")
+        dh0 = _out(out, 2, h0.shape, a)
+    da, db = _out(out, 0, a.shape, a), _out(out, 1, a.shape, a)
+    sh = _stream_handle(stream, a.device)
+    w = _workspace(varlen_workspace_size(Ttot, D), a.device, sh, ws)
+    ptr = lambda x: None if x is None else x.data_ptr()  # noqa: E731
+    _check(load().mg_linear_scan_varlen_bwd(a.data_ptr(), _DT[a.dtype], cu.data_ptr(), nseq,
+                                            ptr(h0), A.data_ptr(), H.data_ptr(), gA.data_ptr(),
+                                            gH.data_ptr(), da.data_ptr(), db.data_ptr(), ptr(dh0),
+                                            Ttot, D, w.data_ptr(), w.numel(), sh),
+           "mg_linear_scan_varlen_bwd")
+    return da, db, dh0
 
 
 def mg_mingru_scan_fwd(x1, x2, *, want_A=True, out=None, ws=None, stream=None):
@@ -456,3 +582,7 @@ affine_scan_fwd = mg_affine_scan_fwd
 affine_scan_bwd = mg_affine_scan_bwd
 mingru_scan_fwd = mg_mingru_scan_fwd
 mingru_scan_bwd = mg_mingru_scan_bwd
+linear_scan_h0_fwd = mg_linear_scan_h0_fwd
+linear_scan_h0_bwd = mg_linear_scan_h0_bwd
+linear_scan_varlen_fwd = mg_linear_scan_varlen_fwd
+linear_scan_varlen_bwd = mg_linear_scan_varlen_bwd

@@ -32,8 +32,10 @@ namespace mg {
 namespace {
 
 // ----------------------------------------------------------- linear forward
-// Element of step t: (a_t, b_t).  State: (running product, h).
-template <typename Tin, int VEC_, int L_>
+// Element of step t: (a_t, b_t).  State: (running product, h).  H0: the
+// recurrence starts from h0[b, d] (a (B, D) float32 array) instead of 0; the
+// state before step 1 is then (1, h0), and the second output is H_t.
+template <typename Tin, int VEC_, int L_, bool H0 = false>
 struct LinFwd {
     static constexpr int NS = 2, VEC = VEC_, L = L_;
     static constexpr bool kReverse = false;
@@ -43,6 +45,7 @@ struct LinFwd {
         const Tin *b;
         float *A;
         float *Bc;
+        const float *h0;   // read only when H0
     };
     struct Regs {
         Raw<Tin, VEC> a[L];
@@ -85,9 +88,13 @@ struct LinFwd {
         }
         return e;
     }
-    __device__ static S initial(const Args &, const ChanGeom &, int64_t, int, bool)
+    __device__ static S initial(const Args &p, const ChanGeom &g, int64_t bb, int d, bool act)
     {
-        return identity();
+        S e = identity();
+        if constexpr (H0) {
+            if (act) load_vec<VEC>(p.h0 + bb * g.D + d, e.v[1]);
+        }
+        return e;
     }
     __device__ static S combine(const S &x, const S &y)
     {
@@ -134,7 +141,9 @@ struct LinFwd {
 // Reverse time.  Element of step t: (c_t = a_{t+1}, gA_t, gBc_t) with
 // c_{T} = 0; state (C, mu, lam): mu_t = gA_t + c_t mu_{t+1}, same for lam.
 // The gradients are stored as Tout (float32, or bf16 rounded to nearest).
-template <typename Tin, int VEC_, int L_, typename Tout = float>
+// H0: the forward started from h0[b, d] (so H_0 = h0 in da_1), and
+// dh0 = a_1 lam_1 is written to dh0[b, d] (both (B, D) float32).
+template <typename Tin, int VEC_, int L_, typename Tout = float, bool H0 = false>
 struct LinBwd {
     static constexpr int NS = 3, VEC = VEC_, L = L_;
     static constexpr bool kReverse = true;
@@ -147,6 +156,8 @@ struct LinBwd {
         const float *gBc;
         Tout *da;
         Tout *db;
+        const float *h0;   // read only when H0
+        float *dh0;        // written only when H0
     };
     struct Regs {
         Raw<Tin, VEC> c[L];
@@ -234,6 +245,9 @@ struct LinBwd {
                     Ap[i][v] = 1.f;
                     Bp[i][v] = 0.f;
                 }
+                if constexpr (H0) {
+                    if (act && t == 0) load_vec<VEC>(p.h0 + bb * g.D + d, Bp[i]);
+                }
             }
         }
         float mu[VEC], lam[VEC];
@@ -256,6 +270,16 @@ struct LinBwd {
                 const int64_t off = (bb * g.T + t) * g.D + d;
                 store_vec<VEC>(p.da + off, da);
                 store_vec<VEC>(p.db + off, lam);
+                if constexpr (H0) {
+                    if (t == 0) {  // dh0 = a_1 lam_1
+                        Raw<Tin, VEC> a0;
+                        a0.load(p.a + off);
+                        float dh[VEC];
+#pragma unroll
+                        for (int v = 0; v < VEC; ++v) dh[v] = a0[v] * lam[v];
+                        store_vec<VEC>(p.dh0 + bb * g.D + d, dh);
+                    }
+                }
             }
         }
         // (the running coefficient product is not needed past the outputs)
@@ -611,6 +635,14 @@ using LinBwdF32 = ChanPlan<LinBwd<float, 4, MG_LINB_L>, MG_LINB_TX, MG_LINB_TY, 
 using LinBwdF32s = ChanPlan<LinBwd<float, 1, 4>, kTX, kTY>;
 using LinBwdB16 = ChanPlan<LinBwd<bf16_t, 4, MG_LINB16_L>, MG_LINB16_TX, MG_LINB16_TY, MG_LINB16_MB, MG_LINB16_R>;
 using LinBwdB16s = ChanPlan<LinBwd<bf16_t, 1, 4>, kTX, kTY>;
+using LinFwdF32h = ChanPlan<LinFwd<float, 4, MG_LINF_L, true>, MG_LINF_TX, MG_LINF_TY, MG_LINF_MB, MG_LINF_R>;
+using LinFwdF32hs = ChanPlan<LinFwd<float, 1, 8, true>, kTX, kTY>;
+using LinFwdB16h = ChanPlan<LinFwd<bf16_t, MG_LINF16_VEC, MG_LINF16_L, true>, MG_LINF16_TX, MG_LINF16_TY, MG_LINF16_MB, MG_LINF16_R>;
+using LinFwdB16hs = ChanPlan<LinFwd<bf16_t, 1, 8, true>, kTX, kTY>;
+using LinBwdF32h = ChanPlan<LinBwd<float, 4, MG_LINB_L, float, true>, MG_LINB_TX, MG_LINB_TY, MG_LINB_MB, MG_LINB_R>;
+using LinBwdF32hs = ChanPlan<LinBwd<float, 1, 4, float, true>, kTX, kTY>;
+using LinBwdB16h = ChanPlan<LinBwd<bf16_t, 4, MG_LINB16_L, float, true>, MG_LINB16_TX, MG_LINB16_TY, MG_LINB16_MB, MG_LINB16_R>;
+using LinBwdB16hs = ChanPlan<LinBwd<bf16_t, 1, 4, float, true>, kTX, kTY>;
 using LinBwdB16G = ChanPlan<LinBwd<bf16_t, 4, MG_LINB16_L, bf16_t>, MG_LINB16_TX, MG_LINB16_TY, MG_LINB16_MB, MG_LINB16_R>;
 using LinBwdB16Gs = ChanPlan<LinBwd<bf16_t, 1, 4, bf16_t>, kTX, kTY>;
 using LinBwdF32G = ChanPlan<LinBwd<float, 4, MG_LINB_L, bf16_t>, MG_LINB_TX, MG_LINB_TY, MG_LINB_MB, MG_LINB_R>;
@@ -634,6 +666,19 @@ size_t linear_bwd_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D)
     return D % 4 == 0 ? LinBwdB16::ws_bytes(B, T, D) : LinBwdB16s::ws_bytes(B, T, D);
 }
 
+size_t linear_h0_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D)
+{
+    size_t f, b;
+    if (dt == MG_F32) {
+        f = D % 4 == 0 ? LinFwdF32h::ws_bytes(B, T, D) : LinFwdF32hs::ws_bytes(B, T, D);
+        b = D % 4 == 0 ? LinBwdF32h::ws_bytes(B, T, D) : LinBwdF32hs::ws_bytes(B, T, D);
+    } else {
+        f = D % MG_LINF16_VEC == 0 ? LinFwdB16h::ws_bytes(B, T, D) : LinFwdB16hs::ws_bytes(B, T, D);
+        b = D % 4 == 0 ? LinBwdB16h::ws_bytes(B, T, D) : LinBwdB16hs::ws_bytes(B, T, D);
+    }
+    return f > b ? f : b;
+}
+
 size_t linear_bwd16_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D)
 {
     if (dt == MG_F32) return D % 4 == 0 ? LinBwdF32G::ws_bytes(B, T, D) : LinBwdF32Gs::ws_bytes(B, T, D);
@@ -646,9 +691,11 @@ size_t linear_ws_bytes(int64_t B, int64_t T, int64_t D)
     for (mg_dtype dt : {MG_F32, MG_BF16}) {
         const size_t f = linear_fwd_ws_bytes(dt, B, T, D), b = linear_bwd_ws_bytes(dt, B, T, D);
         const size_t b16 = linear_bwd16_ws_bytes(dt, B, T, D);
+        const size_t h = linear_h0_ws_bytes(dt, B, T, D);
         m = f > m ? f : m;
         m = b > m ? b : m;
         m = b16 > m ? b16 : m;
+        m = h > m ? h : m;
     }
     return m;
 }
@@ -692,6 +739,40 @@ mg_status launch_linear_bwd(const void *a, mg_dtype dt, const float *A, const fl
     if (D % 4 == 0)
         return LinBwdB16::launch({H(a), A, Bc, gA, gBc, da, db}, B, T, D, ws, wsb, s, o, nm);
     return LinBwdB16s::launch({H(a), A, Bc, gA, gBc, da, db}, B, T, D, ws, wsb, s, o, nm);
+}
+
+mg_status launch_linear_h0_fwd(const void *a, const void *b, mg_dtype dt, const float *h0,
+                               float *A, float *H, int64_t B, int64_t T, int64_t D, void *ws,
+                               size_t wsb, cudaStream_t s, const LaunchOpts &o)
+{
+    const char *nm = "mg_linear_scan_h0_fwd";
+    if (dt == MG_F32) {
+        using F = const float *;
+        if (D % 4 == 0) return LinFwdF32h::launch({F(a), F(b), A, H, h0}, B, T, D, ws, wsb, s, o, nm);
+        return LinFwdF32hs::launch({F(a), F(b), A, H, h0}, B, T, D, ws, wsb, s, o, nm);
+    }
+    using P = const bf16_t *;
+    if (D % MG_LINF16_VEC == 0)
+        return LinFwdB16h::launch({P(a), P(b), A, H, h0}, B, T, D, ws, wsb, s, o, nm);
+    return LinFwdB16hs::launch({P(a), P(b), A, H, h0}, B, T, D, ws, wsb, s, o, nm);
+}
+
+mg_status launch_linear_h0_bwd(const void *a, mg_dtype dt, const float *h0, const float *A,
+                               const float *H, const float *gA, const float *gH, float *da,
+                               float *db, float *dh0, int64_t B, int64_t T, int64_t D, void *ws,
+                               size_t wsb, cudaStream_t s, const LaunchOpts &o)
+{
+    const char *nm = "mg_linear_scan_h0_bwd";
+    if (dt == MG_F32) {
+        using F = const float *;
+        if (D % 4 == 0)
+            return LinBwdF32h::launch({F(a), A, H, gA, gH, da, db, h0, dh0}, B, T, D, ws, wsb, s, o, nm);
+        return LinBwdF32hs::launch({F(a), A, H, gA, gH, da, db, h0, dh0}, B, T, D, ws, wsb, s, o, nm);
+    }
+    using P = const bf16_t *;
+    if (D % 4 == 0)
+        return LinBwdB16h::launch({P(a), A, H, gA, gH, da, db, h0, dh0}, B, T, D, ws, wsb, s, o, nm);
+    return LinBwdB16hs::launch({P(a), A, H, gA, gH, da, db, h0, dh0}, B, T, D, ws, wsb, s, o, nm);
 }
 
 mg_status launch_linear_bwd_bf16_grads(const void *a, mg_dtype dt, const float *A, const float *Bc,

@@ -68,6 +68,24 @@ mg_status launch_linear_bwd(const void *a, mg_dtype dt, const float *A, const fl
                             int64_t B, int64_t T, int64_t D, void *ws, size_t ws_bytes,
                             cudaStream_t s, const LaunchOpts &o);
 size_t linear_bwd16_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D);
+size_t linear_h0_ws_bytes(mg_dtype dt, int64_t B, int64_t T, int64_t D);
+size_t varlen_ws_bytes(int64_t Ttot, int64_t D);
+mg_status launch_varlen_fwd(const void *a, const void *b, mg_dtype dt, const int64_t *cu,
+                            int64_t nseq, const float *h0, float *A, float *H, int64_t Ttot,
+                            int64_t D, void *ws, size_t ws_bytes, cudaStream_t s,
+                            const LaunchOpts &o);
+mg_status launch_varlen_bwd(const void *a, mg_dtype dt, const int64_t *cu, int64_t nseq,
+                            const float *h0, const float *A, const float *H, const float *gA,
+                            const float *gH, float *da, float *db, float *dh0, int64_t Ttot,
+                            int64_t D, void *ws, size_t ws_bytes, cudaStream_t s,
+                            const LaunchOpts &o);
+mg_status launch_linear_h0_fwd(const void *a, const void *b, mg_dtype dt, const float *h0,
+                               float *A, float *H, int64_t B, int64_t T, int64_t D, void *ws,
+                               size_t ws_bytes, cudaStream_t s, const LaunchOpts &o);
+mg_status launch_linear_h0_bwd(const void *a, mg_dtype dt, const float *h0, const float *A,
+                               const float *H, const float *gA, const float *gH, float *da,
+                               float *db, float *dh0, int64_t B, int64_t T, int64_t D, void *ws,
+                               size_t ws_bytes, cudaStream_t s, const LaunchOpts &o);
 mg_status launch_linear_bwd_bf16_grads(const void *a, mg_dtype dt, const float *A, const float *Bc,
                                        const float *gA, const float *gBc, bf16_t *da,
                                        bf16_t *db, int64_t B, int64_t T, int64_t D,

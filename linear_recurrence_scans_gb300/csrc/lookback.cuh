@@ -43,7 +43,7 @@
 namespace mg {
 
 enum : unsigned { kStatusNone = 0, kStatusAggregate = 1, kStatusPrefix = 2 };
-enum : unsigned { kErrLookbackTimeout = 1u, kErrBadTicket = 2u };
+enum : unsigned { kErrLookbackTimeout = 1u, kErrBadTicket = 2u, kErrBadSeqlens = 4u };
 
 struct Control {
     unsigned int ticket;       // next tile ticket of the running launch

@@ -151,6 +151,10 @@ mg_status read_status(const char *fn, void *ws, cudaStream_t stream)
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess)
         return fail(MG_ERR_LAUNCH, "%s: %s", fn, cudaGetErrorString(e));
+    if (words[0] & kErrBadSeqlens)
+        return fail(MG_ERR_INVALID_ARG,
+                    "cu_seqlens was not non-decreasing from 0 to the packed length; the outputs "
+                    "of that launch are unspecified");
     if (words[0] & kErrBadTicket)
         return fail(MG_ERR_INVALID_ARG,
                     "the workspace was not zero-filled before its first use (or is shared by "
@@ -299,6 +303,147 @@ mg_status mg_linear_scan_bwd_bf16_grads(const void *a, mg_dtype a_dt, const floa
     return launch_linear_bwd_bf16_grads(a, a_dt, A, Bc, gA, gBc, static_cast<bf16_t *>(da),
                                         static_cast<bf16_t *>(db), B, T, D, ws, ws_bytes, stream,
                                         default_opts());
+}
+
+mg_status mg_linear_scan_h0_fwd(const void *a, const void *b, mg_dtype in_dt, const float *h0,
+                                float *A, float *H, int64_t B, int64_t T, int64_t D, void *ws,
+                                size_t ws_bytes, cudaStream_t stream)
+{
+    const char *fn = "mg_linear_scan_h0_fwd";
+    g_detail[0] = 0;
+    if (in_dt != MG_F32 && in_dt != MG_BF16)
+        return fail(MG_ERR_UNSUPPORTED, "%s: input dtype %d not supported", fn, int(in_dt));
+    MG_TRY(check_dims(fn, {B, T, D}));
+    MG_TRY(check_channels(fn, D));
+    if (B == 0 || T == 0 || D == 0) return MG_OK;
+    const size_t n = size_t(B) * T * D, isz = in_dt == MG_F32 ? 4 : 2;
+    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D)));
+    MG_TRY(check_bufs(fn, {{a, n * isz, "a", false},
+                           {b, n * isz, "b", false},
+                           {h0, size_t(B) * D * 4, "h0", false},
+                           {A, n * 4, "A", true},
+                           {H, n * 4, "H", true},
+                           {ws, ws_bytes, "workspace", true}}));
+    return launch_linear_h0_fwd(a, b, in_dt, h0, A, H, B, T, D, ws, ws_bytes, stream, default_opts());
+}
+
+mg_status mg_linear_scan_h0_bwd(const void *a, mg_dtype a_dt, const float *h0, const float *A,
+                                const float *H, const float *gA, const float *gH, float *da,
+                                float *db, float *dh0, int64_t B, int64_t T, int64_t D, void *ws,
+                                size_t ws_bytes, cudaStream_t stream)
+{
+    const char *fn = "mg_linear_scan_h0_bwd";
+    g_detail[0] = 0;
+    if (a_dt != MG_F32 && a_dt != MG_BF16)
+        return fail(MG_ERR_UNSUPPORTED, "%s: input dtype %d not supported", fn, int(a_dt));
+    MG_TRY(check_dims(fn, {B, T, D}));
+    MG_TRY(check_channels(fn, D));
+    if (B == 0 || D == 0) return MG_OK;
+    const size_t n = size_t(B) * T * D, isz = a_dt == MG_F32 ? 4 : 2, nh = size_t(B) * D;
+    if (T == 0) {  // L does not depend on h0: its gradient is zero
+        MG_TRY(check_bufs(fn, {{dh0, nh * 4, "dh0", true}}));
+        const cudaError_t e = cudaMemsetAsync(dh0, 0, nh * 4, stream);
+        return e == cudaSuccess ? MG_OK : fail(MG_ERR_LAUNCH, "%s: %s", fn, cudaGetErrorString(e));
+    }
+    MG_TRY(check_ws(fn, ws, ws_bytes, linear_ws_bytes(B, T, D)));
+    MG_TRY(check_bufs(fn, {{a, n * isz, "a", false},
+                           {h0, nh * 4, "h0", false},
+                           {A, n * 4, "A", false},
+                           {H, n * 4, "H", false},
+                           {gA, n * 4, "gA", false},
+                           {gH, n * 4, "gH", false},
+                           {da, n * 4, "da", true},
+                           {db, n * 4, "db", true},
+                           {dh0, nh * 4, "dh0", true},
+                           {ws, ws_bytes, "workspace", true}}));
+    return launch_linear_h0_bwd(a, a_dt, h0, A, H, gA, gH, da, db, dh0, B, T, D, ws, ws_bytes,
+                                stream, default_opts());
+}
+
+size_t mg_linear_scan_varlen_workspace_size(int64_t Ttot, int64_t D)
+{
+    if (Ttot < 0 || D < 0) return 0;
+    if (Ttot == 0 || D == 0) return kControlBytes;
+    return varlen_ws_bytes(Ttot, D);
+}
+
+// cu_seqlens: nseq + 1 int64 offsets, 8-byte aligned; nseq >= 1 when Ttot > 0.
+static mg_status check_varlen(const char *fn, const int64_t *cu, int64_t nseq, int64_t Ttot)
+{
+    if (nseq < 0) return fail(MG_ERR_INVALID_ARG, "%s: negative nseq", fn);
+    if (nseq > (int64_t(1) << 31) - 2) return fail(MG_ERR_UNSUPPORTED, "%s: nseq too large", fn);
+    if (Ttot > 0 && nseq == 0)
+        return fail(MG_ERR_INVALID_ARG, "%s: %lld packed rows but no sequences", fn, (long long)Ttot);
+    if (cu == nullptr) return fail(MG_ERR_INVALID_ARG, "%s: cu_seqlens is NULL", fn);
+    if (reinterpret_cast<uintptr_t>(cu) % 8 != 0)
+        return fail(MG_ERR_INVALID_ARG, "%s: cu_seqlens is not 8-byte aligned", fn);
+    return MG_OK;
+}
+
+mg_status mg_linear_scan_varlen_fwd(const void *a, const void *b, mg_dtype in_dt,
+                                    const int64_t *cu_seqlens, int64_t nseq, const float *h0,
+                                    float *A, float *H, int64_t Ttot, int64_t D, void *ws,
+                                    size_t ws_bytes, cudaStream_t stream)
+{
+    const char *fn = "mg_linear_scan_varlen_fwd";
+    g_detail[0] = 0;
+    if (in_dt != MG_F32 && in_dt != MG_BF16)
+        return fail(MG_ERR_UNSUPPORTED, "%s: input dtype %d not supported", fn, int(in_dt));
+    if (nseq < 0) return fail(MG_ERR_INVALID_ARG, "%s: negative nseq", fn);
+    MG_TRY(check_dims(fn, {Ttot, D}));
+    MG_TRY(check_channels(fn, D));
+    if (Ttot == 0 || D == 0) return MG_OK;
+    MG_TRY(check_varlen(fn, cu_seqlens, nseq, Ttot));
+    const size_t n = size_t(Ttot) * D, isz = in_dt == MG_F32 ? 4 : 2;
+    MG_TRY(check_ws(fn, ws, ws_bytes, varlen_ws_bytes(Ttot, D)));
+    MG_TRY(check_bufs(fn, {{a, n * isz, "a", false},
+                           {b, n * isz, "b", false},
+                           {h0, size_t(nseq) * D * 4, "h0", false, true},
+                           {A, n * 4, "A", true},
+                           {H, n * 4, "H", true},
+                           {ws, ws_bytes, "workspace", true}}));
+    return launch_varlen_fwd(a, b, in_dt, cu_seqlens, nseq, h0, A, H, Ttot, D, ws, ws_bytes,
+                             stream, default_opts());
+}
+
+mg_status mg_linear_scan_varlen_bwd(const void *a, mg_dtype a_dt, const int64_t *cu_seqlens,
+                                    int64_t nseq, const float *h0, const float *A, const float *H,
+                                    const float *gA, const float *gH, float *da, float *db,
+                                    float *dh0, int64_t Ttot, int64_t D, void *ws,
+                                    size_t ws_bytes, cudaStream_t stream)
+{
+    const char *fn = "mg_linear_scan_varlen_bwd";
+    g_detail[0] = 0;
+    if (a_dt != MG_F32 && a_dt != MG_BF16)
+        return fail(MG_ERR_UNSUPPORTED, "%s: input dtype %d not supported", fn, int(a_dt));
+    if (nseq < 0) return fail(MG_ERR_INVALID_ARG, "%s: negative nseq", fn);
+    MG_TRY(check_dims(fn, {Ttot, D}));
+    MG_TRY(check_channels(fn, D));
+    if ((h0 == nullptr) != (dh0 == nullptr))
+        return fail(MG_ERR_INVALID_ARG, "%s: h0 and dh0 must be given together (or both NULL)", fn);
+    if (D == 0) return MG_OK;
+    const size_t nh = size_t(nseq) * D;
+    if (dh0 != nullptr && nh > 0) {   // empty sequences keep dh0 = 0
+        MG_TRY(check_bufs(fn, {{dh0, nh * 4, "dh0", true}}));
+        const cudaError_t e = cudaMemsetAsync(dh0, 0, nh * 4, stream);
+        if (e != cudaSuccess) return fail(MG_ERR_LAUNCH, "%s: %s", fn, cudaGetErrorString(e));
+    }
+    if (Ttot == 0) return MG_OK;
+    MG_TRY(check_varlen(fn, cu_seqlens, nseq, Ttot));
+    const size_t n = size_t(Ttot) * D, isz = a_dt == MG_F32 ? 4 : 2;
+    MG_TRY(check_ws(fn, ws, ws_bytes, varlen_ws_bytes(Ttot, D)));
+    MG_TRY(check_bufs(fn, {{a, n * isz, "a", false},
+                           {h0, nh * 4, "h0", false, true},
+                           {A, n * 4, "A", false},
+                           {H, n * 4, "H", false},
+                           {gA, n * 4, "gA", false},
+                           {gH, n * 4, "gH", false},
+                           {da, n * 4, "da", true},
+                           {db, n * 4, "db", true},
+                           {dh0, nh * 4, "dh0", true, true},
+                           {ws, ws_bytes, "workspace", true}}));
+    return launch_varlen_bwd(a, a_dt, cu_seqlens, nseq, h0, A, H, gA, gH, da, db, dh0, Ttot, D, ws,
+                             ws_bytes, stream, default_opts());
 }
 
 size_t mg_mingru_scan_workspace_size(int64_t B, int64_t T, int64_t D)
