@@ -16,6 +16,7 @@
  *   mg_linear_scan_h0_fwd/bwd, mg_linear_scan_varlen_fwd/bwd <- linear_scan_fwd/bwd
  *                           from start states, over (B,T,D) or packed
  *                           variable-length sequences
+ *   mg_affine_scan_h0_fwd/bwd <- affine_scan_fwd/bwd from start states
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -314,6 +315,30 @@ mg_status mg_affine_scan_bwd(const float *A, const float *Abar, const float *Bba
                              float *dA, float *dB,
                              int64_t B, int64_t T, int64_t n, int k, int v,
                              void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * affine_scan_fwd (page section "affine_scan_fwd") from a start state: H0 is
+ * (B, n, k, v) float32 and, per (b, n),
+ *   Abar_t = A_t @ Abar_{t-1}  (Abar_0 = I),   Bbar_t = A_t @ Bbar_{t-1} + B_t  (Bbar_0 = H0[b, n])
+ * (Bbar = Bbar(H0 = 0) + Abar H0).  Workspace: mg_affine_scan_workspace_size.
+ */
+mg_status mg_affine_scan_h0_fwd(const float *A, const float *Bm, const float *H0,
+                                float *Abar, float *Bbar,
+                                int64_t B, int64_t T, int64_t n, int k, int v,
+                                void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Gradients of L = <gAbar, Abar> + <gBbar, Bbar> for mg_affine_scan_h0_fwd
+ * (Abar, Bbar used as given): dA, dB as mg_affine_scan_bwd with Bbar_0 = H0
+ * in dA_1, and dH0 = A_1^T Lam_1 ((B, n, k, v) float32; zero-filled for
+ * T = 0).  Runs the backward and then one small kernel for the first step.
+ */
+mg_status mg_affine_scan_h0_bwd(const float *A, const float *H0,
+                                const float *Abar, const float *Bbar,
+                                const float *gAbar, const float *gBbar,
+                                float *dA, float *dB, float *dH0,
+                                int64_t B, int64_t T, int64_t n, int k, int v,
+                                void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * mg_linear_scan_fwd without a workspace argument (the page has no

@@ -25,6 +25,8 @@ Ops (names of the C entry points; aliases with the names of the page
 * ``mg_linear_scan_varlen_fwd(a, b, cu_seqlens, h0=None) -> (A, H)`` and
   ``mg_linear_scan_varlen_bwd(a, cu_seqlens, A, H, gA, gH, h0=None) -> (da, db, dh0)``:
   packed variable-length sequences (Ttot, D) with int64 offsets
+* ``mg_affine_scan_h0_fwd(A, Bm, H0) -> (Abar, Bbar)``, ``mg_affine_scan_h0_bwd(A, H0, Abar,
+  Bbar, gAbar, gBbar) -> (dA, dB, dH0)``: the affine scan from start states H0 (B, n, k, v)
 
 Every op accepts optional preallocated outputs (``out=(...)``), a workspace
 tensor (``ws=``, uint8, zero-filled before first use) and a stream
@@ -54,6 +56,7 @@ __all__ = [
     "mingru_workspace_size", "mingru_scan_fwd", "mingru_scan_bwd",
     "mg_linear_scan_h0_fwd", "mg_linear_scan_h0_bwd", "mg_linear_scan_varlen_fwd",
     "mg_linear_scan_varlen_bwd", "varlen_workspace_size",
+    "mg_affine_scan_h0_fwd", "mg_affine_scan_h0_bwd",
 ]
 
 MG_OK, MG_ERR_INVALID_ARG, MG_ERR_UNSUPPORTED, MG_ERR_LAUNCH, MG_ERR_TIMEOUT = range(5)
@@ -69,6 +72,7 @@ SYMBOLS = (
     "mg_mingru_scan_fwd", "mg_mingru_scan_bwd",
     "mg_linear_scan_h0_fwd", "mg_linear_scan_h0_bwd", "mg_linear_scan_varlen_workspace_size",
     "mg_linear_scan_varlen_fwd", "mg_linear_scan_varlen_bwd",
+    "mg_affine_scan_h0_fwd", "mg_affine_scan_h0_bwd",
 )
 
 
@@ -140,6 +144,10 @@ def load():
                                                   sz, vp]
         lib.mg_linear_scan_varlen_bwd.argtypes = [vp, i32, vp, i64, vp, vp, vp, vp, vp, vp, vp,
                                                   vp, i64, i64, vp, sz, vp]
+        lib.mg_affine_scan_h0_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, vp, sz,
+                                              vp]
+        lib.mg_affine_scan_h0_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64,
+                                              i32, i32, vp, sz, vp]
         lib.mg_testing_linear_scan_fwd_stall.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, sz,
                                                          i64, ctypes.c_uint64, vp]
         lib.mg_testing_linear_scan_fwd_stall.restype = st
@@ -154,7 +162,8 @@ def load():
                      "mg_affine_scan_fwd", "mg_affine_scan_bwd", "mg_linear_scan_bwd_bf16_grads",
                      "mg_mingru_scan_fwd", "mg_mingru_scan_bwd", "mg_linear_scan_h0_fwd",
                      "mg_linear_scan_h0_bwd", "mg_linear_scan_varlen_fwd",
-                     "mg_linear_scan_varlen_bwd"):
+                     "mg_linear_scan_varlen_bwd", "mg_affine_scan_h0_fwd",
+                     "mg_affine_scan_h0_bwd"):
             getattr(lib, name).restype = st
         _lib = lib
     return _lib
@@ -546,6 +555,48 @@ def mg_affine_scan_bwd(A, Abar, Bbar, gAbar, gBbar, *, out=None, ws=None, stream
     return dA, dB
 
 
+def mg_affine_scan_h0_fwd(A, Bm, H0, *, out=None, ws=None, stream=None):
+    """(Abar, Bbar) for A (B,T,n,k,k), Bm (B,T,n,k,v) started from H0 (B,n,k,v)."""
+    A, Bm, H0 = _prep(A, "A"), _prep(Bm, "Bm"), _prep(H0, "H0")
+    if A.dim() != 5 or A.shape[3] != A.shape[4] or Bm.dim() != 5 or Bm.shape[:4] != A.shape[:4]:
+        raise ValueError("A must be (B,T,n,k,k) and Bm (B,T,n,k,v)")
+    B, T, n, k, _ = A.shape
+    v = Bm.shape[4]
+    if tuple(H0.shape) != (B, n, k, v):
+        raise ValueError("H0 must be (B, n, k, v)")
+    Abar, Bbar = _out(out, 0, A.shape, A), _out(out, 1, Bm.shape, A)
+    sh = _stream_handle(stream, A.device)
+    w = _workspace(affine_workspace_size(B, T, n, k, v), A.device, sh, ws)
+    _check(load().mg_affine_scan_h0_fwd(A.data_ptr(), Bm.data_ptr(), H0.data_ptr(),
+                                        Abar.data_ptr(), Bbar.data_ptr(), B, T, n, k, v,
+                                        w.data_ptr(), w.numel(), sh),
+           "mg_affine_scan_h0_fwd")
+    return Abar, Bbar
+
+
+def mg_affine_scan_h0_bwd(A, H0, Abar, Bbar, gAbar, gBbar, *, out=None, ws=None, stream=None):
+    """(dA, dB, dH0): gradients of <gAbar, Abar> + <gBbar, Bbar> for mg_affine_scan_h0_fwd."""
+    A, H0, Abar, Bbar, gAbar, gBbar = (_prep(x, nm) for x, nm in (
+        (A, "A"), (H0, "H0"), (Abar, "Abar"), (Bbar, "Bbar"), (gAbar, "gAbar"), (gBbar, "gBbar")))
+    if A.dim() != 5 or Abar.shape != A.shape or gAbar.shape != A.shape \
+            or Bbar.dim() != 5 or gBbar.shape != Bbar.shape or Bbar.shape[:4] != A.shape[:4]:
+        raise ValueError("A, Abar, gAbar must be (B,T,n,k,k) and Bbar, gBbar (B,T,n,k,v)")
+    B, T, n, k, _ = A.shape
+    v = Bbar.shape[4]
+    if tuple(H0.shape) != (B, n, k, v):
+        raise ValueError("H0 must be (B, n, k, v)")
+    dA, dB = _out(out, 0, A.shape, A), _out(out, 1, Bbar.shape, A)
+    dH0 = _out(out, 2, H0.shape, A)
+    sh = _stream_handle(stream, A.device)
+    w = _workspace(affine_workspace_size(B, T, n, k, v), A.device, sh, ws)
+    _check(load().mg_affine_scan_h0_bwd(A.data_ptr(), H0.data_ptr(), Abar.data_ptr(),
+                                        Bbar.data_ptr(), gAbar.data_ptr(), gBbar.data_ptr(),
+                                        dA.data_ptr(), dB.data_ptr(), dH0.data_ptr(), B, T, n, k,
+                                        v, w.data_ptr(), w.numel(), sh),
+           "mg_affine_scan_h0_bwd")
+    return dA, dB, dH0
+
+
 def mg_linear_scan_fwd_noalloc(a, b, *, out=None, stream=None):
     """mg_linear_scan_fwd with the library's static scratch instead of a
     workspace: the C entry point allocates nothing (for callers that cannot
@@ -586,3 +637,5 @@ linear_scan_h0_fwd = mg_linear_scan_h0_fwd
 linear_scan_h0_bwd = mg_linear_scan_h0_bwd
 linear_scan_varlen_fwd = mg_linear_scan_varlen_fwd
 linear_scan_varlen_bwd = mg_linear_scan_varlen_bwd
+affine_scan_h0_fwd = mg_affine_scan_h0_fwd
+affine_scan_h0_bwd = mg_affine_scan_h0_bwd

@@ -120,6 +120,7 @@ struct AffFwdSmall {
         const float *Bm;
         float *Abar;
         float *Bbar;
+        const float *H0;  // (B, n, k, v) start states, or NULL (Bbar_0 = 0)
     };
     struct Regs {
         const float *A;
@@ -159,9 +160,12 @@ struct AffFwdSmall {
         ld_floats<KW>(r.Bm + s * KW, f(e) + KK);
         return e;
     }
-    __device__ static S initial(const Args &, const ChanGeom &, int64_t, int, bool)
+    // State before step 1: (I, H0 of the sequence), or the identity.
+    __device__ static S initial(const Args &p, const ChanGeom &g, int64_t bb, int d, bool act)
     {
-        return identity();
+        S e = identity();
+        if (p.H0 != nullptr && act) ld_floats<KW>(p.H0 + (bb * g.D + d) * KW, f(e) + KK);
+        return e;
     }
     __device__ static S combine(const S &x, const S &y)
     {
@@ -733,6 +737,7 @@ struct AffGeom {
 
 struct AffPtrs {
     const float *A, *Bm;                            // forward inputs
+    const float *H0;                                // forward start states (B, n, k, v) or NULL
     float *Abar_out, *Bbar_out;                     // forward outputs
     const float *Abar, *Bbar, *gAbar, *gBbar;       // backward inputs (A shared)
     float *dA, *dB;                                 // backward outputs
@@ -1108,10 +1113,29 @@ __global__ void __launch_bounds__(Cf::NW * 32)
 #pragma unroll
         for (int r = 0; r < R; ++r) ld_floats<CC>(cta + (rb * R + r) * XS + cb * CC, cblk[r]);
         if (c == 0) {
-            put_block_record<Cf>(rec_pre, rb, cb, cblk);
-            publish(lb, slot, kStatusPrefix, epoch, tile);
-            identity_block<Cf>(rb, cb, o);
-            put_block_smem<Cf>(carry, rb, cb, o);
+            if (!Cf::BWD && p.H0 != nullptr) {
+                // carry = the start state [I | H0]; prefix = carry o cta
+                const float *h0 = p.H0 + (bb * g.n + nn) * KV;
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int cc = 0; cc < CC; ++cc) {
+                        const int row = rb * R + r, col = cb * CC + cc;
+                        o[r][cc] = col < K ? (row == col ? 1.f : 0.f)
+                                           : (col < NC ? h0[row * VV + col - K] : 0.f);
+                    }
+                put_block_smem<Cf>(carry, rb, cb, o);
+                __syncwarp();
+                load_y<Cf, false>(cta, XS, rb, cb, yc, yv);
+                block_gemm<Cf>(carry, yc, yv, cb, o);
+                put_block_record<Cf>(rec_pre, rb, cb, o);
+                publish(lb, slot, kStatusPrefix, epoch, tile);
+            } else {
+                put_block_record<Cf>(rec_pre, rb, cb, cblk);
+                publish(lb, slot, kStatusPrefix, epoch, tile);
+                identity_block<Cf>(rb, cb, o);
+                put_block_smem<Cf>(carry, rb, cb, o);
+            }
         } else {
             if (peek_status(lb, slot - g.nJ, epoch) != kStatusPrefix) {
                 put_block_record<Cf>(rec_agg, rb, cb, cblk);
@@ -1479,19 +1503,21 @@ size_t ws_kv(int64_t B, int64_t T, int64_t n)
 }
 
 template <int K, int V>
-mg_status fwd_kv(const float *A, const float *Bm, float *Abar, float *Bbar, int64_t B, int64_t T,
-                 int64_t n, void *ws, size_t wsb, cudaStream_t s, const LaunchOpts &o)
+mg_status fwd_kv(const float *A, const float *Bm, const float *H0, float *Abar, float *Bbar,
+                 int64_t B, int64_t T, int64_t n, void *ws, size_t wsb, cudaStream_t s,
+                 const LaunchOpts &o)
 {
-    const char *nm = "mg_affine_scan_fwd";
+    const char *nm = H0 ? "mg_affine_scan_h0_fwd" : "mg_affine_scan_fwd";
     if constexpr (K <= 4) {
         if constexpr (lane_kernel_ok<K, V>())
-            return LaneFwd<K, V>::launch({A, Bm, Abar, Bbar}, B, T, n, ws, wsb, s, o, nm);
+            return LaneFwd<K, V>::launch({A, Bm, Abar, Bbar, H0}, B, T, n, ws, wsb, s, o, nm);
         else
-            return SmallFwd<K, V>::launch({A, Bm, Abar, Bbar}, B, T, n, ws, wsb, s, o, nm);
+            return SmallFwd<K, V>::launch({A, Bm, Abar, Bbar, H0}, B, T, n, ws, wsb, s, o, nm);
     } else {
         AffPtrs p{};
         p.A = A;
         p.Bm = Bm;
+        p.H0 = H0;
         p.Abar_out = Abar;
         p.Bbar_out = Bbar;
         return BigFwd<K, V>::launch(p, B, T, n, ws, wsb, s, o, nm);
@@ -1524,6 +1550,60 @@ mg_status bwd_kv(const float *A, const float *Abar, const float *Bbar, const flo
     }
 }
 
+// The backward from a start state H0 differs from the H0 = 0 one only at the
+// first step (the forward's Bbar, passed in, already carries H0 at every
+// later step): dA_1 gains Lam_1 H0^T (Bbar_0 = H0), and dH0 = A_1^T Lam_1,
+// with Lam_1 = dB_1.  One thread per sequence applies both after the main
+// backward on the same stream.
+template <int K, int V>
+__global__ void affine_h0_grad_kernel(const float *A, const float *H0, const float *dB, float *dA,
+                                      float *dH0, int64_t B, int64_t T, int64_t n)
+{
+    constexpr int KK = K * K, KV = K * V;
+    const int64_t q = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (q >= B * n) return;
+    const int64_t bb = q / n, nn = q % n;
+    const int64_t s1 = (bb * T) * n + nn;   // the first step of the sequence
+    float lam[KV], h0[KV], a1[KK], da[KK], dh[KV];
+    ld_floats<KV>(dB + s1 * KV, lam);
+    ld_floats<KV>(H0 + q * KV, h0);
+    ld_floats<KK>(A + s1 * KK, a1);
+    ld_floats<KK>(dA + s1 * KK, da);
+#pragma unroll
+    for (int i = 0; i < K; ++i)
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            float acc = da[i * K + j];
+#pragma unroll
+            for (int l = 0; l < V; ++l) acc = fmaf(lam[i * V + l], h0[j * V + l], acc);
+            da[i * K + j] = acc;
+        }
+#pragma unroll
+    for (int i = 0; i < K; ++i)
+#pragma unroll
+        for (int l = 0; l < V; ++l) {
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < K; ++j) acc = fmaf(a1[j * K + i], lam[j * V + l], acc);
+            dh[i * V + l] = acc;
+        }
+    st_floats<KK>(dA + s1 * KK, da);
+    st_floats<KV>(dH0 + q * KV, dh);
+}
+
+template <int K, int V>
+mg_status h0_grad_kv(const float *A, const float *H0, const float *dB, float *dA, float *dH0,
+                     int64_t B, int64_t T, int64_t n, cudaStream_t s)
+{
+    const int64_t nq = B * n;
+    const unsigned blocks = unsigned((nq + 127) / 128);
+    affine_h0_grad_kernel<K, V><<<blocks, 128, 0, s>>>(A, H0, dB, dA, dH0, B, T, n);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(MG_ERR_LAUNCH, "mg_affine_scan_h0_bwd: launch failed: %s", cudaGetErrorString(e));
+    return MG_OK;
+}
+
 // Expand CALL(K, V) for the runtime (k, v) in {1,2,4,8,16}^2.
 #define MG_KV_DISPATCH(k, v, CALL)                                                        \
     switch ((k) * 32 + (v)) {                                                             \
@@ -1551,14 +1631,24 @@ size_t affine_ws_bytes(int64_t B, int64_t T, int64_t n, int k, int v)
     return 0;
 }
 
-mg_status launch_affine_fwd(const float *A, const float *Bm, float *Abar, float *Bbar, int64_t B,
-                            int64_t T, int64_t n, int k, int v, void *ws, size_t wsb,
-                            cudaStream_t s, const LaunchOpts &o)
+mg_status launch_affine_fwd(const float *A, const float *Bm, const float *H0, float *Abar,
+                            float *Bbar, int64_t B, int64_t T, int64_t n, int k, int v, void *ws,
+                            size_t wsb, cudaStream_t s, const LaunchOpts &o)
 {
-#define MG_CALL(K, V) return fwd_kv<K, V>(A, Bm, Abar, Bbar, B, T, n, ws, wsb, s, o)
+#define MG_CALL(K, V) return fwd_kv<K, V>(A, Bm, H0, Abar, Bbar, B, T, n, ws, wsb, s, o)
     MG_KV_DISPATCH(k, v, MG_CALL)
 #undef MG_CALL
     return fail(MG_ERR_UNSUPPORTED, "mg_affine_scan_fwd: k=%d v=%d outside {1,2,4,8,16}", k, v);
+}
+
+mg_status launch_affine_h0_grad(const float *A, const float *H0, const float *dB, float *dA,
+                                float *dH0, int64_t B, int64_t T, int64_t n, int k, int v,
+                                cudaStream_t s)
+{
+#define MG_CALL(K, V) return h0_grad_kv<K, V>(A, H0, dB, dA, dH0, B, T, n, s)
+    MG_KV_DISPATCH(k, v, MG_CALL)
+#undef MG_CALL
+    return fail(MG_ERR_UNSUPPORTED, "mg_affine_scan_h0_bwd: k=%d v=%d outside {1,2,4,8,16}", k, v);
 }
 
 mg_status launch_affine_bwd(const float *A, const float *Abar, const float *Bbar,

@@ -105,9 +105,12 @@ mg_status launch_log_bwd(const float *lc, const float *lv, const float *h, const
 mg_status launch_log_fwd(const float *lc, const float *lv, float *h, int64_t B, int64_t T,
                          int64_t D, void *ws, size_t ws_bytes, cudaStream_t s,
                          const LaunchOpts &o);
-mg_status launch_affine_fwd(const float *A, const float *Bm, float *Abar, float *Bbar,
-                            int64_t B, int64_t T, int64_t n, int k, int v, void *ws,
+mg_status launch_affine_fwd(const float *A, const float *Bm, const float *H0, float *Abar,
+                            float *Bbar, int64_t B, int64_t T, int64_t n, int k, int v, void *ws,
                             size_t ws_bytes, cudaStream_t s, const LaunchOpts &o);
+mg_status launch_affine_h0_grad(const float *A, const float *H0, const float *dB, float *dA,
+                                float *dH0, int64_t B, int64_t T, int64_t n, int k, int v,
+                                cudaStream_t s);
 mg_status launch_affine_bwd(const float *A, const float *Abar, const float *Bbar,
                             const float *gAbar, const float *gBbar, float *dA, float *dB,
                             int64_t B, int64_t T, int64_t n, int k, int v, void *ws,

@@ -569,7 +569,63 @@ mg_status mg_affine_scan_fwd(const float *A, const float *Bm, float *Abar, float
                            {Abar, s * k * k * 4, "Abar", true},
                            {Bbar, s * k * v * 4, "Bbar", true},
                            {ws, ws_bytes, "workspace", true}}));
-    return launch_affine_fwd(A, Bm, Abar, Bbar, B, T, n, k, v, ws, ws_bytes, stream, default_opts());
+    return launch_affine_fwd(A, Bm, nullptr, Abar, Bbar, B, T, n, k, v, ws, ws_bytes, stream,
+                             default_opts());
+}
+
+mg_status mg_affine_scan_h0_fwd(const float *A, const float *Bm, const float *H0, float *Abar,
+                                float *Bbar, int64_t B, int64_t T, int64_t n, int k, int v,
+                                void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    const char *fn = "mg_affine_scan_h0_fwd";
+    g_detail[0] = 0;
+    if (!valid_kv(k) || !valid_kv(v))
+        return fail(MG_ERR_UNSUPPORTED, "%s: k=%d v=%d outside {1,2,4,8,16}", fn, k, v);
+    MG_TRY(check_dims(fn, {B, T, n, k, k > v ? k : v}));
+    if (B == 0 || T == 0 || n == 0) return MG_OK;
+    const size_t s = size_t(B) * T * n;
+    MG_TRY(check_ws(fn, ws, ws_bytes, affine_ws_bytes(B, T, n, k, v)));
+    MG_TRY(check_bufs(fn, {{A, s * k * k * 4, "A", false},
+                           {Bm, s * k * v * 4, "Bm", false},
+                           {H0, size_t(B) * n * k * v * 4, "H0", false},
+                           {Abar, s * k * k * 4, "Abar", true},
+                           {Bbar, s * k * v * 4, "Bbar", true},
+                           {ws, ws_bytes, "workspace", true}}));
+    return launch_affine_fwd(A, Bm, H0, Abar, Bbar, B, T, n, k, v, ws, ws_bytes, stream,
+                             default_opts());
+}
+
+mg_status mg_affine_scan_h0_bwd(const float *A, const float *H0, const float *Abar,
+                                const float *Bbar, const float *gAbar, const float *gBbar,
+                                float *dA, float *dB, float *dH0, int64_t B, int64_t T, int64_t n,
+                                int k, int v, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    const char *fn = "mg_affine_scan_h0_bwd";
+    g_detail[0] = 0;
+    if (!valid_kv(k) || !valid_kv(v))
+        return fail(MG_ERR_UNSUPPORTED, "%s: k=%d v=%d outside {1,2,4,8,16}", fn, k, v);
+    MG_TRY(check_dims(fn, {B, T, n, k, k > v ? k : v}));
+    if (B == 0 || n == 0) return MG_OK;
+    const size_t s = size_t(B) * T * n, nh = size_t(B) * n * k * v;
+    if (T == 0) {  // L does not depend on H0: its gradient is zero
+        MG_TRY(check_bufs(fn, {{dH0, nh * 4, "dH0", true}}));
+        const cudaError_t e = cudaMemsetAsync(dH0, 0, nh * 4, stream);
+        return e == cudaSuccess ? MG_OK : fail(MG_ERR_LAUNCH, "%s: %s", fn, cudaGetErrorString(e));
+    }
+    MG_TRY(check_ws(fn, ws, ws_bytes, affine_ws_bytes(B, T, n, k, v)));
+    MG_TRY(check_bufs(fn, {{A, s * k * k * 4, "A", false},
+                           {H0, nh * 4, "H0", false},
+                           {Abar, s * k * k * 4, "Abar", false},
+                           {Bbar, s * k * v * 4, "Bbar", false},
+                           {gAbar, s * k * k * 4, "gAbar", false},
+                           {gBbar, s * k * v * 4, "gBbar", false},
+                           {dA, s * k * k * 4, "dA", true},
+                           {dB, s * k * v * 4, "dB", true},
+                           {dH0, nh * 4, "dH0", true},
+                           {ws, ws_bytes, "workspace", true}}));
+    MG_TRY(launch_affine_bwd(A, Abar, Bbar, gAbar, gBbar, dA, dB, B, T, n, k, v, ws, ws_bytes,
+                             stream, default_opts()));
+    return launch_affine_h0_grad(A, H0, dB, dA, dH0, B, T, n, k, v, stream);
 }
 
 mg_status mg_affine_scan_bwd(const float *A, const float *Abar, const float *Bbar,

@@ -189,3 +189,49 @@ def test_varlen_degenerate(cuda_lib, case):
         _, _, dh0 = mg.linear_scan_h0_bwd(a, h0, a, a, a, a,
                                           out=(None, None, torch.full((2, 8), 7.0, device=DEV)))
         assert torch.equal(dh0, torch.zeros(2, 8, device=DEV))
+
+
+@pytest.mark.parametrize("k,v,shape", [(4, 4, (2, 333, 5)), (2, 8, (2, 200, 3)), (1, 4, (2, 300, 7)),
+                                       (4, 16, (1, 700, 3)), (8, 8, (2, 200, 3)),
+                                       (16, 16, (2, 150, 3)), (16, 4, (1, 300, 2))])
+def test_affine_h0(cuda_lib, k, v, shape):
+    """Every kernel family (lane kernel, chunk engine, warp kernel) from a
+    start state; the parity metric as for the plain affine ops."""
+    import oracle
+    from parity import block_rms
+    mg = cuda_lib
+    Bq, Tq, nq = shape
+    A, Bm, gA, gB = wl.haar_affine(Bq, Tq, nq, k, v, seed=57)
+    H0 = torch.randn(Bq, nq, k, v, generator=torch.Generator().manual_seed(58))
+    Abar, Bbar = mg.affine_scan_h0_fwd(A.to(DEV), Bm.to(DEV), H0.to(DEV),
+                                       out=(_nan(A.shape), _nan(Bm.shape)))
+    rAbar, rBbar = oracle.affine_scan_h0_fwd(A, Bm, H0)
+    if k == 1:
+        SA, SB = oracle.affine_scan_h0_fwd(np.abs(_np(A)), np.abs(_np(Bm)), np.abs(_np(H0)))
+    else:
+        SA, SB = block_rms(rAbar), block_rms(rBbar)
+    errs = {"Abar": scaled_error(_np(Abar), rAbar, SA), "Bbar": scaled_error(_np(Bbar), rBbar, SB)}
+    assert max(errs.values()) <= TOL_F32, errs
+    Ab32, Bb32 = torch.from_numpy(rAbar).float(), torch.from_numpy(rBbar).float()
+    dA, dB, dH0 = mg.affine_scan_h0_bwd(A.to(DEV), H0.to(DEV), Ab32.to(DEV), Bb32.to(DEV),
+                                        gA.to(DEV), gB.to(DEV),
+                                        out=(_nan(A.shape), _nan(Bm.shape), _nan(H0.shape)))
+    rdA, rdB, rdH0 = oracle.affine_scan_h0_bwd(A, H0, Ab32, Bb32, gA, gB)
+    if k == 1:
+        S = oracle.affine_scan_h0_bwd(*(np.abs(_np(x)) for x in (A, H0, Ab32, Bb32, gA, gB)))
+    else:
+        S = (block_rms(rdA), block_rms(rdB), block_rms(rdH0))
+    eb = {"dA": scaled_error(_np(dA), rdA, S[0]), "dB": scaled_error(_np(dB), rdB, S[1]),
+          "dH0": scaled_error(_np(dH0), rdH0, S[2])}
+    assert max(eb.values()) <= TOL_F32, eb
+    mg.workspace_status()
+
+
+def test_affine_h0_zero_equals_plain_op(cuda_lib):
+    mg = cuda_lib
+    for k, v in ((4, 4), (16, 16)):
+        A, Bm, _, _ = wl.haar_affine(2, 300, 4, k, v, seed=59, device=DEV, grads=False)
+        Z = torch.zeros(2, 4, k, v, device=DEV)
+        r1 = mg.affine_scan_h0_fwd(A, Bm, Z)
+        r0 = mg.affine_scan_fwd(A, Bm)
+        assert torch.equal(r1[0], r0[0]) and torch.equal(r1[1], r0[1])
