@@ -464,7 +464,44 @@ def run_extra(mg, dev, peak):
         "bwd": {"ms": tb * 1e3, "elements_per_s": n / tb, "GB_s": 28 * n / tb / 1e9,
                 "frac": 28 * n / tb / 1e9 / peak},
         "step_elements_per_s": n / (tf + tb)}
-    del a, b, gA, gBc, A, Bc, da, db
+    # the same batch from start states h0 (B, D)
+    h0 = torch.randn(Bq, Dq, device=dev, generator=torch.Generator(dev).manual_seed(3))
+    dh0 = torch.empty_like(h0)
+    tf = _time_op(lambda: mg.mg_linear_scan_h0_fwd(a, b, h0, out=(A, Bc)), 20, dev, flush)
+    tb = _time_op(lambda: mg.mg_linear_scan_h0_bwd(a, h0, A, Bc, gA, gBc, out=(da, db, dh0)), 20,
+                  dev, flush)
+    fb, bb = 16 * n + 4 * h0.numel(), 28 * n + 8 * h0.numel()
+    out["mingru_linear_h0_8x4096x1024"] = {
+        "op": "mg_linear_scan_h0_fwd + mg_linear_scan_h0_bwd (fp32, start states h0)",
+        "elements": n,
+        "fwd": {"ms": tf * 1e3, "GB_s": fb / tf / 1e9, "frac": fb / tf / 1e9 / peak},
+        "bwd": {"ms": tb * 1e3, "GB_s": bb / tb / 1e9, "frac": bb / tb / 1e9 / peak}}
+    # the same elements as one packed batch of ragged sequences (lengths
+    # 1..4096, seeded), each from its own start state
+    rng = np.random.default_rng(7)
+    lens = []
+    while sum(lens) < Bq * Tq:
+        lens.append(int(min(rng.integers(1, 4097), Bq * Tq - sum(lens))))
+    cu = torch.as_tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int64, device=dev)
+    nseq = len(lens)
+    hs = torch.randn(nseq, Dq, device=dev, generator=torch.Generator(dev).manual_seed(4))
+    dhs = torch.empty_like(hs)
+    pa, pb = a.reshape(Bq * Tq, Dq), b.reshape(Bq * Tq, Dq)
+    pA, pH = A.reshape(Bq * Tq, Dq), Bc.reshape(Bq * Tq, Dq)
+    pgA, pgH = gA.reshape(Bq * Tq, Dq), gBc.reshape(Bq * Tq, Dq)
+    pda, pdb = da.reshape(Bq * Tq, Dq), db.reshape(Bq * Tq, Dq)
+    tf = _time_op(lambda: mg.mg_linear_scan_varlen_fwd(pa, pb, cu, hs, out=(pA, pH)), 20, dev,
+                  flush)
+    tb = _time_op(lambda: mg.mg_linear_scan_varlen_bwd(pa, cu, pA, pH, pgA, pgH, hs,
+                                                       out=(pda, pdb, dhs)), 20, dev, flush)
+    fb = 16 * n + 4 * hs.numel() + 8 * (nseq + 1)
+    bb = 28 * n + 8 * hs.numel() + 8 * (nseq + 1)
+    out["mingru_varlen_packed_32768x1024"] = {
+        "op": "mg_linear_scan_varlen_fwd + _bwd (fp32, packed ragged sequences with start states)",
+        "elements": n, "sequences": nseq,
+        "fwd": {"ms": tf * 1e3, "GB_s": fb / tf / 1e9, "frac": fb / tf / 1e9 / peak},
+        "bwd": {"ms": tb * 1e3, "GB_s": bb / tb / 1e9, "frac": bb / tb / 1e9 / peak}}
+    del a, b, gA, gBc, A, Bc, da, db, h0, dh0, hs, dhs
     # the fused minGRU gate + scan, as a minGRU layer trains: forward without
     # A, backward without gA (the loss depends on h = Bc only)
     for name, (Bq, Tq, Dq, xdt) in (("mingru_fused_8x4096x1024", (8, 4096, 1024, torch.float32)),
@@ -525,6 +562,17 @@ def run_extra(mg, dev, peak):
         ff, bf = S * 2 * (k ** 3 + k * k * v), S * 4 * (k ** 3 + k * k * v)
         rf = max(fb / (peak * 1e9), ff / (fp32_peak_tflops * 1e12))
         rb = max(bb / (peak * 1e9), bf / (fp32_peak_tflops * 1e12))
+        H0 = torch.randn(Bq, nq, k, v, device=dev, generator=torch.Generator(dev).manual_seed(5))
+        dH0 = torch.empty_like(H0)
+        tfh = _time_op(lambda: mg.mg_affine_scan_h0_fwd(Am, Bm, H0, out=(Abar, Bbar)), 10, dev,
+                       flush)
+        tbh = _time_op(lambda: mg.mg_affine_scan_h0_bwd(Am, H0, Abar, Bbar, gAm, gBm,
+                                                        out=(dA, dB, dH0)), 10, dev, flush)
+        out[name + "_h0"] = {"op": "mg_affine_scan_h0_fwd + mg_affine_scan_h0_bwd",
+                             "fwd": {"ms": tfh * 1e3,
+                                     "roofline_frac": (rf + H0.numel() * 4 / (peak * 1e9)) / tfh},
+                             "bwd": {"ms": tbh * 1e3,
+                                     "roofline_frac": (rb + H0.numel() * 8 / (peak * 1e9)) / tbh}}
         out[name] = {"op": "mg_affine_scan_fwd + mg_affine_scan_bwd",
                      "elements": S * k * v,
                      "fwd": {"ms": tf * 1e3, "elements_per_s": S * k * v / tf,
@@ -535,7 +583,7 @@ def run_extra(mg, dev, peak):
                              "roofline_frac": rb / tb},
                      "roofline": "max(bytes / HBM peak, flops / FP32 FFMA peak "
                                  f"{fp32_peak_tflops:.1f} TFLOP/s at 2070 MHz)"}
-        del Am, Bm, gAm, gBm, Abar, Bbar, dA, dB
+        del Am, Bm, gAm, gBm, Abar, Bbar, dA, dB, H0, dH0
     del flush
     mg.workspace_status()
     torch.cuda.empty_cache()
