@@ -20,6 +20,8 @@ evaluated in double precision by ``mg_oracle.c``:
 * ``linear_scan_varlen_fwd/bwd``, ``linear_scan_h0_fwd/bwd`` -- the linear
   scan from a start state h0, over (B,T,D) or a packed variable-length batch
 * ``affine_scan_h0_fwd/bwd`` -- the affine scan from a start state H0
+* ``angle_scan_fwd/bwd`` -- the angle-fused scan (Kernel 4) under the reading
+  stated in mg_oracle.c (parity of that reading is unpinned by the page)
 
 Inputs are converted to contiguous float64 numpy arrays (a float32 or bf16
 value widens exactly).  Outputs are float64 numpy arrays.
@@ -85,6 +87,12 @@ class Oracle:
         lib.orc_linear_scan_varlen_bwd.argtypes = [P, PI, I64, P, P, P, P, P, P, P, P, I64]
         lib.orc_affine_scan_h0_fwd.argtypes = [P, P, P, P, P, I64, I64, I64, I, I]
         lib.orc_affine_scan_h0_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I64, I64, I64, I, I]
+        PI32 = ctypes.POINTER(ctypes.c_int32)
+        lib.orc_angle_scan_fwd.argtypes = [P, P, P, P, P, PI32, P, I, I, P, I64, I64, I64, I, I]
+        lib.orc_angle_scan_bwd.argtypes = [P, P, P, P, P, P, PI32, P, I, I, P, P, P, P, P, I64, I64,
+                                           I64, I, I]
+        lib.orc_angle_scan_fwd.restype = None
+        lib.orc_angle_scan_bwd.restype = None
         for f in (lib.orc_linear_scan_fwd, lib.orc_linear_scan_bwd, lib.orc_log_scan_fwd,
                   lib.orc_log_scan_bwd, lib.orc_affine_scan_fwd, lib.orc_affine_scan_bwd,
                   lib.orc_mingru_gate, lib.orc_mingru_scan_fwd, lib.orc_mingru_scan_bwd,
@@ -261,6 +269,46 @@ class Oracle:
                                          _ptr(gBbar), _ptr(dA), _ptr(dB), _ptr(dH0), B, T, n, k, v)
         return dA, dB, dH0
 
+    # ---------------------------------------------------- angle-fused scan
+
+    @staticmethod
+    def _perm(perm, R, k):
+        perm = np.ascontiguousarray(np.asarray(perm, dtype=np.int32))
+        assert perm.shape == (R, k) and all(sorted(r) == list(range(k)) for r in perm.tolist())
+        return perm
+
+    def angle_scan_fwd(self, theta, scale, gamma, b, h0, perm, sgn, has_scale=1, has_decay=1):
+        """h (B,T,n,k) of the angle-fused scan (reading in mg_oracle.c)."""
+        theta, scale, gamma, b, h0, sgn = (_f64(x) for x in (theta, scale, gamma, b, h0, sgn))
+        B, T, n, R, half = theta.shape
+        k = 2 * half
+        assert scale.shape == (B, T, n) and gamma.shape == (B, T, n)
+        assert b.shape == (B, T, n, k) and h0.shape == (B, n, k) and sgn.shape == (R, k)
+        perm = self._perm(perm, R, k)
+        h = np.empty_like(b)
+        self._lib.orc_angle_scan_fwd(_ptr(theta), _ptr(scale), _ptr(gamma), _ptr(b), _ptr(h0),
+                                     perm.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _ptr(sgn),
+                                     int(has_scale), int(has_decay), _ptr(h), B, T, n, R, k)
+        return h
+
+    def angle_scan_bwd(self, theta, scale, gamma, h0, out, grad_out, perm, sgn, has_scale=1,
+                       has_decay=1):
+        """(dtheta, dscale, dgamma, db, dh0) for L = sum(grad_out * h), out = h as given."""
+        theta, scale, gamma, h0, out, grad_out, sgn = (
+            _f64(x) for x in (theta, scale, gamma, h0, out, grad_out, sgn))
+        B, T, n, R, half = theta.shape
+        k = 2 * half
+        assert out.shape == (B, T, n, k) and grad_out.shape == out.shape
+        perm = self._perm(perm, R, k)
+        dtheta, dscale, dgamma = np.empty_like(theta), np.empty_like(scale), np.empty_like(gamma)
+        db, dh0 = np.empty_like(out), np.empty_like(h0)
+        self._lib.orc_angle_scan_bwd(_ptr(theta), _ptr(scale), _ptr(gamma), _ptr(h0), _ptr(out),
+                                     _ptr(grad_out),
+                                     perm.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _ptr(sgn),
+                                     int(has_scale), int(has_decay), _ptr(dtheta), _ptr(dscale),
+                                     _ptr(dgamma), _ptr(db), _ptr(dh0), B, T, n, R, k)
+        return dtheta, dscale, dgamma, db, dh0
+
 
 _default = None
 
@@ -330,3 +378,12 @@ def affine_scan_h0_fwd(A, Bm, H0):
 
 def affine_scan_h0_bwd(A, H0, Abar, Bbar, gAbar, gBbar):
     return _oracle().affine_scan_h0_bwd(A, H0, Abar, Bbar, gAbar, gBbar)
+
+
+def angle_scan_fwd(theta, scale, gamma, b, h0, perm, sgn, has_scale=1, has_decay=1):
+    return _oracle().angle_scan_fwd(theta, scale, gamma, b, h0, perm, sgn, has_scale, has_decay)
+
+
+def angle_scan_bwd(theta, scale, gamma, h0, out, grad_out, perm, sgn, has_scale=1, has_decay=1):
+    return _oracle().angle_scan_bwd(theta, scale, gamma, h0, out, grad_out, perm, sgn, has_scale,
+                                    has_decay)

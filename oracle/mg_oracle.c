@@ -530,3 +530,138 @@ void orc_affine_scan_h0_bwd(const double *A, const double *H0, const double *Aba
     free(tmp);
     free(eye);
 }
+
+/*
+ * ---------------------------------------------------------------------------
+ * The angle-fused scan (Kernel 4: page sections "angle_scan_fwd",
+ * "angle_scan_bwd", "angle_scan_impl").  The page gives the shapes --
+ * theta (B,T,n,R,half), scale and gamma (B,T,n), b (B,T,n,k), h0 (B,n,k),
+ * perm/sgn/p2p (R,k), half = k/2 -- the returned state h (B,T,n,k), the
+ * backward's outputs (dtheta, dscale, dgamma, db, dh0), and that scale and
+ * gamma are a tanh and an exp(-lambda dt) of the module's parameters, used
+ * only under has_scale / has_decay.  It does not define how theta, perm,
+ * sgn and p2p form the transition.  The reading taken here (the plainest
+ * one those shapes support): the transition of step t is
+ *   A_t = s_t g_t Q_t,   s_t = scale_t (has_scale) or 1,  g_t = gamma_t (has_decay) or 1,
+ *   Q_t = L_{R-1} ... L_1 L_0,   L_r x: for i = 0 .. half-1, with p = perm[r][2i],
+ *         q = perm[r][2i+1] and c, s = cos, sin theta_{t,r,i}:
+ *           (x_p, x_q) <- (c x_p - s x_q,  s x_p + c x_q)
+ *         then x_j <- sgn[r][j] x_j for every j,
+ * and the state runs h_t = A_t h_{t-1} + b_t from h_0 = h0 (the affine
+ * recurrence of affine_scan_fwd with a vector state).  perm[r] is a
+ * permutation of 0..k-1; p2p[r] is its inverse (the position of each
+ * coordinate in perm[r]), which the oracle does not need.
+ */
+
+/* x <- Q_t x for one step: R layers of paired rotations and signs. */
+static void orc_angle_apply(double *x, const double *th, const int32_t *perm, const double *sgn,
+                            int R, int k)
+{
+    const int half = k / 2;
+    for (int r = 0; r < R; ++r) {
+        for (int i = 0; i < half; ++i) {
+            const int p = perm[r * k + 2 * i], q = perm[r * k + 2 * i + 1];
+            const double c = cos(th[r * half + i]), s = sin(th[r * half + i]);
+            const double xp = x[p], xq = x[q];
+            x[p] = c * xp - s * xq;
+            x[q] = s * xp + c * xq;
+        }
+        for (int j = 0; j < k; ++j)
+            x[j] *= sgn[r * k + j];
+    }
+}
+
+void orc_angle_scan_fwd(const double *theta, const double *scale, const double *gamma,
+                        const double *b, const double *h0, const int32_t *perm, const double *sgn,
+                        int has_scale, int has_decay, double *h_out, int64_t B, int64_t T,
+                        int64_t n, int R, int k)
+{
+    const int half = k / 2;
+    double *x = (double *)malloc((size_t)k * sizeof(double));
+    for (int64_t bi = 0; bi < B; ++bi)
+        for (int64_t ni = 0; ni < n; ++ni) {
+            memcpy(x, h0 + (bi * n + ni) * k, (size_t)k * sizeof(double));
+            for (int64_t t = 0; t < T; ++t) {
+                const int64_t s = (bi * T + t) * n + ni;   /* step index (b, t, n) */
+                orc_angle_apply(x, theta + s * R * half, perm, sgn, R, k);
+                const double f = (has_scale ? scale[s] : 1.0) * (has_decay ? gamma[s] : 1.0);
+                for (int j = 0; j < k; ++j) {
+                    x[j] = f * x[j] + b[s * k + j];
+                    h_out[s * k + j] = x[j];
+                }
+            }
+        }
+    free(x);
+}
+
+/*
+ * Gradients of L = sum(grad_out * h) for the forward above, with the stored
+ * states h (out) used as given for every h_{t-1} (h_0 = h0):
+ *   lam_t = grad_out_t + A_{t+1}^T lam_{t+1}   (zero past T),   db_t = lam_t
+ *   y_t = Q_t h_{t-1}:  dscale_t = g_t lam_t . y_t (has_scale),  dgamma_t = s_t lam_t . y_t (has_decay)
+ *   dtheta_{t,r,i}: u = s_t g_t lam_t carried back through the layers
+ *     (through the signs, then the transposed rotations), with x the input of
+ *     layer r recomputed forward from h_{t-1}; for the pair (p, q) of angle i
+ *     and u' the gradient after the signs:
+ *       dtheta = u'_p (-s x_p - c x_q) + u'_q (c x_p - s x_q)
+ *   A_t^T lam_t is that u after layer 0;  dh0 = A_1^T lam_1.
+ * dscale (dgamma) is zero when has_scale (has_decay) is 0.
+ */
+void orc_angle_scan_bwd(const double *theta, const double *scale, const double *gamma,
+                        const double *h0, const double *out, const double *grad_out,
+                        const int32_t *perm, const double *sgn, int has_scale, int has_decay,
+                        double *dtheta, double *dscale, double *dgamma, double *db, double *dh0,
+                        int64_t B, int64_t T, int64_t n, int R, int k)
+{
+    const int half = k / 2;
+    double *xs = (double *)malloc((size_t)(R + 1) * k * sizeof(double));   /* layer inputs */
+    double *u = (double *)malloc((size_t)k * sizeof(double));
+    double *lam = (double *)malloc((size_t)k * sizeof(double));
+    double *carry = (double *)malloc((size_t)k * sizeof(double));
+    for (int64_t bi = 0; bi < B; ++bi)
+        for (int64_t ni = 0; ni < n; ++ni) {
+            for (int j = 0; j < k; ++j) carry[j] = 0.0;
+            for (int64_t t = T - 1; t >= 0; --t) {
+                const int64_t s = (bi * T + t) * n + ni;
+                const double *hp = t > 0 ? out + (s - n) * k : h0 + (bi * n + ni) * k;
+                const double *th = theta + s * R * half;
+                const double sc = has_scale ? scale[s] : 1.0, ga = has_decay ? gamma[s] : 1.0;
+                for (int j = 0; j < k; ++j) {
+                    lam[j] = grad_out[s * k + j] + carry[j];
+                    db[s * k + j] = lam[j];
+                }
+                /* forward through the layers from h_{t-1}, keeping each layer's input */
+                memcpy(xs, hp, (size_t)k * sizeof(double));
+                for (int r = 0; r < R; ++r) {
+                    memcpy(xs + (r + 1) * k, xs + r * k, (size_t)k * sizeof(double));
+                    orc_angle_apply(xs + (r + 1) * k, th + r * half, perm + r * k, sgn + r * k, 1, k);
+                }
+                double dot = 0.0;   /* lam_t . y_t */
+                for (int j = 0; j < k; ++j) dot += lam[j] * xs[R * k + j];
+                dscale[s] = has_scale ? ga * dot : 0.0;
+                dgamma[s] = has_decay ? sc * dot : 0.0;
+                for (int j = 0; j < k; ++j) u[j] = sc * ga * lam[j];
+                for (int r = R - 1; r >= 0; --r) {
+                    const double *x = xs + r * k;
+                    for (int j = 0; j < k; ++j) u[j] *= sgn[r * k + j];
+                    for (int i = 0; i < half; ++i) {
+                        const int p = perm[r * k + 2 * i], q = perm[r * k + 2 * i + 1];
+                        const double c = cos(th[r * half + i]), sn = sin(th[r * half + i]);
+                        dtheta[s * R * half + r * half + i] =
+                            u[p] * (-sn * x[p] - c * x[q]) + u[q] * (c * x[p] - sn * x[q]);
+                        const double up = u[p], uq = u[q];
+                        u[p] = c * up + sn * uq;
+                        u[q] = -sn * up + c * uq;
+                    }
+                }
+                memcpy(carry, u, (size_t)k * sizeof(double));   /* A_t^T lam_t */
+            }
+            memcpy(dh0 + (bi * n + ni) * k, carry, (size_t)k * sizeof(double));
+            if (T == 0)
+                for (int j = 0; j < k; ++j) dh0[(bi * n + ni) * k + j] = 0.0;
+        }
+    free(xs);
+    free(u);
+    free(lam);
+    free(carry);
+}

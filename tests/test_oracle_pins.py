@@ -695,6 +695,167 @@ def pin_new_degenerate_shapes(orc):
     np.testing.assert_array_equal(dH0, np.zeros_like(H0))
 
 
+# ----------------------------------------------- angle-fused scan (reading)
+
+def _angle_inputs(rng, B, T, n, R, k, sgn_pm=True):
+    theta = rng.uniform(-np.pi, np.pi, size=(B, T, n, R, k // 2))
+    scale = np.tanh(rng.normal(size=(B, T, n)))
+    gamma = np.exp(-rng.uniform(0.0, 0.3, size=(B, T, n)))
+    b = rng.normal(size=(B, T, n, k))
+    h0 = rng.normal(size=(B, n, k))
+    perm = np.stack([rng.permutation(k) for _ in range(R)]).astype(np.int32)
+    sgn = rng.choice([-1.0, 1.0], size=(R, k)) if sgn_pm else rng.uniform(0.5, 1.5, size=(R, k))
+    return theta, scale, gamma, b, h0, perm, sgn
+
+
+def _angle_dense(theta, perm, sgn, deriv=None):
+    """Q_t of every step as an explicit k x k product of Givens matrices
+    (numpy); with deriv = (r, i), the derivative of Q_t in theta_{t,r,i}."""
+    B, T, n, R, half = theta.shape
+    k = 2 * half
+    Q = np.zeros((B, T, n, k, k))
+    for idx in np.ndindex(B, T, n):
+        M = np.eye(k)
+        for r in range(R):
+            G = np.eye(k)
+            for i in range(half):
+                p, q = perm[r][2 * i], perm[r][2 * i + 1]
+                c, s_ = np.cos(theta[idx + (r, i)]), np.sin(theta[idx + (r, i)])
+                if deriv == (r, i):
+                    G[p, p], G[p, q], G[q, p], G[q, q] = -s_, -c, c, -s_
+                else:
+                    G[p, p], G[p, q], G[q, p], G[q, q] = c, -s_, s_, c
+            if deriv is not None and deriv[0] == r:
+                for i in range(half):                   # the other pairs do not move
+                    if i != deriv[1]:
+                        p, q = perm[r][2 * i], perm[r][2 * i + 1]
+                        G[p, p] = G[p, q] = G[q, p] = G[q, q] = 0.0
+                for j in range(k):
+                    if j not in (perm[r][2 * deriv[1]], perm[r][2 * deriv[1] + 1]):
+                        G[j, j] = 0.0
+            M = np.diag(sgn[r]) @ G @ M
+        Q[idx] = M
+    return Q
+
+
+def pin_golden_angle(orc):
+    g = _golden("angle_scan_k2.json")
+    a = {k_: np.array(g[k_]) for k_ in ("theta", "scale", "gamma", "b", "h0", "sgn", "grad_out")}
+    h = orc.angle_scan_fwd(a["theta"], a["scale"], a["gamma"], a["b"], a["h0"], g["perm"], a["sgn"])
+    np.testing.assert_allclose(h, np.array(g["h"]), rtol=1e-14, atol=1e-15)
+    r = orc.angle_scan_bwd(a["theta"], a["scale"], a["gamma"], a["h0"], np.array(g["h"]),
+                           a["grad_out"], g["perm"], a["sgn"])
+    for name, got in zip(("dtheta", "dscale", "dgamma", "db", "dh0"), r):
+        np.testing.assert_allclose(got, np.array(g[name]), rtol=1e-14, atol=1e-15, err_msg=name)
+
+
+def pin_angle_vs_dense_affine(orc):
+    """The scan equals the affine scan (pinned above) on the explicit dense
+    transitions A_t = s g Q_t with a vector state, and its gradients are the
+    affine adjoint's carried through A_t by matrix calculus:
+    dscale = g <dA, Q>, dgamma = s <dA, Q>, dtheta = s g <dA, dQ/dtheta>."""
+    rng = np.random.default_rng(71)
+    B, T, n, R, k = 2, 6, 2, 3, 4
+    th, sc, ga, b, h0, perm, sgn = _angle_inputs(rng, B, T, n, R, k, sgn_pm=False)
+    Q = _angle_dense(th, perm, sgn)
+    A = (sc * ga)[..., None, None] * Q
+    h = orc.angle_scan_fwd(th, sc, ga, b, h0, perm, sgn)
+    _, Hb = orc.affine_scan_h0_fwd(A, b[..., None], h0[..., None])
+    np.testing.assert_allclose(h, Hb[..., 0], rtol=1e-12, atol=1e-12)
+    go = rng.normal(size=h.shape)
+    Abar, _ = orc.affine_scan_h0_fwd(A, b[..., None], h0[..., None])
+    dA, dB, dH0 = orc.affine_scan_h0_bwd(A, h0[..., None], Abar, h[..., None],
+                                         np.zeros_like(Abar), go[..., None])
+    dth, dsc, dga, db, dh0 = orc.angle_scan_bwd(th, sc, ga, h0, h, go, perm, sgn)
+    np.testing.assert_allclose(db, dB[..., 0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dh0, dH0[..., 0], rtol=1e-12, atol=1e-12)
+    inner = np.sum(dA * Q, axis=(-2, -1))
+    np.testing.assert_allclose(dsc, ga * inner, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dga, sc * inner, rtol=1e-11, atol=1e-12)
+    for r in range(R):
+        for i in range(k // 2):
+            dQ = _angle_dense(th, perm, sgn, deriv=(r, i))
+            want = sc * ga * np.sum(dA * dQ, axis=(-2, -1))
+            np.testing.assert_allclose(dth[..., r, i], want, rtol=1e-10, atol=1e-11)
+
+
+def pin_angle_special_cases(orc):
+    """theta = 0, sgn = 1: Q = I and every coordinate is the linear scan with
+    a = s g from h0; scale and gamma are ignored (and their gradients zero)
+    without has_scale / has_decay; b = 0, s = g = 1, sgn = +-1 keep |h_t| = |h0|."""
+    rng = np.random.default_rng(72)
+    B, T, n, R, k = 2, 7, 3, 2, 4
+    th, sc, ga, b, h0, perm, sgn = _angle_inputs(rng, B, T, n, R, k)
+    h = orc.angle_scan_fwd(np.zeros_like(th), sc, ga, b, h0, perm, np.ones_like(sgn))
+    a = np.repeat((sc * ga)[..., None], k, axis=-1)
+    _, H = orc.linear_scan_h0_fwd(a.reshape(B, T, n * k), b.reshape(B, T, n * k),
+                                  h0.reshape(B, n * k))
+    np.testing.assert_allclose(h, H.reshape(h.shape), rtol=1e-12, atol=1e-12)
+    h1 = orc.angle_scan_fwd(th, sc, ga, b, h0, perm, sgn, has_scale=0, has_decay=0)
+    h2 = orc.angle_scan_fwd(th, sc * 3 + 1, ga * 0.1, b, h0, perm, sgn, has_scale=0, has_decay=0)
+    np.testing.assert_array_equal(h1, h2)
+    go = rng.normal(size=h1.shape)
+    _, dsc, dga, _, _ = orc.angle_scan_bwd(th, sc, ga, h0, h1, go, perm, sgn, 0, 0)
+    assert not dsc.any() and not dga.any()
+    hn = orc.angle_scan_fwd(th, np.ones_like(sc), np.ones_like(ga), np.zeros_like(b), h0, perm, sgn)
+    np.testing.assert_allclose(np.linalg.norm(hn, axis=-1),
+                               np.broadcast_to(np.linalg.norm(h0, axis=-1)[:, None], hn.shape[:-1]),
+                               rtol=1e-12)
+
+
+def _loss_angle(orc, th, sc, ga, b, h0, perm, sgn, go):
+    return float(np.sum(go * orc.angle_scan_fwd(th, sc, ga, b, h0, perm, sgn)))
+
+
+def pin_angle_adjoint_fd(orc):
+    rng = np.random.default_rng(73)
+    th, sc, ga, b, h0, perm, sgn = _angle_inputs(rng, 1, 5, 2, 2, 4, sgn_pm=False)
+    h = orc.angle_scan_fwd(th, sc, ga, b, h0, perm, sgn)
+    go = rng.normal(size=h.shape)
+    grads = orc.angle_scan_bwd(th, sc, ga, h0, h, go, perm, sgn)
+    eps = 1e-6
+    for arr, grad in zip((th, sc, ga, b, h0), grads):
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + eps
+            lp = _loss_angle(orc, th, sc, ga, b, h0, perm, sgn, go)
+            arr[idx] = old - eps
+            lm = _loss_angle(orc, th, sc, ga, b, h0, perm, sgn, go)
+            arr[idx] = old
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(fd)), (idx, fd, grad[idx])
+
+
+def pin_angle_adjoint_autograd(orc):
+    """torch.autograd through the reading written as a float64 torch loop."""
+    rng = np.random.default_rng(74)
+    B, T, n, R, k = 2, 6, 2, 3, 8
+    th, sc, ga, b, h0, perm, sgn = _angle_inputs(rng, B, T, n, R, k)
+    t = {nm: torch.tensor(x, requires_grad=True) for nm, x in
+         (("th", th), ("sc", sc), ("ga", ga), ("b", b), ("h0", h0))}
+    x = t["h0"]
+    hs = []
+    for ti in range(T):
+        for r in range(R):
+            cols = list(x.unbind(-1))
+            for i in range(k // 2):
+                p, q = int(perm[r][2 * i]), int(perm[r][2 * i + 1])
+                c, s_ = torch.cos(t["th"][:, ti, :, r, i]), torch.sin(t["th"][:, ti, :, r, i])
+                cols[p], cols[q] = c * cols[p] - s_ * cols[q], s_ * cols[p] + c * cols[q]
+            x = torch.stack(cols, -1) * torch.tensor(sgn[r])
+        x = (t["sc"][:, ti] * t["ga"][:, ti])[..., None] * x + t["b"][:, ti]
+        hs.append(x)
+    h = torch.stack(hs, 1)
+    go = rng.normal(size=h.shape)
+    L = (h * torch.tensor(go)).sum()
+    want = torch.autograd.grad(L, [t[nm] for nm in ("th", "sc", "ga", "b", "h0")])
+    hh = orc.angle_scan_fwd(th, sc, ga, b, h0, perm, sgn)
+    np.testing.assert_allclose(hh, h.detach().numpy(), rtol=1e-12, atol=1e-12)
+    got = orc.angle_scan_bwd(th, sc, ga, h0, hh, go, perm, sgn)
+    for nm, g_, w in zip(("th", "sc", "ga", "b", "h0"), got, want):
+        np.testing.assert_allclose(g_, w.numpy(), rtol=1e-11, atol=1e-11, err_msg=nm)
+
+
 PINS = [
     pin_golden_linear, pin_golden_log, pin_golden_affine,
     pin_linear_closed_form, pin_linear_special_cases,
@@ -711,6 +872,8 @@ PINS = [
     pin_golden_varlen_h0, pin_varlen_is_independent_scans, pin_h0_batch_is_varlen,
     pin_varlen_adjoint_fd, pin_golden_affine_h0, pin_affine_h0_identity,
     pin_affine_h0_adjoint_fd, pin_new_degenerate_shapes,
+    pin_golden_angle, pin_angle_vs_dense_affine, pin_angle_special_cases,
+    pin_angle_adjoint_fd, pin_angle_adjoint_autograd,
 ]
 
 
@@ -771,6 +934,15 @@ MUTANTS = {
                                   "const double *Bprev = (t > 0) ? Bbar + (s - n) * kv : Bbar + s * kv;"),
     "affine_dh0_untransposed": ("mat_tmul(A + ((bi * T) * n + ni) * kk, L, dh, k, k, v);",
                                 "mat_mul(A + ((bi * T) * n + ni) * kk, L, dh, k, k, v);"),
+    "angle_rotation_sign": ("x[p] = c * xp - s * xq;", "x[p] = c * xp + s * xq;"),
+    "angle_dropped_signs": ("            x[j] *= sgn[r * k + j];\n", "            x[j] *= 1.0;\n"),
+    "angle_bwd_dtheta_sign": ("u[p] * (-sn * x[p] - c * x[q])", "u[p] * (sn * x[p] - c * x[q])"),
+    "angle_bwd_untransposed": ("u[p] = c * up + sn * uq;", "u[p] = c * up - sn * uq;"),
+    "angle_bwd_dscale_without_gamma": ("dscale[s] = has_scale ? ga * dot : 0.0;",
+                                       "dscale[s] = has_scale ? dot : 0.0;"),
+    "angle_bwd_halo_index": ("const double *hp = t > 0 ? out + (s - n) * k",
+                             "const double *hp = t > 0 ? out + s * k"),
+    "angle_decay_flag_ignored": ("(has_decay ? gamma[s] : 1.0)", "(gamma[s])"),
 }
 
 
