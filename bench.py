@@ -529,6 +529,26 @@ def run_extra(mg, dev, peak):
             "step_elements_per_s": n / (tf + tb)}
         del x1, x2, gBc, Bc, dx1, dx2
         torch.cuda.empty_cache()
+    # the angle-fused scan (Kernel 4): 4096 sequences of k = 16, R = 4 layers
+    Bq, Tq, nq, R, k = 16, 2048, 256, 4, 16
+    th, sc, ga, bv, h0, perm, sgn, p2p, go = wl.angle_inputs(Bq, Tq, nq, R, k, seed=0, device=dev)
+    h = mg.angle_scan_fwd(th, sc, ga, bv, h0, perm, sgn, p2p)
+    outs = tuple(torch.empty_like(x) for x in (th, sc, ga, bv, h0))
+    tf = _time_op(lambda: mg.angle_scan_fwd(th, sc, ga, bv, h0, perm, sgn, p2p, out=h), 10, dev,
+                  flush)
+    tb = _time_op(lambda: mg.angle_scan_bwd(th, sc, ga, h0, h, go, perm, sgn, p2p, out=outs), 10,
+                  dev, flush)
+    S = Bq * Tq * nq
+    fb = S * 4 * (R * k // 2 + 2 + 2 * k) + h0.numel() * 4          # theta, scale, gamma, b, h
+    bb = S * 4 * (2 * (R * k // 2) + 4 + 3 * k) + 2 * h0.numel() * 4  # + out, grad_out; d*
+    out["angle_16x2048x256_k16_R4"] = {
+        "op": "mg_angle_scan_fwd + mg_angle_scan_bwd (has_scale, has_decay)",
+        "elements": S * k,
+        "fwd": {"ms": tf * 1e3, "elements_per_s": S * k / tf, "GB_s": fb / tf / 1e9,
+                "frac": fb / tf / 1e9 / peak, "algorithmic_bytes": fb},
+        "bwd": {"ms": tb * 1e3, "elements_per_s": S * k / tb, "GB_s": bb / tb / 1e9,
+                "frac": bb / tb / 1e9 / peak, "algorithmic_bytes": bb}}
+    del th, sc, ga, bv, h0, go, h, outs
     # log-space scan
     lc, lv = wl.mingru_log(16, 2048, 2048, seed=0, device=dev)
     h = torch.empty_like(lc)

@@ -17,6 +17,7 @@
  *                           from start states, over (B,T,D) or packed
  *                           variable-length sequences
  *   mg_affine_scan_h0_fwd/bwd <- affine_scan_fwd/bwd from start states
+ *   mg_angle_scan_fwd/bwd   <- angle_scan_fwd/bwd   ("Angle-fused forward", Kernel 4)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -339,6 +340,42 @@ mg_status mg_affine_scan_h0_bwd(const float *A, const float *H0,
                                 float *dA, float *dB, float *dH0,
                                 int64_t B, int64_t T, int64_t n, int k, int v,
                                 void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * The angle-fused scan (page sections "angle_scan_fwd", "angle_scan_impl";
+ * Kernel 4).  theta (B,T,n,R,half), scale and gamma (B,T,n), b (B,T,n,k),
+ * h0 (B,n,k) are float32 device arrays, half = k/2; h (B,T,n,k) is written.
+ * perm, p2p (int32) and sgn (float32) are (R,k) HOST arrays (module
+ * constants; validated before launch: every perm[r] a permutation of
+ * 0..k-1, p2p[r] its inverse).  The page does not define the transition;
+ * this library reads it as
+ *   h_t = s_t g_t Q_t h_{t-1} + b_t,  h_0 = h0,   s_t = scale_t if has_scale else 1,
+ *   g_t = gamma_t if has_decay else 1,   Q_t = L_{R-1} ... L_0, where L_r
+ *   rotates each pair (x_p, x_q), p = perm[r][2i], q = perm[r][2i+1], to
+ *   (c x_p - s x_q, s x_p + c x_q) with c, s = cos, sin theta_{t,r,i},
+ *   then multiplies each x_j by sgn[r][j].
+ * scale (gamma) may be NULL when has_scale (has_decay) is 0.  k in
+ * {2, 4, 8, 16, 32}, 1 <= R <= 8.  No workspace.
+ */
+mg_status mg_angle_scan_fwd(const float *theta, const float *scale, const float *gamma,
+                            const float *b, const float *h0,
+                            const int32_t *perm, const float *sgn, const int32_t *p2p,
+                            int has_scale, int has_decay, float *h,
+                            int64_t B, int64_t T, int64_t n, int R, int k, cudaStream_t stream);
+
+/*
+ * Exact backward of mg_angle_scan_fwd from the stored states (page section
+ * "angle_scan_bwd"): out is the forward's h (the source of every h_{t-1}),
+ * grad_out = dL/dh.  Writes dtheta (shape of theta), dscale and dgamma
+ * (B,T,n; zero when the flag is 0, as the page's zeros_like outputs), db
+ * (shape of b) and dh0 (shape of h0).  b itself is not needed.
+ */
+mg_status mg_angle_scan_bwd(const float *theta, const float *scale, const float *gamma,
+                            const float *h0, const float *out, const float *grad_out,
+                            const int32_t *perm, const float *sgn, const int32_t *p2p,
+                            int has_scale, int has_decay,
+                            float *dtheta, float *dscale, float *dgamma, float *db, float *dh0,
+                            int64_t B, int64_t T, int64_t n, int R, int k, cudaStream_t stream);
 
 /*
  * mg_linear_scan_fwd without a workspace argument (the page has no

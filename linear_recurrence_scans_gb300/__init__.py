@@ -27,6 +27,9 @@ Ops (names of the C entry points; aliases with the names of the page
   packed variable-length sequences (Ttot, D) with int64 offsets
 * ``mg_affine_scan_h0_fwd(A, Bm, H0) -> (Abar, Bbar)``, ``mg_affine_scan_h0_bwd(A, H0, Abar,
   Bbar, gAbar, gBbar) -> (dA, dB, dH0)``: the affine scan from start states H0 (B, n, k, v)
+* ``mg_angle_scan_fwd(theta, scale, gamma, b, h0, perm, sgn, p2p=None) -> h`` and
+  ``mg_angle_scan_bwd(...) -> (dtheta, dscale, dgamma, db, dh0)``: the angle-fused
+  scan (aliases ``angle_scan_fwd``, ``angle_scan_bwd``)
 
 Every op accepts optional preallocated outputs (``out=(...)``), a workspace
 tensor (``ws=``, uint8, zero-filled before first use) and a stream
@@ -57,6 +60,7 @@ __all__ = [
     "mg_linear_scan_h0_fwd", "mg_linear_scan_h0_bwd", "mg_linear_scan_varlen_fwd",
     "mg_linear_scan_varlen_bwd", "varlen_workspace_size",
     "mg_affine_scan_h0_fwd", "mg_affine_scan_h0_bwd",
+    "mg_angle_scan_fwd", "mg_angle_scan_bwd", "angle_scan_fwd", "angle_scan_bwd",
 ]
 
 MG_OK, MG_ERR_INVALID_ARG, MG_ERR_UNSUPPORTED, MG_ERR_LAUNCH, MG_ERR_TIMEOUT = range(5)
@@ -73,6 +77,7 @@ SYMBOLS = (
     "mg_linear_scan_h0_fwd", "mg_linear_scan_h0_bwd", "mg_linear_scan_varlen_workspace_size",
     "mg_linear_scan_varlen_fwd", "mg_linear_scan_varlen_bwd",
     "mg_affine_scan_h0_fwd", "mg_affine_scan_h0_bwd",
+    "mg_angle_scan_fwd", "mg_angle_scan_bwd",
 )
 
 
@@ -148,6 +153,10 @@ def load():
                                               vp]
         lib.mg_affine_scan_h0_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64,
                                               i32, i32, vp, sz, vp]
+        lib.mg_angle_scan_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i64, i64,
+                                          i64, i32, i32, vp]
+        lib.mg_angle_scan_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, vp,
+                                          vp, vp, i64, i64, i64, i32, i32, vp]
         lib.mg_testing_linear_scan_fwd_stall.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, sz,
                                                          i64, ctypes.c_uint64, vp]
         lib.mg_testing_linear_scan_fwd_stall.restype = st
@@ -163,7 +172,7 @@ def load():
                      "mg_mingru_scan_fwd", "mg_mingru_scan_bwd", "mg_linear_scan_h0_fwd",
                      "mg_linear_scan_h0_bwd", "mg_linear_scan_varlen_fwd",
                      "mg_linear_scan_varlen_bwd", "mg_affine_scan_h0_fwd",
-                     "mg_affine_scan_h0_bwd"):
+                     "mg_affine_scan_h0_bwd", "mg_angle_scan_fwd", "mg_angle_scan_bwd"):
             getattr(lib, name).restype = st
         _lib = lib
     return _lib
@@ -597,6 +606,76 @@ def mg_affine_scan_h0_bwd(A, H0, Abar, Bbar, gAbar, gBbar, *, out=None, ws=None,
     return dA, dB, dH0
 
 
+def _angle_consts(perm, sgn, p2p, R, k):
+    """Host (R, k) arrays for the C ABI: perm, p2p int32, sgn float32 (p2p is
+    the inverse of perm when not given)."""
+    perm = torch.as_tensor(perm).detach().to("cpu", torch.int32).contiguous()
+    sgn = torch.as_tensor(sgn).detach().to("cpu", torch.float32).contiguous()
+    p2p = (torch.argsort(perm, dim=1) if p2p is None else torch.as_tensor(p2p)).detach() \
+        .to("cpu", torch.int32).contiguous()
+    if any(tuple(x.shape) != (R, k) for x in (perm, sgn, p2p)):
+        raise ValueError("perm, sgn and p2p must be (R, k)")
+    return perm, sgn, p2p
+
+
+def mg_angle_scan_fwd(theta, scale, gamma, b, h0, perm, sgn, p2p=None, *, has_scale=1, has_decay=1,
+                      out=None, stream=None):
+    """h (B,T,n,k) of the angle-fused scan (Kernel 4); theta (B,T,n,R,k/2),
+    scale, gamma (B,T,n), b (B,T,n,k), h0 (B,n,k) float32 on the device;
+    perm, sgn, p2p (R,k) module constants (any device; copied to the host)."""
+    theta, b, h0 = _prep(theta, "theta"), _prep(b, "b"), _prep(h0, "h0")
+    if theta.dim() != 5 or b.dim() != 4:
+        raise ValueError("theta must be (B,T,n,R,half) and b (B,T,n,k)")
+    B, T, n, R, half = theta.shape
+    k = 2 * half
+    scale = _prep(scale, "scale") if has_scale else None
+    gamma = _prep(gamma, "gamma") if has_decay else None
+    if tuple(b.shape) != (B, T, n, k) or tuple(h0.shape) != (B, n, k) or any(
+            x is not None and tuple(x.shape) != (B, T, n) for x in (scale, gamma)):
+        raise ValueError("b must be (B,T,n,k), h0 (B,n,k), scale and gamma (B,T,n)")
+    pm, sg, pp = _angle_consts(perm, sgn, p2p, R, k)
+    h = _out(None if out is None else (out,), 0, b.shape, b)
+    sh = _stream_handle(stream, b.device)
+    ptr = lambda x: None if x is None else x.data_ptr()  # noqa: E731
+    _check(load().mg_angle_scan_fwd(theta.data_ptr(), ptr(scale), ptr(gamma), b.data_ptr(),
+                                    h0.data_ptr(), pm.data_ptr(), sg.data_ptr(), pp.data_ptr(),
+                                    int(bool(has_scale)), int(bool(has_decay)), h.data_ptr(), B, T,
+                                    n, R, k, sh),
+           "mg_angle_scan_fwd")
+    return h
+
+
+def mg_angle_scan_bwd(theta, scale, gamma, h0, out_h, grad_out, perm, sgn, p2p=None, *,
+                      has_scale=1, has_decay=1, out=None, stream=None):
+    """(dtheta, dscale, dgamma, db, dh0) of sum(grad_out * h) for the angle
+    scan, from the stored states out_h = h."""
+    theta, h0 = _prep(theta, "theta"), _prep(h0, "h0")
+    out_h, grad_out = _prep(out_h, "out"), _prep(grad_out, "grad_out")
+    B, T, n, R, half = theta.shape
+    k = 2 * half
+    scale = _prep(scale, "scale") if has_scale else None
+    gamma = _prep(gamma, "gamma") if has_decay else None
+    if tuple(out_h.shape) != (B, T, n, k) or grad_out.shape != out_h.shape \
+            or tuple(h0.shape) != (B, n, k):
+        raise ValueError("out, grad_out must be (B,T,n,k) and h0 (B,n,k)")
+    pm, sg, pp = _angle_consts(perm, sgn, p2p, R, k)
+    dth = _out(out, 0, theta.shape, theta)
+    dsc = _out(out, 1, (B, T, n), theta)
+    dga = _out(out, 2, (B, T, n), theta)
+    db = _out(out, 3, out_h.shape, theta)
+    dh0 = _out(out, 4, h0.shape, theta)
+    sh = _stream_handle(stream, theta.device)
+    ptr = lambda x: None if x is None else x.data_ptr()  # noqa: E731
+    _check(load().mg_angle_scan_bwd(theta.data_ptr(), ptr(scale), ptr(gamma), h0.data_ptr(),
+                                    out_h.data_ptr(), grad_out.data_ptr(), pm.data_ptr(),
+                                    sg.data_ptr(), pp.data_ptr(), int(bool(has_scale)),
+                                    int(bool(has_decay)), dth.data_ptr(), dsc.data_ptr(),
+                                    dga.data_ptr(), db.data_ptr(), dh0.data_ptr(), B, T, n, R, k,
+                                    sh),
+           "mg_angle_scan_bwd")
+    return dth, dsc, dga, db, dh0
+
+
 def mg_linear_scan_fwd_noalloc(a, b, *, out=None, stream=None):
     """mg_linear_scan_fwd with the library's static scratch instead of a
     workspace: the C entry point allocates nothing (for callers that cannot
@@ -639,3 +718,5 @@ linear_scan_varlen_fwd = mg_linear_scan_varlen_fwd
 linear_scan_varlen_bwd = mg_linear_scan_varlen_bwd
 affine_scan_h0_fwd = mg_affine_scan_h0_fwd
 affine_scan_h0_bwd = mg_affine_scan_h0_bwd
+angle_scan_fwd = mg_angle_scan_fwd
+angle_scan_bwd = mg_angle_scan_bwd

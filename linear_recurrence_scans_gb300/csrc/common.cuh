@@ -91,6 +91,23 @@ mg_status launch_linear_bwd_bf16_grads(const void *a, mg_dtype dt, const float *
                                        bf16_t *db, int64_t B, int64_t T, int64_t D,
                                        void *ws, size_t ws_bytes, cudaStream_t s,
                                        const LaunchOpts &o);
+// The angle-fused scan's layer tables (filled on the host from perm, sgn and
+// p2p; passed to the kernels by value): per layer and coordinate, the pair
+// index, the role in the pair (0: first), the partner coordinate, the sign.
+constexpr int kAngleMaxR = 8;
+constexpr int kAngleMaxK = 32;
+struct AngleTables {
+    signed char pair[kAngleMaxR][kAngleMaxK];
+    signed char role[kAngleMaxR][kAngleMaxK];
+    signed char partner[kAngleMaxR][kAngleMaxK];
+    float sgn[kAngleMaxR][kAngleMaxK];
+    int R;
+};
+mg_status launch_angle(bool bwd, const float *theta, const float *scale, const float *gamma,
+                       const float *b, const float *h0, const float *out, const float *grad_out,
+                       float *h, float *dtheta, float *dscale, float *dgamma, float *db, float *dh0,
+                       int64_t B, int64_t T, int64_t n, int k, int has_scale, int has_decay,
+                       const AngleTables &tb, cudaStream_t s);
 size_t mingru_ws_bytes(int64_t B, int64_t T, int64_t D);
 mg_status launch_mingru_fwd(const void *x1, const void *x2, mg_dtype dt, float *A, float *Bc,
                             int64_t B, int64_t T, int64_t D, void *ws, size_t ws_bytes,

@@ -446,6 +446,101 @@ mg_status mg_linear_scan_varlen_bwd(const void *a, mg_dtype a_dt, const int64_t 
                              ws_bytes, stream, default_opts());
 }
 
+// perm, sgn, p2p: host (R, k) arrays; every perm[r] a permutation of
+// 0..k-1 and p2p[r] its inverse.  Fills the per-lane tables of the kernels.
+static mg_status angle_tables(const char *fn, const int32_t *perm, const float *sgn,
+                              const int32_t *p2p, int R, int k, AngleTables &tb)
+{
+    if (k != 2 && k != 4 && k != 8 && k != 16 && k != 32)
+        return fail(MG_ERR_UNSUPPORTED, "%s: k = %d outside {2, 4, 8, 16, 32}", fn, k);
+    if (R < 1 || R > kAngleMaxR)
+        return fail(MG_ERR_UNSUPPORTED, "%s: R = %d outside [1, %d]", fn, R, kAngleMaxR);
+    if (perm == nullptr || sgn == nullptr || p2p == nullptr)
+        return fail(MG_ERR_INVALID_ARG, "%s: perm, sgn and p2p are required (host arrays)", fn);
+    memset(&tb, 0, sizeof(tb));
+    tb.R = R;
+    for (int r = 0; r < R; ++r) {
+        bool seen[kAngleMaxK] = {};
+        for (int pos = 0; pos < k; ++pos) {
+            const int j = perm[r * k + pos];
+            if (j < 0 || j >= k || seen[j])
+                return fail(MG_ERR_INVALID_ARG, "%s: perm[%d] is not a permutation of 0..%d", fn, r, k - 1);
+            seen[j] = true;
+            if (p2p[r * k + j] != pos)
+                return fail(MG_ERR_INVALID_ARG, "%s: p2p[%d] is not the inverse of perm[%d]", fn, r, r);
+        }
+        for (int j = 0; j < k; ++j) {
+            const int pos = p2p[r * k + j];
+            tb.pair[r][j] = static_cast<signed char>(pos >> 1);
+            tb.role[r][j] = static_cast<signed char>(pos & 1);
+            tb.partner[r][j] = static_cast<signed char>(perm[r * k + (pos ^ 1)]);
+            tb.sgn[r][j] = sgn[r * k + j];
+        }
+    }
+    return MG_OK;
+}
+
+mg_status mg_angle_scan_fwd(const float *theta, const float *scale, const float *gamma,
+                            const float *b, const float *h0, const int32_t *perm, const float *sgn,
+                            const int32_t *p2p, int has_scale, int has_decay, float *h, int64_t B,
+                            int64_t T, int64_t n, int R, int k, cudaStream_t stream)
+{
+    const char *fn = "mg_angle_scan_fwd";
+    g_detail[0] = 0;
+    AngleTables tb;
+    MG_TRY(angle_tables(fn, perm, sgn, p2p, R, k, tb));
+    MG_TRY(check_dims(fn, {B, T, n, k}));
+    if (B * n > (int64_t(1) << 40) / k) return fail(MG_ERR_UNSUPPORTED, "%s: too many sequences", fn);
+    if (B == 0 || T == 0 || n == 0) return MG_OK;
+    const size_t st = size_t(B) * T * n;
+    MG_TRY(check_bufs(fn, {{theta, st * R * (k / 2) * 4, "theta", false},
+                           {scale, st * 4, "scale", false, !has_scale},
+                           {gamma, st * 4, "gamma", false, !has_decay},
+                           {b, st * k * 4, "b", false},
+                           {h0, size_t(B) * n * k * 4, "h0", false},
+                           {h, st * k * 4, "h", true}}));
+    return launch_angle(false, theta, scale, gamma, b, h0, nullptr, nullptr, h, nullptr, nullptr,
+                        nullptr, nullptr, nullptr, B, T, n, k, has_scale != 0, has_decay != 0, tb,
+                        stream);
+}
+
+mg_status mg_angle_scan_bwd(const float *theta, const float *scale, const float *gamma,
+                            const float *h0, const float *out, const float *grad_out,
+                            const int32_t *perm, const float *sgn, const int32_t *p2p,
+                            int has_scale, int has_decay, float *dtheta, float *dscale,
+                            float *dgamma, float *db, float *dh0, int64_t B, int64_t T, int64_t n,
+                            int R, int k, cudaStream_t stream)
+{
+    const char *fn = "mg_angle_scan_bwd";
+    g_detail[0] = 0;
+    AngleTables tb;
+    MG_TRY(angle_tables(fn, perm, sgn, p2p, R, k, tb));
+    MG_TRY(check_dims(fn, {B, T, n, k}));
+    if (B * n > (int64_t(1) << 40) / k) return fail(MG_ERR_UNSUPPORTED, "%s: too many sequences", fn);
+    if (B == 0 || n == 0) return MG_OK;
+    const size_t nh = size_t(B) * n * k * 4;
+    if (T == 0) {   // L does not depend on h0: its gradient is zero
+        MG_TRY(check_bufs(fn, {{dh0, nh, "dh0", true}}));
+        const cudaError_t e = cudaMemsetAsync(dh0, 0, nh, stream);
+        return e == cudaSuccess ? MG_OK : fail(MG_ERR_LAUNCH, "%s: %s", fn, cudaGetErrorString(e));
+    }
+    const size_t st = size_t(B) * T * n;
+    MG_TRY(check_bufs(fn, {{theta, st * R * (k / 2) * 4, "theta", false},
+                           {scale, st * 4, "scale", false, !has_scale},
+                           {gamma, st * 4, "gamma", false, !has_decay},
+                           {h0, nh, "h0", false},
+                           {out, st * k * 4, "out", false},
+                           {grad_out, st * k * 4, "grad_out", false},
+                           {dtheta, st * R * (k / 2) * 4, "dtheta", true},
+                           {dscale, st * 4, "dscale", true},
+                           {dgamma, st * 4, "dgamma", true},
+                           {db, st * k * 4, "db", true},
+                           {dh0, nh, "dh0", true}}));
+    return launch_angle(true, theta, scale, gamma, nullptr, h0, out, grad_out, nullptr, dtheta,
+                        dscale, dgamma, db, dh0, B, T, n, k, has_scale != 0, has_decay != 0, tb,
+                        stream);
+}
+
 size_t mg_mingru_scan_workspace_size(int64_t B, int64_t T, int64_t D)
 {
     if (B < 0 || T < 0 || D < 0) return 0;

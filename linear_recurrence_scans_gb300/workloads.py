@@ -22,6 +22,8 @@ kernels"):
 * ``mingru_log``       k, x ~ N(0,1); log_coeffs = -softplus(k);
                        log_values[:, 0] = log 0.5,
                        log_values[:, t] = -softplus(-k_{t-1}) + log g(x_{t-1})
+* ``angle_inputs``     theta ~ U(-pi, pi), scale = tanh(N(0,1)), gamma =
+                       exp(-U(0, 0.3)), b, h0 ~ N(0,1), seeded perm/sgn
 * ``haar_affine``      A_t = 0.95 * Q_t, Q_t Haar on O(k) (QR of a float64
                        N(0,1) matrix with the sign fix Q diag(sign diag R));
                        Bm, gAbar, gBbar ~ N(0,1)
@@ -129,6 +131,27 @@ def haar_affine(B: int, T: int, n: int, k: int, v: int, seed: int = 0, device="c
     gAbar = torch.randn((B, T, n, k, k), generator=_gen(seed + 2), dtype=torch.float32).to(device)
     gBbar = torch.randn((B, T, n, k, v), generator=_gen(seed + 3), dtype=torch.float32).to(device)
     return A, Bm, gAbar, gBbar
+
+
+def angle_inputs(B: int, T: int, n: int, R: int, k: int, seed: int = 0, device="cpu",
+                 grads: bool = True):
+    """Inputs of the angle-fused scan: theta (B,T,n,R,k/2) ~ U(-pi, pi);
+    scale = tanh(u), u ~ N(0,1) and gamma = exp(-lambda), lambda ~ U(0, 0.3)
+    (the module's parameterisations), both (B,T,n); b (B,T,n,k), h0 (B,n,k)
+    ~ N(0,1); perm (R,k) int32, one seeded permutation per layer, p2p its
+    inverse, sgn (R,k) float32 in {-1, +1} (CPU arrays, module constants);
+    grad_out (B,T,n,k) ~ N(0,1).  Streams seed .. seed+6 in that order."""
+    th = (torch.rand((B, T, n, R, k // 2), generator=_gen(seed, device), device=device) * 2 - 1) * math.pi
+    scale = torch.tanh(torch.randn((B, T, n), generator=_gen(seed + 1, device), device=device))
+    gamma = torch.exp(-0.3 * torch.rand((B, T, n), generator=_gen(seed + 2, device), device=device))
+    b = torch.randn((B, T, n, k), generator=_gen(seed + 3, device), device=device)
+    h0 = torch.randn((B, n, k), generator=_gen(seed + 4, device), device=device)
+    g = _gen(seed + 5)
+    perm = torch.stack([torch.randperm(k, generator=g) for _ in range(R)]).to(torch.int32)
+    p2p = torch.argsort(perm, dim=1).to(torch.int32)
+    sgn = torch.where(torch.rand((R, k), generator=g) < 0.5, -1.0, 1.0).to(torch.float32)
+    go = torch.randn((B, T, n, k), generator=_gen(seed + 6, device), device=device) if grads else None
+    return th, scale, gamma, b, h0, perm, sgn, p2p, go
 
 
 # The workloads the library is checked and measured on, by name.
