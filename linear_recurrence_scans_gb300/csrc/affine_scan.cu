@@ -1553,51 +1553,45 @@ mg_status bwd_kv(const float *A, const float *Abar, const float *Bbar, const flo
 // The backward from a start state H0 differs from the H0 = 0 one only at the
 // first step (the forward's Bbar, passed in, already carries H0 at every
 // later step): dA_1 gains Lam_1 H0^T (Bbar_0 = H0), and dH0 = A_1^T Lam_1,
-// with Lam_1 = dB_1.  One thread per sequence applies both after the main
+// with Lam_1 = dB_1.  One thread per output element (k*k of dA_1 and k*v of
+// dH0 per sequence), each a dot product of length v or k, after the main
 // backward on the same stream.
 template <int K, int V>
 __global__ void affine_h0_grad_kernel(const float *A, const float *H0, const float *dB, float *dA,
                                       float *dH0, int64_t B, int64_t T, int64_t n)
 {
-    constexpr int KK = K * K, KV = K * V;
+    constexpr int KK = K * K, KV = K * V, PER = KK + KV;
     const int64_t q = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (q >= B * n) return;
-    const int64_t bb = q / n, nn = q % n;
-    const int64_t s1 = (bb * T) * n + nn;   // the first step of the sequence
-    float lam[KV], h0[KV], a1[KK], da[KK], dh[KV];
-    ld_floats<KV>(dB + s1 * KV, lam);
-    ld_floats<KV>(H0 + q * KV, h0);
-    ld_floats<KK>(A + s1 * KK, a1);
-    ld_floats<KK>(dA + s1 * KK, da);
+    if (q >= B * n * PER) return;
+    const int64_t sq = q / PER;          // sequence (b, n)
+    const int e = int(q % PER);
+    const int64_t bb = sq / n, nn = sq % n;
+    const int64_t s1 = (bb * T) * n + nn;   // its first step
+    const float *lam = dB + s1 * KV;
+    if (e < KK) {   // dA_1[i][j] += sum_l Lam_1[i][l] H0[j][l]
+        const int i = e / K, j = e % K;
+        const float *h = H0 + sq * KV;
+        float acc = dA[s1 * KK + e];
 #pragma unroll
-    for (int i = 0; i < K; ++i)
+        for (int l = 0; l < V; ++l) acc = fmaf(lam[i * V + l], h[j * V + l], acc);
+        dA[s1 * KK + e] = acc;
+    } else {        // dH0[i][l] = sum_j A_1[j][i] Lam_1[j][l]
+        const int i = (e - KK) / V, l = (e - KK) % V;
+        const float *a1 = A + s1 * KK;
+        float acc = 0.f;
 #pragma unroll
-        for (int j = 0; j < K; ++j) {
-            float acc = da[i * K + j];
-#pragma unroll
-            for (int l = 0; l < V; ++l) acc = fmaf(lam[i * V + l], h0[j * V + l], acc);
-            da[i * K + j] = acc;
-        }
-#pragma unroll
-    for (int i = 0; i < K; ++i)
-#pragma unroll
-        for (int l = 0; l < V; ++l) {
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < K; ++j) acc = fmaf(a1[j * K + i], lam[j * V + l], acc);
-            dh[i * V + l] = acc;
-        }
-    st_floats<KK>(dA + s1 * KK, da);
-    st_floats<KV>(dH0 + q * KV, dh);
+        for (int j = 0; j < K; ++j) acc = fmaf(a1[j * K + i], lam[j * V + l], acc);
+        dH0[sq * KV + i * V + l] = acc;
+    }
 }
 
 template <int K, int V>
 mg_status h0_grad_kv(const float *A, const float *H0, const float *dB, float *dA, float *dH0,
                      int64_t B, int64_t T, int64_t n, cudaStream_t s)
 {
-    const int64_t nq = B * n;
-    const unsigned blocks = unsigned((nq + 127) / 128);
-    affine_h0_grad_kernel<K, V><<<blocks, 128, 0, s>>>(A, H0, dB, dA, dH0, B, T, n);
+    const int64_t nq = B * n * (K * K + K * V);
+    const unsigned blocks = unsigned((nq + 255) / 256);
+    affine_h0_grad_kernel<K, V><<<blocks, 256, 0, s>>>(A, H0, dB, dA, dH0, B, T, n);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(MG_ERR_LAUNCH, "mg_affine_scan_h0_bwd: launch failed: %s", cudaGetErrorString(e));

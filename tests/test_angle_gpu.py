@@ -2,11 +2,10 @@
 against the float64 oracle's reading of it, through the C ABI (via the
 Python binding).  Outputs start as NaN so an unwritten element fails.
 
-Tolerance.  Every output is a sum of signed terms; the scale of element i is
-the oracle evaluated on the inputs' magnitudes where that bounds the sum
-(db, dh0, h through |A| |h| + |b|), and the RMS over the state's k
-coordinates otherwise (rotations are stable normwise, not entrywise, as for
-the affine outputs)."""
+Tolerance.  The states and their gradients (h, db, dh0) are measured
+against the RMS over the state's k coordinates (rotations are stable
+normwise, not entrywise, as for the affine outputs); dtheta, dscale and
+dgamma against their Cauchy-Schwarz magnitude |factor| |lam_t| |h_{t-1}|."""
 from __future__ import annotations
 
 import numpy as np
@@ -44,12 +43,18 @@ def _case(mg, B, T, n, R, k, seed, has_scale=1, has_decay=1):
                             go.to(DEV), perm, sgn, p2p, has_scale=has_scale, has_decay=has_decay,
                             out=outs)
     ref = oracle.angle_scan_bwd(th, sc, ga, h0, h32, go, perm, sgn, has_scale, has_decay)
-    # scales: dtheta per pair against the RMS of the step's angles' gradients;
-    # dscale, dgamma against |lam| |h|-sized dot products (RMS over time);
-    # db, dh0 against the state RMS
-    S = [_rms_last(ref[0].reshape(*ref[0].shape[:3], -1)).reshape(ref[0].shape),
-         np.broadcast_to(np.sqrt(np.mean(ref[1] ** 2, axis=1, keepdims=True)), ref[1].shape),
-         np.broadcast_to(np.sqrt(np.mean(ref[2] ** 2, axis=1, keepdims=True)), ref[2].shape),
+    # scales: each of dtheta, dscale, dgamma at step t is an inner product of
+    # the gradient carried back from lam_t = db_t with a vector that the
+    # (norm-preserving for sgn = +-1) layers make from h_{t-1}, so by
+    # Cauchy-Schwarz its natural magnitude is |f| |lam_t| |h_{t-1}| with f the
+    # scalar factor in front (s g, g or s); db, dh0 against the state RMS
+    lam = np.linalg.norm(ref[3], axis=-1)                              # (B,T,n)
+    hp = np.concatenate([_np(h0)[:, None], rh[:, :-1]], axis=1)
+    hn = np.linalg.norm(hp, axis=-1)
+    s_ = _np(sc) if has_scale else np.ones_like(lam)
+    g_ = _np(ga) if has_decay else np.ones_like(lam)
+    S = [np.broadcast_to((np.abs(s_ * g_) * lam * hn)[..., None, None], ref[0].shape),
+         np.abs(g_) * lam * hn, np.abs(s_) * lam * hn,
          _rms_last(ref[3]), _rms_last(ref[4])]
     for name, g, r, s in zip(("dtheta", "dscale", "dgamma", "db", "dh0"), got, ref, S):
         errs[name] = scaled_error(_np(g), r, s)
