@@ -426,13 +426,17 @@ def run_e2e(mg, inputs, dev, args, ws_size):
 
 
 def _time_op(fn, iters, dev, flush):
-    """Median CUDA-event time of fn() with an L2 flush before each repetition."""
+    """Median CUDA-event time of fn() with an L2 flush before each repetition:
+    the flush buffer (larger than L2) is written, then read back, so that L2
+    holds neither the op's inputs nor dirty lines whose write-back would be
+    charged to the op."""
     for _ in range(3):
         fn()
     torch.cuda.synchronize(dev)
     ts = []
     for _ in range(iters):
         flush.zero_()
+        flush.sum(dtype=torch.int64)
         s = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
         s.record()

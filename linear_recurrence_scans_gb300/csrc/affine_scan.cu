@@ -15,13 +15,12 @@
 //     streams its steps through a ring of asynchronous copies
 //     (affine_lane_kernel below).  The other small shapes keep the state in
 //     one thread on the generic chunk engine (scan_engine.cuh).
-//   * k in {8, 16}: one warp owns one sequence's sub-chunk of L steps; the
-//     state X = [C | V] (k x (k + w), padded to a multiple of 8 columns) is
-//     split into 4 row blocks x 8 column blocks, one per lane.  Each step
-//     X <- E_C X + [0 | E_V] reads the column strip of X that the lane needs
-//     from a shared copy and the lane's rows of E_C from the warp's ring of
-//     bulk copies (affine_warp_kernel below).  A CTA of NW warps covers NW*L
-//     consecutive steps of one sequence.
+//   * k = 16 with v in {8, 16}: the state on the tensor cores
+//     (affine_mma_kernel below): one warp owns one sequence's sub-chunk of L
+//     steps and holds S = X^T in mma.sync accumulator fragments; a CTA of NW
+//     warps covers NW*L consecutive steps of one sequence.
+//   * the other k in {8, 16}: the same tiles with one lane per column of X
+//     (affine_col_kernel below).
 // Every shape takes part in the same decoupled look-back as the other scans
 // (lookback.cuh).
 #include <type_traits>
@@ -697,36 +696,7 @@ struct LanePlan {
     }
 };
 
-// ============================================================ k in {8, 16}
-
-template <int K_, int W_, bool BWD_, int NW_, int L_, bool DB_, int NSL_>
-struct WCfg {
-    static constexpr int K = K_, W = W_, NW = NW_, L = L_, NSL = NSL_;
-    static constexpr bool BWD = BWD_, DB = DB_;  // DB: double-buffered state exchange
-    static constexpr int VV = BWD ? W - K : W;  // v
-    static constexpr int KK = K * K, KV = K * VV;
-    static constexpr int NC = K + W;            // columns of X = [C | V]
-    static constexpr int NCP = (NC + 7) / 8 * 8;
-    static constexpr int R = K / 4;             // rows per lane (4 row blocks)
-    static constexpr int CC = NCP / 8;          // columns per lane (8 column blocks)
-    static constexpr int XS = NCP;              // shared row stride (floats)
-    static constexpr int MAT = K * XS;          // floats per shared state matrix
-    static constexpr int REC = K * NC;          // floats per global record
-    static constexpr int TC = NW * L;           // steps per tile (L per warp)
-    static constexpr int JD = K / 8;            // dA columns per lane (8 column blocks)
-    // One ring slot holds the inputs of one step.  Forward: A_t, B_t.
-    // Backward: A_{t+1}, gAbar_t, gBbar_t, Abar_{t-1}, Bbar_{t-1}.  Each block
-    // is a multiple of 16 bytes.
-    static constexpr int STEP = BWD ? 3 * KK + 2 * KV : KK + KV;
-    static constexpr int OFF_G = KK, OFF_GB = 2 * KK, OFF_AP = 2 * KK + KV, OFF_BP = 3 * KK + KV;
-    static constexpr int NXB = DB ? 2 : 1;
-    static constexpr int BAR_FLOATS = (NW * NSL * 2 + 3) / 4 * 4;  // mbarriers, 16-byte padded
-    static constexpr size_t SMEM = size_t(BAR_FLOATS + NW * NSL * STEP) * sizeof(float) +
-                                   size_t((NXB + 1) * NW + 1) * MAT * sizeof(float);
-    static_assert(K == 8 || K == 16, "warp kernel is for k in {8, 16}");
-    static_assert(NSL >= 2, "the ring needs two slots at least");
-    static_assert((KV * 4) % 16 == 0 && (KK * 4) % 16 == 0, "bulk copies need 16-byte blocks");
-};
+// ======================================================= shared by k >= 8
 
 struct AffGeom {
     int64_t B, T, n;
@@ -743,187 +713,10 @@ struct AffPtrs {
     float *dA, *dB;                                 // backward outputs
 };
 
-// Lane block of the combine (x earlier, full matrix in shared memory) o
-// (y later, rows `yc` = y.C[rows][0..K) and `yv` = y.V on the lane's columns).
-template <class Cf>
-__device__ __forceinline__ void block_gemm(const float *xs, const float (&yc)[Cf::R][Cf::K],
-                                           const float (&yv)[Cf::R][Cf::CC], int cb,
-                                           float (&o)[Cf::R][Cf::CC])
-{
-#pragma unroll
-    for (int r = 0; r < Cf::R; ++r)
-#pragma unroll
-        for (int c = 0; c < Cf::CC; ++c) o[r][c] = yv[r][c];
-#pragma unroll
-    for (int l = 0; l < Cf::K; ++l) {
-        float xv[Cf::CC];
-        ld_floats<Cf::CC>(xs + l * Cf::XS + cb * Cf::CC, xv);
-#pragma unroll
-        for (int r = 0; r < Cf::R; ++r)
-#pragma unroll
-            for (int c = 0; c < Cf::CC; ++c) o[r][c] = fmaf(yc[r][l], xv[c], o[r][c]);
-    }
-}
-
-// y operand from a matrix stored with row stride `ld` (shared or global):
-// C part = columns 0..K-1, V part on the lane's columns (zero outside [K, NC)).
-template <class Cf, bool GLOBAL>
-__device__ __forceinline__ void load_y(const float *m, int ld, int rb, int cb,
-                                       float (&yc)[Cf::R][Cf::K], float (&yv)[Cf::R][Cf::CC])
-{
-#pragma unroll
-    for (int r = 0; r < Cf::R; ++r) {
-        const float *row = m + (rb * Cf::R + r) * ld;
-#pragma unroll
-        for (int l = 0; l < Cf::K; ++l) yc[r][l] = GLOBAL ? __ldcg(row + l) : row[l];
-#pragma unroll
-        for (int c = 0; c < Cf::CC; ++c) {
-            const int col = cb * Cf::CC + c;
-            yv[r][c] = (col >= Cf::K && col < Cf::NC) ? (GLOBAL ? __ldcg(row + col) : row[col]) : 0.f;
-        }
-    }
-}
-
-// The element held in a ring slot as a y operand.  `has_next`: step t+1
-// exists (the adjoint's coefficient A_{t+1}^T is zero at t = T-1).
-template <class Cf>
-__device__ __forceinline__ void load_elem(const float *slot, bool has_next, int rb, int cb,
-                                          float (&yc)[Cf::R][Cf::K], float (&yv)[Cf::R][Cf::CC])
-{
-    constexpr int K = Cf::K, KK = Cf::KK, VV = Cf::VV, R = Cf::R;
-    if constexpr (!Cf::BWD) {
-        const float *At = slot;
-        const float *Bt = slot + KK;
-#pragma unroll
-        for (int r = 0; r < R; ++r) ld_floats<K>(At + (rb * R + r) * K, yc[r]);
-        if constexpr (K % Cf::CC == 0 && VV % Cf::CC == 0) {
-            // a lane's columns lie wholly in the C part (zero) or in B_t
-            const int col = cb * Cf::CC;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                if (col >= K) {
-                    ld_floats<Cf::CC>(Bt + (rb * R + r) * VV + col - K, yv[r]);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < Cf::CC; ++c) yv[r][c] = 0.f;
-                }
-            }
-        } else {
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int c = 0; c < Cf::CC; ++c) {
-                    const int col = cb * Cf::CC + c;
-                    yv[r][c] = (col >= K && col < Cf::NC) ? Bt[(rb * R + r) * VV + col - K] : 0.f;
-                }
-        }
-    } else {
-        const float *An = slot;
-        const float *ga = slot + Cf::OFF_G;
-        const float *gb = slot + Cf::OFF_GB;
-        if (has_next) {  // E_C[row][l] = A_{t+1}[l][row]
-#pragma unroll
-            for (int l = 0; l < K; ++l) {
-                float a[R];
-                ld_floats<R>(An + l * K + rb * R, a);
-#pragma unroll
-                for (int r = 0; r < R; ++r) yc[r][l] = a[r];
-            }
-        } else {
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int l = 0; l < K; ++l) yc[r][l] = 0.f;
-        }
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int c = 0; c < Cf::CC; ++c) {
-                const int col = cb * Cf::CC + c, row = rb * R + r;
-                float x = 0.f;
-                if (col >= K && col < 2 * K) x = ga[row * K + col - K];
-                else if (col >= 2 * K && col < Cf::NC) x = gb[row * VV + col - 2 * K];
-                yv[r][c] = x;
-            }
-    }
-}
-
-template <class Cf>
-__device__ __forceinline__ void identity_block(int rb, int cb, float (&o)[Cf::R][Cf::CC])
-{
-#pragma unroll
-    for (int r = 0; r < Cf::R; ++r)
-#pragma unroll
-        for (int c = 0; c < Cf::CC; ++c) o[r][c] = (rb * Cf::R + r == cb * Cf::CC + c) ? 1.f : 0.f;
-}
-
-template <class Cf>
-__device__ __forceinline__ void put_block_smem(float *xs, int rb, int cb,
-                                               const float (&o)[Cf::R][Cf::CC])
-{
-#pragma unroll
-    for (int r = 0; r < Cf::R; ++r) st_floats<Cf::CC>(xs + (rb * Cf::R + r) * Cf::XS + cb * Cf::CC, o[r]);
-}
-
-template <class Cf>
-__device__ __forceinline__ void put_block_record(float *rec, int rb, int cb,
-                                                 const float (&o)[Cf::R][Cf::CC])
-{
-#pragma unroll
-    for (int r = 0; r < Cf::R; ++r)
-#pragma unroll
-        for (int c = 0; c < Cf::CC; ++c) {
-            const int col = cb * Cf::CC + c;
-            if (col < Cf::NC) __stcg(rec + (rb * Cf::R + r) * Cf::NC + col, o[r][c]);
-        }
-}
-
-template <class Cf>
-__device__ __forceinline__ void get_block_record(const float *rec, int rb, int cb,
-                                                 float (&o)[Cf::R][Cf::CC])
-{
-#pragma unroll
-    for (int r = 0; r < Cf::R; ++r)
-#pragma unroll
-        for (int c = 0; c < Cf::CC; ++c) {
-            const int col = cb * Cf::CC + c;
-            o[r][c] = col < Cf::NC ? __ldcg(rec + (rb * Cf::R + r) * Cf::NC + col) : 0.f;
-        }
-}
-
-// One step of a warp's scan: o <- E o X + [0 | E_V] with X read from the warp's
-// shared state buffer(s), then the new X written back.  `cur` selects the
-// buffer holding X (double-buffered) and is advanced.
-template <class Cf>
-__device__ __forceinline__ void warp_step(float *xw, int &cur, const float (&yc)[Cf::R][Cf::K],
-                                          const float (&yv)[Cf::R][Cf::CC], int rb, int cb,
-                                          float (&o)[Cf::R][Cf::CC])
-{
-    if constexpr (Cf::DB) {
-        block_gemm<Cf>(xw + cur * Cf::MAT, yc, yv, cb, o);
-        cur ^= 1;
-        put_block_smem<Cf>(xw + cur * Cf::MAT, rb, cb, o);
-        __syncwarp();
-    } else {
-        block_gemm<Cf>(xw, yc, yv, cb, o);
-        __syncwarp();
-        put_block_smem<Cf>(xw, rb, cb, o);
-        __syncwarp();
-    }
-}
-
-// ------------------------------------------------ dA_t on the tensor cores
-// dA_t = Xv Y^T with Xv = [M_t | Lam_t] (16 x W) and Y = [Abar_{t-1} |
-// Bbar_{t-1}] (16 x W), W = 16 + v: an independent product per step (no
-// recurrence runs through it), done as mma.sync.m16n8k8 tf32 tiles (M = 16,
-// N = 16, K = W).  Each fp32 operand is split into a tf32 high part and a
-// tf32 remainder and the products hi*hi, hi*lo, lo*hi are accumulated in
-// fp32: the dropped lo*lo term is below 2^-22 of each product.
-
-#ifndef MG_AFW_MMA_DA
-#define MG_AFW_MMA_DA 1
-#endif
-
+// 3xTF32 products on the tensor cores: each fp32 operand is split into a
+// tf32 high part and a tf32 remainder, and hi*hi, hi*lo, lo*hi are
+// accumulated in fp32 (the dropped lo*lo term is below 2^-22 of each
+// product).
 __device__ __forceinline__ void split_tf32(float x, unsigned &hi, unsigned &lo)
 {
     unsigned h, l;
@@ -944,61 +737,209 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const unsigned (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// xs: X rows with stride XS (Xv = columns 16 .. 16+W-1); ap, bp: Abar_{t-1}
-// (16 x 16) and Bbar_{t-1} (16 x V) row-major; writes dA (16 x 16) at `out`.
-template <int XS, int V>
-__device__ __forceinline__ void mma_dA16(const float *xs, const float *ap, const float *bp,
-                                         int lane, float *out)
+// ============================================= k in {8, 16}: column lanes
+// One warp owns one sequence's sub-chunk of L steps, and lane l owns columns
+// l, l + 32, ... of the state X = [C | V] (k rows, NC columns).  A step
+// X <- E_C X + [0 | E_V] is, for each of the lane's columns, k dot products
+// of the rows of E_C with that column: the rows are read by all 32 lanes at
+// once from shared memory (broadcast loads, one address per load), the
+// column never leaves the lane's registers, and E_V's entries for the
+// column are the lane's own.  No state is exchanged between lanes, so the
+// only chain from step to step is the lane's k independent dot products.
+// The steps reach shared memory through each warp's ring of bulk copies
+// (one mbarrier per slot), as in the kernels above.  A CTA of NW warps covers
+// NW*L consecutive steps of one sequence.
+// Forward: X = [Abar | Bbar] (NC = k + v).  Backward: X = [C | M | Lam]
+// (NC = 2k + v) in pass 1; pass 2 needs only the value part [M | Lam]
+// (W = k + v columns), whose C columns feed nothing but the aggregates.
+template <int K_, int V_, bool BWD_, int NW_, int L_, int NSL_>
+struct CCfg {
+    static constexpr int K = K_, VV = V_, NW = NW_, L = L_, NSL = NSL_;
+    static constexpr bool BWD = BWD_;
+    static constexpr int KK = K * K, KV = K * VV;
+    static constexpr int W = BWD ? K + VV : VV;     // columns of the value part
+    static constexpr int NC = K + W;                // columns of X
+    static constexpr int NCP = (NC + 3) / 4 * 4;    // row stride of stored matrices
+    static constexpr int CPL = (NC + 31) / 32;      // columns per lane, all of X
+    static constexpr int CPL2 = (W + 31) / 32;      // columns per lane, value part
+    static constexpr int MAT = K * NCP;             // floats per stored matrix
+    static constexpr int REC = MAT;                 // floats per global record
+    static constexpr int TC = NW * L;               // steps per tile
+    // Ring slot contents.  Forward: A_t, B_t.  Backward: A_{t+1}, gAbar_t,
+    // gBbar_t, Abar_{t-1}, Bbar_{t-1}.  Each block is a multiple of 16 bytes.
+    static constexpr int STEP = BWD ? 3 * KK + 2 * KV : KK + KV;
+    static constexpr int OFF_G = KK, OFF_GB = 2 * KK, OFF_AP = 2 * KK + KV, OFF_BP = 3 * KK + KV;
+    // The backward stages [M | Lam] of each step in shared memory for dA_t:
+    // row stride XS keeps the tensor-core fragment loads free of conflicts.
+    static constexpr int XS = (W + 3) / 4 * 4 + 4;
+    static constexpr int XMAT = BWD ? K * XS : 0;
+    static constexpr int BAR_FLOATS = (NW * NSL * 2 + 3) / 4 * 4;
+    static constexpr size_t SMEM =
+        size_t(BAR_FLOATS + NW * NSL * STEP + (NW + 1) * MAT + NW * XMAT) * sizeof(float);
+    static_assert(K == 8 || K == 16, "column kernel is for k in {8, 16}");
+    static_assert(NSL >= 2, "the ring needs two slots at least");
+    static_assert((KV * 4) % 16 == 0 && (KK * 4) % 16 == 0, "bulk copies need 16-byte blocks");
+    static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+};
+
+// The lane's columns COFF + lane + 32 j (j < CN) of a matrix stored with row
+// stride Cf::NCP, in shared (GLOBAL false) or global memory; columns at or
+// past NC read as zero.
+template <class Cf, int COFF, int CN, bool GLOBAL>
+__device__ __forceinline__ void col_get(const float *m, int lane, float (&x)[CN][Cf::K])
 {
-    constexpr int W = 16 + V, NKT = W / 8;
-    const int g = lane >> 2, q = lane & 3;
-    float d[2][4] = {};
 #pragma unroll
-    for (int kt = 0; kt < NKT; ++kt) {
-        unsigned ah[4], al[4];
+    for (int j = 0; j < CN; ++j) {
+        const int col = COFF + lane + 32 * j;
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            split_tf32(xs[(g + 8 * (e & 1)) * XS + 16 + 8 * kt + q + 4 * (e >> 1)], ah[e], al[e]);
+        for (int i = 0; i < Cf::K; ++i) {
+            const float *a = m + i * Cf::NCP + col;
+            x[j][i] = col < Cf::NC ? (GLOBAL ? __ldcg(a) : *a) : 0.f;
+        }
+    }
+}
+
+template <class Cf, int COFF, int CN, bool GLOBAL>
+__device__ __forceinline__ void col_put(float *m, int lane, const float (&x)[CN][Cf::K])
+{
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            unsigned bh[2], bl[2];
+    for (int j = 0; j < CN; ++j) {
+        const int col = COFF + lane + 32 * j;
+        if (col < Cf::NC) {
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {  // B[k][n] = Y[n][k]
-                const int n = 8 * nt + g, k = 8 * kt + q + 4 * e;
-                split_tf32(k < 16 ? ap[n * 16 + k] : bp[n * V + k - 16], bh[e], bl[e]);
+            for (int i = 0; i < Cf::K; ++i) {
+                if (GLOBAL) __stcg(m + i * Cf::NCP + col, x[j][i]);
+                else m[i * Cf::NCP + col] = x[j][i];
             }
-            mma_tf32(d[nt], al, bh[0], bh[1]);
-            mma_tf32(d[nt], ah, bl[0], bl[1]);
-            mma_tf32(d[nt], ah, bh[0], bh[1]);
+        }
+    }
+}
+
+// Columns of the identity element [I | 0].
+template <class Cf, int COFF, int CN>
+__device__ __forceinline__ void col_identity(int lane, float (&x)[CN][Cf::K])
+{
+#pragma unroll
+    for (int j = 0; j < CN; ++j) {
+        const int col = COFF + lane + 32 * j;
+#pragma unroll
+        for (int i = 0; i < Cf::K; ++i) x[j][i] = (i == col) ? 1.f : 0.f;
+    }
+}
+
+// x <- E_C x + E[:, col] (col >= K) for a stored element E = [E_C | E_V]
+// (row stride NCP): the combine (x earlier) o (E later).
+template <class Cf, int COFF, int CN, bool GLOBAL>
+__device__ __forceinline__ void col_apply(const float *E, int lane, float (&x)[CN][Cf::K])
+{
+    constexpr int K = Cf::K;
+    float y[CN][K];
+#pragma unroll
+    for (int j = 0; j < CN; ++j) {
+        const int col = COFF + lane + 32 * j;
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            const float *a = E + i * Cf::NCP + col;
+            y[j][i] = (col >= K && col < Cf::NC) ? (GLOBAL ? __ldcg(a) : *a) : 0.f;
         }
     }
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int i = 0; i < K; ++i) {
+        float e[K];
+        if (GLOBAL) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-            *reinterpret_cast<float2 *>(out + (g + 8 * h) * 16 + 8 * nt + 2 * q) =
-                make_float2(d[nt][2 * h], d[nt][2 * h + 1]);
+            for (int l = 0; l < K; l += 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(E + i * Cf::NCP + l));
+                e[l] = v.x;
+                e[l + 1] = v.y;
+                e[l + 2] = v.z;
+                e[l + 3] = v.w;
+            }
+        } else {
+            ld_floats<K>(E + i * Cf::NCP, e);
+        }
+#pragma unroll
+        for (int j = 0; j < CN; ++j)
+#pragma unroll
+            for (int l = 0; l < K; ++l) y[j][i] = fmaf(e[l], x[j][l], y[j][i]);
+    }
+#pragma unroll
+    for (int j = 0; j < CN; ++j)
+#pragma unroll
+        for (int i = 0; i < K; ++i) x[j][i] = y[j][i];
 }
 
-// One tile = one sequence x TC steps, warp w owning L consecutive steps.
-// Each warp streams its steps through its own ring of NSL slots (1D bulk
-// copies completing on one mbarrier per slot): pass 1 folds them into the
-// warp's aggregate, pass 2 streams them again (now from L2) and writes the
-// outputs.  Both passes form one issue sequence, so the first loads of pass 2
-// are in flight while warp 0 does the look-back.
+// Forward step from a ring slot: x <- A_t x + [0 | B_t] on the lane's column.
+template <class Cf>
+__device__ __forceinline__ void col_step_fwd(const float *slot, int lane, float (&x)[1][Cf::K])
+{
+    constexpr int K = Cf::K, VV = Cf::VV;
+    const int col = lane;
+    float y[K];
+#pragma unroll
+    for (int i = 0; i < K; ++i)
+        y[i] = (col >= K && col < Cf::NC) ? slot[Cf::KK + i * VV + col - K] : 0.f;
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+        float e[K];
+        ld_floats<K>(slot + i * K, e);
+#pragma unroll
+        for (int l = 0; l < K; ++l) y[i] = fmaf(e[l], x[0][l], y[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < K; ++i) x[0][i] = y[i];
+}
+
+// Backward step from a ring slot on columns COFF + lane + 32 j of X = [C | M |
+// Lam]: x <- A_{t+1}^T x + [0 | gAbar_t | gBbar_t] (the first term absent at
+// t = T-1).  Row l of A_{t+1} is read once and scattered over the k sums.
+template <class Cf, int COFF, int CN>
+__device__ __forceinline__ void col_step_bwd(const float *slot, bool has_next, int lane,
+                                             float (&x)[CN][Cf::K])
+{
+    constexpr int K = Cf::K, VV = Cf::VV;
+    float y[CN][K];
+#pragma unroll
+    for (int j = 0; j < CN; ++j) {
+        const int col = COFF + lane + 32 * j;
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            float v = 0.f;
+            if (col >= K && col < 2 * K) v = slot[Cf::OFF_G + i * K + col - K];
+            else if (col >= 2 * K && col < Cf::NC) v = slot[Cf::OFF_GB + i * VV + col - 2 * K];
+            y[j][i] = v;
+        }
+    }
+    if (has_next) {
+#pragma unroll
+        for (int l = 0; l < K; ++l) {
+            float e[K];
+            ld_floats<K>(slot + l * K, e);
+#pragma unroll
+            for (int j = 0; j < CN; ++j)
+#pragma unroll
+                for (int i = 0; i < K; ++i) y[j][i] = fmaf(e[i], x[j][l], y[j][i]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < CN; ++j)
+#pragma unroll
+        for (int i = 0; i < K; ++i) x[j][i] = y[j][i];
+}
+
 template <class Cf>
 __global__ void __launch_bounds__(Cf::NW * 32)
-    affine_warp_kernel(const AffPtrs p, const AffGeom g, const Lookback lb)
+    affine_col_kernel(const AffPtrs p, const AffGeom g, const Lookback lb)
 {
-    constexpr int K = Cf::K, R = Cf::R, CC = Cf::CC, NW = Cf::NW, L = Cf::L, MAT = Cf::MAT;
-    constexpr int XS = Cf::XS, NC = Cf::NC, VV = Cf::VV, KK = Cf::KK, KV = Cf::KV;
-    constexpr int NSL = Cf::NSL, STEP = Cf::STEP;
+    constexpr int K = Cf::K, NW = Cf::NW, L = Cf::L, NSL = Cf::NSL, STEP = Cf::STEP;
+    constexpr int KK = Cf::KK, KV = Cf::KV, VV = Cf::VV, NC = Cf::NC, MAT = Cf::MAT;
+    constexpr int CPL = Cf::CPL, CPL2 = Cf::CPL2, XS = Cf::XS;
     extern __shared__ float4 aff_smem[];
     unsigned long long *const bars = reinterpret_cast<unsigned long long *>(aff_smem);  // [NW][NSL]
     float *const ring = reinterpret_cast<float *>(aff_smem) + Cf::BAR_FLOATS;          // [NW][NSL][STEP]
-    float *const xb = ring + NW * NSL * STEP;                                          // [NW][NXB][MAT]
-    float *const G = xb + NW * Cf::NXB * MAT;                                          // [NW][MAT]
-    float *const carry = G + NW * MAT;                                                 // [MAT]
+    float *const G = ring + NW * NSL * STEP;   // [NW][MAT]: warp aggregates, then inclusive
+    float *const carry = G + NW * MAT;         // [MAT]
+    float *const xst = carry + MAT;            // [NW][XMAT] (backward)
 
     unsigned tile;
     unsigned long long epoch;
@@ -1012,26 +953,21 @@ __global__ void __launch_bounds__(Cf::NW * 32)
     const int j = int(tile % unsigned(g.nJ));
     const int64_t bb = j / g.n, nn = j % g.n;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rb = lane >> 3, cb = lane & 7;
     const int ct = Cf::BWD ? (g.nC - 1 - c) : c;
-    const int64_t t0 = int64_t(ct) * Cf::TC;        // first step of the tile
-    const int nv = int(g.T - t0 < Cf::TC ? g.T - t0 : Cf::TC);  // valid steps in the tile
-    const int wbase = warp * L;                     // first tile step of this warp
-    const int nvw = nv - wbase < 0 ? 0 : (nv - wbase < L ? nv - wbase : L);  // its valid steps
-    const int pw = Cf::BWD ? NW - 1 - warp : warp;  // position in processing order
-    float *const xw = xb + warp * Cf::NXB * MAT;
+    const int64_t t0 = int64_t(ct) * Cf::TC;
+    const int nv = int(g.T - t0 < Cf::TC ? g.T - t0 : Cf::TC);
+    const int wbase = warp * L;
+    const int nvw = nv - wbase < 0 ? 0 : (nv - wbase < L ? nv - wbase : L);
+    const int pw = Cf::BWD ? NW - 1 - warp : warp;
     unsigned long long *const wbar = bars + warp * NSL;
     float *const wring = ring + warp * NSL * STEP;
     auto step_index = [&](int64_t t) { return (bb * g.T + t) * g.n + nn; };
-    // issue-sequence entry q: pass 1 for q < nvw, pass 2 after; the tile step
-    // in processing order (reverse time for the adjoint)
     auto tile_step = [&](int q) {
         const int k = q < nvw ? q : q - nvw;
         return Cf::BWD ? wbase + nvw - 1 - k : wbase + k;
     };
     const int nq = 2 * nvw;
 
-    // lane 0 of each warp: arm slot q % NSL and start its copies
     auto issue = [&](int q) {
         if (q >= nq) return;
         unsigned long long *bar = wbar + q % NSL;
@@ -1053,8 +989,6 @@ __global__ void __launch_bounds__(Cf::NW * 32)
             }
         }
     };
-    // every lane: wait for entry q (bounded; a second bounded wait after a
-    // timeout lets the copies land before the slot is reused or the CTA ends)
     auto wait_slot = [&](int q) -> const float * {
         unsigned long long *bar = wbar + q % NSL;
         const unsigned parity = unsigned(q / NSL) & 1u;
@@ -1064,304 +998,173 @@ __global__ void __launch_bounds__(Cf::NW * 32)
         }
         return wring + (q % NSL) * STEP;
     };
+    // refill slot q % NSL once every lane has used entry q - NSL (each lane's
+    // loads of it have been consumed by its arithmetic before the __syncwarp)
+    auto refill = [&](int q) {
+        __syncwarp();
+        if (lane == 0) issue(q);
+    };
 
     if (lane == 0) {
         for (int q = 0; q < NSL; ++q) mbar_init(wbar + q, 1);
         for (int q = 0; q < NSL; ++q) issue(q);
     }
     __syncwarp();
-    auto refill = [&](int q) {  // after every lane has read entry q - NSL
-        if (lane == 0) issue(q);
-    };
 
-    float yc[R][K], yv[R][CC], o[R][CC];
-
-    // ---- pass 1: aggregate of the warp's steps, in processing order
-    int cur = 0;
+    // ---- pass 1: aggregate of the warp's steps (all NC columns)
     {
-        identity_block<Cf>(rb, cb, o);
-        put_block_smem<Cf>(xw, rb, cb, o);
-        __syncwarp();
+        float x[CPL][K];
+        col_identity<Cf, 0, CPL>(lane, x);
 #pragma unroll 1
         for (int q = 0; q < nvw; ++q) {
             const int64_t t = t0 + tile_step(q);
             const float *slot = wait_slot(q);
-            load_elem<Cf>(slot, t + 1 < g.T, rb, cb, yc, yv);
-            __syncwarp();  // every lane has read the slot
+            if constexpr (!Cf::BWD) col_step_fwd<Cf>(slot, lane, x);
+            else col_step_bwd<Cf, 0, CPL>(slot, t + 1 < g.T, lane, x);
             refill(q + NSL);
-            warp_step<Cf>(xw, cur, yc, yv, rb, cb, o);
         }
-        put_block_smem<Cf>(G + pw * MAT, rb, cb, o);
+        col_put<Cf, 0, CPL, false>(G + pw * MAT, lane, x);
     }
     __syncthreads();
 
     // ---- warp 0: inclusive prefixes over the warps (processing order), then
     //      the look-back for the tile's carry-in
     if (warp == 0) {
+        float x[CPL][K];
+        col_get<Cf, 0, CPL, false>(G, lane, x);
         for (int w = 1; w < NW; ++w) {  // G[w] <- G[w-1] o G[w]
-            load_y<Cf, false>(G + w * MAT, XS, rb, cb, yc, yv);
-            block_gemm<Cf>(G + (w - 1) * MAT, yc, yv, cb, o);
+            col_apply<Cf, 0, CPL, false>(G + w * MAT, lane, x);
             __syncwarp();
-            put_block_smem<Cf>(G + w * MAT, rb, cb, o);
-            __syncwarp();
+            col_put<Cf, 0, CPL, false>(G + w * MAT, lane, x);
         }
+        __syncwarp();
         const float *cta = G + (NW - 1) * MAT;
         const size_t slot = size_t(c) * g.nJ + j;
         float *rec_agg = lb.data + slot * 2 * Cf::REC;
         float *rec_pre = rec_agg + Cf::REC;
-        float cblk[R][CC];
-#pragma unroll
-        for (int r = 0; r < R; ++r) ld_floats<CC>(cta + (rb * R + r) * XS + cb * CC, cblk[r]);
+        float xc[CPL][K];
         if (c == 0) {
             if (!Cf::BWD && p.H0 != nullptr) {
                 // carry = the start state [I | H0]; prefix = carry o cta
                 const float *h0 = p.H0 + (bb * g.n + nn) * KV;
 #pragma unroll
-                for (int r = 0; r < R; ++r)
+                for (int jj = 0; jj < CPL; ++jj) {
+                    const int col = lane + 32 * jj;
 #pragma unroll
-                    for (int cc = 0; cc < CC; ++cc) {
-                        const int row = rb * R + r, col = cb * CC + cc;
-                        o[r][cc] = col < K ? (row == col ? 1.f : 0.f)
-                                           : (col < NC ? h0[row * VV + col - K] : 0.f);
-                    }
-                put_block_smem<Cf>(carry, rb, cb, o);
-                __syncwarp();
-                load_y<Cf, false>(cta, XS, rb, cb, yc, yv);
-                block_gemm<Cf>(carry, yc, yv, cb, o);
-                put_block_record<Cf>(rec_pre, rb, cb, o);
-                publish(lb, slot, kStatusPrefix, epoch, tile);
+                    for (int i = 0; i < K; ++i)
+                        xc[jj][i] = col < K ? (i == col ? 1.f : 0.f)
+                                            : (col < NC ? h0[i * VV + col - K] : 0.f);
+                }
+                col_put<Cf, 0, CPL, false>(carry, lane, xc);
+                col_apply<Cf, 0, CPL, false>(cta, lane, xc);
+                col_put<Cf, 0, CPL, true>(rec_pre, lane, xc);
             } else {
-                put_block_record<Cf>(rec_pre, rb, cb, cblk);
-                publish(lb, slot, kStatusPrefix, epoch, tile);
-                identity_block<Cf>(rb, cb, o);
-                put_block_smem<Cf>(carry, rb, cb, o);
+                col_put<Cf, 0, CPL, true>(rec_pre, lane, x);
+                col_identity<Cf, 0, CPL>(lane, xc);
+                col_put<Cf, 0, CPL, false>(carry, lane, xc);
             }
+            publish(lb, slot, kStatusPrefix, epoch, tile);
         } else {
             if (peek_status(lb, slot - g.nJ, epoch) != kStatusPrefix) {
-                put_block_record<Cf>(rec_agg, rb, cb, cblk);
+                col_put<Cf, 0, CPL, true>(rec_agg, lane, x);
                 publish(lb, slot, kStatusAggregate, epoch, tile);
             }
             const int pp = wait_window(lb, size_t(j), size_t(g.nJ), c, epoch, tile);
             if (pp >= 0) {
-                get_block_record<Cf>(lb.data + (size_t(pp) * g.nJ + j) * 2 * Cf::REC + Cf::REC, rb,
-                                     cb, o);
+                col_get<Cf, 0, CPL, true>(lb.data + (size_t(pp) * g.nJ + j) * 2 * Cf::REC + Cf::REC,
+                                          lane, xc);
+                for (int q = pp + 1; q < c; ++q)  // carry <- carry o agg(q)
+                    col_apply<Cf, 0, CPL, true>(lb.data + (size_t(q) * g.nJ + j) * 2 * Cf::REC,
+                                                lane, xc);
             } else {
-                identity_block<Cf>(rb, cb, o);
+                col_identity<Cf, 0, CPL>(lane, xc);
             }
-            put_block_smem<Cf>(carry, rb, cb, o);
-            __syncwarp();
-            if (pp >= 0) {
-                for (int q = pp + 1; q < c; ++q) {  // carry <- carry o agg(q)
-                    load_y<Cf, true>(lb.data + (size_t(q) * g.nJ + j) * 2 * Cf::REC, NC, rb, cb,
-                                     yc, yv);
-                    block_gemm<Cf>(carry, yc, yv, cb, o);
-                    __syncwarp();
-                    put_block_smem<Cf>(carry, rb, cb, o);
-                    __syncwarp();
-                }
-            }
-            // prefix of this tile = carry o cta
-            load_y<Cf, false>(cta, XS, rb, cb, yc, yv);
-            block_gemm<Cf>(carry, yc, yv, cb, o);
-            put_block_record<Cf>(rec_pre, rb, cb, o);
+            col_put<Cf, 0, CPL, false>(carry, lane, xc);
+            col_apply<Cf, 0, CPL, false>(cta, lane, xc);  // prefix of this tile
+            col_put<Cf, 0, CPL, true>(rec_pre, lane, xc);
             publish(lb, slot, kStatusPrefix, epoch, tile);
         }
     }
     __syncthreads();
 
-    // ---- start state of this warp: carry o G[pw-1]
-    if (pw == 0) {
-#pragma unroll
-        for (int r = 0; r < R; ++r) ld_floats<CC>(carry + (rb * R + r) * XS + cb * CC, o[r]);
-    } else {
-        load_y<Cf, false>(G + (pw - 1) * MAT, XS, rb, cb, yc, yv);
-        block_gemm<Cf>(carry, yc, yv, cb, o);
-    }
-    cur = 0;
-    put_block_smem<Cf>(xw, rb, cb, o);
-    __syncwarp();
-
-    // ---- pass 2 of the k = 16 adjoint on [M | Lam] only: the running
-    //      product C (the first 16 columns of X) feeds the aggregates of pass
-    //      1 and no output, so pass 2 updates the W = 16 + v columns after it
-    //      with C2 = W / 8 columns per lane.
-    if constexpr (Cf::BWD && K == 16 && (K + VV) % 8 == 0 && MG_AFW_MMA_DA != 0) {
-        constexpr int C2 = (K + VV) / 8, WV = K + VV;
+    if constexpr (!Cf::BWD) {
+        // ---- pass 2: re-run the warp's steps from its start state carry o
+        //      G[pw-1] and write Abar_t, Bbar_t
+        float x[1][K];
+        col_get<Cf, 0, 1, false>(carry, lane, x);
+        if (pw > 0) col_apply<Cf, 0, 1, false>(G + (pw - 1) * MAT, lane, x);
+        const int col = lane;
 #pragma unroll 1
         for (int q = nvw; q < nq; ++q) {
             const int64_t t = t0 + tile_step(q), s = step_index(t);
             const float *slot = wait_slot(q);
-            // E rows (A_{t+1}^T) as in the full step; values [gA | gB] on the lane's columns
-            if (t + 1 < g.T) {
+            col_step_fwd<Cf>(slot, lane, x);
+            refill(q + NSL);
+            if (col < K) {
+                float *o = p.Abar_out + s * KK + col;
 #pragma unroll
-                for (int l = 0; l < K; ++l) {
-                    float a[R];
-                    ld_floats<R>(slot + l * K + rb * R, a);
+                for (int i = 0; i < K; ++i) o[i * K] = x[0][i];
+            } else if (col < NC) {
+                float *o = p.Bbar_out + s * KV + col - K;
 #pragma unroll
-                    for (int r = 0; r < R; ++r) yc[r][l] = a[r];
-                }
-            } else {
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-#pragma unroll
-                    for (int l = 0; l < K; ++l) yc[r][l] = 0.f;
+                for (int i = 0; i < K; ++i) o[i * VV] = x[0][i];
             }
-            float y2[R][C2], o2[R][C2];
-            const int col0 = cb * C2;  // in [M | Lam]
+        }
+    } else {
+        // ---- pass 2 of the adjoint on the value part [M | Lam]: dB_t = Lam_t,
+        //      dA_t = [M_t | Lam_t] [Abar_{t-1} | Bbar_{t-1}]^T
+        float x[CPL2][K];
+        col_get<Cf, K, CPL2, false>(carry, lane, x);
+        if (pw > 0) col_apply<Cf, K, CPL2, false>(G + (pw - 1) * MAT, lane, x);
+        float *const xw = xst + warp * Cf::XMAT;   // [M | Lam] of the current step
+#pragma unroll 1
+        for (int q = nvw; q < nq; ++q) {
+            const int64_t t = t0 + tile_step(q), s = step_index(t);
+            const float *slot = wait_slot(q);
+            col_step_bwd<Cf, K, CPL2>(slot, t + 1 < g.T, lane, x);
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int row = rb * R + r;
-                if constexpr (C2 == 4) {
-                    if (col0 < K) ld_floats<4>(slot + Cf::OFF_G + row * K + col0, y2[r]);
-                    else ld_floats<4>(slot + Cf::OFF_GB + row * VV + col0 - K, y2[r]);
-                } else {
+            for (int jj = 0; jj < CPL2; ++jj) {
+                const int c2 = lane + 32 * jj;   // column of [M | Lam]
+                if (c2 < Cf::W) {
 #pragma unroll
-                    for (int c = 0; c < C2; ++c) {
-                        const int j = col0 + c;
-                        y2[r][c] = j < K ? slot[Cf::OFF_G + row * K + j] : slot[Cf::OFF_GB + row * VV + j - K];
+                    for (int i = 0; i < K; ++i) xw[i * XS + c2] = x[jj][i];
+                    if (c2 >= K) {
+                        float *o = p.dB + s * KV + c2 - K;
+#pragma unroll
+                        for (int i = 0; i < K; ++i) o[i * VV] = x[jj][i];
                     }
                 }
             }
-            // o2 = E [M | Lam] + [gA | gB] on the lane's block
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int c = 0; c < C2; ++c) o2[r][c] = y2[r][c];
-#pragma unroll
-            for (int l = 0; l < K; ++l) {
-                float xv[C2];
-                ld_floats<C2>(xw + l * XS + K + col0, xv);
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-#pragma unroll
-                    for (int c = 0; c < C2; ++c) o2[r][c] = fmaf(yc[r][l], xv[c], o2[r][c]);
-            }
-            __syncwarp();  // every lane has read X
-#pragma unroll
-            for (int r = 0; r < R; ++r) st_floats<C2>(xw + (rb * R + r) * XS + K + col0, o2[r]);
             __syncwarp();
-            // dB_t = Lam_t
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int row = rb * R + r;
-                if constexpr (C2 == 4) {
-                    if (col0 >= K) st_floats<4>(p.dB + s * KV + row * VV + col0 - K, o2[r]);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < C2; ++c)
-                        if (col0 + c >= K) p.dB[s * KV + row * VV + col0 + c - K] = o2[r][c];
-                }
-            }
-            // dA_t = M_t Abar_{t-1}^T + Lam_t Bbar_{t-1}^T  (Abar_0 = I, Bbar_0 = 0)
-            if (t > 0) {
-                mma_dA16<XS, VV>(xw, slot + Cf::OFF_AP, slot + Cf::OFF_BP, lane, p.dA + s * KK);
-            } else {
+            const float *Ap = slot + Cf::OFF_AP;
+            const float *Bp = slot + Cf::OFF_BP;
+            {
+                // dA_t[a][b] = sum_q X[a][q] Y[b][q], Y = [Abar_{t-1} | Bbar_{t-1}]
+                // (Abar_0 = I, Bbar_0 = 0): KK / 32 entries per lane
 #pragma unroll
                 for (int e = 0; e < KK / 32; ++e) {
                     const int idx = lane + 32 * e, a = idx / K, b2 = idx % K;
-                    p.dA[s * KK + idx] = xw[a * XS + K + b2];
-                }
-            }
-            (void)WV;
-            __syncwarp();  // the slot and xw are read by every lane before reuse
-            refill(q + NSL);
-        }
-        finish_cta(lb, epoch);
-        return;
-    }
-
-    // ---- pass 2: re-run the warp's steps from its start state, write outputs
-#pragma unroll 1
-    for (int q = nvw; q < nq; ++q) {
-        const int64_t t = t0 + tile_step(q), s = step_index(t);
-        const float *slot = wait_slot(q);
-        load_elem<Cf>(slot, t + 1 < g.T, rb, cb, yc, yv);
-        if constexpr (!Cf::BWD) {
-            __syncwarp();  // every lane has read the slot
-            refill(q + NSL);
-        }
-        warp_step<Cf>(xw, cur, yc, yv, rb, cb, o);
-        if constexpr (!Cf::BWD) {
+                    float acc;
+                    if (t > 0) {
+                        acc = 0.f;
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int row = rb * R + r;
-                if constexpr (CC % 4 == 0 && K % 4 == 0 && VV % 4 == 0) {
+                        for (int qq = 0; qq < K; ++qq) acc = fmaf(xw[a * XS + qq], Ap[b2 * K + qq], acc);
 #pragma unroll
-                    for (int qq = 0; qq < CC; qq += 4) {
-                        const int col = cb * CC + qq;
-                        float v4[4] = {o[r][qq], o[r][qq + 1], o[r][qq + 2], o[r][qq + 3]};
-                        if (col < K) st_floats<4>(p.Abar_out + s * KK + row * K + col, v4);
-                        else if (col < NC) st_floats<4>(p.Bbar_out + s * KV + row * VV + col - K, v4);
+                        for (int qq = 0; qq < VV; ++qq) acc = fmaf(xw[a * XS + K + qq], Bp[b2 * VV + qq], acc);
+                    } else {
+                        acc = xw[a * XS + b2];
                     }
-                } else {
-#pragma unroll
-                    for (int cc = 0; cc < CC; ++cc) {
-                        const int col = cb * CC + cc;
-                        if (col < K) p.Abar_out[s * KK + row * K + col] = o[r][cc];
-                        else if (col < NC) p.Bbar_out[s * KV + row * VV + col - K] = o[r][cc];
-                    }
+                    p.dA[s * KK + idx] = acc;
                 }
             }
-        } else {
-            // dB_t = Lam_t (columns 2K .. NC of X)
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int cc = 0; cc < CC; ++cc) {
-                    const int col = cb * CC + cc, row = rb * R + r;
-                    if (col >= 2 * K && col < NC) p.dB[s * KV + row * VV + col - 2 * K] = o[r][cc];
-                }
-            // dA_t[row][jc] = sum_q X[row][K + q] * Y[jc][q],  Y = [Abar_{t-1} | Bbar_{t-1}]
-            constexpr int JD = Cf::JD, WW = Cf::W;
-            const float *xs = xw + (Cf::DB ? cur * MAT : 0);
-            const float *Ap = slot + Cf::OFF_AP;
-            const float *Bp = slot + Cf::OFF_BP;
-            if constexpr (MG_AFW_MMA_DA != 0 && K == 16 && VV % 8 == 0) {
-                if (t > 0) {
-                    mma_dA16<XS, VV>(xs, Ap, Bp, lane, p.dA + s * KK);
-                    __syncwarp();  // the slot and xw are read by every lane before reuse
-                    refill(q + NSL);
-                    continue;
-                }
-            }
-            // the JD rows of Y first, then each row of X once
-            float y[JD][WW];
-#pragma unroll
-            for (int jj = 0; jj < JD; ++jj) {
-                const int jc = cb * JD + jj;
-                if (t > 0) {
-                    ld_floats<K>(Ap + jc * K, y[jj]);
-                    ld_floats<VV>(Bp + jc * VV, y[jj] + K);
-                } else {  // Abar_0 = I, Bbar_0 = 0
-#pragma unroll
-                    for (int qq = 0; qq < WW; ++qq) y[jj][qq] = (qq == jc) ? 1.f : 0.f;
-                }
-            }
-            float da[R][JD];
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                float xr[WW];
-                ld_floats<WW>(xs + (rb * R + r) * XS + K, xr);
-#pragma unroll
-                for (int jj = 0; jj < JD; ++jj) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int qq = 0; qq < WW; ++qq) acc = fmaf(xr[qq], y[jj][qq], acc);
-                    da[r][jj] = acc;
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-                st_floats<JD>(p.dA + s * KK + (rb * R + r) * K + cb * JD, da[r]);
-            __syncwarp();  // the slot and xw are read by every lane before reuse
-            refill(q + NSL);
+            refill(q + NSL);   // also orders this step's reads of xw before the next writes
         }
     }
     finish_cta(lb, epoch);
 }
 
 template <class Cf>
-struct WarpPlan {
+struct ColPlan {
     static size_t n_tiles(int64_t B, int64_t T, int64_t n)
     {
         return size_t(B * n) * size_t((T + Cf::TC - 1) / Cf::TC);
@@ -1389,11 +1192,576 @@ struct WarpPlan {
         const Lookback lb = make_lookback(ws, nt, o);
         if (Cf::SMEM > 48 * 1024) {
             static const cudaError_t attr = cudaFuncSetAttribute(
-                affine_warp_kernel<Cf>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cf::SMEM));
+                affine_col_kernel<Cf>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cf::SMEM));
             if (attr != cudaSuccess)
                 return fail(MG_ERR_LAUNCH, "%s: %s", name, cudaGetErrorString(attr));
         }
-        affine_warp_kernel<Cf><<<unsigned(nt), Cf::NW * 32, Cf::SMEM, s>>>(p, g, lb);
+        affine_col_kernel<Cf><<<unsigned(nt), Cf::NW * 32, Cf::SMEM, s>>>(p, g, lb);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return fail(MG_ERR_LAUNCH, "%s: launch failed: %s", name, cudaGetErrorString(e));
+        return MG_OK;
+    }
+};
+
+// ================================ k = 16: the state on the tensor cores
+// The same tiles, ring and look-back as the column kernel, with the state
+// held as S = X^T ((k + w) x k) in the accumulator fragments of
+// mma.sync.m16n8k8 (tf32 operands, fp32 accumulation).  A step X <- E_C X +
+// [0 | E_V] is S <- S E_C^T + [0 | E_V]^T: S is the A operand, E_C^T the B
+// operand, [0 | E_V]^T the accumulator's start value.  The accumulator
+// fragment of one step is the A operand fragment of the next once the k
+// index inside each 8-wide k tile is read in the order 0, 2, 4, 6, 1, 3, 5,
+// 7 (fragment slot q holds k = 2q, slot q + 4 holds k = 2q + 1); the B
+// operand is read in the same order, so the sum is unchanged and the state
+// never moves between lanes.  The tensor cores then broadcast E_C to the
+// whole product, which from shared memory costs each lane only its own
+// eight values per step.
+// Every product is done in three parts on the split x = hi + lo (hi = x
+// rounded to tf32, lo = the remainder rounded to tf32): hi*hi + hi*lo +
+// lo*hi, dropping the lo*lo term (below 2^-22 of each product).
+// The outputs are written with streaming stores, so that L2 keeps the
+// inputs that pass 2 reads again rather than the outputs.
+// Stored elements (warp aggregates, carries, look-back records) use the
+// ring slot's layout: C (k x k) first, then the value blocks (forward: B
+// (k x v); backward: M-part (k x k), then Lam-part (k x v)).
+template <int V_, bool BWD_, int NW_, int L_, int NSL_>
+struct MCfg {
+    static constexpr int K = 16, VV = V_, NW = NW_, L = L_, NSL = NSL_;
+    static constexpr bool BWD = BWD_;
+    static constexpr int KK = K * K, KV = K * VV;
+    static constexpr int W = BWD ? K + VV : VV;     // value columns of X
+    static constexpr int NR = K + W;                // rows of S = X^T
+    static constexpr int MT = (NR + 15) / 16;       // 16-row tiles of S
+    static constexpr int EL = (BWD ? 2 * KK : KK) + KV;  // floats per stored element
+    static constexpr int REC = EL;
+    static constexpr int TC = NW * L;
+    static constexpr int STEP = BWD ? 3 * KK + 2 * KV : KK + KV;
+    static constexpr int OFF_AP = 2 * KK + KV, OFF_BP = 3 * KK + KV;
+    static constexpr int XS = 40;                   // staged [M | Lam] row stride (backward)
+    static constexpr int XMAT = BWD ? K * XS : 0;
+    static constexpr int BAR_FLOATS = (NW * NSL * 2 + 3) / 4 * 4;
+    static constexpr size_t SMEM =
+        size_t(BAR_FLOATS + NW * NSL * STEP + (NW + 1) * EL + NW * XMAT) * sizeof(float);
+    static_assert(VV == 8 || VV == 16, "tensor-core state for v in {8, 16}");
+    static_assert(NSL >= 2, "the ring needs two slots at least");
+    static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+};
+
+// Address of value entry (row i, value column rp) of a stored element.
+template <class Cf>
+__device__ __forceinline__ int el_val_off(int i, int rp)
+{
+    if constexpr (!Cf::BWD) return Cf::KK + i * Cf::VV + rp;
+    else return rp < Cf::K ? Cf::KK + i * Cf::K + rp : 2 * Cf::KK + i * Cf::VV + rp - Cf::K;
+}
+
+template <bool GLOBAL>
+__device__ __forceinline__ float ldf(const float *a)
+{
+    return GLOBAL ? __ldcg(a) : *a;
+}
+
+// Fragment entry e of tile (mt, nt): S[16 mt + g + 8 (e >> 1)][8 nt + 2 q + (e & 1)].
+template <class Cf>
+using SFrag = float[Cf::MT][2][4];
+
+template <class Cf, int MBEG>
+__device__ __forceinline__ void mf_identity(int g, int q, SFrag<Cf> &s)
+{
+#pragma unroll
+    for (int mt = MBEG; mt < Cf::MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                s[mt][nt][e] = (16 * mt + g + 8 * (e >> 1) == 8 * nt + 2 * q + (e & 1)) ? 1.f : 0.f;
+}
+
+// S <- the stored element at E (S[r][i] = X[i][r]).
+template <class Cf, int MBEG, bool GLOBAL>
+__device__ __forceinline__ void mf_get(const float *E, int g, int q, SFrag<Cf> &s)
+{
+#pragma unroll
+    for (int mt = MBEG; mt < Cf::MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = 16 * mt + g + 8 * (e >> 1), i = 8 * nt + 2 * q + (e & 1);
+                float v = 0.f;
+                if (r < Cf::K) v = ldf<GLOBAL>(E + i * Cf::K + r);
+                else if (r - Cf::K < Cf::W) v = ldf<GLOBAL>(E + el_val_off<Cf>(i, r - Cf::K));
+                s[mt][nt][e] = v;
+            }
+}
+
+template <class Cf, int MBEG, bool GLOBAL>
+__device__ __forceinline__ void mf_put(float *E, int g, int q, const SFrag<Cf> &s)
+{
+#pragma unroll
+    for (int mt = MBEG; mt < Cf::MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = 16 * mt + g + 8 * (e >> 1), i = 8 * nt + 2 * q + (e & 1);
+                float *a = nullptr;
+                if (r < Cf::K) a = E + i * Cf::K + r;
+                else if (r - Cf::K < Cf::W) a = E + el_val_off<Cf>(i, r - Cf::K);
+                if (a) {
+                    if (GLOBAL) __stcg(a, s[mt][nt][e]);
+                    else *a = s[mt][nt][e];
+                }
+            }
+}
+
+// An element's operands for one step: the B fragments of E_C^T and the
+// accumulator start [0 | E_V]^T (m tiles from MBEG on).
+template <class Cf, int MBEG>
+struct EFrag {
+    float b[2][2][2];            // [kt][nt][slot]
+    float v[Cf::MT][2][4];
+};
+
+// Load the element at E (ring slot or stored element).  TRANS: E holds A
+// with E_C = A^T (the adjoint's ring).  has_c false: E_C = 0.
+template <class Cf, int MBEG, bool GLOBAL, bool TRANS>
+__device__ __forceinline__ void mf_load(const float *E, bool has_c, int g, int q,
+                                        EFrag<Cf, MBEG> &f)
+{
+    constexpr int K = Cf::K;
+#pragma unroll
+    for (int mt = MBEG; mt < Cf::MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = 16 * mt + g + 8 * (e >> 1), i = 8 * nt + 2 * q + (e & 1);
+                f.v[mt][nt][e] = (r >= K && r - K < Cf::W) ? ldf<GLOBAL>(E + el_val_off<Cf>(i, r - K)) : 0.f;
+            }
+#pragma unroll
+    for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            float v0 = 0.f, v1 = 0.f;
+            if (has_c) {
+                if constexpr (!TRANS) {   // B[j][i] = E_C[i][j]
+                    const float *a = E + (8 * nt + g) * K + 8 * kt + 2 * q;
+                    float2 p2;
+                    if constexpr (GLOBAL) p2 = __ldcg(reinterpret_cast<const float2 *>(a));
+                    else p2 = *reinterpret_cast<const float2 *>(a);
+                    v0 = p2.x;
+                    v1 = p2.y;
+                } else {                  // B[j][i] = A[j][i]
+                    v0 = ldf<GLOBAL>(E + (8 * kt + 2 * q) * K + 8 * nt + g);
+                    v1 = ldf<GLOBAL>(E + (8 * kt + 2 * q + 1) * K + 8 * nt + g);
+                }
+            }
+            f.b[kt][nt][0] = v0;
+            f.b[kt][nt][1] = v1;
+        }
+}
+
+// S <- S E_C^T + [0 | E_V]^T on the m tiles from MBEG on (each row of S
+// evolves on its own).
+template <class Cf, int MBEG>
+__device__ __forceinline__ void mf_apply(const EFrag<Cf, MBEG> &f, bool has_c, SFrag<Cf> &s)
+{
+    float d[Cf::MT][2][4];
+#pragma unroll
+    for (int mt = MBEG; mt < Cf::MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d[mt][nt][e] = f.v[mt][nt][e];
+    if (has_c) {
+        unsigned bh[2][2][2], bl[2][2][2];
+#pragma unroll
+        for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                split_tf32(f.b[kt][nt][0], bh[kt][nt][0], bl[kt][nt][0]);
+                split_tf32(f.b[kt][nt][1], bh[kt][nt][1], bl[kt][nt][1]);
+            }
+        // the small terms in an accumulator of their own, added after: each
+        // tensor-core accumulation rounds at its result's magnitude, so only
+        // the hi*hi chain rounds at the state's full size
+        float cr[Cf::MT][2][4];
+#pragma unroll
+        for (int mt = MBEG; mt < Cf::MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) cr[mt][nt][e] = 0.f;
+#pragma unroll
+        for (int mt = MBEG; mt < Cf::MT; ++mt)
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt) {
+                unsigned ah[4], al[4];
+                split_tf32(s[mt][kt][0], ah[0], al[0]);
+                split_tf32(s[mt][kt][2], ah[1], al[1]);
+                split_tf32(s[mt][kt][1], ah[2], al[2]);
+                split_tf32(s[mt][kt][3], ah[3], al[3]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    mma_tf32(cr[mt][nt], al, bh[kt][nt][0], bh[kt][nt][1]);
+                    mma_tf32(cr[mt][nt], ah, bl[kt][nt][0], bl[kt][nt][1]);
+                    mma_tf32(d[mt][nt], ah, bh[kt][nt][0], bh[kt][nt][1]);
+                }
+            }
+#pragma unroll
+        for (int mt = MBEG; mt < Cf::MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) d[mt][nt][e] += cr[mt][nt][e];
+    }
+#pragma unroll
+    for (int mt = MBEG; mt < Cf::MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[mt][nt][e] = d[mt][nt][e];
+}
+
+template <class Cf, int MBEG, bool GLOBAL, bool TRANS>
+__device__ __forceinline__ void mf_step(const float *E, bool has_c, int g, int q, SFrag<Cf> &s)
+{
+    EFrag<Cf, MBEG> f;
+    mf_load<Cf, MBEG, GLOBAL, TRANS>(E, has_c, g, q, f);
+    mf_apply<Cf, MBEG>(f, has_c, s);
+}
+
+// The C rows (m tile 0) of S <- those of the stored element at E, exactly
+// (the product of an identity C part with E's, which the split products
+// would round).
+template <class Cf>
+__device__ __forceinline__ void mf_copy_c_rows(const float *E, int g, int q, SFrag<Cf> &s)
+{
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int r = g + 8 * (e >> 1), i = 8 * nt + 2 * q + (e & 1);
+            s[0][nt][e] = E[i * Cf::K + r];
+        }
+}
+
+template <class Cf>
+__global__ void __launch_bounds__(Cf::NW * 32)
+    affine_mma_kernel(const AffPtrs p, const AffGeom g, const Lookback lb)
+{
+    constexpr int K = Cf::K, NW = Cf::NW, L = Cf::L, NSL = Cf::NSL, STEP = Cf::STEP;
+    constexpr int KK = Cf::KK, KV = Cf::KV, VV = Cf::VV, EL = Cf::EL, XS = Cf::XS;
+    extern __shared__ float4 aff_smem[];
+    unsigned long long *const bars = reinterpret_cast<unsigned long long *>(aff_smem);  // [NW][NSL]
+    float *const ring = reinterpret_cast<float *>(aff_smem) + Cf::BAR_FLOATS;          // [NW][NSL][STEP]
+    float *const G = ring + NW * NSL * STEP;   // [NW][EL]: warp aggregates, then inclusive
+    float *const carry = G + NW * EL;          // [EL]
+    float *const xst = carry + EL;             // [NW][XMAT] (backward)
+
+    unsigned tile;
+    unsigned long long epoch;
+    take_ticket(lb, tile, epoch);
+    if (tile >= g.n_tiles) {
+        if (threadIdx.x == 0) raise_error(lb, epoch, kErrBadTicket);
+        finish_cta(lb, epoch);
+        return;
+    }
+    const int c = int(tile / unsigned(g.nJ));
+    const int j = int(tile % unsigned(g.nJ));
+    const int64_t bb = j / g.n, nn = j % g.n;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int fg = lane >> 2, fq = lane & 3;   // fragment row group, column pair
+    const int ct = Cf::BWD ? (g.nC - 1 - c) : c;
+    const int64_t t0 = int64_t(ct) * Cf::TC;
+    const int nv = int(g.T - t0 < Cf::TC ? g.T - t0 : Cf::TC);
+    const int wbase = warp * L;
+    const int nvw = nv - wbase < 0 ? 0 : (nv - wbase < L ? nv - wbase : L);
+    const int pw = Cf::BWD ? NW - 1 - warp : warp;
+    unsigned long long *const wbar = bars + warp * NSL;
+    float *const wring = ring + warp * NSL * STEP;
+    auto step_index = [&](int64_t t) { return (bb * g.T + t) * g.n + nn; };
+    auto tile_step = [&](int qq) {
+        const int k = qq < nvw ? qq : qq - nvw;
+        return Cf::BWD ? wbase + nvw - 1 - k : wbase + k;
+    };
+    const int nq = 2 * nvw;
+
+    auto issue = [&](int qq) {
+        if (qq >= nq) return;
+        unsigned long long *bar = wbar + qq % NSL;
+        float *buf = wring + (qq % NSL) * STEP;
+        const int64_t t = t0 + tile_step(qq), s = step_index(t);
+        if constexpr (!Cf::BWD) {
+            mbar_arrive_expect_tx(bar, (KK + KV) * 4);
+            tma_load_1d(buf, p.A + s * KK, KK * 4, bar);
+            tma_load_1d(buf + KK, p.Bm + s * KV, KV * 4, bar);
+        } else {
+            const bool next = t + 1 < g.T, prev = qq >= nvw && t >= 1;
+            mbar_arrive_expect_tx(bar, (KK + KV + (next ? KK : 0) + (prev ? KK + KV : 0)) * 4);
+            tma_load_1d(buf + KK, p.gAbar + s * KK, KK * 4, bar);
+            tma_load_1d(buf + 2 * KK, p.gBbar + s * KV, KV * 4, bar);
+            if (next) tma_load_1d(buf, p.A + (s + g.n) * KK, KK * 4, bar);
+            if (prev) {
+                tma_load_1d(buf + Cf::OFF_AP, p.Abar + (s - g.n) * KK, KK * 4, bar);
+                tma_load_1d(buf + Cf::OFF_BP, p.Bbar + (s - g.n) * KV, KV * 4, bar);
+            }
+        }
+    };
+    auto wait_slot = [&](int qq) -> const float * {
+        unsigned long long *bar = wbar + qq % NSL;
+        const unsigned parity = unsigned(qq / NSL) & 1u;
+        if (!mbar_wait_bounded(bar, parity, lb.wait_limit_ns)) {
+            if (lane == 0) raise_error(lb, epoch, kErrLookbackTimeout);
+            mbar_wait_bounded(bar, parity, lb.wait_limit_ns);
+        }
+        return wring + (qq % NSL) * STEP;
+    };
+    // refill slot qq % NSL once every lane has used entry qq - NSL (each
+    // lane's loads of it were consumed by its arithmetic before the
+    // __syncwarp)
+    auto refill = [&](int qq) {
+        __syncwarp();
+        if (lane == 0) issue(qq);
+    };
+
+    if (lane == 0) {
+        for (int qq = 0; qq < NSL; ++qq) mbar_init(wbar + qq, 1);
+        for (int qq = 0; qq < NSL; ++qq) issue(qq);
+    }
+    __syncwarp();
+
+    SFrag<Cf> s;
+    // ---- pass 1: aggregate of the warp's steps (every row of S)
+    mf_identity<Cf, 0>(fg, fq, s);
+#pragma unroll 1
+    for (int qq = 0; qq < nvw; ++qq) {
+        const int64_t t = t0 + tile_step(qq);
+        const float *slot = wait_slot(qq);
+        mf_step<Cf, 0, false, Cf::BWD>(slot, !Cf::BWD || t + 1 < g.T, fg, fq, s);
+        refill(qq + NSL);
+    }
+    mf_put<Cf, 0, false>(G + pw * EL, fg, fq, s);
+    __syncthreads();
+
+    // ---- warp 0: inclusive prefixes over the warps (processing order), then
+    //      the look-back for the tile's carry-in
+    if (warp == 0) {
+        mf_get<Cf, 0, false>(G, fg, fq, s);
+        for (int w = 1; w < NW; ++w) {  // G[w] <- G[w-1] o G[w]
+            mf_step<Cf, 0, false, false>(G + w * EL, true, fg, fq, s);
+            __syncwarp();
+            mf_put<Cf, 0, false>(G + w * EL, fg, fq, s);
+        }
+        __syncwarp();
+        const float *cta = G + (NW - 1) * EL;
+        const size_t slot = size_t(c) * g.nJ + j;
+        float *rec_agg = lb.data + slot * 2 * Cf::REC;
+        float *rec_pre = rec_agg + Cf::REC;
+        SFrag<Cf> sc;
+        if (c == 0) {
+            if (!Cf::BWD && p.H0 != nullptr) {
+                // carry = the start state [I | H0]; prefix = carry o cta
+                const float *h0 = p.H0 + (bb * g.n + nn) * KV;
+#pragma unroll
+                for (int mt = 0; mt < Cf::MT; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int r = 16 * mt + fg + 8 * (e >> 1), i = 8 * nt + 2 * fq + (e & 1);
+                            sc[mt][nt][e] = r < K ? (r == i ? 1.f : 0.f)
+                                                  : (r - K < VV ? h0[i * VV + r - K] : 0.f);
+                        }
+                mf_put<Cf, 0, false>(carry, fg, fq, sc);
+                mf_step<Cf, 1, false, false>(cta, true, fg, fq, sc);   // value rows
+                mf_copy_c_rows<Cf>(cta, fg, fq, sc);                  // C rows: I o cta = cta
+                mf_put<Cf, 0, true>(rec_pre, fg, fq, sc);
+            } else {
+                mf_put<Cf, 0, true>(rec_pre, fg, fq, s);
+                mf_identity<Cf, 0>(fg, fq, sc);
+                mf_put<Cf, 0, false>(carry, fg, fq, sc);
+            }
+            publish(lb, slot, kStatusPrefix, epoch, tile);
+        } else {
+            if (peek_status(lb, slot - g.nJ, epoch) != kStatusPrefix) {
+                mf_put<Cf, 0, true>(rec_agg, fg, fq, s);
+                publish(lb, slot, kStatusAggregate, epoch, tile);
+            }
+            const int pp = wait_window(lb, size_t(j), size_t(g.nJ), c, epoch, tile);
+            if (pp >= 0) {
+                mf_get<Cf, 0, true>(lb.data + (size_t(pp) * g.nJ + j) * 2 * Cf::REC + Cf::REC,
+                                    fg, fq, sc);
+                // carry <- carry o agg(qc), the records fetched four at a time
+                auto rec = [&](int qc) { return lb.data + (size_t(qc) * g.nJ + j) * 2 * Cf::REC; };
+                int qc = pp + 1;
+                for (; qc + 4 <= c; qc += 4) {
+                    EFrag<Cf, 0> f[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) mf_load<Cf, 0, true, false>(rec(qc + u), true, fg, fq, f[u]);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) mf_apply<Cf, 0>(f[u], true, sc);
+                }
+                for (; qc < c; ++qc) mf_step<Cf, 0, true, false>(rec(qc), true, fg, fq, sc);
+            } else {
+                mf_identity<Cf, 0>(fg, fq, sc);
+            }
+            mf_put<Cf, 0, false>(carry, fg, fq, sc);
+            mf_step<Cf, 0, false, false>(cta, true, fg, fq, sc);  // prefix of this tile
+            mf_put<Cf, 0, true>(rec_pre, fg, fq, sc);
+            publish(lb, slot, kStatusPrefix, epoch, tile);
+        }
+    }
+    __syncthreads();
+
+    constexpr int M0 = Cf::BWD ? 1 : 0;   // pass 2 of the adjoint: [M | Lam] rows only
+    mf_get<Cf, M0, false>(carry, fg, fq, s);
+    if (pw > 0) {
+        if (!Cf::BWD && c == 0) {
+            // the carry of chunk 0 is [I | H0] (H0 = 0 without a start
+            // state): the C rows of carry o G[pw-1] are G[pw-1]'s own
+            mf_step<Cf, 1, false, false>(G + (pw - 1) * EL, true, fg, fq, s);
+            mf_copy_c_rows<Cf>(G + (pw - 1) * EL, fg, fq, s);
+        } else {
+            mf_step<Cf, M0, false, false>(G + (pw - 1) * EL, true, fg, fq, s);
+        }
+    }
+    if constexpr (!Cf::BWD) {
+        // ---- pass 2: re-run the warp's steps from its start state, write
+        //      Abar_t (rows r < k of S, transposed) and Bbar_t (rows k..)
+#pragma unroll 1
+        for (int qq = nvw; qq < nq; ++qq) {
+            const int64_t t = t0 + tile_step(qq), si = step_index(t);
+            const float *slot = wait_slot(qq);
+            mf_step<Cf, 0, false, false>(slot, true, fg, fq, s);
+            refill(qq + NSL);
+            float *ab = p.Abar_out + si * KK, *bo = p.Bbar_out + si * KV;
+#pragma unroll
+            for (int mt = 0; mt < Cf::MT; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = 16 * mt + fg + 8 * (e >> 1), i = 8 * nt + 2 * fq + (e & 1);
+                        if (r < K) __stcs(ab + i * K + r, s[mt][nt][e]);
+                        else if (r - K < VV) __stcs(bo + i * VV + r - K, s[mt][nt][e]);
+                    }
+        }
+    } else {
+        // ---- pass 2 of the adjoint: dB_t = Lam_t; dA_t = [M_t | Lam_t]
+        //      [Abar_{t-1} | Bbar_{t-1}]^T, as dA_t^T = Y S_v with Y =
+        //      [Abar_{t-1} | Bbar_{t-1}] (A operand, from the ring slot) and
+        //      S_v = [M_t | Lam_t]^T (B operand, staged in shared memory as
+        //      [M_t | Lam_t], row stride XS)
+        constexpr int W = Cf::W, KTD = W / 8;
+        float *const xw = xst + warp * Cf::XMAT;
+#pragma unroll 1
+        for (int qq = nvw; qq < nq; ++qq) {
+            const int64_t t = t0 + tile_step(qq), si = step_index(t);
+            const float *slot = wait_slot(qq);
+            mf_step<Cf, 1, false, true>(slot, t + 1 < g.T, fg, fq, s);
+#pragma unroll
+            for (int mt = 1; mt < Cf::MT; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = 16 * mt + fg + 8 * (e >> 1), i = 8 * nt + 2 * fq + (e & 1);
+                        if (r - K < W) {
+                            xw[i * XS + r - K] = s[mt][nt][e];
+                            if (r >= 2 * K) __stcs(p.dB + si * KV + i * VV + r - 2 * K, s[mt][nt][e]);
+                        }
+                    }
+            __syncwarp();
+            float *da = p.dA + si * KK;
+            if (t > 0) {
+                const float *Ap = slot + Cf::OFF_AP;
+                const float *Bp = slot + Cf::OFF_BP;
+                float acc[2][4] = {};
+#pragma unroll
+                for (int kt = 0; kt < KTD; ++kt) {
+                    // A operand: Y rows fg, fg + 8, columns 8 kt + 2 fq (+1)
+                    float y0[2], y1[2];
+                    if (kt < 2) {
+                        const float2 u0 = *reinterpret_cast<const float2 *>(Ap + fg * K + 8 * kt + 2 * fq);
+                        const float2 u1 = *reinterpret_cast<const float2 *>(Ap + (fg + 8) * K + 8 * kt + 2 * fq);
+                        y0[0] = u0.x; y0[1] = u0.y; y1[0] = u1.x; y1[1] = u1.y;
+                    } else {
+                        const float2 u0 = *reinterpret_cast<const float2 *>(Bp + fg * VV + 8 * kt - K + 2 * fq);
+                        const float2 u1 = *reinterpret_cast<const float2 *>(Bp + (fg + 8) * VV + 8 * kt - K + 2 * fq);
+                        y0[0] = u0.x; y0[1] = u0.y; y1[0] = u1.x; y1[1] = u1.y;
+                    }
+                    unsigned ah[4], al[4];
+                    split_tf32(y0[0], ah[0], al[0]);
+                    split_tf32(y1[0], ah[1], al[1]);
+                    split_tf32(y0[1], ah[2], al[2]);
+                    split_tf32(y1[1], ah[3], al[3]);
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const float2 xv = *reinterpret_cast<const float2 *>(xw + (8 * nt + fg) * XS + 8 * kt + 2 * fq);
+                        unsigned bh0, bl0, bh1, bl1;
+                        split_tf32(xv.x, bh0, bl0);
+                        split_tf32(xv.y, bh1, bl1);
+                        mma_tf32(acc[nt], al, bh0, bh1);
+                        mma_tf32(acc[nt], ah, bl0, bl1);
+                        mma_tf32(acc[nt], ah, bh0, bh1);
+                    }
+                }
+                // acc[nt][e] = dA^T[fg + 8 (e >> 1)][8 nt + 2 fq + (e & 1)]
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        __stcs(da + (8 * nt + 2 * fq + (e & 1)) * K + fg + 8 * (e >> 1), acc[nt][e]);
+            } else {   // Abar_0 = I, Bbar_0 = 0: dA_0 = M_0
+#pragma unroll
+                for (int e = 0; e < KK / 32; ++e) {
+                    const int idx = lane + 32 * e;
+                    __stcs(da + idx, xw[(idx / K) * XS + idx % K]);
+                }
+            }
+            refill(qq + NSL);   // also orders this step's reads of xw before the next writes
+        }
+    }
+    finish_cta(lb, epoch);
+}
+
+template <class Cf>
+struct MmaPlan {
+    static size_t n_tiles(int64_t B, int64_t T, int64_t n)
+    {
+        return size_t(B * n) * size_t((T + Cf::TC - 1) / Cf::TC);
+    }
+    static size_t ws_bytes(int64_t B, int64_t T, int64_t n)
+    {
+        return tiled_ws_bytes(n_tiles(B, T, n), size_t(2) * Cf::REC * sizeof(float));
+    }
+    static mg_status launch(const AffPtrs &p, int64_t B, int64_t T, int64_t n, void *ws,
+                            size_t wsb, cudaStream_t s, const LaunchOpts &o, const char *name)
+    {
+        const size_t nt = n_tiles(B, T, n);
+        if (nt >= (size_t(1) << 31) || B * n >= (int64_t(1) << 31))
+            return fail(MG_ERR_UNSUPPORTED, "%s: %zu tiles exceed the 2^31 ticket range", name, nt);
+        const size_t need = ws_bytes(B, T, n);
+        if (wsb < need)
+            return fail(MG_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", name, wsb, need);
+        AffGeom g;
+        g.B = B;
+        g.T = T;
+        g.n = n;
+        g.nJ = int(B * n);
+        g.nC = int((T + Cf::TC - 1) / Cf::TC);
+        g.n_tiles = unsigned(nt);
+        const Lookback lb = make_lookback(ws, nt, o);
+        if (Cf::SMEM > 48 * 1024) {
+            static const cudaError_t attr = cudaFuncSetAttribute(
+                affine_mma_kernel<Cf>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cf::SMEM));
+            if (attr != cudaSuccess)
+                return fail(MG_ERR_LAUNCH, "%s: %s", name, cudaGetErrorString(attr));
+        }
+        affine_mma_kernel<Cf><<<unsigned(nt), Cf::NW * 32, Cf::SMEM, s>>>(p, g, lb);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return fail(MG_ERR_LAUNCH, "%s: launch failed: %s", name, cudaGetErrorString(e));
@@ -1443,30 +1811,6 @@ struct WarpPlan {
 #ifndef MG_AFLB_NSL
 #define MG_AFLB_NSL 4
 #endif
-#ifndef MG_AFW_NW
-#define MG_AFW_NW 4
-#endif
-#ifndef MG_AFW_L
-#define MG_AFW_L 16
-#endif
-#ifndef MG_AFW_DB
-#define MG_AFW_DB 1
-#endif
-#ifndef MG_AFW_NSL
-#define MG_AFW_NSL 5
-#endif
-#ifndef MG_AFWB_NW
-#define MG_AFWB_NW 4
-#endif
-#ifndef MG_AFWB_L
-#define MG_AFWB_L 16
-#endif
-#ifndef MG_AFWB_DB
-#define MG_AFWB_DB 0
-#endif
-#ifndef MG_AFWB_NSL
-#define MG_AFWB_NSL 2
-#endif
 
 template <int K, int V>
 using LaneFwd = LanePlan<LCfg<K, V, false, MG_AFL_NW, MG_AFL_L, MG_AFL_NSL>>;
@@ -1476,10 +1820,67 @@ template <int K, int V>
 using SmallFwd = ChanPlan<AffFwdSmall<K, V, MG_AFS_L>, 32, MG_AFS_TY, MG_AFS_MB>;
 template <int K, int V>
 using SmallBwd = ChanPlan<AffBwdSmall<K, V, MG_AFSB_L>, 32, MG_AFSB_TY, MG_AFSB_MB>;
+#ifndef MG_AFC_NW
+#define MG_AFC_NW 4
+#endif
+#ifndef MG_AFC_L
+#define MG_AFC_L 16
+#endif
+#ifndef MG_AFC_NSL
+#define MG_AFC_NSL 4
+#endif
+#ifndef MG_AFCB_NW
+#define MG_AFCB_NW 4
+#endif
+#ifndef MG_AFCB_L
+#define MG_AFCB_L 16
+#endif
+#ifndef MG_AFCB_NSL
+#define MG_AFCB_NSL 3
+#endif
+
+#ifndef MG_AFM_NW
+#define MG_AFM_NW 4
+#endif
+#ifndef MG_AFM_L
+#define MG_AFM_L 32
+#endif
+#ifndef MG_AFM_NSL
+#define MG_AFM_NSL 4
+#endif
+#ifndef MG_AFMB_NW
+#define MG_AFMB_NW 4
+#endif
+#ifndef MG_AFMB_L
+#define MG_AFMB_L 16
+#endif
+#ifndef MG_AFMB_NSL
+#define MG_AFMB_NSL 2
+#endif
+
+// k = 16 with v in {8, 16}: the tensor-core state; other k in {8, 16}: the
+// column kernel.
 template <int K, int V>
-using BigFwd = WarpPlan<WCfg<K, V, false, MG_AFW_NW, MG_AFW_L, bool(MG_AFW_DB), MG_AFW_NSL>>;
+constexpr bool mma_state_ok() { return K == 16 && (V == 8 || V == 16); }
+template <int K, int V, bool BWD>
+struct BigSel {
+    using type = ColPlan<CCfg<K, V, BWD, BWD ? MG_AFCB_NW : MG_AFC_NW, BWD ? MG_AFCB_L : MG_AFC_L,
+                              BWD ? MG_AFCB_NSL : MG_AFC_NSL>>;
+};
+template <int V, bool BWD>
+struct BigSel<16, V, BWD> {
+    using type = std::conditional_t<
+        mma_state_ok<16, V>(),
+        MmaPlan<MCfg<(V == 8 || V == 16) ? V : 16, BWD, BWD ? MG_AFMB_NW : MG_AFM_NW,
+                     BWD ? MG_AFMB_L : MG_AFM_L, BWD ? MG_AFMB_NSL : MG_AFM_NSL>>,
+        ColPlan<CCfg<16, V, BWD, BWD ? MG_AFCB_NW : MG_AFC_NW, BWD ? MG_AFCB_L : MG_AFC_L,
+                     BWD ? MG_AFCB_NSL : MG_AFC_NSL>>>;
+};
+
 template <int K, int V>
-using BigBwd = WarpPlan<WCfg<K, K + V, true, MG_AFWB_NW, MG_AFWB_L, bool(MG_AFWB_DB), MG_AFWB_NSL>>;
+using BigFwd = typename BigSel<K, V, false>::type;
+template <int K, int V>
+using BigBwd = typename BigSel<K, V, true>::type;
 
 // k <= 4: the lane kernel where its blocks are 16 to 128 bytes, the chunk
 // engine otherwise; k in {8, 16}: the warp kernel.
