@@ -551,6 +551,10 @@ void orc_affine_scan_h0_bwd(const double *A, const double *H0, const double *Aba
  * recurrence of affine_scan_fwd with a vector state).  perm[r] is a
  * permutation of 0..k-1; p2p[r] is its inverse (the position of each
  * coordinate in perm[r]), which the oracle does not need.
+ * The arithmetic of this reading is pinned (a hand-derived case, the dense
+ * affine recurrence it equals, finite differences of its adjoint); the
+ * reading itself is not fixed by the page, so against the page the angle
+ * scan is "parity unpinned".
  */
 
 /* x <- Q_t x for one step: R layers of paired rotations and signs. */
