@@ -395,13 +395,13 @@ struct VarBwd {
 #define MG_VLF_TX 16
 #endif
 #ifndef MG_VLF_TY
-#define MG_VLF_TY 8
+#define MG_VLF_TY 16
 #endif
 #ifndef MG_VLF_L
 #define MG_VLF_L 8
 #endif
 #ifndef MG_VLF_MB
-#define MG_VLF_MB 2
+#define MG_VLF_MB 1
 #endif
 #ifndef MG_VLF_R
 #define MG_VLF_R 2
@@ -410,16 +410,16 @@ struct VarBwd {
 #define MG_VLB_TX 32
 #endif
 #ifndef MG_VLB_TY
-#define MG_VLB_TY 4
+#define MG_VLB_TY 8
 #endif
 #ifndef MG_VLB_L
 #define MG_VLB_L 4
 #endif
 #ifndef MG_VLB_MB
-#define MG_VLB_MB 3
+#define MG_VLB_MB 2
 #endif
 #ifndef MG_VLB_R
-#define MG_VLB_R 2
+#define MG_VLB_R 4
 #endif
 constexpr int kVTX = 32, kVTY = 8;
 

@@ -14,6 +14,8 @@ Cases (inputs seeded, resident on cuda:0 before the first launch):
   log_fwd / log_bwd              minGRU log-space scan and its adjoint, B=8 T=2048 D=2048
   affine4_fwd / affine4_bwd      Haar affine scan, B=4 T=2048 n=64 k=v=4
   affine16_fwd / affine16_bwd    Haar affine scan, B=2 T=1024 n=32 k=v=16
+  angle_fwd / angle_bwd          angle-fused scan, B=16 T=512 n=256 k=16 R=4 (a quarter of
+                                 the bench's T; each input larger than L2)
 
 Every case runs its op `repeats` times (default 3) after one set-up call of
 the forward op where the backward needs the forward's outputs.  Each input is
@@ -30,7 +32,7 @@ from linear_recurrence_scans_gb300 import workloads as wl
 
 CASES = ("linear_fwd", "linear_bwd", "linear_bf16_fwd", "linear_bf16_bwd", "log_fwd", "log_bwd",
          "affine4_fwd", "affine4_bwd", "affine16_fwd", "affine16_bwd", "mingru_bf16_fwd",
-         "mingru_bf16_bwd", "varlen_fwd", "varlen_bwd")
+         "mingru_bf16_bwd", "varlen_fwd", "varlen_bwd", "angle_fwd", "angle_bwd")
 
 
 def main(argv):
@@ -41,7 +43,17 @@ def main(argv):
     reps = int(argv[1]) if len(argv) > 1 else 3
     dev = torch.device("cuda", 0)
     mg.load()
-    if case.startswith("mingru"):
+    if case.startswith("angle"):
+        th, sc, ga, bv, h0, perm, sgn, p2p, go = wl.angle_inputs(16, 512, 256, 4, 16, seed=0,
+                                                                 device=dev)
+        h = mg.angle_scan_fwd(th, sc, ga, bv, h0, perm, sgn, p2p)
+        outs = tuple(torch.empty_like(x) for x in (th, sc, ga, bv, h0))
+        for _ in range(reps):
+            if case.endswith("fwd"):
+                mg.angle_scan_fwd(th, sc, ga, bv, h0, perm, sgn, p2p, out=h)
+            else:
+                mg.angle_scan_bwd(th, sc, ga, h0, h, go, perm, sgn, p2p, out=outs)
+    elif case.startswith("mingru"):
         x1, x2, _, gBc = wl.mingru_x(4, 8192, 4096, seed=0, device=dev, in_dtype=torch.bfloat16)
         _, Bc = mg.mingru_scan_fwd(x1, x2, want_A=False)
         dx1, dx2 = torch.empty_like(x1), torch.empty_like(x1)
