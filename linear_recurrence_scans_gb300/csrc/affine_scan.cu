@@ -1140,10 +1140,11 @@ __global__ void __launch_bounds__(Cf::NW * 32)
             const float *Bp = slot + Cf::OFF_BP;
             {
                 // dA_t[a][b] = sum_q X[a][q] Y[b][q], Y = [Abar_{t-1} | Bbar_{t-1}]
-                // (Abar_0 = I, Bbar_0 = 0): KK / 32 entries per lane
+                // (Abar_0 = I, Bbar_0 = 0): entries lane, lane + 32, ...
 #pragma unroll
-                for (int e = 0; e < KK / 32; ++e) {
+                for (int e = 0; e < (KK + 31) / 32; ++e) {
                     const int idx = lane + 32 * e, a = idx / K, b2 = idx % K;
+                    if (idx >= KK) break;
                     float acc;
                     if (t > 0) {
                         acc = 0.f;

@@ -47,6 +47,22 @@ struct op_stashes<Op, decltype(void(Op::kStash))> {
     static constexpr bool value = Op::kStash;
 };
 
+// Before publishing its aggregate, a tile may first look at its
+// predecessor's flag and skip the aggregate when a prefix is already there
+// (Op::kPeek, default on): one L2 round trip more on the tile's look-back
+// path, one record store less.  Which wins depends on the op (measured).
+#ifndef MG_LB_PEEK
+#define MG_LB_PEEK 1
+#endif
+template <class Op, class = void>
+struct op_peeks {
+    static constexpr bool value = MG_LB_PEEK != 0;
+};
+template <class Op>
+struct op_peeks<Op, decltype(void(Op::kPeek))> {
+    static constexpr bool value = Op::kPeek;
+};
+
 template <class Op>
 struct StashView {
     float *base;   // this thread's slot of step 0, state 0 of the round
@@ -252,7 +268,8 @@ __global__ void __launch_bounds__(TX *TY, MINB)
                 cta = (k == 0) ? x : Op::combine(cta, x);
             }
         }
-        publish_first<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch, cta);
+        publish_first<Op, TX, op_peeks<Op>::value>(args, g, lb, c, j, bb, ld, lact, lchan, tile,
+                                                   epoch, cta);
         excl = find_carry<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch);
         if (lact) {
 #pragma unroll

@@ -82,6 +82,7 @@ template <typename Tin, int VEC_, int L_>
 struct VarFwd {
     static constexpr int NS = 3, VEC = VEC_, L = L_;
     static constexpr bool kReverse = false;
+    static constexpr bool kPeek = false;   // look-back without the peek (measured faster)
     using S = St<NS, VEC>;
     struct Args {
         const Tin *a;
@@ -238,6 +239,7 @@ template <typename Tin, int VEC_, int L_>
 struct VarBwd {
     static constexpr int NS = 3, VEC = VEC_, L = L_;
     static constexpr bool kReverse = true;
+    static constexpr bool kPeek = false;   // look-back without the peek (measured faster)
     using S = St<NS, VEC>;
     struct Args {
         const Tin *a;
