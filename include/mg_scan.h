@@ -355,7 +355,8 @@ mg_status mg_affine_scan_h0_bwd(const float *A, const float *H0,
  *   (c x_p - s x_q, s x_p + c x_q) with c, s = cos, sin theta_{t,r,i},
  *   then multiplies each x_j by sgn[r][j].
  * scale (gamma) may be NULL when has_scale (has_decay) is 0.  k in
- * {2, 4, 8, 16, 32}, 1 <= R <= 8.  No workspace.
+ * {2, 4, 8, 16, 32}, 1 <= R <= 8; T and n*R*k below 2^31
+ * (MG_ERR_UNSUPPORTED otherwise).  No workspace.
  */
 mg_status mg_angle_scan_fwd(const float *theta, const float *scale, const float *gamma,
                             const float *b, const float *h0,

@@ -121,7 +121,7 @@ __host__ __device__ inline StepLayout step_layout(int nseq, int R, int k, bool b
 // seven copies per thread cover it.
 struct CopyJobs {
     const float *src[kAngleJobs];
-    int64_t stride[kAngleJobs];
+    int stride[kAngleJobs];   // n * (floats per (b, t, n)) < 2^31 (checked on the host)
     unsigned live, prev;
 };
 
@@ -160,19 +160,19 @@ __device__ __forceinline__ void make_jobs(const float *theta, const float *scale
         const int64_t st0 = (sq / g.n) * g.T * g.n + sq % g.n;   // step index of (b, 0, n)
         // h_{t-1} rows: the source of step t is row t - 1 (only used for t >= 1)
         cj.src[i] = on ? base + (prev ? st0 - g.n : st0) * per + off : theta;
-        cj.stride[i] = g.n * per;
+        cj.stride[i] = int(g.n * per);
         cj.live |= unsigned(on) << i;
         cj.prev |= unsigned(prev) << i;
     }
 }
 
-// Issue this thread's copies of step t into `slot`.
-__device__ __forceinline__ void issue_step(const CopyJobs &cj, float *slot, int64_t t)
+// Issue this thread's copies of step t (t < 2^31) into `slot`.
+__device__ __forceinline__ void issue_step(const CopyJobs &cj, float *slot, int t)
 {
 #pragma unroll
     for (int i = 0; i < kAngleJobs; ++i) {
         if (!((cj.live >> i) & 1u) || (((cj.prev >> i) & 1u) && t == 0)) continue;
-        cp_async4(slot + threadIdx.x + i * kAngleThreads, cj.src[i] + t * cj.stride[i]);
+        cp_async4(slot + threadIdx.x + i * kAngleThreads, cj.src[i] + int64_t(t) * cj.stride[i]);
     }
 }
 
@@ -202,13 +202,15 @@ __global__ void __launch_bounds__(kAngleThreads)
         for (int u = 0; u < kAngleG; ++u) {
             const int64_t t = gi * kAngleG + u;
             if (gi < ngroups && t < g.T)
-                issue_step(cj, ring + int((t % kAngleSteps) * L.floats), t);
+                issue_step(cj, ring + int((t % kAngleSteps) * L.floats), int(t));
         }
         cp_async_commit();
     };
     for (int gi = 0; gi < kAngleNG; ++gi) issue_group(gi);
 
     float x = act ? __ldg(h0 + sq * K + j) : 0.f;
+    float *const h_lane = h + st0 * K + j;   // h of step t at h_lane[t * n * K]
+    const int nK = int(g.n * K);
     for (int64_t gi = 0; gi < ngroups; ++gi) {
         cp_async_wait<kAngleNG - 1>();
         __syncthreads();
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(kAngleThreads)
             }
             const float f = (g.has_scale ? sp[L.o_s + sl] : 1.f) * (g.has_decay ? sp[L.o_g + sl] : 1.f);
             x = fmaf(f, x, sp[L.o_vec + sl * K + j]);
-            if (act) h[(st0 + t * g.n) * K + j] = x;
+            if (act) h_lane[int64_t(int(t)) * nK] = x;
         }
         __syncthreads();   // every thread is done with the group's slots
         issue_group(gi + kAngleNG);
@@ -264,7 +266,7 @@ __global__ void __launch_bounds__(kAngleThreads)
         for (int u = 0; u < kAngleG; ++u) {
             const int64_t q = gi * kAngleG + u;
             if (gi < ngroups && q < g.T)
-                issue_step(cj, ring + int((q % kAngleSteps) * L.floats), g.T - 1 - q);
+                issue_step(cj, ring + int((q % kAngleSteps) * L.floats), int(g.T - 1 - q));
         }
         cp_async_commit();
     };

@@ -491,6 +491,8 @@ mg_status mg_angle_scan_fwd(const float *theta, const float *scale, const float 
     MG_TRY(angle_tables(fn, perm, sgn, p2p, R, k, tb));
     MG_TRY(check_dims(fn, {B, T, n, k}));
     if (B * n > (int64_t(1) << 40) / k) return fail(MG_ERR_UNSUPPORTED, "%s: too many sequences", fn);
+    if (T >= (int64_t(1) << 31) || n * int64_t(R) * k >= (int64_t(1) << 31))
+        return fail(MG_ERR_UNSUPPORTED, "%s: T and n*R*k must stay below 2^31", fn);
     if (B == 0 || T == 0 || n == 0) return MG_OK;
     const size_t st = size_t(B) * T * n;
     MG_TRY(check_bufs(fn, {{theta, st * R * (k / 2) * 4, "theta", false},
@@ -517,6 +519,8 @@ mg_status mg_angle_scan_bwd(const float *theta, const float *scale, const float 
     MG_TRY(angle_tables(fn, perm, sgn, p2p, R, k, tb));
     MG_TRY(check_dims(fn, {B, T, n, k}));
     if (B * n > (int64_t(1) << 40) / k) return fail(MG_ERR_UNSUPPORTED, "%s: too many sequences", fn);
+    if (T >= (int64_t(1) << 31) || n * int64_t(R) * k >= (int64_t(1) << 31))
+        return fail(MG_ERR_UNSUPPORTED, "%s: T and n*R*k must stay below 2^31", fn);
     if (B == 0 || n == 0) return MG_OK;
     const size_t nh = size_t(B) * n * k * 4;
     if (T == 0) {   // L does not depend on h0: its gradient is zero
