@@ -571,8 +571,8 @@ __global__ void __launch_bounds__(Cf::NW * 32)
             }
             cta = (w == 0) ? x : Op::combine(cta, x);
         }
-        publish_first<Op, 32>(args, g, lb, c, j, bb, d, true, act, tile, epoch, cta);
-        excl = find_carry<Op, 32>(args, g, lb, c, j, bb, d, true, act, tile, epoch);
+        const int p0 = publish_first<Op, 32>(args, g, lb, c, j, bb, d, true, act, tile, epoch, cta);
+        excl = find_carry<Op, 32>(args, g, lb, c, j, bb, d, true, act, tile, epoch, p0);
 #pragma unroll
         for (int s = 0; s < NS; ++s) s_carry[s * 32 + lane] = excl.v[s][0];
     }

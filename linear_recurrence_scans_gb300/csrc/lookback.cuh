@@ -230,6 +230,28 @@ static __device__ __noinline__ int wait_window(const Lookback &lb, size_t j, siz
     }
 }
 
+// One poll of the window of wait_window, without waiting or raising errors:
+// the chunk wait_window would return if the window resolves on this poll,
+// else -2.  Warp-collective.
+static __device__ __noinline__ int poll_window(const Lookback &lb, size_t j, size_t stride, int c,
+                                               unsigned long long epoch)
+{
+    const int lane = threadIdx.x & 31;
+    const int q = c - 1 - lane;
+    unsigned st = kStatusPrefix;
+    if (q >= 0) st = flag_status(ld_acquire_u64(lb.flags + size_t(q) * stride + j), epoch);
+    const unsigned pmask = __ballot_sync(0xffffffffu, st == kStatusPrefix);
+    const unsigned xmask = __ballot_sync(0xffffffffu, st == kStatusNone);
+    int p = -2;
+    if (pmask != 0u) {
+        const int first = __ffs(pmask) - 1;
+        const unsigned before = first == 0 ? 0u : (0xffffffffu >> (32 - first));
+        if ((xmask & before) == 0u && first <= c - 1) p = c - 1 - first;
+    }
+    __syncwarp();
+    return p;
+}
+
 // Publish record `slot` with `status` (warp-collective).  Every lane must have
 // written its part of the record (.cg stores) before calling; the __syncwarp
 // orders those writes before lane 0's release store, which is cumulative.

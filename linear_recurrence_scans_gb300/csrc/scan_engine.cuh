@@ -116,24 +116,40 @@ __device__ __forceinline__ typename Op::S get_record(const Lookback &lb, size_t 
 // First half of the look-back (one warp): publish this chunk's record as
 // early as possible.  Chunk 0 publishes its inclusive prefix (initial o cta)
 // at once; any other chunk publishes its aggregate, unless `peek` is set and
-// its predecessor already holds a prefix (then the prefix follows shortly).
+// one poll of its predecessors' flags already resolves its carry (then its
+// prefix follows shortly).  Returns the predecessor that poll resolved to,
+// or -2 (find_carry then waits for one).
+#ifndef MG_LB_FIRSTPOLL
+#define MG_LB_FIRSTPOLL 1
+#endif
 template <class Op, int TX, bool PEEK = true>
-__device__ void publish_first(const typename Op::Args &args, const ChanGeom &g,
-                              const Lookback &lb, int c, int j, int64_t bb, int ld, bool lact,
-                              bool lchan, unsigned tile, unsigned long long epoch,
-                              const typename Op::S &cta)
+__device__ int publish_first(const typename Op::Args &args, const ChanGeom &g,
+                             const Lookback &lb, int c, int j, int64_t bb, int ld, bool lact,
+                             bool lchan, unsigned tile, unsigned long long epoch,
+                             const typename Op::S &cta)
 {
     const int lane = threadIdx.x & 31;
     const size_t slot = size_t(c) * g.nJ + j;
     if (c == 0) {
         if (lact) put_record<Op, TX>(lb, slot, 1, lane, Op::combine(Op::initial(args, g, bb, ld, lchan), cta));
         publish(lb, slot, kStatusPrefix, epoch, tile);
-        return;
+        return -2;
     }
-    if (!PEEK || peek_status(lb, slot - g.nJ, epoch) != kStatusPrefix) {
+    int p0 = -2;
+    bool agg = true;
+    if (PEEK) {
+        if (MG_LB_FIRSTPOLL) {
+            p0 = poll_window(lb, size_t(j), size_t(g.nJ), c, epoch);
+            agg = p0 < 0;
+        } else {
+            agg = peek_status(lb, slot - g.nJ, epoch) != kStatusPrefix;
+        }
+    }
+    if (agg) {
         if (lact) put_record<Op, TX>(lb, slot, 0, lane, cta);
         publish(lb, slot, kStatusAggregate, epoch, tile);
     }
+    return p0;
 }
 
 // Second half (one warp): the exclusive carry-in of chunk c of channel tile j
@@ -142,13 +158,14 @@ template <class Op, int TX>
 __device__ typename Op::S find_carry(const typename Op::Args &args, const ChanGeom &g,
                                      const Lookback &lb, int c, int j, int64_t bb, int ld,
                                      bool lact, bool lchan, unsigned tile,
-                                     unsigned long long epoch)
+                                     unsigned long long epoch, int p0)
 {
     using S = typename Op::S;
     const int lane = threadIdx.x & 31;
     if (c == 0) return Op::initial(args, g, bb, ld, lchan);
     S excl = Op::identity();
-    const int p = wait_window(lb, size_t(j), size_t(g.nJ), c, epoch, tile);
+    // p0: the predecessor publish_first's poll already resolved, if any
+    const int p = p0 >= 0 ? p0 : wait_window(lb, size_t(j), size_t(g.nJ), c, epoch, tile);
     if (p >= 0 && lact) {
         // excl = pref(p) o agg(p+1) o ... o agg(c-1), folded left to right;
         // the record loads of a batch are independent and issued together.
@@ -268,9 +285,9 @@ __global__ void __launch_bounds__(TX *TY, MINB)
                 cta = (k == 0) ? x : Op::combine(cta, x);
             }
         }
-        publish_first<Op, TX, op_peeks<Op>::value>(args, g, lb, c, j, bb, ld, lact, lchan, tile,
-                                                   epoch, cta);
-        excl = find_carry<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch);
+        const int p0 = publish_first<Op, TX, op_peeks<Op>::value>(args, g, lb, c, j, bb, ld, lact,
+                                                                  lchan, tile, epoch, cta);
+        excl = find_carry<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch, p0);
         if (lact) {
 #pragma unroll
             for (int s = 0; s < NS; ++s) store_vec<VEC>(&s_carry[s * DC + lane * VEC], excl.v[s]);
