@@ -1065,11 +1065,14 @@ __global__ void __launch_bounds__(Cf::NW * 32)
             }
             publish(lb, slot, kStatusPrefix, epoch, tile);
         } else {
-            if (peek_status(lb, slot - g.nJ, epoch) != kStatusPrefix) {
+            // one poll of the window; the aggregate is published (and the
+            // wait entered) only when it does not resolve the carry yet
+            int pp = poll_window(lb, size_t(j), size_t(g.nJ), c, epoch);
+            if (pp < 0) {
                 col_put<Cf, 0, CPL, true>(rec_agg, lane, x);
                 publish(lb, slot, kStatusAggregate, epoch, tile);
+                pp = wait_window(lb, size_t(j), size_t(g.nJ), c, epoch, tile);
             }
-            const int pp = wait_window(lb, size_t(j), size_t(g.nJ), c, epoch, tile);
             if (pp >= 0) {
                 col_get<Cf, 0, CPL, true>(lb.data + (size_t(pp) * g.nJ + j) * 2 * Cf::REC + Cf::REC,
                                           lane, xc);
@@ -1587,11 +1590,14 @@ __global__ void __launch_bounds__(Cf::NW * 32)
             }
             publish(lb, slot, kStatusPrefix, epoch, tile);
         } else {
-            if (peek_status(lb, slot - g.nJ, epoch) != kStatusPrefix) {
+            // one poll of the window; the aggregate is published (and the
+            // wait entered) only when it does not resolve the carry yet
+            int pp = poll_window(lb, size_t(j), size_t(g.nJ), c, epoch);
+            if (pp < 0) {
                 mf_put<Cf, 0, true>(rec_agg, fg, fq, s);
                 publish(lb, slot, kStatusAggregate, epoch, tile);
+                pp = wait_window(lb, size_t(j), size_t(g.nJ), c, epoch, tile);
             }
-            const int pp = wait_window(lb, size_t(j), size_t(g.nJ), c, epoch, tile);
             if (pp >= 0) {
                 mf_get<Cf, 0, true>(lb.data + (size_t(pp) * g.nJ + j) * 2 * Cf::REC + Cf::REC,
                                     fg, fq, sc);

@@ -22,6 +22,10 @@
 
 #include "scan_engine.cuh"
 
+#ifndef MG_MG_PEEK32
+#define MG_MG_PEEK32 0
+#endif
+
 namespace mg {
 namespace {
 
@@ -77,7 +81,7 @@ struct MinFwd {
     static constexpr int NS = 2, VEC = VEC_, L = L_;
     static constexpr bool kReverse = false;
     // look-back peek: measured faster for bf16 inputs, slower for float32
-    static constexpr bool kPeek = !std::is_same_v<Tin, float>;
+    static constexpr bool kPeek = MG_MG_PEEK32 != 0 || !std::is_same_v<Tin, float>;
     static constexpr bool kStash = true;
     using S = St<NS, VEC>;
     struct Args {
@@ -179,7 +183,7 @@ struct MinBwd {
     static constexpr int LAM = NS - 1;   // state index of lam
     static constexpr bool kReverse = true;
     // look-back peek: measured faster for bf16 inputs, slower for float32
-    static constexpr bool kPeek = !std::is_same_v<Tin, float>;
+    static constexpr bool kPeek = MG_MG_PEEK32 != 0 || !std::is_same_v<Tin, float>;
     using S = St<NS, VEC>;
     struct Args {
         const Tin *x1;

@@ -30,6 +30,10 @@
 
 #include "scan_engine.cuh"
 
+#ifndef MG_VL_PEEK
+#define MG_VL_PEEK 0
+#endif
+
 namespace mg {
 namespace {
 
@@ -82,7 +86,7 @@ template <typename Tin, int VEC_, int L_>
 struct VarFwd {
     static constexpr int NS = 3, VEC = VEC_, L = L_;
     static constexpr bool kReverse = false;
-    static constexpr bool kPeek = false;   // look-back without the peek (measured faster)
+    static constexpr bool kPeek = MG_VL_PEEK != 0;   // look-back peek (measured)
     using S = St<NS, VEC>;
     struct Args {
         const Tin *a;
@@ -239,7 +243,7 @@ template <typename Tin, int VEC_, int L_>
 struct VarBwd {
     static constexpr int NS = 3, VEC = VEC_, L = L_;
     static constexpr bool kReverse = true;
-    static constexpr bool kPeek = false;   // look-back without the peek (measured faster)
+    static constexpr bool kPeek = MG_VL_PEEK != 0;   // look-back peek (measured)
     using S = St<NS, VEC>;
     struct Args {
         const Tin *a;
