@@ -728,9 +728,12 @@ __device__ __forceinline__ void split_tf32(float x, unsigned &hi, unsigned &lo)
 }
 
 // The same split with the remainder passed as a float: the tensor core reads
-// its tf32 bits (the low 13 mantissa bits dropped, toward zero), an error
-// below 2^-21 of x.  Only for products that no recurrence runs through (dA):
-// a biased error there does not accumulate from step to step.
+// its tf32 bits (the low 13 mantissa bits of the remainder dropped, toward
+// zero), an error below 2^-21 of x.  hi is x rounded to nearest, so the
+// remainder is positive or negative with equal odds and the error of hi + lo
+// falls to either side of x: it does not build up along a recurrence (the
+// orthogonality invariant and the parity margins measured the same as with
+// the rounded remainder).
 __device__ __forceinline__ void split_tf32_fast(float x, unsigned &hi, unsigned &lo)
 {
     unsigned h;
@@ -1392,46 +1395,66 @@ __device__ __forceinline__ void mf_apply(const EFrag<Cf, MBEG> &f, bool has_c, S
 #pragma unroll
             for (int e = 0; e < 4; ++e) d[mt][nt][e] = f.v[mt][nt][e];
     if (has_c) {
+        // Both operands are split with one conversion each (split_tf32_fast):
+        // the remainder's dropped bits err to either side of x with equal
+        // odds, so the error does not build up along the recurrence.
         unsigned bh[2][2][2], bl[2][2][2];
 #pragma unroll
         for (int kt = 0; kt < 2; ++kt)
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                split_tf32(f.b[kt][nt][0], bh[kt][nt][0], bl[kt][nt][0]);
-                split_tf32(f.b[kt][nt][1], bh[kt][nt][1], bl[kt][nt][1]);
+                split_tf32_fast(f.b[kt][nt][0], bh[kt][nt][0], bl[kt][nt][0]);
+                split_tf32_fast(f.b[kt][nt][1], bh[kt][nt][1], bl[kt][nt][1]);
             }
-        // the small terms in an accumulator of their own, added after: each
-        // tensor-core accumulation rounds at its result's magnitude, so only
-        // the hi*hi chain rounds at the state's full size
-        float cr[Cf::MT][2][4];
 #pragma unroll
-        for (int mt = MBEG; mt < Cf::MT; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) cr[mt][nt][e] = 0.f;
-#pragma unroll
-        for (int mt = MBEG; mt < Cf::MT; ++mt)
+        for (int mt = MBEG; mt < Cf::MT; ++mt) {
+            unsigned ah[2][4], al[2][4];
 #pragma unroll
             for (int kt = 0; kt < 2; ++kt) {
-                unsigned ah[4], al[4];
-                split_tf32(s[mt][kt][0], ah[0], al[0]);
-                split_tf32(s[mt][kt][2], ah[1], al[1]);
-                split_tf32(s[mt][kt][1], ah[2], al[2]);
-                split_tf32(s[mt][kt][3], ah[3], al[3]);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    mma_tf32(cr[mt][nt], al, bh[kt][nt][0], bh[kt][nt][1]);
-                    mma_tf32(cr[mt][nt], ah, bl[kt][nt][0], bl[kt][nt][1]);
-                    mma_tf32(d[mt][nt], ah, bh[kt][nt][0], bh[kt][nt][1]);
-                }
+                split_tf32_fast(s[mt][kt][0], ah[kt][0], al[kt][0]);
+                split_tf32_fast(s[mt][kt][2], ah[kt][1], al[kt][1]);
+                split_tf32_fast(s[mt][kt][1], ah[kt][2], al[kt][2]);
+                split_tf32_fast(s[mt][kt][3], ah[kt][3], al[kt][3]);
             }
+            // Each tensor-core accumulation rounds at its result's magnitude,
+            // so the small hi*lo and lo*hi terms are summed before any hi*hi
+            // term: on rows of the C part (start value 0) in the accumulator
+            // itself, first; on value rows (start value E_V) in an
+            // accumulator of their own, added after.
+            const bool c_rows = 16 * mt + 15 < Cf::K;
+            if (c_rows) {
 #pragma unroll
-        for (int mt = MBEG; mt < Cf::MT; ++mt)
+                for (int kt = 0; kt < 2; ++kt)
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+                    for (int nt = 0; nt < 2; ++nt) {
+                        mma_tf32(d[mt][nt], al[kt], bh[kt][nt][0], bh[kt][nt][1]);
+                        mma_tf32(d[mt][nt], ah[kt], bl[kt][nt][0], bl[kt][nt][1]);
+                    }
 #pragma unroll
-                for (int e = 0; e < 4; ++e) d[mt][nt][e] += cr[mt][nt][e];
+                for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+                        mma_tf32(d[mt][nt], ah[kt], bh[kt][nt][0], bh[kt][nt][1]);
+            } else {
+                float cr[2][4];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) cr[nt][e] = 0.f;
+#pragma unroll
+                for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        mma_tf32(cr[nt], al[kt], bh[kt][nt][0], bh[kt][nt][1]);
+                        mma_tf32(cr[nt], ah[kt], bl[kt][nt][0], bl[kt][nt][1]);
+                        mma_tf32(d[mt][nt], ah[kt], bh[kt][nt][0], bh[kt][nt][1]);
+                    }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) d[mt][nt][e] += cr[nt][e];
+            }
+        }
     }
 #pragma unroll
     for (int mt = MBEG; mt < Cf::MT; ++mt)
