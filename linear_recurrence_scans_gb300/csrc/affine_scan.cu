@@ -1244,9 +1244,10 @@ struct ColPlan {
 // Stored elements (warp aggregates, carries, look-back records) use the
 // ring slot's layout: C (k x k) first, then the value blocks (forward: B
 // (k x v); backward: M-part (k x k), then Lam-part (k x v)).
-template <int V_, bool BWD_, int NW_, int L_, int NSL_>
+template <int V_, bool BWD_, int NW_, int L_, int NSL_, int MINB_ = 1>
 struct MCfg {
     static constexpr int K = 16, VV = V_, NW = NW_, L = L_, NSL = NSL_;
+    static constexpr int MINB = MINB_;   // CTAs per SM the registers must allow
     static constexpr bool BWD = BWD_;
     static constexpr int KK = K * K, KV = K * VV;
     static constexpr int W = BWD ? K + VV : VV;     // value columns of X
@@ -1488,7 +1489,7 @@ __device__ __forceinline__ void mf_copy_c_rows(const float *E, int g, int q, SFr
 }
 
 template <class Cf>
-__global__ void __launch_bounds__(Cf::NW * 32)
+__global__ void __launch_bounds__(Cf::NW * 32, Cf::MINB)
     affine_mma_kernel(const AffPtrs p, const AffGeom g, const Lookback lb)
 {
     constexpr int K = Cf::K, NW = Cf::NW, L = Cf::L, NSL = Cf::NSL, STEP = Cf::STEP;
