@@ -60,30 +60,28 @@ struct AngleGeom {
     int has_scale, has_decay;
 };
 
-// The lane's role in each layer r < RR, packed in one word: bits 0-4 the
-// partner lane (absolute lane index in the warp), bits 5-8 the pair index,
-// bit 9 the role in the pair (0: first coordinate), bit 10 a negative sign.
+// The lane's role in each layer r < RR, unpacked once before the time loop:
+// the partner lane (absolute lane index in the warp), the offset of the
+// pair's angle in the sequence's theta row (r * half + pair index), the
+// sign sgn[r][j], and q = +1 for the pair's second coordinate, -1 for its
+// first (the sign of the partner's term in the rotation).
 template <int RR>
 struct LaneTables {
-    unsigned w[RR];
-    __device__ int partner(int r) const { return int(w[r] & 31u); }
-    __device__ int pair(int r) const { return int((w[r] >> 5) & 15u); }
-    __device__ bool second(int r) const { return (w[r] >> 9) & 1u; }
-    __device__ float sgn(int r) const { return (w[r] >> 10) & 1u ? -1.f : 1.f; }
+    int partner[RR], thoff[RR];
+    float sgn[RR], q[RR];
 };
 
-template <int RR>
+template <int RR, int HALF>
 __device__ __forceinline__ void lane_tables(const AngleTables &tb, int j, int gbase,
                                             LaneTables<RR> &lt)
 {
 #pragma unroll
     for (int r = 0; r < RR; ++r) {
         const bool on = r < tb.R;
-        const unsigned partner = unsigned(gbase + (on ? tb.partner[r][j] : j));
-        const unsigned pair = on ? unsigned(tb.pair[r][j]) : 0u;
-        const unsigned second = on ? unsigned(tb.role[r][j]) : 0u;
-        const unsigned neg = (on && tb.sgn[r][j] < 0.f) ? 1u : 0u;
-        lt.w[r] = partner | (pair << 5) | (second << 9) | (neg << 10);
+        lt.partner[r] = gbase + (on ? tb.partner[r][j] : j);
+        lt.thoff[r] = r * HALF + (on ? tb.pair[r][j] : 0);
+        lt.sgn[r] = on ? tb.sgn[r][j] : 1.f;
+        lt.q[r] = (on && tb.role[r][j]) ? 1.f : -1.f;
     }
 }
 
@@ -192,7 +190,7 @@ __global__ void __launch_bounds__(kAngleThreads)
     const int64_t seq = seq0 + sl;
     const bool act = seq < g.B * g.n;
     LaneTables<RR> lt;
-    lane_tables<RR>(tb, j, lane - j, lt);
+    lane_tables<RR, HALF>(tb, j, lane - j, lt);
     CopyJobs cj;
     make_jobs(theta, scale, gamma, b, nullptr, g, L, NSEQ, seq0, R, K, cj);
     const int64_t sq = act ? seq : 0;
@@ -224,9 +222,9 @@ __global__ void __launch_bounds__(kAngleThreads)
             for (int r = 0; r < RR; ++r) {
                 if (r >= R) break;
                 float sn, cs;
-                __sincosf(th[r * HALF + lt.pair(r)], &sn, &cs);
-                const float v = __shfl_sync(0xffffffffu, x, lt.partner(r));
-                x = fmaf(cs, x, (lt.second(r) ? sn : -sn) * v) * lt.sgn(r);
+                __sincosf(th[lt.thoff[r]], &sn, &cs);
+                const float v = __shfl_sync(0xffffffffu, x, lt.partner[r]);
+                x = fmaf(cs, x, lt.q[r] * sn * v) * lt.sgn[r];
             }
             const float f = (g.has_scale ? sp[L.o_s + sl] : 1.f) * (g.has_decay ? sp[L.o_g + sl] : 1.f);
             x = fmaf(f, x, sp[L.o_vec + sl * K + j]);
@@ -255,7 +253,7 @@ __global__ void __launch_bounds__(kAngleThreads)
     const int64_t seq = seq0 + sl;
     const bool act = seq < g.B * g.n;
     LaneTables<RR> lt;
-    lane_tables<RR>(tb, j, lane - j, lt);
+    lane_tables<RR, HALF>(tb, j, lane - j, lt);
     CopyJobs cj;
     make_jobs(theta, scale, gamma, grad_out, out, g, L, NSEQ, seq0, R, K, cj);
     const int64_t sq = act ? seq : 0;
@@ -294,9 +292,9 @@ __global__ void __launch_bounds__(kAngleThreads)
 #pragma unroll
             for (int r = 0; r < RR; ++r) {
                 if (r < R) {
-                    __sincosf(th[r * HALF + lt.pair(r)], &sn[r], &cs[r]);
-                    const float v = __shfl_sync(0xffffffffu, xs[r], lt.partner(r));
-                    xs[r + 1] = fmaf(cs[r], xs[r], (lt.second(r) ? sn[r] : -sn[r]) * v) * lt.sgn(r);
+                    __sincosf(th[lt.thoff[r]], &sn[r], &cs[r]);
+                    const float v = __shfl_sync(0xffffffffu, xs[r], lt.partner[r]);
+                    xs[r + 1] = fmaf(cs[r], xs[r], lt.q[r] * sn[r] * v) * lt.sgn[r];
                 } else {
                     xs[r + 1] = xs[r];
                     sn[r] = 0.f;
@@ -312,14 +310,14 @@ __global__ void __launch_bounds__(kAngleThreads)
 #pragma unroll
             for (int r = RR - 1; r >= 0; --r) {
                 if (r >= R) continue;
-                const float up = uu * lt.sgn(r);   // gradient after the signs
-                const float v = __shfl_sync(0xffffffffu, up, lt.partner(r));
-                const float xq = __shfl_sync(0xffffffffu, xs[r], lt.partner(r));
-                if (act && !lt.second(r)) {   // the pair's first lane: dtheta
+                const float up = uu * lt.sgn[r];   // gradient after the signs
+                const float v = __shfl_sync(0xffffffffu, up, lt.partner[r]);
+                const float xq = __shfl_sync(0xffffffffu, xs[r], lt.partner[r]);
+                if (act && lt.q[r] < 0.f) {   // the pair's first lane: dtheta
                     const float dth = up * (-sn[r] * xs[r] - cs[r] * xq) + v * (cs[r] * xs[r] - sn[r] * xq);
-                    dtheta[(st * R + r) * HALF + lt.pair(r)] = dth;
+                    dtheta[st * R * HALF + lt.thoff[r]] = dth;
                 }
-                uu = fmaf(cs[r], up, (lt.second(r) ? -sn[r] : sn[r]) * v);
+                uu = fmaf(cs[r], up, -lt.q[r] * sn[r] * v);
             }
             if (act) {
                 db[st * K + j] = lam;
