@@ -363,7 +363,7 @@ struct MinBwd {
 #define MG_MGB_MB 3
 #endif
 #ifndef MG_MGB_R
-#define MG_MGB_R 2
+#define MG_MGB_R 4
 #endif
 constexpr int kSTX = 32, kSTY = 8;
 
