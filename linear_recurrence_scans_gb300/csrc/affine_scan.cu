@@ -671,7 +671,7 @@ struct LanePlan {
     }
     static size_t ws_bytes(int64_t B, int64_t T, int64_t n)
     {
-        return tiled_ws_bytes(n_tiles(B, T, n), size_t(2) * Cf::NS * 32 * sizeof(float));
+        return tiled_ws_bytes(n_tiles(B, T, n), size_t(2) * Cf::NS * 32 * sizeof(unsigned long long));
     }
     static mg_status launch(const typename Cf::Op::Args &args, int64_t B, int64_t T, int64_t n,
                             void *ws, size_t wsb, cudaStream_t s, const LaunchOpts &o,

@@ -18,7 +18,9 @@
 //   [0, 256)            Control
 //   [256, 256 + 8*N)    one 64-bit record flag per tile:
 //                       kFlagTag | epoch << 2 | status
-//   then                per-tile data, op-specific (aggregate and prefix)
+//   then                per-tile data, op-specific (aggregate and prefix),
+//                       as tagged 64-bit words where the op's records go
+//                       through the chunk engine (see record_tag)
 // A flag counts only if its epoch equals the launch's epoch, so stale flags
 // of earlier launches need no clearing.  The last CTA of every launch resets
 // the ticket and done counters and advances the epoch.  Where the flags of a
@@ -93,6 +95,25 @@ __device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned l
     asm volatile("st.release.gpu.global.u64 [%0], %1;" : : "l"(p), "l"(v) : "memory");
 }
 
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" : : "l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_v2u64(unsigned long long *p, unsigned long long a,
+                                                 unsigned long long b)
+{
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" : : "l"(p), "l"(a), "l"(b)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ld_relaxed_v2u64(const unsigned long long *p, unsigned long long &a,
+                                                 unsigned long long &b)
+{
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p)
+                 : "memory");
+}
+
 __device__ __forceinline__ unsigned long long global_timer_ns()
 {
     unsigned long long t;
@@ -113,6 +134,35 @@ __device__ __forceinline__ unsigned long long flag_word(unsigned long long epoch
 __device__ __forceinline__ unsigned flag_status(unsigned long long v, unsigned long long epoch)
 {
     return ((v & ~3ull) == flag_word(epoch, 0)) ? unsigned(v & 3ull) : kStatusNone;
+}
+
+// Tagged record words.  Every float of a tile's record is stored as one
+// 64-bit word: the high half tags the launch that wrote it, the low half holds
+// the float's bits.  An aligned 64-bit access is single-copy atomic, so a
+// reader whose relaxed load sees its own launch's tag in a word also sees the
+// value written with it, without first acquiring the record's flag: a chunk
+// can take its predecessor's inclusive prefix in one round trip as soon as the
+// words land (the flags still serve every other look-back step).  The tag's
+// top two bits are 01, so a tagged word never equals zero-filled memory or a
+// flag word (top 13 bits set), and tags of different launches on the same
+// workspace differ (the low 30 bits of the epoch).  The tile that the testing
+// option stalls writes tag 0, which no reader accepts, so its successors wait
+// on its flag as before.
+__device__ __forceinline__ unsigned launch_tag(unsigned long long epoch)
+{
+    return 0x40000000u | unsigned(epoch & 0x3fffffffull);
+}
+
+// The tag `tile` writes into its records.
+__device__ __forceinline__ unsigned record_tag(const Lookback &lb, unsigned long long epoch,
+                                               unsigned tile)
+{
+    return (long long)tile == lb.stall_tile ? 0u : launch_tag(epoch);
+}
+
+__device__ __forceinline__ unsigned long long tag_word(unsigned tag, float x)
+{
+    return (static_cast<unsigned long long>(tag) << 32) | __float_as_uint(x);
 }
 
 // Record an error of the launch of `epoch` (any thread): the sticky bits,

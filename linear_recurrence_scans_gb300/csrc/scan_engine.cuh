@@ -87,31 +87,110 @@ struct StashView {
 
 // ------------------------------------------------------------ the engine
 
+// Records: [slot][kind: aggregate, prefix][state][DC] tagged 64-bit words
+// (record_tag), one per float; a lane owns VEC consecutive words per state.
 template <class Op, int TX>
-__device__ __forceinline__ float *chan_record(const Lookback &lb, size_t slot, int kind, int s,
-                                              int lane)
+__device__ __forceinline__ unsigned long long *chan_record(const Lookback &lb, size_t slot,
+                                                           int kind, int s, int lane)
 {
     constexpr int DC = TX * Op::VEC;
-    return lb.data + ((slot * 2 + kind) * Op::NS + s) * DC + lane * Op::VEC;
+    return reinterpret_cast<unsigned long long *>(lb.data) +
+           ((slot * 2 + kind) * Op::NS + s) * DC + lane * Op::VEC;
 }
+
+// A lane's part of a record as loaded (tags included).
+template <class Op>
+struct RawRecord {
+    unsigned long long w[Op::NS][Op::VEC];
+};
 
 template <class Op, int TX>
 __device__ __forceinline__ void put_record(const Lookback &lb, size_t slot, int kind, int lane,
-                                           const typename Op::S &x)
+                                           const typename Op::S &x, unsigned tag)
 {
 #pragma unroll
-    for (int s = 0; s < Op::NS; ++s) store_vec_cg<Op::VEC>(chan_record<Op, TX>(lb, slot, kind, s, lane), x.v[s]);
+    for (int s = 0; s < Op::NS; ++s) {
+        unsigned long long *p = chan_record<Op, TX>(lb, slot, kind, s, lane);
+        if constexpr (Op::VEC % 2 == 0) {
+#pragma unroll
+            for (int v = 0; v < Op::VEC; v += 2)
+                st_relaxed_v2u64(p + v, tag_word(tag, x.v[s][v]), tag_word(tag, x.v[s][v + 1]));
+        } else {
+#pragma unroll
+            for (int v = 0; v < Op::VEC; ++v) st_relaxed_u64(p + v, tag_word(tag, x.v[s][v]));
+        }
+    }
 }
 
+// Issue the loads of a lane's part of a record; the values are waited for
+// only where they are used.
+template <class Op, int TX>
+__device__ __forceinline__ void read_record(const Lookback &lb, size_t slot, int kind, int lane,
+                                            RawRecord<Op> &r)
+{
+#pragma unroll
+    for (int s = 0; s < Op::NS; ++s) {
+        const unsigned long long *p = chan_record<Op, TX>(lb, slot, kind, s, lane);
+        if constexpr (Op::VEC % 2 == 0) {
+#pragma unroll
+            for (int v = 0; v < Op::VEC; v += 2) ld_relaxed_v2u64(p + v, r.w[s][v], r.w[s][v + 1]);
+        } else {
+#pragma unroll
+            for (int v = 0; v < Op::VEC; ++v) r.w[s][v] = ld_relaxed_u64(p + v);
+        }
+    }
+}
+
+template <class Op>
+__device__ __forceinline__ typename Op::S record_values(const RawRecord<Op> &r)
+{
+    typename Op::S x;
+#pragma unroll
+    for (int s = 0; s < Op::NS; ++s)
+#pragma unroll
+        for (int v = 0; v < Op::VEC; ++v) x.v[s][v] = __uint_as_float(unsigned(r.w[s][v]));
+    return x;
+}
+
+// Whether every word of the lane's part carries `tag`.
+template <class Op>
+__device__ __forceinline__ bool record_tagged(const RawRecord<Op> &r, unsigned tag)
+{
+    bool ok = true;
+#pragma unroll
+    for (int s = 0; s < Op::NS; ++s)
+#pragma unroll
+        for (int v = 0; v < Op::VEC; ++v) ok &= unsigned(r.w[s][v] >> 32) == tag;
+    return ok;
+}
+
+// A record published under a flag this warp has acquired.
 template <class Op, int TX>
 __device__ __forceinline__ typename Op::S get_record(const Lookback &lb, size_t slot, int kind,
                                                      int lane)
 {
-    typename Op::S x;
-#pragma unroll
-    for (int s = 0; s < Op::NS; ++s) load_vec_cg<Op::VEC>(chan_record<Op, TX>(lb, slot, kind, s, lane), x.v[s]);
-    return x;
+    RawRecord<Op> r;
+    read_record<Op, TX>(lb, slot, kind, lane, r);
+    return record_values<Op>(r);
 }
+
+// Before its fold, a chunk may load its predecessor's prefix record and take
+// it as its carry-in if every word already carries this launch's tag
+// (Op::kTagged, default on for records of at most 16 floats per lane): one
+// round trip on the tile's critical path instead of a flag poll followed by
+// the record's loads.  If any word is not there yet, the flag look-back runs
+// as usual.
+#ifndef MG_LB_TAGGED
+#define MG_LB_TAGGED 1
+#endif
+template <class Op, class = void>
+struct op_tagged {
+    static constexpr bool value = MG_LB_TAGGED != 0 && Op::NS * Op::VEC <= 16;
+};
+template <class Op>
+struct op_tagged<Op, decltype(void(Op::kTagged))> {
+    static constexpr bool value = MG_LB_TAGGED != 0 && Op::kTagged;
+};
 
 // First half of the look-back (one warp): publish this chunk's record as
 // early as possible.  Chunk 0 publishes its inclusive prefix (initial o cta)
@@ -130,8 +209,9 @@ __device__ int publish_first(const typename Op::Args &args, const ChanGeom &g,
 {
     const int lane = threadIdx.x & 31;
     const size_t slot = size_t(c) * g.nJ + j;
+    const unsigned tag = record_tag(lb, epoch, tile);
     if (c == 0) {
-        if (lact) put_record<Op, TX>(lb, slot, 1, lane, Op::combine(Op::initial(args, g, bb, ld, lchan), cta));
+        if (lact) put_record<Op, TX>(lb, slot, 1, lane, Op::combine(Op::initial(args, g, bb, ld, lchan), cta), tag);
         publish(lb, slot, kStatusPrefix, epoch, tile);
         return -2;
     }
@@ -146,7 +226,7 @@ __device__ int publish_first(const typename Op::Args &args, const ChanGeom &g,
         }
     }
     if (agg) {
-        if (lact) put_record<Op, TX>(lb, slot, 0, lane, cta);
+        if (lact) put_record<Op, TX>(lb, slot, 0, lane, cta, tag);
         publish(lb, slot, kStatusAggregate, epoch, tile);
     }
     return p0;
@@ -193,7 +273,8 @@ __device__ void publish_prefix(const ChanGeom &g, const Lookback &lb, int c, int
 {
     if (c == 0) return;
     const size_t slot = size_t(c) * g.nJ + j;
-    if (lact) put_record<Op, TX>(lb, slot, 1, threadIdx.x & 31, Op::combine(excl, cta));
+    if (lact) put_record<Op, TX>(lb, slot, 1, threadIdx.x & 31, Op::combine(excl, cta),
+                                 record_tag(lb, epoch, tile));
     publish(lb, slot, kStatusPrefix, epoch, tile);
 }
 
@@ -266,6 +347,9 @@ __global__ void __launch_bounds__(TX *TY, MINB)
         const bool lact = lane < TX;
         const int ld = dbase + lane * VEC;
         const bool lchan = lact && ld < g.D;
+        constexpr bool TAGGED = op_tagged<Op>::value;
+        RawRecord<Op> pre;
+        if (TAGGED && c > 0 && lact) read_record<Op, TX>(lb, size_t(c - 1) * g.nJ + j, 1, lane, pre);
         S cta = Op::identity();
         if (lact) {
             // Fold the rows in processing order; each row but the first gets
@@ -285,9 +369,16 @@ __global__ void __launch_bounds__(TX *TY, MINB)
                 cta = (k == 0) ? x : Op::combine(cta, x);
             }
         }
-        const int p0 = publish_first<Op, TX, op_peeks<Op>::value>(args, g, lb, c, j, bb, ld, lact,
-                                                                  lchan, tile, epoch, cta);
-        excl = find_carry<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch, p0);
+        bool have = false;
+        if (TAGGED && c > 0) {
+            have = __all_sync(0xffffffffu, !lact || record_tagged<Op>(pre, launch_tag(epoch)));
+            if (have && lact) excl = record_values<Op>(pre);
+        }
+        if (!have) {
+            const int p0 = publish_first<Op, TX, op_peeks<Op>::value>(args, g, lb, c, j, bb, ld,
+                                                                      lact, lchan, tile, epoch, cta);
+            excl = find_carry<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch, p0);
+        }
         if (lact) {
 #pragma unroll
             for (int s = 0; s < NS; ++s) store_vec<VEC>(&s_carry[s * DC + lane * VEC], excl.v[s]);
@@ -350,7 +441,7 @@ struct ChanPlan {
     }
     static size_t ws_bytes(int64_t B, int64_t T, int64_t D)
     {
-        return tiled_ws_bytes(n_tiles(B, T, D), size_t(2) * Op::NS * DC * sizeof(float));
+        return tiled_ws_bytes(n_tiles(B, T, D), size_t(2) * Op::NS * DC * sizeof(unsigned long long));
     }
     static mg_status launch(const typename Op::Args &args, int64_t B, int64_t T, int64_t D,
                             void *ws, size_t ws_bytes_given, cudaStream_t s, const LaunchOpts &o,
