@@ -263,6 +263,27 @@ __device__ typename Op::S find_carry(const typename Op::Args &args, const ChanGe
     return excl;
 }
 
+// The whole look-back of chunk c (one warp, after its fold into `cta`): the
+// predecessor's prefix words `pre` (read_record, issued before the fold) if
+// TAGGED and every word already carries this launch's tag, else
+// publish_first and find_carry.
+template <class Op, int TX, bool PEEK, bool TAGGED>
+__device__ __forceinline__ typename Op::S look_back(const typename Op::Args &args,
+                                                    const ChanGeom &g, const Lookback &lb, int c,
+                                                    int j, int64_t bb, int ld, bool lact,
+                                                    bool lchan, unsigned tile,
+                                                    unsigned long long epoch,
+                                                    const typename Op::S &cta,
+                                                    const RawRecord<Op> &pre)
+{
+    if (TAGGED && c > 0 &&
+        __all_sync(0xffffffffu, !lact || record_tagged<Op>(pre, launch_tag(epoch))))
+        return lact ? record_values<Op>(pre) : Op::identity();
+    const int p0 = publish_first<Op, TX, PEEK>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch,
+                                               cta);
+    return find_carry<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch, p0);
+}
+
 // Publish chunk c's inclusive prefix excl o cta (chunk 0 did at once).  Kept
 // apart from find_carry so that the carry can be handed to the consumers
 // before this release store's fence.
@@ -369,16 +390,8 @@ __global__ void __launch_bounds__(TX *TY, MINB)
                 cta = (k == 0) ? x : Op::combine(cta, x);
             }
         }
-        bool have = false;
-        if (TAGGED && c > 0) {
-            have = __all_sync(0xffffffffu, !lact || record_tagged<Op>(pre, launch_tag(epoch)));
-            if (have && lact) excl = record_values<Op>(pre);
-        }
-        if (!have) {
-            const int p0 = publish_first<Op, TX, op_peeks<Op>::value>(args, g, lb, c, j, bb, ld,
-                                                                      lact, lchan, tile, epoch, cta);
-            excl = find_carry<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch, p0);
-        }
+        excl = look_back<Op, TX, op_peeks<Op>::value, TAGGED>(args, g, lb, c, j, bb, ld, lact,
+                                                              lchan, tile, epoch, cta, pre);
         if (lact) {
 #pragma unroll
             for (int s = 0; s < NS; ++s) store_vec<VEC>(&s_carry[s * DC + lane * VEC], excl.v[s]);
