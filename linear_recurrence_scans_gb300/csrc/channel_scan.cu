@@ -582,7 +582,7 @@ struct LogBwd {
 #define MG_LINB16_L 4
 #endif
 #ifndef MG_LINB16_MB
-#define MG_LINB16_MB 3
+#define MG_LINB16_MB 5
 #endif
 #ifndef MG_LOG_TX
 #define MG_LOG_TX 32
@@ -624,7 +624,7 @@ struct LogBwd {
 #define MG_LOGB_MB 4
 #endif
 #ifndef MG_LOGB_R
-#define MG_LOGB_R 4
+#define MG_LOGB_R 3
 #endif
 constexpr int kTX = 32, kTY = 8;
 using LinFwdF32 = ChanPlan<LinFwd<float, 4, MG_LINF_L>, MG_LINF_TX, MG_LINF_TY, MG_LINF_MB, MG_LINF_R>;

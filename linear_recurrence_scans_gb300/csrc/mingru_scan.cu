@@ -339,13 +339,13 @@ struct MinBwd {
 #define MG_MGF_TX 32
 #endif
 #ifndef MG_MGF_TY
-#define MG_MGF_TY 4
+#define MG_MGF_TY 8
 #endif
 #ifndef MG_MGF_L
 #define MG_MGF_L 4
 #endif
 #ifndef MG_MGF_MB
-#define MG_MGF_MB 5
+#define MG_MGF_MB 3
 #endif
 #ifndef MG_MGF_R
 #define MG_MGF_R 2
@@ -354,13 +354,13 @@ struct MinBwd {
 #define MG_MGB_TX 32
 #endif
 #ifndef MG_MGB_TY
-#define MG_MGB_TY 8
+#define MG_MGB_TY 4
 #endif
 #ifndef MG_MGB_L
 #define MG_MGB_L 4
 #endif
 #ifndef MG_MGB_MB
-#define MG_MGB_MB 3
+#define MG_MGB_MB 6
 #endif
 #ifndef MG_MGB_R
 #define MG_MGB_R 4
