@@ -401,13 +401,13 @@ struct VarBwd {
 #define MG_VLF_TX 16
 #endif
 #ifndef MG_VLF_TY
-#define MG_VLF_TY 16
+#define MG_VLF_TY 8
 #endif
 #ifndef MG_VLF_L
 #define MG_VLF_L 8
 #endif
 #ifndef MG_VLF_MB
-#define MG_VLF_MB 1
+#define MG_VLF_MB 2
 #endif
 #ifndef MG_VLF_R
 #define MG_VLF_R 2
