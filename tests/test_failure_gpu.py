@@ -103,3 +103,28 @@ def test_small_then_large_tile_count_on_one_workspace(cuda_lib):
         errs = linear_fwd_errors(a, b, A, Bc)
         assert max(errs.values()) <= TOL_F32, (shape, errs)
     mg.workspace_status(ws)
+
+
+def test_prefix_words_of_an_earlier_launch_are_not_taken(cuda_lib):
+    """A chunk takes its predecessor's prefix record without the flag when
+    every word carries the running launch's tag.  Launches on one workspace
+    with the same shape but different inputs leave the previous launch's
+    words in place: each launch must still match the oracle on its own
+    inputs (a stale word accepted would carry the earlier inputs' prefix)."""
+    from parity import log_fwd_errors
+    mg = cuda_lib
+    shape = (2, 4096, 256)   # 2 x 2 channel tiles, dozens of chunks each
+    ws = mg.new_workspace(max(mg.linear_workspace_size(*shape), mg.log_workspace_size(*shape)),
+                          DEV)
+    for seed in (31, 32, 33):
+        a, b, _, _ = wl.mingru_linear(*shape, seed=seed, grads=False)
+        A, Bc = mg.linear_scan_fwd(a.to(DEV), b.to(DEV), ws=ws)
+        errs = linear_fwd_errors(a, b, A, Bc)
+        assert max(errs.values()) <= TOL_F32, (seed, errs)
+        mg.workspace_status(ws)
+    for seed in (34, 35):
+        lc, lv = wl.mingru_log(*shape, seed=seed)
+        h = mg.parallel_scan_log_fwd(lc.to(DEV), lv.to(DEV), ws=ws)
+        errs = log_fwd_errors(lc, lv, h)
+        assert max(errs.values()) <= TOL_F32, (seed, errs)
+        mg.workspace_status(ws)
