@@ -125,8 +125,8 @@ struct LinFwd {
             const int64_t t = t0 + i;
             if (act && t < g.T) {
                 const int64_t off = (bb * g.T + t) * g.D + d;
-                store_vec<VEC>(p.A + off, P);
-                store_vec<VEC>(p.Bc + off, H);
+                store_out<VEC>(p.A + off, P);
+                store_out<VEC>(p.Bc + off, H);
             }
         }
 #pragma unroll
@@ -268,8 +268,8 @@ struct LinBwd {
             const int64_t t = t0 + i;
             if (act && t < g.T) {
                 const int64_t off = (bb * g.T + t) * g.D + d;
-                store_vec<VEC>(p.da + off, da);
-                store_vec<VEC>(p.db + off, lam);
+                store_out<VEC>(p.da + off, da);
+                store_out<VEC>(p.db + off, lam);
                 if constexpr (H0) {
                     if (t == 0) {  // dh0 = a_1 lam_1
                         Raw<Tin, VEC> a0;
@@ -277,7 +277,7 @@ struct LinBwd {
                         float dh[VEC];
 #pragma unroll
                         for (int v = 0; v < VEC; ++v) dh[v] = a0[v] * lam[v];
-                        store_vec<VEC>(p.dh0 + bb * g.D + d, dh);
+                        store_out<VEC>(p.dh0 + bb * g.D + d, dh);
                     }
                 }
             }
@@ -394,7 +394,7 @@ struct LogFwd {
                 h[v] = s[v] * ex2_sub(m[v] * kLog2eF);
             }
             const int64_t t = t0 + i;
-            if (act && t < g.T) store_vec<VEC>(p.h + (bb * g.T + t) * g.D + d, h);
+            if (act && t < g.T) store_out<VEC>(p.h + (bb * g.T + t) * g.D + d, h);
         }
         // (the summed log-coefficient is not needed past the outputs)
 #pragma unroll
@@ -519,9 +519,9 @@ struct LogBwd {
                     dlc[v] = mu[v] * r.ea[i][v] * hp[v];
                     dlv[v] = mu[v] * ex2_sub(lvv[v] * kLog2eF);
                 }
-                store_vec<VEC>(p.dlc + (bb * g.T + t) * g.D + d, dlc);
-                store_vec<VEC>(p.dlv + (bb * (g.T + 1) + t + 1) * g.D + d, dlv);
-                if (t == 0) store_vec<VEC>(p.dlv + (bb * (g.T + 1)) * g.D + d, dlc);
+                store_out<VEC>(p.dlc + (bb * g.T + t) * g.D + d, dlc);
+                store_out<VEC>(p.dlv + (bb * (g.T + 1) + t + 1) * g.D + d, dlv);
+                if (t == 0) store_out<VEC>(p.dlv + (bb * (g.T + 1)) * g.D + d, dlc);
             }
         }
 #pragma unroll

@@ -296,6 +296,45 @@ __device__ __forceinline__ void store_vec(bf16_t *p, const float (&x)[VEC])
     }
 }
 
+// Output stores of the scan epilogues.  With MG_STREAM_OUT (default on)
+// they carry the streaming cache hint (st.global.cs, evicted first): the
+// outputs are not read again by the kernel, so they do not displace the
+// inputs that its second pass re-reads from L2.
+#ifndef MG_STREAM_OUT
+#define MG_STREAM_OUT 1
+#endif
+template <int VEC>
+__device__ __forceinline__ void store_out(float *p, const float (&x)[VEC])
+{
+    if constexpr (MG_STREAM_OUT != 0 && VEC % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q)
+            __stcs(reinterpret_cast<float4 *>(p + 4 * q),
+                   make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
+    } else if constexpr (MG_STREAM_OUT != 0) {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) __stcs(p + v, x[v]);
+    } else {
+        store_vec<VEC>(p, x);
+    }
+}
+
+template <int VEC>
+__device__ __forceinline__ void store_out(bf16_t *p, const float (&x)[VEC])
+{
+    if constexpr (MG_STREAM_OUT != 0 && VEC % 8 == 0) {
+#pragma unroll
+        for (int q = 0; q < VEC / 8; ++q)
+            __stcs(reinterpret_cast<uint4 *>(p + 8 * q),
+                   make_uint4(pack_bf16x2(x[8 * q], x[8 * q + 1]), pack_bf16x2(x[8 * q + 2], x[8 * q + 3]),
+                              pack_bf16x2(x[8 * q + 4], x[8 * q + 5]), pack_bf16x2(x[8 * q + 6], x[8 * q + 7])));
+    } else if constexpr (MG_STREAM_OUT != 0 && VEC == 4) {
+        __stcs(reinterpret_cast<uint2 *>(p), make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3])));
+    } else {
+        store_vec<VEC>(p, x);
+    }
+}
+
 // L2-only (.cg) variants for look-back records written by one CTA and read
 // by another.
 template <int VEC>

@@ -165,8 +165,8 @@ struct MinFwd {
                     st.v[1][v] = fmaf(e.v[0][v], st.v[1][v], e.v[1][v]);
                 }
                 const int64_t off = (bb * g.T + t0 + i) * g.D + d;
-                if constexpr (WA) store_vec<VEC>(p.A + off, st.v[0]);
-                store_vec<VEC>(p.Bc + off, st.v[1]);
+                if constexpr (WA) store_out<VEC>(p.A + off, st.v[0]);
+                store_out<VEC>(p.Bc + off, st.v[1]);
             }
         }
     }
@@ -322,8 +322,8 @@ struct MinBwd {
                     o2[v] = lam[v] * q.z * q.gp;
                 }
                 const int64_t off = (bb * g.T + t0 + i) * g.D + d;
-                store_vec<VEC>(p.dx1 + off, o1);
-                store_vec<VEC>(p.dx2 + off, o2);
+                store_out<VEC>(p.dx1 + off, o1);
+                store_out<VEC>(p.dx2 + off, o2);
             }
         }
 #pragma unroll

@@ -221,8 +221,8 @@ struct VarFwd {
             const int64_t t = t0 + i;
             if (act && t < g.T) {
                 const int64_t off = (bb * g.T + t) * g.D + d;
-                store_vec<VEC>(p.A + off, Av);
-                store_vec<VEC>(p.H + off, Hv);
+                store_out<VEC>(p.A + off, Av);
+                store_out<VEC>(p.H + off, Hv);
             }
         }
 #pragma unroll
@@ -376,15 +376,15 @@ struct VarBwd {
             const int64_t t = t0 + i;
             if (act && t < g.T) {
                 const int64_t off = (bb * g.T + t) * g.D + d;
-                store_vec<VEC>(p.da + off, da);
-                store_vec<VEC>(p.db + off, lam);
+                store_out<VEC>(p.da + off, da);
+                store_out<VEC>(p.db + off, lam);
                 if (p.h0 != nullptr && (r.start & (1u << i))) {   // dh0 = a_r lam_r
                     Raw<Tin, VEC> ar;
                     ar.load(p.a + off);
                     float dh[VEC];
 #pragma unroll
                     for (int v = 0; v < VEC; ++v) dh[v] = ar[v] * lam[v];
-                    store_vec<VEC>(p.dh0 + int64_t(r.sq[i]) * g.D + d, dh);
+                    store_out<VEC>(p.dh0 + int64_t(r.sq[i]) * g.D + d, dh);
                 }
             }
         }
