@@ -57,21 +57,32 @@ __device__ __forceinline__ void ld_floats(const float *p, float *o)
     }
 }
 
+// Output rows of the small-k kernels, stored with the streaming cache hint
+// under MG_STREAM_OUT (as the channel ops' outputs: not read again, so they
+// do not displace the inputs that pass 2 re-reads from L2).
 template <int N>
 __device__ __forceinline__ void st_floats(float *p, const float *x)
 {
     if constexpr (N % 4 == 0) {
 #pragma unroll
-        for (int q = 0; q < N / 4; ++q)
-            *reinterpret_cast<float4 *>(p + 4 * q) =
-                make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        for (int q = 0; q < N / 4; ++q) {
+            const float4 v = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+            if constexpr (MG_STREAM_OUT != 0) __stcs(reinterpret_cast<float4 *>(p + 4 * q), v);
+            else *reinterpret_cast<float4 *>(p + 4 * q) = v;
+        }
     } else if constexpr (N % 2 == 0) {
 #pragma unroll
-        for (int q = 0; q < N / 2; ++q)
-            *reinterpret_cast<float2 *>(p + 2 * q) = make_float2(x[2 * q], x[2 * q + 1]);
+        for (int q = 0; q < N / 2; ++q) {
+            const float2 v = make_float2(x[2 * q], x[2 * q + 1]);
+            if constexpr (MG_STREAM_OUT != 0) __stcs(reinterpret_cast<float2 *>(p + 2 * q), v);
+            else *reinterpret_cast<float2 *>(p + 2 * q) = v;
+        }
     } else {
 #pragma unroll
-        for (int q = 0; q < N; ++q) p[q] = x[q];
+        for (int q = 0; q < N; ++q) {
+            if constexpr (MG_STREAM_OUT != 0) __stcs(p + q, x[q]);
+            else p[q] = x[q];
+        }
     }
 }
 
