@@ -147,6 +147,7 @@ template <typename Tin, int VEC_, int L_, typename Tout = float, bool H0 = false
 struct LinBwd {
     static constexpr int NS = 3, VEC = VEC_, L = L_;
     static constexpr bool kReverse = true;
+    static constexpr unsigned kPrefixStates = 0b110u;   // a prefix's C feeds no output
     using S = St<NS, VEC>;
     struct Args {
         const Tin *a;
@@ -300,6 +301,7 @@ template <int VEC_, int L_>
 struct LogFwd {
     static constexpr int NS = 3, VEC = VEC_, L = L_;
     static constexpr bool kReverse = false;
+    static constexpr unsigned kPrefixStates = 0b110u;   // a prefix's la feeds no output
     using S = St<NS, VEC>;
     struct Args {
         const float *lc;
@@ -416,6 +418,7 @@ template <int VEC_, int L_>
 struct LogBwd {
     static constexpr int NS = 2, VEC = VEC_, L = L_;
     static constexpr bool kReverse = true;
+    static constexpr unsigned kPrefixStates = 0b10u;    // a prefix's C feeds no output
     using S = St<NS, VEC>;
     struct Args {
         const float *lc;

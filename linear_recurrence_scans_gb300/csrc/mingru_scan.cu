@@ -80,6 +80,8 @@ template <typename Tin, int VEC_, int L_, bool WA>
 struct MinFwd {
     static constexpr int NS = 2, VEC = VEC_, L = L_;
     static constexpr bool kReverse = false;
+    // a prefix's running product is read only when A is written
+    static constexpr unsigned kPrefixStates = WA ? 0b11u : 0b10u;
     // look-back peek: measured faster for bf16 inputs, slower for float32
     static constexpr bool kPeek = MG_MG_PEEK32 != 0 || !std::is_same_v<Tin, float>;
     static constexpr bool kStash = true;
@@ -182,6 +184,7 @@ struct MinBwd {
     static constexpr int NS = GA ? 3 : 2, VEC = VEC_, L = L_;
     static constexpr int LAM = NS - 1;   // state index of lam
     static constexpr bool kReverse = true;
+    static constexpr unsigned kPrefixStates = (1u << NS) - 2u;   // a prefix's C feeds no output
     // look-back peek: measured faster for bf16 inputs, slower for float32
     static constexpr bool kPeek = MG_MG_PEEK32 != 0 || !std::is_same_v<Tin, float>;
     using S = St<NS, VEC>;

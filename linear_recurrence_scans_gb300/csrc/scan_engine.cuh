@@ -104,12 +104,37 @@ struct RawRecord {
     unsigned long long w[Op::NS][Op::VEC];
 };
 
-template <class Op, int TX>
+// The states a prefix record keeps (bit s: state s; Op::kPrefixStates,
+// default all).  A state may be left out when no epilogue reads it and the
+// combine uses the earlier operand's copy of it only for the same state of
+// the result (the running coefficient product of the adjoints, the summed
+// log-coefficient of the log forward): a prefix's copy then feeds nothing
+// but the next prefix's copy.  Readers fill a left-out state with the
+// identity's value.  Aggregate records keep every state.
+#ifndef MG_PREFIX_TRIM
+#define MG_PREFIX_TRIM 1
+#endif
+template <class Op, class = void>
+struct op_prefix_states {
+    static constexpr unsigned value = (1u << Op::NS) - 1u;
+};
+template <class Op>
+struct op_prefix_states<Op, decltype(void(Op::kPrefixStates))> {
+    static constexpr unsigned value = MG_PREFIX_TRIM != 0 ? Op::kPrefixStates : (1u << Op::NS) - 1u;
+};
+template <class Op>
+constexpr unsigned all_states()
+{
+    return (1u << Op::NS) - 1u;
+}
+
+template <class Op, int TX, unsigned MASK = all_states<Op>()>
 __device__ __forceinline__ void put_record(const Lookback &lb, size_t slot, int kind, int lane,
                                            const typename Op::S &x, unsigned tag)
 {
 #pragma unroll
     for (int s = 0; s < Op::NS; ++s) {
+        if (!((MASK >> s) & 1u)) continue;
         unsigned long long *p = chan_record<Op, TX>(lb, slot, kind, s, lane);
         if constexpr (Op::VEC % 2 == 0) {
 #pragma unroll
@@ -124,12 +149,13 @@ __device__ __forceinline__ void put_record(const Lookback &lb, size_t slot, int 
 
 // Issue the loads of a lane's part of a record; the values are waited for
 // only where they are used.
-template <class Op, int TX>
+template <class Op, int TX, unsigned MASK = all_states<Op>()>
 __device__ __forceinline__ void read_record(const Lookback &lb, size_t slot, int kind, int lane,
                                             RawRecord<Op> &r)
 {
 #pragma unroll
     for (int s = 0; s < Op::NS; ++s) {
+        if (!((MASK >> s) & 1u)) continue;
         const unsigned long long *p = chan_record<Op, TX>(lb, slot, kind, s, lane);
         if constexpr (Op::VEC % 2 == 0) {
 #pragma unroll
@@ -141,37 +167,41 @@ __device__ __forceinline__ void read_record(const Lookback &lb, size_t slot, int
     }
 }
 
-template <class Op>
+template <class Op, unsigned MASK = all_states<Op>()>
 __device__ __forceinline__ typename Op::S record_values(const RawRecord<Op> &r)
 {
-    typename Op::S x;
+    typename Op::S x = Op::identity();
 #pragma unroll
     for (int s = 0; s < Op::NS; ++s)
+        if ((MASK >> s) & 1u) {
 #pragma unroll
-        for (int v = 0; v < Op::VEC; ++v) x.v[s][v] = __uint_as_float(unsigned(r.w[s][v]));
+            for (int v = 0; v < Op::VEC; ++v) x.v[s][v] = __uint_as_float(unsigned(r.w[s][v]));
+        }
     return x;
 }
 
-// Whether every word of the lane's part carries `tag`.
-template <class Op>
+// Whether every kept word of the lane's part carries `tag`.
+template <class Op, unsigned MASK = all_states<Op>()>
 __device__ __forceinline__ bool record_tagged(const RawRecord<Op> &r, unsigned tag)
 {
     bool ok = true;
 #pragma unroll
     for (int s = 0; s < Op::NS; ++s)
+        if ((MASK >> s) & 1u) {
 #pragma unroll
-        for (int v = 0; v < Op::VEC; ++v) ok &= unsigned(r.w[s][v] >> 32) == tag;
+            for (int v = 0; v < Op::VEC; ++v) ok &= unsigned(r.w[s][v] >> 32) == tag;
+        }
     return ok;
 }
 
 // A record published under a flag this warp has acquired.
-template <class Op, int TX>
+template <class Op, int TX, unsigned MASK = all_states<Op>()>
 __device__ __forceinline__ typename Op::S get_record(const Lookback &lb, size_t slot, int kind,
                                                      int lane)
 {
     RawRecord<Op> r;
-    read_record<Op, TX>(lb, slot, kind, lane, r);
-    return record_values<Op>(r);
+    read_record<Op, TX, MASK>(lb, slot, kind, lane, r);
+    return record_values<Op, MASK>(r);
 }
 
 // Before its fold, a chunk may load its predecessor's prefix record and take
@@ -211,7 +241,9 @@ __device__ int publish_first(const typename Op::Args &args, const ChanGeom &g,
     const size_t slot = size_t(c) * g.nJ + j;
     const unsigned tag = record_tag(lb, epoch, tile);
     if (c == 0) {
-        if (lact) put_record<Op, TX>(lb, slot, 1, lane, Op::combine(Op::initial(args, g, bb, ld, lchan), cta), tag);
+        if (lact)
+            put_record<Op, TX, op_prefix_states<Op>::value>(
+                lb, slot, 1, lane, Op::combine(Op::initial(args, g, bb, ld, lchan), cta), tag);
         publish(lb, slot, kStatusPrefix, epoch, tile);
         return -2;
     }
@@ -249,7 +281,7 @@ __device__ typename Op::S find_carry(const typename Op::Args &args, const ChanGe
     if (p >= 0 && lact) {
         // excl = pref(p) o agg(p+1) o ... o agg(c-1), folded left to right;
         // the record loads of a batch are independent and issued together.
-        excl = get_record<Op, TX>(lb, size_t(p) * g.nJ + j, 1, lane);
+        excl = get_record<Op, TX, op_prefix_states<Op>::value>(lb, size_t(p) * g.nJ + j, 1, lane);
         int q = p + 1;
         for (; q + 4 <= c; q += 4) {
             const S r0 = get_record<Op, TX>(lb, size_t(q) * g.nJ + j, 0, lane);
@@ -276,9 +308,10 @@ __device__ __forceinline__ typename Op::S look_back(const typename Op::Args &arg
                                                     const typename Op::S &cta,
                                                     const RawRecord<Op> &pre)
 {
+    constexpr unsigned PS = op_prefix_states<Op>::value;
     if (TAGGED && c > 0 &&
-        __all_sync(0xffffffffu, !lact || record_tagged<Op>(pre, launch_tag(epoch))))
-        return lact ? record_values<Op>(pre) : Op::identity();
+        __all_sync(0xffffffffu, !lact || record_tagged<Op, PS>(pre, launch_tag(epoch))))
+        return lact ? record_values<Op, PS>(pre) : Op::identity();
     const int p0 = publish_first<Op, TX, PEEK>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch,
                                                cta);
     return find_carry<Op, TX>(args, g, lb, c, j, bb, ld, lact, lchan, tile, epoch, p0);
@@ -294,8 +327,10 @@ __device__ void publish_prefix(const ChanGeom &g, const Lookback &lb, int c, int
 {
     if (c == 0) return;
     const size_t slot = size_t(c) * g.nJ + j;
-    if (lact) put_record<Op, TX>(lb, slot, 1, threadIdx.x & 31, Op::combine(excl, cta),
-                                 record_tag(lb, epoch, tile));
+    if (lact)
+        put_record<Op, TX, op_prefix_states<Op>::value>(lb, slot, 1, threadIdx.x & 31,
+                                                        Op::combine(excl, cta),
+                                                        record_tag(lb, epoch, tile));
     publish(lb, slot, kStatusPrefix, epoch, tile);
 }
 
@@ -370,7 +405,9 @@ __global__ void __launch_bounds__(TX *TY, MINB)
         const bool lchan = lact && ld < g.D;
         constexpr bool TAGGED = op_tagged<Op>::value;
         RawRecord<Op> pre;
-        if (TAGGED && c > 0 && lact) read_record<Op, TX>(lb, size_t(c - 1) * g.nJ + j, 1, lane, pre);
+        if (TAGGED && c > 0 && lact)
+            read_record<Op, TX, op_prefix_states<Op>::value>(lb, size_t(c - 1) * g.nJ + j, 1,
+                                                              lane, pre);
         S cta = Op::identity();
         if (lact) {
             // Fold the rows in processing order; each row but the first gets

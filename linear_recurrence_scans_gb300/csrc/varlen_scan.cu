@@ -85,6 +85,7 @@ __device__ __forceinline__ unsigned seq_walk(const long long *cu, int nseq, long
 template <typename Tin, int VEC_, int L_>
 struct VarFwd {
     static constexpr int NS = 3, VEC = VEC_, L = L_;
+    static constexpr unsigned kPrefixStates = 0b110u;   // a prefix's m feeds no output
     static constexpr bool kReverse = false;
     static constexpr bool kPeek = MG_VL_PEEK != 0;   // look-back peek (measured)
     using S = St<NS, VEC>;
@@ -242,6 +243,7 @@ struct VarFwd {
 template <typename Tin, int VEC_, int L_>
 struct VarBwd {
     static constexpr int NS = 3, VEC = VEC_, L = L_;
+    static constexpr unsigned kPrefixStates = 0b110u;   // a prefix's m feeds no output
     static constexpr bool kReverse = true;
     static constexpr bool kPeek = MG_VL_PEEK != 0;   // look-back peek (measured)
     using S = St<NS, VEC>;
