@@ -725,20 +725,9 @@ struct AffPtrs {
 };
 
 // 3xTF32 products on the tensor cores: each fp32 operand is split into a
-// tf32 high part and a tf32 remainder, and hi*hi, hi*lo, lo*hi are
-// accumulated in fp32 (the dropped lo*lo term is below 2^-22 of each
-// product).
-__device__ __forceinline__ void split_tf32(float x, unsigned &hi, unsigned &lo)
-{
-    unsigned h, l;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(h) : "f"(x));
-    const float rem = x - __uint_as_float(h);
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(l) : "f"(rem));
-    hi = h;
-    lo = l;
-}
-
-// The same split with the remainder passed as a float: the tensor core reads
+// tf32 high part and a remainder, and hi*hi, hi*lo, lo*hi are accumulated in
+// fp32 (the dropped lo*lo term is below 2^-22 of each product).  The
+// remainder is passed as a float: the tensor core reads
 // its tf32 bits (the low 13 mantissa bits of the remainder dropped, toward
 // zero), an error below 2^-21 of x.  hi is x rounded to nearest, so the
 // remainder is positive or negative with equal odds and the error of hi + lo

@@ -111,21 +111,29 @@ struct RawRecord {
 // log-coefficient of the log forward): a prefix's copy then feeds nothing
 // but the next prefix's copy.  Readers fill a left-out state with the
 // identity's value.  Aggregate records keep every state.
+// A mask names states 0..31 only; states from 32 on (the small-matrix affine
+// ops hold up to 80) are always kept.
 #ifndef MG_PREFIX_TRIM
 #define MG_PREFIX_TRIM 1
 #endif
 template <class Op, class = void>
 struct op_prefix_states {
-    static constexpr unsigned value = (1u << Op::NS) - 1u;
+    static constexpr unsigned value = ~0u;
 };
 template <class Op>
 struct op_prefix_states<Op, decltype(void(Op::kPrefixStates))> {
-    static constexpr unsigned value = MG_PREFIX_TRIM != 0 ? Op::kPrefixStates : (1u << Op::NS) - 1u;
+    static constexpr unsigned value = MG_PREFIX_TRIM != 0 ? Op::kPrefixStates : ~0u;
 };
 template <class Op>
 constexpr unsigned all_states()
 {
-    return (1u << Op::NS) - 1u;
+    return ~0u;
+}
+// Whether mask MASK keeps state s.
+template <unsigned MASK>
+__device__ __forceinline__ constexpr bool keeps(int s)
+{
+    return s >= 32 || ((MASK >> (s & 31)) & 1u) != 0u;
 }
 
 template <class Op, int TX, unsigned MASK = all_states<Op>()>
@@ -134,7 +142,7 @@ __device__ __forceinline__ void put_record(const Lookback &lb, size_t slot, int 
 {
 #pragma unroll
     for (int s = 0; s < Op::NS; ++s) {
-        if (!((MASK >> s) & 1u)) continue;
+        if (!keeps<MASK>(s)) continue;
         unsigned long long *p = chan_record<Op, TX>(lb, slot, kind, s, lane);
         if constexpr (Op::VEC % 2 == 0) {
 #pragma unroll
@@ -155,7 +163,7 @@ __device__ __forceinline__ void read_record(const Lookback &lb, size_t slot, int
 {
 #pragma unroll
     for (int s = 0; s < Op::NS; ++s) {
-        if (!((MASK >> s) & 1u)) continue;
+        if (!keeps<MASK>(s)) continue;
         const unsigned long long *p = chan_record<Op, TX>(lb, slot, kind, s, lane);
         if constexpr (Op::VEC % 2 == 0) {
 #pragma unroll
@@ -173,7 +181,7 @@ __device__ __forceinline__ typename Op::S record_values(const RawRecord<Op> &r)
     typename Op::S x = Op::identity();
 #pragma unroll
     for (int s = 0; s < Op::NS; ++s)
-        if ((MASK >> s) & 1u) {
+        if (keeps<MASK>(s)) {
 #pragma unroll
             for (int v = 0; v < Op::VEC; ++v) x.v[s][v] = __uint_as_float(unsigned(r.w[s][v]));
         }
@@ -187,7 +195,7 @@ __device__ __forceinline__ bool record_tagged(const RawRecord<Op> &r, unsigned t
     bool ok = true;
 #pragma unroll
     for (int s = 0; s < Op::NS; ++s)
-        if ((MASK >> s) & 1u) {
+        if (keeps<MASK>(s)) {
 #pragma unroll
             for (int v = 0; v < Op::VEC; ++v) ok &= unsigned(r.w[s][v] >> 32) == tag;
         }
